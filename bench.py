@@ -1,0 +1,508 @@
+#!/usr/bin/env python3
+"""q=4 MoE verify throughput on the 43-layer synthetic stack; prints one JSON line.
+
+A step is one q = 4 verify pass (top-4 routing) through 43 MoE layers of hidden 4096, 256 routed
+experts (FP2 gate/up [2048 x 4096], FP3 down [4096 x 2048]) and an FP4 shared expert, all resident in
+HBM (about 99 GB), on a batch of 4 synthetic tokens. The metric is packed-weight GB/s: the packed bytes
+of every expert matrix the step touches (|union| * 8,912,896 + 13,369,344 per layer) divided by time.
+
+--impl fpx (default) times the CUDA library; --impl reference times the CPU oracle on bounded samples
+of the same workload. Under torchrun every rank runs an independent replica (no collective on the
+data path); value is the whole job's bytes over the slowest rank's time.
+"""
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+H, I, E, Q, K_TOP, LAYERS = 4096, 2048, 256, 4, 4, 43
+METRIC = "q=4 MoE verify: packed-weight GB/s (frac of B300 HBM peak), layer-steps/s"
+WORKLOAD = ("43-layer synthetic MoE stack, each layer hidden 4096, 256 routed experts (FP2 gate/up "
+            "2048x4096, FP3 down 4096x2048), FP4 shared expert, fp32 router; q=4 verify pass, top-4")
+N_BATCHES = 8
+
+
+def layer_bytes(n_union):
+    import bit_block_quantized_wt_b300 as fpx
+    gu = fpx.fpx_matrix_bytes(2, I, H)
+    d = fpx.fpx_matrix_bytes(3, H, I)
+    s = fpx.fpx_matrix_bytes(4, I, H)
+    return n_union * (2 * gu + d) + 3 * s
+
+
+def gate_up_bytes(n_union):
+    import bit_block_quantized_wt_b300 as fpx
+    return n_union * 2 * fpx.fpx_matrix_bytes(2, I, H) + 2 * fpx.fpx_matrix_bytes(4, I, H)
+
+
+def down_bytes(n_union):
+    import bit_block_quantized_wt_b300 as fpx
+    return n_union * fpx.fpx_matrix_bytes(3, H, I) + fpx.fpx_matrix_bytes(4, H, I)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------- clocks (NVML)
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons with NVML every 20 ms while running."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, index):
+        self.samples, self.reasons, self.ok, self.err = [], 0, False, None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # noqa: BLE001 - reported in the JSON line
+            self.max = None
+            self.err = f"{type(e).__name__}: {e}"[:200]
+        self._stop = threading.Event()
+
+    def _reasons(self):
+        f = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return f(self.h)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                self.reasons |= self._reasons()
+            except Exception:
+                pass
+            time.sleep(0.02)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max, "reasons": [f"nvml unavailable ({self.err})"]}
+        names = [n for b, n in self.REASONS.items() if self.reasons & b and n != "gpu_idle"]
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max, "reasons": names,
+                "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------- device stack
+
+class Stack:
+    def __init__(self, n_layers, seed=0):
+        import torch
+        import bit_block_quantized_wt_b300 as fpx
+        import synth
+        self.fpx, self.torch = fpx, torch
+        mb_gu, mb_d, mb_s = fpx.fpx_matrix_bytes(2, I, H), fpx.fpx_matrix_bytes(3, H, I), fpx.fpx_matrix_bytes(4, I, H)
+        s = torch.cuda.current_stream().cuda_stream
+        self.bufs, self.layers = [], []
+        for l in range(n_layers):
+            g = torch.empty(E * mb_gu, dtype=torch.uint8, device="cuda")
+            u = torch.empty(E * mb_gu, dtype=torch.uint8, device="cuda")
+            d = torch.empty(E * mb_d, dtype=torch.uint8, device="cuda")
+            sh = [torch.empty(mb_s, dtype=torch.uint8, device="cuda") for _ in range(3)]
+            synth.device_matrices(2, seed, l, synth.GATE, 0, E, I, H, g.data_ptr(), mb_gu, s)
+            synth.device_matrices(2, seed, l, synth.UP, 0, E, I, H, u.data_ptr(), mb_gu, s)
+            synth.device_matrices(3, seed, l, synth.DOWN, 0, E, H, I, d.data_ptr(), mb_d, s)
+            for m, (tid, n, kk) in zip(sh, [(synth.SH_GATE, I, H), (synth.SH_UP, I, H), (synth.SH_DOWN, H, I)]):
+                synth.device_matrices(4, seed, l, tid, 0, 1, n, kk, m.data_ptr(), mb_s, s)
+            R = torch.from_numpy(synth.router(E, H, seed, l)).cuda()
+            self.bufs.append((g, u, d, sh, R))
+            self.layers.append(fpx.moe_layer(H=H, I=I, E=E, router=R.data_ptr(), gate=g.data_ptr(), up=u.data_ptr(),
+                                             down=d.data_ptr(), sh_gate=sh[0].data_ptr(), sh_up=sh[1].data_ptr(),
+                                             sh_down=sh[2].data_ptr()))
+        torch.cuda.synchronize()
+
+
+def tokens_fp32(b, q):
+    import synth
+    return synth.tokens_bf16(q, H, seed=1000 + b)[1].astype(np.float32)
+
+
+class Runner:
+    """Holds the buffers of one verify-pass configuration and a captured CUDA graph of one pass."""
+
+    def __init__(self, stack, q, k, graph=True):
+        import torch
+        fpx = stack.fpx
+        self.stack, self.q, self.k, self.torch, self.fpx = stack, q, k, torch, fpx
+        L = len(stack.layers)
+        self.ws_b = fpx.moe_workspace_bytes(stack.layers[0], q, k)
+        self.ws = torch.empty(self.ws_b, dtype=torch.uint8, device="cuda")
+        self.rin = torch.empty(q, H, device="cuda")
+        self.rL = torch.empty(q, H, device="cuda")
+        self.idx = torch.empty(L, q, k, dtype=torch.int32, device="cuda")
+        self.batches = torch.stack([torch.from_numpy(tokens_fp32(b, q)) for b in range(N_BATCHES)]).cuda()
+        self.stream = torch.cuda.Stream()
+        self.stream.wait_stream(torch.cuda.current_stream())
+        self.graph = None
+        if graph:
+            with torch.cuda.stream(self.stream):
+                self.rin.copy_(self.batches[0])
+                self.call()  # warm the launch path (attributes) before capture
+            self.stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                self.call()
+            self.graph = g
+        torch.cuda.synchronize()
+
+    def call(self, events=None):
+        self.fpx.moe_stack_verify(self.stack.layers, self.rin, self.q, self.k, self.rL, self.ws, self.ws_b,
+                                  idx_out=self.idx, events=events)
+
+    def step(self, b):
+        self.rin.copy_(self.batches[b % N_BATCHES], non_blocking=True)
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self.call()
+
+    def union_sizes(self):
+        """Per batch, the number of distinct experts per layer (from the routing of a real pass)."""
+        torch = self.torch
+        out = []
+        with torch.cuda.stream(self.stream):
+            for b in range(N_BATCHES):
+                self.rin.copy_(self.batches[b])
+                self.call()
+                self.stream.synchronize()
+                idx = self.idx.cpu().numpy()
+                out.append([len(set(idx[l].ravel().tolist())) for l in range(idx.shape[0])])
+        status = self.fpx.fpx_read_status(self.ws[:4].view(torch.int32), self.stream)
+        if status != 0:
+            raise RuntimeError(f"device status {status}")
+        return out
+
+
+def timed(runner, steps, warmup, world):
+    torch = runner.torch
+    with torch.cuda.stream(runner.stream):
+        for i in range(warmup):
+            runner.step(i)
+        runner.stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(runner.stream)
+        for i in range(steps):
+            runner.step(i)
+        e1.record(runner.stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def kernel_profile(runner, steps):
+    """Per-kernel average durations (ms) from CUDA events recorded around every kernel, on the stream
+    the kernels run on."""
+    import ctypes as C
+    torch = runner.torch
+    L = len(runner.stack.layers)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(3 * L + 1)]
+    with torch.cuda.stream(runner.stream):
+        for e in evs:
+            e.record(runner.stream)  # materialise the handles
+        runner.stream.synchronize()
+        handles = [e.cuda_event for e in evs]
+        sums = np.zeros(3)
+        per_layer = np.zeros((3, L))
+        for i in range(steps):
+            runner.rin.copy_(runner.batches[i % N_BATCHES])
+            runner.call(events=handles)
+            runner.stream.synchronize()
+            for l in range(L):
+                for j in range(3):
+                    dt = evs[3 * l + j].elapsed_time(evs[3 * l + j + 1])
+                    sums[j] += dt
+                    per_layer[j, l] += dt
+    return sums / (steps * L), per_layer / steps
+
+
+def e2e_pass(runner, steps, world):
+    """The same metric through the public API with host buffers: each step copies the step's tokens
+    from pinned host memory, runs the pass and reads the result (residual and routing) back."""
+    torch = runner.torch
+    host_in = [torch.from_numpy(tokens_fp32(b, runner.q)).pin_memory() for b in range(N_BATCHES)]
+    host_r = torch.empty(runner.q, H).pin_memory()
+    host_idx = torch.empty(runner.idx.shape, dtype=torch.int32).pin_memory()
+    with torch.cuda.stream(runner.stream):
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(runner.stream)
+        for i in range(steps):
+            runner.rin.copy_(host_in[i % N_BATCHES], non_blocking=True)
+            runner.graph.replay() if runner.graph is not None else runner.call()
+            host_r.copy_(runner.rL, non_blocking=True)
+            host_idx.copy_(runner.idx, non_blocking=True)
+        e1.record(runner.stream)
+        e1.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+    h2d = host_in[0].numel() * 4
+    d2h = host_r.numel() * 4 + host_idx.numel() * 4
+    return e0.elapsed_time(e1) / 1e3, h2d, d2h
+
+
+def csrc_digest():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "bit_block_quantized_wt_b300", "csrc")
+    for n in sorted(os.listdir(d)):
+        if n.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(d, n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        if t.get("csrc") == csrc_digest() and kernel in t.get("kernels", {}):
+            return t["kernels"][kernel]["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+def oracle_layer_steps(stack_seed, r_trace, idx, budget_s, max_layers):
+    """Times the oracle on whole layer-steps of the q=4 pass (teacher-forced on the GPU's residual):
+    returns (seconds, packed bytes, layers)."""
+    import oracle
+    import synth
+    spent, nbytes, done = 0.0, 0, 0
+    for l in range(max_layers):
+        uni = sorted(set(int(v) for v in idx[l].ravel()))
+        g, u, d = [None] * E, [None] * E, [None] * E
+        for e in uni:
+            g[e] = synth.matrix(2, I, H, stack_seed, l, synth.GATE, e)
+            u[e] = synth.matrix(2, I, H, stack_seed, l, synth.UP, e)
+            d[e] = synth.matrix(3, H, I, stack_seed, l, synth.DOWN, e)
+        sh = [synth.matrix(4, I, H, stack_seed, l, synth.SH_GATE), synth.matrix(4, I, H, stack_seed, l, synth.SH_UP),
+              synth.matrix(4, H, I, stack_seed, l, synth.SH_DOWN)]
+        R = synth.router(E, H, stack_seed, l)
+        x = oracle.rmsnorm_bf16(r_trace[l])
+        t0 = time.perf_counter()
+        oracle.moe_layer(H, I, E, R, g, u, d, *sh, x, K_TOP)
+        spent += time.perf_counter() - t0
+        nbytes += layer_bytes(len(uni))
+        done += 1
+        if spent >= budget_s:
+            break
+    return spent, nbytes, done
+
+
+def run_fpx(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    import bit_block_quantized_wt_b300 as fpx
+    fpx.lib()
+    peak, peak_kind = peaks()
+
+    stack = Stack(args.layers)
+    r4 = Runner(stack, Q, K_TOP, graph=not args.no_graph)
+    unions = r4.union_sizes()
+    bytes_per_batch = [sum(layer_bytes(n) for n in u) for u in unions]
+    with ClockSampler(local) as clk:
+        secs = timed(r4, args.steps, args.warmup, world)
+    step_bytes = sum(bytes_per_batch[i % N_BATCHES] for i in range(args.steps))
+    # slowest rank decides the time; every rank streams its own replica
+    t = torch.tensor([secs, float(step_bytes)], dtype=torch.float64, device="cuda")
+    if world > 1:
+        tmax = t.clone(); torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
+        tsum = t.clone(); torch.distributed.all_reduce(tsum, op=torch.distributed.ReduceOp.SUM)
+        secs, total_bytes = float(tmax[0]), float(tsum[1])
+    else:
+        total_bytes = float(step_bytes)
+    value = total_bytes / secs / 1e9
+    ms_step = secs / args.steps * 1e3
+
+    # per-kernel durations (events around every kernel of the pass, on its stream)
+    prof_steps = max(3, min(20, args.steps))
+    kavg, kper_layer = kernel_profile(r4, prof_steps)
+    names = ["k_router", "k_gate_up", "k_down"]
+    mean_union = float(np.mean([np.mean(u) for u in unions]))
+    alg = [stack.layers[0].E * H * 4, gate_up_bytes(mean_union), down_bytes(mean_union)]
+    dom = int(np.argmax(kavg))
+    achieved = alg[dom] / (kavg[dom] / 1e3) / 1e9
+
+    # q = 1 autoregressive pass
+    r1 = Runner(stack, 1, K_TOP, graph=not args.no_graph)
+    u1 = r1.union_sizes()
+    b1 = [sum(layer_bytes(n) for n in u) for u in u1]
+    s1 = max(10, args.steps // 2)
+    secs1 = timed(r1, s1, args.warmup, world)
+    bytes1 = sum(b1[i % N_BATCHES] for i in range(s1)) * world
+
+    e2e_steps = max(10, min(args.steps, 200))
+    e2e_secs, h2d, d2h = e2e_pass(r4, e2e_steps, world)
+    e2e_bytes = sum(bytes_per_batch[i % N_BATCHES] for i in range(e2e_steps)) * world
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded generator; packed codes uniform, "
+        "binary16 scales U[0.005,0.05], tokens N(0,1) bfloat16)",
+        "config": {"workload": WORKLOAD, "layers": args.layers, "q": Q, "top_k": K_TOP,
+                   "resident_weight_bytes": len(stack.layers) * layer_bytes(E) + len(stack.layers) * E * H * 4,
+                   "l2": "inputs larger than L2: ~150 MB of distinct expert weights per step out of ~99 GB "
+                         "resident, 8 token batches rotate", "graph": r4.graph is not None,
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_hbm_peak": round(value / world / peak, 4),
+        "layer_steps_per_s": round(args.layers * args.steps * world / secs, 1),
+        "verified_tokens_per_s": round(Q * args.steps * world / secs, 1),
+        "stack_passes_per_s": round(args.steps * world / secs, 2),
+        "mean_union_experts": round(mean_union, 3),
+        "q1": {"value": round(bytes1 / secs1 / 1e9, 2), "unit": "GB/s", "ms_per_step": round(secs1 / s1 * 1e3, 4),
+               "layer_steps_per_s": round(args.layers * s1 * world / secs1, 1),
+               "tokens_per_s": round(s1 * world / secs1, 1)},
+        "kernels_ms": {n: round(float(v), 5) for n, v in zip(names, kavg)},
+        "roofline": {"kernel": names[dom], "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(names[dom]), "algorithmic_bytes_per_launch": round(alg[dom]),
+                     "avg_launch_ms": round(float(kavg[dom]), 5)},
+        "e2e": {"value": round(e2e_bytes / e2e_secs / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps * 3 * args.layers,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        import oracle
+        with torch.cuda.stream(r4.stream):
+            tr = torch.empty(args.layers, Q, H, device="cuda")
+            r4.rin.copy_(r4.batches[0])
+            fpx.moe_stack_verify(stack.layers, r4.rin, Q, K_TOP, r4.rL, r4.ws, r4.ws_b, idx_out=r4.idx, r_trace=tr)
+            r4.stream.synchronize()
+        cs, cb, cl = oracle_layer_steps(0, tr.cpu().numpy(), r4.idx.cpu().numpy(), args.cpu_seconds, args.layers)
+        out["cpu_baseline"] = {"value": round(cb / cs / 1e9, 5), "unit": "GB/s", "cores": oracle.threads(),
+                               "kind": "oracle", "sample": f"{cl} whole layer-steps (layers 0..{cl - 1}) of the q=4 "
+                               f"verify pass on token batch 0, teacher-forced on the GPU residual; {cs:.1f} s",
+                               "seconds": round(cs, 2), "bytes": cb}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle as it stands on this host's cores: each step is a bounded sample of the workload
+    (rows of the routed expert matrices one layer-step touches, applied to the q = 4 tokens)."""
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    import bit_block_quantized_wt_b300 as fpx
+    budget = args.ref_seconds
+    layer = 0
+    R = synth.router(E, H, 0, layer)
+    x = synth.tokens_bf16(Q, H, seed=1000)[1].astype(np.float64)
+    route = oracle.route(R, x, K_TOP)
+    uni = list(route["uni"])
+    mats = []
+    for e in uni:
+        mats.append((2, synth.matrix(2, I, H, 0, layer, synth.GATE, e), I, H))
+        mats.append((2, synth.matrix(2, I, H, 0, layer, synth.UP, e), I, H))
+        mats.append((3, synth.matrix(3, H, I, 0, layer, synth.DOWN, e), H, I))
+    hvec = synth.tokens_bf16(Q, I, seed=7)[1].astype(np.float64)
+
+    def sample(rows):
+        t0, nbytes = time.perf_counter(), 0
+        for i, (fmt, m, N, Kd) in enumerate(mats):
+            rb = Kd // 32 * fpx.fpx_block_bytes(fmt)
+            r0 = (i * 97) % (N - rows + 1)
+            oracle.gemv(fmt, m[r0 * rb:(r0 + rows) * rb], rows, Kd, x if Kd == H else hvec)
+            nbytes += rows * rb
+        return time.perf_counter() - t0, nbytes
+
+    dt, _ = sample(16)
+    per_row = dt / 16
+    rows = int(max(4, min(I, budget / (args.steps + args.warmup) / per_row)))
+    for _ in range(args.warmup):
+        sample(rows)
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = sample(rows)
+        tot_t += dt
+        tot_b += nb
+    v = tot_b / tot_t / 1e9
+    desc = (f"per step: {rows} rows of each of the {len(mats)} routed expert matrices (gate/up FP2, down FP3) "
+            f"that one q=4 layer-step touches, applied to the 4 tokens")
+    out = {"impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "GB/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": WORKLOAD, "layers": LAYERS, "q": Q, "top_k": K_TOP},
+           "cpu_baseline": {"value": round(v, 5), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
+                            "sample": desc},
+           "e2e": {"value": round(v, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["fpx", "reference"], default="fpx")
+    p.add_argument("--layers", type=int, default=LAYERS)
+    p.add_argument("--no-graph", action="store_true", help="launch the pass directly instead of a CUDA graph")
+    p.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--ref-seconds", type=float, default=90.0)
+    args = p.parse_args()
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_fpx(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,166 @@
+"""Python binding of libfpx.so: block-quantized FP2/FP3/FP4 GEMVs and the low-bit MoE decode/verify
+step on sm_103a.
+
+Argument marshalling only: every step of the path runs in the CUDA library. Tensors are torch CUDA
+tensors (device memory); the stream defaults to torch's current stream. There is no CPU fallback: if
+libfpx.so is missing or no GPU is present, calls raise.
+
+Names and semantics mirror include/fpx.h. The operations follow the ROCmFPX and decode-path
+paragraphs of "DeepSeek V4 Flash hits 32 tok/s on AMD Ryzen AI MAX+ 395" and the section
+"Lucebox's Optimization Trio" of "Token Freedom via APU: AMD Ryzen AI MAX+ 395 Runs DeepSeek V4 Flash
+at 32 tok/s on a 284B Model".
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfpx.so")
+
+FPX_OK, FPX_EINVAL, FPX_EALIGN, FPX_ERANGE, FPX_ECUDA, FPX_ETIMEOUT, FPX_EDATA, FPX_ESPACE = range(8)
+FPX_FP2, FPX_FP3, FPX_FP4 = 2, 3, 4
+FPX_DTYPE_F32, FPX_DTYPE_BF16 = 0, 1
+
+
+class FpxError(RuntimeError):
+    def __init__(self, status, what):
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+        self.status = status
+
+
+class moe_layer(ctypes.Structure):
+    """Mirror of the C struct: H, I, E and device pointers (router, stacked routed gate/up/down,
+    shared gate/up/down)."""
+    _fields_ = [("H", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int),
+                ("router", ctypes.c_void_p), ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p),
+                ("down", ctypes.c_void_p), ("sh_gate", ctypes.c_void_p), ("sh_up", ctypes.c_void_p),
+                ("sh_down", ctypes.c_void_p)]
+
+
+_lib = None
+
+_SIGS = {
+    "fpx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "fpx_block_bytes": (ctypes.c_size_t, [ctypes.c_int]),
+    "fpx_matrix_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
+    "fpx_read_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "fpx_quantize": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "fpx_dequantize": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "fpx_gemv_q": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                  ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                  ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_route_topk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(moe_layer), ctypes.c_int, ctypes.c_int]),
+    "moe_layer_decode": (ctypes.c_int, [ctypes.POINTER(moe_layer), ctypes.c_void_p, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                        ctypes.c_void_p]),
+    "moe_stack_verify": (ctypes.c_int, [ctypes.POINTER(moe_layer), ctypes.c_int, ctypes.c_void_p,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                        ctypes.c_void_p, ctypes.c_void_p]),
+}
+
+# Every symbol include/fpx.h declares (the export test checks them against the header).
+EXPORTS = tuple(_SIGS)
+
+
+def lib():
+    """Loads libfpx.so (building it first if only the sources are present). Raises if it cannot."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            from . import build as _build
+            _build.build()
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def status_string(status):
+    return lib().fpx_status_string(status).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _check(st, what):
+    if st != FPX_OK:
+        raise FpxError(st, what)
+
+
+def fpx_block_bytes(fmt):
+    return lib().fpx_block_bytes(fmt)
+
+
+def fpx_matrix_bytes(fmt, N, K):
+    return lib().fpx_matrix_bytes(fmt, N, K)
+
+
+def fpx_read_status(dev_status, stream=None):
+    out = ctypes.c_int32(0)
+    _check(lib().fpx_read_status(_ptr(dev_status), ctypes.addressof(out), _stream(stream)), "fpx_read_status")
+    return out.value
+
+
+def fpx_quantize(fmt, W, N, K, out, block_scales=None, dev_status=None, stream=None):
+    _check(lib().fpx_quantize(fmt, _ptr(W), N, K, _ptr(block_scales), _ptr(out), _ptr(dev_status),
+                              _stream(stream)), "fpx_quantize")
+
+
+def fpx_dequantize(fmt, Wq, N, K, W, dev_status=None, stream=None):
+    _check(lib().fpx_dequantize(fmt, _ptr(Wq), N, K, _ptr(W), _ptr(dev_status), _stream(stream)),
+           "fpx_dequantize")
+
+
+def fpx_gemv_q(fmt, Wq, N, K, x, x_dtype, q, y, dev_status=None, stream=None):
+    _check(lib().fpx_gemv_q(fmt, _ptr(Wq), N, K, _ptr(x), x_dtype, q, _ptr(y), _ptr(dev_status),
+                            _stream(stream)), "fpx_gemv_q")
+
+
+def moe_route_topk(R, E, H, x, q, k, logits, idx, w, uni, n_uni, stream=None):
+    _check(lib().moe_route_topk(_ptr(R), E, H, _ptr(x), q, k, _ptr(logits), _ptr(idx), _ptr(w),
+                                _ptr(uni), _ptr(n_uni), _stream(stream)), "moe_route_topk")
+
+
+def moe_workspace_bytes(layer, q, k):
+    return lib().moe_workspace_bytes(ctypes.byref(layer), q, k)
+
+
+def moe_layer_decode(layer, x, q, k, y, ws, ws_bytes, idx_out=None, w_out=None, logits_out=None,
+                     stream=None):
+    _check(lib().moe_layer_decode(ctypes.byref(layer), _ptr(x), q, k, _ptr(y), _ptr(idx_out),
+                                  _ptr(w_out), _ptr(logits_out), _ptr(ws), ws_bytes, _stream(stream)),
+           "moe_layer_decode")
+
+
+def moe_stack_verify(layers, r0, q, k, rL, ws, ws_bytes, idx_out=None, r_trace=None, events=None,
+                     stream=None):
+    """events: optional list of 3*len(layers)+1 raw cudaEvent_t handles (ints), recorded before each
+    kernel and after the last one."""
+    arr = (moe_layer * len(layers))(*layers)
+    ev = None
+    if events is not None:
+        ev = (ctypes.c_void_p * len(events))(*events)
+    _check(lib().moe_stack_verify(arr, len(layers), _ptr(r0), q, k, _ptr(rL), _ptr(idx_out),
+                                  _ptr(r_trace), _ptr(ws), ws_bytes, ev, _stream(stream)), "moe_stack_verify")

@@ -1,0 +1,252 @@
+// Core entry points: sizes, status, dequantize, quantize, and the dense FPX GEMV (CUDA-core path).
+#include "fpx_common.cuh"
+
+#include <cmath>
+
+using namespace fpx;
+
+namespace {
+
+// ------------------------------------------------------------------ dequantize
+
+template <int FMT>
+__global__ void k_dequantize(const uint8_t* __restrict__ Wq, int64_t nblocks, float* __restrict__ W, int32_t* st) {
+    for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nblocks; b += (int64_t)gridDim.x * blockDim.x) {
+        float v[32];
+        float s = decode_levels<FMT>(Wq + b * block_bytes(FMT), v, st);
+        float4* o = reinterpret_cast<float4*>(W + b * 32);
+#pragma unroll
+        for (int j = 0; j < 8; j++) o[j] = make_float4(s * v[4 * j], s * v[4 * j + 1], s * v[4 * j + 2], s * v[4 * j + 3]);
+    }
+}
+
+// ------------------------------------------------------------------ quantize
+
+// FP2/FP3 code from |v| against the exact midpoints 2d, 4d, 6d (ties to the smaller magnitude).
+template <int FMT>
+__device__ __forceinline__ uint32_t odd_code(float v, float d) {
+    float a = fabsf(v);
+    uint32_t i = 0;
+#pragma unroll
+    for (int m = 1; m <= (FMT == 2 ? 1 : 3); m++) i += (a > 2.0f * m * d) ? 1u : 0u;
+    const uint32_t half = FMT == 2 ? 2u : 4u;
+    return signbit(v) ? half - 1u - i : half + i;
+}
+
+// E2M1 magnitude index of t >= 0 (exact binary64): nearest grid value, ties to the even index.
+__device__ __forceinline__ uint32_t e2m1_round(double t) {
+    // grid 0 .5 1 1.5 2 3 4 6; midpoints .25 .75 1.25 1.75 2.5 3.5 5
+    const double mid[7] = {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0};
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 7; i++) {
+        // above the midpoint -> next level; exactly on it -> the even index of the pair
+        if (t > mid[i] || (t == mid[i] && ((i + 1) & 1) == 0)) m = i + 1;
+    }
+    return m;
+}
+
+template <int FMT>
+__global__ void k_quantize(const float* __restrict__ W, int64_t N, int64_t K, const float* __restrict__ scales,
+                           uint8_t* __restrict__ out, int32_t* st) {
+    const int64_t nb = K / 32, total = N * nb;
+    for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < total; b += (int64_t)gridDim.x * blockDim.x) {
+        const float* v = W + (b / nb) * K + (b % nb) * 32;
+        uint8_t* p = out + b * block_bytes(FMT);
+        float amax = 0.0f;
+        bool finite = true;
+        float x[32];
+#pragma unroll
+        for (int j = 0; j < 32; j++) {
+            x[j] = v[j];
+            finite = finite && isfinite(x[j]);
+            amax = fmaxf(amax, fabsf(x[j]));
+        }
+        if (!finite) { flag(st, FPX_ERANGE); continue; }
+        if constexpr (FMT == 2 || FMT == 3) {
+            double src = scales ? (double)scales[b] : (double)amax / (FMT == 2 ? 3.0 : 7.0);
+            if (scales && !(src >= 0.0 && src <= 3.4e38)) { flag(st, FPX_EINVAL); continue; }
+            __half h = __double2half(src);
+            uint16_t hb = __half_as_ushort(h);
+            if ((hb & 0x7C00u) == 0x7C00u) { flag(st, FPX_ERANGE); continue; }
+            float d = __half2float(h);
+            uint32_t lo[2] = {0u, 0u}, hi = 0u;
+#pragma unroll
+            for (int j = 0; j < 32; j++) {
+                uint32_t c = odd_code<FMT>(x[j], d);
+                lo[j >> 4] |= (c & 3u) << (2 * (j & 15));
+                if (FMT == 3) hi |= ((c >> 2) & 1u) << j;
+            }
+            p[0] = hb & 0xFF; p[1] = hb >> 8;
+#pragma unroll
+            for (int i = 0; i < 4; i++) { p[2 + i] = (lo[0] >> (8 * i)) & 0xFF; p[6 + i] = (lo[1] >> (8 * i)) & 0xFF; }
+            if (FMT == 3) {
+#pragma unroll
+                for (int i = 0; i < 4; i++) p[10 + i] = (hi >> (8 * i)) & 0xFF;
+            }
+        } else {
+            int e;
+            if (scales) {
+                float s = scales[b];
+                int ex;
+                float m = frexpf(s, &ex);
+                e = ex - 1 + 127;
+                if (!(s > 0.0f) || !isfinite(s) || m != 0.5f || e < 0 || e > 254) { flag(st, FPX_EINVAL); continue; }
+            } else if (amax == 0.0f) {
+                e = 0;
+            } else {
+                int ex;
+                frexpf(amax, &ex);  // floor(log2 amax) = ex - 1
+                e = min(254, max(0, ex - 1 - 2 + 127));
+            }
+            const double inv = ldexp(1.0, 127 - e);
+            p[0] = (uint8_t)e;
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                uint32_t q0 = e2m1_round(fabs((double)x[2 * j]) * inv) | (signbit(x[2 * j]) ? 8u : 0u);
+                uint32_t q1 = e2m1_round(fabs((double)x[2 * j + 1]) * inv) | (signbit(x[2 * j + 1]) ? 8u : 0u);
+                p[1 + j] = (uint8_t)(q0 | (q1 << 4));
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ GEMV, CUDA-core path
+
+constexpr int kGemvThreads = 256;
+
+template <int FMT, int Q, bool XSMEM>
+__global__ void __launch_bounds__(kGemvThreads) k_gemv_cc(const uint8_t* __restrict__ Wq, int N, int K, const void* x,
+                                                          int x_bf16, float* __restrict__ y, int32_t* st) {
+    extern __shared__ float xs[];
+    const int xstride = padded_len(K);
+    if (XSMEM) {
+        for (int i = threadIdx.x; i < Q * K; i += blockDim.x) {
+            int t = i / K, k = i % K;
+            float v = x_bf16 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(x)[i]) : reinterpret_cast<const float*>(x)[i];
+            xs[t * xstride + padded_index(k)] = v;
+        }
+        __syncthreads();
+    }
+    const int lane = threadIdx.x & 31;
+    const int warps = blockDim.x / 32;
+    const int nblk = K / 32;
+    const int64_t row_bytes = (int64_t)nblk * block_bytes(FMT);
+    for (int r = blockIdx.x * warps + threadIdx.x / 32; r < N; r += gridDim.x * warps) {
+        float acc[Q];
+        if (XSMEM) row_dot<FMT, Q>(Wq + r * row_bytes, nblk, XShared{xs, xstride}, lane, acc, st);
+        else row_dot<FMT, Q>(Wq + r * row_bytes, nblk, XGlobal{x, K, x_bf16}, lane, acc, st);
+        if (lane < Q) {
+            float o = acc[0];
+#pragma unroll
+            for (int t = 1; t < Q; t++) o = lane == t ? acc[t] : o;
+            y[(int64_t)lane * N + r] = o;
+        }
+    }
+}
+
+template <int FMT, int Q>
+int launch_gemv_cc_q(const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_bf16, float* y, int32_t* st,
+                     cudaStream_t s) {
+    DeviceInfo di = device_info();
+    size_t smem = (size_t)Q * padded_len((int)K) * sizeof(float);
+    int64_t grid64 = (N + 7) / 8;
+    int grid = (int)(grid64 < di.sms * 4 ? grid64 : di.sms * 4);
+    if (grid < 1) grid = 1;
+    if ((int64_t)smem <= di.smem_optin) {
+        if (cudaFuncSetAttribute(k_gemv_cc<FMT, Q, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))
+            return FPX_ECUDA;
+        k_gemv_cc<FMT, Q, true><<<grid, kGemvThreads, smem, s>>>(Wq, (int)N, (int)K, x, x_bf16, y, st);
+    } else {
+        k_gemv_cc<FMT, Q, false><<<grid, kGemvThreads, 0, s>>>(Wq, (int)N, (int)K, x, x_bf16, y, st);
+    }
+    return launch_status();
+}
+
+template <int FMT>
+int launch_gemv_cc(const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_bf16, int q, float* y, int32_t* st,
+                   cudaStream_t s) {
+    switch (q) {
+        case 1: return launch_gemv_cc_q<FMT, 1>(Wq, N, K, x, x_bf16, y, st, s);
+        case 2: return launch_gemv_cc_q<FMT, 2>(Wq, N, K, x, x_bf16, y, st, s);
+        case 3: return launch_gemv_cc_q<FMT, 3>(Wq, N, K, x, x_bf16, y, st, s);
+        case 4: return launch_gemv_cc_q<FMT, 4>(Wq, N, K, x, x_bf16, y, st, s);
+        default: return FPX_EINVAL;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fpx_status_string(int status) {
+    switch (status) {
+        case FPX_OK: return "ok";
+        case FPX_EINVAL: return "invalid argument";
+        case FPX_EALIGN: return "misaligned pointer";
+        case FPX_ERANGE: return "non-finite input or scale overflow";
+        case FPX_ECUDA: return "CUDA error";
+        case FPX_ETIMEOUT: return "device wait timed out";
+        case FPX_EDATA: return "invalid block or routing index";
+        case FPX_ESPACE: return "workspace too small";
+        default: return "unknown status";
+    }
+}
+
+size_t fpx_block_bytes(int fmt) { return (size_t)block_bytes(fmt); }
+
+int64_t fpx_matrix_bytes(int fmt, int64_t N, int64_t K) { return matrix_bytes(fmt, N, K); }
+
+int fpx_read_status(const int32_t* dev_status, int32_t* host_out, void* stream) {
+    if (!dev_status || !host_out) return FPX_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(host_out, dev_status, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess) return FPX_ECUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? FPX_OK : FPX_ECUDA;
+}
+
+int fpx_dequantize(int fmt, const uint8_t* Wq, int64_t N, int64_t K, float* W, int32_t* dev_status, void* stream) {
+    if (matrix_bytes(fmt, N, K) < 0) return FPX_EINVAL;
+    if (N == 0 || K == 0) return FPX_OK;
+    if (!Wq || !W) return FPX_EINVAL;
+    if (!aligned(Wq, 16) || !aligned(W, 16)) return FPX_EALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int64_t nb = N * (K / 32);
+    int grid = (int)((nb + 255) / 256 < 148 * 8 ? (nb + 255) / 256 : 148 * 8);
+    if (fmt == 2) k_dequantize<2><<<grid, 256, 0, s>>>(Wq, nb, W, dev_status);
+    else if (fmt == 3) k_dequantize<3><<<grid, 256, 0, s>>>(Wq, nb, W, dev_status);
+    else k_dequantize<4><<<grid, 256, 0, s>>>(Wq, nb, W, dev_status);
+    return launch_status();
+}
+
+int fpx_quantize(int fmt, const float* W, int64_t N, int64_t K, const float* block_scales, uint8_t* out,
+                 int32_t* dev_status, void* stream) {
+    if (matrix_bytes(fmt, N, K) < 0) return FPX_EINVAL;
+    if (N == 0 || K == 0) return FPX_OK;
+    if (!W || !out) return FPX_EINVAL;
+    if (!aligned(out, 16) || !aligned(W, 16) || (block_scales && !aligned(block_scales, 4))) return FPX_EALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int64_t nb = N * (K / 32);
+    int grid = (int)((nb + 127) / 128 < 148 * 8 ? (nb + 127) / 128 : 148 * 8);
+    if (fmt == 2) k_quantize<2><<<grid, 128, 0, s>>>(W, N, K, block_scales, out, dev_status);
+    else if (fmt == 3) k_quantize<3><<<grid, 128, 0, s>>>(W, N, K, block_scales, out, dev_status);
+    else k_quantize<4><<<grid, 128, 0, s>>>(W, N, K, block_scales, out, dev_status);
+    return launch_status();
+}
+
+int fpx_gemv_q(int fmt, const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_dtype, int q, float* y,
+               int32_t* dev_status, void* stream) {
+    if (matrix_bytes(fmt, N, K) < 0 || q < 1 || q > 4 || (x_dtype != FPX_DTYPE_F32 && x_dtype != FPX_DTYPE_BF16))
+        return FPX_EINVAL;
+    if (N > INT32_MAX || K > INT32_MAX / 8) return FPX_EINVAL;
+    if (N == 0) return FPX_OK;
+    if (!Wq || !x || !y) return FPX_EINVAL;
+    if (!aligned(Wq, 16) || !aligned(x, 4) || !aligned(y, 4)) return FPX_EALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return cudaMemsetAsync(y, 0, sizeof(float) * (size_t)q * N, s) == cudaSuccess ? FPX_OK : FPX_ECUDA;
+    int bf = x_dtype == FPX_DTYPE_BF16;
+    if (fmt == 2) return launch_gemv_cc<2>(Wq, N, K, x, bf, q, y, dev_status, s);
+    if (fmt == 3) return launch_gemv_cc<3>(Wq, N, K, x, bf, q, y, dev_status, s);
+    return launch_gemv_cc<4>(Wq, N, K, x, bf, q, y, dev_status, s);
+}
+
+}  // extern "C"

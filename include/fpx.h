@@ -1,0 +1,159 @@
+/* fpx.h - C ABI of libfpx.so: block-quantized (FP2/FP3/FP4) GEMVs and the low-bit MoE
+ * decode/verify step, hand-written CUDA for sm_103a (B300).
+ *
+ * Sources. The operations follow the public descriptions of the ROCmFPX formats and the DeepSeek V4
+ * Flash decode path:
+ *   [P-dsv4] "DeepSeek V4 Flash hits 32 tok/s on AMD Ryzen AI MAX+ 395" - paragraph 2 (the ROCmFPX
+ *            family: 32-weight blocks of packed codes plus scales, FP2 10 bytes / 2.50 bits,
+ *            FP3 3.50 bits, FP4 4.25 bits; FP2 routed gate/up, FP3 routed down, FP4 dense and
+ *            sensitive projections) and paragraph 3 (memory-bound decode over 43 layers; each packed
+ *            weight decoded once and applied to all four verification columns; TOP_K and ARGSORT
+ *            kernels on the routing path; q = 4 verification in one fused pass).
+ *   [P-apu]  "Token Freedom via APU: AMD Ryzen AI MAX+ 395 Runs DeepSeek V4 Flash at 32 tok/s on a
+ *            284B Model" - section "Lucebox's Optimization Trio" (256 routed + 1 shared expert,
+ *            6 active by default; q = 4 weight reuse; TOP-K / ARGSORT).
+ *   [P-zh]   the zh-TW page, section "DSpark：在記憶體頻寬受限的 APU 上做 speculative decoding"
+ *            (verify four positions, including the seed, in one graph pass).
+ * The pages publish no API, byte layout or code; everything below that they leave open is a reading
+ * made by this project and is stated where it is used.
+ *
+ * Block layouts (little-endian; 32 weights per block; a matrix W[N][K], K % 32 == 0, is row-major
+ * with K/32 blocks per row and occupies fpx_matrix_bytes(), i.e. N*K/32*B rounded up to 16 bytes):
+ *   FP2, 10 B: [0..1] binary16 scale d; [2..9] codes, c_j = bits 2j..2j+1; w_j = d*(2c_j - 3).
+ *   FP3, 14 B: [0..1] binary16 d; [2..9] low bits l_j = bits 2j..2j+1; [10..13] high bit h_j = bit j;
+ *              c = l + 4h; w_j = d*(2c_j - 7).
+ *   FP4, 17 B: [0] E8M0 exponent e (scale 2^(e-127), 255 invalid); [1..16] E2M1 codes,
+ *              q_j = bits 4j..4j+3 (sign bit 3, magnitude {0,.5,1,1.5,2,3,4,6}) - OCP MXFP4.
+ *
+ * Conventions for every call:
+ *   - Pointers named in a signature are DEVICE pointers owned by the caller, unless a comment says
+ *     host. Matrix and workspace pointers must be 16-byte aligned (FPX_EALIGN otherwise); vectors 4-.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream), never
+ *     allocate and never synchronise; they are safe to capture in a CUDA graph. The return value
+ *     reports argument errors and launch failures only.
+ *   - Errors the device detects (an FP4 scale byte of 255, a non-finite quantizer input, an expert
+ *     index out of range) set bit (1 << status) of a device status word: the `dev_status` argument
+ *     (the caller zeroes it), or the first word of the workspace (zeroed by each layer or stack call
+ *     when it starts). Read it after the stream completes (fpx_read_status).
+ *   - Results are deterministic: no floating-point atomics; every reduction has a fixed order that
+ *     depends on neither q nor the other columns, so column t of a q-column call is bit-identical to
+ *     the same column computed alone.
+ */
+#ifndef FPX_H
+#define FPX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FPX_OK = 0,
+    FPX_EINVAL = 1,   /* bad format, shape, q, k or dtype */
+    FPX_EALIGN = 2,   /* a pointer is not aligned as required */
+    FPX_ERANGE = 3,   /* non-finite quantizer input or scale overflow (device-detected) */
+    FPX_ECUDA = 4,    /* a CUDA launch or attribute call failed */
+    FPX_ETIMEOUT = 5, /* a bounded device-side wait gave up */
+    FPX_EDATA = 6,    /* invalid block (FP4 scale 255) or routing index (device-detected) */
+    FPX_ESPACE = 7    /* the workspace passed is smaller than the *_workspace_bytes query */
+} fpx_status;
+
+enum { FPX_FP2 = 2, FPX_FP3 = 3, FPX_FP4 = 4 };
+enum { FPX_DTYPE_F32 = 0, FPX_DTYPE_BF16 = 1 };
+
+const char* fpx_status_string(int status);
+
+/* Bytes per 32-weight block: 10 / 14 / 17 for FP2 / FP3 / FP4, 0 for any other format. [P-dsv4] */
+size_t fpx_block_bytes(int fmt);
+
+/* Storage bytes of a packed N x K matrix (N*K/32 blocks, rounded up to 16), or -1 when K % 32 != 0,
+ * N < 0 or the format is unknown. Stacked expert matrices use this value as their stride. */
+int64_t fpx_matrix_bytes(int fmt, int64_t N, int64_t K);
+
+/* Host call: copies the device status word *dev_status to *host_out after synchronising `stream`.
+ * The only call that synchronises. */
+int fpx_read_status(const int32_t* dev_status, int32_t* host_out, void* stream);
+
+/* Quantize W[N][K] (binary32, row-major) into packed blocks at `out` (fpx_matrix_bytes bytes).
+ * Per block: FP2/FP3 scale d = RN_binary16(amax/3 or amax/7) (or RN_binary16(block_scales[b])),
+ * codes = nearest level, ties toward the smaller magnitude, sign = signbit; FP4 e = floor(log2 amax)
+ * - 2 + 127 clamped to [0, 254] (or the exponent of block_scales[b], which must be a power of two),
+ * codes = E2M1 round-to-nearest-even, saturating. block_scales (nullable) holds N*K/32 binary32
+ * scales to use instead of the amax rule. A non-finite input or a binary16 overflow sets the
+ * FPX_ERANGE bit (an unusable given scale the FPX_EINVAL bit) of *dev_status (nullable) and leaves
+ * that block's bytes undefined. [P-dsv4] paragraph 2. */
+int fpx_quantize(int fmt, const float* W, int64_t N, int64_t K, const float* block_scales,
+                 uint8_t* out, int32_t* dev_status, void* stream);
+
+/* Decode packed blocks into W[N][K] binary32 (every value is exact). An FP4 scale byte of 255 sets
+ * the FPX_EDATA bit of *dev_status (nullable) and decodes that block as zeros. [P-dsv4] paragraph 2. */
+int fpx_dequantize(int fmt, const uint8_t* Wq, int64_t N, int64_t K, float* W, int32_t* dev_status,
+                   void* stream);
+
+/* y[t][n] = sum_k W[n][k] * x[t][k] for t < q (1 <= q <= 4): the dense FPX GEMV of the verify step.
+ * Every packed block is read from memory and decoded once per call, whatever q. x is [q][K]
+ * contiguous, binary32 (x_dtype FPX_DTYPE_F32) or bfloat16 (FPX_DTYPE_BF16); y is [q][N] binary32.
+ * Column t of the result is bit-identical to a q = 1 call on x[t]. An FP4 scale byte of 255 sets
+ * the FPX_EDATA bit of *dev_status (nullable; that block counts as zeros). [P-dsv4] paragraph 3, [P-apu]. */
+int fpx_gemv_q(int fmt, const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_dtype, int q,
+               float* y, int32_t* dev_status, void* stream);
+
+/* Router + top-k + normalise + union for q tokens (1 <= q <= 4): logits[t][e] = sum_h R[e][h] x[t][h]
+ * (R binary32 [E][H], x bfloat16 [q][H]); idx[t][r], r < k, the k largest logits in descending order,
+ * ties to the lower expert index; w[t][r] = sigmoid(l) / sum over the k selected sigmoids; uni the
+ * sorted distinct experts of all tokens (n_uni of them, at most q*k; uni has q*k entries).
+ * Limits: 1 <= k <= 8, k <= E <= 1024, H % 8 == 0. logits [q][E] is required: it is also the
+ * top-k input. [P-apu], [P-dsv4] paragraph 3. */
+int moe_route_topk(const float* R, int E, int H, const uint16_t* x, int q, int k, float* logits,
+                   int32_t* idx, float* w, int32_t* uni, int32_t* n_uni, void* stream);
+
+/* One MoE layer's weights (device pointers inside a host struct). Routed experts e = 0..E-1 are
+ * stacked: expert e's gate matrix starts at gate + e*fpx_matrix_bytes(FP2, I, H); likewise up (FP2,
+ * I x H) and down (FP3, H x I). The shared expert is FP4: sh_gate, sh_up [I][H], sh_down [H][I].
+ * router is binary32 [E][H]. H and I are multiples of 256. [P-dsv4] paragraph 2, [P-apu]. */
+typedef struct {
+    int H, I, E;
+    const float* router;
+    const uint8_t* gate;
+    const uint8_t* up;
+    const uint8_t* down;
+    const uint8_t* sh_gate;
+    const uint8_t* sh_up;
+    const uint8_t* sh_down;
+} moe_layer;
+
+/* Workspace bytes moe_layer_decode / moe_stack_verify need for these shapes (16-byte aligned). */
+size_t moe_workspace_bytes(const moe_layer* layer, int q, int k);
+
+/* One MoE decode/verify layer for q tokens (1 <= q <= 4, 1 <= k <= 8): route each token, run every
+ * selected expert once for all q columns (g = G x, u = U x, h = silu(g) u in binary32, y = D h), the
+ * shared expert for all tokens, and combine out[t] = sum_r w[t][r] y_{e(t,r)}[t] + y_shared[t]
+ * (ranks in order, shared last). x is bfloat16 [q][H], y binary32 [q][H]; idx_out (nullable) gets
+ * idx[q][k], w_out (nullable) w[q][k], logits_out (nullable) logits[q][E]. `ws` must hold
+ * moe_workspace_bytes(layer, q, k) bytes (ws_bytes); its first word is the status word. The layer
+ * pointer is read on the host during the call only. [P-dsv4] paragraph 3, [P-zh], [P-apu]. */
+int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, float* y,
+                     int32_t* idx_out, float* w_out, float* logits_out, void* ws, size_t ws_bytes,
+                     void* stream);
+
+/* The verify pass over a stack of n_layers layers (host array of structs, all with the same H, I,
+ * E): state r binary32 [q][H] starts at r0; layer l takes u_l = RN_bfloat16(r_l / sqrt(mean(r_l^2)
+ * + 1e-6)) and sets r_{l+1} = r_l + MoE_l(u_l). rL receives r_{n_layers}; r0 and rL may alias.
+ * idx_out (nullable) gets idx[n_layers][q][k]; r_trace (nullable) gets r_l for l = 0..n_layers-1
+ * ([n_layers][q][H]). Enqueues 3 kernels per layer (router, gate/up, down) and nothing else, so the
+ * whole pass can be captured as one CUDA graph. events (nullable) is a host array of
+ * 3*n_layers + 1 cudaEvent_t: events[3l + j] is recorded on `stream` just before kernel j of layer
+ * l and events[3*n_layers] after the last kernel, so a caller can time each kernel.
+ * The normalisation is this project's reading (the pages do not define the residual stream):
+ * without it the synthetic state overflows binary32 within a few dozen layers.
+ * [P-dsv4] paragraph 3 (43 layers; every token streams the active weights of all layers). */
+int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int q, int k, float* rL,
+                     int32_t* idx_out, float* r_trace, void* ws, size_t ws_bytes, void* const* events,
+                     void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FPX_H */

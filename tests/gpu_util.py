@@ -1,0 +1,91 @@
+"""Helpers for the GPU parity tests: device tensors, synthetic layers built by the device generator,
+and host copies of the experts the oracle needs."""
+import numpy as np
+import pytest
+import torch
+
+import bit_block_quantized_wt_b300 as fpx
+import synth
+
+
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def status_word():
+    return torch.zeros(4, dtype=torch.int32, device="cuda")
+
+
+def read_status(st):
+    return fpx.fpx_read_status(st)
+
+
+class DeviceLayer:
+    """One MoE layer generated on the device with the seeded generator (layer index `layer`)."""
+
+    def __init__(self, H, I, E, seed=0, layer=0):
+        self.H, self.I, self.E, self.seed, self.layer = H, I, E, seed, layer
+        self.mb_gu = fpx.fpx_matrix_bytes(2, I, H)
+        self.mb_d = fpx.fpx_matrix_bytes(3, H, I)
+        self.mb_s = fpx.fpx_matrix_bytes(4, I, H)
+        self.gate = torch.empty(E * self.mb_gu, dtype=torch.uint8, device="cuda")
+        self.up = torch.empty(E * self.mb_gu, dtype=torch.uint8, device="cuda")
+        self.down = torch.empty(E * self.mb_d, dtype=torch.uint8, device="cuda")
+        self.sh = [torch.empty(self.mb_s, dtype=torch.uint8, device="cuda") for _ in range(3)]
+        s = torch.cuda.current_stream().cuda_stream
+        synth.device_matrices(2, seed, layer, synth.GATE, 0, E, I, H, self.gate.data_ptr(), self.mb_gu, s)
+        synth.device_matrices(2, seed, layer, synth.UP, 0, E, I, H, self.up.data_ptr(), self.mb_gu, s)
+        synth.device_matrices(3, seed, layer, synth.DOWN, 0, E, H, I, self.down.data_ptr(), self.mb_d, s)
+        synth.device_matrices(4, seed, layer, synth.SH_GATE, 0, 1, I, H, self.sh[0].data_ptr(), self.mb_s, s)
+        synth.device_matrices(4, seed, layer, synth.SH_UP, 0, 1, I, H, self.sh[1].data_ptr(), self.mb_s, s)
+        synth.device_matrices(4, seed, layer, synth.SH_DOWN, 0, 1, H, I, self.sh[2].data_ptr(), self.mb_s, s)
+        self.R_host = synth.router(E, H, seed, layer)
+        self.router = dev(self.R_host)
+        self.c = fpx.moe_layer(H=H, I=I, E=E, router=self.router.data_ptr(), gate=self.gate.data_ptr(),
+                               up=self.up.data_ptr(), down=self.down.data_ptr(), sh_gate=self.sh[0].data_ptr(),
+                               sh_up=self.sh[1].data_ptr(), sh_down=self.sh[2].data_ptr())
+
+    def host_experts(self, experts):
+        """Host copies (from the host generator) of the listed routed experts and the shared expert,
+        as the oracle's E-length pointer lists."""
+        H, I, E, seed, layer = self.H, self.I, self.E, self.seed, self.layer
+        g, u, d = [None] * E, [None] * E, [None] * E
+        for e in sorted(set(int(v) for v in experts)):
+            g[e] = synth.matrix(2, I, H, seed, layer, synth.GATE, e)
+            u[e] = synth.matrix(2, I, H, seed, layer, synth.UP, e)
+            d[e] = synth.matrix(3, H, I, seed, layer, synth.DOWN, e)
+        sg = synth.matrix(4, I, H, seed, layer, synth.SH_GATE)
+        su = synth.matrix(4, I, H, seed, layer, synth.SH_UP)
+        sd = synth.matrix(4, H, I, seed, layer, synth.SH_DOWN)
+        return g, u, d, sg, su, sd
+
+    def oracle(self, x, k, idx_force=None):
+        import oracle
+        experts = idx_force.ravel() if idx_force is not None else range(self.E)
+        g, u, d, sg, su, sd = self.host_experts(experts)
+        return oracle.moe_layer(self.H, self.I, self.E, self.R_host, g, u, d, sg, su, sd, x, k, idx_force=idx_force)
+
+
+def topk_of(logits_row, k):
+    """Top-k of one row (descending, ties to the lower index) by a stable sort on the negated value."""
+    order = np.argsort(-np.asarray(logits_row, np.float64), kind="stable")
+    return order[:k]
+
+
+def routing_gap_ok(logits, k, bound):
+    """True when the k-th and (k+1)-th largest logits of every row differ by more than `bound`, so the
+    top-k set is unique within that error."""
+    s = -np.sort(-logits, axis=1)
+    if s.shape[1] <= k:
+        return np.ones(s.shape[0], bool)
+    return (s[:, k - 1] - s[:, k]) > bound

@@ -1,0 +1,91 @@
+"""The C ABI without a GPU: the library loads, exports every symbol include/fpx.h declares, and rejects
+bad arguments before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_block_quantized_wt_b300 as fpx
+from conftest import ROOT
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "fpx.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|int64_t|size_t|int)\s+(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert len(names) >= 10
+    L = fpx.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(fpx.EXPORTS) == names
+
+
+def test_sizes_and_strings():
+    assert [fpx.fpx_block_bytes(f) for f in (2, 3, 4, 5)] == [10, 14, 17, 0]
+    assert fpx.fpx_matrix_bytes(2, 2048, 4096) == 2621440
+    assert fpx.fpx_matrix_bytes(4, 3, 32) == 64
+    assert fpx.fpx_matrix_bytes(3, 1, 33) == -1
+    assert fpx.status_string(fpx.FPX_EDATA) == "invalid block or routing index"
+
+
+FAKE = 1 << 20  # an aligned non-null address; these calls must fail before touching it
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((5, FAKE, 8, 64, FAKE, 1, 1, FAKE), fpx.FPX_EINVAL),   # unknown format
+    ((2, FAKE, 8, 60, FAKE, 1, 1, FAKE), fpx.FPX_EINVAL),   # K % 32 != 0
+    ((2, FAKE, 8, 64, FAKE, 1, 0, FAKE), fpx.FPX_EINVAL),   # q = 0
+    ((2, FAKE, 8, 64, FAKE, 1, 5, FAKE), fpx.FPX_EINVAL),   # q = 5
+    ((2, FAKE, 8, 64, FAKE, 7, 1, FAKE), fpx.FPX_EINVAL),   # dtype
+    ((2, None, 8, 64, FAKE, 1, 1, FAKE), fpx.FPX_EINVAL),   # null weights
+    ((2, FAKE + 8, 8, 64, FAKE, 1, 1, FAKE), fpx.FPX_EALIGN),  # weights not 16-byte aligned
+    ((2, FAKE, 8, 64, FAKE + 2, 1, 1, FAKE), fpx.FPX_EALIGN),  # x not 4-byte aligned
+])
+def test_gemv_argument_errors(args, expect):
+    fmt, W, N, K, x, dt, q, y = args
+    assert fpx.lib().fpx_gemv_q(fmt, W, N, K, x, dt, q, y, None, None) == expect
+
+
+def _layer(**kw):
+    d = dict(H=512, I=256, E=16, router=FAKE, gate=FAKE, up=FAKE, down=FAKE, sh_gate=FAKE, sh_up=FAKE,
+             sh_down=FAKE)
+    d.update(kw)
+    return fpx.moe_layer(**d)
+
+
+def test_layer_argument_errors():
+    L = fpx.lib()
+    ws = fpx.moe_workspace_bytes(_layer(), 4, 4)
+    assert ws > 0 and ws % 16 == 0
+    good = _layer()
+    call = lambda lay, q=4, k=4, wsb=ws, wsp=FAKE: L.moe_layer_decode(ctypes.byref(lay), FAKE, q, k, FAKE, None, None,
+                                                                     None, wsp, wsb, None)
+    assert call(_layer(H=500)) == fpx.FPX_EINVAL
+    assert call(_layer(I=100)) == fpx.FPX_EINVAL
+    assert call(_layer(E=0)) == fpx.FPX_EINVAL
+    assert call(_layer(down=None)) == fpx.FPX_EINVAL
+    assert call(_layer(gate=FAKE + 4)) == fpx.FPX_EALIGN
+    assert call(good, q=5) == fpx.FPX_EINVAL
+    assert call(good, k=9) == fpx.FPX_EINVAL
+    assert call(good, k=17) == fpx.FPX_EINVAL
+    assert call(good, wsb=ws - 16) == fpx.FPX_ESPACE
+    assert call(good, wsp=FAKE + 8) == fpx.FPX_EALIGN
+    arr = (fpx.moe_layer * 2)(good, _layer(I=512))
+    assert L.moe_stack_verify(arr, 2, FAKE, 4, 4, FAKE, None, None, FAKE, ws, None, None) == fpx.FPX_EINVAL
+    assert L.moe_stack_verify(arr, 0, FAKE, 4, 4, FAKE, None, None, FAKE, ws, None, None) == fpx.FPX_EINVAL
+
+
+def test_route_and_quant_argument_errors():
+    L = fpx.lib()
+    assert L.moe_route_topk(FAKE, 8, 64, FAKE, 4, 9, FAKE, FAKE, FAKE, FAKE, FAKE, None) == fpx.FPX_EINVAL
+    assert L.moe_route_topk(FAKE, 8, 64, FAKE, 4, 2, None, FAKE, FAKE, FAKE, FAKE, None) == fpx.FPX_EINVAL
+    assert L.moe_route_topk(FAKE, 2000, 64, FAKE, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None) == fpx.FPX_EINVAL
+    assert L.fpx_quantize(2, FAKE, 4, 48, None, FAKE, None, None) == fpx.FPX_EINVAL
+    assert L.fpx_quantize(2, FAKE, 4, 64, None, FAKE + 1, None, None) == fpx.FPX_EALIGN
+    assert L.fpx_dequantize(9, FAKE, 4, 64, FAKE, None, None) == fpx.FPX_EINVAL
+    assert L.fpx_read_status(None, None, None) == fpx.FPX_EINVAL

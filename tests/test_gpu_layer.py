@@ -1,0 +1,67 @@
+"""moe_layer_decode against the oracle: routing bit-exact, output within 2e-3 * M (the first-order
+error magnitude), columns bit-identical across q."""
+import numpy as np
+import pytest
+import torch
+
+import bit_block_quantized_wt_b300 as fpx
+import synth
+from gpu_util import DeviceLayer, dev, host, need_gpu, read_status, routing_gap_ok, topk_of
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+def run_layer(L, bits, k):
+    q = bits.shape[0]
+    ws_b = fpx.moe_workspace_bytes(L.c, q, k)
+    ws = torch.empty(ws_b, dtype=torch.uint8, device="cuda")
+    y = torch.full((q, L.H), float("nan"), device="cuda")
+    idx = torch.empty(q, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(q, k, device="cuda")
+    lg = torch.empty(q, L.E, device="cuda")
+    fpx.moe_layer_decode(L.c, dev(bits), q, k, y, ws, ws_b, idx_out=idx, w_out=w, logits_out=lg)
+    st = read_status(ws[:4].view(torch.int32))
+    assert st == 0
+    return host(y), host(idx), host(w), host(lg)
+
+
+def check_layer(L, bits, vals, k):
+    y, idx, w, lg = run_layer(L, bits, k)
+    q = bits.shape[0]
+    for t in range(q):
+        assert list(idx[t]) == list(topk_of(lg[t], k))
+    orc = L.oracle(vals.astype(np.float64), k, idx_force=idx)
+    assert np.all(np.abs(lg - orc["logits"]) <= 1e-4 + 1e-4 * np.abs(orc["logits"]))
+    # where the oracle's own top-k is unique within the logit error, it must agree
+    own = L.oracle(vals.astype(np.float64), k) if L.E <= 64 else None
+    if own is not None:
+        ok = routing_gap_ok(own["logits"], k, 1e-4)
+        assert np.array_equal(own["idx"][ok], idx[ok])
+    assert np.allclose(w, orc["w"], rtol=1e-5, atol=0)
+    err = np.abs(y.astype(np.float64) - orc["y"])
+    assert np.all(err <= TOL * orc["M"]), float((err / orc["M"]).max())
+    return y, idx
+
+
+@pytest.mark.parametrize("q", [1, 2, 3, 4])
+@pytest.mark.parametrize("k", [1, 2, 4])
+def test_layer_small(q, k):
+    need_gpu()
+    L = DeviceLayer(256, 256, 16, seed=q * 10 + k)
+    bits, vals = synth.tokens_bf16(q, 256, seed=k)
+    y, idx = check_layer(L, bits, vals, k)
+    for t in range(q):  # q-identity
+        y1, i1, _, _ = run_layer(L, bits[t : t + 1], k)
+        assert np.array_equal(y1[0], y[t]) and np.array_equal(i1[0], idx[t])
+
+
+@pytest.mark.parametrize("k", [4, 6])
+def test_layer_config3_full_size(k):
+    """hidden 4096, 256 routed experts (FP2 gate/up [2048x4096], FP3 down), FP4 shared, q = 4."""
+    need_gpu()
+    L = DeviceLayer(4096, 2048, 256, seed=0, layer=0)
+    bits, vals = synth.tokens_bf16(4, 4096, seed=0)
+    y, idx = check_layer(L, bits, vals, k)
+    y1, i1, _, _ = run_layer(L, bits[3:4], k)
+    assert np.array_equal(y1[0], y[3]) and np.array_equal(i1[0], idx[3])
