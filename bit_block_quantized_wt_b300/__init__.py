@@ -58,6 +58,10 @@ _SIGS = {
                                         ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                         ctypes.c_void_p]),
+    "moe_layer_decode_static_ws": (ctypes.c_int, [ctypes.POINTER(moe_layer), ctypes.c_void_p, ctypes.c_int,
+                                                  ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                  ctypes.c_void_p]),
     "moe_stack_verify": (ctypes.c_int, [ctypes.POINTER(moe_layer), ctypes.c_int, ctypes.c_void_p,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
@@ -152,6 +156,16 @@ def moe_layer_decode(layer, x, q, k, y, ws, ws_bytes, idx_out=None, w_out=None, 
     _check(lib().moe_layer_decode(ctypes.byref(layer), _ptr(x), q, k, _ptr(y), _ptr(idx_out),
                                   _ptr(w_out), _ptr(logits_out), _ptr(ws), ws_bytes, _stream(stream)),
            "moe_layer_decode")
+
+
+def moe_layer_decode_static_ws(layer, x, q, k, y, idx_out=None, w_out=None, logits_out=None,
+                               dev_status=None, stream=None):
+    """moe_layer_decode without a caller workspace, for callers that cannot allocate device memory
+    (see include/fpx.h). The first call on a device must come before any stream capture; calls that
+    overlap on the GPU share one scratch array and race."""
+    _check(lib().moe_layer_decode_static_ws(ctypes.byref(layer), _ptr(x), q, k, _ptr(y), _ptr(idx_out),
+                                            _ptr(w_out), _ptr(logits_out), _ptr(dev_status), _stream(stream)),
+           "moe_layer_decode_static_ws")
 
 
 def moe_stack_verify(layers, r0, q, k, rL, ws, ws_bytes, idx_out=None, r_trace=None, events=None,

@@ -492,3 +492,60 @@ int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ fixed-scratch variant
+//
+// Some callers cannot allocate device memory: code that runs inside a host framework which owns every
+// device allocation (a fixed arena or its own allocator) and forbids others, and latency-critical
+// loops where cudaMalloc/cudaFree are off limits because they can synchronise the device. For them,
+// moe_layer_decode_static_ws runs the same layer with its scratch in the array below, which exists
+// once per device for the life of the process.
+
+#include <mutex>
+
+namespace {
+
+constexpr size_t kStaticWsBytes = size_t(4) << 20;  // 4 MiB: the decode shapes need about 1.1 MB
+__device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
+
+// In host code `g_static_ws` only names the symbol; its device address differs per device and is
+// looked up once per device (with that device current) and cached here.
+constexpr int kMaxDevices = 64;
+void* g_static_ws_addr[kMaxDevices] = {};
+std::mutex g_static_ws_mu;
+
+int static_ws_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FPX_ECUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FPX_EINVAL;
+    std::lock_guard<std::mutex> lock(g_static_ws_mu);
+    if (!g_static_ws_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return FPX_ECUDA;
+        g_static_ws_addr[dev] = p;
+    }
+    *out = g_static_ws_addr[dev];
+    return FPX_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_layer_decode_static_ws(const moe_layer* layer, const uint16_t* x, int q, int k, float* y,
+                                          int32_t* idx_out, float* w_out, float* logits_out, int32_t* dev_status,
+                                          void* stream) {
+    if (!layer || q < 1 || q > kMaxQ || k < 1 || k > kMaxK) return FPX_EINVAL;
+    const size_t need = moe_workspace_bytes(layer, q, k);
+    if (need == 0) return FPX_EINVAL;
+    if (need > kStaticWsBytes) return FPX_ESPACE;
+    if (dev_status && !aligned(dev_status, 4)) return FPX_EALIGN;
+    void* ws = nullptr;
+    int st = static_ws_address(&ws);
+    if (st) return st;
+    st = moe_layer_decode(layer, x, q, k, y, idx_out, w_out, logits_out, ws, need, stream);
+    if (st) return st;
+    if (dev_status &&
+        cudaMemcpyAsync(dev_status, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)) !=
+            cudaSuccess)
+        return FPX_ECUDA;
+    return FPX_OK;
+}

@@ -138,6 +138,25 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
                      int32_t* idx_out, float* w_out, float* logits_out, void* ws, size_t ws_bytes,
                      void* stream);
 
+/* moe_layer_decode for callers that cannot allocate device memory: a plugin or library running
+ * inside a host framework that owns every device allocation (its own arena or allocator) and allows
+ * no others, or a latency-critical loop that must never call cudaMalloc/cudaFree because they can
+ * synchronise the device. The pages have no counterpart to this call; it exists for deployment only.
+ * Same arguments and results as moe_layer_decode, except that the scratch is a 4 MiB array inside
+ * libfpx.so (one per device, held until the process exits) instead of a caller workspace, and the
+ * status word is copied to dev_status (nullable, device, 4-byte aligned) at the end of the call.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *   - Shapes whose moe_workspace_bytes() exceeds 4 MiB fail with FPX_ESPACE (the decode shapes,
+ *     H = 4096, I = 2048, E = 256, q <= 4, k <= 8, need about 1.1 MB).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ *     that device current; make that first call before capturing a stream into a graph.
+ *   - Every call on a device shares the one array, which keeps the previous call's contents: calls
+ *     whose work overlaps on the GPU (different streams, or several host threads) race. Issue them
+ *     in order on one stream. */
+int moe_layer_decode_static_ws(const moe_layer* layer, const uint16_t* x, int q, int k, float* y,
+                               int32_t* idx_out, float* w_out, float* logits_out, int32_t* dev_status,
+                               void* stream);
+
 /* The verify pass over a stack of n_layers layers (host array of structs, all with the same H, I,
  * E): state r binary32 [q][H] starts at r0; layer l takes u_l = RN_bfloat16(r_l / sqrt(mean(r_l^2)
  * + 1e-6)) and sets r_{l+1} = r_l + MoE_l(u_l). rL receives r_{n_layers}; r0 and rL may alias.
