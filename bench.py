@@ -69,37 +69,46 @@ def dist_env():
 # ---------------------------------------------------------------------------- clocks (NVML)
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons with NVML every 20 ms while running."""
+    """Samples SM clock and clock-event reasons through NVML (libnvidia-ml.so.1 via ctypes) every
+    20 ms while running. Reading clocks changes nothing on the GPU."""
     REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
                0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+    NVML_CLOCK_SM = 1
 
-    def __init__(self, index):
-        self.samples, self.reasons, self.ok, self.err = [], 0, False, None
+    def __init__(self, cuda_index):
+        self.samples, self.reasons, self.ok, self.err, self.max = [], 0, False, None, None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit_v2 failed")
+            h = ctypes.c_void_p()
+            rc = -1
+            try:
+                import torch
+                p = torch.cuda.get_device_properties(cuda_index)
+                bus = f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0".encode()
+                rc = nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h))
+            except Exception:  # noqa: BLE001 - fall back to the index
+                rc = -1
+            if rc != 0 and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(h)) != 0:
+                raise RuntimeError("no NVML handle")
+            mx = ctypes.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx))
+            self.nv, self.h, self.max, self.ok = nv, h, int(mx.value), True
+            self.reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
         except Exception as e:  # noqa: BLE001 - reported in the JSON line
-            self.max = None
             self.err = f"{type(e).__name__}: {e}"[:200]
         self._stop = threading.Event()
 
-    def _reasons(self):
-        f = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-            getattr(self.nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
-        return f(self.h)
-
     def _run(self):
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
         while not self._stop.is_set():
-            try:
-                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                self.reasons |= self._reasons()
-            except Exception:
-                pass
+            if self.nv.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, ctypes.byref(clk)) == 0:
+                self.samples.append(int(clk.value))
+            if self.reason_fn(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= int(rs.value)
             time.sleep(0.02)
 
     def __enter__(self):

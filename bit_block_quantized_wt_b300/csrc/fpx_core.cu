@@ -1,5 +1,10 @@
-// Core entry points: sizes, status, dequantize, quantize, and the dense FPX GEMV (CUDA-core path).
-#include "fpx_common.cuh"
+// Core entry points: sizes, status, dequantize, quantize, and the dense FPX GEMV.
+//
+// The GEMV runs on the tensor-core decode engine (fpx_mma.cuh) whenever a row is a whole number of
+// TMA boxes (K % 256 == 0 for FP2/FP3, K % 512 == 0 for FP4) and the activation table fits in shared
+// memory; other shapes use the CUDA-core kernel. The choice depends only on the format and K, never on
+// q, so every column of a call is bit-identical to the same column computed alone.
+#include "fpx_mma.cuh"
 
 #include <cmath>
 
@@ -163,6 +168,157 @@ int launch_gemv_cc_q(const uint8_t* Wq, int64_t N, int64_t K, const void* x, int
     return launch_status();
 }
 
+// ------------------------------------------------------------------ GEMV, tensor-core path
+
+// A CTA processes groups of kWarps / S row tiles; the S warps of a tile split its K range and their
+// partial sums are added in split order. Each warp streams its (tile, split) boxes through its ring.
+struct GemvArgs {
+    CUtensorMap map;
+    int N, K, S;
+    const void* x;
+    int x_bf16;
+    float* y;
+    int32_t* st;
+};
+
+template <int FMT, int Q>
+__global__ void __launch_bounds__(kCtaThreads, 1) k_gemv_mma(const __grid_constant__ GemvArgs A) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int shift[4];
+    __shared__ float red4[(kWarps + 1) * 4];
+    __shared__ float part[kWarps][kTileRows][4];
+    const int K = A.K, N = A.N, S = A.S, tpg = kWarps / S;
+    const Smem Sm = carve(smem, btab_bytes(K), 1);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    init_rings(Sm);
+    const int U = K / (64 * box_chunks(FMT)) / S;  // boxes per (tile, split)
+    const int ntiles = (N + kTileRows - 1) / kTileRows, ngroups = (ntiles + tpg - 1) / tpg;
+    const int my_groups = (int)blockIdx.x < ngroups ? (ngroups - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+
+    // producer: consumer warp w = (tile in group) * S + split streams U boxes per group
+    uint32_t issued[kWarps];
+    const bool producer = warp == kWarps && lane == 0;
+    auto try_issue = [&](int w) -> bool {
+        const uint32_t n = issued[w];
+        if (n >= (uint32_t)(my_groups * U)) return false;
+        const Ring R = warp_ring(Sm, w);
+        if (!ring_free(R, n)) return false;
+        const int grp = (int)blockIdx.x + (int)(n / U) * (int)gridDim.x, u = (int)(n % U);
+        const int tile = grp * tpg + w / S, split = w % S;  // rows past N read as zeros
+        const int slot = n % kStages;
+        mbar_expect_tx(R.full + slot, kTileRows * box_bytes(FMT));
+        tma_load_2d(R.slots + (size_t)slot * kSlotBytes, &A.map, (split * U + u) * (box_bytes(FMT) / elem_bytes(FMT)),
+                    tile * kTileRows, R.full + slot);
+        issued[w] = n + 1;
+        return true;
+    };
+    if (producer) {
+#pragma unroll
+        for (int w = 0; w < kWarps; w++) issued[w] = 0u;
+        for (int i = 0; i < kStages; i++)
+#pragma unroll
+            for (int w = 0; w < kWarps; w++) try_issue(w);
+    }
+
+    if (A.x_bf16) build_tables<FMT, 0, true>(A.x, K, Q, Sm.tab0, nullptr, Sm.csum, shift, red4);
+    else build_tables<FMT, 0, false>(A.x, K, Q, Sm.tab0, nullptr, Sm.csum, shift, red4);
+    __syncthreads();
+
+    if (warp == kWarps) {
+        if (producer) {
+            uint64_t idle_since = 0;
+            for (;;) {
+                bool pending = false, progress = false;
+#pragma unroll
+                for (int w = 0; w < kWarps; w++) {
+                    if (issued[w] < (uint32_t)(my_groups * U)) pending = true;
+                    progress |= try_issue(w);
+                }
+                if (!pending) break;
+                if (progress) {
+                    idle_since = 0;
+                } else {
+                    const uint64_t now = global_ns();
+                    if (!idle_since) idle_since = now;
+                    else if (now - idle_since > kWaitNs) { flag(A.st, FPX_ETIMEOUT); break; }
+                    __nanosleep(100);
+                }
+            }
+        }
+        return;
+    }
+
+    const int split = warp % S;
+    const Ring R = warp_ring(Sm, warp);
+    const int a_idx = b_active_index(lane);
+    uint32_t consumed = 0;
+    bool ok = true;
+    for (int n = 0; n < my_groups; n++) {
+        const int grp = (int)blockIdx.x + n * (int)gridDim.x;
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int u = 0; u < U && ok; u++) {
+            if (!ring_wait(R, consumed, A.st)) { ok = false; break; }
+            const uint8_t* slot = R.slots + (consumed % kStages) * kSlotBytes;
+            box_mma1<FMT>(slot, box_bytes(FMT), Sm.tab0, Sm.csum, (split * U + u) * box_chunks(FMT), a_idx, g, t, y, A.st);
+            ring_release(R, consumed);
+            consumed++;
+        }
+        pair_reduce(y);
+        if (t < 2) {
+#pragma unroll
+            for (int i = 0; i < 4; i++) part[warp][g + 8 * (i >> 1)][2 * t + (i & 1)] = y[i];
+        }
+        consumers_sync();
+        for (int o = threadIdx.x; o < tpg * kTileRows * Q; o += kWarps * 32) {
+            const int tg = o / (kTileRows * Q), row = (o / Q) % kTileRows, tok = o % Q;
+            float acc = part[tg * S][row][tok];
+            for (int s = 1; s < S; s++) acc += part[tg * S + s][row][tok];
+            const int rr = (grp * tpg + tg) * kTileRows + row;
+            if (rr < N) A.y[(size_t)tok * N + rr] = acc * exp2i((FMT == 4 ? 14 : 0) - shift[tok]);
+        }
+        consumers_sync();
+    }
+    if (!ok) ring_drain(R, consumed, (uint32_t)(my_groups * U));
+}
+
+template <int FMT>
+bool gemv_mma_fits(int64_t K) {
+    return mma_shape_ok(FMT, K) && smem_bytes(btab_bytes((int)K), 1) <= (size_t)device_info().smem_optin;
+}
+
+template <int FMT, int Q>
+int launch_gemv_mma_q(const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_bf16, float* y, int32_t* st,
+                      cudaStream_t s) {
+    DeviceInfo di = device_info();
+    GemvArgs A{};
+    const int64_t rb = K / 32 * block_bytes(FMT);
+    int rc = make_row_map(&A.map, Wq, rb, N, rb, box_bytes(FMT), kTileRows, elem_bytes(FMT));
+    if (rc) return rc;
+    const int64_t ntiles = (N + kTileRows - 1) / kTileRows;
+    const int units = (int)(K / (64 * box_chunks(FMT)));
+    int S = 1;
+    while (S < kWarps && ntiles * S < (int64_t)di.sms * kWarps && units % (2 * S) == 0) S *= 2;
+    A.N = (int)N; A.K = (int)K; A.S = S; A.x = x; A.x_bf16 = x_bf16; A.y = y; A.st = st;
+    const int64_t ngroups = (ntiles + kWarps / S - 1) / (kWarps / S);
+    const int grid = (int)(ngroups < di.sms ? ngroups : di.sms);
+    const size_t smem = smem_bytes(btab_bytes((int)K), 1);
+    if (cudaFuncSetAttribute(k_gemv_mma<FMT, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) return FPX_ECUDA;
+    k_gemv_mma<FMT, Q><<<grid, kCtaThreads, smem, s>>>(A);
+    return launch_status();
+}
+
+template <int FMT>
+int launch_gemv_mma(const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_bf16, int q, float* y, int32_t* st,
+                    cudaStream_t s) {
+    switch (q) {
+        case 1: return launch_gemv_mma_q<FMT, 1>(Wq, N, K, x, x_bf16, y, st, s);
+        case 2: return launch_gemv_mma_q<FMT, 2>(Wq, N, K, x, x_bf16, y, st, s);
+        case 3: return launch_gemv_mma_q<FMT, 3>(Wq, N, K, x, x_bf16, y, st, s);
+        case 4: return launch_gemv_mma_q<FMT, 4>(Wq, N, K, x, x_bf16, y, st, s);
+        default: return FPX_EINVAL;
+    }
+}
+
 template <int FMT>
 int launch_gemv_cc(const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_bf16, int q, float* y, int32_t* st,
                    cudaStream_t s) {
@@ -244,9 +400,12 @@ int fpx_gemv_q(int fmt, const uint8_t* Wq, int64_t N, int64_t K, const void* x, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return cudaMemsetAsync(y, 0, sizeof(float) * (size_t)q * N, s) == cudaSuccess ? FPX_OK : FPX_ECUDA;
     int bf = x_dtype == FPX_DTYPE_BF16;
-    if (fmt == 2) return launch_gemv_cc<2>(Wq, N, K, x, bf, q, y, dev_status, s);
-    if (fmt == 3) return launch_gemv_cc<3>(Wq, N, K, x, bf, q, y, dev_status, s);
-    return launch_gemv_cc<4>(Wq, N, K, x, bf, q, y, dev_status, s);
+    if (fmt == 2) return gemv_mma_fits<2>(K) ? launch_gemv_mma<2>(Wq, N, K, x, bf, q, y, dev_status, s)
+                                             : launch_gemv_cc<2>(Wq, N, K, x, bf, q, y, dev_status, s);
+    if (fmt == 3) return gemv_mma_fits<3>(K) ? launch_gemv_mma<3>(Wq, N, K, x, bf, q, y, dev_status, s)
+                                             : launch_gemv_cc<3>(Wq, N, K, x, bf, q, y, dev_status, s);
+    return gemv_mma_fits<4>(K) ? launch_gemv_mma<4>(Wq, N, K, x, bf, q, y, dev_status, s)
+                               : launch_gemv_cc<4>(Wq, N, K, x, bf, q, y, dev_status, s);
 }
 
 }  // extern "C"

@@ -1,0 +1,656 @@
+// Tensor-core decode engine: packed FPX rows staged by TMA, decoded in registers into binary16
+// A fragments, multiplied on the tensor cores (mma.sync m16n8k16, binary32 accumulate) against the
+// q <= 4 activation columns.
+//
+// Why tensor cores for a GEMV: at q = 4 the CUDA-core path needs 4 binary32 FMAs per weight, but an
+// SM receives about 76 FP2 weights per clock from HBM and executes 128 FMAs per clock, so it is
+// ALU-bound near 40% of the memory roofline. One m16n8k16 multiplies 16 rows x 16 weights against 8
+// columns in one instruction, leaving the decode itself (about one ALU operation per weight) as the
+// only per-weight cost.
+//
+// Fragment plan (one warp, lane = 4g + t). A "chunk" is 64 consecutive weights of a row = two blocks.
+// Four MMAs cover a 16-row tile x one chunk. MMA output columns 0..3 are the q tokens against the
+// chunk's first block, columns 4..7 the tokens against its second block, so every accumulator holds
+// one (row, block, token) sum and the per-block scale is applied once per block in binary32. Thread
+// t decodes block t/2, codes 16(t%2) .. 16(t%2)+15, of rows g and g+8: eight binary16 pairs, pair i
+// feeding MMA i/2, k-slots (2t + 8(i%2), +1). The k-slot order inside a block is a permutation of the
+// weights; the B table (activations) is laid out with the same permutation, so the dot product is
+// unchanged.
+//
+// Exact decode. A pair of 2-bit codes is moved into the mantissa of a binary16 pair with one LOP3
+// (mask | 0x6400, the binary16 1024), and one HFMA2 removes the offset and applies the codebook:
+// 2 * (1024 + c * 2^P) - (2048 + 3 * 2^P) = 2^P (2c - 3). Every constant and result is exact in
+// binary16; the activation is stored as x * 2^-P so A * B = (2c - 3) * x exactly. FP3 adds the high bit
+// plane with a second HFMA2 (constants chosen so the intermediate stays exact), FP4 maps E2M1 bits
+// straight onto binary16 bits (value * 2^-14). Products are exact in binary32; only the tensor-core
+// accumulation rounds.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "fpx_common.cuh"
+
+namespace fpx {
+
+// ------------------------------------------------------------------ compile-time binary16 bits
+
+// Bit pattern of a binary16 number that is exactly representable (a small integer times a power of
+// two), computed at compile time.
+__host__ __device__ constexpr uint16_t f16_bits(double v) {
+    uint16_t sign = v < 0 ? 0x8000 : 0;
+    double a = v < 0 ? -v : v;
+    if (a == 0) return sign;
+    int e = 0;
+    while (a >= 2.0) { a /= 2.0; e++; }
+    while (a < 1.0) { a *= 2.0; e--; }
+    // normal numbers only (the constants used here are all >= 2^-14)
+    return static_cast<uint16_t>(sign | ((e + 15) << 10) | static_cast<uint16_t>((a - 1.0) * 1024.0));
+}
+__host__ __device__ constexpr uint32_t f16x2(double v) { return (uint32_t(f16_bits(v)) << 16) | f16_bits(v); }
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase with the given parity, giving up after kWaitNs of wall time (or kSpinLimit
+// polls; each try_wait may itself suspend for a bounded time). Returns false when it gives up.
+constexpr uint32_t kSpinLimit = 1u << 24;
+constexpr uint64_t kWaitNs = 500000000ull;  // 0.5 s
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+    if (mbar_try_wait(b, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < kSpinLimit; i++) {
+        if (mbar_try_wait(b, parity)) return true;
+        if ((i & 63) == 63 && global_ns() - t0 > kWaitNs) return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 2-D tiled TMA load of one box into shared memory, completing on mbarrier `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// D = A * B + C, m16n8k16, binary16 inputs, binary32 accumulators.
+__device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D = A * B (accumulators start at zero).
+__device__ __forceinline__ void mma_first(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    const float z = 0.0f;
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
+}
+
+// ------------------------------------------------------------------ decode into A pairs
+
+// Exponent shift P of pair i (binary16 mantissa position of the code's low bit) for FP2 and FP3;
+// FP4 pairs carry no shift (their values are scaled by 2^-14 instead).
+__host__ __device__ constexpr int pair_shift(int fmt, int i) {
+    return fmt == 4 ? 0 : (i == 0 || i == 1 || i == 5) ? 2 : (i == 2 || i == 6) ? 4 : (i == 3 || i == 7) ? 6 : 8;
+}
+// Code positions (within the thread's 16-code group) held by the low and high half of pair i.
+__host__ __device__ constexpr int pair_lo(int fmt, int i) { return fmt == 4 ? 8 * (i / 4) + (i % 4) : i; }
+__host__ __device__ constexpr int pair_hi(int fmt, int i) { return fmt == 4 ? 8 * (i / 4) + (i % 4) + 4 : i + 8; }
+
+constexpr uint32_t kMagic = 0x64006400u;  // binary16 pair (1024, 1024)
+constexpr uint32_t kTwo = f16x2(2.0);
+
+// Eight A pairs from 16 FP2 codes (2 bits each, code k at bits 2k..2k+1 of w): pair i holds codes
+// (i, i + 8) as the binary16 values 1024 + c * 2^P, one LOP3 each. The MMA then sums
+// sum (1024 + c 2^P) * x 2^-P = sum c x + 1024 sum x 2^-P, and the epilogue recovers
+// sum (2c - 3) x = 2 acc - sum x 2^-P (2048 + 3 2^P) with a per-block constant of the activations.
+__device__ __forceinline__ void decode_fp2(uint32_t w, uint32_t (&a)[8]) {
+    const uint32_t s2 = w << 2, s8 = w >> 8;
+    a[0] = (s2 & 0x000C000Cu) | kMagic;
+    a[1] = (w & 0x000C000Cu) | kMagic;
+    a[2] = (w & 0x00300030u) | kMagic;
+    a[3] = (w & 0x00C000C0u) | kMagic;
+    a[4] = (w & 0x03000300u) | kMagic;
+    a[5] = (s8 & 0x000C000Cu) | kMagic;
+    a[6] = (s8 & 0x00300030u) | kMagic;
+    a[7] = (s8 & 0x00C000C0u) | kMagic;
+}
+
+// FP3 high-bit plane: pair i places its two high bits at mantissa bit Q (i) and uses
+// A = (1024 + 2^Q h) * 2^(P+3-Q) + [2 (1024 + 2^P l) - (2048 + 7 * 2^P + 2^(P+13-Q))]
+//   = 2^P (2l + 8h - 7) = 2^P (2c - 7); the bracket (first HFMA2) is exact for 3 <= Q <= 9.
+template <int P, int Q>
+__host__ __device__ constexpr uint32_t fp3_off() { return f16x2(-(2048.0 + 7.0 * (1 << P) + double(1 << (P + 13 - Q)))); }
+template <int P, int Q>
+__host__ __device__ constexpr uint32_t fp3_mul() { return f16x2(P + 3 - Q >= 0 ? double(1 << (P + 3 - Q)) : 1.0 / double(1 << (Q - P - 3))); }
+
+// lo: 16 low-plane codes as in FP2; hg: the 16 high bits (bit k = code k).
+__device__ __forceinline__ void decode_fp3(uint32_t lo, uint32_t hg, uint32_t (&a)[8]) {
+    const uint32_t s2 = lo << 2, s8 = lo >> 8;
+    // spread the high bits: bit k -> k (k < 8), bit 8 + k -> 16 + k
+    const uint32_t sp = __byte_perm(hg, 0u, 0x4140);
+    const uint32_t h3 = sp << 3, h2 = sp << 2;  // pair i < 7: Q = i + 3; pair 7: Q = 9
+    a[0] = hfma2((h3 & 0x00080008u) | kMagic, fp3_mul<2, 3>(), hfma2((s2 & 0x000C000Cu) | kMagic, kTwo, fp3_off<2, 3>()));
+    a[1] = hfma2((h3 & 0x00100010u) | kMagic, fp3_mul<2, 4>(), hfma2((lo & 0x000C000Cu) | kMagic, kTwo, fp3_off<2, 4>()));
+    a[2] = hfma2((h3 & 0x00200020u) | kMagic, fp3_mul<4, 5>(), hfma2((lo & 0x00300030u) | kMagic, kTwo, fp3_off<4, 5>()));
+    a[3] = hfma2((h3 & 0x00400040u) | kMagic, fp3_mul<6, 6>(), hfma2((lo & 0x00C000C0u) | kMagic, kTwo, fp3_off<6, 6>()));
+    a[4] = hfma2((h3 & 0x00800080u) | kMagic, fp3_mul<8, 7>(), hfma2((lo & 0x03000300u) | kMagic, kTwo, fp3_off<8, 7>()));
+    a[5] = hfma2((h3 & 0x01000100u) | kMagic, fp3_mul<2, 8>(), hfma2((s8 & 0x000C000Cu) | kMagic, kTwo, fp3_off<2, 8>()));
+    a[6] = hfma2((h3 & 0x02000200u) | kMagic, fp3_mul<4, 9>(), hfma2((s8 & 0x00300030u) | kMagic, kTwo, fp3_off<4, 9>()));
+    a[7] = hfma2((h2 & 0x02000200u) | kMagic, fp3_mul<6, 9>(), hfma2((s8 & 0x00C000C0u) | kMagic, kTwo, fp3_off<6, 9>()));
+}
+
+// FP4: E2M1 nibble (s, e1, e0, m) -> binary16 bits (s << 15) | (e1 e0 m) << 9, i.e. the E2M1 value
+// times 2^-14 (exponent field 0 gives the binary16 subnormals 0 and 2^-15 = 0.5 * 2^-14). Pair
+// (k, k + 4) of a word of eight codes sits at bits 4k and 4k + 16.
+template <int K>
+__device__ __forceinline__ uint32_t fp4_pair(uint32_t w) {
+    const uint32_t m = (K <= 2) ? (w << (9 - 4 * K)) : (w >> (4 * K - 9));
+    const uint32_t s = (K <= 3) ? (w << (12 - 4 * K)) : (w >> (4 * K - 12));
+    return (m & 0x0E000E00u) | (s & 0x80008000u);
+}
+
+// w0: codes 0..7, w1: codes 8..15 of the thread's group.
+__device__ __forceinline__ void decode_fp4(uint32_t w0, uint32_t w1, uint32_t (&a)[8]) {
+    a[0] = fp4_pair<0>(w0); a[1] = fp4_pair<1>(w0); a[2] = fp4_pair<2>(w0); a[3] = fp4_pair<3>(w0);
+    a[4] = fp4_pair<0>(w1); a[5] = fp4_pair<1>(w1); a[6] = fp4_pair<2>(w1); a[7] = fp4_pair<3>(w1);
+}
+
+// ------------------------------------------------------------------ B table (activations)
+
+// Layout: for chunk c (64 weights), active lane a (0..15), MMA j (0..3): a uint2 holding the B
+// fragment registers {b0b1, b2b3} = pairs 2j and 2j+1 of that lane's k-slots. Lane (g, t) is active
+// when its column (token g % 4, block g / 4) belongs to the block it decodes (t / 2), i.e.
+// g / 4 == t / 2; then a = 8 (t / 2) + 2 (g % 4) + t % 2. Inactive lanes multiply zeros.
+__host__ __device__ constexpr int btab_bytes(int K) { return (K / 64) * 16 * 4 * 8; }
+
+__device__ __forceinline__ int b_active_index(int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    return ((g >> 2) == (t >> 1)) ? 8 * (t >> 1) + 2 * (g & 3) + (t & 1) : -1;
+}
+
+// Column scale: x' = x * 2^(14 - floor(log2 max|x|)) keeps every column in binary16 normal range with
+// its largest element in [2^14, 2^15). Returns the exponent shift (0 for an all-zero column).
+__device__ __forceinline__ int column_shift(float amax) {
+    if (!(amax > 0.0f) || !isfinite(amax)) return 0;
+    int e;
+    frexpf(amax, &e);  // amax in [2^(e-1), 2^e)
+    return 14 - (e - 1);
+}
+
+// ------------------------------------------------------------------ activation tables, batched
+
+// 2^e as binary32 (exact; bit construction in the normal range).
+__device__ __forceinline__ float exp2i(int e) {
+    return (e >= -126 && e <= 127) ? __int_as_float((e + 127) << 23) : ldexpf(1.0f, e);
+}
+
+// Eight consecutive activations from a binary32 or bfloat16 array (element offset e0, multiple of 8).
+template <bool BF16>
+__device__ __forceinline__ void load8(const void* src, size_t e0, float (&v)[8]) {
+    if constexpr (BF16) {
+        const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(src) + e0);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else {
+        const float4* f = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + e0);
+        const float4 a = f[0], b = f[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
+// Sixteen consecutive activations (one code group) from a binary32 or bfloat16 array.
+template <bool BF16>
+__device__ __forceinline__ void load16(const void* src, size_t e0, float (&v)[16]) {
+    float a[8], b[8];
+    load8<BF16>(src, e0, a);
+    load8<BF16>(src, e0 + 8, b);
+#pragma unroll
+    for (int i = 0; i < 8; i++) { v[i] = a[i]; v[8 + i] = b[i]; }
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// One table entry (32 bytes) = the B registers of one active lane for one chunk: the 16 activations
+// of a code group scaled by 2^(sh - P(pair)), arranged as pairs 0..7. FP2/FP3 pair p holds
+// codes (p, p + 8); FP4 pair p holds codes (8 (p/4) + p%4, +4). Also returns, for FP2, the block
+// offset contribution sum_m B_m (2048 + 3 * 2^P(m)) in code order.
+template <int FMT>
+__device__ __forceinline__ void pack_entry(const float (&v)[16], int sh, uint4& e0, uint4& e1, float& part) {
+    uint32_t w[8];
+#pragma unroll
+    for (int p = 0; p < 8; p++) {
+        const int lo = FMT == 4 ? 8 * (p / 4) + p % 4 : p;
+        const int hi = FMT == 4 ? lo + 4 : p + 8;
+        const float sc = exp2i(sh - pair_shift(FMT, p));
+        w[p] = pack_h2(v[lo] * sc, v[hi] * sc);
+    }
+    e0 = make_uint4(w[0], w[1], w[2], w[3]);
+    e1 = make_uint4(w[4], w[5], w[6], w[7]);
+    part = 0.f;
+    if constexpr (FMT == 2) {
+#pragma unroll
+        for (int m = 0; m < 16; m++) {
+            const int p = m & 7;
+            const float b = __half2float(m < 8 ? __ushort_as_half((uint16_t)(w[p] & 0xFFFFu)) : __ushort_as_half((uint16_t)(w[p] >> 16)));
+            part = fmaf(b, 2048.0f + 3.0f * float(1 << pair_shift(2, p)), part);
+        }
+    }
+}
+
+// Builds the activation tables for columns x[tok][k] (tok < q <= 4, K % 64 == 0): tabA in format
+// FA, tabB in format FB (FB == 0: none) and, when FA == 2, the FP2 block offsets csum[block * 4 +
+// tok]. shift[4] receives the column shifts. Whole CTA (nt threads, nt % 32 == 0). Each thread owns
+// whole 16-weight code groups: it issues all of a pass's loads before using them, and writes each
+// table entry with two 16-byte stores.
+template <int FA, int FB, bool BF16>
+__device__ void build_tables(const void* x, int K, int q, uint2* tabA, uint2* tabB, float* csum, int* shift,
+                             float* red4) {
+    constexpr int V = BF16 ? 4 : 2;  // groups per thread per batch
+    const int ngr = q * K / 16;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    // pass 1: column maxima
+    float m[4] = {0.f, 0.f, 0.f, 0.f};
+    // loops start at the warp's first thread so every lane of a warp runs the same iterations (the
+    // shuffles below need all 32 lanes); lanes past the end are predicated off
+    const int lane = tid & 31;
+    for (int base = tid - lane; base < ngr; base += V * nt) {
+        float v[V][16];
+#pragma unroll
+        for (int it = 0; it < V; it++)
+            if (base + lane + it * nt < ngr) load16<BF16>(x, (size_t)(base + lane + it * nt) * 16, v[it]);
+#pragma unroll
+        for (int it = 0; it < V; it++) {
+            const int gi = base + lane + it * nt;
+            if (gi < ngr) {
+                const int tok = gi * 16 / K;
+                float mm = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; j++) mm = fmaxf(mm, fabsf(v[it][j]));
+#pragma unroll
+                for (int t = 0; t < 4; t++) m[t] = t == tok ? fmaxf(m[t], mm) : m[t];
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; t++) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m[t] = fmaxf(m[t], __shfl_xor_sync(0xffffffffu, m[t], o));
+    }
+    if ((tid & 31) == 0)
+        for (int t = 0; t < 4; t++) red4[(tid >> 5) * 4 + t] = m[t];
+    // entries of absent tokens stay zero
+    for (int i = tid; i < (K / 64) * 16; i += nt) {
+        const int a = i & 15;
+        if (((a >> 1) & 3) >= q) {
+            uint4* ea = reinterpret_cast<uint4*>(tabA + (size_t)i * 4);
+            ea[0] = ea[1] = make_uint4(0u, 0u, 0u, 0u);
+            if (FB) {
+                uint4* eb = reinterpret_cast<uint4*>(tabB + (size_t)i * 4);
+                eb[0] = eb[1] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    }
+    if (FA == 2)
+        for (int i = tid; i < (K / 32) * 4; i += nt)
+            if ((i & 3) >= q) csum[i] = 0.f;
+    __syncthreads();
+    if (tid < 4) {
+        float mm = 0.f;
+        for (int w = 0; w < nt / 32; w++) mm = fmaxf(mm, red4[w * 4 + tid]);
+        shift[tid] = column_shift(mm);
+    }
+    __syncthreads();
+    // pass 2: whole entries
+    for (int base = tid - lane; base < ngr; base += V * nt) {
+        float v[V][16];
+#pragma unroll
+        for (int it = 0; it < V; it++)
+            if (base + lane + it * nt < ngr) load16<BF16>(x, (size_t)(base + lane + it * nt) * 16, v[it]);
+#pragma unroll
+        for (int it = 0; it < V; it++) {
+            const int gi = base + lane + it * nt;
+            float part = 0.f;
+            if (gi < ngr) {
+                const int tok = gi * 16 / K, k0 = gi * 16 - tok * K;
+                const int c = k0 >> 6, half = (k0 >> 5) & 1, hw = (k0 >> 4) & 1;
+                const int a = 8 * half + 2 * tok + hw;
+                const int sh = shift[tok];
+                uint4 e0, e1;
+                pack_entry<FA>(v[it], sh, e0, e1, part);
+                uint4* ea = reinterpret_cast<uint4*>(tabA + ((size_t)c * 16 + a) * 4);
+                ea[0] = e0;
+                ea[1] = e1;
+                if (FB) {
+                    float dummy;
+                    pack_entry<FB>(v[it], sh, e0, e1, dummy);
+                    uint4* eb = reinterpret_cast<uint4*>(tabB + ((size_t)c * 16 + a) * 4);
+                    eb[0] = e0;
+                    eb[1] = e1;
+                }
+            }
+            if (FA == 2) {
+                // a 32-weight block is two consecutive groups (lanes 2i, 2i + 1): add them in order
+                const float nxt = __shfl_down_sync(0xffffffffu, part, 1);
+                if (gi < ngr && (gi & 1) == 0) {
+                    const int tok = gi * 16 / K, blk = (gi * 16 - tok * K) / 32;
+                    csum[blk * 4 + tok] = part + nxt;
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host: tensor maps
+
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;  // the driver entry point, looked up once
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// A 2-D map over `rows` rows of `row_bytes` bytes (row stride `stride` bytes), elements of 1 or 2
+// bytes, box = box_bytes x box_rows. Out-of-range rows read as zeros.
+inline int make_row_map(CUtensorMap* m, const void* base, int64_t row_bytes, int64_t rows, int64_t stride,
+                        int box_bytes, int box_rows, int elem_bytes) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return FPX_ECUDA;
+    const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes / elem_bytes), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes / elem_bytes), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FPX_OK : FPX_ECUDA;
+}
+
+// Per-format staging geometry: a TMA box covers `box_bytes` of each row = `box_chunks` chunks of
+// 64 weights (FP2 4 x 20 B, FP3 4 x 28 B, FP4 8 x 34 B; multiples of 16 bytes, at most 256
+// elements). FP4 uses 2-byte elements so its 272-byte box stays within 256 elements.
+__host__ __device__ constexpr int box_bytes(int fmt) { return fmt == 2 ? 80 : fmt == 3 ? 112 : 272; }
+__host__ __device__ constexpr int box_chunks(int fmt) { return fmt == 4 ? 8 : 4; }
+__host__ __device__ constexpr int chunk_bytes(int fmt) { return 2 * block_bytes(fmt); }
+__host__ __device__ constexpr int elem_bytes(int fmt) { return fmt == 4 ? 2 : 1; }
+
+// Rows decodable by the tensor-core path: whole boxes per row.
+__host__ __device__ constexpr bool mma_shape_ok(int fmt, int64_t K) { return K > 0 && K % (64 * box_chunks(fmt)) == 0; }
+
+// ------------------------------------------------------------------ per-warp chunk processing
+
+// Loads the code groups and block scales of one chunk for rows r (thread's row g) from a staged box
+// with row pitch `pitch`, decodes them into A pairs, and returns the block scale in binary32.
+// `row` points at the start of the row inside the box, `c` is the chunk inside the box, t the thread
+// index in its group of four.
+template <int FMT>
+__device__ __forceinline__ float load_decode(const uint8_t* row, int c, int t, uint32_t (&a)[8], int32_t* st) {
+    const int half = t >> 1, hw = t & 1;
+    if constexpr (FMT == 2) {
+        // chunk = [d0 (2) | codes0 (8) | d1 (2) | codes1 (8)], 4-byte aligned. The thread's code word
+        // is bytes 2+4hw.. (first block) or 12+4hw.. (second): two aligned words and one PRMT.
+        const uint8_t* ch = row + 20 * c;
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(ch + (half ? 12 : 0) + 4 * hw);
+        const uint32_t cw = __byte_perm(w[0], w[1], half ? 0x3210 : 0x5432);
+        decode_fp2(cw, a);
+        const uint16_t d = *reinterpret_cast<const uint16_t*>(ch + 10 * half);
+        return __half2float(__ushort_as_half(d));
+    } else if constexpr (FMT == 3) {
+        // chunk = [d0 (2) | lo0 (8) | hi0 (4) | d1 (2) | lo1 (8) | hi1 (4)], 4-byte aligned
+        const uint8_t* ch = row + 28 * c;
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(ch + (half ? 16 : 0) + 4 * hw);
+        const uint32_t lo = __byte_perm(w[0], w[1], half ? 0x3210 : 0x5432);
+        const uint32_t hg = *reinterpret_cast<const uint16_t*>(ch + 14 * half + 10 + 2 * hw);
+        decode_fp3(lo, hg, a);
+        const uint16_t d = *reinterpret_cast<const uint16_t*>(ch + 14 * half);
+        return __half2float(__ushort_as_half(d));
+    } else {
+        // chunk = [e0 (1) | codes0 (16) | e1 (1) | codes1 (16)], 2-byte aligned
+        const uint8_t* ch = row + 34 * c;
+        const uint8_t* src = ch + 17 * half + 1 + 8 * hw;  // 8 code bytes
+        const uintptr_t addr = reinterpret_cast<uintptr_t>(src);
+        const uint32_t* base = reinterpret_cast<const uint32_t*>(addr & ~uintptr_t(3));
+        const uint32_t sh = static_cast<uint32_t>(addr & 3) * 8;
+        const uint32_t x0 = base[0], x1 = base[1], x2 = base[2];
+        const uint32_t w0 = __funnelshift_r(x0, x1, sh), w1 = __funnelshift_r(x1, x2, sh);
+        decode_fp4(w0, w1, a);
+        const uint32_t e = ch[17 * half];
+        if (e == 255u) {  // NaN scale: the block is invalid and counts as zeros
+            flag(st, FPX_EDATA);
+            return 0.0f;
+        }
+        // 2^(e-127): e in 1..254 is a normal binary32 power of two, e == 0 the subnormal 2^-127
+        return e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);
+    }
+}
+
+// ------------------------------------------------------------------ per-warp TMA ring and tile MMA
+
+constexpr int kWarps = 8;            // consumer warps of a tensor-core CTA
+constexpr int kCtaThreads = (kWarps + 1) * 32;  // + one producer warp that issues every TMA load
+constexpr int kStages = 4;           // TMA ring depth per warp
+constexpr int kSlotBytes = 4352;     // one stage: 16 FP4 rows x 272 B, or G+U FP2 boxes, or an FP3 box
+constexpr int kRingBytes = kWarps * kStages * kSlotBytes;
+constexpr int kTileRows = 16;
+
+// Per-consumer-warp TMA ring: kStages slots of kSlotBytes. full[s] completes when the TMA data of the
+// unit in slot s has landed; empty[s] when the consumer warp has finished reading it. The producer
+// warp waits on empty before refilling a slot, the consumer on full before reading it.
+struct Ring {
+    uint8_t* slots;
+    uint64_t* full;
+    uint64_t* empty;
+};
+
+// Waits for the unit in slot (u % kStages), phase (u / kStages). On timeout flags FPX_ETIMEOUT and
+// returns false.
+__device__ __forceinline__ bool ring_wait(const Ring& R, uint32_t u, int32_t* st) {
+    // every lane waits; the warp proceeds if any lane saw the phase complete, so all 32 lanes take
+    // the same branch (the MMAs and warp syncs that follow need the whole warp)
+    const bool done = __any_sync(0xffffffffu, mbar_wait(R.full + (u % kStages), (u / kStages) & 1u));
+    if (!done && (threadIdx.x & 31) == 0) flag(st, FPX_ETIMEOUT);
+    return done;
+}
+
+// The consumer warp is done with unit u: hand its slot back to the producer.
+__device__ __forceinline__ void ring_release(const Ring& R, uint32_t u) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(R.empty + (u % kStages));
+}
+
+// Producer: may slot (n % kStages) receive the warp's n-th unit? (single poll)
+__device__ __forceinline__ bool ring_free(const Ring& R, uint32_t n) {
+    return n < (uint32_t)kStages || mbar_try_wait(R.empty + (n % kStages), ((n / kStages) + 1u) & 1u);
+}
+
+// After a timeout: wait (bounded) for the units this consumer still expects, so no copy lands after
+// the CTA exits.
+__device__ inline void ring_drain(const Ring& R, uint32_t consumed, uint32_t expected) {
+    if ((threadIdx.x & 31) != 0) return;
+    for (uint32_t u = consumed; u < expected && u < consumed + kStages; u++) mbar_wait(R.full + (u % kStages), (u / kStages) & 1u);
+}
+
+// Accumulates one chunk (64 weights = 2 blocks) of a 16-row tile staged at `tile` (row pitch
+// `pitch`) into y[4] (thread's (row, token) partial sums for its block parity). For FP2, cs holds the
+// block offsets of the thread's two tokens.
+template <int FMT>
+__device__ __forceinline__ void tile_chunk(const uint8_t* tile, int pitch, int c, int g, int t, const uint2 (&b)[4],
+                                           float2 cs, float (&y)[4], int32_t* st) {
+    uint32_t a0[8], a8[8];
+    const float d0 = load_decode<FMT>(tile + g * pitch, c, t, a0, st);
+    const float d8 = load_decode<FMT>(tile + (g + 8) * pitch, c, t, a8, st);
+    float acc[4];
+    mma_first(acc, a0[0], a8[0], a0[1], a8[1], b[0].x, b[0].y);
+    mma_acc(acc, a0[2], a8[2], a0[3], a8[3], b[1].x, b[1].y);
+    mma_acc(acc, a0[4], a8[4], a0[5], a8[5], b[2].x, b[2].y);
+    mma_acc(acc, a0[6], a8[6], a0[7], a8[7], b[3].x, b[3].y);
+    if constexpr (FMT == 2) {
+        y[0] = fmaf(d0, fmaf(2.0f, acc[0], -cs.x), y[0]);
+        y[1] = fmaf(d0, fmaf(2.0f, acc[1], -cs.y), y[1]);
+        y[2] = fmaf(d8, fmaf(2.0f, acc[2], -cs.x), y[2]);
+        y[3] = fmaf(d8, fmaf(2.0f, acc[3], -cs.y), y[3]);
+    } else {
+        y[0] = fmaf(d0, acc[0], y[0]);
+        y[1] = fmaf(d0, acc[1], y[1]);
+        y[2] = fmaf(d8, acc[2], y[2]);
+        y[3] = fmaf(d8, acc[3], y[3]);
+    }
+}
+
+__device__ __forceinline__ void load_b(const uint2* tab, int chunk, int a, uint2 (&b)[4]) {
+    if (a >= 0) {
+        const uint4* p = reinterpret_cast<const uint4*>(tab + ((size_t)chunk * 16 + a) * 4);
+        const uint4 v0 = p[0], v1 = p[1];
+        b[0] = make_uint2(v0.x, v0.y); b[1] = make_uint2(v0.z, v0.w);
+        b[2] = make_uint2(v1.x, v1.y); b[3] = make_uint2(v1.z, v1.w);
+    } else {
+        b[0] = b[1] = b[2] = b[3] = make_uint2(0u, 0u);
+    }
+}
+
+// All chunks of one staged box (chunks chunk0 .. chunk0 + box_chunks - 1 of the row) for one or two
+// row tiles sharing the activations, fully unrolled so the decode of one chunk overlaps the MMAs of
+// another. csum: FP2 block offsets (ignored for FP3/FP4).
+template <int FMT>
+__device__ __forceinline__ void box_mma1(const uint8_t* tile, int pitch, const uint2* tab, const float* csum, int chunk0,
+                                         int a_idx, int g, int t, float (&y)[4], int32_t* st) {
+#pragma unroll 4
+    for (int c = 0; c < box_chunks(FMT); c++) {
+        uint2 b[4];
+        load_b(tab, chunk0 + c, a_idx, b);
+        const float2 cs = FMT == 2 ? *reinterpret_cast<const float2*>(csum + ((chunk0 + c) * 2 + (t >> 1)) * 4 + 2 * (t & 1))
+                                   : make_float2(0.f, 0.f);
+        tile_chunk<FMT>(tile, pitch, c, g, t, b, cs, y, st);
+    }
+}
+
+template <int FMT>
+__device__ __forceinline__ void box_mma2(const uint8_t* tile0, const uint8_t* tile1, int pitch, const uint2* tab,
+                                         const float* csum, int chunk0, int a_idx, int g, int t, float (&y0)[4],
+                                         float (&y1)[4], int32_t* st) {
+#pragma unroll 4
+    for (int c = 0; c < box_chunks(FMT); c++) {
+        uint2 b[4];
+        load_b(tab, chunk0 + c, a_idx, b);
+        const float2 cs = FMT == 2 ? *reinterpret_cast<const float2*>(csum + ((chunk0 + c) * 2 + (t >> 1)) * 4 + 2 * (t & 1))
+                                   : make_float2(0.f, 0.f);
+        tile_chunk<FMT>(tile0, pitch, c, g, t, b, cs, y0, st);
+        tile_chunk<FMT>(tile1, pitch, c, g, t, b, cs, y1, st);
+    }
+}
+
+// Adds the partner thread's block-parity partial sums (lane ^ 2): afterwards lanes t and t ^ 2 hold
+// the full sums of rows (g, g + 8) for tokens 2 (t % 2), 2 (t % 2) + 1.
+__device__ __forceinline__ void pair_reduce(float (&y)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; i++) y[i] += __shfl_xor_sync(0xffffffffu, y[i], 2);
+}
+
+// Shared-memory carve-up common to the tensor-core kernels.
+struct Smem {
+    uint8_t* ring;   // kRingBytes
+    uint64_t* bars;  // full[kWarps * kStages], then empty[kWarps * kStages]
+    uint2* tab0;     // activation tables
+    uint2* tab1;
+    float* csum;     // FP2 block offsets: (K / 32) blocks x 4 tokens floats = K / 2 bytes
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* raw, int tab_bytes, int ntabs) {
+    // TMA destinations: align the ring to 128 bytes (the allocation has 128 bytes of slack)
+    uint8_t* base = raw + ((128u - (smem_u32(raw) & 127u)) & 127u);
+    Smem s;
+    s.ring = base;
+    s.bars = reinterpret_cast<uint64_t*>(base + kRingBytes);
+    s.tab0 = reinterpret_cast<uint2*>(base + kRingBytes + 1024);
+    s.tab1 = reinterpret_cast<uint2*>(base + kRingBytes + 1024 + tab_bytes);
+    s.csum = reinterpret_cast<float*>(base + kRingBytes + 1024 + (size_t)ntabs * tab_bytes);
+    return s;
+}
+
+__host__ __device__ constexpr size_t smem_bytes(int tab_bytes, int ntabs) {
+    // ring, barriers, ntabs activation tables of tab_bytes = K * 8 bytes, FP2 block offsets of
+    // K / 2 bytes = tab_bytes / 16, alignment slack
+    return (size_t)kRingBytes + 1024 + (size_t)tab_bytes * ntabs + tab_bytes / 16 + 128;
+}
+
+__device__ __forceinline__ Ring warp_ring(const Smem& s, int warp) {
+    Ring R;
+    R.slots = s.ring + (size_t)warp * kStages * kSlotBytes;
+    R.full = s.bars + warp * kStages;
+    R.empty = s.bars + kWarps * kStages + warp * kStages;
+    return R;
+}
+
+__device__ inline void init_rings(const Smem& s) {
+    if (threadIdx.x < 2 * kWarps * kStages) mbar_init(s.bars + threadIdx.x, 1);
+    fence_barrier_init();
+    __syncthreads();
+}
+
+// Barrier among the consumer warps only (the producer warp does not take part).
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+}
+
+}  // namespace fpx

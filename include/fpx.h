@@ -104,7 +104,7 @@ int fpx_gemv_q(int fmt, const uint8_t* Wq, int64_t N, int64_t K, const void* x, 
  * (R binary32 [E][H], x bfloat16 [q][H]); idx[t][r], r < k, the k largest logits in descending order,
  * ties to the lower expert index; w[t][r] = sigmoid(l) / sum over the k selected sigmoids; uni the
  * sorted distinct experts of all tokens (n_uni of them, at most q*k; uni has q*k entries).
- * Limits: 1 <= k <= 8, k <= E <= 1024, H % 8 == 0. logits [q][E] is required: it is also the
+ * Limits: 1 <= k <= 8, k <= E <= 1024, H % 16 == 0. logits [q][E] is required: it is also the
  * top-k input. [P-apu], [P-dsv4] paragraph 3. */
 int moe_route_topk(const float* R, int E, int H, const uint16_t* x, int q, int k, float* logits,
                    int32_t* idx, float* w, int32_t* uni, int32_t* n_uni, void* stream);
@@ -112,7 +112,9 @@ int moe_route_topk(const float* R, int E, int H, const uint16_t* x, int q, int k
 /* One MoE layer's weights (device pointers inside a host struct). Routed experts e = 0..E-1 are
  * stacked: expert e's gate matrix starts at gate + e*fpx_matrix_bytes(FP2, I, H); likewise up (FP2,
  * I x H) and down (FP3, H x I). The shared expert is FP4: sh_gate, sh_up [I][H], sh_down [H][I].
- * router is binary32 [E][H]. H and I are multiples of 256. [P-dsv4] paragraph 2, [P-apu]. */
+ * router is binary32 [E][H]. H and I are multiples of 512 and at most 5632 (the tensor-core
+ * kernels stage two activation tables of H/64 * 512 bytes in shared memory). [P-dsv4] paragraph 2,
+ * [P-apu]. */
 typedef struct {
     int H, I, E;
     const float* router;
@@ -147,7 +149,7 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
  * status word is copied to dev_status (nullable, device, 4-byte aligned) at the end of the call.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  *   - Shapes whose moe_workspace_bytes() exceeds 4 MiB fail with FPX_ESPACE (the decode shapes,
- *     H = 4096, I = 2048, E = 256, q <= 4, k <= 8, need about 1.1 MB).
+ *     H = 4096, I = 2048, E = 256, q <= 4, k <= 8, need at most 3.3 MB).
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *     that device current; make that first call before capturing a stream into a graph.
  *   - Every call on a device shares the one array, which keeps the previous call's contents: calls

@@ -52,7 +52,7 @@ def test_gemv_argument_errors(args, expect):
 
 
 def _layer(**kw):
-    d = dict(H=512, I=256, E=16, router=FAKE, gate=FAKE, up=FAKE, down=FAKE, sh_gate=FAKE, sh_up=FAKE,
+    d = dict(H=512, I=512, E=16, router=FAKE, gate=FAKE, up=FAKE, down=FAKE, sh_gate=FAKE, sh_up=FAKE,
              sh_down=FAKE)
     d.update(kw)
     return fpx.moe_layer(**d)
@@ -75,7 +75,7 @@ def test_layer_argument_errors():
     assert call(good, k=17) == fpx.FPX_EINVAL
     assert call(good, wsb=ws - 16) == fpx.FPX_ESPACE
     assert call(good, wsp=FAKE + 8) == fpx.FPX_EALIGN
-    arr = (fpx.moe_layer * 2)(good, _layer(I=512))
+    arr = (fpx.moe_layer * 2)(good, _layer(I=1024))
     assert L.moe_stack_verify(arr, 2, FAKE, 4, 4, FAKE, None, None, FAKE, ws, None, None) == fpx.FPX_EINVAL
     assert L.moe_stack_verify(arr, 0, FAKE, 4, 4, FAKE, None, None, FAKE, ws, None, None) == fpx.FPX_EINVAL
 

@@ -48,8 +48,8 @@ def check_layer(L, bits, vals, k):
 @pytest.mark.parametrize("k", [1, 2, 4])
 def test_layer_small(q, k):
     need_gpu()
-    L = DeviceLayer(256, 256, 16, seed=q * 10 + k)
-    bits, vals = synth.tokens_bf16(q, 256, seed=k)
+    L = DeviceLayer(512, 512, 16, seed=q * 10 + k)
+    bits, vals = synth.tokens_bf16(q, 512, seed=k)
     y, idx = check_layer(L, bits, vals, k)
     for t in range(q):  # q-identity
         y1, i1, _, _ = run_layer(L, bits[t : t + 1], k)

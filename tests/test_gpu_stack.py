@@ -53,7 +53,7 @@ def check_stack(layers, q, k, sample):
 
 def test_stack_small():
     need_gpu()
-    layers = [DeviceLayer(256, 256, 16, seed=7, layer=l) for l in range(5)]
+    layers = [DeviceLayer(512, 512, 16, seed=7, layer=l) for l in range(5)]
     check_stack(layers, 4, 2, range(5))
 
 
