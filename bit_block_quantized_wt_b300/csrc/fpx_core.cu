@@ -179,6 +179,7 @@ struct GemvArgs {
     int x_bf16;
     float* y;
     int32_t* st;
+    uint32_t magic;  // kMagic, kept out of immediates (see decode_fp2)
 };
 
 template <int FMT, int Q>
@@ -220,8 +221,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gemv_mma(const __grid_consta
             for (int w = 0; w < kWarps; w++) try_issue(w);
     }
 
-    if (A.x_bf16) build_tables<FMT, 0, true>(A.x, K, Q, Sm.tab0, nullptr, Sm.csum, shift, red4);
-    else build_tables<FMT, 0, false>(A.x, K, Q, Sm.tab0, nullptr, Sm.csum, shift, red4);
+    if (A.x_bf16) build_tables<FMT, 0>(SrcBF16{reinterpret_cast<const uint16_t*>(A.x)}, K, Q, Sm.tab0, nullptr, Sm.csum, shift, red4);
+    else build_tables<FMT, 0>(SrcF32{reinterpret_cast<const float*>(A.x)}, K, Q, Sm.tab0, nullptr, Sm.csum, shift, red4);
     __syncthreads();
 
     if (warp == kWarps) {
@@ -251,22 +252,24 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gemv_mma(const __grid_consta
     const int split = warp % S;
     const Ring R = warp_ring(Sm, warp);
     const int a_idx = b_active_index(lane);
-    uint32_t consumed = 0;
+    uint32_t consumed = 0, bad = 0;
     bool ok = true;
     for (int n = 0; n < my_groups; n++) {
         const int grp = (int)blockIdx.x + n * (int)gridDim.x;
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        float y[1][4] = {{0.f, 0.f, 0.f, 0.f}};
         for (int u = 0; u < U && ok; u++) {
             if (!ring_wait(R, consumed, A.st)) { ok = false; break; }
             const uint8_t* slot = R.slots + (consumed % kStages) * kSlotBytes;
-            box_mma1<FMT>(slot, box_bytes(FMT), Sm.tab0, Sm.csum, (split * U + u) * box_chunks(FMT), a_idx, g, t, y, A.st);
+            const int chunk0 = (split * U + u) * box_chunks(FMT);
+            box_tiles<FMT, 1, box_chunks(FMT)>(slot + g * box_bytes(FMT), lane_tab(Sm.tab0, Sm.zero, a_idx, chunk0),
+                                               lane_csum(Sm.csum, chunk0, t), t, A.magic, y, bad);
             ring_release(R, consumed);
             consumed++;
         }
-        pair_reduce(y);
+        pair_reduce(y[0]);
         if (t < 2) {
 #pragma unroll
-            for (int i = 0; i < 4; i++) part[warp][g + 8 * (i >> 1)][2 * t + (i & 1)] = y[i];
+            for (int i = 0; i < 4; i++) part[warp][g + 8 * (i >> 1)][2 * t + (i & 1)] = y[0][i];
         }
         consumers_sync();
         for (int o = threadIdx.x; o < tpg * kTileRows * Q; o += kWarps * 32) {
@@ -278,6 +281,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gemv_mma(const __grid_consta
         }
         consumers_sync();
     }
+    report_bad(bad, A.st);
     if (!ok) ring_drain(R, consumed, (uint32_t)(my_groups * U));
 }
 
@@ -299,6 +303,7 @@ int launch_gemv_mma_q(const uint8_t* Wq, int64_t N, int64_t K, const void* x, in
     int S = 1;
     while (S < kWarps && ntiles * S < (int64_t)di.sms * kWarps && units % (2 * S) == 0) S *= 2;
     A.N = (int)N; A.K = (int)K; A.S = S; A.x = x; A.x_bf16 = x_bf16; A.y = y; A.st = st;
+    A.magic = kMagic;
     const int64_t ngroups = (ntiles + kWarps / S - 1) / (kWarps / S);
     const int grid = (int)(ngroups < di.sms ? ngroups : di.sms);
     const size_t smem = smem_bytes(btab_bytes((int)K), 1);

@@ -150,19 +150,22 @@ constexpr uint32_t kMagic = 0x64006400u;  // binary16 pair (1024, 1024)
 constexpr uint32_t kTwo = f16x2(2.0);
 
 // Eight A pairs from 16 FP2 codes (2 bits each, code k at bits 2k..2k+1 of w): pair i holds codes
-// (i, i + 8) as the binary16 values 1024 + c * 2^P, one LOP3 each. The MMA then sums
-// sum (1024 + c 2^P) * x 2^-P = sum c x + 1024 sum x 2^-P, and the epilogue recovers
-// sum (2c - 3) x = 2 acc - sum x 2^-P (2048 + 3 2^P) with a per-block constant of the activations.
-__device__ __forceinline__ void decode_fp2(uint32_t w, uint32_t (&a)[8]) {
+// (i, i + 8) as the binary16 values 1024 + c * 2^P, one LOP3 each. The activations are stored as
+// B = 2 x 2^-P, so the MMA sums sum (1024 + c 2^P) * 2 x 2^-P = 2 sum c x + 2048 sum x 2^-P; started
+// from C = -sum x 2^-P (2048 + 3 2^P), a per-block constant of the activations, it yields
+// sum (2c - 3) x directly.
+// `magic` is kMagic, passed in a register: with both the mask and the magic as immediates the
+// compiler splits each (w & mask) | magic into two logic operations.
+__device__ __forceinline__ void decode_fp2(uint32_t w, uint32_t magic, uint32_t (&a)[8]) {
     const uint32_t s2 = w << 2, s8 = w >> 8;
-    a[0] = (s2 & 0x000C000Cu) | kMagic;
-    a[1] = (w & 0x000C000Cu) | kMagic;
-    a[2] = (w & 0x00300030u) | kMagic;
-    a[3] = (w & 0x00C000C0u) | kMagic;
-    a[4] = (w & 0x03000300u) | kMagic;
-    a[5] = (s8 & 0x000C000Cu) | kMagic;
-    a[6] = (s8 & 0x00300030u) | kMagic;
-    a[7] = (s8 & 0x00C000C0u) | kMagic;
+    a[0] = (s2 & 0x000C000Cu) | magic;
+    a[1] = (w & 0x000C000Cu) | magic;
+    a[2] = (w & 0x00300030u) | magic;
+    a[3] = (w & 0x00C000C0u) | magic;
+    a[4] = (w & 0x03000300u) | magic;
+    a[5] = (s8 & 0x000C000Cu) | magic;
+    a[6] = (s8 & 0x00300030u) | magic;
+    a[7] = (s8 & 0x00C000C0u) | magic;
 }
 
 // FP3 high-bit plane: pair i places its two high bits at mantissa bit Q (i) and uses
@@ -174,19 +177,19 @@ template <int P, int Q>
 __host__ __device__ constexpr uint32_t fp3_mul() { return f16x2(P + 3 - Q >= 0 ? double(1 << (P + 3 - Q)) : 1.0 / double(1 << (Q - P - 3))); }
 
 // lo: 16 low-plane codes as in FP2; hg: the 16 high bits (bit k = code k).
-__device__ __forceinline__ void decode_fp3(uint32_t lo, uint32_t hg, uint32_t (&a)[8]) {
+__device__ __forceinline__ void decode_fp3(uint32_t lo, uint32_t hg, uint32_t magic, uint32_t (&a)[8]) {
     const uint32_t s2 = lo << 2, s8 = lo >> 8;
     // spread the high bits: bit k -> k (k < 8), bit 8 + k -> 16 + k
     const uint32_t sp = __byte_perm(hg, 0u, 0x4140);
     const uint32_t h3 = sp << 3, h2 = sp << 2;  // pair i < 7: Q = i + 3; pair 7: Q = 9
-    a[0] = hfma2((h3 & 0x00080008u) | kMagic, fp3_mul<2, 3>(), hfma2((s2 & 0x000C000Cu) | kMagic, kTwo, fp3_off<2, 3>()));
-    a[1] = hfma2((h3 & 0x00100010u) | kMagic, fp3_mul<2, 4>(), hfma2((lo & 0x000C000Cu) | kMagic, kTwo, fp3_off<2, 4>()));
-    a[2] = hfma2((h3 & 0x00200020u) | kMagic, fp3_mul<4, 5>(), hfma2((lo & 0x00300030u) | kMagic, kTwo, fp3_off<4, 5>()));
-    a[3] = hfma2((h3 & 0x00400040u) | kMagic, fp3_mul<6, 6>(), hfma2((lo & 0x00C000C0u) | kMagic, kTwo, fp3_off<6, 6>()));
-    a[4] = hfma2((h3 & 0x00800080u) | kMagic, fp3_mul<8, 7>(), hfma2((lo & 0x03000300u) | kMagic, kTwo, fp3_off<8, 7>()));
-    a[5] = hfma2((h3 & 0x01000100u) | kMagic, fp3_mul<2, 8>(), hfma2((s8 & 0x000C000Cu) | kMagic, kTwo, fp3_off<2, 8>()));
-    a[6] = hfma2((h3 & 0x02000200u) | kMagic, fp3_mul<4, 9>(), hfma2((s8 & 0x00300030u) | kMagic, kTwo, fp3_off<4, 9>()));
-    a[7] = hfma2((h2 & 0x02000200u) | kMagic, fp3_mul<6, 9>(), hfma2((s8 & 0x00C000C0u) | kMagic, kTwo, fp3_off<6, 9>()));
+    a[0] = hfma2((h3 & 0x00080008u) | magic, fp3_mul<2, 3>(), hfma2((s2 & 0x000C000Cu) | magic, kTwo, fp3_off<2, 3>()));
+    a[1] = hfma2((h3 & 0x00100010u) | magic, fp3_mul<2, 4>(), hfma2((lo & 0x000C000Cu) | magic, kTwo, fp3_off<2, 4>()));
+    a[2] = hfma2((h3 & 0x00200020u) | magic, fp3_mul<4, 5>(), hfma2((lo & 0x00300030u) | magic, kTwo, fp3_off<4, 5>()));
+    a[3] = hfma2((h3 & 0x00400040u) | magic, fp3_mul<6, 6>(), hfma2((lo & 0x00C000C0u) | magic, kTwo, fp3_off<6, 6>()));
+    a[4] = hfma2((h3 & 0x00800080u) | magic, fp3_mul<8, 7>(), hfma2((lo & 0x03000300u) | magic, kTwo, fp3_off<8, 7>()));
+    a[5] = hfma2((h3 & 0x01000100u) | magic, fp3_mul<2, 8>(), hfma2((s8 & 0x000C000Cu) | magic, kTwo, fp3_off<2, 8>()));
+    a[6] = hfma2((h3 & 0x02000200u) | magic, fp3_mul<4, 9>(), hfma2((s8 & 0x00300030u) | magic, kTwo, fp3_off<4, 9>()));
+    a[7] = hfma2((h2 & 0x02000200u) | magic, fp3_mul<6, 9>(), hfma2((s8 & 0x00C000C0u) | magic, kTwo, fp3_off<6, 9>()));
 }
 
 // FP4: E2M1 nibble (s, e1, e0, m) -> binary16 bits (s << 15) | (e1 e0 m) << 9, i.e. the E2M1 value
@@ -234,33 +237,53 @@ __device__ __forceinline__ float exp2i(int e) {
     return (e >= -126 && e <= 127) ? __int_as_float((e + 127) << 23) : ldexpf(1.0f, e);
 }
 
-// Eight consecutive activations from a binary32 or bfloat16 array (element offset e0, multiple of 8).
-template <bool BF16>
-__device__ __forceinline__ void load8(const void* src, size_t e0, float (&v)[8]) {
-    if constexpr (BF16) {
-        const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(src) + e0);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+// Activation sources for the table builder: load16 returns the 16 consecutive values (one code
+// group) at element offset e0 (a multiple of 16) of a [q][K] column array; V is how many groups a
+// thread loads before using them.
+struct SrcBF16 {  // bfloat16 columns
+    static constexpr int V = 4;
+    const uint16_t* x;
+    __device__ __forceinline__ void load16(size_t e0, float (&v)[16]) const {
+        const uint4* p = reinterpret_cast<const uint4*>(x + e0);
+        const uint4 a = p[0], b = p[1];
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
+        for (int i = 0; i < 8; i++) {
             v[2 * i] = __uint_as_float(w[i] << 16);
             v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
         }
-    } else {
-        const float4* f = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + e0);
-        const float4 a = f[0], b = f[1];
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     }
-}
-
-// Sixteen consecutive activations (one code group) from a binary32 or bfloat16 array.
-template <bool BF16>
-__device__ __forceinline__ void load16(const void* src, size_t e0, float (&v)[16]) {
-    float a[8], b[8];
-    load8<BF16>(src, e0, a);
-    load8<BF16>(src, e0 + 8, b);
+};
+struct SrcF32 {  // binary32 columns
+    static constexpr int V = 2;
+    const float* x;
+    __device__ __forceinline__ void load16(size_t e0, float (&v)[16]) const {
+        const float4* p = reinterpret_cast<const float4*>(x + e0);
 #pragma unroll
-    for (int i = 0; i < 8; i++) { v[i] = a[i]; v[8 + i] = b[i]; }
-}
+        for (int i = 0; i < 4; i++) {
+            const float4 f = p[i];
+            v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+        }
+    }
+};
+struct SrcSilu {  // h = silu(g) * u from binary32 g and u columns (an expert's gated activation)
+    static constexpr int V = 1;
+    const float* g;
+    const float* u;
+    __device__ __forceinline__ void load16(size_t e0, float (&v)[16]) const {
+        const float4* pg = reinterpret_cast<const float4*>(g + e0);
+        const float4* pu = reinterpret_cast<const float4*>(u + e0);
+        float gg[16], uu[16];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float4 a = pg[i], b = pu[i];
+            gg[4 * i] = a.x; gg[4 * i + 1] = a.y; gg[4 * i + 2] = a.z; gg[4 * i + 3] = a.w;
+            uu[4 * i] = b.x; uu[4 * i + 1] = b.y; uu[4 * i + 2] = b.z; uu[4 * i + 3] = b.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; i++) v[i] = (gg[i] / (1.0f + expf(-gg[i]))) * uu[i];
+    }
+};
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
@@ -268,9 +291,9 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 }
 
 // One table entry (32 bytes) = the B registers of one active lane for one chunk: the 16 activations
-// of a code group scaled by 2^(sh - P(pair)), arranged as pairs 0..7. FP2/FP3 pair p holds
-// codes (p, p + 8); FP4 pair p holds codes (8 (p/4) + p%4, +4). Also returns, for FP2, the block
-// offset contribution sum_m B_m (2048 + 3 * 2^P(m)) in code order.
+// of a code group scaled by 2^(sh - P(pair)) (FP2: 2^(sh + 1 - P)), arranged as pairs 0..7. FP2/FP3
+// pair p holds codes (p, p + 8); FP4 pair p holds codes (8 (p/4) + p%4, +4). Also returns, for FP2,
+// the block offset contribution sum_m B_m (1024 + 1.5 * 2^P(m)) in code order.
 template <int FMT>
 __device__ __forceinline__ void pack_entry(const float (&v)[16], int sh, uint4& e0, uint4& e1, float& part) {
     uint32_t w[8];
@@ -278,7 +301,7 @@ __device__ __forceinline__ void pack_entry(const float (&v)[16], int sh, uint4& 
     for (int p = 0; p < 8; p++) {
         const int lo = FMT == 4 ? 8 * (p / 4) + p % 4 : p;
         const int hi = FMT == 4 ? lo + 4 : p + 8;
-        const float sc = exp2i(sh - pair_shift(FMT, p));
+        const float sc = exp2i(sh - pair_shift(FMT, p) + (FMT == 2 ? 1 : 0));
         w[p] = pack_h2(v[lo] * sc, v[hi] * sc);
     }
     e0 = make_uint4(w[0], w[1], w[2], w[3]);
@@ -289,20 +312,20 @@ __device__ __forceinline__ void pack_entry(const float (&v)[16], int sh, uint4& 
         for (int m = 0; m < 16; m++) {
             const int p = m & 7;
             const float b = __half2float(m < 8 ? __ushort_as_half((uint16_t)(w[p] & 0xFFFFu)) : __ushort_as_half((uint16_t)(w[p] >> 16)));
-            part = fmaf(b, 2048.0f + 3.0f * float(1 << pair_shift(2, p)), part);
+            part = fmaf(b, 1024.0f + 1.5f * float(1 << pair_shift(2, p)), part);
         }
     }
 }
 
-// Builds the activation tables for columns x[tok][k] (tok < q <= 4, K % 64 == 0): tabA in format
-// FA, tabB in format FB (FB == 0: none) and, when FA == 2, the FP2 block offsets csum[block * 4 +
-// tok]. shift[4] receives the column shifts. Whole CTA (nt threads, nt % 32 == 0). Each thread owns
+// Builds the activation tables for columns src[tok][k] (tok < q <= 4, K % 64 == 0): tabA in format
+// FA, tabB in format FB (FB == 0: none) and, when FA == 2, the negated FP2 block offsets
+// csum[block * 4 + tok] (the MMA's initial accumulator). shift[4] receives the column shifts. Whole CTA (nt threads, nt % 32 == 0). Each thread owns
 // whole 16-weight code groups: it issues all of a pass's loads before using them, and writes each
 // table entry with two 16-byte stores.
-template <int FA, int FB, bool BF16>
-__device__ void build_tables(const void* x, int K, int q, uint2* tabA, uint2* tabB, float* csum, int* shift,
+template <int FA, int FB, class SRC>
+__device__ void build_tables(const SRC src, int K, int q, uint2* tabA, uint2* tabB, float* csum, int* shift,
                              float* red4) {
-    constexpr int V = BF16 ? 4 : 2;  // groups per thread per batch
+    constexpr int V = SRC::V;
     const int ngr = q * K / 16;
     const int tid = threadIdx.x, nt = blockDim.x;
     // pass 1: column maxima
@@ -314,7 +337,7 @@ __device__ void build_tables(const void* x, int K, int q, uint2* tabA, uint2* ta
         float v[V][16];
 #pragma unroll
         for (int it = 0; it < V; it++)
-            if (base + lane + it * nt < ngr) load16<BF16>(x, (size_t)(base + lane + it * nt) * 16, v[it]);
+            if (base + lane + it * nt < ngr) src.load16((size_t)(base + lane + it * nt) * 16, v[it]);
 #pragma unroll
         for (int it = 0; it < V; it++) {
             const int gi = base + lane + it * nt;
@@ -362,7 +385,7 @@ __device__ void build_tables(const void* x, int K, int q, uint2* tabA, uint2* ta
         float v[V][16];
 #pragma unroll
         for (int it = 0; it < V; it++)
-            if (base + lane + it * nt < ngr) load16<BF16>(x, (size_t)(base + lane + it * nt) * 16, v[it]);
+            if (base + lane + it * nt < ngr) src.load16((size_t)(base + lane + it * nt) * 16, v[it]);
 #pragma unroll
         for (int it = 0; it < V; it++) {
             const int gi = base + lane + it * nt;
@@ -390,7 +413,7 @@ __device__ void build_tables(const void* x, int K, int q, uint2* tabA, uint2* ta
                 const float nxt = __shfl_down_sync(0xffffffffu, part, 1);
                 if (gi < ngr && (gi & 1) == 0) {
                     const int tok = gi * 16 / K, blk = (gi * 16 - tok * K) / 32;
-                    csum[blk * 4 + tok] = part + nxt;
+                    csum[blk * 4 + tok] = -(part + nxt);
                 }
             }
         }
@@ -438,14 +461,15 @@ __host__ __device__ constexpr int elem_bytes(int fmt) { return fmt == 4 ? 2 : 1;
 // Rows decodable by the tensor-core path: whole boxes per row.
 __host__ __device__ constexpr bool mma_shape_ok(int fmt, int64_t K) { return K > 0 && K % (64 * box_chunks(fmt)) == 0; }
 
-// ------------------------------------------------------------------ per-warp chunk processing
+// ------------------------------------------------------------------ chunk processing
 
-// Loads the code groups and block scales of one chunk for rows r (thread's row g) from a staged box
-// with row pitch `pitch`, decodes them into A pairs, and returns the block scale in binary32.
-// `row` points at the start of the row inside the box, `c` is the chunk inside the box, t the thread
-// index in its group of four.
+// Loads the code groups and block scale of one chunk of one row from a staged box, decodes them into
+// A pairs and returns the block scale in binary32. `row` points at the row inside the box, `c` is the
+// chunk inside the box, t the thread index in its group of four, magic = kMagic in a register. An
+// FP4 block with the NaN scale (255) counts as zeros and sets `bad`.
 template <int FMT>
-__device__ __forceinline__ float load_decode(const uint8_t* row, int c, int t, uint32_t (&a)[8], int32_t* st) {
+__device__ __forceinline__ float load_decode(const uint8_t* row, int c, int t, uint32_t magic, uint32_t (&a)[8],
+                                             uint32_t& bad) {
     const int half = t >> 1, hw = t & 1;
     if constexpr (FMT == 2) {
         // chunk = [d0 (2) | codes0 (8) | d1 (2) | codes1 (8)], 4-byte aligned. The thread's code word
@@ -453,7 +477,7 @@ __device__ __forceinline__ float load_decode(const uint8_t* row, int c, int t, u
         const uint8_t* ch = row + 20 * c;
         const uint32_t* w = reinterpret_cast<const uint32_t*>(ch + (half ? 12 : 0) + 4 * hw);
         const uint32_t cw = __byte_perm(w[0], w[1], half ? 0x3210 : 0x5432);
-        decode_fp2(cw, a);
+        decode_fp2(cw, magic, a);
         const uint16_t d = *reinterpret_cast<const uint16_t*>(ch + 10 * half);
         return __half2float(__ushort_as_half(d));
     } else if constexpr (FMT == 3) {
@@ -462,7 +486,7 @@ __device__ __forceinline__ float load_decode(const uint8_t* row, int c, int t, u
         const uint32_t* w = reinterpret_cast<const uint32_t*>(ch + (half ? 16 : 0) + 4 * hw);
         const uint32_t lo = __byte_perm(w[0], w[1], half ? 0x3210 : 0x5432);
         const uint32_t hg = *reinterpret_cast<const uint16_t*>(ch + 14 * half + 10 + 2 * hw);
-        decode_fp3(lo, hg, a);
+        decode_fp3(lo, hg, magic, a);
         const uint16_t d = *reinterpret_cast<const uint16_t*>(ch + 14 * half);
         return __half2float(__ushort_as_half(d));
     } else {
@@ -476,21 +500,92 @@ __device__ __forceinline__ float load_decode(const uint8_t* row, int c, int t, u
         const uint32_t w0 = __funnelshift_r(x0, x1, sh), w1 = __funnelshift_r(x1, x2, sh);
         decode_fp4(w0, w1, a);
         const uint32_t e = ch[17 * half];
-        if (e == 255u) {  // NaN scale: the block is invalid and counts as zeros
-            flag(st, FPX_EDATA);
-            return 0.0f;
-        }
+        bad |= e == 255u;
         // 2^(e-127): e in 1..254 is a normal binary32 power of two, e == 0 the subnormal 2^-127
-        return e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);
+        const float sc = e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);
+        return e == 255u ? 0.0f : sc;
     }
 }
 
-// ------------------------------------------------------------------ per-warp TMA ring and tile MMA
+// D = A * B + C with C given (the FP2 block offsets), m16n8k16, binary16 inputs, binary32 accumulators.
+__device__ __forceinline__ void mma_from(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1, float c0, float c1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%10,%11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+}
+
+// Accumulates one chunk (64 weights = 2 blocks) of a 16-row tile into y[4] (the thread's (row, token)
+// partial sums for its block parity). r0 and r8 point at the tile's rows g and g + 8. For FP2, ncs
+// holds the negated block offsets of the thread's two tokens.
+template <int FMT>
+__device__ __forceinline__ void tile_chunk(const uint8_t* r0, const uint8_t* r8, int c, int t, uint32_t magic,
+                                           const uint2 (&b)[4], float2 ncs, float (&y)[4], uint32_t& bad) {
+    uint32_t a0[8], a8[8];
+    const float d0 = load_decode<FMT>(r0, c, t, magic, a0, bad);
+    const float d8 = load_decode<FMT>(r8, c, t, magic, a8, bad);
+    float acc[4];
+    if constexpr (FMT == 2) mma_from(acc, a0[0], a8[0], a0[1], a8[1], b[0].x, b[0].y, ncs.x, ncs.y);
+    else mma_first(acc, a0[0], a8[0], a0[1], a8[1], b[0].x, b[0].y);
+    mma_acc(acc, a0[2], a8[2], a0[3], a8[3], b[1].x, b[1].y);
+    mma_acc(acc, a0[4], a8[4], a0[5], a8[5], b[2].x, b[2].y);
+    mma_acc(acc, a0[6], a8[6], a0[7], a8[7], b[3].x, b[3].y);
+    y[0] = fmaf(d0, acc[0], y[0]);
+    y[1] = fmaf(d0, acc[1], y[1]);
+    y[2] = fmaf(d8, acc[2], y[2]);
+    y[3] = fmaf(d8, acc[3], y[3]);
+}
+
+// The lane's B registers for one chunk: two 16-byte loads, no branch (inactive lanes read zeros).
+__device__ __forceinline__ void load_b(const uint2* p, uint2 (&b)[4]) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+    const uint4 v0 = q[0], v1 = q[1];
+    b[0] = make_uint2(v0.x, v0.y); b[1] = make_uint2(v0.z, v0.w);
+    b[2] = make_uint2(v1.x, v1.y); b[3] = make_uint2(v1.z, v1.w);
+}
+
+// Zero area read by inactive lanes in place of table entries: one entry per chunk of a box.
+constexpr int kZeroBytes = 8 * 64 * 8;  // box_chunks <= 8 chunks x 512 bytes
+
+// Per-lane pointer to the table entries of chunk `chunk0` (64 uint2 per chunk), or to the zero area
+// for lanes whose B fragment is structurally zero.
+__device__ __forceinline__ const uint2* lane_tab(const uint2* tab, const uint2* zero, int a_idx, int chunk0) {
+    return a_idx >= 0 ? tab + (size_t)chunk0 * 64 + a_idx * 4 : zero;
+}
+
+// Per-lane pointer to the FP2 block offsets (8 floats per chunk) of chunk `chunk0`.
+__device__ __forceinline__ const float* lane_csum(const float* csum, int chunk0, int t) {
+    return csum + (size_t)chunk0 * 8 + (t >> 1) * 4 + 2 * (t & 1);
+}
+
+// NC chunks of a staged box for NT consecutive 16-row tiles sharing the activations; row points at
+// the thread's row g of the first tile, bp / csp are the lane pointers for the box's first chunk.
+// Fully unrolled so the decode of one chunk overlaps the MMAs of another.
+template <int FMT, int NT, int NC>
+__device__ __forceinline__ void box_tiles(const uint8_t* row, const uint2* bp, const float* csp, int t, uint32_t magic,
+                                          float (&y)[NT][4], uint32_t& bad) {
+    constexpr int P = box_bytes(FMT);
+#pragma unroll
+    for (int c = 0; c < NC; c++) {
+        uint2 b[4];
+        load_b(bp + c * 64, b);
+        const float2 ncs = FMT == 2 ? *reinterpret_cast<const float2*>(csp + c * 8) : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < NT; i++) tile_chunk<FMT>(row + i * 16 * P, row + (i * 16 + 8) * P, c, t, magic, b, ncs, y[i], bad);
+    }
+}
+
+// Whole warp: flags FPX_EDATA once if any lane decoded an FP4 block with the NaN scale.
+__device__ __forceinline__ void report_bad(uint32_t bad, int32_t* st) {
+    if (__any_sync(0xffffffffu, bad != 0u) && (threadIdx.x & 31) == 0) flag(st, FPX_EDATA);
+}
+
+// ------------------------------------------------------------------ per-warp TMA ring (dense GEMV)
 
 constexpr int kWarps = 8;            // consumer warps of a tensor-core CTA
 constexpr int kCtaThreads = (kWarps + 1) * 32;  // + one producer warp that issues every TMA load
 constexpr int kStages = 4;           // TMA ring depth per warp
-constexpr int kSlotBytes = 4352;     // one stage: 16 FP4 rows x 272 B, or G+U FP2 boxes, or an FP3 box
+constexpr int kSlotBytes = 4352;     // one stage: 16 FP4 rows x 272 B, or an FP2 / FP3 box
 constexpr int kRingBytes = kWarps * kStages * kSlotBytes;
 constexpr int kTileRows = 16;
 
@@ -531,75 +626,6 @@ __device__ inline void ring_drain(const Ring& R, uint32_t consumed, uint32_t exp
     for (uint32_t u = consumed; u < expected && u < consumed + kStages; u++) mbar_wait(R.full + (u % kStages), (u / kStages) & 1u);
 }
 
-// Accumulates one chunk (64 weights = 2 blocks) of a 16-row tile staged at `tile` (row pitch
-// `pitch`) into y[4] (thread's (row, token) partial sums for its block parity). For FP2, cs holds the
-// block offsets of the thread's two tokens.
-template <int FMT>
-__device__ __forceinline__ void tile_chunk(const uint8_t* tile, int pitch, int c, int g, int t, const uint2 (&b)[4],
-                                           float2 cs, float (&y)[4], int32_t* st) {
-    uint32_t a0[8], a8[8];
-    const float d0 = load_decode<FMT>(tile + g * pitch, c, t, a0, st);
-    const float d8 = load_decode<FMT>(tile + (g + 8) * pitch, c, t, a8, st);
-    float acc[4];
-    mma_first(acc, a0[0], a8[0], a0[1], a8[1], b[0].x, b[0].y);
-    mma_acc(acc, a0[2], a8[2], a0[3], a8[3], b[1].x, b[1].y);
-    mma_acc(acc, a0[4], a8[4], a0[5], a8[5], b[2].x, b[2].y);
-    mma_acc(acc, a0[6], a8[6], a0[7], a8[7], b[3].x, b[3].y);
-    if constexpr (FMT == 2) {
-        y[0] = fmaf(d0, fmaf(2.0f, acc[0], -cs.x), y[0]);
-        y[1] = fmaf(d0, fmaf(2.0f, acc[1], -cs.y), y[1]);
-        y[2] = fmaf(d8, fmaf(2.0f, acc[2], -cs.x), y[2]);
-        y[3] = fmaf(d8, fmaf(2.0f, acc[3], -cs.y), y[3]);
-    } else {
-        y[0] = fmaf(d0, acc[0], y[0]);
-        y[1] = fmaf(d0, acc[1], y[1]);
-        y[2] = fmaf(d8, acc[2], y[2]);
-        y[3] = fmaf(d8, acc[3], y[3]);
-    }
-}
-
-__device__ __forceinline__ void load_b(const uint2* tab, int chunk, int a, uint2 (&b)[4]) {
-    if (a >= 0) {
-        const uint4* p = reinterpret_cast<const uint4*>(tab + ((size_t)chunk * 16 + a) * 4);
-        const uint4 v0 = p[0], v1 = p[1];
-        b[0] = make_uint2(v0.x, v0.y); b[1] = make_uint2(v0.z, v0.w);
-        b[2] = make_uint2(v1.x, v1.y); b[3] = make_uint2(v1.z, v1.w);
-    } else {
-        b[0] = b[1] = b[2] = b[3] = make_uint2(0u, 0u);
-    }
-}
-
-// All chunks of one staged box (chunks chunk0 .. chunk0 + box_chunks - 1 of the row) for one or two
-// row tiles sharing the activations, fully unrolled so the decode of one chunk overlaps the MMAs of
-// another. csum: FP2 block offsets (ignored for FP3/FP4).
-template <int FMT>
-__device__ __forceinline__ void box_mma1(const uint8_t* tile, int pitch, const uint2* tab, const float* csum, int chunk0,
-                                         int a_idx, int g, int t, float (&y)[4], int32_t* st) {
-#pragma unroll 4
-    for (int c = 0; c < box_chunks(FMT); c++) {
-        uint2 b[4];
-        load_b(tab, chunk0 + c, a_idx, b);
-        const float2 cs = FMT == 2 ? *reinterpret_cast<const float2*>(csum + ((chunk0 + c) * 2 + (t >> 1)) * 4 + 2 * (t & 1))
-                                   : make_float2(0.f, 0.f);
-        tile_chunk<FMT>(tile, pitch, c, g, t, b, cs, y, st);
-    }
-}
-
-template <int FMT>
-__device__ __forceinline__ void box_mma2(const uint8_t* tile0, const uint8_t* tile1, int pitch, const uint2* tab,
-                                         const float* csum, int chunk0, int a_idx, int g, int t, float (&y0)[4],
-                                         float (&y1)[4], int32_t* st) {
-#pragma unroll 4
-    for (int c = 0; c < box_chunks(FMT); c++) {
-        uint2 b[4];
-        load_b(tab, chunk0 + c, a_idx, b);
-        const float2 cs = FMT == 2 ? *reinterpret_cast<const float2*>(csum + ((chunk0 + c) * 2 + (t >> 1)) * 4 + 2 * (t & 1))
-                                   : make_float2(0.f, 0.f);
-        tile_chunk<FMT>(tile0, pitch, c, g, t, b, cs, y0, st);
-        tile_chunk<FMT>(tile1, pitch, c, g, t, b, cs, y1, st);
-    }
-}
-
 // Adds the partner thread's block-parity partial sums (lane ^ 2): afterwards lanes t and t ^ 2 hold
 // the full sums of rows (g, g + 8) for tokens 2 (t % 2), 2 (t % 2) + 1.
 __device__ __forceinline__ void pair_reduce(float (&y)[4]) {
@@ -607,10 +633,11 @@ __device__ __forceinline__ void pair_reduce(float (&y)[4]) {
     for (int i = 0; i < 4; i++) y[i] += __shfl_xor_sync(0xffffffffu, y[i], 2);
 }
 
-// Shared-memory carve-up common to the tensor-core kernels.
+// Shared-memory carve-up of the per-warp-ring kernels.
 struct Smem {
     uint8_t* ring;   // kRingBytes
     uint64_t* bars;  // full[kWarps * kStages], then empty[kWarps * kStages]
+    uint2* zero;     // kZeroBytes of zeros
     uint2* tab0;     // activation tables
     uint2* tab1;
     float* csum;     // FP2 block offsets: (K / 32) blocks x 4 tokens floats = K / 2 bytes
@@ -622,16 +649,17 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, int tab_bytes, int ntabs) {
     Smem s;
     s.ring = base;
     s.bars = reinterpret_cast<uint64_t*>(base + kRingBytes);
-    s.tab0 = reinterpret_cast<uint2*>(base + kRingBytes + 1024);
-    s.tab1 = reinterpret_cast<uint2*>(base + kRingBytes + 1024 + tab_bytes);
-    s.csum = reinterpret_cast<float*>(base + kRingBytes + 1024 + (size_t)ntabs * tab_bytes);
+    s.zero = reinterpret_cast<uint2*>(base + kRingBytes + 1024);
+    s.tab0 = reinterpret_cast<uint2*>(base + kRingBytes + 1024 + kZeroBytes);
+    s.tab1 = reinterpret_cast<uint2*>(base + kRingBytes + 1024 + kZeroBytes + tab_bytes);
+    s.csum = reinterpret_cast<float*>(base + kRingBytes + 1024 + kZeroBytes + (size_t)ntabs * tab_bytes);
     return s;
 }
 
 __host__ __device__ constexpr size_t smem_bytes(int tab_bytes, int ntabs) {
-    // ring, barriers, ntabs activation tables of tab_bytes = K * 8 bytes, FP2 block offsets of
-    // K / 2 bytes = tab_bytes / 16, alignment slack
-    return (size_t)kRingBytes + 1024 + (size_t)tab_bytes * ntabs + tab_bytes / 16 + 128;
+    // ring, barriers, zero area, ntabs activation tables of tab_bytes = K * 8 bytes, FP2 block offsets
+    // of K / 2 bytes = tab_bytes / 16, alignment slack
+    return (size_t)kRingBytes + 1024 + kZeroBytes + (size_t)tab_bytes * ntabs + tab_bytes / 16 + 128;
 }
 
 __device__ __forceinline__ Ring warp_ring(const Smem& s, int warp) {
@@ -644,6 +672,7 @@ __device__ __forceinline__ Ring warp_ring(const Smem& s, int warp) {
 
 __device__ inline void init_rings(const Smem& s) {
     if (threadIdx.x < 2 * kWarps * kStages) mbar_init(s.bars + threadIdx.x, 1);
+    for (int i = threadIdx.x; i < kZeroBytes / 16; i += blockDim.x) reinterpret_cast<uint4*>(s.zero)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_barrier_init();
     __syncthreads();
 }
@@ -651,6 +680,97 @@ __device__ inline void init_rings(const Smem& s) {
 // Barrier among the consumer warps only (the producer warp does not take part).
 __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+}
+
+// ------------------------------------------------------------------ CTA-wide stages
+
+// A TMA instruction occupies its issuing thread for a few hundred nanoseconds whatever the box size,
+// so small per-warp boxes cannot keep up with HBM from one issuing thread. The MoE kernels therefore
+// stage one large box per step for the whole CTA: FP2/FP3 boxes of 256 rows (20 and 28 KB), FP4 boxes
+// of 64 rows (17 KB). One producer thread issues them into a ring of NS slots of SB bytes; consumer
+// warp w decodes rows [32w, 32w + 32) of an FP2/FP3 box (two 16-row tiles). FP4 rows come in pairs
+// of boxes (rows 0-63, then rows 64-127 of the same columns): warps 0-3 decode the first box of a
+// pair, warps 4-7 the second, 16 rows each. Every consumer warp arrives once on each slot's empty
+// barrier, whether or not it read the box.
+constexpr int kCtaRing = 143360;  // 7 x 20480 (FP2 boxes) = 5 x 28672 (FP3 boxes)
+
+__host__ __device__ constexpr int stage_rows(int fmt) { return fmt == 4 ? 64 : 256; }
+__host__ __device__ constexpr int stage_bytes(int fmt) { return box_bytes(fmt) * stage_rows(fmt); }
+// weights of a row covered by one box
+__host__ __device__ constexpr int stage_k(int fmt) { return 64 * box_chunks(fmt); }
+static_assert(stage_rows(2) == 32 * kWarps && 2 * stage_rows(4) == 16 * kWarps, "rows per consumer warp");
+
+template <int NS, int SB>
+struct CtaRing {
+    static_assert(NS * SB <= kCtaRing && SB % 128 == 0 && 2 * NS * 8 <= 256, "ring geometry");
+    uint8_t* slots;
+    uint64_t* full;   // arrival count 1 (the producer's expect_tx) + the box's transaction bytes
+    uint64_t* empty;  // arrival count kWarps
+
+    __device__ __forceinline__ uint8_t* slot(uint32_t n) const { return slots + (size_t)(n % NS) * SB; }
+
+    // Consumer warp: waits for stage n. The result is the same on all 32 lanes; on timeout lane 0
+    // flags FPX_ETIMEOUT.
+    __device__ __forceinline__ bool wait(uint32_t n, int32_t* st) const {
+        const bool done = __any_sync(0xffffffffu, mbar_wait(full + (n % NS), (n / NS) & 1u));
+        if (!done && (threadIdx.x & 31) == 0) flag(st, FPX_ETIMEOUT);
+        return done;
+    }
+
+    // Consumer warp: done with stage n.
+    __device__ __forceinline__ void release(uint32_t n) const {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(empty + (n % NS));
+    }
+
+    // Producer: waits (bounded) until stage n's slot is free, i.e. every consumer released stage
+    // n - NS.
+    __device__ __forceinline__ bool acquire(uint32_t n) const {
+        return n < (uint32_t)NS || mbar_wait(empty + (n % NS), ((n / NS) + 1u) & 1u);
+    }
+
+    // Producer, before exiting: waits (bounded) for the copies of the last stages it issued, so that
+    // no copy lands after the CTA is gone even if the consumers gave up.
+    __device__ void drain(uint32_t issued) const {
+        for (uint32_t n = issued > (uint32_t)NS ? issued - NS : 0u; n < issued; n++) mbar_wait(full + (n % NS), (n / NS) & 1u);
+    }
+};
+
+struct CtaSmem {
+    uint8_t* ring;
+    uint64_t* bars;  // 256 bytes
+    uint2* zero;     // kZeroBytes of zeros
+    uint2* tab[2];   // activation tables
+    float* csum;     // FP2 block offsets, K / 2 bytes
+};
+
+// ring, barriers, zero area, two tables of tab_bytes = K * 8 bytes, FP2 block offsets
+// (tab_bytes / 16), alignment slack
+__host__ __device__ constexpr size_t cta_smem_bytes(int tab_bytes) {
+    return (size_t)kCtaRing + 256 + kZeroBytes + 2 * (size_t)tab_bytes + tab_bytes / 16 + 128;
+}
+
+__device__ __forceinline__ CtaSmem cta_carve(uint8_t* raw, int tab_bytes) {
+    uint8_t* base = raw + ((128u - (smem_u32(raw) & 127u)) & 127u);
+    CtaSmem s;
+    s.ring = base;
+    s.bars = reinterpret_cast<uint64_t*>(base + kCtaRing);
+    s.zero = reinterpret_cast<uint2*>(base + kCtaRing + 256);
+    s.tab[0] = reinterpret_cast<uint2*>(base + kCtaRing + 256 + kZeroBytes);
+    s.tab[1] = reinterpret_cast<uint2*>(base + kCtaRing + 256 + kZeroBytes + tab_bytes);
+    s.csum = reinterpret_cast<float*>(base + kCtaRing + 256 + kZeroBytes + 2 * (size_t)tab_bytes);
+    return s;
+}
+
+template <int NS, int SB>
+__device__ inline CtaRing<NS, SB> cta_init(const CtaSmem& s) {
+    CtaRing<NS, SB> R{s.ring, s.bars, s.bars + NS};
+    if (threadIdx.x < NS) mbar_init(R.full + threadIdx.x, 1);
+    else if (threadIdx.x < 2 * NS) mbar_init(R.empty + (threadIdx.x - NS), kWarps);
+    for (int i = threadIdx.x; i < kZeroBytes / 16; i += blockDim.x) reinterpret_cast<uint4*>(s.zero)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_barrier_init();
+    __syncthreads();
+    return R;
 }
 
 }  // namespace fpx

@@ -11,8 +11,8 @@
 // bfloat16 RMS normalisation (eps 1e-6, no gain) of a binary32 residual.
 //
 // Per layer three kernels: k_router (normalise + router GEMV), k_gate_up (top-k + union recomputed
-// per CTA, then gate/up on the tensor cores, h = silu(g) u), k_down (down projection on the tensor
-// cores; the last task to finish a 16-row output tile combines it).
+// per CTA, then gate/up on the tensor cores), k_down (h = silu(g) u, down projection on the tensor
+// cores; the last task to finish a 128-row output group combines it).
 #include "fpx_mma.cuh"
 
 using namespace fpx;
@@ -27,7 +27,7 @@ constexpr int kMaxE = 1024;
 // ------------------------------------------------------------------ workspace
 
 struct Ws {
-    size_t status, logits, u, idx, w, uni, nuni, h, yi, cnt, total;
+    size_t status, logits, u, idx, w, uni, nuni, gu, yi, cnt, total;
 };
 
 inline size_t up16(size_t v) { return (v + 15) & ~size_t(15); }
@@ -42,9 +42,9 @@ inline Ws ws_layout(int H, int I, int E, int q, int k) {
     w.w = o; o = up16(o + sizeof(float) * q * k);
     w.uni = o; o = up16(o + sizeof(int32_t) * q * k);
     w.nuni = o; o += 16;
-    w.h = o; o = up16(o + sizeof(float) * (size_t)(q * k + 1) * q * I);
+    w.gu = o; o = up16(o + sizeof(float) * (size_t)2 * (q * k + 1) * q * I);
     w.yi = o; o = up16(o + sizeof(float) * (size_t)(q * k + 1) * q * H);
-    w.cnt = o; o = up16(o + sizeof(int32_t) * (size_t)(H / kTileRows));
+    w.cnt = o; o = up16(o + sizeof(int32_t) * (size_t)(H / 128));
     w.total = o;
     return w;
 }
@@ -57,8 +57,8 @@ struct WsPtrs {
     float* w;
     int32_t* uni;
     int32_t* nuni;
-    float* h;
-    float* yi;
+    float* gu;  // g and u of every item: [2 * item + (0 | 1)][q][I]
+    float* yi;  // per-item outputs [item][q][H]
     int32_t* cnt;
 };
 
@@ -67,7 +67,7 @@ inline WsPtrs ws_ptrs(void* ws, const Ws& l) {
     return WsPtrs{reinterpret_cast<int32_t*>(b + l.status), reinterpret_cast<float*>(b + l.logits),
                   reinterpret_cast<uint16_t*>(b + l.u),     reinterpret_cast<int32_t*>(b + l.idx),
                   reinterpret_cast<float*>(b + l.w),        reinterpret_cast<int32_t*>(b + l.uni),
-                  reinterpret_cast<int32_t*>(b + l.nuni),   reinterpret_cast<float*>(b + l.h),
+                  reinterpret_cast<int32_t*>(b + l.nuni),   reinterpret_cast<float*>(b + l.gu),
                   reinterpret_cast<float*>(b + l.yi),       reinterpret_cast<int32_t*>(b + l.cnt)};
 }
 
@@ -82,12 +82,12 @@ int make_layer_maps(const moe_layer& L, LayerMaps* m) {
     m->H = L.H; m->I = L.I; m->E = L.E;
     const int64_t rb2 = (int64_t)(L.H / 32) * 10, rb4h = (int64_t)(L.H / 32) * 17;
     const int64_t rb3 = (int64_t)(L.I / 32) * 14, rb4i = (int64_t)(L.I / 32) * 17;
-    int st = make_row_map(&m->gate, L.gate, rb2, (int64_t)L.E * L.I, rb2, box_bytes(2), kTileRows, 1);
-    st = st ? st : make_row_map(&m->up, L.up, rb2, (int64_t)L.E * L.I, rb2, box_bytes(2), kTileRows, 1);
-    st = st ? st : make_row_map(&m->down, L.down, rb3, (int64_t)L.E * L.H, rb3, box_bytes(3), kTileRows, 1);
-    st = st ? st : make_row_map(&m->sh_gate, L.sh_gate, rb4h, L.I, rb4h, box_bytes(4), kTileRows, 2);
-    st = st ? st : make_row_map(&m->sh_up, L.sh_up, rb4h, L.I, rb4h, box_bytes(4), kTileRows, 2);
-    st = st ? st : make_row_map(&m->sh_down, L.sh_down, rb4i, L.H, rb4i, box_bytes(4), kTileRows, 2);
+    int st = make_row_map(&m->gate, L.gate, rb2, (int64_t)L.E * L.I, rb2, box_bytes(2), stage_rows(2), 1);
+    st = st ? st : make_row_map(&m->up, L.up, rb2, (int64_t)L.E * L.I, rb2, box_bytes(2), stage_rows(2), 1);
+    st = st ? st : make_row_map(&m->down, L.down, rb3, (int64_t)L.E * L.H, rb3, box_bytes(3), stage_rows(3), 1);
+    st = st ? st : make_row_map(&m->sh_gate, L.sh_gate, rb4h, L.I, rb4h, box_bytes(4), stage_rows(4), 2);
+    st = st ? st : make_row_map(&m->sh_up, L.sh_up, rb4h, L.I, rb4h, box_bytes(4), stage_rows(4), 2);
+    st = st ? st : make_row_map(&m->sh_down, L.sh_down, rb4i, L.H, rb4i, box_bytes(4), stage_rows(4), 2);
     return st;
 }
 
@@ -240,19 +240,20 @@ __global__ void __launch_bounds__(kThreads) k_router(const float* __restrict__ R
 // ------------------------------------------------------------------ top-k + union
 
 // Warp-level top-k of lg[0..E) (descending, ties to the lower index), with sigmoid weights
-// normalised over the selected k. Each lane keeps its E / 32 logits in registers.
-__device__ void warp_topk(const float* lg, int E, int k, int32_t* idx, float* w) {
+// normalised over the selected k. Each lane keeps its E / 32 logits in registers (NM >= E / 32 slots).
+template <int NM>
+__device__ void warp_topk_n(const float* lg, int E, int k, int32_t* idx, float* w) {
     const int lane = threadIdx.x & 31;
-    float v[kMaxE / 32];
+    float v[NM];
 #pragma unroll
-    for (int m = 0; m < kMaxE / 32; m++) v[m] = lane + 32 * m < E ? lg[lane + 32 * m] : 0.0f;
+    for (int m = 0; m < NM; m++) v[m] = lane + 32 * m < E ? lg[lane + 32 * m] : 0.0f;
     uint32_t taken = 0;  // bit m: element lane + 32 m already selected
     float sig[kMaxK];
     for (int r = 0; r < k; r++) {
         float bv = 0.0f;
         int bi = -1;
 #pragma unroll
-        for (int m = 0; m < kMaxE / 32; m++) {
+        for (int m = 0; m < NM; m++) {
             const int e = lane + 32 * m;  // ascending: equal values keep the lower index
             if (e < E && !((taken >> m) & 1u) && (bi < 0 || v[m] > bv)) { bv = v[m]; bi = e; }
         }
@@ -270,6 +271,11 @@ __device__ void warp_topk(const float* lg, int E, int k, int32_t* idx, float* w)
     float S = sig[0];
     for (int r = 1; r < k; r++) S += sig[r];
     for (int r = 0; r < k; r++) w[r] = sig[r] / S;
+}
+
+__device__ void warp_topk(const float* lg, int E, int k, int32_t* idx, float* w) {
+    if (E <= 256) warp_topk_n<8>(lg, E, k, idx, w);
+    else warp_topk_n<kMaxE / 32>(lg, E, k, idx, w);
 }
 
 // Shared-memory routing state.
@@ -324,12 +330,15 @@ __global__ void k_topk(const float* __restrict__ logits, int E, int q, int k, in
     if (threadIdx.x == 0) *n_uni = r.n_uni;
 }
 
-// ------------------------------------------------------------------ K2: gate/up + SiLU
+// ------------------------------------------------------------------ K2: gate/up
 
-// Task = (item, 16-row tile of I); items are the union's experts in order, then the shared expert.
-// A routed task streams H/256 units, each a G box and a U box (16 rows x 80 B of FP2); the shared
-// task streams 2 * H/512 units, alternately G and U boxes of 16 rows x 272 B of FP4. Consumer warp w
-// of a CTA takes the CTA's tasks w, w + 8, ...; the producer warp keeps every consumer's ring full.
+// Task = (output matrix, row block): the union's gate and up matrices (FP2, 256-row blocks of I,
+// H/256 stages each), then the shared expert's gate and up (FP4, 128-row blocks, 2 * H/512 stages:
+// the two 64-row halves alternate).
+// Matrix m = 2 * item + (0 gate | 1 up), the shared expert being item n_uni. Each CTA owns a
+// contiguous task range; its producer thread streams the range's boxes through the CTA ring and all
+// eight consumer warps decode every box. Outputs g and u (binary32) go to ws.gu[m][token][row]; the
+// down kernel forms h = silu(g) u while building its activation table.
 struct GateUpArgs {
     LayerMaps m;
     int q, k;
@@ -338,30 +347,60 @@ struct GateUpArgs {
     int32_t* idx_out;
     float* w_out;
     float* logits_out;
+    uint32_t magic;  // kMagic, kept out of immediates (see decode_fp2)
 };
 
-__device__ __forceinline__ int gu_units(int shared_item, int H) { return shared_item ? 2 * (H / 512) : H / 256; }
+// Ring geometry of the two layer kernels: 7 slots of one FP2 box, 5 slots of one FP3 box.
+using GuRing = CtaRing<7, stage_bytes(2)>;
+using DnRing = CtaRing<5, stage_bytes(3)>;
 
-// Issues unit `u` of task (item, tile) into slot.
-__device__ __forceinline__ void gu_issue(const GateUpArgs& A, const Route& r, int item, int tile, int u, uint8_t* slot,
-                                         uint64_t* bar) {
-    const int row0 = tile * kTileRows;
-    if (item < r.n_uni) {
-        const int e = r.uni[item];
-        mbar_expect_tx(bar, 2 * kTileRows * box_bytes(2));
-        tma_load_2d(slot, &A.m.gate, u * box_bytes(2), e * A.m.I + row0, bar);
-        tma_load_2d(slot + kTileRows * box_bytes(2), &A.m.up, u * box_bytes(2), e * A.m.I + row0, bar);
+struct GuTask {
+    int mat;    // output matrix index
+    int fp4;    // shared expert (FP4) task
+    int row0;   // first output row
+    int grow0;  // first row in the stacked tensor map
+};
+
+__device__ __forceinline__ int gu_tasks(int n_uni, int I) { return 2 * n_uni * (I / 256) + 2 * (I / 128); }
+
+__device__ __forceinline__ GuTask gu_task(int t, const Route& r, int I) {
+    const int rb2 = I / 256, n2 = 2 * r.n_uni * rb2;
+    GuTask k;
+    if (t < n2) {
+        k.mat = t / rb2;
+        k.fp4 = 0;
+        k.row0 = (t % rb2) * 256;
+        k.grow0 = r.uni[k.mat >> 1] * I + k.row0;
     } else {
-        mbar_expect_tx(bar, kTileRows * box_bytes(4));
-        tma_load_2d(slot, (u & 1) ? &A.m.sh_up : &A.m.sh_gate, (u >> 1) * (box_bytes(4) / 2), row0, bar);
+        const int t4 = t - n2, rb4 = I / 128;
+        k.mat = 2 * r.n_uni + t4 / rb4;
+        k.fp4 = 1;
+        k.row0 = (t4 % rb4) * 128;
+        k.grow0 = k.row0;
+    }
+    return k;
+}
+
+__device__ __forceinline__ void gu_issue(const GateUpArgs& A, const GuTask& k, int s, uint8_t* slot, uint64_t* bar) {
+    if (!k.fp4) {
+        mbar_expect_tx(bar, stage_bytes(2));
+        tma_load_2d(slot, (k.mat & 1) ? &A.m.up : &A.m.gate, s * box_bytes(2), k.grow0, bar);
+    } else {
+        mbar_expect_tx(bar, stage_bytes(4));
+        tma_load_2d(slot, (k.mat & 1) ? &A.m.sh_up : &A.m.sh_gate, (s >> 1) * (box_bytes(4) / 2), k.grow0 + 64 * (s & 1), bar);
     }
 }
 
-// Producer state for one consumer warp: next task ordinal, next unit in it, units issued.
-struct Cursor {
-    int pt, pu;
+// Producer-side walk over a CTA's (task, stage) sequence.
+struct StageCursor {
+    int task, stage;
     uint32_t issued;
 };
+
+// Stages of a task: FP2/FP3 tasks stream one box per stage_k columns, FP4 tasks two (row halves).
+__device__ __forceinline__ int task_stages(int fp4, int fmt_other, int K) {
+    return fp4 ? 2 * (K / stage_k(4)) : K / stage_k(fmt_other);
+}
 
 template <int Q>
 __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constant__ GateUpArgs A) {
@@ -370,9 +409,9 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
     __shared__ int shift[kMaxQ];
     __shared__ float red4[(kWarps + 1) * 4];
     const int H = A.m.H, I = A.m.I;
-    const Smem S = carve(smem, btab_bytes(H), 2);
+    const CtaSmem S = cta_carve(smem, btab_bytes(H));
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    init_rings(S);
+    const GuRing R = cta_init<7, stage_bytes(2)>(S);
 
     // routing (every CTA), published by CTA 0
     if (warp < Q) warp_topk(A.ws.logits + (size_t)warp * A.m.E, A.m.E, A.k, r.idx + warp * A.k, r.w + warp * A.k);
@@ -390,138 +429,129 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
         if (threadIdx.x == 0) *A.ws.nuni = r.n_uni;
     }
 
-    // the CTA's task range; consumer warp w takes tasks c0 + w, c0 + w + kWarps, ...
-    const int tiles = I / kTileRows, n_items = r.n_uni + 1;
-    const int total = n_items * tiles;
+    const int total = gu_tasks(r.n_uni, I);
     const int c0 = (int)((int64_t)total * blockIdx.x / gridDim.x), c1 = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
-    auto tasks_of = [&](int w) { return c1 - c0 > w ? (c1 - c0 - w + kWarps - 1) / kWarps : 0; };
-
-    // producer: fill every ring before building the activation tables, so the first loads overlap it
-    Cursor cur[kWarps];
-    const bool producer = warp == kWarps && lane == 0;
-    auto try_issue = [&](int w) -> bool {
-        Cursor& cw = cur[w];
-        if (cw.pt >= tasks_of(w)) return false;
-        const Ring R = warp_ring(S, w);
-        if (!ring_free(R, cw.issued)) return false;
-        const int task = c0 + w + cw.pt * kWarps, item = task / tiles, tile = task % tiles;
-        const int slot = cw.issued % kStages;
-        gu_issue(A, r, item, tile, cw.pu, R.slots + (size_t)slot * kSlotBytes, R.full + slot);
-        cw.issued++;
-        if (++cw.pu == gu_units(item == r.n_uni, H)) { cw.pu = 0; cw.pt++; }
-        return true;
+    const bool producer = threadIdx.x == kWarps * 32;
+    StageCursor pc{c0, 0, 0u};
+    auto issue_next = [&]() {
+        const GuTask k = gu_task(pc.task, r, I);
+        gu_issue(A, k, pc.stage, R.slot(pc.issued), R.full + pc.issued % 7);
+        pc.issued++;
+        if (++pc.stage == task_stages(k.fp4, 2, H)) { pc.stage = 0; pc.task++; }
     };
-    if (producer) {
-#pragma unroll
-        for (int w = 0; w < kWarps; w++) cur[w] = Cursor{0, 0, 0u};
-        for (int i = 0; i < kStages; i++)
-#pragma unroll
-            for (int w = 0; w < kWarps; w++) try_issue(w);
-    }
+    // fill the ring before building the activation tables, so the first loads overlap it
+    if (producer)
+        while (pc.task < c1 && pc.issued < 7u) issue_next();
 
     // activation tables: x scaled per token, FP2 (pair-shifted, with block offsets) and FP4
-    build_tables<2, 4, true>(A.x, H, Q, S.tab0, S.tab1, S.csum, shift, red4);
+    build_tables<2, 4>(SrcBF16{A.x}, H, Q, S.tab[0], S.tab[1], S.csum, shift, red4);
     __syncthreads();
 
     if (warp == kWarps) {
         if (producer) {
-            uint64_t idle_since = 0;
-            for (;;) {
-                bool pending = false, progress = false;
-#pragma unroll
-                for (int w = 0; w < kWarps; w++) {
-                    if (cur[w].pt < tasks_of(w)) pending = true;
-                    progress |= try_issue(w);
-                }
-                if (!pending) break;
-                if (progress) {
-                    idle_since = 0;
-                } else {
-                    const uint64_t now = global_ns();
-                    if (!idle_since) idle_since = now;
-                    else if (now - idle_since > kWaitNs) { flag(A.ws.status, FPX_ETIMEOUT); break; }
-                    __nanosleep(100);
-                }
+            while (pc.task < c1) {
+                if (!R.acquire(pc.issued)) { flag(A.ws.status, FPX_ETIMEOUT); break; }
+                issue_next();
             }
+            R.drain(pc.issued);
         }
         return;
     }
 
-    // consumers
-    const Ring R = warp_ring(S, warp);
-    const int my_n = tasks_of(warp);
     const int a_idx = b_active_index(lane);
-    uint32_t consumed = 0, expected = 0;
-    for (int n = 0; n < my_n; n++) {
-        const int task = c0 + warp + n * kWarps;
-        expected += gu_units((task / tiles) == r.n_uni, H);
-    }
+    const uint32_t magic = A.magic;
+    uint32_t n = 0, bad = 0;
     bool ok = true;
-    for (int n = 0; n < my_n && ok; n++) {
-        const int task = c0 + warp + n * kWarps, item = task / tiles, tile = task % tiles;
-        const bool sh = item == r.n_uni;
-        float yg[4] = {0.f, 0.f, 0.f, 0.f}, yu[4] = {0.f, 0.f, 0.f, 0.f};
-        const int units = gu_units(sh, H);
-        for (int u = 0; u < units; u++) {
-            if (!ring_wait(R, consumed, A.ws.status)) { ok = false; break; }
-            const uint8_t* slot = R.slots + (consumed % kStages) * kSlotBytes;
-            if (!sh) {
-                box_mma2<2>(slot, slot + kTileRows * box_bytes(2), box_bytes(2), S.tab0, S.csum, u * box_chunks(2), a_idx, g, t,
-                            yg, yu, A.ws.status);
-            } else if (u & 1) {
-                box_mma1<4>(slot, box_bytes(4), S.tab1, nullptr, (u >> 1) * box_chunks(4), a_idx, g, t, yu, A.ws.status);
-            } else {
-                box_mma1<4>(slot, box_bytes(4), S.tab1, nullptr, (u >> 1) * box_chunks(4), a_idx, g, t, yg, A.ws.status);
+    for (int tk = c0; tk < c1; tk++) {
+        const GuTask k = gu_task(tk, r, I);
+        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const int ns = task_stages(k.fp4, 2, H);
+        for (int s = 0; s < ns; s++, n++) {
+            if (ok) ok = R.wait(n, A.ws.status);
+            if (!ok) continue;  // the producer gives up too once this warp stops releasing
+            const uint8_t* slot = R.slot(n);
+            if (!k.fp4) {
+                const int ch0 = s * box_chunks(2);
+                box_tiles<2, 2, box_chunks(2)>(slot + (warp * 32 + g) * box_bytes(2), lane_tab(S.tab[0], S.zero, a_idx, ch0),
+                                               lane_csum(S.csum, ch0, t), t, magic, y, bad);
+            } else if ((s & 1) == (warp >> 2)) {
+                const int ch0 = (s >> 1) * box_chunks(4);
+                box_tiles<4, 1, box_chunks(4)>(slot + ((warp & 3) * 16 + g) * box_bytes(4),
+                                               lane_tab(S.tab[1], S.zero, a_idx, ch0), nullptr, t, magic,
+                                               *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
             }
-            ring_release(R, consumed);
-            consumed++;
+            R.release(n);
         }
-        if (!ok) break;
-        pair_reduce(yg);
-        pair_reduce(yu);
+        if (!ok) continue;
+        pair_reduce(y[0]);
+        pair_reduce(y[1]);
         if (t < 2) {
-            const int row = tile * kTileRows + g;
+            const int rb = k.row0 + (k.fp4 ? 64 * (warp >> 2) + 16 * (warp & 3) : 32 * warp) + g;
+            float* out = A.ws.gu + (size_t)k.mat * Q * I;
 #pragma unroll
             for (int i = 0; i < 4; i++) {
-                const int tok = 2 * t + (i & 1), rr = row + 8 * (i >> 1);
+                const int tok = 2 * t + (i & 1), rr = rb + 8 * (i >> 1);
                 if (tok < Q) {
                     // undo the per-token activation scale (and the 2^-14 of the FP4 decode)
-                    const float sc = exp2i((sh ? 14 : 0) - shift[tok]);
-                    const float gv = yg[i] * sc, uv = yu[i] * sc;
-                    A.ws.h[((size_t)item * Q + tok) * I + rr] = (gv / (1.0f + expf(-gv))) * uv;
+                    const float sc = exp2i((k.fp4 ? 14 : 0) - shift[tok]);
+                    out[(size_t)tok * I + rr] = y[0][i] * sc;
+                    if (!k.fp4) out[(size_t)tok * I + rr + 16] = y[1][i] * sc;
                 }
             }
         }
     }
-    if (!ok) ring_drain(R, consumed, expected);
+    report_bad(bad, A.ws.status);
 }
 
 // ------------------------------------------------------------------ K3: down + combine
 
-// Task = (item, 16-row tile of H). A routed task streams I/256 FP3 units (16 rows x 112 B), the
-// shared task I/512 FP4 units (16 rows x 272 B). Each CTA owns a contiguous item-major task range,
-// which spans at most two items; it builds their activation tables from h at start. After a task
-// writes its 16 x q outputs to ws.yi, the last task to finish that row tile (integer counter)
-// combines the tile for every token: selected experts in ascending expert order, then the shared
-// expert.
+// Task = (item, row block of H): the union's down matrices (FP3, 256-row blocks, I/256 stages each),
+// then the shared expert's (FP4, 128-row blocks, 2 * I/512 stages: the two 64-row halves alternate). Each CTA owns a contiguous task range,
+// which spans at most two items (the grid has at least kMinDownCtas CTAs); it builds their
+// activation tables from h = silu(g) u at start. Every 128-row group of the output has a counter;
+// after a task's rows are in ws.yi, the task adds one to each group it covers, and the CTA that
+// brings a group's count to n_uni + 1 combines the group for every token: selected experts in
+// ascending expert order, then the shared expert.
+constexpr int kMinDownCtas = 2 * (kMaxQ * kMaxK + 1);
+
 struct DownArgs {
     LayerMaps m;
     int q, k;
     WsPtrs ws;
     float* out;  // MODE 0: y [q][H]; MODE 1: residual r [q][H], updated in place
+    uint32_t magic;
 };
 
-__device__ __forceinline__ int dn_units(int shared_item, int I) { return shared_item ? I / 512 : I / 256; }
+struct DnTask {
+    int item, fp4, row0, grow0;
+};
 
-__device__ __forceinline__ void dn_issue(const DownArgs& A, const Route& r, int item, int tile, int u, uint8_t* slot,
-                                         uint64_t* bar) {
-    const int row0 = tile * kTileRows;
-    if (item < r.n_uni) {
-        mbar_expect_tx(bar, kTileRows * box_bytes(3));
-        tma_load_2d(slot, &A.m.down, u * box_bytes(3), r.uni[item] * A.m.H + row0, bar);
+__device__ __forceinline__ int dn_tasks(int n_uni, int H) { return n_uni * (H / 256) + H / 128; }
+
+__device__ __forceinline__ DnTask dn_task(int t, const Route& r, int H) {
+    const int rb3 = H / 256, n3 = r.n_uni * rb3;
+    DnTask k;
+    if (t < n3) {
+        k.item = t / rb3;
+        k.fp4 = 0;
+        k.row0 = (t % rb3) * 256;
+        k.grow0 = r.uni[k.item] * H + k.row0;
     } else {
-        mbar_expect_tx(bar, kTileRows * box_bytes(4));
-        tma_load_2d(slot, &A.m.sh_down, u * (box_bytes(4) / 2), row0, bar);
+        k.item = r.n_uni;
+        k.fp4 = 1;
+        k.row0 = (t - n3) * 128;
+        k.grow0 = k.row0;
+    }
+    return k;
+}
+
+__device__ __forceinline__ void dn_issue(const DownArgs& A, const DnTask& k, int s, uint8_t* slot, uint64_t* bar) {
+    if (!k.fp4) {
+        mbar_expect_tx(bar, stage_bytes(3));
+        tma_load_2d(slot, &A.m.down, s * box_bytes(3), k.grow0, bar);
+    } else {
+        mbar_expect_tx(bar, stage_bytes(4));
+        tma_load_2d(slot, &A.m.sh_down, (s >> 1) * (box_bytes(4) / 2), k.grow0 + 64 * (s & 1), bar);
     }
 }
 
@@ -532,10 +562,11 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
     __shared__ float wsel[kMaxQ * kMaxK + 1][kMaxQ];  // weight of token t for union item j, NaN if unselected
     __shared__ int shift[2][kMaxQ];
     __shared__ float red4[(kWarps + 1) * 4];
+    __shared__ int last_grp[2];
     const int H = A.m.H, I = A.m.I;
-    const Smem S = carve(smem, btab_bytes(I), 2);
+    const CtaSmem S = cta_carve(smem, btab_bytes(I));
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    init_rings(S);
+    const DnRing R = cta_init<5, stage_bytes(3)>(S);
 
     if (threadIdx.x == 0) r.n_uni = *A.ws.nuni;
     for (int i = threadIdx.x; i < Q * A.k; i += blockDim.x) { r.idx[i] = A.ws.idx[i]; r.w[i] = A.ws.w[i]; r.uni[i] = A.ws.uni[i]; }
@@ -548,128 +579,137 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
         wsel[j][tok] = wv;
     }
 
-    const int tiles = H / kTileRows, n_items = r.n_uni + 1;
-    const int total = n_items * tiles;
+    const int total = dn_tasks(r.n_uni, H);
     const int c0 = (int)((int64_t)total * blockIdx.x / gridDim.x), c1 = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
-    const int item_lo = c0 / tiles;
-    auto tasks_of = [&](int w) { return c1 - c0 > w ? (c1 - c0 - w + kWarps - 1) / kWarps : 0; };
-
-    Cursor cur[kWarps];
-    const bool producer = warp == kWarps && lane == 0;
-    auto try_issue = [&](int w) -> bool {
-        Cursor& cw = cur[w];
-        if (cw.pt >= tasks_of(w)) return false;
-        const Ring R = warp_ring(S, w);
-        if (!ring_free(R, cw.issued)) return false;
-        const int task = c0 + w + cw.pt * kWarps, item = task / tiles, tile = task % tiles;
-        const int slot = cw.issued % kStages;
-        dn_issue(A, r, item, tile, cw.pu, R.slots + (size_t)slot * kSlotBytes, R.full + slot);
-        cw.issued++;
-        if (++cw.pu == dn_units(item == r.n_uni, I)) { cw.pu = 0; cw.pt++; }
-        return true;
-    };
-    if (producer) {
-#pragma unroll
-        for (int w = 0; w < kWarps; w++) cur[w] = Cursor{0, 0, 0u};
-        for (int i = 0; i < kStages; i++)
-#pragma unroll
-            for (int w = 0; w < kWarps; w++) try_issue(w);
+    if (c0 >= c1) return;  // CTA-uniform: nothing to do
+    const int item_lo = dn_task(c0, r, H).item, item_hi = dn_task(c1 - 1, r, H).item;
+    if (item_hi - item_lo > 1) {  // too small a grid (the host launches at least kMinDownCtas CTAs)
+        if (threadIdx.x == 0) flag(A.ws.status, FPX_EINVAL);
+        return;
     }
 
-    // activation tables for the (at most two) items of this CTA's range
-    for (int s = 0; s < 2; s++) {
-        const int item = item_lo + s;
-        if (c1 <= c0 || item >= n_items || item * tiles >= c1) continue;
-        const float* hsrc = A.ws.h + (size_t)item * Q * I;
-        if (item == r.n_uni) build_tables<4, 0, false>(hsrc, I, Q, s ? S.tab1 : S.tab0, nullptr, nullptr, shift[s], red4);
-        else build_tables<3, 0, false>(hsrc, I, Q, s ? S.tab1 : S.tab0, nullptr, nullptr, shift[s], red4);
+    const bool producer = threadIdx.x == kWarps * 32;
+    StageCursor pc{c0, 0, 0u};
+    auto issue_next = [&]() {
+        const DnTask k = dn_task(pc.task, r, H);
+        dn_issue(A, k, pc.stage, R.slot(pc.issued), R.full + pc.issued % 5);
+        pc.issued++;
+        if (++pc.stage == task_stages(k.fp4, 3, I)) { pc.stage = 0; pc.task++; }
+    };
+    if (producer)
+        while (pc.task < c1 && pc.issued < 5u) issue_next();
+
+    // activation tables for the (at most two) items of this CTA's range: h = silu(g) u
+    for (int sl = 0; sl <= item_hi - item_lo; sl++) {
+        const int item = item_lo + sl;
+        const SrcSilu src{A.ws.gu + (size_t)(2 * item) * Q * I, A.ws.gu + (size_t)(2 * item + 1) * Q * I};
+        uint2* tab = sl ? S.tab[1] : S.tab[0];
+        if (item == r.n_uni) build_tables<4, 0>(src, I, Q, tab, nullptr, nullptr, shift[sl], red4);
+        else build_tables<3, 0>(src, I, Q, tab, nullptr, nullptr, shift[sl], red4);
         __syncthreads();
     }
-    __syncthreads();
 
     if (warp == kWarps) {
         if (producer) {
-            uint64_t idle_since = 0;
-            for (;;) {
-                bool pending = false, progress = false;
-#pragma unroll
-                for (int w = 0; w < kWarps; w++) {
-                    if (cur[w].pt < tasks_of(w)) pending = true;
-                    progress |= try_issue(w);
-                }
-                if (!pending) break;
-                if (progress) {
-                    idle_since = 0;
-                } else {
-                    const uint64_t now = global_ns();
-                    if (!idle_since) idle_since = now;
-                    else if (now - idle_since > kWaitNs) { flag(A.ws.status, FPX_ETIMEOUT); break; }
-                    __nanosleep(100);
-                }
+            while (pc.task < c1) {
+                if (!R.acquire(pc.issued)) { flag(A.ws.status, FPX_ETIMEOUT); break; }
+                issue_next();
             }
+            R.drain(pc.issued);
         }
         return;
     }
 
-    const Ring R = warp_ring(S, warp);
-    const int my_n = tasks_of(warp);
+    // Consumers. Every consumer warp runs the same sequence of consumers_sync() whether or not a wait
+    // timed out, so a timeout never leaves a barrier short of arrivals.
     const int a_idx = b_active_index(lane);
-    uint32_t consumed = 0, expected = 0;
-    for (int n = 0; n < my_n; n++) expected += dn_units(((c0 + warp + n * kWarps) / tiles) == r.n_uni, I);
+    const uint32_t magic = A.magic;
+    uint32_t n = 0, bad = 0;
     bool ok = true;
-    for (int n = 0; n < my_n && ok; n++) {
-        const int task = c0 + warp + n * kWarps, item = task / tiles, tile = task % tiles;
-        const bool sh = item == r.n_uni;
-        const int s = item - item_lo;
-        const uint2* tab = s ? S.tab1 : S.tab0;
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
-        const int units = dn_units(sh, I);
-        for (int u = 0; u < units; u++) {
-            if (!ring_wait(R, consumed, A.ws.status)) { ok = false; break; }
-            const uint8_t* slot = R.slots + (consumed % kStages) * kSlotBytes;
-            if (!sh) box_mma1<3>(slot, box_bytes(3), tab, nullptr, u * box_chunks(3), a_idx, g, t, y, A.ws.status);
-            else box_mma1<4>(slot, box_bytes(4), tab, nullptr, u * box_chunks(4), a_idx, g, t, y, A.ws.status);
-            ring_release(R, consumed);
-            consumed++;
+    for (int tk = c0; tk < c1; tk++) {
+        const DnTask k = dn_task(tk, r, H);
+        const int sl = k.item - item_lo;
+        const uint2* tab = sl ? S.tab[1] : S.tab[0];
+        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const int ns = task_stages(k.fp4, 3, I);
+        for (int s = 0; s < ns; s++, n++) {
+            if (ok) ok = R.wait(n, A.ws.status);
+            if (!ok) continue;
+            const uint8_t* slot = R.slot(n);
+            if (!k.fp4) {
+                const int ch0 = s * box_chunks(3);
+                box_tiles<3, 2, box_chunks(3)>(slot + (warp * 32 + g) * box_bytes(3), lane_tab(tab, S.zero, a_idx, ch0), nullptr,
+                                               t, magic, y, bad);
+            } else if ((s & 1) == (warp >> 2)) {
+                const int ch0 = (s >> 1) * box_chunks(4);
+                box_tiles<4, 1, box_chunks(4)>(slot + ((warp & 3) * 16 + g) * box_bytes(4), lane_tab(tab, S.zero, a_idx, ch0),
+                                               nullptr, t, magic, *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
+            }
+            R.release(n);
         }
-        if (!ok) break;
-        pair_reduce(y);
-        if (t < 2) {
-            const int row = tile * kTileRows + g;
+        if (ok) {
+            pair_reduce(y[0]);
+            pair_reduce(y[1]);
+            if (t < 2) {
+                const int rb = k.row0 + (k.fp4 ? 64 * (warp >> 2) + 16 * (warp & 3) : 32 * warp) + g;
+                float* out = A.ws.yi + (size_t)k.item * Q * H;
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const int tok = 2 * t + (i & 1), rr = row + 8 * (i >> 1);
-                if (tok < Q) A.ws.yi[((size_t)item * Q + tok) * H + rr] = y[i] * exp2i((sh ? 14 : 0) - shift[s][tok]);
+                for (int i = 0; i < 4; i++) {
+                    const int tok = 2 * t + (i & 1), rr = rb + 8 * (i >> 1);
+                    if (tok < Q) {
+                        const float sc = exp2i((k.fp4 ? 14 : 0) - shift[sl][tok]);
+                        out[(size_t)tok * H + rr] = y[0][i] * sc;
+                        if (!k.fp4) out[(size_t)tok * H + rr + 16] = y[1][i] * sc;
+                    }
+                }
             }
         }
-        // the last task to finish this row tile combines it
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomicAdd(A.ws.cnt + tile, 1) == n_items - 1;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
+        // count this task into its 128-row groups; the last contributor combines a group (one thread
+        // publishes the CTA's writes: the barrier orders them before its fence and atomic)
+        consumers_sync();
+        if (threadIdx.x == 0) {
             __threadfence();
-            for (int o = lane; o < kTileRows * Q; o += 32) {
-                const int rr = tile * kTileRows + o / Q, tok = o % Q;
-                float acc = 0.0f;
+            const int g0 = k.row0 / 128, ng = k.fp4 ? 1 : 2;
+            for (int j = 0; j < 2; j++) last_grp[j] = (j < ng && atomicAdd(A.ws.cnt + g0 + j, 1) == r.n_uni) ? g0 + j : -1;
+            __threadfence();
+        }
+        consumers_sync();
+        for (int j = 0; j < 2; j++) {
+            const int gi = last_grp[j];
+            if (gi < 0) continue;
+            for (int o = threadIdx.x; o < 128 * Q; o += kWarps * 32) {
+                const int rr = gi * 128 + o / Q, tok = o % Q;
+                // loads in batches of 8 (independent, in flight together), then the fixed-order sum;
+                // item n_uni is the shared expert, added last
+                const float* col = A.ws.yi + (size_t)tok * H + rr;
+                const size_t istride = (size_t)Q * H;
+                float acc = 0.0f, ysh = 0.0f;
                 bool first = true;
-                for (int j = 0; j < r.n_uni; j++) {
-                    const float wv = wsel[j][tok];
-                    if (wv != wv) continue;  // expert not selected by this token
-                    const float yv = __ldcg(A.ws.yi + ((size_t)j * Q + tok) * H + rr);
-                    acc = first ? wv * yv : fmaf(wv, yv, acc);
-                    first = false;
+                for (int j0 = 0; j0 <= r.n_uni; j0 += 8) {
+                    float yv[8];
+#pragma unroll
+                    for (int u = 0; u < 8; u++) yv[u] = j0 + u <= r.n_uni ? __ldcg(col + (size_t)(j0 + u) * istride) : 0.0f;
+#pragma unroll
+                    for (int u = 0; u < 8; u++) {
+                        const int jj = j0 + u;
+                        if (jj == r.n_uni) ysh = yv[u];
+                        if (jj >= r.n_uni) continue;
+                        const float wv = wsel[jj][tok];
+                        if (wv != wv) continue;  // expert not selected by this token
+                        acc = first ? wv * yv[u] : fmaf(wv, yv[u], acc);
+                        first = false;
+                    }
                 }
-                acc += __ldcg(A.ws.yi + ((size_t)r.n_uni * Q + tok) * H + rr);
+                acc += ysh;
                 const size_t oi = (size_t)tok * H + rr;
                 if (MODE == 0) A.out[oi] = acc;
                 else A.out[oi] = A.out[oi] + acc;
             }
-            if (lane == 0) A.ws.cnt[tile] = 0;  // ready for the next call
+            if (threadIdx.x == 0) A.ws.cnt[gi] = 0;  // ready for the next call
         }
+        consumers_sync();  // last_grp is rewritten by the next task
     }
-    if (!ok) ring_drain(R, consumed, expected);
+    report_bad(bad, A.ws.status);
 }
 
 // ------------------------------------------------------------------ launch plumbing
@@ -680,7 +720,7 @@ int check_layer(const moe_layer* L) {
     if (!aligned(L->router, 16) || !aligned(L->gate, 16) || !aligned(L->up, 16) || !aligned(L->down, 16) ||
         !aligned(L->sh_gate, 16) || !aligned(L->sh_up, 16) || !aligned(L->sh_down, 16))
         return FPX_EALIGN;
-    if (smem_bytes(btab_bytes(L->H > L->I ? L->H : L->I), 2) > 227 * 1024) return FPX_EINVAL;
+    if (cta_smem_bytes(btab_bytes(L->H > L->I ? L->H : L->I)) + 2048 > 227 * 1024) return FPX_EINVAL;  // + static
     return FPX_OK;
 }
 
@@ -695,9 +735,9 @@ Plan make_plan(const moe_layer& L, int q) {
     p.g_router = (L.E + 1) / 2;
     p.sm_router = sizeof(float) * ((size_t)q * L.H + 8 * kMaxQ + 8);
     p.g_gate = di.sms;
-    p.sm_gate = smem_bytes(btab_bytes(L.H), 2);
-    p.g_down = di.sms;
-    p.sm_down = smem_bytes(btab_bytes(L.I), 2);
+    p.sm_gate = cta_smem_bytes(btab_bytes(L.H));
+    p.g_down = di.sms > kMinDownCtas ? di.sms : kMinDownCtas;
+    p.sm_down = cta_smem_bytes(btab_bytes(L.I));
     return p;
 }
 
@@ -717,6 +757,7 @@ int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, co
     ga.idx_out = idx_out;
     ga.w_out = w_out;
     ga.logits_out = logits_out;
+    ga.magic = da.magic = kMagic;
     da.out = out;
     if (cudaFuncSetAttribute(k_router<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_router) ||
         cudaFuncSetAttribute(k_gate_up<Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_gate) ||
@@ -778,7 +819,7 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     WsPtrs wp = ws_ptrs(ws, wl);
     // the row-tile counters must start at zero; the kernels leave them at zero
-    if (cudaMemsetAsync(wp.cnt, 0, sizeof(int32_t) * (layer->H / kTileRows), s) != cudaSuccess) return FPX_ECUDA;
+    if (cudaMemsetAsync(wp.cnt, 0, sizeof(int32_t) * (layer->H / 128), s) != cudaSuccess) return FPX_ECUDA;
     Plan p = make_plan(*layer, q);
     return dispatch_q<0>(q, *layer, p, k, x, nullptr, y, idx_out, w_out, logits_out, nullptr, wp, true, nullptr, s);
 }
@@ -799,7 +840,7 @@ int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int
     WsPtrs wp = ws_ptrs(ws, wl);
     const size_t state = sizeof(float) * (size_t)q * layers[0].H;
     if (r0 != rL && cudaMemcpyAsync(rL, r0, state, cudaMemcpyDeviceToDevice, s) != cudaSuccess) return FPX_ECUDA;
-    if (cudaMemsetAsync(wp.cnt, 0, sizeof(int32_t) * (layers[0].H / kTileRows), s) != cudaSuccess) return FPX_ECUDA;
+    if (cudaMemsetAsync(wp.cnt, 0, sizeof(int32_t) * (layers[0].H / 128), s) != cudaSuccess) return FPX_ECUDA;
     Plan p = make_plan(layers[0], q);
     for (int l = 0; l < n_layers; l++) {
         int32_t* io = idx_out ? idx_out + (size_t)l * q * k : nullptr;
@@ -827,7 +868,7 @@ int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int
 
 namespace {
 
-constexpr size_t kStaticWsBytes = size_t(4) << 20;  // 4 MiB: the decode shapes need at most 3.3 MB
+constexpr size_t kStaticWsBytes = size_t(8) << 20;  // 8 MiB: the decode shapes need at most 4.4 MB
 __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
 // In host code `g_static_ws` only names the symbol; its device address differs per device and is

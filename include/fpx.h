@@ -112,8 +112,9 @@ int moe_route_topk(const float* R, int E, int H, const uint16_t* x, int q, int k
 /* One MoE layer's weights (device pointers inside a host struct). Routed experts e = 0..E-1 are
  * stacked: expert e's gate matrix starts at gate + e*fpx_matrix_bytes(FP2, I, H); likewise up (FP2,
  * I x H) and down (FP3, H x I). The shared expert is FP4: sh_gate, sh_up [I][H], sh_down [H][I].
- * router is binary32 [E][H]. H and I are multiples of 512 and at most 5632 (the tensor-core
- * kernels stage two activation tables of H/64 * 512 bytes in shared memory). [P-dsv4] paragraph 2,
+ * router is binary32 [E][H]. H and I are multiples of 512 and at most 4608 (the tensor-core
+ * kernels hold a 144 KB ring of weight boxes and two activation tables of 8*H bytes in shared
+ * memory). [P-dsv4] paragraph 2,
  * [P-apu]. */
 typedef struct {
     int H, I, E;
@@ -144,12 +145,12 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
  * inside a host framework that owns every device allocation (its own arena or allocator) and allows
  * no others, or a latency-critical loop that must never call cudaMalloc/cudaFree because they can
  * synchronise the device. The pages have no counterpart to this call; it exists for deployment only.
- * Same arguments and results as moe_layer_decode, except that the scratch is a 4 MiB array inside
+ * Same arguments and results as moe_layer_decode, except that the scratch is an 8 MiB array inside
  * libfpx.so (one per device, held until the process exits) instead of a caller workspace, and the
  * status word is copied to dev_status (nullable, device, 4-byte aligned) at the end of the call.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
- *   - Shapes whose moe_workspace_bytes() exceeds 4 MiB fail with FPX_ESPACE (the decode shapes,
- *     H = 4096, I = 2048, E = 256, q <= 4, k <= 8, need at most 3.3 MB).
+ *   - Shapes whose moe_workspace_bytes() exceeds 8 MiB fail with FPX_ESPACE (the decode shapes,
+ *     H = 4096, I = 2048, E = 256, q <= 4, k <= 8, need at most 4.4 MB).
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *     that device current; make that first call before capturing a stream into a graph.
  *   - Every call on a device shares the one array, which keeps the previous call's contents: calls
