@@ -32,6 +32,8 @@ WORKLOAD = ("43-layer synthetic MoE stack, each layer hidden 4096, 256 routed ex
 N_BATCHES = 8
 
 
+NK = 4  # kernels per layer: router, gate/up, down, combine
+
 def layer_bytes(n_union):
     import bit_block_quantized_wt_b300 as fpx
     gu = fpx.fpx_matrix_bytes(2, I, H)
@@ -247,21 +249,21 @@ def kernel_profile(runner, steps):
     import ctypes as C
     torch = runner.torch
     L = len(runner.stack.layers)
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(3 * L + 1)]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(NK * L + 1)]
     with torch.cuda.stream(runner.stream):
         for e in evs:
             e.record(runner.stream)  # materialise the handles
         runner.stream.synchronize()
         handles = [e.cuda_event for e in evs]
-        sums = np.zeros(3)
-        per_layer = np.zeros((3, L))
+        sums = np.zeros(NK)
+        per_layer = np.zeros((NK, L))
         for i in range(steps):
             runner.rin.copy_(runner.batches[i % N_BATCHES])
             runner.call(events=handles)
             runner.stream.synchronize()
             for l in range(L):
-                for j in range(3):
-                    dt = evs[3 * l + j].elapsed_time(evs[3 * l + j + 1])
+                for j in range(NK):
+                    dt = evs[NK * l + j].elapsed_time(evs[NK * l + j + 1])
                     sums[j] += dt
                     per_layer[j, l] += dt
     return sums / (steps * L), per_layer / steps
@@ -375,9 +377,11 @@ def run_fpx(args):
     # per-kernel durations (events around every kernel of the pass, on its stream)
     prof_steps = max(3, min(20, args.steps))
     kavg, kper_layer = kernel_profile(r4, prof_steps)
-    names = ["k_router", "k_gate_up", "k_down"]
+    names = ["k_router", "k_gate_up", "k_down", "k_combine"]
     mean_union = float(np.mean([np.mean(u) for u in unions]))
-    alg = [stack.layers[0].E * H * 4, gate_up_bytes(mean_union), down_bytes(mean_union)]
+    # k_combine reads the 2 K parts of every routed output, the shared output and r, and writes r
+    alg = [stack.layers[0].E * H * 4, gate_up_bytes(mean_union), down_bytes(mean_union),
+           (2 * mean_union + 3) * Q * H * 4]
     dom = int(np.argmax(kavg))
     achieved = alg[dom] / (kavg[dom] / 1e3) / 1e9
 
@@ -418,7 +422,7 @@ def run_fpx(args):
                      "avg_launch_ms": round(float(kavg[dom]), 5)},
         "e2e": {"value": round(e2e_bytes / e2e_secs / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": args.steps * 3 * args.layers,
+        "gpu_launches": args.steps * NK * args.layers,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.skip_cpu:

@@ -33,6 +33,13 @@
 
 namespace fpx {
 
+constexpr int kWarps = 8;  // consumer warps of a tensor-core CTA (plus one producer warp)
+
+// Barrier among the kWarps consumer warps only (the producer warp does not take part).
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+}
+
 // ------------------------------------------------------------------ compile-time binary16 bits
 
 // Bit pattern of a binary16 number that is exactly representable (a small integer times a power of
@@ -270,6 +277,7 @@ struct SrcSilu {  // h = silu(g) * u from binary32 g and u columns (an expert's 
     static constexpr int V = 1;
     const float* g;
     const float* u;
+    size_t half;  // nonzero: g and u are each the sum of two partials, the second `half` floats on
     __device__ __forceinline__ void load16(size_t e0, float (&v)[16]) const {
         const float4* pg = reinterpret_cast<const float4*>(g + e0);
         const float4* pu = reinterpret_cast<const float4*>(u + e0);
@@ -279,6 +287,16 @@ struct SrcSilu {  // h = silu(g) * u from binary32 g and u columns (an expert's 
             const float4 a = pg[i], b = pu[i];
             gg[4 * i] = a.x; gg[4 * i + 1] = a.y; gg[4 * i + 2] = a.z; gg[4 * i + 3] = a.w;
             uu[4 * i] = b.x; uu[4 * i + 1] = b.y; uu[4 * i + 2] = b.z; uu[4 * i + 3] = b.w;
+        }
+        if (half) {
+            const float4* qg = reinterpret_cast<const float4*>(g + half + e0);
+            const float4* qu = reinterpret_cast<const float4*>(u + half + e0);
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const float4 a = qg[i], b = qu[i];
+                gg[4 * i] += a.x; gg[4 * i + 1] += a.y; gg[4 * i + 2] += a.z; gg[4 * i + 3] += a.w;
+                uu[4 * i] += b.x; uu[4 * i + 1] += b.y; uu[4 * i + 2] += b.z; uu[4 * i + 3] += b.w;
+            }
         }
 #pragma unroll
         for (int i = 0; i < 16; i++) v[i] = (gg[i] / (1.0f + expf(-gg[i]))) * uu[i];
@@ -322,12 +340,14 @@ __device__ __forceinline__ void pack_entry(const float (&v)[16], int sh, uint4& 
 // csum[block * 4 + tok] (the MMA's initial accumulator). shift[4] receives the column shifts. Whole CTA (nt threads, nt % 32 == 0). Each thread owns
 // whole 16-weight code groups: it issues all of a pass's loads before using them, and writes each
 // table entry with two 16-byte stores.
-template <int FA, int FB, class SRC>
+// CONS: only the kWarps consumer warps (threads 0 .. 32 kWarps - 1) take part and synchronise on
+// the consumer barrier, so the producer warp can issue loads meanwhile; otherwise the whole CTA.
+template <int FA, int FB, bool CONS = false, class SRC>
 __device__ void build_tables(const SRC src, int K, int q, uint2* tabA, uint2* tabB, float* csum, int* shift,
                              float* red4) {
     constexpr int V = SRC::V;
     const int ngr = q * K / 16;
-    const int tid = threadIdx.x, nt = blockDim.x;
+    const int tid = threadIdx.x, nt = CONS ? kWarps * 32 : blockDim.x;
     // pass 1: column maxima
     float m[4] = {0.f, 0.f, 0.f, 0.f};
     // loops start at the warp's first thread so every lane of a warp runs the same iterations (the
@@ -373,13 +393,13 @@ __device__ void build_tables(const SRC src, int K, int q, uint2* tabA, uint2* ta
     if (FA == 2)
         for (int i = tid; i < (K / 32) * 4; i += nt)
             if ((i & 3) >= q) csum[i] = 0.f;
-    __syncthreads();
+    if (CONS) consumers_sync(); else __syncthreads();
     if (tid < 4) {
         float mm = 0.f;
         for (int w = 0; w < nt / 32; w++) mm = fmaxf(mm, red4[w * 4 + tid]);
         shift[tid] = column_shift(mm);
     }
-    __syncthreads();
+    if (CONS) consumers_sync(); else __syncthreads();
     // pass 2: whole entries
     for (int base = tid - lane; base < ngr; base += V * nt) {
         float v[V][16];
@@ -582,7 +602,6 @@ __device__ __forceinline__ void report_bad(uint32_t bad, int32_t* st) {
 
 // ------------------------------------------------------------------ per-warp TMA ring (dense GEMV)
 
-constexpr int kWarps = 8;            // consumer warps of a tensor-core CTA
 constexpr int kCtaThreads = (kWarps + 1) * 32;  // + one producer warp that issues every TMA load
 constexpr int kStages = 4;           // TMA ring depth per warp
 constexpr int kSlotBytes = 4352;     // one stage: 16 FP4 rows x 272 B, or an FP2 / FP3 box
@@ -677,44 +696,41 @@ __device__ inline void init_rings(const Smem& s) {
     __syncthreads();
 }
 
-// Barrier among the consumer warps only (the producer warp does not take part).
-__device__ __forceinline__ void consumers_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
-}
 
 // ------------------------------------------------------------------ CTA-wide stages
 
 // A TMA instruction occupies its issuing thread for a few hundred nanoseconds whatever the box size,
-// so small per-warp boxes cannot keep up with HBM from one issuing thread. The MoE kernels therefore
-// stage one large box per step for the whole CTA: FP2/FP3 boxes of 256 rows (20 and 28 KB), FP4 boxes
-// of 64 rows (17 KB). One producer thread issues them into a ring of NS slots of SB bytes; consumer
-// warp w decodes rows [32w, 32w + 32) of an FP2/FP3 box (two 16-row tiles). FP4 rows come in pairs
-// of boxes (rows 0-63, then rows 64-127 of the same columns): warps 0-3 decode the first box of a
-// pair, warps 4-7 the second, 16 rows each. Every consumer warp arrives once on each slot's empty
-// barrier, whether or not it read the box.
+// so small per-warp boxes cannot keep up with HBM, and the issuing must stay off the consumers'
+// path. The MoE kernels stage one large box per step for the whole CTA: FP2/FP3 boxes of 256 rows
+// (20 and 28 KB), FP4 boxes of 64 rows (17 KB), in a ring of NS slots of SB bytes filled by one
+// producer thread (warp kWarps). All kWarps consumer warps read every stage:
+//   FP2/FP3 box: warp w decodes rows [32w, 32w + 32) (two 16-row tiles), all 4 chunks.
+//   FP4 box: warp w decodes rows [16 (w % 4), +16), chunks 4 (w / 4) .. 4 (w / 4) + 3; the two
+//   partial sums of a row (warps w, w + 4) are added in warp order at the end of the task.
 constexpr int kCtaRing = 143360;  // 7 x 20480 (FP2 boxes) = 5 x 28672 (FP3 boxes)
 
 __host__ __device__ constexpr int stage_rows(int fmt) { return fmt == 4 ? 64 : 256; }
 __host__ __device__ constexpr int stage_bytes(int fmt) { return box_bytes(fmt) * stage_rows(fmt); }
 // weights of a row covered by one box
 __host__ __device__ constexpr int stage_k(int fmt) { return 64 * box_chunks(fmt); }
-static_assert(stage_rows(2) == 32 * kWarps && 2 * stage_rows(4) == 16 * kWarps, "rows per consumer warp");
+static_assert(stage_rows(2) == 32 * kWarps && stage_rows(4) * 2 == 16 * kWarps, "rows per warp");
 
 template <int NS, int SB>
 struct CtaRing {
-    static_assert(NS * SB <= kCtaRing && SB % 128 == 0 && 2 * NS * 8 <= 256, "ring geometry");
+    static_assert(NS * SB <= kCtaRing && SB % 128 == 0 && NS <= 8, "ring geometry");
     uint8_t* slots;
     uint64_t* full;   // arrival count 1 (the producer's expect_tx) + the box's transaction bytes
     uint64_t* empty;  // arrival count kWarps
 
     __device__ __forceinline__ uint8_t* slot(uint32_t n) const { return slots + (size_t)(n % NS) * SB; }
+    __device__ __forceinline__ uint64_t* bar(uint32_t n) const { return full + (n % NS); }
 
     // Consumer warp: waits for stage n. The result is the same on all 32 lanes; on timeout lane 0
     // flags FPX_ETIMEOUT.
     __device__ __forceinline__ bool wait(uint32_t n, int32_t* st) const {
-        const bool done = __any_sync(0xffffffffu, mbar_wait(full + (n % NS), (n / NS) & 1u));
-        if (!done && (threadIdx.x & 31) == 0) flag(st, FPX_ETIMEOUT);
-        return done;
+        const bool ok = __any_sync(0xffffffffu, mbar_wait(full + (n % NS), (n / NS) & 1u));
+        if (!ok && (threadIdx.x & 31) == 0) flag(st, FPX_ETIMEOUT);
+        return ok;
     }
 
     // Consumer warp: done with stage n.
@@ -723,8 +739,7 @@ struct CtaRing {
         if ((threadIdx.x & 31) == 0) mbar_arrive(empty + (n % NS));
     }
 
-    // Producer: waits (bounded) until stage n's slot is free, i.e. every consumer released stage
-    // n - NS.
+    // Producer: waits (bounded) until stage n's slot is free, i.e. every consumer released n - NS.
     __device__ __forceinline__ bool acquire(uint32_t n) const {
         return n < (uint32_t)NS || mbar_wait(empty + (n % NS), ((n / NS) + 1u) & 1u);
     }
@@ -732,33 +747,39 @@ struct CtaRing {
     // Producer, before exiting: waits (bounded) for the copies of the last stages it issued, so that
     // no copy lands after the CTA is gone even if the consumers gave up.
     __device__ void drain(uint32_t issued) const {
-        for (uint32_t n = issued > (uint32_t)NS ? issued - NS : 0u; n < issued; n++) mbar_wait(full + (n % NS), (n / NS) & 1u);
+        for (uint32_t n = issued > (uint32_t)NS ? issued - NS : 0u; n < issued; n++)
+            if (!mbar_wait(full + (n % NS), (n / NS) & 1u)) return;
     }
 };
 
 struct CtaSmem {
     uint8_t* ring;
-    uint64_t* bars;  // 256 bytes
+    uint64_t* bars;  // 256 bytes: full[NS], empty[NS]
     uint2* zero;     // kZeroBytes of zeros
+    float* red;      // kWarps * 64 floats: cross-warp partial sums
     uint2* tab[2];   // activation tables
     float* csum;     // FP2 block offsets, K / 2 bytes
 };
 
-// ring, barriers, zero area, two tables of tab_bytes = K * 8 bytes, FP2 block offsets
+constexpr int kRedBytes = kWarps * 64 * 4;
+
+// ring, barriers, zero area, reduction area, two tables of tab_bytes = K * 8 bytes, FP2 block offsets
 // (tab_bytes / 16), alignment slack
 __host__ __device__ constexpr size_t cta_smem_bytes(int tab_bytes) {
-    return (size_t)kCtaRing + 256 + kZeroBytes + 2 * (size_t)tab_bytes + tab_bytes / 16 + 128;
+    return (size_t)kCtaRing + 256 + kZeroBytes + kRedBytes + 2 * (size_t)tab_bytes + tab_bytes / 16 + 128;
 }
 
 __device__ __forceinline__ CtaSmem cta_carve(uint8_t* raw, int tab_bytes) {
     uint8_t* base = raw + ((128u - (smem_u32(raw) & 127u)) & 127u);
     CtaSmem s;
+    size_t o = kCtaRing;
     s.ring = base;
-    s.bars = reinterpret_cast<uint64_t*>(base + kCtaRing);
-    s.zero = reinterpret_cast<uint2*>(base + kCtaRing + 256);
-    s.tab[0] = reinterpret_cast<uint2*>(base + kCtaRing + 256 + kZeroBytes);
-    s.tab[1] = reinterpret_cast<uint2*>(base + kCtaRing + 256 + kZeroBytes + tab_bytes);
-    s.csum = reinterpret_cast<float*>(base + kCtaRing + 256 + kZeroBytes + 2 * (size_t)tab_bytes);
+    s.bars = reinterpret_cast<uint64_t*>(base + o); o += 256;
+    s.zero = reinterpret_cast<uint2*>(base + o); o += kZeroBytes;
+    s.red = reinterpret_cast<float*>(base + o); o += kRedBytes;
+    s.tab[0] = reinterpret_cast<uint2*>(base + o); o += tab_bytes;
+    s.tab[1] = reinterpret_cast<uint2*>(base + o); o += tab_bytes;
+    s.csum = reinterpret_cast<float*>(base + o);
     return s;
 }
 
@@ -771,6 +792,20 @@ __device__ inline CtaRing<NS, SB> cta_init(const CtaSmem& s) {
     fence_barrier_init();
     __syncthreads();
     return R;
+}
+
+// Adds the two FP4 partial sums of each row (warps w, w + 4) in warp order. Every consumer warp calls
+// it with its pair-reduced y; afterwards warps 0..3 hold the sums. Contains two consumer barriers.
+__device__ inline void fp4_reduce(float* red, float (&y)[4]) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    if (warp >= 4 && t < 2)
+#pragma unroll
+        for (int i = 0; i < 4; i++) red[(warp - 4) * 64 + (g + 8 * (i >> 1)) * 4 + 2 * t + (i & 1)] = y[i];
+    consumers_sync();
+    if (warp < 4 && t < 2)
+#pragma unroll
+        for (int i = 0; i < 4; i++) y[i] += red[warp * 64 + (g + 8 * (i >> 1)) * 4 + 2 * t + (i & 1)];
+    consumers_sync();
 }
 
 }  // namespace fpx

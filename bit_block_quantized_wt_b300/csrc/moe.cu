@@ -10,9 +10,9 @@
 // zero-weight term is ever added) and then the shared expert; the stack's layer input is the
 // bfloat16 RMS normalisation (eps 1e-6, no gain) of a binary32 residual.
 //
-// Per layer three kernels: k_router (normalise + router GEMV), k_gate_up (top-k + union recomputed
-// per CTA, then gate/up on the tensor cores), k_down (h = silu(g) u, down projection on the tensor
-// cores; the last task to finish a 128-row output group combines it).
+// Per layer four kernels, each launched to overlap the previous one's tail: k_router (normalise,
+// router GEMV; its last CTA routes every token), k_gate_up (gate/up on the tensor cores), k_down
+// (h = silu(g) u, down projection on the tensor cores) and k_combine (weighted sum per token).
 #include "fpx_mma.cuh"
 
 using namespace fpx;
@@ -24,10 +24,18 @@ constexpr int kMaxK = 8;
 constexpr int kMaxQ = 4;
 constexpr int kMaxE = 1024;
 
+// Programmatic dependent launch: each layer kernel is launched so that it may start while the
+// previous kernel's last CTAs still run; grid_dep_wait() blocks until that kernel has completed and
+// its writes are visible. Work that does not read the previous kernel's output goes before it.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel launch early (it still waits for this one with grid_dep_wait()).
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ workspace
 
 struct Ws {
-    size_t status, logits, u, idx, w, uni, nuni, gu, yi, cnt, total;
+    size_t status, logits, u, idx, w, uni, nuni, gu, yi, total;
+    size_t gu_half, yi_half;  // floats between the two K-split partial buffers
 };
 
 inline size_t up16(size_t v) { return (v + 15) & ~size_t(15); }
@@ -41,10 +49,11 @@ inline Ws ws_layout(int H, int I, int E, int q, int k) {
     w.idx = o; o = up16(o + sizeof(int32_t) * q * k);
     w.w = o; o = up16(o + sizeof(float) * q * k);
     w.uni = o; o = up16(o + sizeof(int32_t) * q * k);
-    w.nuni = o; o += 16;
-    w.gu = o; o = up16(o + sizeof(float) * (size_t)2 * (q * k + 1) * q * I);
-    w.yi = o; o = up16(o + sizeof(float) * (size_t)(q * k + 1) * q * H);
-    w.cnt = o; o = up16(o + sizeof(int32_t) * (size_t)(H / 128));
+    w.nuni = o; o += 16;  // n_uni, then the router's arrival counter
+    w.gu_half = (size_t)2 * (q * k + 1) * q * I;
+    w.yi_half = (size_t)(q * k + 1) * q * H;
+    w.gu = o; o = up16(o + sizeof(float) * 2 * w.gu_half);
+    w.yi = o; o = up16(o + sizeof(float) * 2 * w.yi_half);
     w.total = o;
     return w;
 }
@@ -57,9 +66,9 @@ struct WsPtrs {
     float* w;
     int32_t* uni;
     int32_t* nuni;
-    float* gu;  // g and u of every item: [2 * item + (0 | 1)][q][I]
-    float* yi;  // per-item outputs [item][q][H]
-    int32_t* cnt;
+    float* gu;  // g and u of every item: [K half][2 * item + (0 | 1)][q][I]
+    float* yi;  // per-item outputs [K half][item][q][H]
+    size_t gu_half, yi_half;
 };
 
 inline WsPtrs ws_ptrs(void* ws, const Ws& l) {
@@ -68,7 +77,8 @@ inline WsPtrs ws_ptrs(void* ws, const Ws& l) {
                   reinterpret_cast<uint16_t*>(b + l.u),     reinterpret_cast<int32_t*>(b + l.idx),
                   reinterpret_cast<float*>(b + l.w),        reinterpret_cast<int32_t*>(b + l.uni),
                   reinterpret_cast<int32_t*>(b + l.nuni),   reinterpret_cast<float*>(b + l.gu),
-                  reinterpret_cast<float*>(b + l.yi),       reinterpret_cast<int32_t*>(b + l.cnt)};
+                  reinterpret_cast<float*>(b + l.yi),       l.gu_half,
+                  l.yi_half};
 }
 
 // Everything the gate/up and down kernels need about one layer: tensor maps over the stacked
@@ -117,126 +127,6 @@ __device__ float block_max(float v, float* red) {
     return s;
 }
 
-// ------------------------------------------------------------------ K1: router logits
-
-// Computes the layer input u (binary32 values of bfloat16) and logits[t][e] for this CTA's experts.
-// MODE 0: input x is bfloat16. MODE 1: input is the residual r; u = RN_bf16(r / rms(r)), and CTA 0
-// publishes u (for the gate/up kernel) and r (the trace). Each CTA handles 2 experts with 4 warps per
-// expert, each warp a quarter of H; the quarter sums are added in order.
-template <int MODE>
-__global__ void __launch_bounds__(kThreads) k_router(const float* __restrict__ R, int E, int H, int q,
-                                                     const uint16_t* __restrict__ xin, const float* __restrict__ rin,
-                                                     float* __restrict__ logits, uint16_t* __restrict__ u_out,
-                                                     float* __restrict__ r_trace, int32_t* status_to_clear) {
-    extern __shared__ __align__(16) float sm[];
-    float* u_s = sm;                      // [q][H]
-    float* part = sm + (size_t)q * H;     // [8 warps][kMaxQ]
-    float* red = part + 8 * kMaxQ;        // [8]
-    if (status_to_clear && blockIdx.x == 0 && threadIdx.x == 0) *status_to_clear = 0;
-    if (MODE == 0) {
-        for (int i = threadIdx.x; i < q * H; i += blockDim.x) u_s[i] = bf16_bits_to_float(xin[i]);
-    } else {
-        // each thread loads its float4s of r for all tokens at once (H % 4 == 0), then reduces
-        constexpr int V = 16;
-        const int n4 = q * H / 4;
-        const float4* r4 = reinterpret_cast<const float4*>(rin);
-        float ss[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
-        for (int base = threadIdx.x; base < n4; base += V * blockDim.x) {
-            float4 rv[V];
-#pragma unroll
-            for (int i = 0; i < V; i++) {
-                const int idx = base + i * blockDim.x;
-                rv[i] = idx < n4 ? r4[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int i = 0; i < V; i++) {
-                const int idx = base + i * blockDim.x;
-                if (idx < n4) {
-                    const int t = idx * 4 / H;
-                    float a = 0.f;
-                    a = fmaf(rv[i].x, rv[i].x, a); a = fmaf(rv[i].y, rv[i].y, a);
-                    a = fmaf(rv[i].z, rv[i].z, a); a = fmaf(rv[i].w, rv[i].w, a);
-#pragma unroll
-                    for (int tt = 0; tt < kMaxQ; tt++) ss[tt] += tt == t ? a : 0.f;
-                }
-            }
-        }
-        float inv[kMaxQ];
-        for (int t = 0; t < kMaxQ; t++) inv[t] = 1.0f / sqrtf(block_sum(ss[t], red) / (float)H + 1e-6f);
-        for (int base = threadIdx.x; base < n4; base += V * blockDim.x) {
-            float4 rv[V];
-#pragma unroll
-            for (int i = 0; i < V; i++) {
-                const int idx = base + i * blockDim.x;
-                rv[i] = idx < n4 ? r4[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int i = 0; i < V; i++) {
-                const int idx = base + i * blockDim.x;
-                if (idx < n4) {
-                    const int t = idx * 4 / H;
-                    const float iv = inv[0] * (t == 0) + inv[1] * (t == 1) + inv[2] * (t == 2) + inv[3] * (t == 3);
-                    const float vv[4] = {rv[i].x, rv[i].y, rv[i].z, rv[i].w};
-                    uint16_t ub[4];
-#pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        const __nv_bfloat16 b = __float2bfloat16_rn(vv[j] * iv);
-                        u_s[(size_t)idx * 4 + j] = __bfloat162float(b);
-                        ub[j] = __bfloat16_as_ushort(b);
-                    }
-                    if (blockIdx.x == 0) {
-                        reinterpret_cast<uint2*>(u_out)[idx] = make_uint2(ub[0] | (uint32_t(ub[1]) << 16), ub[2] | (uint32_t(ub[3]) << 16));
-                        if (r_trace) reinterpret_cast<float4*>(r_trace)[idx] = rv[i];
-                    }
-                }
-            }
-        }
-    }
-    __syncthreads();
-    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * 2 + warp / 4, slice = warp % 4;
-    const int h0 = H * slice / 4, h1 = H * (slice + 1) / 4;  // H % 16 == 0: quarters are float4-aligned
-    float acc[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
-    if (e < E) {
-        const float4* row = reinterpret_cast<const float4*>(R + (size_t)e * H);
-        // batches of 8 independent loads per lane, then the FMAs (same order as a plain loop)
-        for (int base = h0 / 4 + lane; base < h1 / 4; base += 8 * 32) {
-            float4 rv[8];
-#pragma unroll
-            for (int b = 0; b < 8; b++) rv[b] = base + 32 * b < h1 / 4 ? __ldg(row + base + 32 * b) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int b = 0; b < 8; b++) {
-                const int h4 = base + 32 * b;
-                if (h4 >= h1 / 4) break;
-#pragma unroll
-                for (int t = 0; t < kMaxQ; t++) {
-                    if (t < q) {
-                        const float4 uv = *reinterpret_cast<const float4*>(u_s + (size_t)t * H + 4 * h4);
-                        acc[t] = fmaf(rv[b].x, uv.x, acc[t]);
-                        acc[t] = fmaf(rv[b].y, uv.y, acc[t]);
-                        acc[t] = fmaf(rv[b].z, uv.z, acc[t]);
-                        acc[t] = fmaf(rv[b].w, uv.w, acc[t]);
-                    }
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < kMaxQ; t++) acc[t] = warp_sum(acc[t]);
-    if (lane == 0)
-        for (int t = 0; t < q; t++) part[warp * kMaxQ + t] = acc[t];
-    __syncthreads();
-    if (threadIdx.x < 2 * q) {
-        int el = threadIdx.x / q, t = threadIdx.x % q;
-        int ee = blockIdx.x * 2 + el;
-        if (ee < E) {
-            float s = part[(el * 4) * kMaxQ + t];
-            for (int sl = 1; sl < 4; sl++) s += part[(el * 4 + sl) * kMaxQ + t];
-            logits[(size_t)t * E + ee] = s;
-        }
-    }
-}
-
 // ------------------------------------------------------------------ top-k + union
 
 // Warp-level top-k of lg[0..E) (descending, ties to the lower index), with sigmoid weights
@@ -246,7 +136,7 @@ __device__ void warp_topk_n(const float* lg, int E, int k, int32_t* idx, float* 
     const int lane = threadIdx.x & 31;
     float v[NM];
 #pragma unroll
-    for (int m = 0; m < NM; m++) v[m] = lane + 32 * m < E ? lg[lane + 32 * m] : 0.0f;
+    for (int m = 0; m < NM; m++) v[m] = lane + 32 * m < E ? __ldcg(lg + lane + 32 * m) : 0.0f;
     uint32_t taken = 0;  // bit m: element lane + 32 m already selected
     float sig[kMaxK];
     for (int r = 0; r < k; r++) {
@@ -330,53 +220,271 @@ __global__ void k_topk(const float* __restrict__ logits, int E, int q, int k, in
     if (threadIdx.x == 0) *n_uni = r.n_uni;
 }
 
+// ------------------------------------------------------------------ K1: router logits
+
+// Computes the layer input u (bfloat16, in shared memory) and logits[t][e] for this CTA's 2 experts.
+// MODE 0: input x is bfloat16. MODE 1: input is the residual r; u = RN_bf16(r / rms(r)) in one pass
+// over r held in registers (q * H / 4 <= kRouterV * kRouterThreads float4 groups), and CTA 0
+// publishes u (for the gate/up kernel) and r (the trace). 16 warps per expert, each a sixteenth of
+// H; the slice sums are added in order. With k > 0, the last CTA to finish routes every token (top-k,
+// weights, union) and publishes the routing for the gate/up and down kernels.
+constexpr int kRouterThreads = 1024;
+constexpr int kRouterV = 5;  // q * H <= 20480: H <= 5120 at q = 4
+
+struct RouterArgs {
+    const float* R;
+    int E, H, q, k;  // k == 0: logits only
+    const uint16_t* xin;
+    const float* rin;
+    float* logits;
+    uint16_t* u_out;
+    float* r_trace;
+    int32_t* status_to_clear;
+    WsPtrs ws;  // routing outputs and the arrival counter (k > 0)
+    int32_t* idx_out;
+    float* w_out;
+    float* logits_out;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant__ RouterArgs A) {
+    const float* __restrict__ R = A.R;
+    const int E = A.E, H = A.H, q = A.q;
+    const uint16_t* __restrict__ xin = A.xin;
+    const float* __restrict__ rin = A.rin;
+    float* __restrict__ logits = A.logits;
+    uint16_t* __restrict__ u_out = A.u_out;
+    float* __restrict__ r_trace = A.r_trace;
+    int32_t* status_to_clear = A.status_to_clear;
+    extern __shared__ __align__(16) uint16_t u_s[];  // [q][H] bfloat16 bits
+    __shared__ float red[kRouterThreads / 32][kMaxQ];
+    __shared__ float inv_s[kMaxQ];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    // expert e = 2 * blockIdx + (warp / 16); warp slice of the row's H / 4 float4 groups. The first
+    // batch of router weights does not depend on the previous kernel: load it before waiting.
+    const int e = blockIdx.x * 2 + warp / 16, sl = warp % 16;
+    const int h4r = H / 4, g0 = h4r * sl / 16, g1 = h4r * (sl + 1) / 16;
+    const float4* row = reinterpret_cast<const float4*>(R + (size_t)(e < E ? e : 0) * H);
+    float4 pre[4];
+#pragma unroll
+    for (int b = 0; b < 4; b++) pre[b] = e < E && g0 + lane + 32 * b < g1 ? __ldg(row + g0 + lane + 32 * b) : make_float4(0.f, 0.f, 0.f, 0.f);
+    grid_dep_trigger();
+    grid_dep_wait();  // r and the workspace come from the previous kernel
+    if (status_to_clear && blockIdx.x == 0 && threadIdx.x == 0) *status_to_clear = 0;
+    const int n4 = q * H / 4;  // groups of 4 consecutive elements (H % 16 == 0: never across tokens)
+    if (MODE == 0) {
+        for (int i = threadIdx.x; i < n4; i += blockDim.x) reinterpret_cast<uint2*>(u_s)[i] = reinterpret_cast<const uint2*>(xin)[i];
+    } else {
+        const float4* r4 = reinterpret_cast<const float4*>(rin);
+        float4 rv[kRouterV];
+        float ss[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < kRouterV; i++) {
+            const int idx = threadIdx.x + i * kRouterThreads;
+            rv[i] = idx < n4 ? r4[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kRouterV; i++) {
+            const int idx = threadIdx.x + i * kRouterThreads;
+            if (idx < n4) {
+                const int t = idx * 4 / H;
+                float a = 0.f;
+                a = fmaf(rv[i].x, rv[i].x, a); a = fmaf(rv[i].y, rv[i].y, a);
+                a = fmaf(rv[i].z, rv[i].z, a); a = fmaf(rv[i].w, rv[i].w, a);
+#pragma unroll
+                for (int tt = 0; tt < kMaxQ; tt++) ss[tt] += tt == t ? a : 0.f;
+            }
+        }
+#pragma unroll
+        for (int tt = 0; tt < kMaxQ; tt++) ss[tt] = warp_sum(ss[tt]);
+        if (lane == 0)
+#pragma unroll
+            for (int tt = 0; tt < kMaxQ; tt++) red[warp][tt] = ss[tt];
+        __syncthreads();
+        if (threadIdx.x < kMaxQ) {
+            float s = 0.f;
+            for (int w = 0; w < kRouterThreads / 32; w++) s += red[w][threadIdx.x];
+            inv_s[threadIdx.x] = 1.0f / sqrtf(s / (float)H + 1e-6f);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kRouterV; i++) {
+            const int idx = threadIdx.x + i * kRouterThreads;
+            if (idx < n4) {
+                const float iv = inv_s[idx * 4 / H];
+                const uint32_t b0 = __bfloat16_as_ushort(__float2bfloat16_rn(rv[i].x * iv));
+                const uint32_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(rv[i].y * iv));
+                const uint32_t b2 = __bfloat16_as_ushort(__float2bfloat16_rn(rv[i].z * iv));
+                const uint32_t b3 = __bfloat16_as_ushort(__float2bfloat16_rn(rv[i].w * iv));
+                const uint2 pk = make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
+                reinterpret_cast<uint2*>(u_s)[idx] = pk;
+                if (blockIdx.x == 0) {
+                    reinterpret_cast<uint2*>(u_out)[idx] = pk;
+                    if (r_trace) reinterpret_cast<float4*>(r_trace)[idx] = rv[i];
+                }
+            }
+        }
+    }
+    __syncthreads();
+    float acc[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
+    if (e < E) {
+        for (int base = g0 + lane; base < g1; base += 4 * 32) {
+            float4 rv[4];
+#pragma unroll
+            for (int b = 0; b < 4; b++)
+                rv[b] = base == g0 + lane ? pre[b] : base + 32 * b < g1 ? __ldg(row + base + 32 * b) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int b = 0; b < 4; b++) {
+                const int h4 = base + 32 * b;
+                if (h4 >= g1) break;
+#pragma unroll
+                for (int t = 0; t < kMaxQ; t++) {
+                    if (t < q) {
+                        const uint2 ub = reinterpret_cast<const uint2*>(u_s + (size_t)t * H)[h4];
+                        acc[t] = fmaf(rv[b].x, __uint_as_float(ub.x << 16), acc[t]);
+                        acc[t] = fmaf(rv[b].y, __uint_as_float(ub.x & 0xFFFF0000u), acc[t]);
+                        acc[t] = fmaf(rv[b].z, __uint_as_float(ub.y << 16), acc[t]);
+                        acc[t] = fmaf(rv[b].w, __uint_as_float(ub.y & 0xFFFF0000u), acc[t]);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kMaxQ; t++) acc[t] = warp_sum(acc[t]);
+    if (lane == 0)
+        for (int t = 0; t < q; t++) red[warp][t] = acc[t];
+    __syncthreads();
+    if (threadIdx.x < 2 * q) {
+        const int el = threadIdx.x / q, t = threadIdx.x % q;
+        const int ee = blockIdx.x * 2 + el;
+        if (ee < E) {
+            float s = red[el * 16][t];
+            for (int w = 1; w < 16; w++) s += red[el * 16 + w][t];
+            logits[(size_t)t * E + ee] = s;
+        }
+    }
+    if (A.k == 0) return;
+    // the last CTA to finish routes every token (one thread publishes the CTA's logits: the barrier
+    // orders them before its fence and atomic)
+    __shared__ Route rt;
+    __shared__ int last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        last = atomicAdd(A.ws.nuni + 1, 1) == (int)gridDim.x - 1;
+        __threadfence();
+    }
+    __syncthreads();
+    if (!last) return;  // CTA-uniform
+    const int k = A.k;
+    if (warp < q) warp_topk(logits + (size_t)warp * E, E, k, rt.idx + warp * k, rt.w + warp * k);
+    build_union(rt, q, k, E);
+    for (int i = threadIdx.x; i < q * k; i += blockDim.x) {
+        A.ws.idx[i] = rt.idx[i];
+        A.ws.w[i] = rt.w[i];
+        A.ws.uni[i] = i < rt.n_uni ? rt.uni[i] : -1;
+        if (A.idx_out) A.idx_out[i] = rt.idx[i];
+        if (A.w_out) A.w_out[i] = rt.w[i];
+    }
+    if (A.logits_out)
+        for (int i = threadIdx.x; i < q * E; i += blockDim.x) A.logits_out[i] = __ldcg(logits + i);
+    if (threadIdx.x == 0) {
+        A.ws.nuni[0] = rt.n_uni;
+        A.ws.nuni[1] = 0;  // ready for the next call
+    }
+}
+
+// ------------------------------------------------------------------ routing state
+
+// Loads the routing the router kernel published (whole CTA; ends with __syncthreads()).
+__device__ inline void load_route(Route& r, const WsPtrs& ws, int qk) {
+    if (threadIdx.x == 0) r.n_uni = __ldcg(ws.nuni);
+    for (int i = threadIdx.x; i < qk; i += blockDim.x) {
+        r.idx[i] = __ldcg(ws.idx + i);
+        r.w[i] = __ldcg(ws.w + i);
+        r.uni[i] = __ldcg(ws.uni + i);
+    }
+    __syncthreads();
+}
+
+// Position in a CTA's (task, stage) sequence.
+struct Cursor {
+    int task, stage;
+};
+
+// CTA task range [c0, c1) over nA tasks of cost cA followed by nB tasks of cost cB: task t goes to
+// the CTA whose share of the total cost contains the cost before t, so CTAs get about equal work.
+__device__ __forceinline__ int cost_split(int64_t nA, int64_t cA, int64_t nB, int64_t cB, int64_t b, int64_t G) {
+    const int64_t tot = nA * cA + nB * cB, target = tot * b;  // first t with prefix(t) * G >= target
+    if (target <= nA * cA * G) return (int)((target + G * cA - 1) / (G * cA));
+    return (int)(nA + (target - nA * cA * G + G * cB - 1) / (G * cB));
+}
+
+__device__ __forceinline__ void task_range(int nA, int cA, int nB, int cB, int& c0, int& c1) {
+    c0 = cost_split(nA, cA, nB, cB, blockIdx.x, gridDim.x);
+    c1 = cost_split(nA, cA, nB, cB, blockIdx.x + 1, gridDim.x);
+}
+
+// Relative cost of a stage: bytes streamed, FP4 boxes weighted by 4/3 (their decode costs more per
+// byte).
+constexpr int kCostFP2 = stage_bytes(2), kCostFP3 = stage_bytes(3), kCostFP4 = stage_bytes(4) * 4 / 3;
+
+// Number of K halves a routed task is split into (1 when the row does not split into whole boxes).
+__device__ __forceinline__ int k_split(int K, int fmt) { return (K / stage_k(fmt)) % 2 == 0 ? 2 : 1; }
+
 // ------------------------------------------------------------------ K2: gate/up
 
-// Task = (output matrix, row block): the union's gate and up matrices (FP2, 256-row blocks of I,
-// H/256 stages each), then the shared expert's gate and up (FP4, 128-row blocks, 2 * H/512 stages:
-// the two 64-row halves alternate).
-// Matrix m = 2 * item + (0 gate | 1 up), the shared expert being item n_uni. Each CTA owns a
-// contiguous task range; its producer thread streams the range's boxes through the CTA ring and all
-// eight consumer warps decode every box. Outputs g and u (binary32) go to ws.gu[m][token][row]; the
-// down kernel forms h = silu(g) u while building its activation table.
+// Task = (output matrix, row block, K part): the union's gate and up matrices (FP2, 256-row blocks of
+// I, each split into ks K parts of H/256/ks stages), then the shared expert's gate and up (FP4,
+// 64-row blocks, H/512 stages). Matrix m = 2 * item + (0 gate | 1 up), the shared expert being item
+// n_uni. Each CTA owns a contiguous task range of about equal cost; its producer thread streams the
+// range's boxes through the CTA ring and all consumer warps decode every box. Outputs g and u
+// (binary32) go to ws.gu[K part][m][token][row]; the down kernel adds the parts and forms
+// h = silu(g) u while building its activation table.
 struct GateUpArgs {
     LayerMaps m;
     int q, k;
     const uint16_t* x;  // layer input, bfloat16 [q][H]
     WsPtrs ws;
-    int32_t* idx_out;
-    float* w_out;
-    float* logits_out;
     uint32_t magic;  // kMagic, kept out of immediates (see decode_fp2)
 };
 
-// Ring geometry of the two layer kernels: 7 slots of one FP2 box, 5 slots of one FP3 box.
-using GuRing = CtaRing<7, stage_bytes(2)>;
-using DnRing = CtaRing<5, stage_bytes(3)>;
+// Ring geometry of the two layer kernels: 7 slots of one FP2 box, 5 slots of one FP3 box (an FP4
+// box, 17 KB, fits either).
+constexpr int kGuNS = 7, kDnNS = 5;
+using GuRing = CtaRing<kGuNS, stage_bytes(2)>;
+using DnRing = CtaRing<kDnNS, stage_bytes(3)>;
+static_assert(stage_bytes(4) <= stage_bytes(2), "FP4 box fits a slot");
 
 struct GuTask {
     int mat;    // output matrix index
     int fp4;    // shared expert (FP4) task
     int row0;   // first output row
     int grow0;  // first row in the stacked tensor map
+    int kpart;  // K part
+    int ns;     // stages
 };
 
-__device__ __forceinline__ int gu_tasks(int n_uni, int I) { return 2 * n_uni * (I / 256) + 2 * (I / 128); }
-
-__device__ __forceinline__ GuTask gu_task(int t, const Route& r, int I) {
-    const int rb2 = I / 256, n2 = 2 * r.n_uni * rb2;
+__device__ __forceinline__ GuTask gu_task(int t, const Route& r, int H, int I, int ks) {
+    const int rb2 = I / 256, n2 = 2 * r.n_uni * rb2 * ks;
     GuTask k;
     if (t < n2) {
-        k.mat = t / rb2;
+        const int rem = t % (rb2 * ks);
+        k.mat = t / (rb2 * ks);
         k.fp4 = 0;
-        k.row0 = (t % rb2) * 256;
+        k.row0 = (rem / ks) * 256;
+        k.kpart = rem % ks;
         k.grow0 = r.uni[k.mat >> 1] * I + k.row0;
+        k.ns = H / stage_k(2) / ks;
     } else {
-        const int t4 = t - n2, rb4 = I / 128;
+        const int t4 = t - n2, rb4 = I / 64;
         k.mat = 2 * r.n_uni + t4 / rb4;
         k.fp4 = 1;
-        k.row0 = (t4 % rb4) * 128;
+        k.row0 = (t4 % rb4) * 64;
+        k.kpart = 0;
         k.grow0 = k.row0;
+        k.ns = H / stage_k(4);
     }
     return k;
 }
@@ -384,22 +492,11 @@ __device__ __forceinline__ GuTask gu_task(int t, const Route& r, int I) {
 __device__ __forceinline__ void gu_issue(const GateUpArgs& A, const GuTask& k, int s, uint8_t* slot, uint64_t* bar) {
     if (!k.fp4) {
         mbar_expect_tx(bar, stage_bytes(2));
-        tma_load_2d(slot, (k.mat & 1) ? &A.m.up : &A.m.gate, s * box_bytes(2), k.grow0, bar);
+        tma_load_2d(slot, (k.mat & 1) ? &A.m.up : &A.m.gate, (k.kpart * k.ns + s) * box_bytes(2), k.grow0, bar);
     } else {
         mbar_expect_tx(bar, stage_bytes(4));
-        tma_load_2d(slot, (k.mat & 1) ? &A.m.sh_up : &A.m.sh_gate, (s >> 1) * (box_bytes(4) / 2), k.grow0 + 64 * (s & 1), bar);
+        tma_load_2d(slot, (k.mat & 1) ? &A.m.sh_up : &A.m.sh_gate, s * (box_bytes(4) / 2), k.grow0, bar);
     }
-}
-
-// Producer-side walk over a CTA's (task, stage) sequence.
-struct StageCursor {
-    int task, stage;
-    uint32_t issued;
-};
-
-// Stages of a task: FP2/FP3 tasks stream one box per stage_k columns, FP4 tasks two (row halves).
-__device__ __forceinline__ int task_stages(int fp4, int fmt_other, int K) {
-    return fp4 ? 2 * (K / stage_k(4)) : K / stage_k(fmt_other);
 }
 
 template <int Q>
@@ -407,87 +504,69 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ Route r;
     __shared__ int shift[kMaxQ];
-    __shared__ float red4[(kWarps + 1) * 4];
+    __shared__ float red4[kWarps * 4];
     const int H = A.m.H, I = A.m.I;
     const CtaSmem S = cta_carve(smem, btab_bytes(H));
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const GuRing R = cta_init<7, stage_bytes(2)>(S);
+    const GuRing R = cta_init<kGuNS, stage_bytes(2)>(S);
+    grid_dep_wait();  // routing and u come from the router kernel
+    grid_dep_trigger();  // after the wait: the down kernel reads the router's output before its own
+    load_route(r, A.ws, Q * A.k);
 
-    // routing (every CTA), published by CTA 0
-    if (warp < Q) warp_topk(A.ws.logits + (size_t)warp * A.m.E, A.m.E, A.k, r.idx + warp * A.k, r.w + warp * A.k);
-    build_union(r, Q, A.k, A.m.E);
-    if (blockIdx.x == 0) {
-        for (int i = threadIdx.x; i < Q * A.k; i += blockDim.x) {
-            A.ws.idx[i] = r.idx[i];
-            A.ws.w[i] = r.w[i];
-            A.ws.uni[i] = i < r.n_uni ? r.uni[i] : -1;
-            if (A.idx_out) A.idx_out[i] = r.idx[i];
-            if (A.w_out) A.w_out[i] = r.w[i];
-        }
-        if (A.logits_out)
-            for (int i = threadIdx.x; i < Q * A.m.E; i += blockDim.x) A.logits_out[i] = A.ws.logits[i];
-        if (threadIdx.x == 0) *A.ws.nuni = r.n_uni;
-    }
+    const int ks = k_split(H, 2);
+    int c0, c1;
+    task_range(2 * r.n_uni * (I / 256) * ks, (H / stage_k(2) / ks) * kCostFP2, 2 * (I / 64), (H / stage_k(4)) * kCostFP4, c0, c1);
 
-    const int total = gu_tasks(r.n_uni, I);
-    const int c0 = (int)((int64_t)total * blockIdx.x / gridDim.x), c1 = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
-    const bool producer = threadIdx.x == kWarps * 32;
-    StageCursor pc{c0, 0, 0u};
-    auto issue_next = [&]() {
-        const GuTask k = gu_task(pc.task, r, I);
-        gu_issue(A, k, pc.stage, R.slot(pc.issued), R.full + pc.issued % 7);
-        pc.issued++;
-        if (++pc.stage == task_stages(k.fp4, 2, H)) { pc.stage = 0; pc.task++; }
-    };
-    // fill the ring before building the activation tables, so the first loads overlap it
-    if (producer)
-        while (pc.task < c1 && pc.issued < 7u) issue_next();
-
-    // activation tables: x scaled per token, FP2 (pair-shifted, with block offsets) and FP4
-    build_tables<2, 4>(SrcBF16{A.x}, H, Q, S.tab[0], S.tab[1], S.csum, shift, red4);
-    __syncthreads();
-
-    if (warp == kWarps) {
-        if (producer) {
-            while (pc.task < c1) {
-                if (!R.acquire(pc.issued)) { flag(A.ws.status, FPX_ETIMEOUT); break; }
-                issue_next();
+    if (warp == kWarps) {  // producer: streams the range's boxes while the consumers build tables
+        if (lane == 0) {
+            uint32_t issued = 0;
+            for (int tk = c0; tk < c1; tk++) {
+                const GuTask k = gu_task(tk, r, H, I, ks);
+                for (int s = 0; s < k.ns; s++, issued++) {
+                    if (!R.acquire(issued)) { flag(A.ws.status, FPX_ETIMEOUT); tk = c1; break; }
+                    gu_issue(A, k, s, R.slot(issued), R.bar(issued));
+                }
             }
-            R.drain(pc.issued);
+            R.drain(issued);
         }
         return;
     }
 
+    // activation tables: x scaled per token, FP2 (pair-shifted, with block offsets) and FP4
+    build_tables<2, 4, true>(SrcBF16{A.x}, H, Q, S.tab[0], S.tab[1], S.csum, shift, red4);
+    consumers_sync();
+
+    // Every consumer warp runs the same sequence of consumer barriers whether or not a wait timed
+    // out, so a timeout never leaves a barrier short of arrivals.
     const int a_idx = b_active_index(lane);
     const uint32_t magic = A.magic;
     uint32_t n = 0, bad = 0;
     bool ok = true;
     for (int tk = c0; tk < c1; tk++) {
-        const GuTask k = gu_task(tk, r, I);
+        const GuTask k = gu_task(tk, r, H, I, ks);
         float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        const int ns = task_stages(k.fp4, 2, H);
-        for (int s = 0; s < ns; s++, n++) {
+        for (int s = 0; s < k.ns; s++, n++) {
             if (ok) ok = R.wait(n, A.ws.status);
             if (!ok) continue;  // the producer gives up too once this warp stops releasing
             const uint8_t* slot = R.slot(n);
             if (!k.fp4) {
-                const int ch0 = s * box_chunks(2);
+                const int ch0 = (k.kpart * k.ns + s) * box_chunks(2);
                 box_tiles<2, 2, box_chunks(2)>(slot + (warp * 32 + g) * box_bytes(2), lane_tab(S.tab[0], S.zero, a_idx, ch0),
                                                lane_csum(S.csum, ch0, t), t, magic, y, bad);
-            } else if ((s & 1) == (warp >> 2)) {
-                const int ch0 = (s >> 1) * box_chunks(4);
-                box_tiles<4, 1, box_chunks(4)>(slot + ((warp & 3) * 16 + g) * box_bytes(4),
-                                               lane_tab(S.tab[1], S.zero, a_idx, ch0), nullptr, t, magic,
-                                               *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
+            } else {
+                const int ch0 = s * box_chunks(4) + 4 * (warp >> 2);
+                box_tiles<4, 1, 4>(slot + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4),
+                                   lane_tab(S.tab[1], S.zero, a_idx, ch0), nullptr, t, magic,
+                                   *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
             }
             R.release(n);
         }
-        if (!ok) continue;
         pair_reduce(y[0]);
         pair_reduce(y[1]);
-        if (t < 2) {
-            const int rb = k.row0 + (k.fp4 ? 64 * (warp >> 2) + 16 * (warp & 3) : 32 * warp) + g;
-            float* out = A.ws.gu + (size_t)k.mat * Q * I;
+        if (k.fp4) fp4_reduce(S.red, y[0]);  // the same tasks run on every consumer warp
+        if (ok && t < 2 && (!k.fp4 || warp < 4)) {
+            const int rb = k.row0 + (k.fp4 ? 16 : 32) * warp + g;
+            float* out = A.ws.gu + k.kpart * A.ws.gu_half + (size_t)k.mat * Q * I;
 #pragma unroll
             for (int i = 0; i < 4; i++) {
                 const int tok = 2 * t + (i & 1), rr = rb + 8 * (i >> 1);
@@ -505,13 +584,11 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
 
 // ------------------------------------------------------------------ K3: down + combine
 
-// Task = (item, row block of H): the union's down matrices (FP3, 256-row blocks, I/256 stages each),
-// then the shared expert's (FP4, 128-row blocks, 2 * I/512 stages: the two 64-row halves alternate). Each CTA owns a contiguous task range,
-// which spans at most two items (the grid has at least kMinDownCtas CTAs); it builds their
-// activation tables from h = silu(g) u at start. Every 128-row group of the output has a counter;
-// after a task's rows are in ws.yi, the task adds one to each group it covers, and the CTA that
-// brings a group's count to n_uni + 1 combines the group for every token: selected experts in
-// ascending expert order, then the shared expert.
+// Task = (item, row block of H, K part): the union's down matrices (FP3, 256-row blocks, each split
+// into ks K parts of I/256/ks stages), then the shared expert's (FP4, 64-row blocks, I/512 stages).
+// Each CTA owns a contiguous task range of about equal cost, which spans at most two items (the grid
+// has at least kMinDownCtas CTAs); it builds their activation tables from h = silu(g) u at start.
+// Outputs go to ws.yi[K part][item][token][row]; k_combine adds them up.
 constexpr int kMinDownCtas = 2 * (kMaxQ * kMaxK + 1);
 
 struct DownArgs {
@@ -523,24 +600,27 @@ struct DownArgs {
 };
 
 struct DnTask {
-    int item, fp4, row0, grow0;
+    int item, fp4, row0, grow0, kpart, ns;
 };
 
-__device__ __forceinline__ int dn_tasks(int n_uni, int H) { return n_uni * (H / 256) + H / 128; }
-
-__device__ __forceinline__ DnTask dn_task(int t, const Route& r, int H) {
-    const int rb3 = H / 256, n3 = r.n_uni * rb3;
+__device__ __forceinline__ DnTask dn_task(int t, const Route& r, int H, int I, int ks) {
+    const int rb3 = H / 256, n3 = r.n_uni * rb3 * ks;
     DnTask k;
     if (t < n3) {
-        k.item = t / rb3;
+        const int rem = t % (rb3 * ks);
+        k.item = t / (rb3 * ks);
         k.fp4 = 0;
-        k.row0 = (t % rb3) * 256;
+        k.row0 = (rem / ks) * 256;
+        k.kpart = rem % ks;
         k.grow0 = r.uni[k.item] * H + k.row0;
+        k.ns = I / stage_k(3) / ks;
     } else {
         k.item = r.n_uni;
         k.fp4 = 1;
-        k.row0 = (t - n3) * 128;
+        k.row0 = (t - n3) * 64;
+        k.kpart = 0;
         k.grow0 = k.row0;
+        k.ns = I / stage_k(4);
     }
     return k;
 }
@@ -548,10 +628,10 @@ __device__ __forceinline__ DnTask dn_task(int t, const Route& r, int H) {
 __device__ __forceinline__ void dn_issue(const DownArgs& A, const DnTask& k, int s, uint8_t* slot, uint64_t* bar) {
     if (!k.fp4) {
         mbar_expect_tx(bar, stage_bytes(3));
-        tma_load_2d(slot, &A.m.down, s * box_bytes(3), k.grow0, bar);
+        tma_load_2d(slot, &A.m.down, (k.kpart * k.ns + s) * box_bytes(3), k.grow0, bar);
     } else {
         mbar_expect_tx(bar, stage_bytes(4));
-        tma_load_2d(slot, &A.m.sh_down, (s >> 1) * (box_bytes(4) / 2), k.grow0 + 64 * (s & 1), bar);
+        tma_load_2d(slot, &A.m.sh_down, s * (box_bytes(4) / 2), k.grow0, bar);
     }
 }
 
@@ -559,18 +639,123 @@ template <int Q, int MODE>
 __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__ DownArgs A) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ Route r;
-    __shared__ float wsel[kMaxQ * kMaxK + 1][kMaxQ];  // weight of token t for union item j, NaN if unselected
     __shared__ int shift[2][kMaxQ];
-    __shared__ float red4[(kWarps + 1) * 4];
-    __shared__ int last_grp[2];
+    __shared__ float red4[kWarps * 4];
     const int H = A.m.H, I = A.m.I;
     const CtaSmem S = cta_carve(smem, btab_bytes(I));
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const DnRing R = cta_init<5, stage_bytes(3)>(S);
+    const DnRing R = cta_init<kDnNS, stage_bytes(3)>(S);
+    // the routing comes from the router kernel, which completed before the gate/up kernel passed its
+    // own grid_dep_wait(); the weights do not depend on the gate/up kernel either, so the producer
+    // starts streaming before grid_dep_wait()
+    grid_dep_trigger();
+    load_route(r, A.ws, Q * A.k);
 
-    if (threadIdx.x == 0) r.n_uni = *A.ws.nuni;
-    for (int i = threadIdx.x; i < Q * A.k; i += blockDim.x) { r.idx[i] = A.ws.idx[i]; r.w[i] = A.ws.w[i]; r.uni[i] = A.ws.uni[i]; }
-    __syncthreads();
+    const int ks = k_split(I, 3);
+    int c0, c1;
+    task_range(r.n_uni * (H / 256) * ks, (I / stage_k(3) / ks) * kCostFP3, H / 64, (I / stage_k(4)) * kCostFP4, c0, c1);
+    if (c0 >= c1) return;  // CTA-uniform: nothing to do
+    const int item_lo = dn_task(c0, r, H, I, ks).item, item_hi = dn_task(c1 - 1, r, H, I, ks).item;
+    if (item_hi - item_lo > 1) {  // too small a grid (the host launches at least kMinDownCtas CTAs)
+        if (threadIdx.x == 0) flag(A.ws.status, FPX_EINVAL);
+        return;
+    }
+
+    if (warp == kWarps) {  // producer: streams the range's boxes while the consumers build tables
+        if (lane == 0) {
+            uint32_t issued = 0;
+            for (int tk = c0; tk < c1; tk++) {
+                const DnTask k = dn_task(tk, r, H, I, ks);
+                for (int s = 0; s < k.ns; s++, issued++) {
+                    if (!R.acquire(issued)) { flag(A.ws.status, FPX_ETIMEOUT); tk = c1; break; }
+                    dn_issue(A, k, s, R.slot(issued), R.bar(issued));
+                }
+            }
+            R.drain(issued);
+        }
+        return;
+    }
+
+    // activation tables for the (at most two) items of this CTA's range: h = silu(g) u, the K parts
+    // of g and u added first (the shared expert has one part)
+    grid_dep_wait();
+    for (int sl = 0; sl <= item_hi - item_lo; sl++) {
+        const int item = item_lo + sl;
+        const size_t part2 = item < r.n_uni && k_split(H, 2) == 2 ? A.ws.gu_half : 0;
+        const SrcSilu src{A.ws.gu + (size_t)(2 * item) * Q * I, A.ws.gu + (size_t)(2 * item + 1) * Q * I, part2};
+        uint2* tab = sl ? S.tab[1] : S.tab[0];
+        if (item == r.n_uni) build_tables<4, 0, true>(src, I, Q, tab, nullptr, nullptr, shift[sl], red4);
+        else build_tables<3, 0, true>(src, I, Q, tab, nullptr, nullptr, shift[sl], red4);
+        consumers_sync();
+    }
+
+    // Every consumer warp runs the same sequence of consumer barriers whether or not a wait timed
+    // out, so a timeout never leaves a barrier short of arrivals.
+    const int a_idx = b_active_index(lane);
+    const uint32_t magic = A.magic;
+    uint32_t n = 0, bad = 0;
+    bool ok = true;
+    for (int tk = c0; tk < c1; tk++) {
+        const DnTask k = dn_task(tk, r, H, I, ks);
+        const int sl = k.item - item_lo;
+        const uint2* tab = sl ? S.tab[1] : S.tab[0];
+        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int s = 0; s < k.ns; s++, n++) {
+            if (ok) ok = R.wait(n, A.ws.status);
+            if (!ok) continue;
+            const uint8_t* slot = R.slot(n);
+            if (!k.fp4) {
+                const int ch0 = (k.kpart * k.ns + s) * box_chunks(3);
+                box_tiles<3, 2, box_chunks(3)>(slot + (warp * 32 + g) * box_bytes(3), lane_tab(tab, S.zero, a_idx, ch0), nullptr,
+                                               t, magic, y, bad);
+            } else {
+                const int ch0 = s * box_chunks(4) + 4 * (warp >> 2);
+                box_tiles<4, 1, 4>(slot + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4),
+                                   lane_tab(tab, S.zero, a_idx, ch0), nullptr, t, magic,
+                                   *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
+            }
+            R.release(n);
+        }
+        pair_reduce(y[0]);
+        pair_reduce(y[1]);
+        if (k.fp4) fp4_reduce(S.red, y[0]);
+        if (ok && t < 2 && (!k.fp4 || warp < 4)) {
+            const int rb = k.row0 + (k.fp4 ? 16 : 32) * warp + g;
+            float* out = A.ws.yi + k.kpart * A.ws.yi_half + (size_t)k.item * Q * H;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int tok = 2 * t + (i & 1), rr = rb + 8 * (i >> 1);
+                if (tok < Q) {
+                    const float sc = exp2i((k.fp4 ? 14 : 0) - shift[sl][tok]);
+                    out[(size_t)tok * H + rr] = y[0][i] * sc;
+                    if (!k.fp4) out[(size_t)tok * H + rr + 16] = y[1][i] * sc;
+                }
+            }
+        }
+    }
+    report_bad(bad, A.ws.status);
+}
+
+// ------------------------------------------------------------------ K4: combine
+
+// out[t][h] (MODE 0) or r[t][h] += (MODE 1) sum over token t's selected experts, in ascending expert
+// order, of w * y_e[t][h] (K parts added first), then the shared expert's y[t][h]. One thread per
+// output; consecutive threads take consecutive rows.
+struct CombineArgs {
+    int H, k;
+    WsPtrs ws;
+    int ks;      // K parts of the routed down outputs
+    float* out;  // MODE 0: y [q][H]; MODE 1: residual r [q][H], updated in place
+};
+
+constexpr int kCombineThreads = 256;
+
+template <int Q, int MODE>
+__global__ void __launch_bounds__(kCombineThreads) k_combine(const __grid_constant__ CombineArgs A) {
+    __shared__ Route r;
+    __shared__ float wsel[kMaxQ * kMaxK + 1][kMaxQ];  // weight of token t for union item j, NaN if unselected
+    grid_dep_trigger();
+    load_route(r, A.ws, Q * A.k);  // from the router kernel (completed two launches ago)
     for (int i = threadIdx.x; i < r.n_uni * Q; i += blockDim.x) {
         const int j = i / Q, tok = i % Q;
         float wv = __int_as_float(0x7fc00000);
@@ -578,138 +763,41 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
             if (r.idx[tok * A.k + rr] == r.uni[j]) wv = r.w[tok * A.k + rr];
         wsel[j][tok] = wv;
     }
-
-    const int total = dn_tasks(r.n_uni, H);
-    const int c0 = (int)((int64_t)total * blockIdx.x / gridDim.x), c1 = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
-    if (c0 >= c1) return;  // CTA-uniform: nothing to do
-    const int item_lo = dn_task(c0, r, H).item, item_hi = dn_task(c1 - 1, r, H).item;
-    if (item_hi - item_lo > 1) {  // too small a grid (the host launches at least kMinDownCtas CTAs)
-        if (threadIdx.x == 0) flag(A.ws.status, FPX_EINVAL);
-        return;
-    }
-
-    const bool producer = threadIdx.x == kWarps * 32;
-    StageCursor pc{c0, 0, 0u};
-    auto issue_next = [&]() {
-        const DnTask k = dn_task(pc.task, r, H);
-        dn_issue(A, k, pc.stage, R.slot(pc.issued), R.full + pc.issued % 5);
-        pc.issued++;
-        if (++pc.stage == task_stages(k.fp4, 3, I)) { pc.stage = 0; pc.task++; }
-    };
-    if (producer)
-        while (pc.task < c1 && pc.issued < 5u) issue_next();
-
-    // activation tables for the (at most two) items of this CTA's range: h = silu(g) u
-    for (int sl = 0; sl <= item_hi - item_lo; sl++) {
-        const int item = item_lo + sl;
-        const SrcSilu src{A.ws.gu + (size_t)(2 * item) * Q * I, A.ws.gu + (size_t)(2 * item + 1) * Q * I};
-        uint2* tab = sl ? S.tab[1] : S.tab[0];
-        if (item == r.n_uni) build_tables<4, 0>(src, I, Q, tab, nullptr, nullptr, shift[sl], red4);
-        else build_tables<3, 0>(src, I, Q, tab, nullptr, nullptr, shift[sl], red4);
-        __syncthreads();
-    }
-
-    if (warp == kWarps) {
-        if (producer) {
-            while (pc.task < c1) {
-                if (!R.acquire(pc.issued)) { flag(A.ws.status, FPX_ETIMEOUT); break; }
-                issue_next();
-            }
-            R.drain(pc.issued);
-        }
-        return;
-    }
-
-    // Consumers. Every consumer warp runs the same sequence of consumers_sync() whether or not a wait
-    // timed out, so a timeout never leaves a barrier short of arrivals.
-    const int a_idx = b_active_index(lane);
-    const uint32_t magic = A.magic;
-    uint32_t n = 0, bad = 0;
-    bool ok = true;
-    for (int tk = c0; tk < c1; tk++) {
-        const DnTask k = dn_task(tk, r, H);
-        const int sl = k.item - item_lo;
-        const uint2* tab = sl ? S.tab[1] : S.tab[0];
-        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        const int ns = task_stages(k.fp4, 3, I);
-        for (int s = 0; s < ns; s++, n++) {
-            if (ok) ok = R.wait(n, A.ws.status);
-            if (!ok) continue;
-            const uint8_t* slot = R.slot(n);
-            if (!k.fp4) {
-                const int ch0 = s * box_chunks(3);
-                box_tiles<3, 2, box_chunks(3)>(slot + (warp * 32 + g) * box_bytes(3), lane_tab(tab, S.zero, a_idx, ch0), nullptr,
-                                               t, magic, y, bad);
-            } else if ((s & 1) == (warp >> 2)) {
-                const int ch0 = (s >> 1) * box_chunks(4);
-                box_tiles<4, 1, box_chunks(4)>(slot + ((warp & 3) * 16 + g) * box_bytes(4), lane_tab(tab, S.zero, a_idx, ch0),
-                                               nullptr, t, magic, *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
-            }
-            R.release(n);
-        }
-        if (ok) {
-            pair_reduce(y[0]);
-            pair_reduce(y[1]);
-            if (t < 2) {
-                const int rb = k.row0 + (k.fp4 ? 64 * (warp >> 2) + 16 * (warp & 3) : 32 * warp) + g;
-                float* out = A.ws.yi + (size_t)k.item * Q * H;
+    __syncthreads();
+    grid_dep_wait();  // the down kernel's outputs
+    const int H = A.H;
+    const int o = blockIdx.x * kCombineThreads + threadIdx.x;
+    if (o >= Q * H) return;
+    const int tok = o / H, rr = o % H;
+    const float* col = A.ws.yi + (size_t)tok * H + rr;
+    const float* col2 = col + A.ws.yi_half;
+    const size_t istride = (size_t)Q * H;
+    // loads in batches of 8 (independent, in flight together), then the fixed-order sum; item n_uni
+    // is the shared expert, added last
+    float acc = 0.0f, ysh = 0.0f;
+    bool first = true;
+    for (int j0 = 0; j0 <= r.n_uni; j0 += 8) {
+        float yv[8];
 #pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    const int tok = 2 * t + (i & 1), rr = rb + 8 * (i >> 1);
-                    if (tok < Q) {
-                        const float sc = exp2i((k.fp4 ? 14 : 0) - shift[sl][tok]);
-                        out[(size_t)tok * H + rr] = y[0][i] * sc;
-                        if (!k.fp4) out[(size_t)tok * H + rr + 16] = y[1][i] * sc;
-                    }
-                }
-            }
-        }
-        // count this task into its 128-row groups; the last contributor combines a group (one thread
-        // publishes the CTA's writes: the barrier orders them before its fence and atomic)
-        consumers_sync();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            const int g0 = k.row0 / 128, ng = k.fp4 ? 1 : 2;
-            for (int j = 0; j < 2; j++) last_grp[j] = (j < ng && atomicAdd(A.ws.cnt + g0 + j, 1) == r.n_uni) ? g0 + j : -1;
-            __threadfence();
-        }
-        consumers_sync();
-        for (int j = 0; j < 2; j++) {
-            const int gi = last_grp[j];
-            if (gi < 0) continue;
-            for (int o = threadIdx.x; o < 128 * Q; o += kWarps * 32) {
-                const int rr = gi * 128 + o / Q, tok = o % Q;
-                // loads in batches of 8 (independent, in flight together), then the fixed-order sum;
-                // item n_uni is the shared expert, added last
-                const float* col = A.ws.yi + (size_t)tok * H + rr;
-                const size_t istride = (size_t)Q * H;
-                float acc = 0.0f, ysh = 0.0f;
-                bool first = true;
-                for (int j0 = 0; j0 <= r.n_uni; j0 += 8) {
-                    float yv[8];
+        for (int u = 0; u < 8; u++) yv[u] = j0 + u <= r.n_uni ? __ldcg(col + (size_t)(j0 + u) * istride) : 0.0f;
+        if (A.ks == 2)
 #pragma unroll
-                    for (int u = 0; u < 8; u++) yv[u] = j0 + u <= r.n_uni ? __ldcg(col + (size_t)(j0 + u) * istride) : 0.0f;
+            for (int u = 0; u < 8; u++)
+                if (j0 + u < r.n_uni) yv[u] += __ldcg(col2 + (size_t)(j0 + u) * istride);
 #pragma unroll
-                    for (int u = 0; u < 8; u++) {
-                        const int jj = j0 + u;
-                        if (jj == r.n_uni) ysh = yv[u];
-                        if (jj >= r.n_uni) continue;
-                        const float wv = wsel[jj][tok];
-                        if (wv != wv) continue;  // expert not selected by this token
-                        acc = first ? wv * yv[u] : fmaf(wv, yv[u], acc);
-                        first = false;
-                    }
-                }
-                acc += ysh;
-                const size_t oi = (size_t)tok * H + rr;
-                if (MODE == 0) A.out[oi] = acc;
-                else A.out[oi] = A.out[oi] + acc;
-            }
-            if (threadIdx.x == 0) A.ws.cnt[gi] = 0;  // ready for the next call
+        for (int u = 0; u < 8; u++) {
+            const int jj = j0 + u;
+            if (jj == r.n_uni) ysh = yv[u];
+            if (jj >= r.n_uni) continue;
+            const float wv = wsel[jj][tok];
+            if (wv != wv) continue;  // expert not selected by this token
+            acc = first ? wv * yv[u] : fmaf(wv, yv[u], acc);
+            first = false;
         }
-        consumers_sync();  // last_grp is rewritten by the next task
     }
-    report_bad(bad, A.ws.status);
+    acc += ysh;
+    if (MODE == 0) A.out[o] = acc;
+    else A.out[o] = A.out[o] + acc;
 }
 
 // ------------------------------------------------------------------ launch plumbing
@@ -720,12 +808,12 @@ int check_layer(const moe_layer* L) {
     if (!aligned(L->router, 16) || !aligned(L->gate, 16) || !aligned(L->up, 16) || !aligned(L->down, 16) ||
         !aligned(L->sh_gate, 16) || !aligned(L->sh_up, 16) || !aligned(L->sh_down, 16))
         return FPX_EALIGN;
-    if (cta_smem_bytes(btab_bytes(L->H > L->I ? L->H : L->I)) + 2048 > 227 * 1024) return FPX_EINVAL;  // + static
+    if (cta_smem_bytes(btab_bytes(L->H > L->I ? L->H : L->I)) + 2048 > 227 * 1024) return FPX_EINVAL;  // + static smem
     return FPX_OK;
 }
 
 struct Plan {
-    int g_router, g_gate, g_down;
+    int g_router, g_gate, g_down, g_comb;
     size_t sm_router, sm_gate, sm_down;
 };
 
@@ -733,18 +821,37 @@ Plan make_plan(const moe_layer& L, int q) {
     DeviceInfo di = device_info();
     Plan p{};
     p.g_router = (L.E + 1) / 2;
-    p.sm_router = sizeof(float) * ((size_t)q * L.H + 8 * kMaxQ + 8);
+    p.sm_router = sizeof(uint16_t) * (size_t)q * L.H;
     p.g_gate = di.sms;
     p.sm_gate = cta_smem_bytes(btab_bytes(L.H));
     p.g_down = di.sms > kMinDownCtas ? di.sms : kMinDownCtas;
     p.sm_down = cta_smem_bytes(btab_bytes(L.I));
+    p.g_comb = (q * L.H + kCombineThreads - 1) / kCombineThreads;
     return p;
+}
+
+// Launches kern<<<grid, block, smem, s>>>(args), as a programmatic dependent launch when pdl is set
+// (the kernel calls grid_dep_wait() before reading what the previous kernel wrote).
+template <typename Args>
+cudaError_t launch(void (*kern)(Args), int grid, int block, size_t smem, cudaStream_t s, bool pdl, const Args& args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
 template <int Q, int MODE>
 int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, const float* r, float* out,
                  int32_t* idx_out, float* w_out, float* logits_out, float* r_trace, WsPtrs ws, bool clear,
-                 cudaEvent_t const* ev, cudaStream_t s) {
+                 cudaEvent_t const* ev, bool pdl_first, cudaStream_t s) {
+    if (MODE == 1 && (size_t)Q * L.H > (size_t)4 * kRouterV * kRouterThreads) return FPX_EINVAL;  // router registers
     GateUpArgs ga{};
     DownArgs da{};
     int st = make_layer_maps(L, &ga.m);
@@ -754,34 +861,45 @@ int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, co
     ga.k = da.k = k;
     ga.x = MODE == 0 ? x : ws.u;
     ga.ws = da.ws = ws;
-    ga.idx_out = idx_out;
-    ga.w_out = w_out;
-    ga.logits_out = logits_out;
     ga.magic = da.magic = kMagic;
     da.out = out;
+    RouterArgs ra{};
+    ra.R = L.router;
+    ra.E = L.E; ra.H = L.H; ra.q = Q; ra.k = k;
+    ra.xin = x; ra.rin = r;
+    ra.logits = ws.logits; ra.u_out = ws.u; ra.r_trace = r_trace;
+    ra.status_to_clear = clear ? ws.status : nullptr;
+    ra.ws = ws;
+    ra.idx_out = idx_out; ra.w_out = w_out; ra.logits_out = logits_out;
     if (cudaFuncSetAttribute(k_router<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_router) ||
         cudaFuncSetAttribute(k_gate_up<Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_gate) ||
         cudaFuncSetAttribute(k_down<Q, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_down))
         return FPX_ECUDA;
+    CombineArgs ca{};
+    ca.H = L.H; ca.k = k; ca.ws = ws; ca.ks = (L.I / stage_k(3)) % 2 == 0 ? 2 : 1; ca.out = out;
+    // timing events between the kernels would break the dependent-launch edges: no overlap then
+    const bool pdl = ev == nullptr;
+    cudaError_t e = cudaSuccess;
     if (ev) cudaEventRecord(ev[0], s);
-    k_router<MODE><<<p.g_router, kThreads, p.sm_router, s>>>(L.router, L.E, L.H, Q, x, r, ws.logits, ws.u, r_trace,
-                                                             clear ? ws.status : nullptr);
+    e = e ? e : launch(k_router<MODE>, p.g_router, kRouterThreads, p.sm_router, s, pdl && pdl_first, ra);
     if (ev) cudaEventRecord(ev[1], s);
-    k_gate_up<Q><<<p.g_gate, kCtaThreads, p.sm_gate, s>>>(ga);
+    e = e ? e : launch(k_gate_up<Q>, p.g_gate, kCtaThreads, p.sm_gate, s, pdl, ga);
     if (ev) cudaEventRecord(ev[2], s);
-    k_down<Q, MODE><<<p.g_down, kCtaThreads, p.sm_down, s>>>(da);
-    return launch_status();
+    e = e ? e : launch(k_down<Q, MODE>, p.g_down, kCtaThreads, p.sm_down, s, pdl, da);
+    if (ev) cudaEventRecord(ev[3], s);
+    e = e ? e : launch(k_combine<Q, MODE>, p.g_comb, kCombineThreads, 0, s, pdl, ca);
+    return e == cudaSuccess ? launch_status() : FPX_ECUDA;
 }
 
 template <int MODE>
 int dispatch_q(int q, const moe_layer& L, const Plan& p, int k, const uint16_t* x, const float* r, float* out,
                int32_t* idx_out, float* w_out, float* logits_out, float* r_trace, WsPtrs ws, bool clear,
-               cudaEvent_t const* ev, cudaStream_t s) {
+               cudaEvent_t const* ev, bool pdl_first, cudaStream_t s) {
     switch (q) {
-        case 1: return launch_layer<1, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, s);
-        case 2: return launch_layer<2, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, s);
-        case 3: return launch_layer<3, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, s);
-        case 4: return launch_layer<4, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, s);
+        case 1: return launch_layer<1, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, pdl_first, s);
+        case 2: return launch_layer<2, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, pdl_first, s);
+        case 3: return launch_layer<3, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, pdl_first, s);
+        case 4: return launch_layer<4, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, pdl_first, s);
         default: return FPX_EINVAL;
     }
 }
@@ -796,9 +914,14 @@ int moe_route_topk(const float* R, int E, int H, const uint16_t* x, int q, int k
     if (!R || !x || !logits || !idx || !w || !uni || !n_uni) return FPX_EINVAL;
     if (!aligned(R, 16) || !aligned(x, 4) || !aligned(logits, 4)) return FPX_EALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    size_t sm = sizeof(float) * ((size_t)q * H + 8 * kMaxQ + 8);
+    const size_t sm = sizeof(uint16_t) * (size_t)q * H;
+    if (sm > (size_t)device_info().smem_optin) return FPX_EINVAL;
     if (cudaFuncSetAttribute(k_router<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) return FPX_ECUDA;
-    k_router<0><<<(E + 1) / 2, kThreads, sm, s>>>(R, E, H, q, x, nullptr, logits, nullptr, nullptr, nullptr);
+    RouterArgs ra{};
+    ra.R = R;
+    ra.E = E; ra.H = H; ra.q = q; ra.k = 0;  // logits only; k_topk routes
+    ra.xin = x; ra.logits = logits;
+    k_router<0><<<(E + 1) / 2, kRouterThreads, sm, s>>>(ra);
     k_topk<<<1, 32 * kMaxQ, 0, s>>>(logits, E, q, k, idx, w, uni, n_uni);
     return launch_status();
 }
@@ -818,10 +941,10 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
     if (ws_bytes < wl.total) return FPX_ESPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     WsPtrs wp = ws_ptrs(ws, wl);
-    // the row-tile counters must start at zero; the kernels leave them at zero
-    if (cudaMemsetAsync(wp.cnt, 0, sizeof(int32_t) * (layer->H / 128), s) != cudaSuccess) return FPX_ECUDA;
+    // the router's arrival counter must start at zero; the router leaves it at zero
+    if (cudaMemsetAsync(wp.nuni, 0, 16, s) != cudaSuccess) return FPX_ECUDA;
     Plan p = make_plan(*layer, q);
-    return dispatch_q<0>(q, *layer, p, k, x, nullptr, y, idx_out, w_out, logits_out, nullptr, wp, true, nullptr, s);
+    return dispatch_q<0>(q, *layer, p, k, x, nullptr, y, idx_out, w_out, logits_out, nullptr, wp, true, nullptr, false, s);
 }
 
 int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int q, int k, float* rL, int32_t* idx_out,
@@ -840,16 +963,16 @@ int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int
     WsPtrs wp = ws_ptrs(ws, wl);
     const size_t state = sizeof(float) * (size_t)q * layers[0].H;
     if (r0 != rL && cudaMemcpyAsync(rL, r0, state, cudaMemcpyDeviceToDevice, s) != cudaSuccess) return FPX_ECUDA;
-    if (cudaMemsetAsync(wp.cnt, 0, sizeof(int32_t) * (layers[0].H / 128), s) != cudaSuccess) return FPX_ECUDA;
+    if (cudaMemsetAsync(wp.nuni, 0, 16, s) != cudaSuccess) return FPX_ECUDA;
     Plan p = make_plan(layers[0], q);
     for (int l = 0; l < n_layers; l++) {
         int32_t* io = idx_out ? idx_out + (size_t)l * q * k : nullptr;
         float* tr = r_trace ? r_trace + (size_t)l * q * layers[0].H : nullptr;
-        cudaEvent_t const* ev = events ? reinterpret_cast<cudaEvent_t const*>(events) + 3 * l : nullptr;
-        int st = dispatch_q<1>(q, layers[l], p, k, nullptr, rL, rL, io, nullptr, nullptr, tr, wp, l == 0, ev, s);
+        cudaEvent_t const* ev = events ? reinterpret_cast<cudaEvent_t const*>(events) + 4 * l : nullptr;
+        int st = dispatch_q<1>(q, layers[l], p, k, nullptr, rL, rL, io, nullptr, nullptr, tr, wp, l == 0, ev, l > 0, s);
         if (st) return st;
     }
-    if (events && cudaEventRecord(reinterpret_cast<cudaEvent_t const*>(events)[3 * n_layers], s) != cudaSuccess)
+    if (events && cudaEventRecord(reinterpret_cast<cudaEvent_t const*>(events)[4 * n_layers], s) != cudaSuccess)
         return FPX_ECUDA;
     return FPX_OK;
 }
@@ -868,7 +991,7 @@ int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int
 
 namespace {
 
-constexpr size_t kStaticWsBytes = size_t(8) << 20;  // 8 MiB: the decode shapes need at most 4.4 MB
+constexpr size_t kStaticWsBytes = size_t(16) << 20;  // 16 MiB: the decode shapes need at most 8.7 MB
 __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
 // In host code `g_static_ws` only names the symbol; its device address differs per device and is

@@ -145,12 +145,12 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
  * inside a host framework that owns every device allocation (its own arena or allocator) and allows
  * no others, or a latency-critical loop that must never call cudaMalloc/cudaFree because they can
  * synchronise the device. The pages have no counterpart to this call; it exists for deployment only.
- * Same arguments and results as moe_layer_decode, except that the scratch is an 8 MiB array inside
+ * Same arguments and results as moe_layer_decode, except that the scratch is a 16 MiB array inside
  * libfpx.so (one per device, held until the process exits) instead of a caller workspace, and the
  * status word is copied to dev_status (nullable, device, 4-byte aligned) at the end of the call.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
- *   - Shapes whose moe_workspace_bytes() exceeds 8 MiB fail with FPX_ESPACE (the decode shapes,
- *     H = 4096, I = 2048, E = 256, q <= 4, k <= 8, need at most 4.4 MB).
+ *   - Shapes whose moe_workspace_bytes() exceeds 16 MiB fail with FPX_ESPACE (the decode shapes,
+ *     H = 4096, I = 2048, E = 256, q <= 4, k <= 8, need at most 8.7 MB).
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *     that device current; make that first call before capturing a stream into a graph.
  *   - Every call on a device shares the one array, which keeps the previous call's contents: calls
@@ -164,10 +164,12 @@ int moe_layer_decode_static_ws(const moe_layer* layer, const uint16_t* x, int q,
  * E): state r binary32 [q][H] starts at r0; layer l takes u_l = RN_bfloat16(r_l / sqrt(mean(r_l^2)
  * + 1e-6)) and sets r_{l+1} = r_l + MoE_l(u_l). rL receives r_{n_layers}; r0 and rL may alias.
  * idx_out (nullable) gets idx[n_layers][q][k]; r_trace (nullable) gets r_l for l = 0..n_layers-1
- * ([n_layers][q][H]). Enqueues 3 kernels per layer (router, gate/up, down) and nothing else, so the
- * whole pass can be captured as one CUDA graph. events (nullable) is a host array of
- * 3*n_layers + 1 cudaEvent_t: events[3l + j] is recorded on `stream` just before kernel j of layer
- * l and events[3*n_layers] after the last kernel, so a caller can time each kernel.
+ * ([n_layers][q][H]). Enqueues two small memsets and then 4 kernels per layer (router, gate/up, down,
+ * combine), each launched as a programmatic dependent launch so that it overlaps the previous
+ * kernel's tail, and nothing else, so the whole pass can be captured as one CUDA graph. events
+ * (nullable) is a host array of 4*n_layers + 1 cudaEvent_t: events[4l + j] is recorded on `stream`
+ * just before kernel j of layer l and events[4*n_layers] after the last kernel, so a caller can time
+ * each kernel (with events the kernels run without overlap).
  * The normalisation is this project's reading (the pages do not define the residual stream):
  * without it the synthetic state overflows binary32 within a few dozen layers.
  * [P-dsv4] paragraph 3 (43 layers; every token streams the active weights of all layers). */
