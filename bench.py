@@ -32,7 +32,7 @@ WORKLOAD = ("43-layer synthetic MoE stack, each layer hidden 4096, 256 routed ex
 N_BATCHES = 8
 
 
-NK = 4  # kernels per layer: router, gate/up, down, combine
+NK = 5  # kernels per layer: router, gate/up, h + down tables, down, combine
 
 def layer_bytes(n_union):
     import bit_block_quantized_wt_b300 as fpx
@@ -377,10 +377,12 @@ def run_fpx(args):
     # per-kernel durations (events around every kernel of the pass, on its stream)
     prof_steps = max(3, min(20, args.steps))
     kavg, kper_layer = kernel_profile(r4, prof_steps)
-    names = ["k_router", "k_gate_up", "k_down", "k_combine"]
+    names = ["k_router", "k_gate_up", "k_hpack", "k_down", "k_combine"]
     mean_union = float(np.mean([np.mean(u) for u in unions]))
-    # k_combine reads the 2 K parts of every routed output, the shared output and r, and writes r
-    alg = [stack.layers[0].E * H * 4, gate_up_bytes(mean_union), down_bytes(mean_union),
+    # k_hpack reads the 2 K parts of g and u of every item and writes the down table sets (17 I bytes
+    # each); k_combine reads the 2 K parts of every routed output, the shared output and r, and writes r
+    alg = [stack.layers[0].E * H * 4, gate_up_bytes(mean_union),
+           (mean_union + 1) * (4 * Q * I * 4 + 17 * I), down_bytes(mean_union),
            (2 * mean_union + 3) * Q * H * 4]
     dom = int(np.argmax(kavg))
     achieved = alg[dom] / (kavg[dom] / 1e3) / 1e9

@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gemv_mma(const __grid_consta
     __shared__ float red4[(kWarps + 1) * 4];
     __shared__ float part[kWarps][kTileRows][4];
     const int K = A.K, N = A.N, S = A.S, tpg = kWarps / S;
-    const Smem Sm = carve(smem, btab_bytes(K), 1);
+    const Smem Sm = carve(smem, btab_bytes(K), FMT == 3 ? 2 : 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     init_rings(Sm);
     const int U = K / (64 * box_chunks(FMT)) / S;  // boxes per (tile, split)
@@ -221,8 +221,10 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gemv_mma(const __grid_consta
             for (int w = 0; w < kWarps; w++) try_issue(w);
     }
 
-    if (A.x_bf16) build_tables<FMT, 0>(SrcBF16{reinterpret_cast<const uint16_t*>(A.x)}, K, Q, Sm.tab0, nullptr, Sm.csum, shift, red4);
-    else build_tables<FMT, 0>(SrcF32{reinterpret_cast<const float*>(A.x)}, K, Q, Sm.tab0, nullptr, Sm.csum, shift, red4);
+    if (A.x_bf16)
+        build_tables<FMT, false>(SrcBF16{reinterpret_cast<const uint16_t*>(A.x)}, K, Q, Sm.tab0, Sm.tab1, nullptr, Sm.oq, shift, red4);
+    else
+        build_tables<FMT, false>(SrcF32{reinterpret_cast<const float*>(A.x)}, K, Q, Sm.tab0, Sm.tab1, nullptr, Sm.oq, shift, red4);
     __syncthreads();
 
     if (warp == kWarps) {
@@ -252,6 +254,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gemv_mma(const __grid_consta
     const int split = warp % S;
     const Ring R = warp_ring(Sm, warp);
     const int a_idx = b_active_index(lane);
+    const LaneOfs lofs = lane_ofs<FMT>(t);
     uint32_t consumed = 0, bad = 0;
     bool ok = true;
     for (int n = 0; n < my_groups; n++) {
@@ -261,8 +264,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gemv_mma(const __grid_consta
             if (!ring_wait(R, consumed, A.st)) { ok = false; break; }
             const uint8_t* slot = R.slots + (consumed % kStages) * kSlotBytes;
             const int chunk0 = (split * U + u) * box_chunks(FMT);
-            box_tiles<FMT, 1, box_chunks(FMT)>(slot + g * box_bytes(FMT), lane_tab(Sm.tab0, Sm.zero, a_idx, chunk0),
-                                               lane_csum(Sm.csum, chunk0, t), t, A.magic, y, bad);
+            box_tiles<FMT, 1, box_chunks(FMT)>(smem_u32(slot) + g * box_bytes(FMT), lofs, lane_tab(Sm.tab0, Sm.zero, a_idx, chunk0),
+                                               lane_tab(Sm.tab1, Sm.zero, a_idx, chunk0), lane_oq(Sm.oq, chunk0, t), A.magic, y, bad);
             ring_release(R, consumed);
             consumed++;
         }
@@ -287,7 +290,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gemv_mma(const __grid_consta
 
 template <int FMT>
 bool gemv_mma_fits(int64_t K) {
-    return mma_shape_ok(FMT, K) && smem_bytes(btab_bytes((int)K), 1) <= (size_t)device_info().smem_optin;
+    return mma_shape_ok(FMT, K) && smem_bytes(btab_bytes((int)K), FMT == 3 ? 2 : 1) <= (size_t)device_info().smem_optin;
 }
 
 template <int FMT, int Q>
@@ -306,7 +309,7 @@ int launch_gemv_mma_q(const uint8_t* Wq, int64_t N, int64_t K, const void* x, in
     A.magic = kMagic;
     const int64_t ngroups = (ntiles + kWarps / S - 1) / (kWarps / S);
     const int grid = (int)(ngroups < di.sms ? ngroups : di.sms);
-    const size_t smem = smem_bytes(btab_bytes((int)K), 1);
+    const size_t smem = smem_bytes(btab_bytes((int)K), FMT == 3 ? 2 : 1);
     if (cudaFuncSetAttribute(k_gemv_mma<FMT, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) return FPX_ECUDA;
     k_gemv_mma<FMT, Q><<<grid, kCtaThreads, smem, s>>>(A);
     return launch_status();

@@ -119,6 +119,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// Bulk (1-D) TMA copy of `bytes` (a multiple of 16) from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
     asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
@@ -308,42 +315,109 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// One table entry (32 bytes) = the B registers of one active lane for one chunk: the 16 activations
-// of a code group scaled by 2^(sh - P(pair)) (FP2: 2^(sh + 1 - P)), arranged as pairs 0..7. FP2/FP3
-// pair p holds codes (p, p + 8); FP4 pair p holds codes (8 (p/4) + p%4, +4). Also returns, for FP2,
-// the block offset contribution sum_m B_m (1024 + 1.5 * 2^P(m)) in code order.
-template <int FMT>
-__device__ __forceinline__ void pack_entry(const float (&v)[16], int sh, uint4& e0, uint4& e1, float& part) {
-    uint32_t w[8];
+__device__ __forceinline__ float h2lo(uint32_t w) { return __half2float(__ushort_as_half((uint16_t)(w & 0xFFFFu))); }
+__device__ __forceinline__ float h2hi(uint32_t w) { return __half2float(__ushort_as_half((uint16_t)(w >> 16))); }
+
+// FP3 high-plane pair p carries its two bits at binary16 mantissa position Q(p).
+__host__ __device__ constexpr int hi_shift(int p) { return p < 7 ? p + 3 : 9; }
+
+// Table entries (32 bytes each) = the B registers of one active lane for one chunk, pairs 0..7 of a
+// 16-activation code group. FP2/FP3 pair p holds codes (p, p + 8), FP4 pair p codes
+// (8 (p/4) + p%4, +4). Scales: FP2 and the FP3 low plane 2^(sh + 1 - P(p)), the FP3 high plane
+// 2^(sh + 3 - Q(p)), FP4 2^sh. `part` returns the group's share of the block offset that the MMA's
+// initial accumulator removes: FP2 sum B (1024 + 1.5 2^P); FP3 sum [1024 B_lo + 1024 B_hi
+// + 3.5 2^P B_lo] (from the binary16 values the MMA sees).
+__device__ __forceinline__ void pack_fp2(const float (&v)[16], int sh, uint32_t (&w)[8], float& part) {
+    part = 0.f;
 #pragma unroll
     for (int p = 0; p < 8; p++) {
-        const int lo = FMT == 4 ? 8 * (p / 4) + p % 4 : p;
-        const int hi = FMT == 4 ? lo + 4 : p + 8;
-        const float sc = exp2i(sh - pair_shift(FMT, p) + (FMT == 2 ? 1 : 0));
-        w[p] = pack_h2(v[lo] * sc, v[hi] * sc);
+        const float sc = exp2i(sh + 1 - pair_shift(2, p));
+        w[p] = pack_h2(v[p] * sc, v[p + 8] * sc);
+        part = fmaf(h2lo(w[p]) + h2hi(w[p]), 1024.0f + 1.5f * float(1 << pair_shift(2, p)), part);
     }
-    e0 = make_uint4(w[0], w[1], w[2], w[3]);
-    e1 = make_uint4(w[4], w[5], w[6], w[7]);
+}
+__device__ __forceinline__ void pack_fp3(const float (&v)[16], int sh, uint32_t (&lo)[8], uint32_t (&hi)[8], float& part) {
     part = 0.f;
-    if constexpr (FMT == 2) {
 #pragma unroll
-        for (int m = 0; m < 16; m++) {
-            const int p = m & 7;
-            const float b = __half2float(m < 8 ? __ushort_as_half((uint16_t)(w[p] & 0xFFFFu)) : __ushort_as_half((uint16_t)(w[p] >> 16)));
-            part = fmaf(b, 1024.0f + 1.5f * float(1 << pair_shift(2, p)), part);
-        }
+    for (int p = 0; p < 8; p++) {
+        const float sl = exp2i(sh + 1 - pair_shift(3, p)), sh8 = exp2i(sh + 3 - hi_shift(p));
+        lo[p] = pack_h2(v[p] * sl, v[p + 8] * sl);
+        hi[p] = pack_h2(v[p] * sh8, v[p + 8] * sh8);
+        const float bl = h2lo(lo[p]) + h2hi(lo[p]), bh = h2lo(hi[p]) + h2hi(hi[p]);
+        part = fmaf(bl, 1024.0f + 3.5f * float(1 << pair_shift(3, p)), fmaf(bh, 1024.0f, part));
+    }
+}
+__device__ __forceinline__ void pack_fp4(const float (&v)[16], int sh, uint32_t (&w)[8]) {
+    const float sc = exp2i(sh);
+#pragma unroll
+    for (int p = 0; p < 8; p++) w[p] = pack_h2(v[8 * (p / 4) + p % 4] * sc, v[8 * (p / 4) + p % 4 + 4] * sc);
+}
+__device__ __forceinline__ void store_entry(uint2* tab, size_t e, const uint32_t (&w)[8]) {
+    uint4* d = reinterpret_cast<uint4*>(tab + e * 4);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Bytes of the FP2/FP3 offset quads: per block, two float4 {o(2h), o(2h+1), o(2h), o(2h+1)} (h = 0, 1)
+// laid out as the MMA's initial accumulator of the lanes that decode the block.
+__host__ __device__ constexpr int oq_bytes(int K) { return K; }
+
+// A table set for K weights, as built in global memory and copied as one block into shared memory:
+// [table A (8K) | table B (8K) | offset quads (K)] and, in global memory only, 16 bytes of column
+// shifts. Gate/up: A = FP2, B = FP4. Down, routed expert: A = FP3 low plane, B = FP3 high plane;
+// shared expert: A = FP4.
+__host__ __device__ constexpr int tset_copy_bytes(int K) { return 2 * btab_bytes(K) + oq_bytes(K); }
+__host__ __device__ constexpr int tset_bytes(int K) { return tset_copy_bytes(K) + 16; }
+
+// Packs code group gi (16 consecutive activations v of token tok, starting at weight k0 of K) into a
+// table set at `ts` (global memory): FA is the format of table A (2: FP2 with FP4 in table B; 3: FP3
+// planes; 4: FP4 only). Returns the group's share of its block offset (0 for FP4). Lanes holding the
+// two groups of a block (gi even, gi + 1) add the shares with add_offsets().
+template <int FA>
+__device__ __forceinline__ float pack_group(uint8_t* ts, int K, int tok, int k0, const float (&v)[16], int sh) {
+    const int c = k0 >> 6, half = (k0 >> 5) & 1, hw = (k0 >> 4) & 1;
+    const size_t e = (size_t)c * 16 + 8 * half + 2 * tok + hw;
+    uint2* ta = reinterpret_cast<uint2*>(ts);
+    uint2* tb = reinterpret_cast<uint2*>(ts + btab_bytes(K));
+    uint32_t w[8];
+    float part = 0.f;
+    if constexpr (FA == 2) {
+        pack_fp2(v, sh, w, part);
+        store_entry(ta, e, w);
+        pack_fp4(v, sh, w);
+        store_entry(tb, e, w);
+    } else if constexpr (FA == 3) {
+        uint32_t wh[8];
+        pack_fp3(v, sh, w, wh, part);
+        store_entry(ta, e, w);
+        store_entry(tb, e, wh);
+    } else {
+        pack_fp4(v, sh, w);
+        store_entry(ta, e, w);
+    }
+    return part;
+}
+
+// Whole warp, after pack_group on lane pairs (2i, 2i + 1) = the two groups of one block: writes the
+// block's negated offset quad entries (valid lanes only).
+__device__ __forceinline__ void add_offsets(uint8_t* ts, int K, int tok, int k0, float part, bool valid) {
+    const float nxt = __shfl_down_sync(0xffffffffu, part, 1);
+    if (valid && ((k0 >> 4) & 1) == 0) {
+        float* qd = reinterpret_cast<float*>(ts + 2 * btab_bytes(K)) + (size_t)((k0 >> 5) * 2 + (tok >> 1)) * 4 + (tok & 1);
+        qd[0] = qd[2] = -(part + nxt);
     }
 }
 
-// Builds the activation tables for columns src[tok][k] (tok < q <= 4, K % 64 == 0): tabA in format
-// FA, tabB in format FB (FB == 0: none) and, when FA == 2, the negated FP2 block offsets
-// csum[block * 4 + tok] (the MMA's initial accumulator). shift[4] receives the column shifts. Whole CTA (nt threads, nt % 32 == 0). Each thread owns
-// whole 16-weight code groups: it issues all of a pass's loads before using them, and writes each
-// table entry with two 16-byte stores.
-// CONS: only the kWarps consumer warps (threads 0 .. 32 kWarps - 1) take part and synchronise on
-// the consumer barrier, so the producer warp can issue loads meanwhile; otherwise the whole CTA.
-template <int FA, int FB, bool CONS = false, class SRC>
-__device__ void build_tables(const SRC src, int K, int q, uint2* tabA, uint2* tabB, float* csum, int* shift,
+// Builds the activation tables for columns src[tok][k] (tok < q <= 4, K % 64 == 0) in format FMT:
+// tab (FP2, FP3 low plane, or FP4), tab_hi (FP3 high plane) and, for FP2/FP3, the negated block
+// offsets oq (the MMA's initial accumulator); WITH4 also builds the FP4 table tab4 from the same
+// columns. shift[4] receives the column shifts. Each thread owns whole 16-weight code groups: it
+// issues all of a pass's loads before using them and writes each table entry with two 16-byte
+// stores. CONS: only the kWarps consumer warps (threads 0 .. 32 kWarps - 1) take part and
+// synchronise on the consumer barrier, so the producer warp can issue loads meanwhile; otherwise the
+// whole CTA.
+template <int FMT, bool WITH4, bool CONS = false, class SRC>
+__device__ void build_tables(const SRC src, int K, int q, uint2* tab, uint2* tab_hi, uint2* tab4, float* oq, int* shift,
                              float* red4) {
     constexpr int V = SRC::V;
     const int ngr = q * K / 16;
@@ -379,20 +453,24 @@ __device__ void build_tables(const SRC src, int K, int q, uint2* tabA, uint2* ta
     if ((tid & 31) == 0)
         for (int t = 0; t < 4; t++) red4[(tid >> 5) * 4 + t] = m[t];
     // entries of absent tokens stay zero
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     for (int i = tid; i < (K / 64) * 16; i += nt) {
-        const int a = i & 15;
-        if (((a >> 1) & 3) >= q) {
-            uint4* ea = reinterpret_cast<uint4*>(tabA + (size_t)i * 4);
-            ea[0] = ea[1] = make_uint4(0u, 0u, 0u, 0u);
-            if (FB) {
-                uint4* eb = reinterpret_cast<uint4*>(tabB + (size_t)i * 4);
-                eb[0] = eb[1] = make_uint4(0u, 0u, 0u, 0u);
+        if (((i & 15) >> 1 & 3) >= q) {
+            reinterpret_cast<uint4*>(tab + (size_t)i * 4)[0] = z;
+            reinterpret_cast<uint4*>(tab + (size_t)i * 4)[1] = z;
+            if (FMT == 3) {
+                reinterpret_cast<uint4*>(tab_hi + (size_t)i * 4)[0] = z;
+                reinterpret_cast<uint4*>(tab_hi + (size_t)i * 4)[1] = z;
+            }
+            if (WITH4) {
+                reinterpret_cast<uint4*>(tab4 + (size_t)i * 4)[0] = z;
+                reinterpret_cast<uint4*>(tab4 + (size_t)i * 4)[1] = z;
             }
         }
     }
-    if (FA == 2)
-        for (int i = tid; i < (K / 32) * 4; i += nt)
-            if ((i & 3) >= q) csum[i] = 0.f;
+    if (FMT != 4)
+        for (int i = tid; i < (K / 32) * 8; i += nt)
+            if (2 * ((i >> 2) & 1) + (i & 1) >= q) oq[i] = 0.f;
     if (CONS) consumers_sync(); else __syncthreads();
     if (tid < 4) {
         float mm = 0.f;
@@ -413,27 +491,33 @@ __device__ void build_tables(const SRC src, int K, int q, uint2* tabA, uint2* ta
             if (gi < ngr) {
                 const int tok = gi * 16 / K, k0 = gi * 16 - tok * K;
                 const int c = k0 >> 6, half = (k0 >> 5) & 1, hw = (k0 >> 4) & 1;
-                const int a = 8 * half + 2 * tok + hw;
+                const size_t e = (size_t)c * 16 + 8 * half + 2 * tok + hw;
                 const int sh = shift[tok];
-                uint4 e0, e1;
-                pack_entry<FA>(v[it], sh, e0, e1, part);
-                uint4* ea = reinterpret_cast<uint4*>(tabA + ((size_t)c * 16 + a) * 4);
-                ea[0] = e0;
-                ea[1] = e1;
-                if (FB) {
-                    float dummy;
-                    pack_entry<FB>(v[it], sh, e0, e1, dummy);
-                    uint4* eb = reinterpret_cast<uint4*>(tabB + ((size_t)c * 16 + a) * 4);
-                    eb[0] = e0;
-                    eb[1] = e1;
+                uint32_t w[8];
+                if constexpr (FMT == 2) {
+                    pack_fp2(v[it], sh, w, part);
+                    store_entry(tab, e, w);
+                } else if constexpr (FMT == 3) {
+                    uint32_t wh[8];
+                    pack_fp3(v[it], sh, w, wh, part);
+                    store_entry(tab, e, w);
+                    store_entry(tab_hi, e, wh);
+                } else {
+                    pack_fp4(v[it], sh, w);
+                    store_entry(tab, e, w);
+                }
+                if (WITH4) {
+                    pack_fp4(v[it], sh, w);
+                    store_entry(tab4, e, w);
                 }
             }
-            if (FA == 2) {
+            if (FMT != 4) {
                 // a 32-weight block is two consecutive groups (lanes 2i, 2i + 1): add them in order
                 const float nxt = __shfl_down_sync(0xffffffffu, part, 1);
                 if (gi < ngr && (gi & 1) == 0) {
                     const int tok = gi * 16 / K, blk = (gi * 16 - tok * K) / 32;
-                    csum[blk * 4 + tok] = -(part + nxt);
+                    float* qd = oq + (size_t)(blk * 2 + (tok >> 1)) * 4 + (tok & 1);
+                    qd[0] = qd[2] = -(part + nxt);
                 }
             }
         }
@@ -483,115 +567,194 @@ __host__ __device__ constexpr bool mma_shape_ok(int fmt, int64_t K) { return K >
 
 // ------------------------------------------------------------------ chunk processing
 
-// Loads the code groups and block scale of one chunk of one row from a staged box, decodes them into
-// A pairs and returns the block scale in binary32. `row` points at the row inside the box, `c` is the
-// chunk inside the box, t the thread index in its group of four, magic = kMagic in a register. An
-// FP4 block with the NaN scale (255) counts as zeros and sets `bad`.
+// Shared-memory loads from a 32-bit shared address plus a compile-time byte offset, so the hot loop
+// needs one base register per stream and no address arithmetic.
+template <int OFF>
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(v) : "r"(a), "n"(OFF));
+    return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1+%2];" : "=h"(v) : "r"(a), "n"(OFF));
+    return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint32_t lds8(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u8 %0, [%1+%2];" : "=h"(v) : "r"(a), "n"(OFF));
+    return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4+%5];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a), "n"(OFF));
+    return v;
+}
+
+// Per-thread byte offsets inside a chunk, for thread t of its group of four (which decodes block
+// t / 2, codes 16 (t % 2) .. 16 (t % 2) + 15):
+//   FP2 chunk [d0 (2) | codes0 (8) | d1 (2) | codes1 (8)] = words 0..4: thread t reads words t and
+//   t + 1 (so the 8 rows x 4 threads of a load touch 32 distinct banks at the 80-byte row pitch) and
+//   takes its code bytes 2 + 4t .. (t < 2) or word t + 1 (t >= 2) with one PRMT; scale at 10 (t / 2).
+//   FP3 chunk [d0 | lo0 (8) | hi0 (4) | d1 | lo1 | hi1]: low-plane word as FP2 (base 0 or 16), high
+//   bits at 14 (t / 2) + 10 + 2hw, scale at 14 (t / 2).
+//   FP4 chunk [e0 (1) | codes0 (16) | e1 | codes1]: 8 code bytes at 17 (t / 2) + 1 + 8hw, read as three
+//   aligned words and a funnel shift; the alignment differs between even and odd chunks (chunks are
+//   34 bytes); scale byte at 17 (t / 2).
+struct LaneOfs {
+    int w, w_odd;       // aligned code word offset (FP4: even / odd chunks)
+    uint32_t sel, sh_odd;  // FP2/FP3: PRMT selector; FP4: funnel shifts (even / odd chunks)
+    int s, h;           // scale and FP3 high-plane offsets
+};
+
 template <int FMT>
-__device__ __forceinline__ float load_decode(const uint8_t* row, int c, int t, uint32_t magic, uint32_t (&a)[8],
-                                             uint32_t& bad) {
+__device__ __forceinline__ LaneOfs lane_ofs(int t) {
     const int half = t >> 1, hw = t & 1;
-    if constexpr (FMT == 2) {
-        // chunk = [d0 (2) | codes0 (8) | d1 (2) | codes1 (8)], 4-byte aligned. The thread's code word
-        // is bytes 2+4hw.. (first block) or 12+4hw.. (second): two aligned words and one PRMT.
-        const uint8_t* ch = row + 20 * c;
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(ch + (half ? 12 : 0) + 4 * hw);
-        const uint32_t cw = __byte_perm(w[0], w[1], half ? 0x3210 : 0x5432);
-        decode_fp2(cw, magic, a);
-        const uint16_t d = *reinterpret_cast<const uint16_t*>(ch + 10 * half);
-        return __half2float(__ushort_as_half(d));
-    } else if constexpr (FMT == 3) {
-        // chunk = [d0 (2) | lo0 (8) | hi0 (4) | d1 (2) | lo1 (8) | hi1 (4)], 4-byte aligned
-        const uint8_t* ch = row + 28 * c;
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(ch + (half ? 16 : 0) + 4 * hw);
-        const uint32_t lo = __byte_perm(w[0], w[1], half ? 0x3210 : 0x5432);
-        const uint32_t hg = *reinterpret_cast<const uint16_t*>(ch + 14 * half + 10 + 2 * hw);
-        decode_fp3(lo, hg, magic, a);
-        const uint16_t d = *reinterpret_cast<const uint16_t*>(ch + 14 * half);
-        return __half2float(__ushort_as_half(d));
+    LaneOfs L{};
+    if (FMT == 2) {
+        L.w = 4 * t;
+        L.sel = half ? 0x7654u : 0x5432u;
+        L.s = 10 * half;
+    } else if (FMT == 3) {
+        L.w = half ? 16 + 4 * hw : 4 * hw;
+        L.sel = half ? 0x3210u : 0x5432u;
+        L.h = 14 * half + 10 + 2 * hw;
+        L.s = 14 * half;
     } else {
-        // chunk = [e0 (1) | codes0 (16) | e1 (1) | codes1 (16)], 2-byte aligned
-        const uint8_t* ch = row + 34 * c;
-        const uint8_t* src = ch + 17 * half + 1 + 8 * hw;  // 8 code bytes
-        const uintptr_t addr = reinterpret_cast<uintptr_t>(src);
-        const uint32_t* base = reinterpret_cast<const uint32_t*>(addr & ~uintptr_t(3));
-        const uint32_t sh = static_cast<uint32_t>(addr & 3) * 8;
-        const uint32_t x0 = base[0], x1 = base[1], x2 = base[2];
-        const uint32_t w0 = __funnelshift_r(x0, x1, sh), w1 = __funnelshift_r(x1, x2, sh);
-        decode_fp4(w0, w1, a);
-        const uint32_t e = ch[17 * half];
-        bad |= e == 255u;
+        const int o = 17 * half + 1 + 8 * hw;
+        L.w = o - (o & 3);
+        L.sel = (uint32_t)(o & 3) * 8;
+        L.w_odd = o - ((o + 2) & 3);
+        L.sh_odd = (uint32_t)((o + 2) & 3) * 8;
+        L.s = 17 * half;
+    }
+    return L;
+}
+
+// Per-stage base addresses of one thread: its row g of the first tile, plus the lane offsets.
+struct RowAddr {
+    uint32_t w, w_odd, s, h;
+};
+__device__ __forceinline__ RowAddr row_addr(uint32_t row, const LaneOfs& L) {
+    return RowAddr{row + (uint32_t)L.w, row + (uint32_t)L.w_odd, row + (uint32_t)L.s, row + (uint32_t)L.h};
+}
+
+// FP3 as two exact binary16 planes: low-plane pair i = 1024 + l 2^P (as FP2), high-plane pair
+// i = 1024 + h 2^Q(i). With B_lo = 2 x 2^-P and B_hi = 8 x 2^-Q the two MMAs sum 2 l x + 8 h x plus
+// a per-block constant of the activations, removed by the initial accumulator: (2c - 7) x with
+// c = l + 4h.
+__device__ __forceinline__ void decode_fp3_planes(uint32_t lo, uint32_t hg, uint32_t magic, uint32_t (&al)[8],
+                                                  uint32_t (&ah)[8]) {
+    decode_fp2(lo, magic, al);
+    const uint32_t sp = __byte_perm(hg, 0u, 0x4140);  // bit k -> k (k < 8), bit 8 + k -> 16 + k
+    const uint32_t h3 = sp << 3, h2 = sp << 2;
+    ah[0] = (h3 & 0x00080008u) | magic;
+    ah[1] = (h3 & 0x00100010u) | magic;
+    ah[2] = (h3 & 0x00200020u) | magic;
+    ah[3] = (h3 & 0x00400040u) | magic;
+    ah[4] = (h3 & 0x00800080u) | magic;
+    ah[5] = (h3 & 0x01000100u) | magic;
+    ah[6] = (h3 & 0x02000200u) | magic;
+    ah[7] = (h2 & 0x02000200u) | magic;
+}
+
+// Decodes chunk C (compile-time) of the row at byte offset RO (compile-time) from the thread's base:
+// A pairs (FP3: both planes) and the block scale in binary32.
+template <int FMT, int RO, int C>
+__device__ __forceinline__ float row_decode(const RowAddr& ra, const LaneOfs& L, uint32_t magic, uint32_t (&a)[8],
+                                            uint32_t (&ah)[8], uint32_t& bad) {
+    constexpr int CB = chunk_bytes(FMT);
+    if constexpr (FMT == 2) {
+        const uint32_t cw = __byte_perm(lds32<RO + C * CB>(ra.w), lds32<RO + C * CB + 4>(ra.w), L.sel);
+        decode_fp2(cw, magic, a);
+        return __half2float(__ushort_as_half((uint16_t)lds16<RO + C * CB>(ra.s)));
+    } else if constexpr (FMT == 3) {
+        const uint32_t lo = __byte_perm(lds32<RO + C * CB>(ra.w), lds32<RO + C * CB + 4>(ra.w), L.sel);
+        decode_fp3_planes(lo, lds16<RO + C * CB>(ra.h), magic, a, ah);
+        return __half2float(__ushort_as_half((uint16_t)lds16<RO + C * CB>(ra.s)));
+    } else {
+        const uint32_t base = (C & 1) ? ra.w_odd : ra.w;
+        const uint32_t sh = (C & 1) ? L.sh_odd : L.sel;
+        const uint32_t x0 = lds32<RO + C * CB>(base), x1 = lds32<RO + C * CB + 4>(base), x2 = lds32<RO + C * CB + 8>(base);
+        decode_fp4(__funnelshift_r(x0, x1, sh), __funnelshift_r(x1, x2, sh), a);
+        const uint32_t e = lds8<RO + C * CB>(ra.s);
+        bad |= e == 255u;  // NaN scale: the block is invalid and counts as zeros
         // 2^(e-127): e in 1..254 is a normal binary32 power of two, e == 0 the subnormal 2^-127
         const float sc = e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);
         return e == 255u ? 0.0f : sc;
     }
 }
 
-// D = A * B + C with C given (the FP2 block offsets), m16n8k16, binary16 inputs, binary32 accumulators.
-__device__ __forceinline__ void mma_from(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1, float c0, float c1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%10,%11};"
+// D = A * B + C with C = {c.x, c.y, c.z, c.w} (m16n8k16, binary16 inputs, binary32 accumulators).
+__device__ __forceinline__ void mma_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                      uint32_t b1, const float4& c) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c.x), "f"(c.y), "f"(c.z), "f"(c.w));
 }
 
-// Accumulates one chunk (64 weights = 2 blocks) of a 16-row tile into y[4] (the thread's (row, token)
-// partial sums for its block parity). r0 and r8 point at the tile's rows g and g + 8. For FP2, ncs
-// holds the negated block offsets of the thread's two tokens.
-template <int FMT>
-__device__ __forceinline__ void tile_chunk(const uint8_t* r0, const uint8_t* r8, int c, int t, uint32_t magic,
-                                           const uint2 (&b)[4], float2 ncs, float (&y)[4], uint32_t& bad) {
-    uint32_t a0[8], a8[8];
-    const float d0 = load_decode<FMT>(r0, c, t, magic, a0, bad);
-    const float d8 = load_decode<FMT>(r8, c, t, magic, a8, bad);
-    float acc[4];
-    if constexpr (FMT == 2) mma_from(acc, a0[0], a8[0], a0[1], a8[1], b[0].x, b[0].y, ncs.x, ncs.y);
-    else mma_first(acc, a0[0], a8[0], a0[1], a8[1], b[0].x, b[0].y);
-    mma_acc(acc, a0[2], a8[2], a0[3], a8[3], b[1].x, b[1].y);
-    mma_acc(acc, a0[4], a8[4], a0[5], a8[5], b[2].x, b[2].y);
-    mma_acc(acc, a0[6], a8[6], a0[7], a8[7], b[3].x, b[3].y);
-    y[0] = fmaf(d0, acc[0], y[0]);
-    y[1] = fmaf(d0, acc[1], y[1]);
-    y[2] = fmaf(d8, acc[2], y[2]);
-    y[3] = fmaf(d8, acc[3], y[3]);
-}
-
-// The lane's B registers for one chunk: two 16-byte loads, no branch (inactive lanes read zeros).
-__device__ __forceinline__ void load_b(const uint2* p, uint2 (&b)[4]) {
-    const uint4* q = reinterpret_cast<const uint4*>(p);
-    const uint4 v0 = q[0], v1 = q[1];
-    b[0] = make_uint2(v0.x, v0.y); b[1] = make_uint2(v0.z, v0.w);
-    b[2] = make_uint2(v1.x, v1.y); b[3] = make_uint2(v1.z, v1.w);
+// Four MMAs over one plane of a 16-row tile x 64 weights: rows g (a0) and g + 8 (a8), B registers
+// from the lane's 32-byte table entry (two 16-byte halves).
+__device__ __forceinline__ void plane_mma(float (&acc)[4], const uint32_t (&a0)[8], const uint32_t (&a8)[8], const uint4& b0,
+                                          const uint4& b1) {
+    mma_acc(acc, a0[0], a8[0], a0[1], a8[1], b0.x, b0.y);
+    mma_acc(acc, a0[2], a8[2], a0[3], a8[3], b0.z, b0.w);
+    mma_acc(acc, a0[4], a8[4], a0[5], a8[5], b1.x, b1.y);
+    mma_acc(acc, a0[6], a8[6], a0[7], a8[7], b1.z, b1.w);
 }
 
 // Zero area read by inactive lanes in place of table entries: one entry per chunk of a box.
 constexpr int kZeroBytes = 8 * 64 * 8;  // box_chunks <= 8 chunks x 512 bytes
 
-// Per-lane pointer to the table entries of chunk `chunk0` (64 uint2 per chunk), or to the zero area
-// for lanes whose B fragment is structurally zero.
-__device__ __forceinline__ const uint2* lane_tab(const uint2* tab, const uint2* zero, int a_idx, int chunk0) {
-    return a_idx >= 0 ? tab + (size_t)chunk0 * 64 + a_idx * 4 : zero;
+// Per-lane shared address of the table entry of chunk `chunk0` (512 bytes per chunk), or of the zero
+// area for lanes whose B fragment is structurally zero.
+__device__ __forceinline__ uint32_t lane_tab(const uint2* tab, const uint2* zero, int a_idx, int chunk0) {
+    return a_idx >= 0 ? smem_u32(tab) + (uint32_t)chunk0 * 512u + (uint32_t)a_idx * 32u : smem_u32(zero);
 }
 
-// Per-lane pointer to the FP2 block offsets (8 floats per chunk) of chunk `chunk0`.
-__device__ __forceinline__ const float* lane_csum(const float* csum, int chunk0, int t) {
-    return csum + (size_t)chunk0 * 8 + (t >> 1) * 4 + 2 * (t & 1);
+// Per-lane shared address of the FP2/FP3 offset quad of chunk `chunk0` (64 bytes per chunk).
+__device__ __forceinline__ uint32_t lane_oq(const float* oq, int chunk0, int t) {
+    return smem_u32(oq) + (uint32_t)chunk0 * 64u + (uint32_t)(t >> 1) * 32u + (uint32_t)(t & 1) * 16u;
 }
 
-// NC chunks of a staged box for NT consecutive 16-row tiles sharing the activations; row points at
-// the thread's row g of the first tile, bp / csp are the lane pointers for the box's first chunk.
-// Fully unrolled so the decode of one chunk overlaps the MMAs of another.
-template <int FMT, int NT, int NC>
-__device__ __forceinline__ void box_tiles(const uint8_t* row, const uint2* bp, const float* csp, int t, uint32_t magic,
-                                          float (&y)[NT][4], uint32_t& bad) {
-    constexpr int P = box_bytes(FMT);
+// NC chunks of a staged box (row pitch box_bytes(FMT)) for NT consecutive 16-row tiles sharing the
+// activations. `row` is the shared address of the thread's row g of the first tile at the box's first
+// chunk; b / bh / oq are the lane addresses of the table entries (FP3: low and high plane) and offset
+// quads for that chunk. Fully unrolled so the decode of one chunk overlaps the MMAs of another.
+template <int FMT, int NT, int NC, int C = 0>
+__device__ __forceinline__ void box_tiles(uint32_t row, const LaneOfs& L, uint32_t b, uint32_t bh, uint32_t oq,
+                                          uint32_t magic, float (&y)[NT][4], uint32_t& bad) {
+    if constexpr (C < NC) {
+        constexpr int P = box_bytes(FMT);
+        const RowAddr ra = row_addr(row, L);
+        const uint4 b0 = lds128<C * 512>(b), b1 = lds128<C * 512 + 16>(b);
+        uint4 h0 = make_uint4(0u, 0u, 0u, 0u), h1 = h0;
+        if constexpr (FMT == 3) { h0 = lds128<C * 512>(bh); h1 = lds128<C * 512 + 16>(bh); }
+        float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (FMT != 4) {
+            const uint4 q = lds128<C * 64>(oq);
+            c4 = make_float4(__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z), __uint_as_float(q.w));
+        }
 #pragma unroll
-    for (int c = 0; c < NC; c++) {
-        uint2 b[4];
-        load_b(bp + c * 64, b);
-        const float2 ncs = FMT == 2 ? *reinterpret_cast<const float2*>(csp + c * 8) : make_float2(0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < NT; i++) tile_chunk<FMT>(row + i * 16 * P, row + (i * 16 + 8) * P, c, t, magic, b, ncs, y[i], bad);
+        for (int i = 0; i < NT; i++) {
+            uint32_t a0[8], a8[8], g0[8], g8[8];
+            const float d0 = i == 0 ? row_decode<FMT, 0, C>(ra, L, magic, a0, g0, bad) : row_decode<FMT, 16 * P, C>(ra, L, magic, a0, g0, bad);
+            const float d8 = i == 0 ? row_decode<FMT, 8 * P, C>(ra, L, magic, a8, g8, bad) : row_decode<FMT, 24 * P, C>(ra, L, magic, a8, g8, bad);
+            float acc[4];
+            mma_c(acc, a0[0], a8[0], a0[1], a8[1], b0.x, b0.y, c4);
+            mma_acc(acc, a0[2], a8[2], a0[3], a8[3], b0.z, b0.w);
+            mma_acc(acc, a0[4], a8[4], a0[5], a8[5], b1.x, b1.y);
+            mma_acc(acc, a0[6], a8[6], a0[7], a8[7], b1.z, b1.w);
+            if constexpr (FMT == 3) plane_mma(acc, g0, g8, h0, h1);
+            y[i][0] = fmaf(d0, acc[0], y[i][0]);
+            y[i][1] = fmaf(d0, acc[1], y[i][1]);
+            y[i][2] = fmaf(d8, acc[2], y[i][2]);
+            y[i][3] = fmaf(d8, acc[3], y[i][3]);
+        }
+        box_tiles<FMT, NT, NC, C + 1>(row, L, b, bh, oq, magic, y, bad);
     }
 }
 
@@ -657,9 +820,9 @@ struct Smem {
     uint8_t* ring;   // kRingBytes
     uint64_t* bars;  // full[kWarps * kStages], then empty[kWarps * kStages]
     uint2* zero;     // kZeroBytes of zeros
-    uint2* tab0;     // activation tables
-    uint2* tab1;
-    float* csum;     // FP2 block offsets: (K / 32) blocks x 4 tokens floats = K / 2 bytes
+    uint2* tab0;     // activation tables (FP3: low plane)
+    uint2* tab1;     // FP3 high plane
+    float* oq;       // FP2/FP3 offset quads, K bytes
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* raw, int tab_bytes, int ntabs) {
@@ -668,17 +831,17 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, int tab_bytes, int ntabs) {
     Smem s;
     s.ring = base;
     s.bars = reinterpret_cast<uint64_t*>(base + kRingBytes);
-    s.zero = reinterpret_cast<uint2*>(base + kRingBytes + 1024);
-    s.tab0 = reinterpret_cast<uint2*>(base + kRingBytes + 1024 + kZeroBytes);
-    s.tab1 = reinterpret_cast<uint2*>(base + kRingBytes + 1024 + kZeroBytes + tab_bytes);
-    s.csum = reinterpret_cast<float*>(base + kRingBytes + 1024 + kZeroBytes + (size_t)ntabs * tab_bytes);
+    s.zero = reinterpret_cast<uint2*>(base + kRingBytes + 1024 + 16);  // odd 16-byte slot (see cta_carve)
+    s.tab0 = reinterpret_cast<uint2*>(base + kRingBytes + 1024 + kZeroBytes + 32);
+    s.tab1 = reinterpret_cast<uint2*>(base + kRingBytes + 1024 + kZeroBytes + 32 + tab_bytes);
+    s.oq = reinterpret_cast<float*>(base + kRingBytes + 1024 + kZeroBytes + 32 + (size_t)ntabs * tab_bytes);
     return s;
 }
 
 __host__ __device__ constexpr size_t smem_bytes(int tab_bytes, int ntabs) {
-    // ring, barriers, zero area, ntabs activation tables of tab_bytes = K * 8 bytes, FP2 block offsets
-    // of K / 2 bytes = tab_bytes / 16, alignment slack
-    return (size_t)kRingBytes + 1024 + kZeroBytes + (size_t)tab_bytes * ntabs + tab_bytes / 16 + 128;
+    // ring, barriers, zero area, ntabs activation tables of tab_bytes = K * 8 bytes, offset quads of
+    // K bytes = tab_bytes / 8, alignment slack
+    return (size_t)kRingBytes + 1024 + kZeroBytes + 32 + (size_t)tab_bytes * ntabs + tab_bytes / 8 + 128;
 }
 
 __device__ __forceinline__ Ring warp_ring(const Smem& s, int warp) {
@@ -718,6 +881,7 @@ static_assert(stage_rows(2) == 32 * kWarps && stage_rows(4) * 2 == 16 * kWarps, 
 template <int NS, int SB>
 struct CtaRing {
     static_assert(NS * SB <= kCtaRing && SB % 128 == 0 && NS <= 8, "ring geometry");
+    static constexpr int kBytes = NS * SB;
     uint8_t* slots;
     uint64_t* full;   // arrival count 1 (the producer's expect_tx) + the box's transaction bytes
     uint64_t* empty;  // arrival count kWarps
@@ -754,32 +918,32 @@ struct CtaRing {
 
 struct CtaSmem {
     uint8_t* ring;
-    uint64_t* bars;  // 256 bytes: full[NS], empty[NS]
+    uint64_t* bars;  // 256 bytes: full[NS], empty[NS], then (at bars + 16) the tables' barrier
     uint2* zero;     // kZeroBytes of zeros
     float* red;      // kWarps * 64 floats: cross-warp partial sums
-    uint2* tab[2];   // activation tables
-    float* csum;     // FP2 block offsets, K / 2 bytes
+    uint8_t* tabs;   // activation tables, copied from global memory
+    uint64_t* tbar;
 };
 
 constexpr int kRedBytes = kWarps * 64 * 4;
 
-// ring, barriers, zero area, reduction area, two tables of tab_bytes = K * 8 bytes, FP2 block offsets
-// (tab_bytes / 16), alignment slack
-__host__ __device__ constexpr size_t cta_smem_bytes(int tab_bytes) {
-    return (size_t)kCtaRing + 256 + kZeroBytes + kRedBytes + 2 * (size_t)tab_bytes + tab_bytes / 16 + 128;
+// ring (ring_bytes), barriers, zero area, reduction area, tables (tab_bytes), alignment slack
+__host__ __device__ constexpr size_t cta_smem_bytes(int ring_bytes, int tab_bytes) {
+    return (size_t)ring_bytes + 256 + kZeroBytes + 32 + kRedBytes + (size_t)tab_bytes + 128;
 }
 
-__device__ __forceinline__ CtaSmem cta_carve(uint8_t* raw, int tab_bytes) {
+__device__ __forceinline__ CtaSmem cta_carve(uint8_t* raw, int ring_bytes) {
     uint8_t* base = raw + ((128u - (smem_u32(raw) & 127u)) & 127u);
     CtaSmem s;
-    size_t o = kCtaRing;
+    size_t o = ring_bytes;
     s.ring = base;
     s.bars = reinterpret_cast<uint64_t*>(base + o); o += 256;
-    s.zero = reinterpret_cast<uint2*>(base + o); o += kZeroBytes;
+    s.tbar = s.bars + 16;
+    // the zero area starts 16 bytes past a 32-byte boundary, so the broadcast zero reads of inactive
+    // lanes use other banks than the active lanes' table entries (32-byte aligned)
+    s.zero = reinterpret_cast<uint2*>(base + o + 16); o += kZeroBytes + 32;
     s.red = reinterpret_cast<float*>(base + o); o += kRedBytes;
-    s.tab[0] = reinterpret_cast<uint2*>(base + o); o += tab_bytes;
-    s.tab[1] = reinterpret_cast<uint2*>(base + o); o += tab_bytes;
-    s.csum = reinterpret_cast<float*>(base + o);
+    s.tabs = base + o;  // 32-byte aligned (ring_bytes, the areas above are multiples of 32)
     return s;
 }
 
@@ -788,6 +952,7 @@ __device__ inline CtaRing<NS, SB> cta_init(const CtaSmem& s) {
     CtaRing<NS, SB> R{s.ring, s.bars, s.bars + NS};
     if (threadIdx.x < NS) mbar_init(R.full + threadIdx.x, 1);
     else if (threadIdx.x < 2 * NS) mbar_init(R.empty + (threadIdx.x - NS), kWarps);
+    else if (threadIdx.x == 2 * NS) mbar_init(s.tbar, 1);
     for (int i = threadIdx.x; i < kZeroBytes / 16; i += blockDim.x) reinterpret_cast<uint4*>(s.zero)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_barrier_init();
     __syncthreads();

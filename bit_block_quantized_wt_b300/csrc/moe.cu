@@ -10,9 +10,10 @@
 // zero-weight term is ever added) and then the shared expert; the stack's layer input is the
 // bfloat16 RMS normalisation (eps 1e-6, no gain) of a binary32 residual.
 //
-// Per layer four kernels, each launched to overlap the previous one's tail: k_router (normalise,
-// router GEMV; its last CTA routes every token), k_gate_up (gate/up on the tensor cores), k_down
-// (h = silu(g) u, down projection on the tensor cores) and k_combine (weighted sum per token).
+// Per layer five kernels, each launched to overlap the previous one's tail: k_router (normalise,
+// router GEMV, gate/up activation tables; its last CTA routes every token), k_gate_up (gate/up on the
+// tensor cores), k_hpack (h = silu(g) u and the down activation tables), k_down (down projection on
+// the tensor cores) and k_combine (weighted sum per token).
 #include "fpx_mma.cuh"
 
 using namespace fpx;
@@ -34,7 +35,7 @@ __device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontro
 // ------------------------------------------------------------------ workspace
 
 struct Ws {
-    size_t status, logits, u, idx, w, uni, nuni, gu, yi, total;
+    size_t status, logits, u, idx, w, uni, nuni, gu, yi, gt, dt, total;
     size_t gu_half, yi_half;  // floats between the two K-split partial buffers
 };
 
@@ -54,6 +55,8 @@ inline Ws ws_layout(int H, int I, int E, int q, int k) {
     w.yi_half = (size_t)(q * k + 1) * q * H;
     w.gu = o; o = up16(o + sizeof(float) * 2 * w.gu_half);
     w.yi = o; o = up16(o + sizeof(float) * 2 * w.yi_half);
+    w.gt = o; o = up16(o + tset_bytes(H));
+    w.dt = o; o = up16(o + (size_t)(q * k + 1) * tset_bytes(I));
     w.total = o;
     return w;
 }
@@ -69,6 +72,8 @@ struct WsPtrs {
     float* gu;  // g and u of every item: [K half][2 * item + (0 | 1)][q][I]
     float* yi;  // per-item outputs [K half][item][q][H]
     size_t gu_half, yi_half;
+    uint8_t* gt;  // gate/up activation tables (table set for K = H), built by the router kernel
+    uint8_t* dt;  // down activation tables, one table set for K = I per item, built by k_hpack
 };
 
 inline WsPtrs ws_ptrs(void* ws, const Ws& l) {
@@ -78,7 +83,8 @@ inline WsPtrs ws_ptrs(void* ws, const Ws& l) {
                   reinterpret_cast<float*>(b + l.w),        reinterpret_cast<int32_t*>(b + l.uni),
                   reinterpret_cast<int32_t*>(b + l.nuni),   reinterpret_cast<float*>(b + l.gu),
                   reinterpret_cast<float*>(b + l.yi),       l.gu_half,
-                  l.yi_half};
+                  l.yi_half,                                reinterpret_cast<uint8_t*>(b + l.gt),
+                  reinterpret_cast<uint8_t*>(b + l.dt)};
 }
 
 // Everything the gate/up and down kernels need about one layer: tensor maps over the stacked
@@ -326,6 +332,54 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
         }
     }
     __syncthreads();
+    if (A.k > 0) {
+        // the gate/up activation tables (FP2, FP4, offsets) of u: every CTA has all of u, computes the
+        // column shifts and packs its slice of the code groups into the global table set
+        __shared__ int sh_s[kMaxQ];
+        float m[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
+        for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+            const uint2 pk = reinterpret_cast<const uint2*>(u_s)[i];
+            const float mm = fmaxf(fmaxf(fabsf(__uint_as_float(pk.x << 16)), fabsf(__uint_as_float(pk.x & 0xFFFF0000u))),
+                                   fmaxf(fabsf(__uint_as_float(pk.y << 16)), fabsf(__uint_as_float(pk.y & 0xFFFF0000u))));
+            const int t = i * 4 / H;
+#pragma unroll
+            for (int tt = 0; tt < kMaxQ; tt++) m[tt] = tt == t ? fmaxf(m[tt], mm) : m[tt];
+        }
+#pragma unroll
+        for (int tt = 0; tt < kMaxQ; tt++) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m[tt] = fmaxf(m[tt], __shfl_xor_sync(0xffffffffu, m[tt], o));
+        }
+        if (lane == 0)
+#pragma unroll
+            for (int tt = 0; tt < kMaxQ; tt++) red[warp][tt] = m[tt];
+        __syncthreads();
+        if (threadIdx.x < kMaxQ) {
+            float mm = 0.f;
+            for (int w = 0; w < kRouterThreads / 32; w++) mm = fmaxf(mm, red[w][threadIdx.x]);
+            sh_s[threadIdx.x] = column_shift(mm);
+            if (blockIdx.x == 0) reinterpret_cast<int*>(A.ws.gt + tset_copy_bytes(H))[threadIdx.x] = sh_s[threadIdx.x];
+        }
+        __syncthreads();
+        // 4 token slots x H / 16 groups; this CTA's slice has an even length, so the two groups of a
+        // block sit on lanes (2i, 2i + 1) of warp 0; absent tokens get zero entries
+        const int ngr = 4 * H / 16, per = (((ngr + (int)gridDim.x - 1) / (int)gridDim.x) + 1) & ~1;
+        const int gs = blockIdx.x * per;
+        if (warp == 0)
+            for (int gb = gs; gb < gs + per && gb < ngr; gb += 32) {
+                const int gi = gb + lane;
+                const bool valid = gi < ngr && gi < gs + per;
+                const int tok = valid ? gi * 16 / H : 0, k0 = valid ? gi * 16 - tok * H : 0;
+                float part = 0.f;
+                if (valid) {
+                    float v[16];
+#pragma unroll
+                    for (int j = 0; j < 16; j++) v[j] = tok < q ? __uint_as_float((uint32_t)u_s[(size_t)tok * H + k0 + j] << 16) : 0.f;
+                    part = pack_group<2>(A.ws.gt, H, tok, k0, v, sh_s[tok]);
+                }
+                add_offsets(A.ws.gt, H, tok, k0, part, valid);
+            }
+    }
     float acc[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
     if (e < E) {
         for (int base = g0 + lane; base < g1; base += 4 * 32) {
@@ -451,10 +505,12 @@ struct GateUpArgs {
 };
 
 // Ring geometry of the two layer kernels: 7 slots of one FP2 box, 5 slots of one FP3 box (an FP4
-// box, 17 KB, fits either).
-constexpr int kGuNS = 7, kDnNS = 5;
+// box, 17 KB, fits either). The down kernel holds four tables of I * 8 bytes; for I > 2048 it runs
+// with a 2-slot ring so that they fit.
+constexpr int kGuNS = 7;
 using GuRing = CtaRing<kGuNS, stage_bytes(2)>;
-using DnRing = CtaRing<kDnNS, stage_bytes(3)>;
+template <int NS>
+using DnRing = CtaRing<NS, stage_bytes(3)>;
 static_assert(stage_bytes(4) <= stage_bytes(2), "FP4 box fits a slot");
 
 struct GuTask {
@@ -504,20 +560,23 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ Route r;
     __shared__ int shift[kMaxQ];
-    __shared__ float red4[kWarps * 4];
     const int H = A.m.H, I = A.m.I;
-    const CtaSmem S = cta_carve(smem, btab_bytes(H));
+    const CtaSmem S = cta_carve(smem, GuRing::kBytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const GuRing R = cta_init<kGuNS, stage_bytes(2)>(S);
-    grid_dep_wait();  // routing and u come from the router kernel
-    grid_dep_trigger();  // after the wait: the down kernel reads the router's output before its own
+    grid_dep_wait();     // routing and the activation tables come from the router kernel
+    grid_dep_trigger();  // after the wait: the later kernels read the router's output before their own
+    if (threadIdx.x == 0) {
+        mbar_expect_tx(S.tbar, tset_copy_bytes(H));
+        bulk_load(S.tabs, A.ws.gt, tset_copy_bytes(H), S.tbar);
+    }
     load_route(r, A.ws, Q * A.k);
 
     const int ks = k_split(H, 2);
     int c0, c1;
     task_range(2 * r.n_uni * (I / 256) * ks, (H / stage_k(2) / ks) * kCostFP2, 2 * (I / 64), (H / stage_k(4)) * kCostFP4, c0, c1);
 
-    if (warp == kWarps) {  // producer: streams the range's boxes while the consumers build tables
+    if (warp == kWarps) {  // producer: streams the range's boxes while the consumers load the tables
         if (lane == 0) {
             uint32_t issued = 0;
             for (int tk = c0; tk < c1; tk++) {
@@ -532,16 +591,21 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
         return;
     }
 
-    // activation tables: x scaled per token, FP2 (pair-shifted, with block offsets) and FP4
-    build_tables<2, 4, true>(SrcBF16{A.x}, H, Q, S.tab[0], S.tab[1], S.csum, shift, red4);
+    // activation tables (FP2 with block offsets, FP4), copied from the router kernel's table set
+    if (threadIdx.x < kMaxQ) shift[threadIdx.x] = __ldcg(reinterpret_cast<const int*>(A.ws.gt + tset_copy_bytes(H)) + threadIdx.x);
+    bool ok = __any_sync(0xffffffffu, mbar_wait(S.tbar, 0));
+    if (!ok && lane == 0) flag(A.ws.status, FPX_ETIMEOUT);
     consumers_sync();
+    const uint2* tab2 = reinterpret_cast<const uint2*>(S.tabs);
+    const uint2* tab4 = reinterpret_cast<const uint2*>(S.tabs + btab_bytes(H));
+    const float* oq2 = reinterpret_cast<const float*>(S.tabs + 2 * btab_bytes(H));
 
     // Every consumer warp runs the same sequence of consumer barriers whether or not a wait timed
     // out, so a timeout never leaves a barrier short of arrivals.
     const int a_idx = b_active_index(lane);
     const uint32_t magic = A.magic;
+    const LaneOfs L2 = lane_ofs<2>(t), L4 = lane_ofs<4>(t);
     uint32_t n = 0, bad = 0;
-    bool ok = true;
     for (int tk = c0; tk < c1; tk++) {
         const GuTask k = gu_task(tk, r, H, I, ks);
         float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -551,12 +615,12 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
             const uint8_t* slot = R.slot(n);
             if (!k.fp4) {
                 const int ch0 = (k.kpart * k.ns + s) * box_chunks(2);
-                box_tiles<2, 2, box_chunks(2)>(slot + (warp * 32 + g) * box_bytes(2), lane_tab(S.tab[0], S.zero, a_idx, ch0),
-                                               lane_csum(S.csum, ch0, t), t, magic, y, bad);
+                box_tiles<2, 2, box_chunks(2)>(smem_u32(slot) + (warp * 32 + g) * box_bytes(2), L2,
+                                               lane_tab(tab2, S.zero, a_idx, ch0), 0u, lane_oq(oq2, ch0, t), magic, y, bad);
             } else {
                 const int ch0 = s * box_chunks(4) + 4 * (warp >> 2);
-                box_tiles<4, 1, 4>(slot + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4),
-                                   lane_tab(S.tab[1], S.zero, a_idx, ch0), nullptr, t, magic,
+                box_tiles<4, 1, 4>(smem_u32(slot) + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4), L4,
+                                   lane_tab(tab4, S.zero, a_idx, ch0), 0u, 0u, magic,
                                    *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
             }
             R.release(n);
@@ -580,6 +644,90 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
         }
     }
     report_bad(bad, A.ws.status);
+}
+
+// ------------------------------------------------------------------ K2b: h and the down tables
+
+// One CTA per union item (and one for the shared expert): h = silu(g) u over the item's I rows for
+// every token (the K parts of g and u added first), the column shifts of h, and the down activation
+// table set (FP3 planes with block offsets; FP4 for the shared expert) in global memory.
+struct HpackArgs {
+    int I, k, ks;  // ks: K parts of the routed gate/up outputs
+    WsPtrs ws;
+};
+
+constexpr int kHpackThreads = 512;
+
+template <int Q>
+__global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__ HpackArgs A) {
+    extern __shared__ __align__(16) float h_s[];  // [Q][I]
+    __shared__ float red[kHpackThreads / 32][kMaxQ];
+    __shared__ int sh_s[kMaxQ];
+    grid_dep_trigger();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int I = A.I, j = blockIdx.x;
+    const int n_uni = __ldcg(A.ws.nuni);  // the router kernel's (completed before the gate/up kernel ran)
+    if (j > n_uni) return;
+    grid_dep_wait();  // g and u come from the gate/up kernel
+    const float* g = A.ws.gu + (size_t)(2 * j) * Q * I;
+    const float* u = g + (size_t)Q * I;
+    const size_t part2 = j < n_uni && A.ks == 2 ? A.ws.gu_half : 0;
+    float m[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
+    for (int e = threadIdx.x; e < Q * I / 4; e += blockDim.x) {
+        float4 a = __ldcg(reinterpret_cast<const float4*>(g) + e), b = __ldcg(reinterpret_cast<const float4*>(u) + e);
+        if (part2) {
+            const float4 a2 = __ldcg(reinterpret_cast<const float4*>(g + part2) + e);
+            const float4 b2 = __ldcg(reinterpret_cast<const float4*>(u + part2) + e);
+            a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
+            b.x += b2.x; b.y += b2.y; b.z += b2.z; b.w += b2.w;
+        }
+        float4 h;
+        h.x = (a.x / (1.0f + expf(-a.x))) * b.x;
+        h.y = (a.y / (1.0f + expf(-a.y))) * b.y;
+        h.z = (a.z / (1.0f + expf(-a.z))) * b.z;
+        h.w = (a.w / (1.0f + expf(-a.w))) * b.w;
+        reinterpret_cast<float4*>(h_s)[e] = h;
+        const float mm = fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w)));
+        const int t = e * 4 / I;
+#pragma unroll
+        for (int tt = 0; tt < kMaxQ; tt++) m[tt] = tt == t ? fmaxf(m[tt], mm) : m[tt];
+    }
+#pragma unroll
+    for (int tt = 0; tt < kMaxQ; tt++) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m[tt] = fmaxf(m[tt], __shfl_xor_sync(0xffffffffu, m[tt], o));
+    }
+    if (lane == 0)
+#pragma unroll
+        for (int tt = 0; tt < kMaxQ; tt++) red[warp][tt] = m[tt];
+    __syncthreads();
+    uint8_t* ts = A.ws.dt + (size_t)j * tset_bytes(I);
+    if (threadIdx.x < kMaxQ) {
+        float mm = 0.f;
+        for (int w = 0; w < kHpackThreads / 32; w++) mm = fmaxf(mm, red[w][threadIdx.x]);
+        sh_s[threadIdx.x] = column_shift(mm);
+        reinterpret_cast<int*>(ts + tset_copy_bytes(I))[threadIdx.x] = sh_s[threadIdx.x];
+    }
+    __syncthreads();
+    // 4 token slots x I / 16 groups; the two groups of a block sit on lanes (2i, 2i + 1); absent tokens
+    // get zero entries
+    const int ngr = 4 * I / 16;
+    for (int gb = warp * 32; gb < ngr; gb += kHpackThreads) {
+        const int gi = gb + lane;
+        const bool valid = gi < ngr;
+        const int tok = valid ? gi * 16 / I : 0, k0 = valid ? gi * 16 - tok * I : 0;
+        float part = 0.f;
+        if (valid) {
+            float v[16];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; q4++) {
+                const float4 f = tok < Q ? reinterpret_cast<const float4*>(h_s + (size_t)tok * I + k0)[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[4 * q4] = f.x; v[4 * q4 + 1] = f.y; v[4 * q4 + 2] = f.z; v[4 * q4 + 3] = f.w;
+            }
+            part = j < n_uni ? pack_group<3>(ts, I, tok, k0, v, sh_s[tok]) : pack_group<4>(ts, I, tok, k0, v, sh_s[tok]);
+        }
+        if (j < n_uni) add_offsets(ts, I, tok, k0, part, valid);  // CTA-uniform condition
+    }
 }
 
 // ------------------------------------------------------------------ K3: down + combine
@@ -635,18 +783,17 @@ __device__ __forceinline__ void dn_issue(const DownArgs& A, const DnTask& k, int
     }
 }
 
-template <int Q, int MODE>
+template <int Q, int MODE, int NS>
 __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__ DownArgs A) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ Route r;
     __shared__ int shift[2][kMaxQ];
-    __shared__ float red4[kWarps * 4];
     const int H = A.m.H, I = A.m.I;
-    const CtaSmem S = cta_carve(smem, btab_bytes(I));
+    const CtaSmem S = cta_carve(smem, DnRing<NS>::kBytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const DnRing R = cta_init<kDnNS, stage_bytes(3)>(S);
+    const DnRing<NS> R = cta_init<NS, stage_bytes(3)>(S);
     // the routing comes from the router kernel, which completed before the gate/up kernel passed its
-    // own grid_dep_wait(); the weights do not depend on the gate/up kernel either, so the producer
+    // own grid_dep_wait(); the weights do not depend on the kernels in between either, so the producer
     // starts streaming before grid_dep_wait()
     grid_dep_trigger();
     load_route(r, A.ws, Q * A.k);
@@ -661,7 +808,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
         return;
     }
 
-    if (warp == kWarps) {  // producer: streams the range's boxes while the consumers build tables
+    if (warp == kWarps) {  // producer: streams the range's boxes while the consumers load the tables
         if (lane == 0) {
             uint32_t issued = 0;
             for (int tk = c0; tk < c1; tk++) {
@@ -676,29 +823,36 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
         return;
     }
 
-    // activation tables for the (at most two) items of this CTA's range: h = silu(g) u, the K parts
-    // of g and u added first (the shared expert has one part)
+    // activation tables of the (at most two) items of this CTA's range, built by k_hpack
     grid_dep_wait();
-    for (int sl = 0; sl <= item_hi - item_lo; sl++) {
-        const int item = item_lo + sl;
-        const size_t part2 = item < r.n_uni && k_split(H, 2) == 2 ? A.ws.gu_half : 0;
-        const SrcSilu src{A.ws.gu + (size_t)(2 * item) * Q * I, A.ws.gu + (size_t)(2 * item + 1) * Q * I, part2};
-        uint2* tab = sl ? S.tab[1] : S.tab[0];
-        if (item == r.n_uni) build_tables<4, 0, true>(src, I, Q, tab, nullptr, nullptr, shift[sl], red4);
-        else build_tables<3, 0, true>(src, I, Q, tab, nullptr, nullptr, shift[sl], red4);
-        consumers_sync();
+    const int nit = item_hi - item_lo + 1;
+    if (threadIdx.x == 0) {
+        mbar_expect_tx(S.tbar, nit * tset_copy_bytes(I));
+        for (int sl = 0; sl < nit; sl++)
+            bulk_load(S.tabs + (size_t)sl * tset_copy_bytes(I), A.ws.dt + (size_t)(item_lo + sl) * tset_bytes(I), tset_copy_bytes(I),
+                      S.tbar);
     }
+    if (threadIdx.x < 2 * kMaxQ) {
+        const int sl = threadIdx.x / kMaxQ, tk = threadIdx.x % kMaxQ;
+        shift[sl][tk] = sl < nit ? __ldcg(reinterpret_cast<const int*>(A.ws.dt + (size_t)(item_lo + sl) * tset_bytes(I) + tset_copy_bytes(I)) + tk) : 0;
+    }
+    bool ok = __any_sync(0xffffffffu, mbar_wait(S.tbar, 0));
+    if (!ok && lane == 0) flag(A.ws.status, FPX_ETIMEOUT);
+    consumers_sync();
 
     // Every consumer warp runs the same sequence of consumer barriers whether or not a wait timed
     // out, so a timeout never leaves a barrier short of arrivals.
     const int a_idx = b_active_index(lane);
     const uint32_t magic = A.magic;
+    const LaneOfs L3 = lane_ofs<3>(t), L4 = lane_ofs<4>(t);
     uint32_t n = 0, bad = 0;
-    bool ok = true;
     for (int tk = c0; tk < c1; tk++) {
         const DnTask k = dn_task(tk, r, H, I, ks);
         const int sl = k.item - item_lo;
-        const uint2* tab = sl ? S.tab[1] : S.tab[0];
+        const uint8_t* ts = S.tabs + (size_t)sl * tset_copy_bytes(I);
+        const uint2* tlo = reinterpret_cast<const uint2*>(ts);
+        const uint2* thi = reinterpret_cast<const uint2*>(ts + btab_bytes(I));
+        const float* oq = reinterpret_cast<const float*>(ts + 2 * btab_bytes(I));
         float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         for (int s = 0; s < k.ns; s++, n++) {
             if (ok) ok = R.wait(n, A.ws.status);
@@ -706,12 +860,12 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
             const uint8_t* slot = R.slot(n);
             if (!k.fp4) {
                 const int ch0 = (k.kpart * k.ns + s) * box_chunks(3);
-                box_tiles<3, 2, box_chunks(3)>(slot + (warp * 32 + g) * box_bytes(3), lane_tab(tab, S.zero, a_idx, ch0), nullptr,
-                                               t, magic, y, bad);
+                box_tiles<3, 2, box_chunks(3)>(smem_u32(slot) + (warp * 32 + g) * box_bytes(3), L3, lane_tab(tlo, S.zero, a_idx, ch0),
+                                               lane_tab(thi, S.zero, a_idx, ch0), lane_oq(oq, ch0, t), magic, y, bad);
             } else {
                 const int ch0 = s * box_chunks(4) + 4 * (warp >> 2);
-                box_tiles<4, 1, 4>(slot + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4),
-                                   lane_tab(tab, S.zero, a_idx, ch0), nullptr, t, magic,
+                box_tiles<4, 1, 4>(smem_u32(slot) + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4), L4,
+                                   lane_tab(tlo, S.zero, a_idx, ch0), 0u, 0u, magic,
                                    *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
             }
             R.release(n);
@@ -749,6 +903,7 @@ struct CombineArgs {
 };
 
 constexpr int kCombineThreads = 256;
+constexpr int kKernelsPerLayer = 5;  // router, gate/up, h + down tables, down, combine
 
 template <int Q, int MODE>
 __global__ void __launch_bounds__(kCombineThreads) k_combine(const __grid_constant__ CombineArgs A) {
@@ -808,13 +963,17 @@ int check_layer(const moe_layer* L) {
     if (!aligned(L->router, 16) || !aligned(L->gate, 16) || !aligned(L->up, 16) || !aligned(L->down, 16) ||
         !aligned(L->sh_gate, 16) || !aligned(L->sh_up, 16) || !aligned(L->sh_down, 16))
         return FPX_EALIGN;
-    if (cta_smem_bytes(btab_bytes(L->H > L->I ? L->H : L->I)) + 2048 > 227 * 1024) return FPX_EINVAL;  // + static smem
+    // shared memory (plus up to 2 KB of static): gate/up ring + one table set for K = H; down ring
+    // (2 slots at least) + two table sets for K = I
+    if (cta_smem_bytes(GuRing::kBytes, tset_copy_bytes(L->H)) + 2048 > 227 * 1024 ||
+        cta_smem_bytes(DnRing<2>::kBytes, 2 * tset_copy_bytes(L->I)) + 2048 > 227 * 1024)
+        return FPX_EINVAL;
     return FPX_OK;
 }
 
 struct Plan {
-    int g_router, g_gate, g_down, g_comb;
-    size_t sm_router, sm_gate, sm_down;
+    int g_router, g_gate, g_down, g_comb, ns_down;
+    size_t sm_router, sm_gate, sm_down, sm_hpack;
 };
 
 Plan make_plan(const moe_layer& L, int q) {
@@ -823,9 +982,11 @@ Plan make_plan(const moe_layer& L, int q) {
     p.g_router = (L.E + 1) / 2;
     p.sm_router = sizeof(uint16_t) * (size_t)q * L.H;
     p.g_gate = di.sms;
-    p.sm_gate = cta_smem_bytes(btab_bytes(L.H));
+    p.sm_gate = cta_smem_bytes(GuRing::kBytes, tset_copy_bytes(L.H));
     p.g_down = di.sms > kMinDownCtas ? di.sms : kMinDownCtas;
-    p.sm_down = cta_smem_bytes(btab_bytes(L.I));
+    p.ns_down = cta_smem_bytes(DnRing<5>::kBytes, 2 * tset_copy_bytes(L.I)) + 2048 <= 227 * 1024 ? 5 : 2;
+    p.sm_down = cta_smem_bytes(p.ns_down == 5 ? DnRing<5>::kBytes : DnRing<2>::kBytes, 2 * tset_copy_bytes(L.I));
+    p.sm_hpack = sizeof(float) * (size_t)q * L.I;
     p.g_comb = (q * L.H + kCombineThreads - 1) / kCombineThreads;
     return p;
 }
@@ -871,9 +1032,13 @@ int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, co
     ra.status_to_clear = clear ? ws.status : nullptr;
     ra.ws = ws;
     ra.idx_out = idx_out; ra.w_out = w_out; ra.logits_out = logits_out;
-    if (cudaFuncSetAttribute(k_router<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_router) ||
+    auto kdown = p.ns_down == 5 ? k_down<Q, MODE, 5> : k_down<Q, MODE, 2>;
+    HpackArgs ha{};
+    ha.I = L.I; ha.k = k; ha.ks = (L.H / stage_k(2)) % 2 == 0 ? 2 : 1; ha.ws = ws;
+    if (cudaFuncSetAttribute(k_hpack<Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_hpack) ||
+        cudaFuncSetAttribute(k_router<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_router) ||
         cudaFuncSetAttribute(k_gate_up<Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_gate) ||
-        cudaFuncSetAttribute(k_down<Q, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_down))
+        cudaFuncSetAttribute(kdown, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_down))
         return FPX_ECUDA;
     CombineArgs ca{};
     ca.H = L.H; ca.k = k; ca.ws = ws; ca.ks = (L.I / stage_k(3)) % 2 == 0 ? 2 : 1; ca.out = out;
@@ -885,8 +1050,10 @@ int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, co
     if (ev) cudaEventRecord(ev[1], s);
     e = e ? e : launch(k_gate_up<Q>, p.g_gate, kCtaThreads, p.sm_gate, s, pdl, ga);
     if (ev) cudaEventRecord(ev[2], s);
-    e = e ? e : launch(k_down<Q, MODE>, p.g_down, kCtaThreads, p.sm_down, s, pdl, da);
+    e = e ? e : launch(k_hpack<Q>, Q * k + 1, kHpackThreads, p.sm_hpack, s, pdl, ha);
     if (ev) cudaEventRecord(ev[3], s);
+    e = e ? e : launch(kdown, p.g_down, kCtaThreads, p.sm_down, s, pdl, da);
+    if (ev) cudaEventRecord(ev[4], s);
     e = e ? e : launch(k_combine<Q, MODE>, p.g_comb, kCombineThreads, 0, s, pdl, ca);
     return e == cudaSuccess ? launch_status() : FPX_ECUDA;
 }
@@ -968,11 +1135,11 @@ int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int
     for (int l = 0; l < n_layers; l++) {
         int32_t* io = idx_out ? idx_out + (size_t)l * q * k : nullptr;
         float* tr = r_trace ? r_trace + (size_t)l * q * layers[0].H : nullptr;
-        cudaEvent_t const* ev = events ? reinterpret_cast<cudaEvent_t const*>(events) + 4 * l : nullptr;
+        cudaEvent_t const* ev = events ? reinterpret_cast<cudaEvent_t const*>(events) + kKernelsPerLayer * l : nullptr;
         int st = dispatch_q<1>(q, layers[l], p, k, nullptr, rL, rL, io, nullptr, nullptr, tr, wp, l == 0, ev, l > 0, s);
         if (st) return st;
     }
-    if (events && cudaEventRecord(reinterpret_cast<cudaEvent_t const*>(events)[4 * n_layers], s) != cudaSuccess)
+    if (events && cudaEventRecord(reinterpret_cast<cudaEvent_t const*>(events)[kKernelsPerLayer * n_layers], s) != cudaSuccess)
         return FPX_ECUDA;
     return FPX_OK;
 }

@@ -164,12 +164,12 @@ int moe_layer_decode_static_ws(const moe_layer* layer, const uint16_t* x, int q,
  * E): state r binary32 [q][H] starts at r0; layer l takes u_l = RN_bfloat16(r_l / sqrt(mean(r_l^2)
  * + 1e-6)) and sets r_{l+1} = r_l + MoE_l(u_l). rL receives r_{n_layers}; r0 and rL may alias.
  * idx_out (nullable) gets idx[n_layers][q][k]; r_trace (nullable) gets r_l for l = 0..n_layers-1
- * ([n_layers][q][H]). Enqueues two small memsets and then 4 kernels per layer (router, gate/up, down,
- * combine), each launched as a programmatic dependent launch so that it overlaps the previous
- * kernel's tail, and nothing else, so the whole pass can be captured as one CUDA graph. events
- * (nullable) is a host array of 4*n_layers + 1 cudaEvent_t: events[4l + j] is recorded on `stream`
- * just before kernel j of layer l and events[4*n_layers] after the last kernel, so a caller can time
- * each kernel (with events the kernels run without overlap).
+ * ([n_layers][q][H]). Enqueues a copy and a small memset and then 5 kernels per layer (router,
+ * gate/up, h + down tables, down, combine), each launched as a programmatic dependent launch so that
+ * it overlaps the previous kernel's tail, and nothing else, so the whole pass can be captured as one
+ * CUDA graph. events (nullable) is a host array of 5*n_layers + 1 cudaEvent_t: events[5l + j] is
+ * recorded on `stream` just before kernel j of layer l and events[5*n_layers] after the last kernel,
+ * so a caller can time each kernel (with events the kernels run without overlap).
  * The normalisation is this project's reading (the pages do not define the residual stream):
  * without it the synthetic state overflows binary32 within a few dozen layers.
  * [P-dsv4] paragraph 3 (43 layers; every token streams the active weights of all layers). */
