@@ -170,7 +170,7 @@ def moe_layer_decode_static_ws(layer, x, q, k, y, idx_out=None, w_out=None, logi
 
 def moe_stack_verify(layers, r0, q, k, rL, ws, ws_bytes, idx_out=None, r_trace=None, events=None,
                      stream=None):
-    """events: optional list of 3*len(layers)+1 raw cudaEvent_t handles (ints), recorded before each
+    """events: optional list of 5*len(layers)+1 raw cudaEvent_t handles (ints), recorded before each
     kernel and after the last one."""
     arr = (moe_layer * len(layers))(*layers)
     ev = None

@@ -648,83 +648,87 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
 
 // ------------------------------------------------------------------ K2b: h and the down tables
 
-// One CTA per union item (and one for the shared expert): h = silu(g) u over the item's I rows for
-// every token (the K parts of g and u added first), the column shifts of h, and the down activation
-// table set (FP3 planes with block offsets; FP4 for the shared expert) in global memory.
+// One CTA per (union item or shared expert, token slot): h = silu(g) u over the item's I rows for the
+// token (the K parts of g and u added first), its column shift, and that token's entries of the item's
+// down activation table set (FP3 planes with block offsets; FP4 for the shared expert) in global
+// memory. Token slots >= q get zero entries.
 struct HpackArgs {
     int I, k, ks;  // ks: K parts of the routed gate/up outputs
     WsPtrs ws;
 };
 
 constexpr int kHpackThreads = 512;
+constexpr int kHpackV = 4;  // float4 groups per thread, all loaded at once: I <= 4 * 4 * 512
 
 template <int Q>
 __global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__ HpackArgs A) {
-    extern __shared__ __align__(16) float h_s[];  // [Q][I]
-    __shared__ float red[kHpackThreads / 32][kMaxQ];
-    __shared__ int sh_s[kMaxQ];
+    __shared__ __align__(16) float h_s[kHpackV * 4 * kHpackThreads];  // [I]
+    __shared__ float red[kHpackThreads / 32];
+    __shared__ int sh_s;
     grid_dep_trigger();
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    const int I = A.I, j = blockIdx.x;
+    const int I = A.I, j = blockIdx.x / 4, tok = blockIdx.x % 4;
     const int n_uni = __ldcg(A.ws.nuni);  // the router kernel's (completed before the gate/up kernel ran)
     if (j > n_uni) return;
-    grid_dep_wait();  // g and u come from the gate/up kernel
-    const float* g = A.ws.gu + (size_t)(2 * j) * Q * I;
-    const float* u = g + (size_t)Q * I;
-    const size_t part2 = j < n_uni && A.ks == 2 ? A.ws.gu_half : 0;
-    float m[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
-    for (int e = threadIdx.x; e < Q * I / 4; e += blockDim.x) {
-        float4 a = __ldcg(reinterpret_cast<const float4*>(g) + e), b = __ldcg(reinterpret_cast<const float4*>(u) + e);
-        if (part2) {
-            const float4 a2 = __ldcg(reinterpret_cast<const float4*>(g + part2) + e);
-            const float4 b2 = __ldcg(reinterpret_cast<const float4*>(u + part2) + e);
-            a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
-            b.x += b2.x; b.y += b2.y; b.z += b2.z; b.w += b2.w;
-        }
-        float4 h;
-        h.x = (a.x / (1.0f + expf(-a.x))) * b.x;
-        h.y = (a.y / (1.0f + expf(-a.y))) * b.y;
-        h.z = (a.z / (1.0f + expf(-a.z))) * b.z;
-        h.w = (a.w / (1.0f + expf(-a.w))) * b.w;
-        reinterpret_cast<float4*>(h_s)[e] = h;
-        const float mm = fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w)));
-        const int t = e * 4 / I;
-#pragma unroll
-        for (int tt = 0; tt < kMaxQ; tt++) m[tt] = tt == t ? fmaxf(m[tt], mm) : m[tt];
-    }
-#pragma unroll
-    for (int tt = 0; tt < kMaxQ; tt++) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m[tt] = fmaxf(m[tt], __shfl_xor_sync(0xffffffffu, m[tt], o));
-    }
-    if (lane == 0)
-#pragma unroll
-        for (int tt = 0; tt < kMaxQ; tt++) red[warp][tt] = m[tt];
-    __syncthreads();
     uint8_t* ts = A.ws.dt + (size_t)j * tset_bytes(I);
-    if (threadIdx.x < kMaxQ) {
+    float m = 0.f;
+    if (tok < Q) {
+        grid_dep_wait();  // g and u come from the gate/up kernel
+        const float4* g = reinterpret_cast<const float4*>(A.ws.gu + ((size_t)(2 * j) * Q + tok) * I);
+        const float4* u = reinterpret_cast<const float4*>(A.ws.gu + ((size_t)(2 * j + 1) * Q + tok) * I);
+        const size_t p2 = (j < n_uni && A.ks == 2 ? A.ws.gu_half : 0) / 4;
+        float4 ga[kHpackV], ua[kHpackV], gb[kHpackV], ub[kHpackV];
+#pragma unroll
+        for (int v = 0; v < kHpackV; v++) {
+            const int e = threadIdx.x + v * kHpackThreads;
+            const bool in = e < I / 4;
+            ga[v] = in ? __ldcg(g + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ua[v] = in ? __ldcg(u + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            gb[v] = in && p2 ? __ldcg(g + p2 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ub[v] = in && p2 ? __ldcg(u + p2 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int v = 0; v < kHpackV; v++) {
+            const int e = threadIdx.x + v * kHpackThreads;
+            if (e < I / 4) {
+                const float a[4] = {ga[v].x + gb[v].x, ga[v].y + gb[v].y, ga[v].z + gb[v].z, ga[v].w + gb[v].w};
+                const float b[4] = {ua[v].x + ub[v].x, ua[v].y + ub[v].y, ua[v].z + ub[v].z, ua[v].w + ub[v].w};
+                float h[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    h[i] = (a[i] / (1.0f + expf(-a[i]))) * b[i];
+                    m = fmaxf(m, fabsf(h[i]));
+                }
+                reinterpret_cast<float4*>(h_s)[e] = make_float4(h[0], h[1], h[2], h[3]);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
         float mm = 0.f;
-        for (int w = 0; w < kHpackThreads / 32; w++) mm = fmaxf(mm, red[w][threadIdx.x]);
-        sh_s[threadIdx.x] = column_shift(mm);
-        reinterpret_cast<int*>(ts + tset_copy_bytes(I))[threadIdx.x] = sh_s[threadIdx.x];
+        for (int w = 0; w < kHpackThreads / 32; w++) mm = fmaxf(mm, red[w]);
+        sh_s = column_shift(mm);
+        reinterpret_cast<int*>(ts + tset_copy_bytes(I))[tok] = sh_s;
     }
     __syncthreads();
-    // 4 token slots x I / 16 groups; the two groups of a block sit on lanes (2i, 2i + 1); absent tokens
-    // get zero entries
-    const int ngr = 4 * I / 16;
+    // this token's I / 16 groups; the two groups of a block sit on lanes (2i, 2i + 1)
+    const int ngr = I / 16;
     for (int gb = warp * 32; gb < ngr; gb += kHpackThreads) {
         const int gi = gb + lane;
         const bool valid = gi < ngr;
-        const int tok = valid ? gi * 16 / I : 0, k0 = valid ? gi * 16 - tok * I : 0;
+        const int k0 = valid ? gi * 16 : 0;
         float part = 0.f;
         if (valid) {
             float v[16];
 #pragma unroll
             for (int q4 = 0; q4 < 4; q4++) {
-                const float4 f = tok < Q ? reinterpret_cast<const float4*>(h_s + (size_t)tok * I + k0)[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 f = tok < Q ? reinterpret_cast<const float4*>(h_s + k0)[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
                 v[4 * q4] = f.x; v[4 * q4 + 1] = f.y; v[4 * q4 + 2] = f.z; v[4 * q4 + 3] = f.w;
             }
-            part = j < n_uni ? pack_group<3>(ts, I, tok, k0, v, sh_s[tok]) : pack_group<4>(ts, I, tok, k0, v, sh_s[tok]);
+            part = j < n_uni ? pack_group<3>(ts, I, tok, k0, v, sh_s) : pack_group<4>(ts, I, tok, k0, v, sh_s);
         }
         if (j < n_uni) add_offsets(ts, I, tok, k0, part, valid);  // CTA-uniform condition
     }
@@ -973,7 +977,7 @@ int check_layer(const moe_layer* L) {
 
 struct Plan {
     int g_router, g_gate, g_down, g_comb, ns_down;
-    size_t sm_router, sm_gate, sm_down, sm_hpack;
+    size_t sm_router, sm_gate, sm_down;
 };
 
 Plan make_plan(const moe_layer& L, int q) {
@@ -986,7 +990,6 @@ Plan make_plan(const moe_layer& L, int q) {
     p.g_down = di.sms > kMinDownCtas ? di.sms : kMinDownCtas;
     p.ns_down = cta_smem_bytes(DnRing<5>::kBytes, 2 * tset_copy_bytes(L.I)) + 2048 <= 227 * 1024 ? 5 : 2;
     p.sm_down = cta_smem_bytes(p.ns_down == 5 ? DnRing<5>::kBytes : DnRing<2>::kBytes, 2 * tset_copy_bytes(L.I));
-    p.sm_hpack = sizeof(float) * (size_t)q * L.I;
     p.g_comb = (q * L.H + kCombineThreads - 1) / kCombineThreads;
     return p;
 }
@@ -1035,8 +1038,7 @@ int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, co
     auto kdown = p.ns_down == 5 ? k_down<Q, MODE, 5> : k_down<Q, MODE, 2>;
     HpackArgs ha{};
     ha.I = L.I; ha.k = k; ha.ks = (L.H / stage_k(2)) % 2 == 0 ? 2 : 1; ha.ws = ws;
-    if (cudaFuncSetAttribute(k_hpack<Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_hpack) ||
-        cudaFuncSetAttribute(k_router<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_router) ||
+    if (cudaFuncSetAttribute(k_router<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_router) ||
         cudaFuncSetAttribute(k_gate_up<Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_gate) ||
         cudaFuncSetAttribute(kdown, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_down))
         return FPX_ECUDA;
@@ -1050,7 +1052,7 @@ int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, co
     if (ev) cudaEventRecord(ev[1], s);
     e = e ? e : launch(k_gate_up<Q>, p.g_gate, kCtaThreads, p.sm_gate, s, pdl, ga);
     if (ev) cudaEventRecord(ev[2], s);
-    e = e ? e : launch(k_hpack<Q>, Q * k + 1, kHpackThreads, p.sm_hpack, s, pdl, ha);
+    e = e ? e : launch(k_hpack<Q>, 4 * (Q * k + 1), kHpackThreads, 0, s, pdl, ha);
     if (ev) cudaEventRecord(ev[3], s);
     e = e ? e : launch(kdown, p.g_down, kCtaThreads, p.sm_down, s, pdl, da);
     if (ev) cudaEventRecord(ev[4], s);
