@@ -143,21 +143,26 @@ class Stack:
         mb_gu, mb_d, mb_s = fpx.fpx_matrix_bytes(2, I, H), fpx.fpx_matrix_bytes(3, H, I), fpx.fpx_matrix_bytes(4, I, H)
         s = torch.cuda.current_stream().cuda_stream
         self.bufs, self.layers = [], []
+        # the kernels read box-tiled expert matrices: generate row-major into scratch, then tile
+        tmp = torch.empty(E * max(mb_gu, mb_d), dtype=torch.uint8, device="cuda")
         for l in range(n_layers):
             g = torch.empty(E * mb_gu, dtype=torch.uint8, device="cuda")
             u = torch.empty(E * mb_gu, dtype=torch.uint8, device="cuda")
             d = torch.empty(E * mb_d, dtype=torch.uint8, device="cuda")
             sh = [torch.empty(mb_s, dtype=torch.uint8, device="cuda") for _ in range(3)]
-            synth.device_matrices(2, seed, l, synth.GATE, 0, E, I, H, g.data_ptr(), mb_gu, s)
-            synth.device_matrices(2, seed, l, synth.UP, 0, E, I, H, u.data_ptr(), mb_gu, s)
-            synth.device_matrices(3, seed, l, synth.DOWN, 0, E, H, I, d.data_ptr(), mb_d, s)
-            for m, (tid, n, kk) in zip(sh, [(synth.SH_GATE, I, H), (synth.SH_UP, I, H), (synth.SH_DOWN, H, I)]):
-                synth.device_matrices(4, seed, l, tid, 0, 1, n, kk, m.data_ptr(), mb_s, s)
+            for dst, fmt, tensor, count, n, kk, mb in ((g, 2, synth.GATE, E, I, H, mb_gu), (u, 2, synth.UP, E, I, H, mb_gu),
+                                                       (d, 3, synth.DOWN, E, H, I, mb_d),
+                                                       (sh[0], 4, synth.SH_GATE, 1, I, H, mb_s),
+                                                       (sh[1], 4, synth.SH_UP, 1, I, H, mb_s),
+                                                       (sh[2], 4, synth.SH_DOWN, 1, H, I, mb_s)):
+                synth.device_matrices(fmt, seed, l, tensor, 0, count, n, kk, tmp.data_ptr(), mb, s)
+                fpx.fpx_tile_matrices(fmt, tmp, n, kk, count, mb, dst, mb, 0, s)
             R = torch.from_numpy(synth.router(E, H, seed, l)).cuda()
             self.bufs.append((g, u, d, sh, R))
             self.layers.append(fpx.moe_layer(H=H, I=I, E=E, router=R.data_ptr(), gate=g.data_ptr(), up=u.data_ptr(),
                                              down=d.data_ptr(), sh_gate=sh[0].data_ptr(), sh_up=sh[1].data_ptr(),
                                              sh_down=sh[2].data_ptr()))
+        del tmp
         torch.cuda.synchronize()
 
 

@@ -47,6 +47,9 @@ _SIGS = {
                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "fpx_dequantize": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "fpx_tile_matrices": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                                         ctypes.c_int, ctypes.c_void_p]),
     "fpx_gemv_q": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                   ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                   ctypes.c_void_p, ctypes.c_void_p]),
@@ -130,6 +133,11 @@ def fpx_read_status(dev_status, stream=None):
 def fpx_quantize(fmt, W, N, K, out, block_scales=None, dev_status=None, stream=None):
     _check(lib().fpx_quantize(fmt, _ptr(W), N, K, _ptr(block_scales), _ptr(out), _ptr(dev_status),
                               _stream(stream)), "fpx_quantize")
+
+
+def fpx_tile_matrices(fmt, src, N, K, count, src_stride, dst, dst_stride, inverse=0, stream=None):
+    _check(lib().fpx_tile_matrices(fmt, _ptr(src), N, K, count, src_stride, _ptr(dst), dst_stride, inverse,
+                                   _stream(stream)), "fpx_tile_matrices")
 
 
 def fpx_dequantize(fmt, Wq, N, K, W, dev_status=None, stream=None):

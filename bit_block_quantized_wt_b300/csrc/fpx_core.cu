@@ -341,6 +341,29 @@ int launch_gemv_cc(const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x
 
 }  // namespace
 
+// ------------------------------------------------------------------ box-tiled matrices
+
+// Box-tiled layout (the MoE layer kernels stream it with 1-D bulk copies): a matrix of N rows is cut
+// into tiles of tile_rows(fmt) rows x box_bytes(fmt) bytes of each row (256 x 80 FP2, 256 x 112 FP3,
+// 64 x 272 FP4), stored contiguously in the order (row block, column piece) with the tile's rows at a
+// pitch of box_bytes(fmt): the byte at (row r, offset j of the row) goes to
+// ((r / R) * P + j / B) * R * B + (r % R) * B + j % B, with R = tile_rows, B = box_bytes,
+// P = row_bytes / B. The permutation moves whole 16-byte units (B and row_bytes are multiples of 16).
+__global__ void k_tile(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t units, int64_t row_units,
+                       int R, int B16, int64_t src_stride, int64_t dst_stride, int inverse) {
+    const uint8_t* sm = src + (int64_t)blockIdx.y * src_stride;
+    uint8_t* dm = dst + (int64_t)blockIdx.y * dst_stride;
+    const int64_t P = row_units / B16, tile_units = (int64_t)R * B16;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += (int64_t)gridDim.x * blockDim.x) {
+        // u: 16-byte unit of the tiled matrix -> its row-major unit
+        const int64_t t = u / tile_units, o = u % tile_units;
+        const int64_t r = (t / P) * R + o / B16, j = (t % P) * B16 + o % B16;
+        const int64_t v = r * row_units + j;
+        if (inverse) reinterpret_cast<uint4*>(dm)[v] = reinterpret_cast<const uint4*>(sm)[u];
+        else reinterpret_cast<uint4*>(dm)[u] = reinterpret_cast<const uint4*>(sm)[v];
+    }
+}
+
 extern "C" {
 
 const char* fpx_status_string(int status) {
@@ -394,6 +417,25 @@ int fpx_quantize(int fmt, const float* W, int64_t N, int64_t K, const float* blo
     if (fmt == 2) k_quantize<2><<<grid, 128, 0, s>>>(W, N, K, block_scales, out, dev_status);
     else if (fmt == 3) k_quantize<3><<<grid, 128, 0, s>>>(W, N, K, block_scales, out, dev_status);
     else k_quantize<4><<<grid, 128, 0, s>>>(W, N, K, block_scales, out, dev_status);
+    return launch_status();
+}
+
+int fpx_tile_matrices(int fmt, const uint8_t* src, int64_t N, int64_t K, int count, int64_t src_stride, uint8_t* dst,
+                      int64_t dst_stride, int inverse, void* stream) {
+    if (matrix_bytes(fmt, N, K) < 0 || count < 0 || (inverse != 0 && inverse != 1)) return FPX_EINVAL;
+    const int R = stage_rows(fmt), B = box_bytes(fmt);
+    const int64_t row_bytes = K / 32 * block_bytes(fmt);
+    if (N % R || row_bytes % B || N > INT32_MAX) return FPX_EINVAL;
+    if (count == 0 || N == 0 || K == 0) return FPX_OK;
+    if (!src || !dst || src == dst) return FPX_EINVAL;
+    const int64_t bytes = N * row_bytes;
+    if (src_stride < bytes || dst_stride < bytes) return FPX_EINVAL;
+    if (!aligned(src, 16) || !aligned(dst, 16) || src_stride % 16 || dst_stride % 16) return FPX_EALIGN;
+    const int64_t units = bytes / 16;
+    const int64_t gx = (units + 255) / 256 < 148 * 4 ? (units + 255) / 256 : 148 * 4;
+    if (count > 65535) return FPX_EINVAL;
+    k_tile<<<dim3((unsigned)gx, (unsigned)count), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        src, dst, units, row_bytes / 16, R, B / 16, src_stride, dst_stride, inverse);
     return launch_status();
 }
 

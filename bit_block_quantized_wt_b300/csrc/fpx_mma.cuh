@@ -90,16 +90,30 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
+// try_wait that may suspend the thread for up to `ns` nanoseconds while the phase is incomplete (it
+// resumes as soon as the phase completes): a waiting warp then stops taking issue slots from the
+// warps that do work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* b, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity, giving up after kWaitNs of wall time (or kSpinLimit
-// polls; each try_wait may itself suspend for a bounded time). Returns false when it gives up.
+// polls; each poll may suspend the thread for up to kSleepNs). Returns false when it gives up.
 constexpr uint32_t kSpinLimit = 1u << 24;
 constexpr uint64_t kWaitNs = 500000000ull;  // 0.5 s
+constexpr uint32_t kSleepNs = 20000;       // 20 us per poll
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
     if (mbar_try_wait(b, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 0; i < kSpinLimit; i++) {
-        if (mbar_try_wait(b, parity)) return true;
-        if ((i & 63) == 63 && global_ns() - t0 > kWaitNs) return false;
+        if (mbar_try_wait_sleep(b, parity, kSleepNs)) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
     }
     return false;
 }

@@ -24,6 +24,7 @@ constexpr int kThreads = 256;  // router and top-k kernels
 constexpr int kMaxK = 8;
 constexpr int kMaxQ = 4;
 constexpr int kMaxE = 1024;
+constexpr int kMaxPieces = 3;  // partial results per task (see StageList)
 
 // Programmatic dependent launch: each layer kernel is launched so that it may start while the
 // previous kernel's last CTAs still run; grid_dep_wait() blocks until that kernel has completed and
@@ -36,7 +37,7 @@ __device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontro
 
 struct Ws {
     size_t status, logits, u, idx, w, uni, nuni, gu, yi, gt, dt, total;
-    size_t gu_half, yi_half;  // floats between the two K-split partial buffers
+    size_t gu_piece, yi_piece;  // floats between consecutive piece buffers
 };
 
 inline size_t up16(size_t v) { return (v + 15) & ~size_t(15); }
@@ -51,10 +52,10 @@ inline Ws ws_layout(int H, int I, int E, int q, int k) {
     w.w = o; o = up16(o + sizeof(float) * q * k);
     w.uni = o; o = up16(o + sizeof(int32_t) * q * k);
     w.nuni = o; o += 16;  // n_uni, then the router's arrival counter
-    w.gu_half = (size_t)2 * (q * k + 1) * q * I;
-    w.yi_half = (size_t)(q * k + 1) * q * H;
-    w.gu = o; o = up16(o + sizeof(float) * 2 * w.gu_half);
-    w.yi = o; o = up16(o + sizeof(float) * 2 * w.yi_half);
+    w.gu_piece = (size_t)2 * (q * k + 1) * q * I;
+    w.yi_piece = (size_t)(q * k + 1) * q * H;
+    w.gu = o; o = up16(o + sizeof(float) * kMaxPieces * w.gu_piece);
+    w.yi = o; o = up16(o + sizeof(float) * kMaxPieces * w.yi_piece);
     w.gt = o; o = up16(o + tset_bytes(H));
     w.dt = o; o = up16(o + (size_t)(q * k + 1) * tset_bytes(I));
     w.total = o;
@@ -69,9 +70,9 @@ struct WsPtrs {
     float* w;
     int32_t* uni;
     int32_t* nuni;
-    float* gu;  // g and u of every item: [K half][2 * item + (0 | 1)][q][I]
-    float* yi;  // per-item outputs [K half][item][q][H]
-    size_t gu_half, yi_half;
+    float* gu;  // g and u of every item: [piece][2 * item + (0 | 1)][q][I]
+    float* yi;  // per-item outputs [piece][item][q][H]
+    size_t gu_piece, yi_piece;
     uint8_t* gt;  // gate/up activation tables (table set for K = H), built by the router kernel
     uint8_t* dt;  // down activation tables, one table set for K = I per item, built by k_hpack
 };
@@ -82,29 +83,31 @@ inline WsPtrs ws_ptrs(void* ws, const Ws& l) {
                   reinterpret_cast<uint16_t*>(b + l.u),     reinterpret_cast<int32_t*>(b + l.idx),
                   reinterpret_cast<float*>(b + l.w),        reinterpret_cast<int32_t*>(b + l.uni),
                   reinterpret_cast<int32_t*>(b + l.nuni),   reinterpret_cast<float*>(b + l.gu),
-                  reinterpret_cast<float*>(b + l.yi),       l.gu_half,
-                  l.yi_half,                                reinterpret_cast<uint8_t*>(b + l.gt),
+                  reinterpret_cast<float*>(b + l.yi),       l.gu_piece,
+                  l.yi_piece,                                reinterpret_cast<uint8_t*>(b + l.gt),
                   reinterpret_cast<uint8_t*>(b + l.dt)};
 }
 
-// Everything the gate/up and down kernels need about one layer: tensor maps over the stacked
-// matrices (rows of all experts), shapes and strides.
+// Everything the gate/up and down kernels need about one layer: the stacked box-tiled matrices
+// (fpx_tile_matrices) and the shapes. A stage is one tile, streamed with one 1-D bulk copy.
 struct LayerMaps {
-    CUtensorMap gate, up, down, sh_gate, sh_up, sh_down;  // 64-byte aligned members first
+    const uint8_t *gate, *up, *down, *sh_gate, *sh_up, *sh_down;
+    int64_t mb2, mb3;  // bytes of one routed FP2 (I x H) and FP3 (H x I) matrix
     int H, I, E;
 };
 
 int make_layer_maps(const moe_layer& L, LayerMaps* m) {
+    m->gate = L.gate; m->up = L.up; m->down = L.down;
+    m->sh_gate = L.sh_gate; m->sh_up = L.sh_up; m->sh_down = L.sh_down;
+    m->mb2 = matrix_bytes(2, L.I, L.H);
+    m->mb3 = matrix_bytes(3, L.H, L.I);
     m->H = L.H; m->I = L.I; m->E = L.E;
-    const int64_t rb2 = (int64_t)(L.H / 32) * 10, rb4h = (int64_t)(L.H / 32) * 17;
-    const int64_t rb3 = (int64_t)(L.I / 32) * 14, rb4i = (int64_t)(L.I / 32) * 17;
-    int st = make_row_map(&m->gate, L.gate, rb2, (int64_t)L.E * L.I, rb2, box_bytes(2), stage_rows(2), 1);
-    st = st ? st : make_row_map(&m->up, L.up, rb2, (int64_t)L.E * L.I, rb2, box_bytes(2), stage_rows(2), 1);
-    st = st ? st : make_row_map(&m->down, L.down, rb3, (int64_t)L.E * L.H, rb3, box_bytes(3), stage_rows(3), 1);
-    st = st ? st : make_row_map(&m->sh_gate, L.sh_gate, rb4h, L.I, rb4h, box_bytes(4), stage_rows(4), 2);
-    st = st ? st : make_row_map(&m->sh_up, L.sh_up, rb4h, L.I, rb4h, box_bytes(4), stage_rows(4), 2);
-    st = st ? st : make_row_map(&m->sh_down, L.sh_down, rb4i, L.H, rb4i, box_bytes(4), stage_rows(4), 2);
-    return st;
+    return FPX_OK;
+}
+
+// Byte offset of tile (row block of `row0`, column piece 0) of a box-tiled matrix with K columns.
+__host__ __device__ constexpr int64_t tile_offset(int fmt, int row0, int K) {
+    return (int64_t)(row0 / stage_rows(fmt)) * (K / stage_k(fmt)) * stage_bytes(fmt);
 }
 
 // ------------------------------------------------------------------ block-wide helpers
@@ -462,43 +465,66 @@ __device__ inline void load_route(Route& r, const WsPtrs& ws, int qk) {
     __syncthreads();
 }
 
-// Position in a CTA's (task, stage) sequence.
-struct Cursor {
-    int task, stage;
+// The work of a streaming kernel as a list of stages: nA tasks of sA stages of cost cA each, then nB
+// tasks of sB stages of cost cB. CTA b of G owns the stages whose start cost c has
+// floor(c G / total) == b: a contiguous range of about total / G, so every CTA streams about the same
+// bytes whatever the task sizes. A task cut by CTA boundaries is computed in pieces (at most
+// kMaxPieces: the host caps G so that every CTA's share is at least the largest task / (kMaxPieces -
+// 1)), each written to its own partial buffer; the next kernel adds a task's pieces in order.
+struct StageList {
+    int64_t nA, sA, cA, nB, sB, cB;
+    __host__ __device__ __forceinline__ int64_t stages() const { return nA * sA + nB * sB; }
+    __host__ __device__ __forceinline__ int64_t total() const { return nA * sA * cA + nB * sB * cB; }
+    __host__ __device__ __forceinline__ int64_t cost_before(int64_t s) const {
+        const int64_t a = nA * sA;
+        return s <= a ? s * cA : a * cA + (s - a) * cB;
+    }
+    __host__ __device__ __forceinline__ int64_t owner(int64_t s, int64_t G) const { return cost_before(s) * G / total(); }
+    // first stage of CTA b (b == G: stages())
+    __host__ __device__ __forceinline__ int64_t first(int64_t b, int64_t G) const {
+        const int64_t a = nA * sA, tgt = total() * b;  // smallest s with cost_before(s) * G >= tgt
+        if (tgt <= a * cA * G) return (tgt + G * cA - 1) / (G * cA);
+        return a + (tgt - a * cA * G + G * cB - 1) / (G * cB);
+    }
+    __host__ __device__ __forceinline__ int64_t task_of(int64_t s) const {
+        const int64_t a = nA * sA;
+        return s < a ? s / sA : nA + (s - a) / sB;
+    }
+    __host__ __device__ __forceinline__ int64_t task_first(int64_t t) const { return t < nA ? t * sA : nA * sA + (t - nA) * sB; }
+    __host__ __device__ __forceinline__ int64_t task_len(int64_t t) const { return t < nA ? sA : sB; }
+    __host__ __device__ __forceinline__ int pieces(int64_t t, int64_t G) const {
+        const int64_t f = task_first(t);
+        return (int)(owner(f + task_len(t) - 1, G) - owner(f, G) + 1);
+    }
+    __host__ __device__ __forceinline__ int piece(int64_t t, int64_t b, int64_t G) const { return (int)(b - owner(task_first(t), G)); }
 };
-
-// CTA task range [c0, c1) over nA tasks of cost cA followed by nB tasks of cost cB: task t goes to
-// the CTA whose share of the total cost contains the cost before t, so CTAs get about equal work.
-__device__ __forceinline__ int cost_split(int64_t nA, int64_t cA, int64_t nB, int64_t cB, int64_t b, int64_t G) {
-    const int64_t tot = nA * cA + nB * cB, target = tot * b;  // first t with prefix(t) * G >= target
-    if (target <= nA * cA * G) return (int)((target + G * cA - 1) / (G * cA));
-    return (int)(nA + (target - nA * cA * G + G * cB - 1) / (G * cB));
-}
-
-__device__ __forceinline__ void task_range(int nA, int cA, int nB, int cB, int& c0, int& c1) {
-    c0 = cost_split(nA, cA, nB, cB, blockIdx.x, gridDim.x);
-    c1 = cost_split(nA, cA, nB, cB, blockIdx.x + 1, gridDim.x);
-}
 
 // Relative cost of a stage: bytes streamed, FP4 boxes weighted by 4/3 (their decode costs more per
 // byte).
 constexpr int kCostFP2 = stage_bytes(2), kCostFP3 = stage_bytes(3), kCostFP4 = stage_bytes(4) * 4 / 3;
 
-// Number of K halves a routed task is split into (1 when the row does not split into whole boxes).
-__device__ __forceinline__ int k_split(int K, int fmt) { return (K / stage_k(fmt)) % 2 == 0 ? 2 : 1; }
+// Stage lists of the gate/up kernel (FP2 tasks: matrix x 256-row block, H/256 stages; FP4: matrix x
+// 64-row block, H/512 stages) and of the down kernel (FP3: item x 256-row block, I/256 stages; FP4:
+// 64-row block, I/512 stages).
+__host__ __device__ inline StageList gate_up_stages(int n_uni, int H, int I) {
+    return StageList{(int64_t)2 * n_uni * (I / 256), H / stage_k(2), kCostFP2, (int64_t)2 * (I / 64), H / stage_k(4), kCostFP4};
+}
+__host__ __device__ inline StageList down_stages(int n_uni, int H, int I) {
+    return StageList{(int64_t)n_uni * (H / 256), I / stage_k(3), kCostFP3, (int64_t)(H / 64), I / stage_k(4), kCostFP4};
+}
 
 // ------------------------------------------------------------------ K2: gate/up
 
-// Task = (output matrix, row block, K part): the union's gate and up matrices (FP2, 256-row blocks of
-// I, each split into ks K parts of H/256/ks stages), then the shared expert's gate and up (FP4,
-// 64-row blocks, H/512 stages). Matrix m = 2 * item + (0 gate | 1 up), the shared expert being item
-// n_uni. Each CTA owns a contiguous task range of about equal cost; its producer thread streams the
+// Task = (output matrix, row block): the union's gate and up matrices (FP2, 256-row blocks of I,
+// H/256 stages each), then the shared expert's gate and up (FP4, 64-row blocks, H/512 stages).
+// Matrix m = 2 * item + (0 gate | 1 up), the shared expert being item n_uni. Each CTA owns a
+// contiguous range of stages of about equal cost (StageList); its producer thread streams the
 // range's boxes through the CTA ring and all consumer warps decode every box. Outputs g and u
-// (binary32) go to ws.gu[K part][m][token][row]; the down kernel adds the parts and forms
-// h = silu(g) u while building its activation table.
+// (binary32) go to ws.gu[piece][m][token][row]; k_hpack adds the pieces and forms h = silu(g) u.
 struct GateUpArgs {
     LayerMaps m;
     int q, k;
+    int G;  // grid size (the stage partition depends on it)
     const uint16_t* x;  // layer input, bfloat16 [q][H]
     WsPtrs ws;
     uint32_t magic;  // kMagic, kept out of immediates (see decode_fp2)
@@ -514,45 +540,35 @@ using DnRing = CtaRing<NS, stage_bytes(3)>;
 static_assert(stage_bytes(4) <= stage_bytes(2), "FP4 box fits a slot");
 
 struct GuTask {
-    int mat;    // output matrix index
-    int fp4;    // shared expert (FP4) task
-    int row0;   // first output row
-    int grow0;  // first row in the stacked tensor map
-    int kpart;  // K part
-    int ns;     // stages
+    int mat;      // output matrix index
+    int fp4;      // shared expert (FP4) task
+    int row0;     // first output row
+    int64_t off;  // byte offset of the task's first tile in its (stacked) matrix
 };
 
-__device__ __forceinline__ GuTask gu_task(int t, const Route& r, int H, int I, int ks) {
-    const int rb2 = I / 256, n2 = 2 * r.n_uni * rb2 * ks;
+__device__ __forceinline__ GuTask gu_task(int64_t t, const Route& r, const LayerMaps& m) {
+    const int I = m.I, rb2 = I / 256, n2 = 2 * r.n_uni * rb2;
     GuTask k;
     if (t < n2) {
-        const int rem = t % (rb2 * ks);
-        k.mat = t / (rb2 * ks);
+        k.mat = (int)t / rb2;
         k.fp4 = 0;
-        k.row0 = (rem / ks) * 256;
-        k.kpart = rem % ks;
-        k.grow0 = r.uni[k.mat >> 1] * I + k.row0;
-        k.ns = H / stage_k(2) / ks;
+        k.row0 = ((int)t % rb2) * 256;
+        k.off = r.uni[k.mat >> 1] * m.mb2 + tile_offset(2, k.row0, m.H);
     } else {
-        const int t4 = t - n2, rb4 = I / 64;
+        const int t4 = (int)t - n2, rb4 = I / 64;
         k.mat = 2 * r.n_uni + t4 / rb4;
         k.fp4 = 1;
         k.row0 = (t4 % rb4) * 64;
-        k.kpart = 0;
-        k.grow0 = k.row0;
-        k.ns = H / stage_k(4);
+        k.off = tile_offset(4, k.row0, m.H);
     }
     return k;
 }
 
 __device__ __forceinline__ void gu_issue(const GateUpArgs& A, const GuTask& k, int s, uint8_t* slot, uint64_t* bar) {
-    if (!k.fp4) {
-        mbar_expect_tx(bar, stage_bytes(2));
-        tma_load_2d(slot, (k.mat & 1) ? &A.m.up : &A.m.gate, (k.kpart * k.ns + s) * box_bytes(2), k.grow0, bar);
-    } else {
-        mbar_expect_tx(bar, stage_bytes(4));
-        tma_load_2d(slot, (k.mat & 1) ? &A.m.sh_up : &A.m.sh_gate, s * (box_bytes(4) / 2), k.grow0, bar);
-    }
+    const int fmt = k.fp4 ? 4 : 2;
+    const uint8_t* base = k.fp4 ? ((k.mat & 1) ? A.m.sh_up : A.m.sh_gate) : ((k.mat & 1) ? A.m.up : A.m.gate);
+    mbar_expect_tx(bar, stage_bytes(fmt));
+    bulk_load(slot, base + k.off + (int64_t)s * stage_bytes(fmt), stage_bytes(fmt), bar);
 }
 
 template <int Q>
@@ -572,18 +588,19 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
     }
     load_route(r, A.ws, Q * A.k);
 
-    const int ks = k_split(H, 2);
-    int c0, c1;
-    task_range(2 * r.n_uni * (I / 256) * ks, (H / stage_k(2) / ks) * kCostFP2, 2 * (I / 64), (H / stage_k(4)) * kCostFP4, c0, c1);
+    const StageList SL = gate_up_stages(r.n_uni, H, I);
+    const int64_t G = A.G, s0 = SL.first(blockIdx.x, G), s1 = SL.first(blockIdx.x + 1, G);
 
     if (warp == kWarps) {  // producer: streams the range's boxes while the consumers load the tables
         if (lane == 0) {
             uint32_t issued = 0;
-            for (int tk = c0; tk < c1; tk++) {
-                const GuTask k = gu_task(tk, r, H, I, ks);
-                for (int s = 0; s < k.ns; s++, issued++) {
-                    if (!R.acquire(issued)) { flag(A.ws.status, FPX_ETIMEOUT); tk = c1; break; }
-                    gu_issue(A, k, s, R.slot(issued), R.bar(issued));
+            bool live = true;
+            for (int64_t sg = s0; sg < s1 && live;) {
+                const int64_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
+                const GuTask k = gu_task(tk, r, A.m);
+                for (; sg < te; sg++, issued++) {
+                    if (!R.acquire(issued)) { flag(A.ws.status, FPX_ETIMEOUT); live = false; break; }
+                    gu_issue(A, k, (int)(sg - tf), R.slot(issued), R.bar(issued));
                 }
             }
             R.drain(issued);
@@ -606,15 +623,18 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
     const uint32_t magic = A.magic;
     const LaneOfs L2 = lane_ofs<2>(t), L4 = lane_ofs<4>(t);
     uint32_t n = 0, bad = 0;
-    for (int tk = c0; tk < c1; tk++) {
-        const GuTask k = gu_task(tk, r, H, I, ks);
+    for (int64_t sg = s0; sg < s1;) {
+        // the stages of one task inside this CTA's range: one piece of the task
+        const int64_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
+        const GuTask k = gu_task(tk, r, A.m);
         float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        for (int s = 0; s < k.ns; s++, n++) {
+        for (; sg < te; sg++, n++) {
+            const int s = (int)(sg - tf);
             if (ok) ok = R.wait(n, A.ws.status);
             if (!ok) continue;  // the producer gives up too once this warp stops releasing
             const uint8_t* slot = R.slot(n);
             if (!k.fp4) {
-                const int ch0 = (k.kpart * k.ns + s) * box_chunks(2);
+                const int ch0 = s * box_chunks(2);
                 box_tiles<2, 2, box_chunks(2)>(smem_u32(slot) + (warp * 32 + g) * box_bytes(2), L2,
                                                lane_tab(tab2, S.zero, a_idx, ch0), 0u, lane_oq(oq2, ch0, t), magic, y, bad);
             } else {
@@ -630,7 +650,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
         if (k.fp4) fp4_reduce(S.red, y[0]);  // the same tasks run on every consumer warp
         if (ok && t < 2 && (!k.fp4 || warp < 4)) {
             const int rb = k.row0 + (k.fp4 ? 16 : 32) * warp + g;
-            float* out = A.ws.gu + k.kpart * A.ws.gu_half + (size_t)k.mat * Q * I;
+            float* out = A.ws.gu + SL.piece(tk, blockIdx.x, G) * A.ws.gu_piece + (size_t)k.mat * Q * I;
 #pragma unroll
             for (int i = 0; i < 4; i++) {
                 const int tok = 2 * t + (i & 1), rr = rb + 8 * (i >> 1);
@@ -649,22 +669,24 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
 // ------------------------------------------------------------------ K2b: h and the down tables
 
 // One CTA per (union item or shared expert, token slot): h = silu(g) u over the item's I rows for the
-// token (the K parts of g and u added first), its column shift, and that token's entries of the item's
-// down activation table set (FP3 planes with block offsets; FP4 for the shared expert) in global
-// memory. Token slots >= q get zero entries.
+// token (the pieces of g and u added in order first), its column shift, and that token's entries of
+// the item's down activation table set (FP3 planes with block offsets; FP4 for the shared expert) in
+// global memory. Token slots >= q get zero entries.
 struct HpackArgs {
-    int I, k, ks;  // ks: K parts of the routed gate/up outputs
+    int H, I, k;
+    int G;  // grid of the gate/up kernel (its stage partition)
     WsPtrs ws;
 };
 
 constexpr int kHpackThreads = 512;
-constexpr int kHpackV = 4;  // float4 groups per thread, all loaded at once: I <= 4 * 4 * 512
+constexpr int kHpackV = 3;  // float4 groups per thread, all loaded at once: I <= 3 * 4 * 512
 
 template <int Q>
 __global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__ HpackArgs A) {
     __shared__ __align__(16) float h_s[kHpackV * 4 * kHpackThreads];  // [I]
     __shared__ float red[kHpackThreads / 32];
     __shared__ int sh_s;
+    __shared__ int8_t np_s[2][kHpackV * 4 * kHpackThreads / 64];  // pieces of the gate / up task of each row block
     grid_dep_trigger();
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int I = A.I, j = blockIdx.x / 4, tok = blockIdx.x % 4;
@@ -676,23 +698,42 @@ __global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__
         grid_dep_wait();  // g and u come from the gate/up kernel
         const float4* g = reinterpret_cast<const float4*>(A.ws.gu + ((size_t)(2 * j) * Q + tok) * I);
         const float4* u = reinterpret_cast<const float4*>(A.ws.gu + ((size_t)(2 * j + 1) * Q + tok) * I);
-        const size_t p2 = (j < n_uni && A.ks == 2 ? A.ws.gu_half : 0) / 4;
-        float4 ga[kHpackV], ua[kHpackV], gb[kHpackV], ub[kHpackV];
+        const size_t pstride = A.ws.gu_piece / 4;
+        // pieces of the item's gate and up tasks (routed: 256-row blocks 2j * (I/256) + rb and
+        // (2j+1) * (I/256) + rb; shared: 64-row blocks nA + rb and nA + I/64 + rb), one thread each
+        const StageList SL = gate_up_stages(n_uni, A.H, I);
+        const int rbs = j < n_uni ? 256 : 64, nrb = I / rbs;
+        if (threadIdx.x < 2 * nrb) {
+            const int m = threadIdx.x / nrb, rb = threadIdx.x % nrb;
+            const int64_t tk = j < n_uni ? (int64_t)(2 * j + m) * nrb + rb : SL.nA + (int64_t)m * nrb + rb;
+            np_s[m][rb] = (int8_t)SL.pieces(tk, A.G);
+        }
+        __syncthreads();
+        float4 ga[kHpackV], ua[kHpackV];
 #pragma unroll
         for (int v = 0; v < kHpackV; v++) {
             const int e = threadIdx.x + v * kHpackThreads;
             const bool in = e < I / 4;
-            ga[v] = in ? __ldcg(g + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-            ua[v] = in ? __ldcg(u + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-            gb[v] = in && p2 ? __ldcg(g + p2 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-            ub[v] = in && p2 ? __ldcg(u + p2 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int ng = in ? np_s[0][4 * e / rbs] : 0, nu = in ? np_s[1][4 * e / rbs] : 0;
+            float4 gp[kMaxPieces], up[kMaxPieces];
+#pragma unroll
+            for (int p = 0; p < kMaxPieces; p++) {
+                gp[p] = p < ng ? __ldcg(g + p * pstride + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                up[p] = p < nu ? __ldcg(u + p * pstride + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            ga[v] = gp[0]; ua[v] = up[0];
+#pragma unroll
+            for (int p = 1; p < kMaxPieces; p++) {
+                if (p < ng) { ga[v].x += gp[p].x; ga[v].y += gp[p].y; ga[v].z += gp[p].z; ga[v].w += gp[p].w; }
+                if (p < nu) { ua[v].x += up[p].x; ua[v].y += up[p].y; ua[v].z += up[p].z; ua[v].w += up[p].w; }
+            }
         }
 #pragma unroll
         for (int v = 0; v < kHpackV; v++) {
             const int e = threadIdx.x + v * kHpackThreads;
             if (e < I / 4) {
-                const float a[4] = {ga[v].x + gb[v].x, ga[v].y + gb[v].y, ga[v].z + gb[v].z, ga[v].w + gb[v].w};
-                const float b[4] = {ua[v].x + ub[v].x, ua[v].y + ub[v].y, ua[v].z + ub[v].z, ua[v].w + ub[v].w};
+                const float a[4] = {ga[v].x, ga[v].y, ga[v].z, ga[v].w};
+                const float b[4] = {ua[v].x, ua[v].y, ua[v].z, ua[v].w};
                 float h[4];
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
@@ -736,55 +777,45 @@ __global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__
 
 // ------------------------------------------------------------------ K3: down + combine
 
-// Task = (item, row block of H, K part): the union's down matrices (FP3, 256-row blocks, each split
-// into ks K parts of I/256/ks stages), then the shared expert's (FP4, 64-row blocks, I/512 stages).
-// Each CTA owns a contiguous task range of about equal cost, which spans at most two items (the grid
-// has at least kMinDownCtas CTAs); it builds their activation tables from h = silu(g) u at start.
-// Outputs go to ws.yi[K part][item][token][row]; k_combine adds them up.
-constexpr int kMinDownCtas = 2 * (kMaxQ * kMaxK + 1);
-
+// Task = (item, row block of H): the union's down matrices (FP3, 256-row blocks, I/256 stages), then
+// the shared expert's (FP4, 64-row blocks, I/512 stages). Each CTA owns a contiguous range of stages
+// of about equal cost (StageList), which spans at most two items; it copies their activation tables
+// (built by k_hpack) at start. Outputs go to ws.yi[piece][item][token][row]; k_combine adds them up.
 struct DownArgs {
     LayerMaps m;
     int q, k;
+    int G;  // grid size (the stage partition depends on it)
     WsPtrs ws;
     float* out;  // MODE 0: y [q][H]; MODE 1: residual r [q][H], updated in place
     uint32_t magic;
 };
 
 struct DnTask {
-    int item, fp4, row0, grow0, kpart, ns;
+    int item, fp4, row0;
+    int64_t off;  // byte offset of the task's first tile in its (stacked) matrix
 };
 
-__device__ __forceinline__ DnTask dn_task(int t, const Route& r, int H, int I, int ks) {
-    const int rb3 = H / 256, n3 = r.n_uni * rb3 * ks;
+__device__ __forceinline__ DnTask dn_task(int64_t t, const Route& r, const LayerMaps& m) {
+    const int H = m.H, rb3 = H / 256, n3 = r.n_uni * rb3;
     DnTask k;
     if (t < n3) {
-        const int rem = t % (rb3 * ks);
-        k.item = t / (rb3 * ks);
+        k.item = (int)t / rb3;
         k.fp4 = 0;
-        k.row0 = (rem / ks) * 256;
-        k.kpart = rem % ks;
-        k.grow0 = r.uni[k.item] * H + k.row0;
-        k.ns = I / stage_k(3) / ks;
+        k.row0 = ((int)t % rb3) * 256;
+        k.off = r.uni[k.item] * m.mb3 + tile_offset(3, k.row0, m.I);
     } else {
         k.item = r.n_uni;
         k.fp4 = 1;
-        k.row0 = (t - n3) * 64;
-        k.kpart = 0;
-        k.grow0 = k.row0;
-        k.ns = I / stage_k(4);
+        k.row0 = ((int)t - n3) * 64;
+        k.off = tile_offset(4, k.row0, m.I);
     }
     return k;
 }
 
 __device__ __forceinline__ void dn_issue(const DownArgs& A, const DnTask& k, int s, uint8_t* slot, uint64_t* bar) {
-    if (!k.fp4) {
-        mbar_expect_tx(bar, stage_bytes(3));
-        tma_load_2d(slot, &A.m.down, (k.kpart * k.ns + s) * box_bytes(3), k.grow0, bar);
-    } else {
-        mbar_expect_tx(bar, stage_bytes(4));
-        tma_load_2d(slot, &A.m.sh_down, s * (box_bytes(4) / 2), k.grow0, bar);
-    }
+    const int fmt = k.fp4 ? 4 : 3;
+    mbar_expect_tx(bar, stage_bytes(fmt));
+    bulk_load(slot, (k.fp4 ? A.m.sh_down : A.m.down) + k.off + (int64_t)s * stage_bytes(fmt), stage_bytes(fmt), bar);
 }
 
 template <int Q, int MODE, int NS>
@@ -802,12 +833,11 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
     grid_dep_trigger();
     load_route(r, A.ws, Q * A.k);
 
-    const int ks = k_split(I, 3);
-    int c0, c1;
-    task_range(r.n_uni * (H / 256) * ks, (I / stage_k(3) / ks) * kCostFP3, H / 64, (I / stage_k(4)) * kCostFP4, c0, c1);
-    if (c0 >= c1) return;  // CTA-uniform: nothing to do
-    const int item_lo = dn_task(c0, r, H, I, ks).item, item_hi = dn_task(c1 - 1, r, H, I, ks).item;
-    if (item_hi - item_lo > 1) {  // too small a grid (the host launches at least kMinDownCtas CTAs)
+    const StageList SL = down_stages(r.n_uni, H, I);
+    const int64_t G = A.G, s0 = SL.first(blockIdx.x, G), s1 = SL.first(blockIdx.x + 1, G);
+    if (s0 >= s1) return;  // CTA-uniform: nothing to do
+    const int item_lo = dn_task(SL.task_of(s0), r, A.m).item, item_hi = dn_task(SL.task_of(s1 - 1), r, A.m).item;
+    if (item_hi - item_lo > 1) {  // cannot happen for the grids make_plan picks (each share < one item)
         if (threadIdx.x == 0) flag(A.ws.status, FPX_EINVAL);
         return;
     }
@@ -815,11 +845,13 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
     if (warp == kWarps) {  // producer: streams the range's boxes while the consumers load the tables
         if (lane == 0) {
             uint32_t issued = 0;
-            for (int tk = c0; tk < c1; tk++) {
-                const DnTask k = dn_task(tk, r, H, I, ks);
-                for (int s = 0; s < k.ns; s++, issued++) {
-                    if (!R.acquire(issued)) { flag(A.ws.status, FPX_ETIMEOUT); tk = c1; break; }
-                    dn_issue(A, k, s, R.slot(issued), R.bar(issued));
+            bool live = true;
+            for (int64_t sg = s0; sg < s1 && live;) {
+                const int64_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
+                const DnTask k = dn_task(tk, r, A.m);
+                for (; sg < te; sg++, issued++) {
+                    if (!R.acquire(issued)) { flag(A.ws.status, FPX_ETIMEOUT); live = false; break; }
+                    dn_issue(A, k, (int)(sg - tf), R.slot(issued), R.bar(issued));
                 }
             }
             R.drain(issued);
@@ -850,20 +882,23 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
     const uint32_t magic = A.magic;
     const LaneOfs L3 = lane_ofs<3>(t), L4 = lane_ofs<4>(t);
     uint32_t n = 0, bad = 0;
-    for (int tk = c0; tk < c1; tk++) {
-        const DnTask k = dn_task(tk, r, H, I, ks);
+    for (int64_t sg = s0; sg < s1;) {
+        // the stages of one task inside this CTA's range: one piece of the task
+        const int64_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
+        const DnTask k = dn_task(tk, r, A.m);
         const int sl = k.item - item_lo;
         const uint8_t* ts = S.tabs + (size_t)sl * tset_copy_bytes(I);
         const uint2* tlo = reinterpret_cast<const uint2*>(ts);
         const uint2* thi = reinterpret_cast<const uint2*>(ts + btab_bytes(I));
         const float* oq = reinterpret_cast<const float*>(ts + 2 * btab_bytes(I));
         float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        for (int s = 0; s < k.ns; s++, n++) {
+        for (; sg < te; sg++, n++) {
+            const int s = (int)(sg - tf);
             if (ok) ok = R.wait(n, A.ws.status);
             if (!ok) continue;
             const uint8_t* slot = R.slot(n);
             if (!k.fp4) {
-                const int ch0 = (k.kpart * k.ns + s) * box_chunks(3);
+                const int ch0 = s * box_chunks(3);
                 box_tiles<3, 2, box_chunks(3)>(smem_u32(slot) + (warp * 32 + g) * box_bytes(3), L3, lane_tab(tlo, S.zero, a_idx, ch0),
                                                lane_tab(thi, S.zero, a_idx, ch0), lane_oq(oq, ch0, t), magic, y, bad);
             } else {
@@ -879,7 +914,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
         if (k.fp4) fp4_reduce(S.red, y[0]);
         if (ok && t < 2 && (!k.fp4 || warp < 4)) {
             const int rb = k.row0 + (k.fp4 ? 16 : 32) * warp + g;
-            float* out = A.ws.yi + k.kpart * A.ws.yi_half + (size_t)k.item * Q * H;
+            float* out = A.ws.yi + SL.piece(tk, blockIdx.x, G) * A.ws.yi_piece + (size_t)k.item * Q * H;
 #pragma unroll
             for (int i = 0; i < 4; i++) {
                 const int tok = 2 * t + (i & 1), rr = rb + 8 * (i >> 1);
@@ -897,12 +932,12 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
 // ------------------------------------------------------------------ K4: combine
 
 // out[t][h] (MODE 0) or r[t][h] += (MODE 1) sum over token t's selected experts, in ascending expert
-// order, of w * y_e[t][h] (K parts added first), then the shared expert's y[t][h]. One thread per
+// order, of w * y_e[t][h] (pieces added in order first), then the shared expert's y[t][h]. One thread per
 // output; consecutive threads take consecutive rows.
 struct CombineArgs {
-    int H, k;
+    int H, I, k;
+    int G;  // grid of the down kernel (its stage partition)
     WsPtrs ws;
-    int ks;      // K parts of the routed down outputs
     float* out;  // MODE 0: y [q][H]; MODE 1: residual r [q][H], updated in place
 };
 
@@ -913,6 +948,7 @@ template <int Q, int MODE>
 __global__ void __launch_bounds__(kCombineThreads) k_combine(const __grid_constant__ CombineArgs A) {
     __shared__ Route r;
     __shared__ float wsel[kMaxQ * kMaxK + 1][kMaxQ];  // weight of token t for union item j, NaN if unselected
+    __shared__ int8_t np_s[kMaxQ * kMaxK + 1][4];       // pieces of each item's task for this CTA's rows
     grid_dep_trigger();
     load_route(r, A.ws, Q * A.k);  // from the router kernel (completed two launches ago)
     for (int i = threadIdx.x; i < r.n_uni * Q; i += blockDim.x) {
@@ -922,27 +958,43 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(const __grid_consta
             if (r.idx[tok * A.k + rr] == r.uni[j]) wv = r.w[tok * A.k + rr];
         wsel[j][tok] = wv;
     }
+    // this CTA's kCombineThreads consecutive outputs lie in one token's rows [row0, row0 + 256): one
+    // 256-row block of each routed down task, four 64-row blocks of the shared one
+    const int H = A.H;
+    const StageList SL = down_stages(r.n_uni, H, A.I);
+    const int row0 = (blockIdx.x * kCombineThreads) % H;
+    for (int i = threadIdx.x; i < (r.n_uni + 1) * 4; i += blockDim.x) {
+        const int jj = i / 4, sub = i % 4;
+        int np = 0;
+        if (jj < r.n_uni) np = sub == 0 ? SL.pieces((int64_t)jj * (H / 256) + row0 / 256, A.G) : 0;
+        else np = SL.pieces(SL.nA + row0 / 64 + sub, A.G);
+        np_s[jj][sub] = (int8_t)np;
+    }
     __syncthreads();
     grid_dep_wait();  // the down kernel's outputs
-    const int H = A.H;
     const int o = blockIdx.x * kCombineThreads + threadIdx.x;
     if (o >= Q * H) return;
     const int tok = o / H, rr = o % H;
     const float* col = A.ws.yi + (size_t)tok * H + rr;
-    const float* col2 = col + A.ws.yi_half;
     const size_t istride = (size_t)Q * H;
-    // loads in batches of 8 (independent, in flight together), then the fixed-order sum; item n_uni
-    // is the shared expert, added last
+    // loads in batches of 8 items (pieces added in order), then the fixed-order sum; item n_uni is
+    // the shared expert, added last
     float acc = 0.0f, ysh = 0.0f;
     bool first = true;
     for (int j0 = 0; j0 <= r.n_uni; j0 += 8) {
         float yv[8];
 #pragma unroll
-        for (int u = 0; u < 8; u++) yv[u] = j0 + u <= r.n_uni ? __ldcg(col + (size_t)(j0 + u) * istride) : 0.0f;
-        if (A.ks == 2)
+        for (int u = 0; u < 8; u++) {
+            const int jj = j0 + u;
+            const int np = jj > r.n_uni ? 0 : jj < r.n_uni ? np_s[jj][0] : np_s[jj][(rr - row0) / 64];
+            float pv[kMaxPieces];
 #pragma unroll
-            for (int u = 0; u < 8; u++)
-                if (j0 + u < r.n_uni) yv[u] += __ldcg(col2 + (size_t)(j0 + u) * istride);
+            for (int p = 0; p < kMaxPieces; p++) pv[p] = p < np ? __ldcg(col + p * A.ws.yi_piece + (size_t)jj * istride) : 0.0f;
+            yv[u] = pv[0];
+#pragma unroll
+            for (int p = 1; p < kMaxPieces; p++)
+                if (p < np) yv[u] += pv[p];
+        }
 #pragma unroll
         for (int u = 0; u < 8; u++) {
             const int jj = j0 + u;
@@ -976,18 +1028,25 @@ int check_layer(const moe_layer* L) {
 }
 
 struct Plan {
-    int g_router, g_gate, g_down, g_comb, ns_down;
+    int g_router, g_gate, g_down, g_comb, ns_down;  // g_gate, g_down: grids of the stage partitions
     size_t sm_router, sm_gate, sm_down;
 };
 
-Plan make_plan(const moe_layer& L, int q) {
+Plan make_plan(const moe_layer& L, int q, int k) {
     DeviceInfo di = device_info();
     Plan p{};
     p.g_router = (L.E + 1) / 2;
     p.sm_router = sizeof(uint16_t) * (size_t)q * L.H;
-    p.g_gate = di.sms;
+    // largest grid (at most the SM count) whose per-CTA share of the smallest possible stage list (a
+    // union of k experts) is at least the largest task / (kMaxPieces - 1): no task has more pieces
+    auto grid_for = [&](const StageList& L) {
+        const int64_t big = L.sA * L.cA > L.sB * L.cB ? L.sA * L.cA : L.sB * L.cB;
+        int64_t gg = L.total() * (kMaxPieces - 1) / big;
+        return (int)(gg < di.sms ? (gg < 1 ? 1 : gg) : di.sms);
+    };
+    p.g_gate = grid_for(gate_up_stages(k, L.H, L.I));
     p.sm_gate = cta_smem_bytes(GuRing::kBytes, tset_copy_bytes(L.H));
-    p.g_down = di.sms > kMinDownCtas ? di.sms : kMinDownCtas;
+    p.g_down = grid_for(down_stages(k, L.H, L.I));
     p.ns_down = cta_smem_bytes(DnRing<5>::kBytes, 2 * tset_copy_bytes(L.I)) + 2048 <= 227 * 1024 ? 5 : 2;
     p.sm_down = cta_smem_bytes(p.ns_down == 5 ? DnRing<5>::kBytes : DnRing<2>::kBytes, 2 * tset_copy_bytes(L.I));
     p.g_comb = (q * L.H + kCombineThreads - 1) / kCombineThreads;
@@ -1023,6 +1082,8 @@ int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, co
     da.m = ga.m;
     ga.q = da.q = Q;
     ga.k = da.k = k;
+    ga.G = p.g_gate;
+    da.G = p.g_down;
     ga.x = MODE == 0 ? x : ws.u;
     ga.ws = da.ws = ws;
     ga.magic = da.magic = kMagic;
@@ -1037,13 +1098,13 @@ int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, co
     ra.idx_out = idx_out; ra.w_out = w_out; ra.logits_out = logits_out;
     auto kdown = p.ns_down == 5 ? k_down<Q, MODE, 5> : k_down<Q, MODE, 2>;
     HpackArgs ha{};
-    ha.I = L.I; ha.k = k; ha.ks = (L.H / stage_k(2)) % 2 == 0 ? 2 : 1; ha.ws = ws;
+    ha.H = L.H; ha.I = L.I; ha.k = k; ha.G = p.g_gate; ha.ws = ws;
     if (cudaFuncSetAttribute(k_router<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_router) ||
         cudaFuncSetAttribute(k_gate_up<Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_gate) ||
         cudaFuncSetAttribute(kdown, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_down))
         return FPX_ECUDA;
     CombineArgs ca{};
-    ca.H = L.H; ca.k = k; ca.ws = ws; ca.ks = (L.I / stage_k(3)) % 2 == 0 ? 2 : 1; ca.out = out;
+    ca.H = L.H; ca.I = L.I; ca.k = k; ca.G = p.g_down; ca.ws = ws; ca.out = out;
     // timing events between the kernels would break the dependent-launch edges: no overlap then
     const bool pdl = ev == nullptr;
     cudaError_t e = cudaSuccess;
@@ -1112,7 +1173,7 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
     WsPtrs wp = ws_ptrs(ws, wl);
     // the router's arrival counter must start at zero; the router leaves it at zero
     if (cudaMemsetAsync(wp.nuni, 0, 16, s) != cudaSuccess) return FPX_ECUDA;
-    Plan p = make_plan(*layer, q);
+    Plan p = make_plan(*layer, q, k);
     return dispatch_q<0>(q, *layer, p, k, x, nullptr, y, idx_out, w_out, logits_out, nullptr, wp, true, nullptr, false, s);
 }
 
@@ -1133,7 +1194,7 @@ int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int
     const size_t state = sizeof(float) * (size_t)q * layers[0].H;
     if (r0 != rL && cudaMemcpyAsync(rL, r0, state, cudaMemcpyDeviceToDevice, s) != cudaSuccess) return FPX_ECUDA;
     if (cudaMemsetAsync(wp.nuni, 0, 16, s) != cudaSuccess) return FPX_ECUDA;
-    Plan p = make_plan(layers[0], q);
+    Plan p = make_plan(layers[0], q, k);
     for (int l = 0; l < n_layers; l++) {
         int32_t* io = idx_out ? idx_out + (size_t)l * q * k : nullptr;
         float* tr = r_trace ? r_trace + (size_t)l * q * layers[0].H : nullptr;
@@ -1160,7 +1221,7 @@ int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int
 
 namespace {
 
-constexpr size_t kStaticWsBytes = size_t(16) << 20;  // 16 MiB: the decode shapes need at most 8.7 MB
+constexpr size_t kStaticWsBytes = size_t(16) << 20;  // 16 MiB: the decode shapes need at most 14.3 MB
 __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
 // In host code `g_static_ws` only names the symbol; its device address differs per device and is

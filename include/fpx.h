@@ -92,6 +92,19 @@ int fpx_quantize(int fmt, const float* W, int64_t N, int64_t K, const float* blo
 int fpx_dequantize(int fmt, const uint8_t* Wq, int64_t N, int64_t K, float* W, int32_t* dev_status,
                    void* stream);
 
+/* Rearranges `count` packed matrices (N x K, format fmt; matrix m at src + m * src_stride) between the
+ * row-major layout and the box-tiled layout the MoE layer kernels read (matrix m at dst + m *
+ * dst_stride; the same number of bytes). Box-tiled: each matrix is cut into tiles of R rows x B bytes
+ * of each row (R x B = 256 x 80 for FP2, 256 x 112 for FP3, 64 x 272 for FP4); the tiles are stored
+ * contiguously in (row block, column piece) order, each with its R rows at a pitch of B bytes, so the
+ * byte at (row r, offset j within the row) is at ((r / R) * P + j / B) * R * B + (r % R) * B + j % B
+ * with P = row bytes / B. inverse = 0 tiles a row-major src, 1 restores row-major from a tiled src.
+ * Requires N % R == 0 and the row bytes (K / 32 * block bytes) a multiple of B; src, dst and the
+ * strides 16-byte aligned; src != dst. The blocks themselves are unchanged: this is a layout for
+ * streaming whole tiles with one bulk copy each, not part of the pages' format. */
+int fpx_tile_matrices(int fmt, const uint8_t* src, int64_t N, int64_t K, int count, int64_t src_stride,
+                      uint8_t* dst, int64_t dst_stride, int inverse, void* stream);
+
 /* y[t][n] = sum_k W[n][k] * x[t][k] for t < q (1 <= q <= 4): the dense FPX GEMV of the verify step.
  * Every packed block is read from memory and decoded once per call, whatever q. x is [q][K]
  * contiguous, binary32 (x_dtype FPX_DTYPE_F32) or bfloat16 (FPX_DTYPE_BF16); y is [q][N] binary32.
@@ -112,6 +125,7 @@ int moe_route_topk(const float* R, int E, int H, const uint16_t* x, int q, int k
 /* One MoE layer's weights (device pointers inside a host struct). Routed experts e = 0..E-1 are
  * stacked: expert e's gate matrix starts at gate + e*fpx_matrix_bytes(FP2, I, H); likewise up (FP2,
  * I x H) and down (FP3, H x I). The shared expert is FP4: sh_gate, sh_up [I][H], sh_down [H][I].
+ * Every expert matrix is in the box-tiled layout of fpx_tile_matrices.
  * router is binary32 [E][H]. H and I are multiples of 512 and at most 4608 (the tensor-core
  * kernels hold a 144 KB ring of weight boxes and two activation tables of 8*H bytes in shared
  * memory). [P-dsv4] paragraph 2,
@@ -150,7 +164,7 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
  * status word is copied to dev_status (nullable, device, 4-byte aligned) at the end of the call.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  *   - Shapes whose moe_workspace_bytes() exceeds 16 MiB fail with FPX_ESPACE (the decode shapes,
- *     H = 4096, I = 2048, E = 256, q <= 4, k <= 8, need at most 8.7 MB).
+ *     H = 4096, I = 2048, E = 256, q <= 4, k <= 8, need at most 14.3 MB).
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *     that device current; make that first call before capturing a stream into a graph.
  *   - Every call on a device shares the one array, which keeps the previous call's contents: calls

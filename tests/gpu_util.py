@@ -31,9 +31,11 @@ def read_status(st):
 
 
 class DeviceLayer:
-    """One MoE layer generated on the device with the seeded generator (layer index `layer`)."""
+    """One MoE layer generated on the device with the seeded generator (layer index `layer`), its expert
+    matrices rearranged into the box-tiled layout the layer kernels read. `scratch` (optional) is a
+    uint8 device tensor of at least E * max(matrix bytes) used for the row-major copies."""
 
-    def __init__(self, H, I, E, seed=0, layer=0):
+    def __init__(self, H, I, E, seed=0, layer=0, scratch=None):
         self.H, self.I, self.E, self.seed, self.layer = H, I, E, seed, layer
         self.mb_gu = fpx.fpx_matrix_bytes(2, I, H)
         self.mb_d = fpx.fpx_matrix_bytes(3, H, I)
@@ -42,13 +44,17 @@ class DeviceLayer:
         self.up = torch.empty(E * self.mb_gu, dtype=torch.uint8, device="cuda")
         self.down = torch.empty(E * self.mb_d, dtype=torch.uint8, device="cuda")
         self.sh = [torch.empty(self.mb_s, dtype=torch.uint8, device="cuda") for _ in range(3)]
+        need = E * max(self.mb_gu, self.mb_d)
+        tmp = scratch if scratch is not None and scratch.numel() >= need else torch.empty(need, dtype=torch.uint8, device="cuda")
         s = torch.cuda.current_stream().cuda_stream
-        synth.device_matrices(2, seed, layer, synth.GATE, 0, E, I, H, self.gate.data_ptr(), self.mb_gu, s)
-        synth.device_matrices(2, seed, layer, synth.UP, 0, E, I, H, self.up.data_ptr(), self.mb_gu, s)
-        synth.device_matrices(3, seed, layer, synth.DOWN, 0, E, H, I, self.down.data_ptr(), self.mb_d, s)
-        synth.device_matrices(4, seed, layer, synth.SH_GATE, 0, 1, I, H, self.sh[0].data_ptr(), self.mb_s, s)
-        synth.device_matrices(4, seed, layer, synth.SH_UP, 0, 1, I, H, self.sh[1].data_ptr(), self.mb_s, s)
-        synth.device_matrices(4, seed, layer, synth.SH_DOWN, 0, 1, H, I, self.sh[2].data_ptr(), self.mb_s, s)
+        for dst, fmt, tensor, count, N, K, mb in ((self.gate, 2, synth.GATE, E, I, H, self.mb_gu),
+                                                 (self.up, 2, synth.UP, E, I, H, self.mb_gu),
+                                                 (self.down, 3, synth.DOWN, E, H, I, self.mb_d),
+                                                 (self.sh[0], 4, synth.SH_GATE, 1, I, H, self.mb_s),
+                                                 (self.sh[1], 4, synth.SH_UP, 1, I, H, self.mb_s),
+                                                 (self.sh[2], 4, synth.SH_DOWN, 1, H, I, self.mb_s)):
+            synth.device_matrices(fmt, seed, layer, tensor, 0, count, N, K, tmp.data_ptr(), mb, s)
+            fpx.fpx_tile_matrices(fmt, tmp, N, K, count, mb, dst, mb, 0, s)
         self.R_host = synth.router(E, H, seed, layer)
         self.router = dev(self.R_host)
         self.c = fpx.moe_layer(H=H, I=I, E=E, router=self.router.data_ptr(), gate=self.gate.data_ptr(),

@@ -1,5 +1,6 @@
-"""moe_stack_verify against the oracle, layer by layer (teacher-forced on the GPU's residual), and the
-q = 1 pass bit-identical to column 0 of the q = 4 pass."""
+"""moe_stack_verify against the oracle, layer by layer (teacher-forced on the GPU's residual), for the
+q = 4 pass and for the q = 1 pass of its first column (checked on its own trace: the two may differ in
+rounding, since the kernels split the streamed work by the size of the expert union)."""
 import numpy as np
 import pytest
 import torch
@@ -37,18 +38,21 @@ def check_layer_step(L, r_in, r_out, idx, k):
     assert np.array_equal(own["idx"][ok], idx[ok])
 
 
-def check_stack(layers, q, k, sample):
-    H = layers[0].H
-    bits, vals = synth.tokens_bf16(q, H, seed=99)
-    r0 = vals.astype(np.float32)
-    rL, idx, tr = run_stack(layers, r0, q, k)
+def check_pass(layers, r0, k, sample):
+    rL, idx, tr = run_stack(layers, r0, r0.shape[0], k)
     assert np.array_equal(tr[0], r0)
     assert np.all(np.isfinite(rL))
     for l in sample:
         r_out = tr[l + 1] if l + 1 < len(layers) else rL
         check_layer_step(layers[l], tr[l], r_out, idx[l], k)
-    rL1, idx1, _ = run_stack(layers, r0[:1], 1, k)
-    assert np.array_equal(rL1[0], rL[0]) and np.array_equal(idx1[:, 0], idx[:, 0])
+
+
+def check_stack(layers, q, k, sample):
+    H = layers[0].H
+    bits, vals = synth.tokens_bf16(q, H, seed=99)
+    r0 = vals.astype(np.float32)
+    check_pass(layers, r0, k, sample)
+    check_pass(layers, r0[:1], k, sample)
 
 
 def test_stack_small():
