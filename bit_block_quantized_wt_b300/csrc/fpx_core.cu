@@ -344,11 +344,14 @@ int launch_gemv_cc(const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x
 // ------------------------------------------------------------------ box-tiled matrices
 
 // Box-tiled layout (the MoE layer kernels stream it with 1-D bulk copies): a matrix of N rows is cut
-// into tiles of tile_rows(fmt) rows x box_bytes(fmt) bytes of each row (256 x 80 FP2, 256 x 112 FP3,
-// 64 x 272 FP4), stored contiguously in the order (row block, column piece) with the tile's rows at a
-// pitch of box_bytes(fmt): the byte at (row r, offset j of the row) goes to
-// ((r / R) * P + j / B) * R * B + (r % R) * B + j % B, with R = tile_rows, B = box_bytes,
-// P = row_bytes / B. The permutation moves whole 16-byte units (B and row_bytes are multiples of 16).
+// into tiles of R = stage_rows(fmt) rows x B = box_bytes(fmt) bytes of each row (256 x 80 FP2, 256 x 112
+// FP3, 64 x 272 FP4), stored contiguously in the order (row block, column piece): tile
+// (r / R) * P + j / B for byte j of row r, P = row_bytes / B.
+// FP4 tiles hold the rows' bytes at a pitch of B. FP2 / FP3 tiles hold a code area of R rows x 64 / 96
+// bytes and then a scale area of R rows x 16 bytes, regrouped per row as described with
+// box_code_bytes (fpx_mma.cuh): FP2 word 4t + C = code word t % 2 of block 2C + t / 2; FP3 bytes
+// 24t .. 24t + 23 = the 3-bit codes of blocks 2C + t / 2, codes 16 (t % 2) .. +15, at the fields of
+// fp3_slot; scale 4h + C = the scale of block 2C + h.
 __global__ void k_tile(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t units, int64_t row_units,
                        int R, int B16, int64_t src_stride, int64_t dst_stride, int inverse) {
     const uint8_t* sm = src + (int64_t)blockIdx.y * src_stride;
@@ -361,6 +364,109 @@ __global__ void k_tile(const uint8_t* __restrict__ src, uint8_t* __restrict__ ds
         const int64_t v = r * row_units + j;
         if (inverse) reinterpret_cast<uint4*>(dm)[v] = reinterpret_cast<const uint4*>(sm)[u];
         else reinterpret_cast<uint4*>(dm)[u] = reinterpret_cast<const uint4*>(sm)[v];
+    }
+}
+
+// 3-bit code c of FP3 field (odd, p, half hh) in the three words W of a chunk pair.
+__device__ __forceinline__ void fp3_put(uint32_t (&W)[3], int odd, int p, int hh, uint32_t c) {
+    const int f = fp3_slot(odd, p);
+    if (f < 0) {
+        for (int i = 0; i < 3; i++) W[i] |= ((c >> i) & 1u) << (16 * hh);
+    } else {
+        W[f / 16] |= c << (16 * hh + f % 16);
+    }
+}
+__device__ __forceinline__ uint32_t fp3_get(const uint32_t (&W)[3], int odd, int p, int hh) {
+    const int f = fp3_slot(odd, p);
+    if (f < 0) {
+        uint32_t c = 0;
+        for (int i = 0; i < 3; i++) c |= ((W[i] >> (16 * hh)) & 1u) << i;
+        return c;
+    }
+    return (W[f / 16] >> (16 * hh + f % 16)) & 7u;
+}
+
+// FP2 / FP3: one thread per (row, column piece) regroups the B row-major bytes of the piece into the
+// tile's code and scale areas (or back, inverse).
+template <int FMT>
+__global__ void k_tile_rows(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t pieces, int64_t P,
+                            int64_t row_bytes, int64_t src_stride, int64_t dst_stride, int inverse) {
+    constexpr int B = box_bytes(FMT), BB = block_bytes(FMT), CB = box_code_bytes(FMT), R = 256;
+    const uint8_t* sm = src + (int64_t)blockIdx.y * src_stride;
+    uint8_t* dm = dst + (int64_t)blockIdx.y * dst_stride;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < pieces; u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = u / P, jt = u % P;
+        const int64_t rm = r * row_bytes + jt * B;  // row-major offset of the piece
+        const int64_t tb = ((r / R) * P + jt) * (int64_t)R * B;
+        const int64_t co = tb + (r % R) * CB, so = tb + (int64_t)R * CB + (r % R) * 16;
+        alignas(16) uint8_t x[B];
+        alignas(16) uint8_t c[CB];
+        alignas(16) uint8_t sc[16];
+        if (!inverse) {
+            for (int i = 0; i < B / 16; i++) reinterpret_cast<uint4*>(x)[i] = reinterpret_cast<const uint4*>(sm + rm)[i];
+            for (int h = 0; h < 2; h++)
+                for (int C = 0; C < 4; C++) {
+                    sc[2 * (4 * h + C)] = x[BB * (2 * C + h)];
+                    sc[2 * (4 * h + C) + 1] = x[BB * (2 * C + h) + 1];
+                }
+            if constexpr (FMT == 2) {
+                for (int t = 0; t < 4; t++)
+                    for (int C = 0; C < 4; C++)
+                        for (int b = 0; b < 4; b++) c[4 * (4 * t + C) + b] = x[BB * (2 * C + t / 2) + 2 + 4 * (t % 2) + b];
+            } else {
+                for (int t = 0; t < 4; t++)
+                    for (int m = 0; m < 2; m++) {
+                        uint32_t W[3] = {0u, 0u, 0u};
+                        for (int odd = 0; odd < 2; odd++) {
+                            const uint8_t* blk = x + BB * (2 * (2 * m + odd) + t / 2);
+                            for (int j = 0; j < 16; j++) {
+                                const int k = 16 * (t % 2) + j;
+                                const uint32_t l = (blk[2 + k / 4] >> (2 * (k % 4))) & 3u, hb = (blk[10 + k / 8] >> (k % 8)) & 1u;
+                                fp3_put(W, odd, j % 8, j / 8, l + 4u * hb);
+                            }
+                        }
+                        for (int i = 0; i < 3; i++)
+                            for (int b = 0; b < 4; b++) c[24 * t + 12 * m + 4 * i + b] = (uint8_t)(W[i] >> (8 * b));
+                    }
+            }
+            for (int i = 0; i < CB / 16; i++) reinterpret_cast<uint4*>(dm + co)[i] = reinterpret_cast<const uint4*>(c)[i];
+            reinterpret_cast<uint4*>(dm + so)[0] = reinterpret_cast<const uint4*>(sc)[0];
+        } else {
+            for (int i = 0; i < CB / 16; i++) reinterpret_cast<uint4*>(c)[i] = reinterpret_cast<const uint4*>(sm + co)[i];
+            reinterpret_cast<uint4*>(sc)[0] = reinterpret_cast<const uint4*>(sm + so)[0];
+            for (int h = 0; h < 2; h++)
+                for (int C = 0; C < 4; C++) {
+                    x[BB * (2 * C + h)] = sc[2 * (4 * h + C)];
+                    x[BB * (2 * C + h) + 1] = sc[2 * (4 * h + C) + 1];
+                }
+            if constexpr (FMT == 2) {
+                for (int t = 0; t < 4; t++)
+                    for (int C = 0; C < 4; C++)
+                        for (int b = 0; b < 4; b++) x[BB * (2 * C + t / 2) + 2 + 4 * (t % 2) + b] = c[4 * (4 * t + C) + b];
+            } else {
+                for (int i = 0; i < 8; i++) {  // clear the code bytes (lo and hi planes) of the 8 blocks
+                    for (int b = 2; b < BB; b++) x[BB * i + b] = 0;
+                }
+                for (int t = 0; t < 4; t++)
+                    for (int m = 0; m < 2; m++) {
+                        uint32_t W[3];
+                        for (int i = 0; i < 3; i++) {
+                            W[i] = 0u;
+                            for (int b = 0; b < 4; b++) W[i] |= (uint32_t)c[24 * t + 12 * m + 4 * i + b] << (8 * b);
+                        }
+                        for (int odd = 0; odd < 2; odd++) {
+                            uint8_t* blk = x + BB * (2 * (2 * m + odd) + t / 2);
+                            for (int j = 0; j < 16; j++) {
+                                const int k = 16 * (t % 2) + j;
+                                const uint32_t cc = fp3_get(W, odd, j % 8, j / 8);
+                                blk[2 + k / 4] |= (uint8_t)((cc & 3u) << (2 * (k % 4)));
+                                blk[10 + k / 8] |= (uint8_t)((cc >> 2) << (k % 8));
+                            }
+                        }
+                    }
+            }
+            for (int i = 0; i < B / 16; i++) reinterpret_cast<uint4*>(dm + rm)[i] = reinterpret_cast<const uint4*>(x)[i];
+        }
     }
 }
 
@@ -431,11 +537,23 @@ int fpx_tile_matrices(int fmt, const uint8_t* src, int64_t N, int64_t K, int cou
     const int64_t bytes = N * row_bytes;
     if (src_stride < bytes || dst_stride < bytes) return FPX_EINVAL;
     if (!aligned(src, 16) || !aligned(dst, 16) || src_stride % 16 || dst_stride % 16) return FPX_EALIGN;
-    const int64_t units = bytes / 16;
-    const int64_t gx = (units + 255) / 256 < 148 * 4 ? (units + 255) / 256 : 148 * 4;
     if (count > 65535) return FPX_EINVAL;
-    k_tile<<<dim3((unsigned)gx, (unsigned)count), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        src, dst, units, row_bytes / 16, R, B / 16, src_stride, dst_stride, inverse);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (fmt == 4) {
+        const int64_t units = bytes / 16;
+        const int64_t gx = (units + 255) / 256 < 148 * 4 ? (units + 255) / 256 : 148 * 4;
+        k_tile<<<dim3((unsigned)gx, (unsigned)count), 256, 0, s>>>(src, dst, units, row_bytes / 16, R, B / 16, src_stride,
+                                                                     dst_stride, inverse);
+    } else {
+        const int64_t pieces = N * (row_bytes / B);
+        const int64_t gx = (pieces + 127) / 128 < 148 * 8 ? (pieces + 127) / 128 : 148 * 8;
+        if (fmt == 2)
+            k_tile_rows<2><<<dim3((unsigned)gx, (unsigned)count), 128, 0, s>>>(src, dst, pieces, row_bytes / B, row_bytes,
+                                                                               src_stride, dst_stride, inverse);
+        else
+            k_tile_rows<3><<<dim3((unsigned)gx, (unsigned)count), 128, 0, s>>>(src, dst, pieces, row_bytes / B, row_bytes,
+                                                                               src_stride, dst_stride, inverse);
+    }
     return launch_status();
 }
 

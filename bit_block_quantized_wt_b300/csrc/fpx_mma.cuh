@@ -118,6 +118,42 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
     return false;
 }
 
+// The same on 32-bit shared addresses, for the consumer hot loops: one poll inline, the bounded
+// sleeping wait out of line (taken only when a stage has not landed yet).
+__device__ __forceinline__ bool mbar_poll(uint32_t b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(b), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Whole warp; true when every lane saw the phase complete within the wait limits.
+static __device__ __noinline__ bool mbar_wait_warp_slow(uint32_t b, uint32_t parity) {
+    bool done = mbar_poll(b, parity);
+    if (!done) {
+        const uint64_t t0 = global_ns();
+        for (uint32_t i = 0; i < kSpinLimit && !done; i++) {
+            uint32_t ok;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(ok)
+                : "r"(b), "r"(parity), "r"(kSleepNs)
+                : "memory");
+            done = ok != 0;
+            if (!done && global_ns() - t0 > kWaitNs) break;
+        }
+    }
+    return __all_sync(0xffffffffu, done);
+}
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t b, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_poll(b, parity)) || mbar_wait_warp_slow(b, parity);
+}
+__device__ __forceinline__ void mbar_arrive_u32(uint32_t b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(b) : "memory");
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -173,6 +209,18 @@ __host__ __device__ constexpr int pair_shift(int fmt, int i) {
 // Code positions (within the thread's 16-code group) held by the low and high half of pair i.
 __host__ __device__ constexpr int pair_lo(int fmt, int i) { return fmt == 4 ? 8 * (i / 4) + (i % 4) : i; }
 __host__ __device__ constexpr int pair_hi(int fmt, int i) { return fmt == 4 ? 8 * (i / 4) + (i % 4) + 4 : i + 8; }
+
+// FP3 field of pair p (0..7) of the even (odd = 0) or odd (odd = 1) chunk of a chunk pair: word w
+// (0..2 within the pair's three words) * 16 + bit position x of the code's low bit inside each binary16
+// half (x = 1, 4, 7: the code is already at mantissa bit x; x = 10, 13: after a shift right by 9, at
+// x - 9). -1: the pair of spare bits, code bit i at bit 0 of the half in word i.
+__host__ __device__ constexpr int fp3_slot(int odd, int p) {
+    return odd == 0 ? (p < 5 ? 3 * p + 1 : 16 + 3 * (p - 5) + 1) : (p < 2 ? 16 + 10 + 3 * p : p < 7 ? 32 + 3 * (p - 2) + 1 : -1);
+}
+// Mantissa position P of the code's low bit in the decoded binary16 (1024 + c 2^P).
+__host__ __device__ constexpr int fp3_box_shift(int odd, int p) {
+    return fp3_slot(odd, p) < 0 ? 1 : (fp3_slot(odd, p) % 16 > 9 ? fp3_slot(odd, p) % 16 - 9 : fp3_slot(odd, p) % 16);
+}
 
 constexpr uint32_t kMagic = 0x64006400u;  // binary16 pair (1024, 1024)
 constexpr uint32_t kTwo = f16x2(2.0);
@@ -361,6 +409,19 @@ __device__ __forceinline__ void pack_fp3(const float (&v)[16], int sh, uint32_t 
         part = fmaf(bl, 1024.0f + 3.5f * float(1 << pair_shift(3, p)), fmaf(bh, 1024.0f, part));
     }
 }
+// FP3 in the box layout (one plane, codes 0..7 at mantissa position P = fp3_box_shift(odd, p), odd =
+// the parity of the group's chunk): B = 2^(sh + 1 - P); the MMA sees sum (1024 + c 2^P) B = 2 sum c x'
+// + sum 1024 B, so the offset removed is sum B (1024 + 3.5 2^P), leaving sum (2c - 7) x'.
+__device__ __forceinline__ void pack_fp3b(const float (&v)[16], int sh, int odd, uint32_t (&w)[8], float& part) {
+    part = 0.f;
+#pragma unroll
+    for (int p = 0; p < 8; p++) {
+        const int P = odd ? fp3_box_shift(1, p) : fp3_box_shift(0, p);
+        const float sc = exp2i(sh + 1 - P);
+        w[p] = pack_h2(v[p] * sc, v[p + 8] * sc);
+        part = fmaf(h2lo(w[p]) + h2hi(w[p]), 1024.0f + 3.5f * float(1 << P), part);
+    }
+}
 __device__ __forceinline__ void pack_fp4(const float (&v)[16], int sh, uint32_t (&w)[8]) {
     const float sc = exp2i(sh);
 #pragma unroll
@@ -376,17 +437,21 @@ __device__ __forceinline__ void store_entry(uint2* tab, size_t e, const uint32_t
 // laid out as the MMA's initial accumulator of the lanes that decode the block.
 __host__ __device__ constexpr int oq_bytes(int K) { return K; }
 
-// A table set for K weights, as built in global memory and copied as one block into shared memory:
-// [table A (8K) | table B (8K) | offset quads (K)] and, in global memory only, 16 bytes of column
-// shifts. Gate/up: A = FP2, B = FP4. Down, routed expert: A = FP3 low plane, B = FP3 high plane;
-// shared expert: A = FP4.
+// Table sets for K weights, as built in global memory and copied as one block into shared memory,
+// followed in global memory only by 16 bytes of column shifts. Gate/up: [FP2 table (8K) | FP4 table
+// (8K) | offset quads (K)]. Down: [FP3 table (box layout, 8K) | offset quads (K)] for a routed expert,
+// [FP4 table (8K)] for the shared expert.
 __host__ __device__ constexpr int tset_copy_bytes(int K) { return 2 * btab_bytes(K) + oq_bytes(K); }
 __host__ __device__ constexpr int tset_bytes(int K) { return tset_copy_bytes(K) + 16; }
+__host__ __device__ constexpr int dset_copy_bytes(int K) { return btab_bytes(K) + oq_bytes(K); }
+__host__ __device__ constexpr int dset_bytes(int K) { return dset_copy_bytes(K) + 16; }
+// offset of the offset quads in a table set whose first table has format FA
+__host__ __device__ constexpr int set_oq_offset(int FA, int K) { return FA == 2 ? 2 * btab_bytes(K) : btab_bytes(K); }
 
 // Packs code group gi (16 consecutive activations v of token tok, starting at weight k0 of K) into a
-// table set at `ts` (global memory): FA is the format of table A (2: FP2 with FP4 in table B; 3: FP3
-// planes; 4: FP4 only). Returns the group's share of its block offset (0 for FP4). Lanes holding the
-// two groups of a block (gi even, gi + 1) add the shares with add_offsets().
+// table set at `ts` (global memory): FA is the format of the first table (2: FP2 with FP4 second; 3:
+// FP3 in the box layout; 4: FP4 only). Returns the group's share of its block offset (0 for FP4). Lanes
+// holding the two groups of a block (gi even, gi + 1) add the shares with add_offsets().
 template <int FA>
 __device__ __forceinline__ float pack_group(uint8_t* ts, int K, int tok, int k0, const float (&v)[16], int sh) {
     const int c = k0 >> 6, half = (k0 >> 5) & 1, hw = (k0 >> 4) & 1;
@@ -401,10 +466,9 @@ __device__ __forceinline__ float pack_group(uint8_t* ts, int K, int tok, int k0,
         pack_fp4(v, sh, w);
         store_entry(tb, e, w);
     } else if constexpr (FA == 3) {
-        uint32_t wh[8];
-        pack_fp3(v, sh, w, wh, part);
+        (void)tb;
+        pack_fp3b(v, sh, c & 1, w, part);
         store_entry(ta, e, w);
-        store_entry(tb, e, wh);
     } else {
         pack_fp4(v, sh, w);
         store_entry(ta, e, w);
@@ -414,10 +478,11 @@ __device__ __forceinline__ float pack_group(uint8_t* ts, int K, int tok, int k0,
 
 // Whole warp, after pack_group on lane pairs (2i, 2i + 1) = the two groups of one block: writes the
 // block's negated offset quad entries (valid lanes only).
+template <int FA>
 __device__ __forceinline__ void add_offsets(uint8_t* ts, int K, int tok, int k0, float part, bool valid) {
     const float nxt = __shfl_down_sync(0xffffffffu, part, 1);
     if (valid && ((k0 >> 4) & 1) == 0) {
-        float* qd = reinterpret_cast<float*>(ts + 2 * btab_bytes(K)) + (size_t)((k0 >> 5) * 2 + (tok >> 1)) * 4 + (tok & 1);
+        float* qd = reinterpret_cast<float*>(ts + set_oq_offset(FA, K)) + (size_t)((k0 >> 5) * 2 + (tok >> 1)) * 4 + (tok & 1);
         qd[0] = qd[2] = -(part + nxt);
     }
 }
@@ -917,6 +982,23 @@ struct CtaRing {
         if ((threadIdx.x & 31) == 0) mbar_arrive(empty + (n % NS));
     }
 
+    // Consumer position (slot index n % NS and phase (n / NS) & 1 of stage n), advanced
+    // incrementally so the hot loops need no division.
+    struct Pos {
+        uint32_t idx, ph;
+    };
+    __device__ __forceinline__ void next(Pos& p) const {
+        if (++p.idx == (uint32_t)NS) { p.idx = 0; p.ph ^= 1u; }
+    }
+    __device__ __forceinline__ uint32_t slot_at(const Pos& p) const { return smem_u32(slots) + p.idx * (uint32_t)SB; }
+    // Whole consumer warp: waits (bounded) for the stage at p; false on a timeout.
+    __device__ __forceinline__ bool wait_at(const Pos& p) const { return mbar_wait_warp(smem_u32(full) + p.idx * 8u, p.ph); }
+
+    __device__ __forceinline__ void release_at(const Pos& p) const {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive_u32(smem_u32(empty) + p.idx * 8u);
+    }
+
     // Producer: waits (bounded) until stage n's slot is free, i.e. every consumer released n - NS.
     __device__ __forceinline__ bool acquire(uint32_t n) const {
         return n < (uint32_t)NS || mbar_wait(empty + (n % NS), ((n / NS) + 1u) & 1u);
@@ -971,6 +1053,188 @@ __device__ inline CtaRing<NS, SB> cta_init(const CtaSmem& s) {
     fence_barrier_init();
     __syncthreads();
     return R;
+}
+
+// ------------------------------------------------------------------ box-internal layout
+
+// The layer kernels' FP2 and FP3 boxes are regrouped by the tiling transform (fpx_tile_matrices) so
+// that one thread reads its code words for all four chunks of a row with one or three loads and the
+// scales of a row with one load, and FP3 codes sit as contiguous 3-bit fields c = l + 4h (one MMA plane
+// instead of a low and a high plane). Thread t of a row decodes, for chunk C = 0..3, block 2C + t/2,
+// codes 16 (t % 2) + j (j = 0..15); pair p holds codes j = p (low binary16 half) and p + 8 (high half).
+//   FP2 box: codes [256 rows x 64 B]: word 4t + C of a row = code word t % 2 of block 2C + t / 2 (the
+//            row-major block's bytes 2 + 4 (t % 2) .. +3); scales [256 rows x 16 B].
+//   FP3 box: codes [256 rows x 96 B]: bytes 24t .. 24t + 23 of a row = words W0..W5; chunk pair
+//            (2m, 2m + 1) uses W3m..W3m+2 with the field positions of fp3_slot; scales as FP2.
+//   Scales: binary16 4h + C of a row = the scale of block 2C + h.
+// FP4 boxes keep the row-major bytes.
+__host__ __device__ constexpr int box_code_bytes(int fmt) { return fmt == 2 ? 64 : 96; }  // per box row
+__host__ __device__ constexpr int box_scale_offset(int fmt) { return 256 * box_code_bytes(fmt); }
+
+// Sixteen A pairs (two chunks) from the three words of a chunk pair, one LOP3 per pair (plus four
+// shifts): value 1024 + c 2^P with c the 3-bit code and P = fp3_box_shift.
+__device__ __forceinline__ void decode_fp3_box(uint32_t W0, uint32_t W1, uint32_t W2, uint32_t magic, uint32_t (&a)[8],
+                                               uint32_t (&b)[8]) {
+    const uint32_t u0 = W0 >> 9, u1 = W1 >> 9, u2 = W2 >> 9;
+    a[0] = (W0 & 0x000E000Eu) | magic;
+    a[1] = (W0 & 0x00700070u) | magic;
+    a[2] = (W0 & 0x03800380u) | magic;
+    a[3] = (u0 & 0x000E000Eu) | magic;
+    a[4] = (u0 & 0x00700070u) | magic;
+    a[5] = (W1 & 0x000E000Eu) | magic;
+    a[6] = (W1 & 0x00700070u) | magic;
+    a[7] = (W1 & 0x03800380u) | magic;
+    b[0] = (u1 & 0x000E000Eu) | magic;
+    b[1] = (u1 & 0x00700070u) | magic;
+    b[2] = (W2 & 0x000E000Eu) | magic;
+    b[3] = (W2 & 0x00700070u) | magic;
+    b[4] = (W2 & 0x03800380u) | magic;
+    b[5] = (u2 & 0x000E000Eu) | magic;
+    b[6] = (u2 & 0x00700070u) | magic;
+    b[7] = (((W0 << 1) & 0x00020002u) | ((W1 << 2) & 0x00040004u)) | (((W2 << 3) & 0x00080008u) | magic);
+}
+
+template <int OFF>
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(a), "n"(OFF));
+    return v;
+}
+
+// Scale of chunk C from a thread's four binary16 scales (chunks 0..3).
+template <int C>
+__device__ __forceinline__ float scale_of(const uint2& s) {
+    const uint32_t w = C < 2 ? s.x : s.y;
+    const __half2 h = *reinterpret_cast<const __half2*>(&w);
+    return (C & 1) ? __high2float(h) : __low2float(h);
+}
+
+// One consumer warp's share of a staged FP2/FP3 box (rows g and g + 8 of its two 16-row tiles): the
+// code words and scales, loaded in one pass so the ring slot can be released before the MMAs run.
+template <int FMT>
+struct Frag;
+template <>
+struct Frag<2> {
+    uint4 c[2][2];  // [tile][row g / g + 8]: words of chunks 0..3
+    uint2 s[2][2];
+};
+template <>
+struct Frag<3> {
+    uint2 c[2][2][3];  // words W0..W5
+    uint2 s[2][2];
+};
+
+// `row` = the warp's first row + g; t = lane % 4.
+template <int FMT>
+__device__ __forceinline__ void frag_load(Frag<FMT>& f, uint32_t slot, int row, int t) {
+    constexpr int CB = box_code_bytes(FMT);
+    const uint32_t cb = slot + (uint32_t)(row * CB + (FMT == 2 ? 16 : 24) * t);
+    const uint32_t sb = slot + (uint32_t)(box_scale_offset(FMT) + row * 16 + 8 * (t >> 1));
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const uint32_t r = (uint32_t)(16 * i + 8 * h);
+            if constexpr (FMT == 2) {
+                f.c[i][h] = lds128<0>(cb + r * CB);
+            } else {
+                f.c[i][h][0] = lds64<0>(cb + r * CB);
+                f.c[i][h][1] = lds64<8>(cb + r * CB);
+                f.c[i][h][2] = lds64<16>(cb + r * CB);
+            }
+            f.s[i][h] = lds64<0>(sb + r * 16);
+        }
+    }
+}
+
+template <int C>
+__device__ __forceinline__ uint32_t word_of(const uint4& c) {
+    return C == 0 ? c.x : C == 1 ? c.y : C == 2 ? c.z : c.w;
+}
+
+// MMAs of chunk C of both tiles: B registers from the lane's table entry b (32 bytes per chunk, 512
+// bytes per chunk in the table) and the offset quad from oq (64 bytes per chunk).
+__device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint32_t (&a0)[8], const uint32_t (&a8)[8], const uint4& b0,
+                                          const uint4& b1, const float4& c4) {
+    mma_c(acc, a0[0], a8[0], a0[1], a8[1], b0.x, b0.y, c4);
+    mma_acc(acc, a0[2], a8[2], a0[3], a8[3], b0.z, b0.w);
+    mma_acc(acc, a0[4], a8[4], a0[5], a8[5], b1.x, b1.y);
+    mma_acc(acc, a0[6], a8[6], a0[7], a8[7], b1.z, b1.w);
+}
+
+template <int C>
+__device__ __forceinline__ float4 oq_quad(uint32_t oq) {
+    const uint4 q = lds128<C * 64>(oq);
+    return make_float4(__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z), __uint_as_float(q.w));
+}
+
+// Chunks C0 and C0 + 1 of a fragment, accumulated into y[tile][4] (rows g, g + 8 as in box_tiles).
+template <int FMT, int C0>
+__device__ __forceinline__ void frag_mma(const Frag<FMT>& f, uint32_t b, uint32_t oq, uint32_t magic, float (&y)[2][4]) {
+    const uint4 b0 = lds128<C0 * 512>(b), b1 = lds128<C0 * 512 + 16>(b);
+    const uint4 e0 = lds128<(C0 + 1) * 512>(b), e1 = lds128<(C0 + 1) * 512 + 16>(b);
+    const float4 q0 = oq_quad<C0>(oq), q1 = oq_quad<C0 + 1>(oq);
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+        uint32_t a0[8], a8[8], c0[8], c8[8];
+        if constexpr (FMT == 2) {
+            decode_fp2(word_of<C0>(f.c[i][0]), magic, a0);
+            decode_fp2(word_of<C0>(f.c[i][1]), magic, a8);
+            decode_fp2(word_of<C0 + 1>(f.c[i][0]), magic, c0);
+            decode_fp2(word_of<C0 + 1>(f.c[i][1]), magic, c8);
+        } else {
+            constexpr int m = C0 / 2;
+            const uint32_t x0[6] = {f.c[i][0][0].x, f.c[i][0][0].y, f.c[i][0][1].x, f.c[i][0][1].y, f.c[i][0][2].x, f.c[i][0][2].y};
+            const uint32_t x8[6] = {f.c[i][1][0].x, f.c[i][1][0].y, f.c[i][1][1].x, f.c[i][1][1].y, f.c[i][1][2].x, f.c[i][1][2].y};
+            decode_fp3_box(x0[3 * m], x0[3 * m + 1], x0[3 * m + 2], magic, a0, c0);
+            decode_fp3_box(x8[3 * m], x8[3 * m + 1], x8[3 * m + 2], magic, a8, c8);
+        }
+        float acc[4], acd[4];
+        chunk_mma(acc, a0, a8, b0, b1, q0);
+        chunk_mma(acd, c0, c8, e0, e1, q1);
+        const float d0 = scale_of<C0>(f.s[i][0]), d8 = scale_of<C0>(f.s[i][1]);
+        const float f0 = scale_of<C0 + 1>(f.s[i][0]), f8 = scale_of<C0 + 1>(f.s[i][1]);
+        y[i][0] = fmaf(f0, acd[0], fmaf(d0, acc[0], y[i][0]));
+        y[i][1] = fmaf(f0, acd[1], fmaf(d0, acc[1], y[i][1]));
+        y[i][2] = fmaf(f8, acd[2], fmaf(d8, acc[2], y[i][2]));
+        y[i][3] = fmaf(f8, acd[3], fmaf(d8, acc[3], y[i][3]));
+    }
+}
+
+// Runs stages s_first .. s_end - 1 of one FP2/FP3 task (ring positions p, p + 1, ...) through a
+// double-buffered fragment: the next stage's words are loaded between the two halves of the current
+// stage's MMAs, and a stage's slot is released as soon as its words are in registers. b / q: the
+// lane's table entry and offset quad addresses for the task's stage s_first (advanced by b_step and
+// 256 bytes per stage). On a timeout the warp stops waiting and releasing (so the producer gives up
+// too) and ok turns false; the caller reports it.
+template <int FMT, class RING>
+__device__ __forceinline__ bool frag_step(const RING& R, const Frag<FMT>& cur, Frag<FMT>& nxt, typename RING::Pos& p, int& left,
+                                          int row, int t, uint32_t& b, uint32_t b_step, uint32_t& q, uint32_t magic,
+                                          float (&y)[2][4], bool& ok) {
+    if (ok) R.release_at(p);
+    R.next(p);
+    const bool more = --left > 0;
+    frag_mma<FMT, 0>(cur, b, q, magic, y);
+    if (more && ok) {
+        ok = R.wait_at(p);
+        if (ok) frag_load<FMT>(nxt, R.slot_at(p), row, t);
+    }
+    frag_mma<FMT, 2>(cur, b, q, magic, y);
+    b += b_step;
+    q += 256u;
+    return more;
+}
+
+template <int FMT, class RING>
+__device__ __forceinline__ void frag_stages(const RING& R, typename RING::Pos& p, int count, int row, int t, uint32_t b,
+                                            uint32_t b_step, uint32_t q, uint32_t magic, float (&y)[2][4], bool& ok) {
+    Frag<FMT> fa, fb;
+    if (ok) ok = R.wait_at(p);
+    if (ok) frag_load<FMT>(fa, R.slot_at(p), row, t);
+    int left = count;
+    while (frag_step<FMT>(R, fa, fb, p, left, row, t, b, b_step, q, magic, y, ok) &&
+           frag_step<FMT>(R, fb, fa, p, left, row, t, b, b_step, q, magic, y, ok)) {
+    }
 }
 
 // Adds the two FP4 partial sums of each row (warps w, w + 4) in warp order. Every consumer warp calls

@@ -57,7 +57,7 @@ inline Ws ws_layout(int H, int I, int E, int q, int k) {
     w.gu = o; o = up16(o + sizeof(float) * kMaxPieces * w.gu_piece);
     w.yi = o; o = up16(o + sizeof(float) * kMaxPieces * w.yi_piece);
     w.gt = o; o = up16(o + tset_bytes(H));
-    w.dt = o; o = up16(o + (size_t)(q * k + 1) * tset_bytes(I));
+    w.dt = o; o = up16(o + (size_t)(q * k + 1) * dset_bytes(I));
     w.total = o;
     return w;
 }
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
                     for (int j = 0; j < 16; j++) v[j] = tok < q ? __uint_as_float((uint32_t)u_s[(size_t)tok * H + k0 + j] << 16) : 0.f;
                     part = pack_group<2>(A.ws.gt, H, tok, k0, v, sh_s[tok]);
                 }
-                add_offsets(A.ws.gt, H, tok, k0, part, valid);
+                add_offsets<2>(A.ws.gt, H, tok, k0, part, valid);
             }
     }
     float acc[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
@@ -472,45 +472,48 @@ __device__ inline void load_route(Route& r, const WsPtrs& ws, int qk) {
 // kMaxPieces: the host caps G so that every CTA's share is at least the largest task / (kMaxPieces -
 // 1)), each written to its own partial buffer; the next kernel adds a task's pieces in order.
 struct StageList {
-    int64_t nA, sA, cA, nB, sB, cB;
-    __host__ __device__ __forceinline__ int64_t stages() const { return nA * sA + nB * sB; }
-    __host__ __device__ __forceinline__ int64_t total() const { return nA * sA * cA + nB * sB * cB; }
-    __host__ __device__ __forceinline__ int64_t cost_before(int64_t s) const {
-        const int64_t a = nA * sA;
+    // All products stay below 2^32: stages <= 22032, costs <= 64 and G <= 148 (checked on the host by
+    // partition_fits), so the partition needs only 32-bit divisions.
+    uint32_t nA, sA, cA, nB, sB, cB;
+    __host__ __device__ __forceinline__ uint32_t stages() const { return nA * sA + nB * sB; }
+    __host__ __device__ __forceinline__ uint32_t total() const { return nA * sA * cA + nB * sB * cB; }
+    __host__ __device__ __forceinline__ uint32_t cost_before(uint32_t s) const {
+        const uint32_t a = nA * sA;
         return s <= a ? s * cA : a * cA + (s - a) * cB;
     }
-    __host__ __device__ __forceinline__ int64_t owner(int64_t s, int64_t G) const { return cost_before(s) * G / total(); }
+    __host__ __device__ __forceinline__ uint32_t owner(uint32_t s, uint32_t G) const { return cost_before(s) * G / total(); }
     // first stage of CTA b (b == G: stages())
-    __host__ __device__ __forceinline__ int64_t first(int64_t b, int64_t G) const {
-        const int64_t a = nA * sA, tgt = total() * b;  // smallest s with cost_before(s) * G >= tgt
+    __host__ __device__ __forceinline__ uint32_t first(uint32_t b, uint32_t G) const {
+        const uint32_t a = nA * sA, tgt = total() * b;  // smallest s with cost_before(s) * G >= tgt
         if (tgt <= a * cA * G) return (tgt + G * cA - 1) / (G * cA);
         return a + (tgt - a * cA * G + G * cB - 1) / (G * cB);
     }
-    __host__ __device__ __forceinline__ int64_t task_of(int64_t s) const {
-        const int64_t a = nA * sA;
+    __host__ __device__ __forceinline__ uint32_t task_of(uint32_t s) const {
+        const uint32_t a = nA * sA;
         return s < a ? s / sA : nA + (s - a) / sB;
     }
-    __host__ __device__ __forceinline__ int64_t task_first(int64_t t) const { return t < nA ? t * sA : nA * sA + (t - nA) * sB; }
-    __host__ __device__ __forceinline__ int64_t task_len(int64_t t) const { return t < nA ? sA : sB; }
-    __host__ __device__ __forceinline__ int pieces(int64_t t, int64_t G) const {
-        const int64_t f = task_first(t);
+    __host__ __device__ __forceinline__ uint32_t task_first(uint32_t t) const { return t < nA ? t * sA : nA * sA + (t - nA) * sB; }
+    __host__ __device__ __forceinline__ uint32_t task_len(uint32_t t) const { return t < nA ? sA : sB; }
+    __host__ __device__ __forceinline__ int pieces(uint32_t t, uint32_t G) const {
+        const uint32_t f = task_first(t);
         return (int)(owner(f + task_len(t) - 1, G) - owner(f, G) + 1);
     }
-    __host__ __device__ __forceinline__ int piece(int64_t t, int64_t b, int64_t G) const { return (int)(b - owner(task_first(t), G)); }
+    __host__ __device__ __forceinline__ int piece(uint32_t t, uint32_t b, uint32_t G) const { return (int)(b - owner(task_first(t), G)); }
+    __host__ bool partition_fits(uint32_t G) const { return (uint64_t)nA * sA * cA + (uint64_t)nB * sB * cB <= 0xFFFFFFFFull / (G + 1); }
 };
 
-// Relative cost of a stage: bytes streamed, FP4 boxes weighted by 4/3 (their decode costs more per
-// byte).
-constexpr int kCostFP2 = stage_bytes(2), kCostFP3 = stage_bytes(3), kCostFP4 = stage_bytes(4) * 4 / 3;
+// Relative time of a stage (in units of about 1 KB of a fast decode): bytes streamed for FP2 and FP3;
+// FP4 boxes (17 KB) weighted for their slower decode, which the down kernel's FP3 stages outpace more.
+constexpr uint32_t kCostFP2 = 20, kCostFP3 = 28, kCostFP4Gu = 23, kCostFP4Dn = 34;
 
 // Stage lists of the gate/up kernel (FP2 tasks: matrix x 256-row block, H/256 stages; FP4: matrix x
 // 64-row block, H/512 stages) and of the down kernel (FP3: item x 256-row block, I/256 stages; FP4:
 // 64-row block, I/512 stages).
 __host__ __device__ inline StageList gate_up_stages(int n_uni, int H, int I) {
-    return StageList{(int64_t)2 * n_uni * (I / 256), H / stage_k(2), kCostFP2, (int64_t)2 * (I / 64), H / stage_k(4), kCostFP4};
+    return StageList{2u * n_uni * (I / 256), (uint32_t)(H / stage_k(2)), kCostFP2, 2u * (I / 64), (uint32_t)(H / stage_k(4)), kCostFP4Gu};
 }
 __host__ __device__ inline StageList down_stages(int n_uni, int H, int I) {
-    return StageList{(int64_t)n_uni * (H / 256), I / stage_k(3), kCostFP3, (int64_t)(H / 64), I / stage_k(4), kCostFP4};
+    return StageList{(uint32_t)n_uni * (H / 256), (uint32_t)(I / stage_k(3)), kCostFP3, (uint32_t)(H / 64), (uint32_t)(I / stage_k(4)), kCostFP4Dn};
 }
 
 // ------------------------------------------------------------------ K2: gate/up
@@ -546,7 +549,7 @@ struct GuTask {
     int64_t off;  // byte offset of the task's first tile in its (stacked) matrix
 };
 
-__device__ __forceinline__ GuTask gu_task(int64_t t, const Route& r, const LayerMaps& m) {
+__device__ __forceinline__ GuTask gu_task(uint32_t t, const Route& r, const LayerMaps& m) {
     const int I = m.I, rb2 = I / 256, n2 = 2 * r.n_uni * rb2;
     GuTask k;
     if (t < n2) {
@@ -589,14 +592,14 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
     load_route(r, A.ws, Q * A.k);
 
     const StageList SL = gate_up_stages(r.n_uni, H, I);
-    const int64_t G = A.G, s0 = SL.first(blockIdx.x, G), s1 = SL.first(blockIdx.x + 1, G);
+    const uint32_t G = A.G, s0 = SL.first(blockIdx.x, G), s1 = SL.first(blockIdx.x + 1, G);
 
     if (warp == kWarps) {  // producer: streams the range's boxes while the consumers load the tables
         if (lane == 0) {
             uint32_t issued = 0;
             bool live = true;
-            for (int64_t sg = s0; sg < s1 && live;) {
-                const int64_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
+            for (uint32_t sg = s0; sg < s1 && live;) {
+                const uint32_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
                 const GuTask k = gu_task(tk, r, A.m);
                 for (; sg < te; sg++, issued++) {
                     if (!R.acquire(issued)) { flag(A.ws.status, FPX_ETIMEOUT); live = false; break; }
@@ -621,29 +624,32 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
     // out, so a timeout never leaves a barrier short of arrivals.
     const int a_idx = b_active_index(lane);
     const uint32_t magic = A.magic;
-    const LaneOfs L2 = lane_ofs<2>(t), L4 = lane_ofs<4>(t);
-    uint32_t n = 0, bad = 0;
-    for (int64_t sg = s0; sg < s1;) {
+    const LaneOfs L4 = lane_ofs<4>(t);
+    const uint32_t tab2_lane = lane_tab(tab2, S.zero, a_idx, 0), tab2_step = a_idx >= 0 ? 4u * 512u : 0u;
+    const uint32_t oq2_lane = lane_oq(oq2, 0, t);
+    uint32_t bad = 0;
+    typename decltype(R)::Pos pos{0u, 0u};
+    for (uint32_t sg = s0; sg < s1;) {
         // the stages of one task inside this CTA's range: one piece of the task
-        const int64_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
+        const uint32_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
         const GuTask k = gu_task(tk, r, A.m);
         float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        for (; sg < te; sg++, n++) {
+        if (!k.fp4) {
+            const uint32_t s = (uint32_t)(sg - tf);
+            frag_stages<2>(R, pos, (int)(te - sg), warp * 32 + g, t, tab2_lane + s * tab2_step, tab2_step, oq2_lane + s * 256u,
+                           magic, y, ok);
+            sg = te;
+        }
+        for (; sg < te; sg++) {  // FP4 (shared expert) stages
             const int s = (int)(sg - tf);
-            if (ok) ok = R.wait(n, A.ws.status);
-            if (!ok) continue;  // the producer gives up too once this warp stops releasing
-            const uint8_t* slot = R.slot(n);
-            if (!k.fp4) {
-                const int ch0 = s * box_chunks(2);
-                box_tiles<2, 2, box_chunks(2)>(smem_u32(slot) + (warp * 32 + g) * box_bytes(2), L2,
-                                               lane_tab(tab2, S.zero, a_idx, ch0), 0u, lane_oq(oq2, ch0, t), magic, y, bad);
-            } else {
+            if (ok) ok = R.wait_at(pos);
+            if (ok) {  // after a timeout the producer gives up too once this warp stops releasing
                 const int ch0 = s * box_chunks(4) + 4 * (warp >> 2);
-                box_tiles<4, 1, 4>(smem_u32(slot) + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4), L4,
-                                   lane_tab(tab4, S.zero, a_idx, ch0), 0u, 0u, magic,
-                                   *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
+                box_tiles<4, 1, 4>(R.slot_at(pos) + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4), L4,
+                                   lane_tab(tab4, S.zero, a_idx, ch0), 0u, 0u, magic, *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
+                R.release_at(pos);
             }
-            R.release(n);
+            R.next(pos);
         }
         pair_reduce(y[0]);
         pair_reduce(y[1]);
@@ -663,6 +669,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
             }
         }
     }
+    if (!ok && lane == 0) flag(A.ws.status, FPX_ETIMEOUT);
     report_bad(bad, A.ws.status);
 }
 
@@ -692,7 +699,7 @@ __global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__
     const int I = A.I, j = blockIdx.x / 4, tok = blockIdx.x % 4;
     const int n_uni = __ldcg(A.ws.nuni);  // the router kernel's (completed before the gate/up kernel ran)
     if (j > n_uni) return;
-    uint8_t* ts = A.ws.dt + (size_t)j * tset_bytes(I);
+    uint8_t* ts = A.ws.dt + (size_t)j * dset_bytes(I);
     float m = 0.f;
     if (tok < Q) {
         grid_dep_wait();  // g and u come from the gate/up kernel
@@ -705,7 +712,7 @@ __global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__
         const int rbs = j < n_uni ? 256 : 64, nrb = I / rbs;
         if (threadIdx.x < 2 * nrb) {
             const int m = threadIdx.x / nrb, rb = threadIdx.x % nrb;
-            const int64_t tk = j < n_uni ? (int64_t)(2 * j + m) * nrb + rb : SL.nA + (int64_t)m * nrb + rb;
+            const uint32_t tk = j < n_uni ? (uint32_t)(2 * j + m) * nrb + rb : SL.nA + (uint32_t)m * nrb + rb;
             np_s[m][rb] = (int8_t)SL.pieces(tk, A.G);
         }
         __syncthreads();
@@ -752,7 +759,7 @@ __global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__
         float mm = 0.f;
         for (int w = 0; w < kHpackThreads / 32; w++) mm = fmaxf(mm, red[w]);
         sh_s = column_shift(mm);
-        reinterpret_cast<int*>(ts + tset_copy_bytes(I))[tok] = sh_s;
+        reinterpret_cast<int*>(ts + dset_copy_bytes(I))[tok] = sh_s;
     }
     __syncthreads();
     // this token's I / 16 groups; the two groups of a block sit on lanes (2i, 2i + 1)
@@ -771,7 +778,7 @@ __global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__
             }
             part = j < n_uni ? pack_group<3>(ts, I, tok, k0, v, sh_s) : pack_group<4>(ts, I, tok, k0, v, sh_s);
         }
-        if (j < n_uni) add_offsets(ts, I, tok, k0, part, valid);  // CTA-uniform condition
+        if (j < n_uni) add_offsets<3>(ts, I, tok, k0, part, valid);  // CTA-uniform condition
     }
 }
 
@@ -795,7 +802,7 @@ struct DnTask {
     int64_t off;  // byte offset of the task's first tile in its (stacked) matrix
 };
 
-__device__ __forceinline__ DnTask dn_task(int64_t t, const Route& r, const LayerMaps& m) {
+__device__ __forceinline__ DnTask dn_task(uint32_t t, const Route& r, const LayerMaps& m) {
     const int H = m.H, rb3 = H / 256, n3 = r.n_uni * rb3;
     DnTask k;
     if (t < n3) {
@@ -834,7 +841,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
     load_route(r, A.ws, Q * A.k);
 
     const StageList SL = down_stages(r.n_uni, H, I);
-    const int64_t G = A.G, s0 = SL.first(blockIdx.x, G), s1 = SL.first(blockIdx.x + 1, G);
+    const uint32_t G = A.G, s0 = SL.first(blockIdx.x, G), s1 = SL.first(blockIdx.x + 1, G);
     if (s0 >= s1) return;  // CTA-uniform: nothing to do
     const int item_lo = dn_task(SL.task_of(s0), r, A.m).item, item_hi = dn_task(SL.task_of(s1 - 1), r, A.m).item;
     if (item_hi - item_lo > 1) {  // cannot happen for the grids make_plan picks (each share < one item)
@@ -846,8 +853,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
         if (lane == 0) {
             uint32_t issued = 0;
             bool live = true;
-            for (int64_t sg = s0; sg < s1 && live;) {
-                const int64_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
+            for (uint32_t sg = s0; sg < s1 && live;) {
+                const uint32_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
                 const DnTask k = dn_task(tk, r, A.m);
                 for (; sg < te; sg++, issued++) {
                     if (!R.acquire(issued)) { flag(A.ws.status, FPX_ETIMEOUT); live = false; break; }
@@ -863,14 +870,14 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
     grid_dep_wait();
     const int nit = item_hi - item_lo + 1;
     if (threadIdx.x == 0) {
-        mbar_expect_tx(S.tbar, nit * tset_copy_bytes(I));
+        mbar_expect_tx(S.tbar, nit * dset_copy_bytes(I));
         for (int sl = 0; sl < nit; sl++)
-            bulk_load(S.tabs + (size_t)sl * tset_copy_bytes(I), A.ws.dt + (size_t)(item_lo + sl) * tset_bytes(I), tset_copy_bytes(I),
+            bulk_load(S.tabs + (size_t)sl * dset_copy_bytes(I), A.ws.dt + (size_t)(item_lo + sl) * dset_bytes(I), dset_copy_bytes(I),
                       S.tbar);
     }
     if (threadIdx.x < 2 * kMaxQ) {
         const int sl = threadIdx.x / kMaxQ, tk = threadIdx.x % kMaxQ;
-        shift[sl][tk] = sl < nit ? __ldcg(reinterpret_cast<const int*>(A.ws.dt + (size_t)(item_lo + sl) * tset_bytes(I) + tset_copy_bytes(I)) + tk) : 0;
+        shift[sl][tk] = sl < nit ? __ldcg(reinterpret_cast<const int*>(A.ws.dt + (size_t)(item_lo + sl) * dset_bytes(I) + dset_copy_bytes(I)) + tk) : 0;
     }
     bool ok = __any_sync(0xffffffffu, mbar_wait(S.tbar, 0));
     if (!ok && lane == 0) flag(A.ws.status, FPX_ETIMEOUT);
@@ -880,34 +887,34 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
     // out, so a timeout never leaves a barrier short of arrivals.
     const int a_idx = b_active_index(lane);
     const uint32_t magic = A.magic;
-    const LaneOfs L3 = lane_ofs<3>(t), L4 = lane_ofs<4>(t);
-    uint32_t n = 0, bad = 0;
-    for (int64_t sg = s0; sg < s1;) {
+    const LaneOfs L4 = lane_ofs<4>(t);
+    uint32_t bad = 0;
+    typename decltype(R)::Pos pos{0u, 0u};
+    for (uint32_t sg = s0; sg < s1;) {
         // the stages of one task inside this CTA's range: one piece of the task
-        const int64_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
+        const uint32_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
         const DnTask k = dn_task(tk, r, A.m);
         const int sl = k.item - item_lo;
-        const uint8_t* ts = S.tabs + (size_t)sl * tset_copy_bytes(I);
-        const uint2* tlo = reinterpret_cast<const uint2*>(ts);
-        const uint2* thi = reinterpret_cast<const uint2*>(ts + btab_bytes(I));
-        const float* oq = reinterpret_cast<const float*>(ts + 2 * btab_bytes(I));
+        const uint8_t* ts = S.tabs + (size_t)sl * dset_copy_bytes(I);
+        const uint2* tab = reinterpret_cast<const uint2*>(ts);
+        const float* oq = reinterpret_cast<const float*>(ts + btab_bytes(I));
         float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        for (; sg < te; sg++, n++) {
+        if (!k.fp4) {
+            const uint32_t s = (uint32_t)(sg - tf), b_step = a_idx >= 0 ? 4u * 512u : 0u;
+            frag_stages<3>(R, pos, (int)(te - sg), warp * 32 + g, t, lane_tab(tab, S.zero, a_idx, 0) + s * b_step, b_step,
+                           lane_oq(oq, 0, t) + s * 256u, magic, y, ok);
+            sg = te;
+        }
+        for (; sg < te; sg++) {  // FP4 (shared expert) stages
             const int s = (int)(sg - tf);
-            if (ok) ok = R.wait(n, A.ws.status);
-            if (!ok) continue;
-            const uint8_t* slot = R.slot(n);
-            if (!k.fp4) {
-                const int ch0 = s * box_chunks(3);
-                box_tiles<3, 2, box_chunks(3)>(smem_u32(slot) + (warp * 32 + g) * box_bytes(3), L3, lane_tab(tlo, S.zero, a_idx, ch0),
-                                               lane_tab(thi, S.zero, a_idx, ch0), lane_oq(oq, ch0, t), magic, y, bad);
-            } else {
+            if (ok) ok = R.wait_at(pos);
+            if (ok) {
                 const int ch0 = s * box_chunks(4) + 4 * (warp >> 2);
-                box_tiles<4, 1, 4>(smem_u32(slot) + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4), L4,
-                                   lane_tab(tlo, S.zero, a_idx, ch0), 0u, 0u, magic,
-                                   *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
+                box_tiles<4, 1, 4>(R.slot_at(pos) + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4), L4,
+                                   lane_tab(tab, S.zero, a_idx, ch0), 0u, 0u, magic, *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
+                R.release_at(pos);
             }
-            R.release(n);
+            R.next(pos);
         }
         pair_reduce(y[0]);
         pair_reduce(y[1]);
@@ -926,6 +933,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
             }
         }
     }
+    if (!ok && lane == 0) flag(A.ws.status, FPX_ETIMEOUT);
     report_bad(bad, A.ws.status);
 }
 
@@ -966,7 +974,7 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(const __grid_consta
     for (int i = threadIdx.x; i < (r.n_uni + 1) * 4; i += blockDim.x) {
         const int jj = i / 4, sub = i % 4;
         int np = 0;
-        if (jj < r.n_uni) np = sub == 0 ? SL.pieces((int64_t)jj * (H / 256) + row0 / 256, A.G) : 0;
+        if (jj < r.n_uni) np = sub == 0 ? SL.pieces((uint32_t)jj * (H / 256) + row0 / 256, A.G) : 0;
         else np = SL.pieces(SL.nA + row0 / 64 + sub, A.G);
         np_s[jj][sub] = (int8_t)np;
     }
@@ -1022,7 +1030,11 @@ int check_layer(const moe_layer* L) {
     // shared memory (plus up to 2 KB of static): gate/up ring + one table set for K = H; down ring
     // (2 slots at least) + two table sets for K = I
     if (cta_smem_bytes(GuRing::kBytes, tset_copy_bytes(L->H)) + 2048 > 227 * 1024 ||
-        cta_smem_bytes(DnRing<2>::kBytes, 2 * tset_copy_bytes(L->I)) + 2048 > 227 * 1024)
+        cta_smem_bytes(DnRing<2>::kBytes, 2 * dset_copy_bytes(L->I)) + 2048 > 227 * 1024)
+        return FPX_EINVAL;
+    // the stage partitions' 32-bit arithmetic, for the largest union and grid
+    const int nmax = kMaxQ * kMaxK < L->E ? kMaxQ * kMaxK : L->E;
+    if (!gate_up_stages(nmax, L->H, L->I).partition_fits(1024) || !down_stages(nmax, L->H, L->I).partition_fits(1024))
         return FPX_EINVAL;
     return FPX_OK;
 }
@@ -1047,8 +1059,8 @@ Plan make_plan(const moe_layer& L, int q, int k) {
     p.g_gate = grid_for(gate_up_stages(k, L.H, L.I));
     p.sm_gate = cta_smem_bytes(GuRing::kBytes, tset_copy_bytes(L.H));
     p.g_down = grid_for(down_stages(k, L.H, L.I));
-    p.ns_down = cta_smem_bytes(DnRing<5>::kBytes, 2 * tset_copy_bytes(L.I)) + 2048 <= 227 * 1024 ? 5 : 2;
-    p.sm_down = cta_smem_bytes(p.ns_down == 5 ? DnRing<5>::kBytes : DnRing<2>::kBytes, 2 * tset_copy_bytes(L.I));
+    p.ns_down = cta_smem_bytes(DnRing<5>::kBytes, 2 * dset_copy_bytes(L.I)) + 2048 <= 227 * 1024 ? 5 : 2;
+    p.sm_down = cta_smem_bytes(p.ns_down == 5 ? DnRing<5>::kBytes : DnRing<2>::kBytes, 2 * dset_copy_bytes(L.I));
     p.g_comb = (q * L.H + kCombineThreads - 1) / kCombineThreads;
     return p;
 }
