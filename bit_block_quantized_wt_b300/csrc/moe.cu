@@ -234,8 +234,9 @@ __global__ void k_topk(const float* __restrict__ logits, int E, int q, int k, in
 // Computes the layer input u (bfloat16, in shared memory) and logits[t][e] for this CTA's 2 experts.
 // MODE 0: input x is bfloat16. MODE 1: input is the residual r; u = RN_bf16(r / rms(r)) in one pass
 // over r held in registers (q * H / 4 <= kRouterV * kRouterThreads float4 groups), and CTA 0
-// publishes u (for the gate/up kernel) and r (the trace). 16 warps per expert, each a sixteenth of
-// H; the slice sums are added in order. With k > 0, the last CTA to finish routes every token (top-k,
+// publishes u (for the gate/up kernel) and r (the trace). 15 warps per expert, each a fifteenth of H;
+// the slice sums are added in order; the last warp packs this CTA's slice of the gate/up activation
+// tables meanwhile. With k > 0, the last CTA to finish routes every token (top-k,
 // weights, union) and publishes the routing for the gate/up and down kernels.
 constexpr int kRouterThreads = 1024;
 constexpr int kRouterV = 5;  // q * H <= 20480: H <= 5120 at q = 4
@@ -255,6 +256,34 @@ struct RouterArgs {
     float* logits_out;
 };
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// One warp packs this CTA's slice of the gate/up activation table set (4 token slots x H / 16 code
+// groups; FP2, FP4 and block offsets) from u in shared memory. The slice has an even length, so the two
+// groups of a block sit on lanes (2i, 2i + 1); absent tokens get zero entries.
+__device__ __forceinline__ void pack_gate_up_slice(const uint16_t* u_s, const int* sh_s, uint8_t* gt, int H, int q) {
+    const int lane = threadIdx.x & 31;
+    const int ngr = 4 * H / 16, per = (((ngr + (int)gridDim.x - 1) / (int)gridDim.x) + 1) & ~1;
+    const int gs = blockIdx.x * per;
+    for (int gb = gs; gb < gs + per && gb < ngr; gb += 32) {
+        const int gi = gb + lane;
+        const bool valid = gi < ngr && gi < gs + per;
+        const int tok = valid ? gi * 16 / H : 0, k0 = valid ? gi * 16 - tok * H : 0;
+        float part = 0.f;
+        if (valid) {
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++) v[j] = tok < q ? __uint_as_float((uint32_t)u_s[(size_t)tok * H + k0 + j] << 16) : 0.f;
+            part = pack_group<2>(gt, H, tok, k0, v, sh_s[tok]);
+        }
+        add_offsets<2>(gt, H, tok, k0, part, valid);
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant__ RouterArgs A) {
     const float* __restrict__ R = A.R;
@@ -267,12 +296,18 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
     int32_t* status_to_clear = A.status_to_clear;
     extern __shared__ __align__(16) uint16_t u_s[];  // [q][H] bfloat16 bits
     __shared__ float red[kRouterThreads / 32][kMaxQ];
+    __shared__ float redm[kRouterThreads / 32][kMaxQ];
     __shared__ float inv_s[kMaxQ];
+    __shared__ int sh_s[kMaxQ];
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    // expert e = 2 * blockIdx + (warp / 16); warp slice of the row's H / 4 float4 groups. The first
-    // batch of router weights does not depend on the previous kernel: load it before waiting.
-    const int e = blockIdx.x * 2 + warp / 16, sl = warp % 16;
-    const int h4r = H / 4, g0 = h4r * sl / 16, g1 = h4r * (sl + 1) / 16;
+    // expert e = 2 * blockIdx + (warp >= kSlices): warps 0 .. kSlices - 1 and kSlices .. 2 kSlices - 1
+    // each take a slice of the row's H / 4 float4 groups (the same slicing for both, so equal rows
+    // give bit-equal logits); the last warp packs the gate/up tables meanwhile (k > 0). The first batch
+    // of router weights does not depend on the previous kernel: load it before waiting.
+    constexpr int kSlices = 15, kPackWarp = kRouterThreads / 32 - 1;
+    const int e = blockIdx.x * 2 + (warp >= kSlices), sl = warp % kSlices;
+    const bool dots = warp < 2 * kSlices;
+    const int h4r = H / 4, g0 = h4r * sl / kSlices, g1 = dots ? h4r * (sl + 1) / kSlices : g0;
     const float4* row = reinterpret_cast<const float4*>(R + (size_t)(e < E ? e : 0) * H);
     float4 pre[4];
 #pragma unroll
@@ -281,12 +316,23 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
     grid_dep_wait();  // r and the workspace come from the previous kernel
     if (status_to_clear && blockIdx.x == 0 && threadIdx.x == 0) *status_to_clear = 0;
     const int n4 = q * H / 4;  // groups of 4 consecutive elements (H % 16 == 0: never across tokens)
+    // token of group idx (H / 4 groups per token), without a division
+    auto tok_of = [h4r](int idx) { return (idx >= h4r) + (idx >= 2 * h4r) + (idx >= 3 * h4r); };
+    // per-token maxima of |u| (the tables' column scales) and, MODE 1, sums of squares of r
+    float ss[kMaxQ] = {0.f, 0.f, 0.f, 0.f}, mx[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
+    float4 rv[kRouterV];
     if (MODE == 0) {
-        for (int i = threadIdx.x; i < n4; i += blockDim.x) reinterpret_cast<uint2*>(u_s)[i] = reinterpret_cast<const uint2*>(xin)[i];
+        for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+            const uint2 pk = reinterpret_cast<const uint2*>(xin)[i];
+            reinterpret_cast<uint2*>(u_s)[i] = pk;
+            const float mm = fmaxf(fmaxf(fabsf(__uint_as_float(pk.x << 16)), fabsf(__uint_as_float(pk.x & 0xFFFF0000u))),
+                                   fmaxf(fabsf(__uint_as_float(pk.y << 16)), fabsf(__uint_as_float(pk.y & 0xFFFF0000u))));
+            const int t = tok_of(i);
+#pragma unroll
+            for (int tt = 0; tt < kMaxQ; tt++) mx[tt] = tt == t ? fmaxf(mx[tt], mm) : mx[tt];
+        }
     } else {
         const float4* r4 = reinterpret_cast<const float4*>(rin);
-        float4 rv[kRouterV];
-        float ss[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < kRouterV; i++) {
             const int idx = threadIdx.x + i * kRouterThreads;
@@ -296,36 +342,53 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
         for (int i = 0; i < kRouterV; i++) {
             const int idx = threadIdx.x + i * kRouterThreads;
             if (idx < n4) {
-                const int t = idx * 4 / H;
+                const int t = tok_of(idx);
                 float a = 0.f;
                 a = fmaf(rv[i].x, rv[i].x, a); a = fmaf(rv[i].y, rv[i].y, a);
                 a = fmaf(rv[i].z, rv[i].z, a); a = fmaf(rv[i].w, rv[i].w, a);
+                const float mm = fmaxf(fmaxf(fabsf(rv[i].x), fabsf(rv[i].y)), fmaxf(fabsf(rv[i].z), fabsf(rv[i].w)));
 #pragma unroll
-                for (int tt = 0; tt < kMaxQ; tt++) ss[tt] += tt == t ? a : 0.f;
+                for (int tt = 0; tt < kMaxQ; tt++) {
+                    ss[tt] += tt == t ? a : 0.f;
+                    mx[tt] = tt == t ? fmaxf(mx[tt], mm) : mx[tt];
+                }
             }
         }
+    }
+    // block reductions (fixed xor butterflies over lanes, then over warps)
 #pragma unroll
-        for (int tt = 0; tt < kMaxQ; tt++) ss[tt] = warp_sum(ss[tt]);
-        if (lane == 0)
+    for (int tt = 0; tt < kMaxQ; tt++) {
+        if (MODE == 1) ss[tt] = warp_sum(ss[tt]);
+        mx[tt] = warp_max(mx[tt]);
+    }
+    if (lane == 0)
 #pragma unroll
-            for (int tt = 0; tt < kMaxQ; tt++) red[warp][tt] = ss[tt];
-        __syncthreads();
-        if (threadIdx.x < kMaxQ) {
-            float s = 0.f;
-            for (int w = 0; w < kRouterThreads / 32; w++) s += red[w][threadIdx.x];
-            inv_s[threadIdx.x] = 1.0f / sqrtf(s / (float)H + 1e-6f);
+        for (int tt = 0; tt < kMaxQ; tt++) { red[warp][tt] = ss[tt]; redm[warp][tt] = mx[tt]; }
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int tt = 0; tt < kMaxQ; tt++) {
+            const float s = MODE == 1 ? warp_sum(red[lane][tt]) : 0.f, m = warp_max(redm[lane][tt]);
+            if (lane == 0) {
+                // max |u| = RN_bf16(max |r| * inv): rounding and scaling by inv > 0 are monotonic
+                const float iv = MODE == 1 ? 1.0f / sqrtf(s / (float)H + 1e-6f) : 1.0f;
+                const float mu = MODE == 1 ? __bfloat162float(__float2bfloat16_rn(m * iv)) : m;
+                inv_s[tt] = iv;
+                sh_s[tt] = column_shift(mu);
+                if (A.k > 0 && blockIdx.x == 0) reinterpret_cast<int*>(A.ws.gt + tset_copy_bytes(H))[tt] = sh_s[tt];
+            }
         }
-        __syncthreads();
+    }
+    __syncthreads();
+    if (MODE == 1) {
 #pragma unroll
         for (int i = 0; i < kRouterV; i++) {
             const int idx = threadIdx.x + i * kRouterThreads;
             if (idx < n4) {
-                const float iv = inv_s[idx * 4 / H];
-                const uint32_t b0 = __bfloat16_as_ushort(__float2bfloat16_rn(rv[i].x * iv));
-                const uint32_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(rv[i].y * iv));
-                const uint32_t b2 = __bfloat16_as_ushort(__float2bfloat16_rn(rv[i].z * iv));
-                const uint32_t b3 = __bfloat16_as_ushort(__float2bfloat16_rn(rv[i].w * iv));
-                const uint2 pk = make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
+                const float iv = inv_s[tok_of(idx)];
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(rv[i].x * iv, rv[i].y * iv);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(rv[i].z * iv, rv[i].w * iv);
+                const uint2 pk = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
                 reinterpret_cast<uint2*>(u_s)[idx] = pk;
                 if (blockIdx.x == 0) {
                     reinterpret_cast<uint2*>(u_out)[idx] = pk;
@@ -333,63 +396,16 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
                 }
             }
         }
-    }
-    __syncthreads();
-    if (A.k > 0) {
-        // the gate/up activation tables (FP2, FP4, offsets) of u: every CTA has all of u, computes the
-        // column shifts and packs its slice of the code groups into the global table set
-        __shared__ int sh_s[kMaxQ];
-        float m[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
-        for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-            const uint2 pk = reinterpret_cast<const uint2*>(u_s)[i];
-            const float mm = fmaxf(fmaxf(fabsf(__uint_as_float(pk.x << 16)), fabsf(__uint_as_float(pk.x & 0xFFFF0000u))),
-                                   fmaxf(fabsf(__uint_as_float(pk.y << 16)), fabsf(__uint_as_float(pk.y & 0xFFFF0000u))));
-            const int t = i * 4 / H;
-#pragma unroll
-            for (int tt = 0; tt < kMaxQ; tt++) m[tt] = tt == t ? fmaxf(m[tt], mm) : m[tt];
-        }
-#pragma unroll
-        for (int tt = 0; tt < kMaxQ; tt++) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m[tt] = fmaxf(m[tt], __shfl_xor_sync(0xffffffffu, m[tt], o));
-        }
-        if (lane == 0)
-#pragma unroll
-            for (int tt = 0; tt < kMaxQ; tt++) red[warp][tt] = m[tt];
         __syncthreads();
-        if (threadIdx.x < kMaxQ) {
-            float mm = 0.f;
-            for (int w = 0; w < kRouterThreads / 32; w++) mm = fmaxf(mm, red[w][threadIdx.x]);
-            sh_s[threadIdx.x] = column_shift(mm);
-            if (blockIdx.x == 0) reinterpret_cast<int*>(A.ws.gt + tset_copy_bytes(H))[threadIdx.x] = sh_s[threadIdx.x];
-        }
-        __syncthreads();
-        // 4 token slots x H / 16 groups; this CTA's slice has an even length, so the two groups of a
-        // block sit on lanes (2i, 2i + 1) of warp 0; absent tokens get zero entries
-        const int ngr = 4 * H / 16, per = (((ngr + (int)gridDim.x - 1) / (int)gridDim.x) + 1) & ~1;
-        const int gs = blockIdx.x * per;
-        if (warp == 0)
-            for (int gb = gs; gb < gs + per && gb < ngr; gb += 32) {
-                const int gi = gb + lane;
-                const bool valid = gi < ngr && gi < gs + per;
-                const int tok = valid ? gi * 16 / H : 0, k0 = valid ? gi * 16 - tok * H : 0;
-                float part = 0.f;
-                if (valid) {
-                    float v[16];
-#pragma unroll
-                    for (int j = 0; j < 16; j++) v[j] = tok < q ? __uint_as_float((uint32_t)u_s[(size_t)tok * H + k0 + j] << 16) : 0.f;
-                    part = pack_group<2>(A.ws.gt, H, tok, k0, v, sh_s[tok]);
-                }
-                add_offsets<2>(A.ws.gt, H, tok, k0, part, valid);
-            }
     }
+    if (A.k > 0 && warp == kPackWarp) pack_gate_up_slice(u_s, sh_s, A.ws.gt, H, q);
     float acc[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
     if (e < E) {
         for (int base = g0 + lane; base < g1; base += 4 * 32) {
-            float4 rv[4];
+            float4 wv[4];
 #pragma unroll
             for (int b = 0; b < 4; b++)
-                rv[b] = base == g0 + lane ? pre[b] : base + 32 * b < g1 ? __ldg(row + base + 32 * b) : make_float4(0.f, 0.f, 0.f, 0.f);
+                wv[b] = base == g0 + lane ? pre[b] : base + 32 * b < g1 ? __ldg(row + base + 32 * b) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int b = 0; b < 4; b++) {
                 const int h4 = base + 32 * b;
@@ -398,10 +414,10 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
                 for (int t = 0; t < kMaxQ; t++) {
                     if (t < q) {
                         const uint2 ub = reinterpret_cast<const uint2*>(u_s + (size_t)t * H)[h4];
-                        acc[t] = fmaf(rv[b].x, __uint_as_float(ub.x << 16), acc[t]);
-                        acc[t] = fmaf(rv[b].y, __uint_as_float(ub.x & 0xFFFF0000u), acc[t]);
-                        acc[t] = fmaf(rv[b].z, __uint_as_float(ub.y << 16), acc[t]);
-                        acc[t] = fmaf(rv[b].w, __uint_as_float(ub.y & 0xFFFF0000u), acc[t]);
+                        acc[t] = fmaf(wv[b].x, __uint_as_float(ub.x << 16), acc[t]);
+                        acc[t] = fmaf(wv[b].y, __uint_as_float(ub.x & 0xFFFF0000u), acc[t]);
+                        acc[t] = fmaf(wv[b].z, __uint_as_float(ub.y << 16), acc[t]);
+                        acc[t] = fmaf(wv[b].w, __uint_as_float(ub.y & 0xFFFF0000u), acc[t]);
                     }
                 }
             }
@@ -416,14 +432,15 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
         const int el = threadIdx.x / q, t = threadIdx.x % q;
         const int ee = blockIdx.x * 2 + el;
         if (ee < E) {
-            float s = red[el * 16][t];
-            for (int w = 1; w < 16; w++) s += red[el * 16 + w][t];
+            const int w0 = el * kSlices;
+            float s = red[w0][t];
+            for (int w = 1; w < kSlices; w++) s += red[w0 + w][t];
             logits[(size_t)t * E + ee] = s;
         }
     }
     if (A.k == 0) return;
-    // the last CTA to finish routes every token (one thread publishes the CTA's logits: the barrier
-    // orders them before its fence and atomic)
+    // The last CTA to finish routes every token (one thread publishes the CTA's logits: the barrier
+    // orders them before its fence and atomic).
     __shared__ Route rt;
     __shared__ int last;
     __syncthreads();
@@ -950,6 +967,7 @@ struct CombineArgs {
 };
 
 constexpr int kCombineThreads = 256;
+constexpr int kCombineBatch = 17;  // items whose loads are in flight together: q * k = 16 routed + shared
 constexpr int kKernelsPerLayer = 5;  // router, gate/up, h + down tables, down, combine
 
 template <int Q, int MODE>
@@ -985,32 +1003,33 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(const __grid_consta
     const int tok = o / H, rr = o % H;
     const float* col = A.ws.yi + (size_t)tok * H + rr;
     const size_t istride = (size_t)Q * H;
-    // loads in batches of 8 items (pieces added in order), then the fixed-order sum; item n_uni is
-    // the shared expert, added last
+    // every piece slot of items 0 .. q * k lies in the workspace, so the loads of a batch are issued
+    // unconditionally (all in flight at once) and unused values are dropped; then the fixed-order sum
+    // (pieces of an item in order, items in ascending expert order, the shared expert n_uni last)
     float acc = 0.0f, ysh = 0.0f;
     bool first = true;
-    for (int j0 = 0; j0 <= r.n_uni; j0 += 8) {
-        float yv[8];
+    const int jmax = Q * A.k;  // last item slot of the workspace
+    for (int j0 = 0; j0 <= r.n_uni; j0 += kCombineBatch) {
+        float pv[kCombineBatch][kMaxPieces];
 #pragma unroll
-        for (int u = 0; u < 8; u++) {
-            const int jj = j0 + u;
-            const int np = jj > r.n_uni ? 0 : jj < r.n_uni ? np_s[jj][0] : np_s[jj][(rr - row0) / 64];
-            float pv[kMaxPieces];
+        for (int u = 0; u < kCombineBatch; u++) {
+            const int jj = min(j0 + u, jmax);
 #pragma unroll
-            for (int p = 0; p < kMaxPieces; p++) pv[p] = p < np ? __ldcg(col + p * A.ws.yi_piece + (size_t)jj * istride) : 0.0f;
-            yv[u] = pv[0];
-#pragma unroll
-            for (int p = 1; p < kMaxPieces; p++)
-                if (p < np) yv[u] += pv[p];
+            for (int p = 0; p < kMaxPieces; p++) pv[u][p] = __ldcg(col + p * A.ws.yi_piece + (size_t)jj * istride);
         }
 #pragma unroll
-        for (int u = 0; u < 8; u++) {
+        for (int u = 0; u < kCombineBatch; u++) {
             const int jj = j0 + u;
-            if (jj == r.n_uni) ysh = yv[u];
-            if (jj >= r.n_uni) continue;
+            if (jj > r.n_uni) break;
+            const int np = jj < r.n_uni ? np_s[jj][0] : np_s[jj][(rr - row0) / 64];
+            float yv = pv[u][0];
+#pragma unroll
+            for (int p = 1; p < kMaxPieces; p++)
+                if (p < np) yv += pv[u][p];
+            if (jj == r.n_uni) { ysh = yv; break; }
             const float wv = wsel[jj][tok];
             if (wv != wv) continue;  // expert not selected by this token
-            acc = first ? wv * yv[u] : fmaf(wv, yv[u], acc);
+            acc = first ? wv * yv : fmaf(wv, yv, acc);
             first = false;
         }
     }
