@@ -301,22 +301,29 @@ def e2e_pass(runner, steps, world):
     return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
 
+LAYER_SOURCES = ("fpx_common.cuh", "fpx_mma.cuh", "moe.cu")  # what the MoE layer kernels are built from
+
+
 def csrc_digest():
+    """Digest of the layer kernels' sources and header: a recorded DRAM count is used only while it
+    matches, i.e. while the profiled kernels are unchanged."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "bit_block_quantized_wt_b300", "csrc")
-    for n in sorted(os.listdir(d)):
-        if n.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(d, n), "rb").read())
+    for n in LAYER_SOURCES:
+        h.update(open(os.path.join(d, n), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "fpx.h"), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current sources."""
+def recorded_traffic(kernel, alg_bytes):
+    """DRAM bytes per launch from the committed ncu capture, if it was taken on the current sources: the
+    captured launch's DRAM bytes per algorithmic byte (its union differs from the average one) times
+    this run's algorithmic bytes per launch."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
         if t.get("csrc") == csrc_digest() and kernel in t.get("kernels", {}):
-            return t["kernels"][kernel]["dram_bytes_per_launch"]
+            return round(t["kernels"][kernel]["dram_per_algorithmic_byte"] * alg_bytes)
     except Exception:
         pass
     return None
@@ -425,7 +432,7 @@ def run_fpx(args):
         "kernels_ms": {n: round(float(v), 5) for n, v in zip(names, kavg)},
         "roofline": {"kernel": names[dom], "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(names[dom]), "algorithmic_bytes_per_launch": round(alg[dom]),
+                     "traffic": recorded_traffic(names[dom], alg[dom]), "algorithmic_bytes_per_launch": round(alg[dom]),
                      "avg_launch_ms": round(float(kavg[dom]), 5)},
         "e2e": {"value": round(e2e_bytes / e2e_secs / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
