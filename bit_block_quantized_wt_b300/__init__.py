@@ -69,6 +69,11 @@ _SIGS = {
                                         ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                         ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_prefill_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(moe_layer), ctypes.c_int, ctypes.c_int]),
+    "moe_layer_prefill": (ctypes.c_int, [ctypes.POINTER(moe_layer), ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                         ctypes.c_void_p]),
 }
 
 # Every symbol include/fpx.h declares (the export test checks them against the header).
@@ -186,3 +191,16 @@ def moe_stack_verify(layers, r0, q, k, rL, ws, ws_bytes, idx_out=None, r_trace=N
         ev = (ctypes.c_void_p * len(events))(*events)
     _check(lib().moe_stack_verify(arr, len(layers), _ptr(r0), q, k, _ptr(rL), _ptr(idx_out),
                                   _ptr(r_trace), _ptr(ws), ws_bytes, ev, _stream(stream)), "moe_stack_verify")
+
+
+def moe_prefill_workspace_bytes(layer, T, k):
+    return lib().moe_prefill_workspace_bytes(ctypes.byref(layer), T, k)
+
+
+def moe_layer_prefill(layer, x, T, k, y, ws, ws_bytes, idx_out=None, w_out=None, logits_out=None, perm_out=None,
+                      offsets_out=None, stream=None):
+    """Batched prefill of one layer over T tokens (see include/fpx.h)."""
+    _check(lib().moe_layer_prefill(ctypes.byref(layer), _ptr(x), T, k, _ptr(y), _ptr(idx_out), _ptr(w_out),
+                                   _ptr(logits_out), _ptr(perm_out), _ptr(offsets_out), _ptr(ws), ws_bytes,
+                                   _stream(stream)),
+           "moe_layer_prefill")

@@ -191,6 +191,30 @@ int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int
                      int32_t* idx_out, float* r_trace, void* ws, size_t ws_bytes, void* const* events,
                      void* stream);
 
+/* Workspace bytes moe_layer_prefill needs for T tokens and top-k (16-byte aligned; about
+ * T*k*(10 I + 4 H) + T*(10 I + 6 H) bytes: 0.55 GB at T = 2048, k = 6, H = 4096, I = 2048).
+ * 0 for invalid arguments. */
+size_t moe_prefill_workspace_bytes(const moe_layer* layer, int T, int k);
+
+/* Batched prefill of one MoE layer over T tokens (T >= 1, 1 <= k <= 8, k <= E <= 1024):
+ *   - route every token as moe_route_topk does (binary32 logits, top-k by logit with ties to the
+ *     lower expert index, sigmoid weights renormalised over the k selected);
+ *   - stable argsort of the T*k pairs p = t*k + r by expert: perm[s] = p lists the pairs in expert
+ *     order, p ascending within an expert; offsets[e] .. offsets[e+1] is expert e's range;
+ *   - run each routed expert once over its pairs (grouped GEMMs on the tensor cores over the same
+ *     box-tiled weights as moe_layer_decode: g = G x, u = U x, h = silu(g) u in binary32, y = D h)
+ *     and the shared expert over all tokens;
+ *   - out[t] = sum_r w[t][r] y_{e(t,r)}[t] (ranks in order) + y_shared[t].
+ * x is bfloat16 [T][H], y binary32 [T][H]. Nullable outputs: idx_out [T][k], w_out [T][k],
+ * logits_out [T][E], perm_out [T*k], offsets_out [E+1]. The GEMMs take the activations as binary16 rows scaled by a
+ * power of two per row (h likewise), so every product is exact and only binary32 sums round. ws
+ * holds moe_prefill_workspace_bytes(layer, T, k) bytes (ws_bytes); its first word is the status
+ * word. [P-dsv4] paragraph 3 (TOP_K, ARGSORT), [P-apu] section "Lucebox's Optimization Trio"; the
+ * grouping of a batch by expert is this project's reading (the pages describe decode). */
+int moe_layer_prefill(const moe_layer* layer, const uint16_t* x, int T, int k, float* y, int32_t* idx_out,
+                      float* w_out, float* logits_out, int32_t* perm_out, int32_t* offsets_out, void* ws,
+                      size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
