@@ -61,6 +61,49 @@ def peaks():
         return 6400.0, "fallback"
 
 
+def bf16_peak():
+    """Measured dense bf16 tensor throughput (TFLOP/s) of the B300s: burst (a kernel timed on
+    its own), or the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1800.0, "fallback"
+
+
+PF_T, PF_K = 2048, 6  # the prefill workload: one layer, 2048 tokens, top-6
+
+
+def prefill_measure(fpx, layer, warmup, reps=10):
+    """moe_layer_prefill of one stack layer on 2048 synthetic tokens (bfloat16 N(0,1), seeded), timed
+    with CUDA events over `reps` calls after `warmup` calls; FLOPs are the dense contraction's
+    2 * (2 I H (T k + T) + H I (T k + T))."""
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(5)
+    x = torch.randn(PF_T, H, device="cuda", generator=g).to(torch.bfloat16)
+    wsb = fpx.moe_prefill_workspace_bytes(layer, PF_T, PF_K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    y = torch.empty(PF_T, H, device="cuda")
+    for _ in range(warmup):
+        fpx.moe_layer_prefill(layer, x, PF_T, PF_K, y, ws, wsb)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        fpx.moe_layer_prefill(layer, x, PF_T, PF_K, y, ws, wsb)
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    P = PF_T * PF_K
+    flops = 2 * (2 * I * H * (P + PF_T) + H * I * (P + PF_T))
+    peak, kind = bf16_peak()
+    tf = flops / (ms / 1e3) / 1e12
+    return {"workload": f"prefill of one layer (config above): {PF_T} tokens, top-{PF_K}, bfloat16 N(0,1) "
+                        "synthetic tokens", "ms_per_layer": round(ms, 4), "tflops": round(tf, 1),
+            "gflop_per_layer": round(flops / 1e9, 1), "peak_tflops": peak, "peak_kind": f"{kind} bf16 dense (burst)",
+            "frac": round(tf / peak, 4), "tokens_per_s": round(PF_T / (ms / 1e3), 1), "reps": reps}
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -301,7 +344,7 @@ def e2e_pass(runner, steps, world):
     return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
 
-LAYER_SOURCES = ("fpx_common.cuh", "fpx_mma.cuh", "moe.cu")  # what the MoE layer kernels are built from
+LAYER_SOURCES = ("fpx_common.cuh", "fpx_mma.cuh", "route.cuh", "moe.cu")  # what the MoE layer kernels are built from
 
 
 def csrc_digest():
@@ -411,6 +454,8 @@ def run_fpx(args):
     e2e_secs, h2d, d2h = e2e_pass(r4, e2e_steps, world)
     e2e_bytes = sum(bytes_per_batch[i % N_BATCHES] for i in range(e2e_steps)) * world
 
+    pf = prefill_measure(fpx, stack.layers[0], args.warmup)
+
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -436,6 +481,7 @@ def run_fpx(args):
                      "avg_launch_ms": round(float(kavg[dom]), 5)},
         "e2e": {"value": round(e2e_bytes / e2e_secs / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "prefill": pf,
         "gpu_launches": args.steps * NK * args.layers,
         "clocks": clk.summary(),
     }

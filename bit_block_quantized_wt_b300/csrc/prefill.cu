@@ -112,33 +112,45 @@ __global__ void __launch_bounds__(256) k_to_f16(const void* __restrict__ src, in
 // ------------------------------------------------------------------ routing
 
 // logits[t][e] = sum_h R[e][h] x[t][h] (binary32; the sum runs over h in order for every (t, e), so
-// equal router rows give equal logits). Tile: 64 tokens x 64 experts, 16 x 16 threads of 4 x 4.
+// equal router rows give equal logits). Tile: 64 tokens x 64 experts, 16 x 16 threads of 4 x 4; the
+// next 32-wide slice of h is loaded into registers while the current one is used.
 __global__ void __launch_bounds__(256) k_plogits(const float* __restrict__ R, const uint16_t* __restrict__ x, int T,
                                                  int E, int H, float* __restrict__ logits) {
-    __shared__ float xs[32][65];
-    __shared__ float rs[32][65];
+    __shared__ float xs[2][32][65];
+    __shared__ float rs[2][32][65];
     const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
     const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
     float acc[4][4] = {};
-    for (int h0 = 0; h0 < H; h0 += 32) {
-        for (int i = threadIdx.x; i < 64 * 32; i += 256) {
-            const int rr = i / 32, kk = i % 32;
+    float xv[8], rv[8];
+    auto load = [&](int h0) {
+#pragma unroll
+        for (int v = 0; v < 8; v++) {
+            const int i = threadIdx.x + 256 * v, rr = i / 32, kk = i % 32;
             const int t = t0 + rr, e = e0 + rr;
-            xs[kk][rr] = t < T ? __uint_as_float((uint32_t)x[(size_t)t * H + h0 + kk] << 16) : 0.f;
-            rs[kk][rr] = e < E ? R[(size_t)e * H + h0 + kk] : 0.f;
+            xv[v] = t < T ? __uint_as_float((uint32_t)x[(size_t)t * H + h0 + kk] << 16) : 0.f;
+            rv[v] = e < E ? R[(size_t)e * H + h0 + kk] : 0.f;
+        }
+    };
+    load(0);
+    for (int h0 = 0, buf = 0; h0 < H; h0 += 32, buf ^= 1) {
+#pragma unroll
+        for (int v = 0; v < 8; v++) {
+            const int i = threadIdx.x + 256 * v, rr = i / 32, kk = i % 32;
+            xs[buf][kk][rr] = xv[v];
+            rs[buf][kk][rr] = rv[v];
         }
         __syncthreads();
+        if (h0 + 32 < H) load(h0 + 32);
 #pragma unroll 8
         for (int kk = 0; kk < 32; kk++) {
             float a[4], b[4];
 #pragma unroll
-            for (int i = 0; i < 4; i++) { a[i] = xs[kk][ty + 16 * i]; b[i] = rs[kk][tx + 16 * i]; }
+            for (int i = 0; i < 4; i++) { a[i] = xs[buf][kk][ty + 16 * i]; b[i] = rs[buf][kk][tx + 16 * i]; }
 #pragma unroll
             for (int i = 0; i < 4; i++)
 #pragma unroll
                 for (int j = 0; j < 4; j++) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
-        __syncthreads();
     }
 #pragma unroll
     for (int i = 0; i < 4; i++)
@@ -350,7 +362,7 @@ __device__ __forceinline__ float blk_scale(uint32_t wbox, int row, int b, uint32
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kGemmThreads, 1) k_pgemm(const __grid_constant__ PGemmArgs A) {
+__global__ void __launch_bounds__(kGemmThreads, 2) k_pgemm(const __grid_constant__ PGemmArgs A) {
     using G = PGeo<FMT>;
     extern __shared__ __align__(128) uint8_t smem[];
     int32_t* brow_s = reinterpret_cast<int32_t*>(smem + 2 * G::BUF);
