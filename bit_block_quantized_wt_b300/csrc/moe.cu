@@ -1214,7 +1214,7 @@ int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int
 
 namespace {
 
-constexpr size_t kStaticWsBytes = size_t(16) << 20;  // 16 MiB: the decode shapes need at most 14.3 MB
+constexpr size_t kStaticWsBytes = size_t(16) << 20;  // 16 MiB: the decode shapes need at most 13.7 MB
 __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
 // In host code `g_static_ws` only names the symbol; its device address differs per device and is

@@ -35,9 +35,11 @@
  *     index out of range) set bit (1 << status) of a device status word: the `dev_status` argument
  *     (the caller zeroes it), or the first word of the workspace (zeroed by each layer or stack call
  *     when it starts). Read it after the stream completes (fpx_read_status).
- *   - Results are deterministic: no floating-point atomics; every reduction has a fixed order that
- *     depends on neither q nor the other columns, so column t of a q-column call is bit-identical to
- *     the same column computed alone.
+ *   - Results are deterministic: no floating-point atomics, and every reduction has a fixed order
+ *     for given inputs and shapes, so a repeated call gives the same bits. In fpx_gemv_q that order
+ *     depends on neither q nor the other columns (column t is bit-identical to a q = 1 call). In the
+ *     layer calls the streamed work is split by the size of the expert union, so a column's rounding
+ *     can change with the other columns of the batch (never its routing), within the tolerance.
  */
 #ifndef FPX_H
 #define FPX_H
@@ -164,7 +166,7 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
  * status word is copied to dev_status (nullable, device, 4-byte aligned) at the end of the call.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  *   - Shapes whose moe_workspace_bytes() exceeds 16 MiB fail with FPX_ESPACE (the decode shapes,
- *     H = 4096, I = 2048, E = 256, q <= 4, k <= 8, need at most 14.3 MB).
+ *     H = 4096, I = 2048, E = 256, q <= 4, k <= 8, need at most 13.7 MB).
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *     that device current; make that first call before capturing a stream into a graph.
  *   - Every call on a device shares the one array, which keeps the previous call's contents: calls
