@@ -19,11 +19,11 @@
 //   k_ph       h = silu(g) u (binary32), then binary16 rows scaled by a per-row power of two
 //   k_pcombine out[t] = sum_r w[t][r] y[inv[t*k+r]] (ranks in order) + y_shared[t]
 //
-// GEMM arithmetic. The tensor-core A operand is the code itself as an exact binary16 value
-// (2c - 3 for FP2, 2c - 7 for FP3, the E2M1 value times 2^-14 for FP4); B is the activation row in
-// binary16 times its power-of-two scale. Each MMA pair covers one 32-weight block, so its binary32
-// partial is multiplied by the block's scale (binary32) before it joins the accumulator:
-// y = sum_blocks d_b * sum_k code_k x_k, every product exact, only the binary32 sums round.
+// GEMM arithmetic. B is the activation row in binary16 times its power-of-two scale (exact). FP2 /
+// FP3: the A operand is the weight d (2c - 3) or d (2c - 7) rounded once to binary16 (relative error
+// at most 2^-11 per weight, a quarter of the 2e-3 bound), so the MMAs accumulate across blocks. FP4:
+// A is the E2M1 value times 2^-14 (exact) and each MMA pair covers one 32-weight block whose binary32
+// partial is multiplied by the block scale 2^(e-127) (exact for every exponent).
 #include "fpx_mma.cuh"
 #include "route.cuh"
 
@@ -306,6 +306,12 @@ __device__ __forceinline__ uint32_t fp3_code(uint32_t W0, uint32_t W1, uint32_t 
 // holding codes 16 ww + 4t + {0, 1} and {2, 3} of the block (B is loaded with the same order). A code c
 // placed at binary16 mantissa bit P reads 1024 + c 2^P; one HFMA2 maps it to 2c - 3 (FP2) or 2c - 7
 // (FP3) with constants exact in binary16 (P >= 1 keeps them within 11 significant bits).
+__device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 template <int FMT>
 __device__ __forceinline__ void a_frag(uint32_t wbox, int row, int b, int ww, int t, uint32_t& a0, uint32_t& a2) {
     if constexpr (FMT == 2) {
@@ -342,6 +348,15 @@ __device__ __forceinline__ void a_frag(uint32_t wbox, int row, int b, int ww, in
         a0 = ((v2 & 0x00070007u) << 9) | ((v2 & 0x00080008u) << 12);
         a2 = ((v3 & 0x00070007u) << 9) | ((v3 & 0x00080008u) << 12);
     }
+}
+
+// FP2 / FP3: the binary16 scale of block b of a row, in both halves of a pair.
+template <int FMT>
+__device__ __forceinline__ uint32_t blk_scale2(uint32_t wbox, int row, int b) {
+    const int C = b >> 1, hb = b & 1;
+    uint16_t d;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(d) : "r"(wbox + (uint32_t)(box_scale_offset(FMT) + row * 16 + 2 * (4 * hb + C))));
+    return (uint32_t)d | ((uint32_t)d << 16);
 }
 
 // Scale of block b of a row (binary32); FP4: 2^(e - 127) * 2^14 (undoing the decode's 2^-14), 0 and a
@@ -440,8 +455,19 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_pgemm(const __grid_constant
                     a_frag<FMT>(wbox, r0, b, ww, t, af[i][ww][0], af[i][ww][2]);
                     a_frag<FMT>(wbox, r8, b, ww, t, af[i][ww][1], af[i][ww][3]);
                 }
-                d[i][0] = blk_scale<FMT>(wbox, r0, b, bad);
-                d[i][1] = blk_scale<FMT>(wbox, r8, b, bad);
+                if constexpr (FMT == 4) {
+                    d[i][0] = blk_scale<FMT>(wbox, r0, b, bad);
+                    d[i][1] = blk_scale<FMT>(wbox, r8, b, bad);
+                } else {  // fold the block scale into the binary16 weights
+                    const uint32_t d0 = blk_scale2<FMT>(wbox, r0, b), d8 = blk_scale2<FMT>(wbox, r8, b);
+#pragma unroll
+                    for (int ww = 0; ww < 2; ww++) {
+                        af[i][ww][0] = hmul2_u(af[i][ww][0], d0);
+                        af[i][ww][2] = hmul2_u(af[i][ww][2], d0);
+                        af[i][ww][1] = hmul2_u(af[i][ww][1], d8);
+                        af[i][ww][3] = hmul2_u(af[i][ww][3], d8);
+                    }
+                }
             }
 #pragma unroll
             for (int j = 0; j < G::NT; j++) {
@@ -451,13 +477,18 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_pgemm(const __grid_constant
                 asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(b10), "=r"(b11) : "r"(ba + 32));
 #pragma unroll
                 for (int i = 0; i < G::RT; i++) {
-                    float p[4];
-                    mma_first(p, af[i][0][0], af[i][0][1], af[i][0][2], af[i][0][3], b00, b01);
-                    mma_acc(p, af[i][1][0], af[i][1][1], af[i][1][2], af[i][1][3], b10, b11);
-                    y[i][j][0] = fmaf(d[i][0], p[0], y[i][j][0]);
-                    y[i][j][1] = fmaf(d[i][0], p[1], y[i][j][1]);
-                    y[i][j][2] = fmaf(d[i][1], p[2], y[i][j][2]);
-                    y[i][j][3] = fmaf(d[i][1], p[3], y[i][j][3]);
+                    if constexpr (FMT == 4) {
+                        float p[4];
+                        mma_first(p, af[i][0][0], af[i][0][1], af[i][0][2], af[i][0][3], b00, b01);
+                        mma_acc(p, af[i][1][0], af[i][1][1], af[i][1][2], af[i][1][3], b10, b11);
+                        y[i][j][0] = fmaf(d[i][0], p[0], y[i][j][0]);
+                        y[i][j][1] = fmaf(d[i][0], p[1], y[i][j][1]);
+                        y[i][j][2] = fmaf(d[i][1], p[2], y[i][j][2]);
+                        y[i][j][3] = fmaf(d[i][1], p[3], y[i][j][3]);
+                    } else {
+                        mma_acc(y[i][j], af[i][0][0], af[i][0][1], af[i][0][2], af[i][0][3], b00, b01);
+                        mma_acc(y[i][j], af[i][1][0], af[i][1][1], af[i][1][2], af[i][1][3], b10, b11);
+                    }
                 }
             }
         }
