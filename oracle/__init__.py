@@ -51,6 +51,7 @@ def lib():
             "orc_moe_layer": (I, [I, I, I, P, P, P, P, P, P, P, P, I, I, P, P, P, P, P, P]),
             "orc_rmsnorm_bf16": (I, [P, I, I, P]),
             "orc_stable_argsort": (I, [P, I, I, P, P]),
+            "orc_dspark_commit": (I, [P, I, I, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -176,3 +177,15 @@ def stable_argsort(keys, nkeys):
     offsets = np.zeros(nkeys + 1, np.int32)
     _check(lib().orc_stable_argsort(_p(keys), keys.size, nkeys, _p(perm), _p(offsets)), "stable_argsort")
     return perm, offsets
+
+
+def dspark_commit(logits, drafts):
+    """logits float32 [q][V], drafts int [q-1] -> (pred [q], n_accept, committed [q], status)."""
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    q, V = logits.shape
+    d = np.ascontiguousarray(drafts, dtype=np.int32).reshape(-1)
+    pred = np.zeros(q, np.int32); n = np.zeros(1, np.int32); com = np.zeros(q, np.int32)
+    st = lib().orc_dspark_commit(_p(logits), q, V, _p(d) if d.size else None, _p(pred), _p(n), _p(com))
+    if st not in (0, ERANGE):
+        _check(st, "dspark_commit")
+    return pred, int(n[0]), com, st

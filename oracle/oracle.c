@@ -488,3 +488,30 @@ int orc_stable_argsort(const int32_t* keys, int n, int nkeys, int32_t* perm, int
     free(kp);
     return ORC_OK;
 }
+
+
+/* ------------------------------------------------------------------ speculative verify / commit */
+
+/* The target's choice at each verified position is its largest logit (plain scan, lowest index kept
+ * on ties, NaN skipped); drafts are accepted while they equal those choices; the first mismatch (or
+ * the position after the last draft) takes the target's choice. */
+int orc_dspark_commit(const float* logits, int q, int V, const int32_t* drafts, int32_t* pred, int32_t* n_accept,
+                      int32_t* committed) {
+    if (!logits || q < 1 || V < 1 || (q > 1 && !drafts) || !pred || !n_accept || !committed) return ORC_EINVAL;
+    int st = ORC_OK;
+    for (int i = 0; i < q; i++) {
+        int best = -1;
+        for (int v = 0; v < V; v++) {
+            const float x = logits[(size_t)i * V + v];
+            if (x != x) continue;
+            if (best < 0 || x > logits[(size_t)i * V + best]) best = v;
+        }
+        if (best < 0) { best = 0; st = ORC_ERANGE; }
+        pred[i] = best;
+    }
+    int n = 0;
+    while (n < q - 1 && drafts[n] == pred[n]) n++;
+    *n_accept = n;
+    for (int i = 0; i < q; i++) committed[i] = i < n ? drafts[i] : (i == n ? pred[n] : -1);
+    return st;
+}

@@ -70,4 +70,16 @@ int orc_rmsnorm_bf16(const float* r, int q, int H, double* u);
  * position order; offsets[e] = number of keys < e (nkeys + 1 entries). */
 int orc_stable_argsort(const int32_t* keys, int n, int nkeys, int32_t* perm, int32_t* offsets);
 
+/* Speculative verify/commit of one sequence ("DeepSeek V4 Flash hits 32 tok/s on AMD Ryzen AI MAX+
+ * 395", paragraph 3, and the zh-TW page, section "DSpark", steps Propose / Verify / Commit): the
+ * target scored q positions (the seed and q - 1 draft tokens) in one pass, logits [q][V]. pred[i] is
+ * the target's choice at position i: the index of the largest logit, the lowest index among equal
+ * maxima, NaN logits never chosen (all-NaN row: index 0 and ORC_ERANGE). Draft token d[j] (j = 0 ..
+ * q - 2) proposes the token after position j; the accepted count n is the largest n <= q - 1 with
+ * d[j] == pred[j] for every j < n. committed[0 .. n] = d[0 .. n-1] then pred[n] (the target's
+ * correction at the first mismatch, or its next token after an all-accepted draft); entries past n
+ * are -1. */
+int orc_dspark_commit(const float* logits, int q, int V, const int32_t* drafts, int32_t* pred, int32_t* n_accept,
+                      int32_t* committed);
+
 #endif
