@@ -104,6 +104,38 @@ def prefill_measure(fpx, layer, warmup, reps=10):
             "frac": round(tf / peak, 4), "tokens_per_s": round(PF_T / (ms / 1e3), 1), "reps": reps}
 
 
+DS_B, DS_Q, DS_V = 128, 4, 131072  # verify/commit: sequences, positions, stand-in vocabulary size
+
+
+def commit_measure(fpx, peak, reps=20):
+    """dspark_verify_commit over 128 sequences x 4 positions x 131,072 binary32 logits (256 MB, larger
+    than L2; synthetic N(0,1), drafts that match the target's choice half of the time), timed with
+    CUDA events; HBM-bound: bytes are the logits read once."""
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(7)
+    lg = torch.randn(DS_B, DS_Q, DS_V, device="cuda", generator=g)
+    best = lg.argmax(dim=2).to(torch.int32)
+    flip = torch.rand(DS_B, DS_Q - 1, device="cuda", generator=g) < 0.5
+    drafts = torch.where(flip, (best[:, : DS_Q - 1] + 1) % DS_V, best[:, : DS_Q - 1]).to(torch.int32).contiguous()
+    pred = torch.empty(DS_B, DS_Q, dtype=torch.int32, device="cuda")
+    n = torch.empty(DS_B, dtype=torch.int32, device="cuda")
+    com = torch.empty(DS_B, DS_Q, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        fpx.dspark_verify_commit(lg, DS_B, DS_Q, DS_V, drafts, pred, n, com)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        fpx.dspark_verify_commit(lg, DS_B, DS_Q, DS_V, drafts, pred, n, com)
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    gbs = DS_B * DS_Q * DS_V * 4 / (ms / 1e3) / 1e9
+    return {"workload": f"{DS_B} sequences x {DS_Q} verified positions x {DS_V} binary32 logits (synthetic)",
+            "ms": round(ms, 4), "value": round(gbs, 1), "unit": "GB/s", "frac_of_hbm_peak": round(gbs / peak, 4),
+            "mean_accepted": round(float(n.float().mean()), 3), "reps": reps}
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -455,6 +487,7 @@ def run_fpx(args):
     e2e_bytes = sum(bytes_per_batch[i % N_BATCHES] for i in range(e2e_steps)) * world
 
     pf = prefill_measure(fpx, stack.layers[0], args.warmup)
+    dc = commit_measure(fpx, peak)
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -482,6 +515,7 @@ def run_fpx(args):
         "e2e": {"value": round(e2e_bytes / e2e_secs / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "prefill": pf,
+        "verify_commit": dc,
         "gpu_launches": args.steps * NK * args.layers,
         "clocks": clk.summary(),
     }

@@ -74,6 +74,9 @@ _SIGS = {
                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                          ctypes.c_void_p]),
+    "dspark_verify_commit": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_void_p]),
 }
 
 # Every symbol include/fpx.h declares (the export test checks them against the header).
@@ -204,3 +207,9 @@ def moe_layer_prefill(layer, x, T, k, y, ws, ws_bytes, idx_out=None, w_out=None,
                                    _ptr(logits_out), _ptr(perm_out), _ptr(offsets_out), _ptr(ws), ws_bytes,
                                    _stream(stream)),
            "moe_layer_prefill")
+
+
+def dspark_verify_commit(logits, B, q, V, drafts, pred, n_accept, committed, dev_status=None, stream=None):
+    """Speculative verify/commit for B sequences (see include/fpx.h)."""
+    _check(lib().dspark_verify_commit(_ptr(logits), B, q, V, _ptr(drafts), _ptr(pred), _ptr(n_accept),
+                                      _ptr(committed), _ptr(dev_status), _stream(stream)), "dspark_verify_commit")

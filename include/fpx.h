@@ -217,6 +217,18 @@ int moe_layer_prefill(const moe_layer* layer, const uint16_t* x, int T, int k, f
                       float* w_out, float* logits_out, int32_t* perm_out, int32_t* offsets_out, void* ws,
                       size_t ws_bytes, void* stream);
 
+/* Speculative verify/commit for B sequences (B >= 0, 1 <= q <= 16, V >= 1): the target scored q
+ * positions of each sequence (the seed and q - 1 draft tokens) in one pass; logits is binary32
+ * [B][q][V], drafts int32 [B][q-1] (nullable when q == 1). Outputs: pred [B][q], the target's choice
+ * at each position (the largest logit, lowest index among equal maxima, NaN never chosen; an all-NaN
+ * row gives 0 and sets FPX_ERANGE in *dev_status, nullable); n_accept [B], the largest n <= q - 1
+ * with drafts[b][j] == pred[b][j] for all j < n; committed [B][q] = the n accepted drafts, then
+ * pred[b][n], then -1. Reads the logits once (HBM-bound). [P-dsv4] paragraph 3 (four positions
+ * including the seed; correct proposals commit, the first error is corrected by the target),
+ * [P-zh] section "DSpark" (Propose / Verify / Commit). */
+int dspark_verify_commit(const float* logits, int B, int q, int V, const int32_t* drafts, int32_t* pred,
+                         int32_t* n_accept, int32_t* committed, int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -90,3 +90,26 @@ def test_route_and_quant_argument_errors():
     assert L.fpx_quantize(2, FAKE, 4, 64, None, FAKE + 1, None, None) == fpx.FPX_EALIGN
     assert L.fpx_dequantize(9, FAKE, 4, 64, FAKE, None, None) == fpx.FPX_EINVAL
     assert L.fpx_read_status(None, None, None) == fpx.FPX_EINVAL
+
+
+def test_prefill_and_commit_argument_errors():
+    L = fpx.lib()
+    lay = _layer()
+    assert fpx.moe_prefill_workspace_bytes(lay, 0, 4) == 0
+    assert fpx.moe_prefill_workspace_bytes(lay, 16, 9) == 0
+    ws = fpx.moe_prefill_workspace_bytes(lay, 16, 4)
+    assert ws > 0 and ws % 16 == 0
+    call = lambda lay, T=16, k=4, x=FAKE, wsb=ws: L.moe_layer_prefill(ctypes.byref(lay), x, T, k, FAKE, None, None, None,
+                                                                      None, None, FAKE, wsb, None)
+    assert call(lay, T=0) == fpx.FPX_EINVAL
+    assert call(lay, k=9) == fpx.FPX_EINVAL
+    assert call(_layer(H=500)) == fpx.FPX_EINVAL
+    assert call(lay, x=FAKE + 2) == fpx.FPX_EALIGN
+    assert call(lay, wsb=ws - 16) == fpx.FPX_ESPACE
+    c = L.dspark_verify_commit
+    assert c(FAKE, 4, 0, 10, FAKE, FAKE, FAKE, FAKE, None, None) == fpx.FPX_EINVAL   # q = 0
+    assert c(FAKE, 4, 17, 10, FAKE, FAKE, FAKE, FAKE, None, None) == fpx.FPX_EINVAL  # q > 16
+    assert c(FAKE, 4, 4, 0, FAKE, FAKE, FAKE, FAKE, None, None) == fpx.FPX_EINVAL    # V = 0
+    assert c(FAKE, 4, 4, 10, None, FAKE, FAKE, FAKE, None, None) == fpx.FPX_EINVAL   # drafts needed
+    assert c(FAKE + 2, 4, 4, 10, FAKE, FAKE, FAKE, FAKE, None, None) == fpx.FPX_EALIGN
+    assert c(None, 0, 4, 10, None, None, None, None, None, None) == fpx.FPX_OK       # B = 0: nothing
