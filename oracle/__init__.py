@@ -52,6 +52,7 @@ def lib():
             "orc_rmsnorm_bf16": (I, [P, I, I, P]),
             "orc_stable_argsort": (I, [P, I, I, P, P]),
             "orc_dspark_commit": (I, [P, I, I, P, P, P, P]),
+            "orc_quantize_weighted": (I, [I, P, I64, I64, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -189,3 +190,13 @@ def dspark_commit(logits, drafts):
     if st not in (0, ERANGE):
         _check(st, "dspark_commit")
     return pred, int(n[0]), com, st
+
+
+def quantize_weighted(fmt, W, imp=None):
+    """(status, packed bytes) of the importance-weighted quantizer; imp [K] or None (all ones)."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    N, K = W.shape
+    out = np.zeros(max(matrix_bytes(fmt, N, K), 1), np.uint8)
+    im = None if imp is None else np.ascontiguousarray(imp, dtype=np.float32)
+    st = lib().orc_quantize_weighted(fmt, _p(W), N, K, _p(im), _p(out))
+    return st, out

@@ -255,6 +255,90 @@ int orc_quantize(int fmt, const float* W, int64_t N, int64_t K, const float* sca
     return ORC_OK;
 }
 
+/* One block under one candidate scale: its bytes (as orc_quantize writes them) and its weighted
+ * squared error in binary64, summed in weight order. d16 / e: the binary16 scale or E8M0 exponent. */
+static double weighted_block(int fmt, const float* v, const float* imp, unsigned d16, int e, uint8_t* p) {
+    int bb = orc_block_bytes(fmt);
+    memset(p, 0, (size_t)bb);
+    double err = 0.0;
+    if (fmt == 2 || fmt == 3) {
+        int kmax = fmt == 2 ? 3 : 7;
+        double d = binary16_to_double(d16);
+        p[0] = (uint8_t)(d16 & 0xFF);
+        p[1] = (uint8_t)(d16 >> 8);
+        for (int j = 0; j < 32; j++) {
+            int c = odd_level_code((double)v[j], d, kmax);
+            p[2 + j / 4] |= (uint8_t)((c & 3) << (2 * (j % 4)));
+            if (fmt == 3) p[10 + j / 8] |= (uint8_t)(((c >> 2) & 1) << (j % 8));
+            double diff = (double)v[j] - d * (double)(2 * c - kmax);
+            err += (imp ? (double)imp[j] : 1.0) * (diff * diff);
+        }
+    } else {
+        double scale = ldexp(1.0, e - 127);
+        p[0] = (uint8_t)e;
+        for (int j = 0; j < 32; j++) {
+            int m = e2m1_index(fabs((double)v[j]) / scale);
+            int qc = m | (signbit(v[j]) ? 8 : 0);
+            p[1 + j / 2] |= (uint8_t)(qc << (4 * (j % 2)));
+            double w = (signbit(v[j]) ? -kE2M1[m] : kE2M1[m]) * scale;
+            double diff = (double)v[j] - w;
+            err += (imp ? (double)imp[j] : 1.0) * (diff * diff);
+        }
+    }
+    return err;
+}
+
+int orc_quantize_weighted(int fmt, const float* W, int64_t N, int64_t K, const float* imp, uint8_t* out) {
+    int bb = orc_block_bytes(fmt);
+    if (!bb || N < 0 || K < 0 || K % 32) return ORC_EINVAL;
+    if (imp)
+        for (int64_t k = 0; k < K; k++)
+            if (!isfinite(imp[k]) || imp[k] < 0.0f) return ORC_ERANGE;
+    int64_t nb = K / 32;
+    uint8_t cand[17];
+    for (int64_t r = 0; r < N; r++) {
+        for (int64_t b = 0; b < nb; b++) {
+            const float* v = W + r * K + b * 32;
+            const float* im = imp ? imp + b * 32 : NULL;
+            uint8_t* p = out + (r * nb + b) * bb;
+            double amax = 0.0;
+            for (int j = 0; j < 32; j++) {
+                if (!isfinite(v[j])) return ORC_ERANGE;
+                if (fabs((double)v[j]) > amax) amax = fabs((double)v[j]);
+            }
+            double best = 0.0;
+            int found = 0;
+            if (fmt == 2 || fmt == 3) {
+                int kmax = fmt == 2 ? 3 : 7;
+                for (int j = 0; j < 16; j++) {
+                    unsigned d16 = double_to_binary16(amax / kmax * ((double)(12 + j) / 20.0));
+                    if ((d16 & 0x7C00u) == 0x7C00u) continue; /* overflows binary16 */
+                    double err = weighted_block(fmt, v, im, d16, 0, cand);
+                    if (!found || err < best) { best = err; found = 1; memcpy(p, cand, (size_t)bb); }
+                }
+            } else {
+                int e0;
+                if (amax == 0.0) {
+                    e0 = 0;
+                } else {
+                    int ex;
+                    frexp(amax, &ex);
+                    e0 = ex - 1 - 2 + 127;
+                    if (e0 < 0) e0 = 0;
+                    if (e0 > 254) e0 = 254;
+                }
+                for (int j = -1; j <= 1; j++) {
+                    int e = e0 + j < 0 ? 0 : (e0 + j > 254 ? 254 : e0 + j);
+                    double err = weighted_block(fmt, v, im, 0, e, cand);
+                    if (!found || err < best) { best = err; found = 1; memcpy(p, cand, (size_t)bb); }
+                }
+            }
+            if (!found) return ORC_ERANGE;
+        }
+    }
+    return ORC_OK;
+}
+
 int orc_topk(const double* v, int n, int k, int32_t* idx) {
     if (n < 1 || k < 1 || k > n) return ORC_EINVAL;
     char* taken = (char*)calloc((size_t)n, 1);

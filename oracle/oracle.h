@@ -70,6 +70,15 @@ int orc_rmsnorm_bf16(const float* r, int q, int H, double* u);
  * position order; offsets[e] = number of keys < e (nkeys + 1 entries). */
 int orc_stable_argsort(const int32_t* keys, int n, int nkeys, int32_t* perm, int32_t* offsets);
 
+/* Importance-weighted quantizer ([zh] page, section "ROCmFPX": quantization guided by an importance
+ * matrix; the real matrix needs calibration data, so the importance here is any caller vector): for
+ * each block, try the scales (amax / Kmax) * f, f = 0.60, 0.65, ..., 1.35 rounded to binary16
+ * (FP2/FP3), or the E8M0 exponents e0 - 1, e0, e0 + 1 around the plain quantizer's e0 (FP4); under
+ * each, the codes of orc_quantize; keep the one with the least sum over the block's 32 weights of
+ * imp[col] * (w - w_hat)^2 (binary64, summed in weight order; the earliest candidate on equal sums).
+ * imp [K] per column, NULL = all ones; a negative or non-finite importance or input is ORC_ERANGE. */
+int orc_quantize_weighted(int fmt, const float* W, int64_t N, int64_t K, const float* imp, uint8_t* out);
+
 /* Speculative verify/commit of one sequence ("DeepSeek V4 Flash hits 32 tok/s on AMD Ryzen AI MAX+
  * 395", paragraph 3, and the zh-TW page, section "DSpark", steps Propose / Verify / Commit): the
  * target scored q positions (the seed and q - 1 draft tokens) in one pass, logits [q][V]. pred[i] is
