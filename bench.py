@@ -136,6 +136,30 @@ def commit_measure(fpx, peak, reps=20):
             "mean_accepted": round(float(n.float().mean()), 3), "reps": reps}
 
 
+def quantize_weighted_measure(fpx, reps=5):
+    """fpx_quantize_weighted on one FP2 gate matrix shape (2048 x 4096 binary32 weights, N(0, 0.02)),
+    importance U[0, 3) per column, CUDA events. Binary64-bound: 16 candidates x 32 weights x 5 binary64
+    operations per block."""
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(9)
+    W = torch.randn(I, H, device="cuda", generator=g) * 0.02
+    imp = torch.rand(H, device="cuda", generator=g) * 3
+    out = torch.empty(fpx.fpx_matrix_bytes(2, I, H), dtype=torch.uint8, device="cuda")
+    fpx.fpx_quantize_weighted(2, W, I, H, out, importance=imp)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        fpx.fpx_quantize_weighted(2, W, I, H, out, importance=imp)
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    blocks = I * H // 32
+    return {"workload": f"FP2 {I}x{H} weights, per-column importance", "ms": round(ms, 4),
+            "blocks_per_s": round(blocks / (ms / 1e3)), "fp64_ops_per_s": round(blocks * 16 * 32 * 5 / (ms / 1e3) / 1e12, 3),
+            "fp64_unit": "Tops/s", "reps": reps}
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -488,6 +512,7 @@ def run_fpx(args):
 
     pf = prefill_measure(fpx, stack.layers[0], args.warmup)
     dc = commit_measure(fpx, peak)
+    qw = quantize_weighted_measure(fpx)
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -516,6 +541,7 @@ def run_fpx(args):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "prefill": pf,
         "verify_commit": dc,
+        "quantize_weighted": qw,
         "gpu_launches": args.steps * NK * args.layers,
         "clocks": clk.summary(),
     }

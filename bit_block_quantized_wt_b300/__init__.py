@@ -77,6 +77,8 @@ _SIGS = {
     "dspark_verify_commit": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                             ctypes.c_void_p, ctypes.c_void_p]),
+    "fpx_quantize_weighted": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
 }
 
 # Every symbol include/fpx.h declares (the export test checks them against the header).
@@ -213,3 +215,9 @@ def dspark_verify_commit(logits, B, q, V, drafts, pred, n_accept, committed, dev
     """Speculative verify/commit for B sequences (see include/fpx.h)."""
     _check(lib().dspark_verify_commit(_ptr(logits), B, q, V, _ptr(drafts), _ptr(pred), _ptr(n_accept),
                                       _ptr(committed), _ptr(dev_status), _stream(stream)), "dspark_verify_commit")
+
+
+def fpx_quantize_weighted(fmt, W, N, K, out, importance=None, dev_status=None, stream=None):
+    """Importance-weighted quantizer (see include/fpx.h)."""
+    _check(lib().fpx_quantize_weighted(fmt, _ptr(W), N, K, _ptr(importance), _ptr(out), _ptr(dev_status),
+                                       _stream(stream)), "fpx_quantize_weighted")

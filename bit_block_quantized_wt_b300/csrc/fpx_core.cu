@@ -116,6 +116,107 @@ __global__ void k_quantize(const float* __restrict__ W, int64_t N, int64_t K, co
     }
 }
 
+// Importance-weighted quantizer: per block, the candidate scales (amax / Kmax) * (12 + j) / 20,
+// j = 0..15, rounded to binary16 (FP2/FP3), or the E8M0 exponents e0 - 1, e0, e0 + 1 (FP4); under each,
+// the codes of k_quantize; the kept candidate has the least sum over the block of
+// imp[col] * (w - w_hat)^2, evaluated in binary64 in weight order with explicitly rounded operations
+// (no fused multiply-add), the earliest candidate on equal sums. The zh-TW page, section "ROCmFPX"
+// (quantization guided by an importance matrix); the importance here is any caller vector.
+template <int FMT>
+__device__ __forceinline__ double block_werr(const float (&x)[32], const float* imp, float d, int e) {
+    double err = 0.0;
+#pragma unroll
+    for (int j = 0; j < 32; j++) {
+        double w;
+        if constexpr (FMT == 4) {
+            const double inv = ldexp(1.0, 127 - e), sc = ldexp(1.0, e - 127);
+            const uint32_t m = e2m1_round(fabs((double)x[j]) * inv);
+            const double g[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+            w = __dmul_rn(signbit(x[j]) ? -g[m] : g[m], sc);
+        } else {
+            const int kmax = FMT == 2 ? 3 : 7;
+            const int c = (int)odd_code<FMT>(x[j], d);
+            w = __dmul_rn((double)d, (double)(2 * c - kmax));
+        }
+        const double diff = __dsub_rn((double)x[j], w);
+        err = __dadd_rn(err, __dmul_rn(imp ? (double)imp[j] : 1.0, __dmul_rn(diff, diff)));
+    }
+    return err;
+}
+
+template <int FMT>
+__global__ void k_quantize_weighted(const float* __restrict__ W, int64_t N, int64_t K, const float* __restrict__ imp,
+                                    uint8_t* __restrict__ out, int32_t* st) {
+    const int64_t nb = K / 32, total = N * nb;
+    for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < total; b += (int64_t)gridDim.x * blockDim.x) {
+        const float* v = W + (b / nb) * K + (b % nb) * 32;
+        const float* im = imp ? imp + (b % nb) * 32 : nullptr;
+        uint8_t* p = out + b * block_bytes(FMT);
+        float x[32];
+        float amax = 0.0f;
+        bool finite = true;
+#pragma unroll
+        for (int j = 0; j < 32; j++) {
+            x[j] = v[j];
+            finite = finite && isfinite(x[j]) && (!im || (isfinite(im[j]) && im[j] >= 0.0f));
+            amax = fmaxf(amax, fabsf(x[j]));
+        }
+        if (!finite) { flag(st, FPX_ERANGE); continue; }
+        if constexpr (FMT == 2 || FMT == 3) {
+            const double kmax = FMT == 2 ? 3.0 : 7.0;
+            bool found = false;
+            double best = 0.0;
+            uint16_t bh = 0;
+            for (int j = 0; j < 16; j++) {
+                const __half h = __double2half(__dmul_rn(__ddiv_rn((double)amax, kmax), __ddiv_rn((double)(12 + j), 20.0)));
+                const uint16_t hb = __half_as_ushort(h);
+                if ((hb & 0x7C00u) == 0x7C00u) continue;
+                const double err = block_werr<FMT>(x, im, __half2float(h), 0);
+                if (!found || err < best) { best = err; bh = hb; found = true; }
+            }
+            if (!found) { flag(st, FPX_ERANGE); continue; }
+            const float d = __half2float(__ushort_as_half(bh));
+            uint32_t lo[2] = {0u, 0u}, hi = 0u;
+#pragma unroll
+            for (int j = 0; j < 32; j++) {
+                const uint32_t c = odd_code<FMT>(x[j], d);
+                lo[j >> 4] |= (c & 3u) << (2 * (j & 15));
+                if (FMT == 3) hi |= ((c >> 2) & 1u) << j;
+            }
+            p[0] = bh & 0xFF; p[1] = bh >> 8;
+#pragma unroll
+            for (int i = 0; i < 4; i++) { p[2 + i] = (lo[0] >> (8 * i)) & 0xFF; p[6 + i] = (lo[1] >> (8 * i)) & 0xFF; }
+            if (FMT == 3) {
+#pragma unroll
+                for (int i = 0; i < 4; i++) p[10 + i] = (hi >> (8 * i)) & 0xFF;
+            }
+        } else {
+            int e0 = 0;
+            if (amax != 0.0f) {
+                int ex;
+                frexpf(amax, &ex);  // floor(log2 amax) = ex - 1
+                e0 = min(254, max(0, ex - 1 - 2 + 127));
+            }
+            bool found = false;
+            double best = 0.0;
+            int be = e0;
+            for (int j = -1; j <= 1; j++) {
+                const int e = min(254, max(0, e0 + j));
+                const double err = block_werr<FMT>(x, im, 0.0f, e);
+                if (!found || err < best) { best = err; be = e; found = true; }
+            }
+            const double inv = ldexp(1.0, 127 - be);
+            p[0] = (uint8_t)be;
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                uint32_t q0 = e2m1_round(fabs((double)x[2 * j]) * inv) | (signbit(x[2 * j]) ? 8u : 0u);
+                uint32_t q1 = e2m1_round(fabs((double)x[2 * j + 1]) * inv) | (signbit(x[2 * j + 1]) ? 8u : 0u);
+                p[1 + j] = (uint8_t)(q0 | (q1 << 4));
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ GEMV, CUDA-core path
 
 constexpr int kGemvThreads = 256;
@@ -523,6 +624,21 @@ int fpx_quantize(int fmt, const float* W, int64_t N, int64_t K, const float* blo
     if (fmt == 2) k_quantize<2><<<grid, 128, 0, s>>>(W, N, K, block_scales, out, dev_status);
     else if (fmt == 3) k_quantize<3><<<grid, 128, 0, s>>>(W, N, K, block_scales, out, dev_status);
     else k_quantize<4><<<grid, 128, 0, s>>>(W, N, K, block_scales, out, dev_status);
+    return launch_status();
+}
+
+int fpx_quantize_weighted(int fmt, const float* W, int64_t N, int64_t K, const float* importance, uint8_t* out,
+                          int32_t* dev_status, void* stream) {
+    if (matrix_bytes(fmt, N, K) < 0) return FPX_EINVAL;
+    if (N == 0 || K == 0) return FPX_OK;
+    if (!W || !out) return FPX_EINVAL;
+    if (!aligned(out, 16) || !aligned(W, 16) || (importance && !aligned(importance, 4))) return FPX_EALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int64_t nb = N * (K / 32);
+    int grid = (int)((nb + 127) / 128 < 148 * 8 ? (nb + 127) / 128 : 148 * 8);
+    if (fmt == 2) k_quantize_weighted<2><<<grid, 128, 0, s>>>(W, N, K, importance, out, dev_status);
+    else if (fmt == 3) k_quantize_weighted<3><<<grid, 128, 0, s>>>(W, N, K, importance, out, dev_status);
+    else k_quantize_weighted<4><<<grid, 128, 0, s>>>(W, N, K, importance, out, dev_status);
     return launch_status();
 }
 

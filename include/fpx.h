@@ -94,6 +94,18 @@ int fpx_quantize(int fmt, const float* W, int64_t N, int64_t K, const float* blo
 int fpx_dequantize(int fmt, const uint8_t* Wq, int64_t N, int64_t K, float* W, int32_t* dev_status,
                    void* stream);
 
+/* Importance-weighted quantizer (same block layouts and codes as fpx_quantize): for each block, tries
+ * the scales (amax / Kmax) * f, f = 0.60, 0.65, ..., 1.35 rounded to binary16 (FP2/FP3; overflowing
+ * ones skipped), or the E8M0 exponents e0 - 1, e0, e0 + 1 around fpx_quantize's e0 (FP4), and keeps
+ * the one whose quantization has the least sum over the block's 32 weights of
+ * importance[col] * (w - w_hat)^2 (binary64, summed in weight order, the earliest candidate on equal
+ * sums). importance [K] per column (nullable: all ones); the plain scale is among the candidates, so
+ * the weighted error never exceeds fpx_quantize's. A non-finite input or a negative or non-finite
+ * importance sets FPX_ERANGE in *dev_status (that block's bytes are unspecified). [P-zh] section
+ * "ROCmFPX" (quantization guided by an importance matrix; the real one needs calibration data). */
+int fpx_quantize_weighted(int fmt, const float* W, int64_t N, int64_t K, const float* importance, uint8_t* out,
+                          int32_t* dev_status, void* stream);
+
 /* Rearranges `count` packed matrices (N x K, format fmt; matrix m at src + m * src_stride) between the
  * row-major layout and the box-tiled layout the MoE layer kernels read (matrix m at dst + m *
  * dst_stride; the same number of bytes). Box-tiled: each matrix is cut into tiles of R rows x B bytes

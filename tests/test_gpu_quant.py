@@ -81,3 +81,37 @@ def test_dequantize_invalid_fp4_block():
     assert read_status(st) == 1 << fpx.FPX_EDATA
     o = host(out)
     assert np.all(o[0, 32:] == 0)
+
+
+def gpu_quantize_weighted(fmt, W, imp=None):
+    N, K = W.shape
+    out = torch.zeros(max(fpx.fpx_matrix_bytes(fmt, N, K), 16), dtype=torch.uint8, device="cuda")
+    st = status_word()
+    fpx.fpx_quantize_weighted(fmt, dev(W), N, K, out, importance=None if imp is None else dev(imp), dev_status=st)
+    return host(out)[: fpx.fpx_matrix_bytes(fmt, N, K)], read_status(st)
+
+
+@pytest.mark.parametrize("fmt", [2, 3, 4])
+@pytest.mark.parametrize("N,K,with_imp", [(3, 32, True), (17, 256, False), (256, 4096, True)])
+def test_quantize_weighted_matches_oracle(fmt, N, K, with_imp):
+    """The importance-weighted quantizer: every candidate choice and code bit-exact against the oracle
+    (the binary64 error sums are taken in the same order with the same roundings on both sides)."""
+    need_gpu()
+    W = weights(N, K, N * K + fmt + 7)
+    imp = np.random.default_rng(N + K).uniform(0.0, 3.0, K).astype(np.float32) if with_imp else None
+    if imp is not None:
+        imp[:3] = [0.0, 1e-30, 100.0]
+    got, st = gpu_quantize_weighted(fmt, W, imp)
+    assert st == 0
+    ost, ref = oracle.quantize_weighted(fmt, W, imp)
+    assert ost == 0
+    assert np.array_equal(got, ref[: got.size])
+
+
+def test_quantize_weighted_flags_bad_importance():
+    need_gpu()
+    W = weights(4, 64, 1)
+    imp = np.ones(64, np.float32)
+    imp[40] = -1.0
+    _, st = gpu_quantize_weighted(2, W, imp)
+    assert st & (1 << fpx.FPX_ERANGE)
