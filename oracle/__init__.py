@@ -53,6 +53,7 @@ def lib():
             "orc_stable_argsort": (I, [P, I, I, P, P]),
             "orc_dspark_commit": (I, [P, I, I, P, P, P, P]),
             "orc_quantize_weighted": (I, [I, P, I64, I64, P, P]),
+            "orc_quantize_act16": (I, [P, I, I64, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -200,3 +201,21 @@ def quantize_weighted(fmt, W, imp=None):
     im = None if imp is None else np.ascontiguousarray(imp, dtype=np.float32)
     st = lib().orc_quantize_weighted(fmt, _p(W), N, K, _p(im), _p(out))
     return st, out
+
+
+def quantize_act16(x):
+    """Integer-dot activations of x [q][K] -> (status, X int32 [q][K], e int32 [q][K/32], xhat [q][K])."""
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float64)
+    q, K = x.shape
+    X = np.zeros((q, K), np.int32)
+    e = np.zeros((q, max(K // 32, 1)), np.int32)
+    xhat = np.zeros((q, K), np.float64)
+    st = lib().orc_quantize_act16(_p(x), q, K, _p(X), _p(e), _p(xhat))
+    return st, X, e[:, : K // 32], xhat
+
+
+def gemv_idot(fmt, Wq, N, K, x):
+    """The integer-dot GEMV: exactly W * xhat (the integer dot products are exact), as (y, M) of gemv."""
+    st, _, _, xhat = quantize_act16(x)
+    _check(st, "quantize_act16")
+    return gemv(fmt, Wq, N, K, xhat)

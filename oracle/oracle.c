@@ -599,3 +599,31 @@ int orc_dspark_commit(const float* logits, int q, int V, const int32_t* drafts, 
     for (int i = 0; i < q; i++) committed[i] = i < n ? drafts[i] : (i == n ? pred[n] : -1);
     return st;
 }
+
+/* Integer-dot activations: per (column, 32-entry block), the exponent e of the largest magnitude
+ * (2^(e-1) <= a < 2^e, from frexp) and X = nearest integer to x * 2^(14-e), ties to even (nearbyint
+ * in the default rounding mode). x * 2^(14-e) is exact in binary64 for every binary32 input. */
+int orc_quantize_act16(const double* x, int q, int64_t K, int32_t* X, int32_t* e, double* xhat) {
+    if (q < 1 || K < 0 || K % 32) return ORC_EINVAL;
+    int64_t nb = K / 32;
+    for (int t = 0; t < q; t++) {
+        for (int64_t b = 0; b < nb; b++) {
+            const double* v = x + (int64_t)t * K + b * 32;
+            double a = 0.0;
+            for (int j = 0; j < 32; j++) {
+                if (!isfinite(v[j])) return ORC_ERANGE;
+                if (fabs(v[j]) > a) a = fabs(v[j]);
+            }
+            int ex = 0;
+            if (a > 0.0) frexp(a, &ex); /* a = f * 2^ex, 0.5 <= f < 1 */
+            if (e) e[(int64_t)t * nb + b] = ex;
+            for (int j = 0; j < 32; j++) {
+                double r = a > 0.0 ? nearbyint(ldexp(v[j], 14 - ex)) : 0.0;
+                int64_t i = (int64_t)t * K + b * 32 + j;
+                if (X) X[i] = (int32_t)r;
+                if (xhat) xhat[i] = ldexp(r, ex - 14);
+            }
+        }
+    }
+    return ORC_OK;
+}

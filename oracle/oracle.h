@@ -91,4 +91,13 @@ int orc_quantize_weighted(int fmt, const float* W, int64_t N, int64_t K, const f
 int orc_dspark_commit(const float* logits, int q, int V, const int32_t* drafts, int32_t* pred, int32_t* n_accept,
                       int32_t* committed);
 
+/* Activations of the integer-dot GEMV ("DeepSeek V4 Flash hits 32 tok/s on AMD Ryzen AI MAX+ 395",
+ * paragraph 3: codebooks expanded in registers feed integer dot products; the pages leave the
+ * activation side open). For each column t and each run of 32 consecutive entries (a block): a = the
+ * largest |x|; e = the integer with 2^(e-1) <= a < 2^e (e = 0 for an all-zero block); X = x * 2^(14-e)
+ * rounded to the nearest integer, ties to even, so |X| <= 2^14. xhat = X * 2^(e-14) is the value the
+ * integer dot products see; the variant's result is exactly W * xhat. X [q][K], e [q][K/32] and xhat
+ * [q][K] may each be NULL; a non-finite x is ORC_ERANGE. */
+int orc_quantize_act16(const double* x, int q, int64_t K, int32_t* X, int32_t* e, double* xhat);
+
 #endif
