@@ -457,6 +457,44 @@ def oracle_layer_steps(stack_seed, r_trace, idx, budget_s, max_layers):
     return spent, nbytes, done
 
 
+ID_N, ID_K = 148 * 64 * 16, 4096  # integer-dot comparison: 151,552 rows (FP2 194 MB, larger than L2)
+
+
+def idot_measure(fpx, peak, reps=10):
+    """fpx_gemv_q_idot (byte-permute expansion + dp4a) against fpx_gemv_q (binary16 decode + tensor-core
+    MMA) on the same packed matrices, q = 4 and q = 1, CUDA events. Packed bytes are uniform (scales
+    included; the values do not change the work). Bytes per call: the packed matrix."""
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(13)
+    res = {}
+    x = torch.randn(4, ID_K, device="cuda", generator=g).to(torch.bfloat16).contiguous()
+    y = torch.empty(4, ID_N, device="cuda")
+    wsb = fpx.fpx_gemv_idot_workspace_bytes(ID_K, 4)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for fmt in (2, 3, 4):
+        nb = fpx.fpx_matrix_bytes(fmt, ID_N, ID_K)
+        Wq = torch.randint(0, 256, (nb,), dtype=torch.uint8, device="cuda", generator=g)
+        for q in ((4, 1) if fmt == 2 else (4,)):
+            for name, call in (("int_dot", lambda: fpx.fpx_gemv_q_idot(fmt, Wq, ID_N, ID_K, x, fpx.FPX_DTYPE_BF16, q,
+                                                                        y, ws, wsb)),
+                               ("tensor_core", lambda: fpx.fpx_gemv_q(fmt, Wq, ID_N, ID_K, x, fpx.FPX_DTYPE_BF16, q, y))):
+                for _ in range(3):
+                    call()
+                torch.cuda.synchronize()
+                e0.record()
+                for _ in range(reps):
+                    call()
+                e1.record()
+                e1.synchronize()
+                ms = e0.elapsed_time(e1) / reps
+                res[f"fp{fmt}_q{q}_{name}"] = {"ms": round(ms, 4), "GB/s": round(nb / (ms / 1e3) / 1e9, 1),
+                                               "frac_of_hbm_peak": round(nb / (ms / 1e3) / 1e9 / peak, 4)}
+        del Wq
+    return {"workload": f"dense {ID_N}x{ID_K} packed matrices (FP2 {fpx.fpx_matrix_bytes(2, ID_N, ID_K) / 1e6:.0f} MB, "
+                        "larger than L2), bfloat16 N(0,1) activations", "reps": reps, "results": res}
+
+
 def run_fpx(args):
     import torch
     world, rank, local = dist_env()
@@ -513,6 +551,7 @@ def run_fpx(args):
     pf = prefill_measure(fpx, stack.layers[0], args.warmup)
     dc = commit_measure(fpx, peak)
     qw = quantize_weighted_measure(fpx)
+    idm = idot_measure(fpx, peak)
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -542,6 +581,7 @@ def run_fpx(args):
         "prefill": pf,
         "verify_commit": dc,
         "quantize_weighted": qw,
+        "gemv_int_dot": idm,
         "gpu_launches": args.steps * NK * args.layers,
         "clocks": clk.summary(),
     }

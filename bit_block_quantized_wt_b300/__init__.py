@@ -53,6 +53,10 @@ _SIGS = {
     "fpx_gemv_q": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                   ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                   ctypes.c_void_p, ctypes.c_void_p]),
+    "fpx_gemv_idot_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int]),
+    "fpx_gemv_q_idot": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                       ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
     "moe_route_topk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
@@ -158,6 +162,16 @@ def fpx_dequantize(fmt, Wq, N, K, W, dev_status=None, stream=None):
 def fpx_gemv_q(fmt, Wq, N, K, x, x_dtype, q, y, dev_status=None, stream=None):
     _check(lib().fpx_gemv_q(fmt, _ptr(Wq), N, K, _ptr(x), x_dtype, q, _ptr(y), _ptr(dev_status),
                             _stream(stream)), "fpx_gemv_q")
+
+
+def fpx_gemv_idot_workspace_bytes(K, q):
+    return lib().fpx_gemv_idot_workspace_bytes(K, q)
+
+
+def fpx_gemv_q_idot(fmt, Wq, N, K, x, x_dtype, q, y, ws, ws_bytes, dev_status=None, stream=None):
+    """Integer-dot variant of fpx_gemv_q (see include/fpx.h)."""
+    _check(lib().fpx_gemv_q_idot(fmt, _ptr(Wq), N, K, _ptr(x), x_dtype, q, _ptr(y), _ptr(ws), ws_bytes,
+                                 _ptr(dev_status), _stream(stream)), "fpx_gemv_q_idot")
 
 
 def moe_route_topk(R, E, H, x, q, k, logits, idx, w, uni, n_uni, stream=None):

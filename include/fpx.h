@@ -127,6 +127,28 @@ int fpx_tile_matrices(int fmt, const uint8_t* src, int64_t N, int64_t K, int cou
 int fpx_gemv_q(int fmt, const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_dtype, int q,
                float* y, int32_t* dev_status, void* stream);
 
+/* Workspace bytes fpx_gemv_q_idot needs for K and q: (K/32 rounded up to a multiple of 32) * q * 68
+ * (the activation table). 0 for invalid arguments. */
+size_t fpx_gemv_idot_workspace_bytes(int64_t K, int q);
+
+/* Integer-dot variant of fpx_gemv_q: the packed blocks are expanded with byte permutes into signed
+ * bytes (FP2 2c - 3, FP3 2c - 7, FP4 twice the E2M1 value) and multiplied against integer activations
+ * with 4-way byte dot products ([P-dsv4] paragraph 3: codebooks expanded in registers feed integer
+ * dot products). The pages leave the activation side open; here, per column t and block b of 32
+ * entries, a = max |x|, e with 2^(e-1) <= a < 2^e (0 for an all-zero block), X = RN_even(x 2^(14-e))
+ * (|X| <= 2^14, sent as a signed high byte and an unsigned low byte), so every block dot product is an
+ * exact integer and y[t][n] = sum_b d_nb 2^(e_tb - 14) sum_j v_j X_j, i.e. the plain GEMV of
+ * x_hat = X 2^(e-14) up to binary32 rounding of the block terms and of their sums (|x_hat - x| <=
+ * 2^(e-15)). Same arguments and layouts as fpx_gemv_q, plus a caller workspace ws (16-byte aligned,
+ * >= fpx_gemv_idot_workspace_bytes(K, q) bytes, else FPX_ESPACE; overwritten) that carries the activation table from the
+ * first kernel to the second. Requires K % 256 == 0 (FP2 / FP3) or K % 512 == 0 (FP4), so rows are
+ * whole 16-byte units, and K * q small enough for the table to sit in shared memory next to two weight
+ * stages (FPX_EINVAL otherwise; about K * q <= 2^16). A non-finite x entry sets FPX_ERANGE (it counts
+ * as 0); an FP4 scale byte of 255 sets FPX_EDATA (that block counts as zeros). Column t of the result
+ * is bit-identical to a q = 1 call on x[t]; the sums run in a fixed order. */
+int fpx_gemv_q_idot(int fmt, const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_dtype, int q,
+                    float* y, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /* Router + top-k + normalise + union for q tokens (1 <= q <= 4): logits[t][e] = sum_h R[e][h] x[t][h]
  * (R binary32 [E][H], x bfloat16 [q][H]); idx[t][r], r < k, the k largest logits in descending order,
  * ties to the lower expert index; w[t][r] = sigmoid(l) / sum over the k selected sigmoids; uni the

@@ -113,3 +113,23 @@ def test_prefill_and_commit_argument_errors():
     assert c(FAKE, 4, 4, 10, None, FAKE, FAKE, FAKE, None, None) == fpx.FPX_EINVAL   # drafts needed
     assert c(FAKE + 2, 4, 4, 10, FAKE, FAKE, FAKE, FAKE, None, None) == fpx.FPX_EALIGN
     assert c(None, 0, 4, 10, None, None, None, None, None, None) == fpx.FPX_OK       # B = 0: nothing
+
+
+def test_idot_argument_errors():
+    L = fpx.lib()
+    assert fpx.fpx_gemv_idot_workspace_bytes(4096, 4) == 128 * 4 * 68
+    assert fpx.fpx_gemv_idot_workspace_bytes(1280, 1) == 64 * 68  # 40 blocks padded to 64
+    assert fpx.fpx_gemv_idot_workspace_bytes(4096, 5) == 0
+    assert fpx.fpx_gemv_idot_workspace_bytes(100, 1) == 0
+    ws = fpx.fpx_gemv_idot_workspace_bytes(1024, 2)
+    c = lambda fmt=2, W=FAKE, N=8, K=1024, x=FAKE, dt=1, q=2, wsp=FAKE, wsb=ws: L.fpx_gemv_q_idot(
+        fmt, W, N, K, x, dt, q, FAKE, wsp, wsb, None, None)
+    assert c(K=992) == fpx.FPX_EINVAL            # rows not whole 16-byte units (K % 256)
+    assert c(fmt=4, K=768) == fpx.FPX_EINVAL     # FP4 needs K % 512
+    assert c(q=5) == fpx.FPX_EINVAL
+    assert c(dt=7) == fpx.FPX_EINVAL
+    assert c(wsp=None) == fpx.FPX_EINVAL
+    assert c(wsb=ws - 16) == fpx.FPX_ESPACE
+    assert c(wsp=FAKE + 8) == fpx.FPX_EALIGN
+    assert c(W=FAKE + 8) == fpx.FPX_EALIGN
+    assert c(N=0) == fpx.FPX_OK                  # nothing to do
