@@ -13,7 +13,8 @@
 // Kernels:
 //   k_xquant   - builds the activation table (hi / lo bytes in the order the weight expansion
 //                produces them, plus 2^(e-14) per column block) in the caller's workspace.
-//   k_gemv_idot - persistent CTAs over 64-row blocks; a producer thread streams stages of 64 rows x
+//   k_gemv_idot - persistent CTAs over 64-row blocks (CTA c starts with block c, then takes the next
+//                free one from a counter); a producer thread streams stages of 64 rows x
 //                one slice of 32 blocks (2-D TMA boxes of 20 / 28 / 34 KB) into a ring; 8 consumer
 //                warps take 8 rows each, lane l owns block l of the slice: it keeps that block's
 //                activation bytes in registers, expands each row's block with byte permutes, runs the
@@ -43,6 +44,8 @@ __host__ __device__ constexpr int id_stage_bytes(int fmt) { return kIdRows * sli
 // float 2^(e-14) of (column t, block b) at index t * nbp + b.
 __host__ __device__ constexpr size_t xtab_code_bytes(int nbp, int q) { return (size_t)nbp * q * 64; }
 __host__ __device__ constexpr size_t xtab_bytes(int nbp, int q) { return (size_t)nbp * q * 68; }
+// workspace: the table, then a 16-byte row-block counter (zeroed by k_xquant)
+__host__ __device__ constexpr size_t idot_ws_bytes(int nbp, int q) { return xtab_bytes(nbp, q) + 16; }
 
 // Position of code j of a block among the expanded weight words: (word, byte).
 //   FP2 / FP3: the 16 codes of a code word h expand into words 4h .. 4h + 3 holding the codes
@@ -98,6 +101,7 @@ __global__ void __launch_bounds__(256) k_xquant(const void* __restrict__ x, int 
     tab[((size_t)c_hi * nbp + b) * 16 + off] = (uint8_t)(X >> 8);
     tab[((size_t)c_lo * nbp + b) * 16 + off] = (uint8_t)(X & 255);
     if (lane == 0) reinterpret_cast<float*>(tab + xtab_code_bytes(nbp, q))[t * nbp + b] = scale;
+    if (unit == 0 && lane == 0) *reinterpret_cast<uint32_t*>(tab + xtab_bytes(nbp, q)) = 0u;  // row-block counter
 }
 
 __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
@@ -214,6 +218,7 @@ struct IdotArgs {
     int N, nsl, nbp, nrb, NS;
     uint32_t tab_bytes;
     const uint8_t* tab;    // activation table in the workspace
+    uint32_t* counter;     // row blocks handed out past the first gridDim.x
     float* y;
     int32_t* st;
 };
@@ -230,10 +235,9 @@ __global__ void __launch_bounds__(kIdThreads, 1) k_gemv_idot(const __grid_consta
     uint64_t* full = reinterpret_cast<uint64_t*>(tab + A.tab_bytes);
     uint64_t* empty = full + A.NS;
     uint64_t* tbar = empty + A.NS;
+    int* slot_rb = reinterpret_cast<int*>(tbar + 1);  // row block of the stage in each slot (-1: no more)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NS = A.NS, nsl = A.nsl;
-    const int my_rb = (int)blockIdx.x < A.nrb ? (A.nrb - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-    const uint32_t total = (uint32_t)my_rb * (uint32_t)nsl;
 
     if (threadIdx.x < 2 * NS + 1) mbar_init(full + threadIdx.x, threadIdx.x < NS ? 1u : threadIdx.x < 2 * NS ? (uint32_t)kIdWarps : 1u);
     fence_barrier_init();
@@ -241,31 +245,48 @@ __global__ void __launch_bounds__(kIdThreads, 1) k_gemv_idot(const __grid_consta
 
     if (warp == kIdWarps) {
         if (lane != 0) return;
-        auto issue = [&](uint32_t n) {
-            const int rb = (int)blockIdx.x + (int)(n / nsl) * (int)gridDim.x, s = (int)(n % nsl);
-            const int slot = (int)(n % NS);
+        // stages in order: the nsl slices of row block blockIdx.x (gridDim.x <= row blocks), then of
+        // each block taken from the counter, then one end marker (a slot completed without data)
+        uint32_t issued = 0;
+        bool marker = false;
+        int rb = (int)blockIdx.x, s = 0;
+        auto issue = [&]() {
+            const int slot = (int)(issued % NS);
+            slot_rb[slot] = rb;
             mbar_expect_tx(full + slot, SB);
             tma_load_2d(ring + (size_t)slot * SB, &A.map, s * (SLB / 4), rb * kIdRows, full + slot);
+            issued++;
+            s++;
         };
-        uint32_t issued = 0;
-        for (; issued < total && issued < (uint32_t)NS; issued++) issue(issued);  // weights: no dependency
+        while (issued < (uint32_t)NS && s < nsl) issue();  // the weights do not depend on k_xquant
         grid_dep_wait();
         mbar_expect_tx(tbar, A.tab_bytes);
         bulk_load(tab, A.tab, A.tab_bytes, tbar);
-        bool ok = true;
-        for (; issued < total; issued++) {
-            if (!mbar_wait(empty + issued % NS, ((issued / NS) + 1u) & 1u)) {
+        for (;;) {
+            if (s == nsl) {
+                rb = (int)gridDim.x + (int)atomicAdd(A.counter, 1u);
+                s = 0;
+            }
+            if (issued >= (uint32_t)NS && !mbar_wait(empty + issued % NS, ((issued / NS) + 1u) & 1u)) {
                 flag(A.st, FPX_ETIMEOUT);
-                ok = false;
                 break;
             }
-            issue(issued);
+            if (rb >= A.nrb) {
+                slot_rb[issued % NS] = -1;
+                mbar_arrive(full + issued % NS);
+                marker = true;
+                break;
+            }
+            issue();
         }
-        // nothing may land after the CTA exits: wait (bounded) for the table and the last copies
+        // nothing may land after the CTA exits: wait (bounded) for the table and the copies of the last
+        // NS stages. With the end marker placed, its slot's previous copy was consumed (the marker
+        // waited for that slot to be released) and the slot's barrier has moved one phase further, so
+        // that stage is skipped.
         mbar_wait(tbar, 0u);
-        const uint32_t first = issued > (uint32_t)NS ? issued - NS : 0u;
+        uint32_t first = issued > (uint32_t)NS ? issued - NS : 0u;
+        if (marker && issued >= (uint32_t)NS) first = issued - NS + 1;
         for (uint32_t n = first; n < issued; n++) mbar_wait(full + n % NS, (n / NS) & 1u);
-        (void)ok;
         return;
     }
 
@@ -279,13 +300,15 @@ __global__ void __launch_bounds__(kIdThreads, 1) k_gemv_idot(const __grid_consta
     const float* cscale = reinterpret_cast<const float*>(tab + xtab_code_bytes(A.nbp, Q));
     uint32_t bad = 0;
     float yacc = 0.0f;
-    for (uint32_t n = 0; n < total; n++) {
-        const int s = (int)(n % nsl);
+    int s = 0;
+    for (uint32_t n = 0;; n++) {
         const int slot = (int)(n % NS);
         if (!mbar_wait_warp(smem_u32(full + slot), (n / NS) & 1u)) {
             if (lane == 0) flag(A.st, FPX_ETIMEOUT);
             break;
         }
+        const int rbi = slot_rb[slot];
+        if (rbi < 0) break;
         // activation bytes of block 32 s + lane: hi[t][8], lo[t][8] words, and the column scales
         uint32_t xh[Q][8], xl[Q][8];
         float cs[Q];
@@ -311,13 +334,14 @@ __global__ void __launch_bounds__(kIdThreads, 1) k_gemv_idot(const __grid_consta
 #pragma unroll
             for (int t = 0; t < QP; t++) {
                 if (t < Q) {
-                    int acc = 0;
+                    // two independent chains (high and low activation bytes), joined once
+                    int ah = 0, al = 0;
 #pragma unroll
-                    for (int i = 0; i < 8; i++) acc = dp4a_ss(w[i], xh[t][i], acc);
-                    acc *= 256;
-#pragma unroll
-                    for (int i = 0; i < 8; i++) acc = dp4a_su(w[i], xl[t][i], acc);
-                    v[rr * QP + t] = (__int2float_rn(acc) * d) * cs[t];
+                    for (int i = 0; i < 8; i++) {
+                        ah = dp4a_ss(w[i], xh[t][i], ah);
+                        al = dp4a_su(w[i], xl[t][i], al);
+                    }
+                    v[rr * QP + t] = (__int2float_rn(ah * 256 + al) * d) * cs[t];
                 } else {
                     v[rr * QP + t] = 0.0f;
                 }
@@ -338,9 +362,11 @@ __global__ void __launch_bounds__(kIdThreads, 1) k_gemv_idot(const __grid_consta
         if (s == nsl - 1) {
             const int i = lane >> (5 - L);
             const int rr = i / QP, t = i % QP;
-            const int rbi = (int)blockIdx.x + (int)(n / nsl) * (int)gridDim.x;
             const int r = rbi * kIdRows + warp * kIdRowsPerWarp + rr;
             if ((lane & ((1 << (5 - L)) - 1)) == 0 && t < Q && r < A.N) A.y[(size_t)t * A.N + r] = yacc;
+            s = 0;
+        } else {
+            s++;
         }
     }
     if (__any_sync(0xffffffffu, bad != 0u) && lane == 0) flag(A.st, FPX_EDATA);
@@ -359,7 +385,7 @@ inline int make_slice_map(CUtensorMap* m, const void* base, int64_t row_bytes, i
     return r == CUDA_SUCCESS ? FPX_OK : FPX_ECUDA;
 }
 
-constexpr size_t kIdBarBytes = 8 * (2 * kIdMaxStages + 1);
+constexpr size_t kIdBarBytes = 8 * (2 * kIdMaxStages + 1) + 4 * kIdMaxStages;  // barriers, slot row blocks
 
 template <int FMT, int Q>
 int launch_idot(const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_bf16, float* y, uint8_t* ws,
@@ -375,7 +401,7 @@ int launch_idot(const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_bf
     int rc = make_slice_map(&A.map, Wq, row_bytes, N, slice_bytes(FMT));
     if (rc) return rc;
     A.N = (int)N; A.nsl = nsl; A.nbp = nbp; A.nrb = (int)((N + kIdRows - 1) / kIdRows); A.NS = NS;
-    A.tab_bytes = (uint32_t)tabB; A.tab = ws; A.y = y; A.st = st;
+    A.tab_bytes = (uint32_t)tabB; A.tab = ws; A.counter = reinterpret_cast<uint32_t*>(ws + tabB); A.y = y; A.st = st;
     const int units = Q * nbp;
     k_xquant<FMT><<<(units + 7) / 8, 256, 0, s>>>(x, x_bf16, (int)K, Q, nbp, ws, st);
     if (cudaGetLastError() != cudaSuccess) return FPX_ECUDA;
@@ -417,7 +443,7 @@ extern "C" {
 size_t fpx_gemv_idot_workspace_bytes(int64_t K, int q) {
     if (K < 0 || K % 32 || q < 1 || q > 4 || K > INT32_MAX / 8) return 0;
     const int64_t nbp = (K / 32 + 31) / 32 * 32;
-    return xtab_bytes((int)nbp, q);
+    return idot_ws_bytes((int)nbp, q);
 }
 
 int fpx_gemv_q_idot(int fmt, const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_dtype, int q, float* y,

@@ -128,7 +128,7 @@ int fpx_gemv_q(int fmt, const uint8_t* Wq, int64_t N, int64_t K, const void* x, 
                float* y, int32_t* dev_status, void* stream);
 
 /* Workspace bytes fpx_gemv_q_idot needs for K and q: (K/32 rounded up to a multiple of 32) * q * 68
- * (the activation table). 0 for invalid arguments. */
+ * (the activation table) + 16 (a row-block counter). 0 for invalid arguments. */
 size_t fpx_gemv_idot_workspace_bytes(int64_t K, int q);
 
 /* Integer-dot variant of fpx_gemv_q: the packed blocks are expanded with byte permutes into signed

@@ -117,8 +117,8 @@ def test_prefill_and_commit_argument_errors():
 
 def test_idot_argument_errors():
     L = fpx.lib()
-    assert fpx.fpx_gemv_idot_workspace_bytes(4096, 4) == 128 * 4 * 68
-    assert fpx.fpx_gemv_idot_workspace_bytes(1280, 1) == 64 * 68  # 40 blocks padded to 64
+    assert fpx.fpx_gemv_idot_workspace_bytes(4096, 4) == 128 * 4 * 68 + 16
+    assert fpx.fpx_gemv_idot_workspace_bytes(1280, 1) == 64 * 68 + 16  # 40 blocks padded to 64
     assert fpx.fpx_gemv_idot_workspace_bytes(4096, 5) == 0
     assert fpx.fpx_gemv_idot_workspace_bytes(100, 1) == 0
     ws = fpx.fpx_gemv_idot_workspace_bytes(1024, 2)
