@@ -668,11 +668,19 @@ def main():
     p.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--ref-seconds", type=float, default=90.0)
+    p.add_argument("--part", choices=["all", "idot"], default="all",
+                   help="idot: only the integer-dot / tensor-core GEMV comparison (one JSON object)")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.part == "idot":
+        import torch
+        import bit_block_quantized_wt_b300 as fpx
+        torch.cuda.set_device(0)
+        fpx.lib()
+        print(json.dumps(idot_measure(fpx, peaks()[0])), flush=True)
     else:
         run_fpx(args)
 
