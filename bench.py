@@ -495,6 +495,72 @@ def idot_measure(fpx, peak, reps=10):
                         "larger than L2), bfloat16 N(0,1) activations", "reps": reps, "results": res}
 
 
+def tiered_measure(fpx, stack, reps=16):
+    """moe_layer_decode_tiered on layer 0 with the 128 even-numbered experts in HBM slots and the other
+    128 in pinned host memory (Q * K_TOP staging slots), against moe_layer_decode on the all-HBM layer;
+    q = 4, top-4, 8 token batches rotating, CUDA events. Staged bytes: the cold experts of each batch's
+    union (gate + up + down), counted from the routing."""
+    import torch
+    import synth
+    g, u, d, sh, R = stack.bufs[0]
+    mb_gu, mb_d = fpx.fpx_matrix_bytes(2, I, H), fpx.fpx_matrix_bytes(3, H, I)
+    hot = torch.arange(0, E, 2)
+    n_hot, n_stage = len(hot), Q * K_TOP
+    n_slots = n_hot + n_stage
+    arrays = []
+    for full, mb in ((g, mb_gu), (u, mb_gu), (d, mb_d)):
+        a = torch.zeros(n_slots * mb, dtype=torch.uint8, device="cuda")
+        a.view(n_slots, mb)[:n_hot] = full.view(E, mb)[hot.cuda()]
+        arrays.append(a)
+    cold = [full.cpu().pin_memory() for full in (g, u, d)]
+    slot_of = torch.full((E,), -1, dtype=torch.int32)
+    slot_of[hot] = torch.arange(n_hot, dtype=torch.int32)
+    slot_of = slot_of.cuda()
+    lay = fpx.moe_layer(H=H, I=I, E=E, router=R.data_ptr(), gate=arrays[0].data_ptr(), up=arrays[1].data_ptr(),
+                        down=arrays[2].data_ptr(), sh_gate=sh[0].data_ptr(), sh_up=sh[1].data_ptr(),
+                        sh_down=sh[2].data_ptr())
+    tiers = fpx.moe_tiers(slot_of=slot_of.data_ptr(), cold_gate=cold[0].data_ptr(), cold_up=cold[1].data_ptr(),
+                          cold_down=cold[2].data_ptr(), n_slots=n_slots, stage_slot0=n_hot, n_stage=n_stage)
+    ws_b = fpx.moe_workspace_bytes(lay, Q, K_TOP)
+    ws = torch.empty(ws_b, dtype=torch.uint8, device="cuda")
+    xs = [torch.from_numpy(synth.tokens_bf16(Q, H, seed=2000 + b)[0].view(np.int16)).cuda() for b in range(N_BATCHES)]
+    y = torch.empty(Q, H, device="cuda")
+    idx = torch.empty(Q, K_TOP, dtype=torch.int32, device="cuda")
+
+    def run(tiered, b):
+        if tiered:
+            fpx.moe_layer_decode_tiered(lay, tiers, xs[b % N_BATCHES], Q, K_TOP, y, ws, ws_b, idx_out=idx)
+        else:
+            fpx.moe_layer_decode(stack.layers[0], xs[b % N_BATCHES], Q, K_TOP, y, ws, ws_b, idx_out=idx)
+
+    n_cold = []
+    for b in range(N_BATCHES):
+        run(False, b)
+        torch.cuda.synchronize()
+        uni = set(idx.cpu().numpy().ravel().tolist())
+        n_cold.append(sum(1 for e in uni if e % 2 == 1))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    res = {}
+    for name, tiered in (("all_hbm", False), ("two_tier", True)):
+        for b in range(3):
+            run(tiered, b)
+        torch.cuda.synchronize()
+        e0.record()
+        for b in range(reps):
+            run(tiered, b)
+        e1.record()
+        e1.synchronize()
+        res[name] = e0.elapsed_time(e1) / reps
+    st = fpx.fpx_read_status(ws[:4].view(torch.int32))
+    staged = float(np.mean([n_cold[b % N_BATCHES] for b in range(reps)])) * (2 * mb_gu + mb_d)
+    extra = res["two_tier"] - res["all_hbm"]
+    return {"workload": f"layer 0 (H {H}, I {I}, {E} experts, q {Q}, top-{K_TOP}); even experts in HBM, odd in pinned "
+                        "host memory", "hot_experts": n_hot, "status": st,
+            "ms_per_layer_all_hbm": round(res["all_hbm"], 4), "ms_per_layer_two_tier": round(res["two_tier"], 4),
+            "cold_experts_per_call": round(staged / (2 * mb_gu + mb_d), 2), "staged_MB_per_call": round(staged / 1e6, 2),
+            "staged_GB_per_s": round(staged / (extra / 1e3) / 1e9, 1) if extra > 0 else None, "reps": reps}
+
+
 def run_fpx(args):
     import torch
     world, rank, local = dist_env()
@@ -552,6 +618,7 @@ def run_fpx(args):
     dc = commit_measure(fpx, peak)
     qw = quantize_weighted_measure(fpx)
     idm = idot_measure(fpx, peak)
+    tm = tiered_measure(fpx, stack)
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -582,6 +649,7 @@ def run_fpx(args):
         "verify_commit": dc,
         "quantize_weighted": qw,
         "gemv_int_dot": idm,
+        "two_tier": tm,
         "gpu_launches": args.steps * NK * args.layers,
         "clocks": clk.summary(),
     }
@@ -668,8 +736,9 @@ def main():
     p.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--ref-seconds", type=float, default=90.0)
-    p.add_argument("--part", choices=["all", "idot"], default="all",
-                   help="idot: only the integer-dot / tensor-core GEMV comparison (one JSON object)")
+    p.add_argument("--part", choices=["all", "idot", "tiered"], default="all",
+                   help="idot: only the integer-dot / tensor-core GEMV comparison; tiered: only the two-tier "
+                        "residency measurement on a one-layer stack (one JSON object each)")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -681,6 +750,12 @@ def main():
         torch.cuda.set_device(0)
         fpx.lib()
         print(json.dumps(idot_measure(fpx, peaks()[0])), flush=True)
+    elif args.part == "tiered":
+        import torch
+        import bit_block_quantized_wt_b300 as fpx
+        torch.cuda.set_device(0)
+        fpx.lib()
+        print(json.dumps(tiered_measure(fpx, Stack(1))), flush=True)
     else:
         run_fpx(args)
 

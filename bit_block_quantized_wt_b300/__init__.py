@@ -36,6 +36,14 @@ class moe_layer(ctypes.Structure):
                 ("sh_down", ctypes.c_void_p)]
 
 
+class moe_tiers(ctypes.Structure):
+    """Mirror of the C struct: device slot_of [E], host (pinned) cold-tier gate/up/down arrays, the
+    number of HBM slots and the staging slot range."""
+    _fields_ = [("slot_of", ctypes.c_void_p), ("cold_gate", ctypes.c_void_p), ("cold_up", ctypes.c_void_p),
+                ("cold_down", ctypes.c_void_p), ("n_slots", ctypes.c_int), ("stage_slot0", ctypes.c_int),
+                ("n_stage", ctypes.c_int)]
+
+
 _lib = None
 
 _SIGS = {
@@ -69,6 +77,10 @@ _SIGS = {
                                                   ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                   ctypes.c_void_p]),
+    "moe_layer_decode_tiered": (ctypes.c_int, [ctypes.POINTER(moe_layer), ctypes.POINTER(moe_tiers), ctypes.c_void_p,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                               ctypes.c_void_p]),
     "moe_stack_verify": (ctypes.c_int, [ctypes.POINTER(moe_layer), ctypes.c_int, ctypes.c_void_p,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
@@ -188,6 +200,14 @@ def moe_layer_decode(layer, x, q, k, y, ws, ws_bytes, idx_out=None, w_out=None, 
     _check(lib().moe_layer_decode(ctypes.byref(layer), _ptr(x), q, k, _ptr(y), _ptr(idx_out),
                                   _ptr(w_out), _ptr(logits_out), _ptr(ws), ws_bytes, _stream(stream)),
            "moe_layer_decode")
+
+
+def moe_layer_decode_tiered(layer, tiers, x, q, k, y, ws, ws_bytes, idx_out=None, w_out=None, logits_out=None,
+                            stream=None):
+    """moe_layer_decode on a two-tier layer (see include/fpx.h)."""
+    _check(lib().moe_layer_decode_tiered(ctypes.byref(layer), ctypes.byref(tiers), _ptr(x), q, k, _ptr(y),
+                                         _ptr(idx_out), _ptr(w_out), _ptr(logits_out), _ptr(ws), ws_bytes,
+                                         _stream(stream)), "moe_layer_decode_tiered")
 
 
 def moe_layer_decode_static_ws(layer, x, q, k, y, idx_out=None, w_out=None, logits_out=None,

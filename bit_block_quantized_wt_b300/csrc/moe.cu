@@ -37,7 +37,7 @@ __device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontro
 // ------------------------------------------------------------------ workspace
 
 struct Ws {
-    size_t status, logits, u, idx, w, uni, nuni, gu, yi, gt, dt, total;
+    size_t status, logits, u, idx, w, uni, uslot, nuni, gu, yi, gt, dt, total;
     size_t gu_piece, yi_piece;  // floats between consecutive piece buffers
 };
 
@@ -52,6 +52,7 @@ inline Ws ws_layout(int H, int I, int E, int q, int k) {
     w.idx = o; o = up16(o + sizeof(int32_t) * q * k);
     w.w = o; o = up16(o + sizeof(float) * q * k);
     w.uni = o; o = up16(o + sizeof(int32_t) * q * k);
+    w.uslot = o; o = up16(o + sizeof(int32_t) * q * k);
     w.nuni = o; o += 16;  // n_uni, then the router's arrival counter
     w.gu_piece = (size_t)2 * (q * k + 1) * q * I;
     w.yi_piece = (size_t)(q * k + 1) * q * H;
@@ -76,6 +77,7 @@ struct WsPtrs {
     size_t gu_piece, yi_piece;
     uint8_t* gt;  // gate/up activation tables (table set for K = H), built by the router kernel
     uint8_t* dt;  // down activation tables, one table set for K = I per item, built by k_hpack
+    int32_t* uslot;  // matrix slot of every union item (the expert id, or its slot in a two-tier layer)
 };
 
 inline WsPtrs ws_ptrs(void* ws, const Ws& l) {
@@ -86,7 +88,7 @@ inline WsPtrs ws_ptrs(void* ws, const Ws& l) {
                   reinterpret_cast<int32_t*>(b + l.nuni),   reinterpret_cast<float*>(b + l.gu),
                   reinterpret_cast<float*>(b + l.yi),       l.gu_piece,
                   l.yi_piece,                                reinterpret_cast<uint8_t*>(b + l.gt),
-                  reinterpret_cast<uint8_t*>(b + l.dt)};
+                  reinterpret_cast<uint8_t*>(b + l.dt),      reinterpret_cast<int32_t*>(b + l.uslot)};
 }
 
 // Everything the gate/up and down kernels need about one layer: the stacked box-tiled matrices
@@ -144,6 +146,7 @@ struct Route {
     int32_t idx[kMaxQ * kMaxK];
     float w[kMaxQ * kMaxK];
     int32_t uni[kMaxQ * kMaxK];
+    int32_t slot[kMaxQ * kMaxK];  // where item j's matrices sit in the stacked arrays (see WsPtrs::uslot)
     uint32_t mask[kMaxE / 32];
     int32_t n_uni;
 };
@@ -420,6 +423,7 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
         A.ws.idx[i] = rt.idx[i];
         A.ws.w[i] = rt.w[i];
         A.ws.uni[i] = i < rt.n_uni ? rt.uni[i] : -1;
+        A.ws.uslot[i] = i < rt.n_uni ? rt.uni[i] : -1;  // a two-tier call rewrites cold items (k_stage)
         if (A.idx_out) A.idx_out[i] = rt.idx[i];
         if (A.w_out) A.w_out[i] = rt.w[i];
     }
@@ -440,6 +444,7 @@ __device__ inline void load_route(Route& r, const WsPtrs& ws, int qk) {
         r.idx[i] = __ldcg(ws.idx + i);
         r.w[i] = __ldcg(ws.w + i);
         r.uni[i] = __ldcg(ws.uni + i);
+        r.slot[i] = __ldcg(ws.uslot + i);
     }
     __syncthreads();
 }
@@ -535,7 +540,7 @@ __device__ __forceinline__ GuTask gu_task(uint32_t t, const Route& r, const Laye
         k.mat = (int)t / rb2;
         k.fp4 = 0;
         k.row0 = ((int)t % rb2) * 256;
-        k.off = r.uni[k.mat >> 1] * m.mb2 + tile_offset(2, k.row0, m.H);
+        k.off = r.slot[k.mat >> 1] * m.mb2 + tile_offset(2, k.row0, m.H);
     } else {
         const int t4 = (int)t - n2, rb4 = I / 64;
         k.mat = 2 * r.n_uni + t4 / rb4;
@@ -788,7 +793,7 @@ __device__ __forceinline__ DnTask dn_task(uint32_t t, const Route& r, const Laye
         k.item = (int)t / rb3;
         k.fp4 = 0;
         k.row0 = ((int)t % rb3) * 256;
-        k.off = r.uni[k.item] * m.mb3 + tile_offset(3, k.row0, m.I);
+        k.off = r.slot[k.item] * m.mb3 + tile_offset(3, k.row0, m.I);
     } else {
         k.item = r.n_uni;
         k.fp4 = 1;
@@ -1046,6 +1051,101 @@ Plan make_plan(const moe_layer& L, int q, int k) {
     return p;
 }
 
+// ------------------------------------------------------------------ two-tier residency
+//
+// A two-tier layer keeps the hot experts' matrices in HBM slots and the others (the cold tier) in
+// pinned host memory ("Token Freedom via APU ...", section "Asymmetric Dual-GPU": frequently used
+// experts stay in the fast memory, the rest in the larger, slower one). After routing, k_stage gives
+// every cold expert of the union a staging slot, copies its gate, up and down matrices from host
+// memory into that slot (reads over the host link, 16 bytes per thread per load), and rewrites the
+// union's slot list; the gate/up and down kernels then stream every item from HBM as usual, and the
+// combine still matches tokens to items by expert id, so the result is bit-identical to a layer whose
+// experts are all in HBM.
+
+struct StageArgs {
+    const int32_t* slot_of;               // [E]: HBM slot of expert e, or < 0 for the cold tier
+    const uint8_t *cgate, *cup, *cdown;   // cold tier: all E experts, stacked (device view of host memory)
+    uint8_t *gate, *up, *down;            // the layer's HBM slot arrays
+    int64_t mb2, mb3;
+    int E, n_slots, stage0, n_stage, qk;
+    WsPtrs ws;
+};
+
+constexpr int kStageThreads = 256;
+
+__global__ void __launch_bounds__(kStageThreads) k_stage(const __grid_constant__ StageArgs A) {
+    grid_dep_trigger();  // the gate/up kernel waits for this grid before it reads the slots or weights
+    grid_dep_wait();     // the union comes from the router kernel
+    __shared__ int32_t src[kMaxQ * kMaxK], dst[kMaxQ * kMaxK];
+    __shared__ int ncold;
+    if (threadIdx.x == 0) {
+        const int n = __ldcg(A.ws.nuni);
+        int nc = 0;
+        bool bad = false;
+        for (int j = 0; j < n && j < A.qk; j++) {
+            const int e = __ldcg(A.ws.uni + j);
+            int sl = e >= 0 && e < A.E ? A.slot_of[e] : -1;
+            // a slot outside the arrays or inside the staging range cannot hold a hot expert
+            if (sl >= A.n_slots || (sl >= A.stage0 && sl < A.stage0 + A.n_stage)) {
+                bad = true;
+                sl = -1;
+            }
+            if (sl < 0 && e >= 0 && e < A.E && nc < A.n_stage) {
+                src[nc] = e;
+                dst[nc] = A.stage0 + nc;
+                sl = A.stage0 + nc;
+                nc++;
+            }
+            if (blockIdx.x == 0) A.ws.uslot[j] = sl;
+        }
+        if (bad && blockIdx.x == 0) flag(A.ws.status, FPX_EDATA);
+        ncold = nc;
+    }
+    __syncthreads();
+    // copy the cold items: per item gate (mb2), up (mb2), down (mb3) bytes, in 16-byte units
+    const int64_t u2 = A.mb2 / 16, u3 = A.mb3 / 16, per = 2 * u2 + u3;
+    const int64_t total = per * ncold;
+    const int64_t stride = (int64_t)gridDim.x * kStageThreads;
+    int64_t u = (int64_t)blockIdx.x * kStageThreads + threadIdx.x;
+    auto addr = [&](int64_t v, const uint4*& from, uint4*& to) {
+        const int it = (int)(v / per);
+        int64_t r = v - (int64_t)it * per;
+        const int64_t e = src[it], sl = dst[it];
+        if (r < u2) {
+            from = reinterpret_cast<const uint4*>(A.cgate + e * A.mb2) + r;
+            to = reinterpret_cast<uint4*>(A.gate + sl * A.mb2) + r;
+        } else if (r < 2 * u2) {
+            r -= u2;
+            from = reinterpret_cast<const uint4*>(A.cup + e * A.mb2) + r;
+            to = reinterpret_cast<uint4*>(A.up + sl * A.mb2) + r;
+        } else {
+            r -= 2 * u2;
+            from = reinterpret_cast<const uint4*>(A.cdown + e * A.mb3) + r;
+            to = reinterpret_cast<uint4*>(A.down + sl * A.mb3) + r;
+        }
+    };
+    // four loads in flight per thread before their stores
+    for (; u + 3 * stride < total; u += 4 * stride) {
+        const uint4 *f0, *f1, *f2, *f3;
+        uint4 *t0, *t1, *t2, *t3;
+        addr(u, f0, t0);
+        addr(u + stride, f1, t1);
+        addr(u + 2 * stride, f2, t2);
+        addr(u + 3 * stride, f3, t3);
+        const uint4 v0 = *f0, v1 = *f1, v2 = *f2, v3 = *f3;
+        *t0 = v0;
+        *t1 = v1;
+        *t2 = v2;
+        *t3 = v3;
+    }
+    for (; u < total; u += stride) {
+        const uint4* f;
+        uint4* t;
+        addr(u, f, t);
+        *t = *f;
+    }
+}
+
 // Launches kern<<<grid, block, smem, s>>>(args), as a programmatic dependent launch when pdl is set
 // (the kernel calls grid_dep_wait() before reading what the previous kernel wrote).
 template <typename Args>
@@ -1066,7 +1166,7 @@ cudaError_t launch(void (*kern)(Args), int grid, int block, size_t smem, cudaStr
 template <int Q, int MODE>
 int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, const float* r, float* out,
                  int32_t* idx_out, float* w_out, float* logits_out, float* r_trace, WsPtrs ws, bool clear,
-                 cudaEvent_t const* ev, bool pdl_first, cudaStream_t s) {
+                 cudaEvent_t const* ev, bool pdl_first, cudaStream_t s, const StageArgs* tier = nullptr) {
     if (MODE == 1 && (size_t)Q * L.H > (size_t)4 * kRouterV * kRouterThreads) return FPX_EINVAL;  // router registers
     GateUpArgs ga{};
     DownArgs da{};
@@ -1103,6 +1203,11 @@ int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, co
     cudaError_t e = cudaSuccess;
     if (ev) cudaEventRecord(ev[0], s);
     e = e ? e : launch(k_router<MODE>, p.g_router, kRouterThreads, p.sm_router, s, pdl && pdl_first, ra);
+    if (tier) {
+        StageArgs sa = *tier;
+        sa.ws = ws;
+        e = e ? e : launch(k_stage, 4 * device_info().sms, kStageThreads, 0, s, pdl, sa);
+    }
     if (ev) cudaEventRecord(ev[1], s);
     e = e ? e : launch(k_gate_up<Q>, p.g_gate, kCtaThreads, p.sm_gate, s, pdl, ga);
     if (ev) cudaEventRecord(ev[2], s);
@@ -1117,12 +1222,12 @@ int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, co
 template <int MODE>
 int dispatch_q(int q, const moe_layer& L, const Plan& p, int k, const uint16_t* x, const float* r, float* out,
                int32_t* idx_out, float* w_out, float* logits_out, float* r_trace, WsPtrs ws, bool clear,
-               cudaEvent_t const* ev, bool pdl_first, cudaStream_t s) {
+               cudaEvent_t const* ev, bool pdl_first, cudaStream_t s, const StageArgs* tier = nullptr) {
     switch (q) {
-        case 1: return launch_layer<1, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, pdl_first, s);
-        case 2: return launch_layer<2, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, pdl_first, s);
-        case 3: return launch_layer<3, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, pdl_first, s);
-        case 4: return launch_layer<4, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, pdl_first, s);
+        case 1: return launch_layer<1, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, pdl_first, s, tier);
+        case 2: return launch_layer<2, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, pdl_first, s, tier);
+        case 3: return launch_layer<3, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, pdl_first, s, tier);
+        case 4: return launch_layer<4, MODE>(L, p, k, x, r, out, idx_out, w_out, logits_out, r_trace, ws, clear, ev, pdl_first, s, tier);
         default: return FPX_EINVAL;
     }
 }
@@ -1168,6 +1273,52 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
     if (cudaMemsetAsync(wp.nuni, 0, 16, s) != cudaSuccess) return FPX_ECUDA;
     Plan p = make_plan(*layer, q, k);
     return dispatch_q<0>(q, *layer, p, k, x, nullptr, y, idx_out, w_out, logits_out, nullptr, wp, true, nullptr, false, s);
+}
+
+int moe_layer_decode_tiered(const moe_layer* layer, const moe_tiers* tiers, const uint16_t* x, int q, int k, float* y,
+                            int32_t* idx_out, float* w_out, float* logits_out, void* ws, size_t ws_bytes, void* stream) {
+    int st = check_layer(layer);
+    if (st) return st;
+    if (!tiers || q < 1 || q > kMaxQ || k < 1 || k > kMaxK || k > layer->E || !x || !y || !ws) return FPX_EINVAL;
+    if (!tiers->slot_of || !tiers->cold_gate || !tiers->cold_up || !tiers->cold_down) return FPX_EINVAL;
+    const int need = q * k < layer->E ? q * k : layer->E;  // the largest union
+    if (tiers->n_slots < 1 || tiers->stage_slot0 < 0 || tiers->n_stage < need ||
+        (int64_t)tiers->stage_slot0 + tiers->n_stage > tiers->n_slots)
+        return FPX_EINVAL;
+    if (!aligned(ws, 16) || !aligned(x, 4) || !aligned(y, 4) || !aligned(tiers->slot_of, 4)) return FPX_EALIGN;
+    Ws wl = ws_layout(layer->H, layer->I, layer->E, q, k);
+    if (ws_bytes < wl.total) return FPX_ESPACE;
+    // the cold tier must be pinned host memory the device can read
+    void* dv[3] = {nullptr, nullptr, nullptr};
+    const uint8_t* hv[3] = {tiers->cold_gate, tiers->cold_up, tiers->cold_down};
+    for (int i = 0; i < 3; i++) {
+        if (cudaHostGetDevicePointer(&dv[i], const_cast<uint8_t*>(hv[i]), 0) != cudaSuccess || !dv[i]) {
+            cudaGetLastError();  // not pinned: report it here, leave no error behind
+            return FPX_EINVAL;
+        }
+        if (!aligned(dv[i], 16)) return FPX_EALIGN;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsPtrs wp = ws_ptrs(ws, wl);
+    if (cudaMemsetAsync(wp.nuni, 0, 16, s) != cudaSuccess) return FPX_ECUDA;
+    StageArgs sa{};
+    sa.slot_of = tiers->slot_of;
+    sa.cgate = static_cast<const uint8_t*>(dv[0]);
+    sa.cup = static_cast<const uint8_t*>(dv[1]);
+    sa.cdown = static_cast<const uint8_t*>(dv[2]);
+    sa.gate = const_cast<uint8_t*>(layer->gate);
+    sa.up = const_cast<uint8_t*>(layer->up);
+    sa.down = const_cast<uint8_t*>(layer->down);
+    sa.mb2 = matrix_bytes(2, layer->I, layer->H);
+    sa.mb3 = matrix_bytes(3, layer->H, layer->I);
+    sa.E = layer->E;
+    sa.n_slots = tiers->n_slots;
+    sa.stage0 = tiers->stage_slot0;
+    sa.n_stage = tiers->n_stage;
+    sa.qk = q * k;
+    Plan p = make_plan(*layer, q, k);
+    return dispatch_q<0>(q, *layer, p, k, x, nullptr, y, idx_out, w_out, logits_out, nullptr, wp, true, nullptr, false, s,
+                         &sa);
 }
 
 int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int q, int k, float* rL, int32_t* idx_out,

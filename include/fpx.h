@@ -191,6 +191,41 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
                      int32_t* idx_out, float* w_out, float* logits_out, void* ws, size_t ws_bytes,
                      void* stream);
 
+/* Two-tier expert residency for moe_layer_decode_tiered ("Token Freedom via APU ...", section
+ * "Asymmetric Dual-GPU": the frequently used experts live in the fast memory, the rest in the larger,
+ * slower one). The layer's gate / up / down arrays then hold n_slots expert slots in HBM (stacked as
+ * in moe_layer, slot s at s * fpx_matrix_bytes), not E experts:
+ *   slot_of     device int32 [E]: the HBM slot that holds expert e's three matrices, or -1 when e is
+ *               cold (only in the cold tier);
+ *   cold_gate, cold_up, cold_down: HOST pointers to pinned (page-locked) memory holding all E experts
+ *               stacked exactly as moe_layer's arrays (box-tiled); read by the device over the host
+ *               link, so they must stay pinned and unchanged during the call;
+ *   stage_slot0, n_stage: the HBM slots [stage_slot0, stage_slot0 + n_stage) that receive the cold
+ *               experts a call needs; n_stage >= min(q * k, E), stage_slot0 + n_stage <= n_slots,
+ *               and no hot expert may sit in that range. */
+typedef struct {
+    const int32_t* slot_of;
+    const uint8_t* cold_gate;
+    const uint8_t* cold_up;
+    const uint8_t* cold_down;
+    int n_slots;
+    int stage_slot0;
+    int n_stage;
+} moe_tiers;
+
+/* moe_layer_decode on a two-tier layer: after routing, every cold expert of the union is copied from
+ * the host tier into a staging slot (in ascending expert order: the i-th cold item takes slot
+ * stage_slot0 + i), and the layer runs on the slots. Results (y, routing, logits) are bit-identical to
+ * moe_layer_decode on a layer holding all E experts in HBM. A slot_of entry >= n_slots or inside the
+ * staging range sets FPX_EDATA in the status word and that expert is treated as cold. Same workspace
+ * as moe_layer_decode. Returns FPX_EINVAL if a cold pointer is not pinned host memory; the staging
+ * slots are overwritten by every call, so calls sharing them must be ordered on one stream. The
+ * pages' own design computes cold experts on the CPU cores; here every expert runs on the GPU and
+ * only the weights move. */
+int moe_layer_decode_tiered(const moe_layer* layer, const moe_tiers* tiers, const uint16_t* x, int q, int k,
+                            float* y, int32_t* idx_out, float* w_out, float* logits_out, void* ws,
+                            size_t ws_bytes, void* stream);
+
 /* moe_layer_decode for callers that cannot allocate device memory: a plugin or library running
  * inside a host framework that owns every device allocation (its own arena or allocator) and allows
  * no others, or a latency-critical loop that must never call cudaMalloc/cudaFree because they can

@@ -133,3 +133,23 @@ def test_idot_argument_errors():
     assert c(wsp=FAKE + 8) == fpx.FPX_EALIGN
     assert c(W=FAKE + 8) == fpx.FPX_EALIGN
     assert c(N=0) == fpx.FPX_OK                  # nothing to do
+
+
+def test_tiered_argument_errors():
+    L = fpx.lib()
+    lay = _layer()
+    ws = fpx.moe_workspace_bytes(lay, 4, 4)
+    t = lambda **kw: fpx.moe_tiers(**dict(dict(slot_of=FAKE, cold_gate=FAKE, cold_up=FAKE, cold_down=FAKE,
+                                                   n_slots=24, stage_slot0=8, n_stage=16), **kw))
+    call = lambda tiers, q=4, k=4, wsb=ws: L.moe_layer_decode_tiered(ctypes.byref(lay), ctypes.byref(tiers), FAKE, q, k,
+                                                                      FAKE, None, None, None, FAKE, wsb, None)
+    assert L.moe_layer_decode_tiered(ctypes.byref(lay), None, FAKE, 4, 4, FAKE, None, None, None, FAKE, ws,
+                                     None) == fpx.FPX_EINVAL
+    assert call(t(slot_of=None)) == fpx.FPX_EINVAL
+    assert call(t(cold_up=None)) == fpx.FPX_EINVAL
+    assert call(t(n_stage=15)) == fpx.FPX_EINVAL       # fewer staging slots than the largest union (16)
+    assert call(t(stage_slot0=9)) == fpx.FPX_EINVAL    # staging range past the slots
+    assert call(t(stage_slot0=-1)) == fpx.FPX_EINVAL
+    assert call(t(), q=5) == fpx.FPX_EINVAL
+    assert call(t(slot_of=FAKE + 2)) == fpx.FPX_EALIGN
+    assert call(t(), wsb=ws - 16) == fpx.FPX_ESPACE
