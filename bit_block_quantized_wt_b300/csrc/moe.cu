@@ -1054,8 +1054,9 @@ Plan make_plan(const moe_layer& L, int q, int k) {
 // ------------------------------------------------------------------ two-tier residency
 //
 // A two-tier layer keeps the hot experts' matrices in HBM slots and the others (the cold tier) in
-// pinned host memory ("Token Freedom via APU ...", section "Asymmetric Dual-GPU": frequently used
-// experts stay in the fast memory, the rest in the larger, slower one). After routing, k_stage gives
+// pinned host memory ("Token Freedom via APU ...", section "Asymmetric Dual-GPU": popular experts in
+// the fast memory, cold ones in the large pool; the Paiton page on DeepSeek V4.1 Flash, section
+// "Keeping useful work on the GPU": cold experts streamed to the GPU when that pays). After routing, k_stage gives
 // every cold expert of the union a staging slot, copies its gate, up and down matrices from host
 // memory into that slot (reads over the host link, 16 bytes per thread per load), and rewrites the
 // union's slot list; the gate/up and down kernels then stream every item from HBM as usual, and the

@@ -191,9 +191,10 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
                      int32_t* idx_out, float* w_out, float* logits_out, void* ws, size_t ws_bytes,
                      void* stream);
 
-/* Two-tier expert residency for moe_layer_decode_tiered ("Token Freedom via APU ...", section
- * "Asymmetric Dual-GPU": the frequently used experts live in the fast memory, the rest in the larger,
- * slower one). The layer's gate / up / down arrays then hold n_slots expert slots in HBM (stacked as
+/* Two-tier expert residency for moe_layer_decode_tiered ([P-apu] section "Asymmetric Dual-GPU": the
+ * popular experts live in the fast memory, the cold ones in the large pool, results merged on one
+ * device; the Paiton page on DeepSeek V4.1 Flash, section "Keeping useful work on the GPU": the most
+ * used experts on the GPU, the rest in host memory, streamed to the GPU for long prompts). The layer's gate / up / down arrays then hold n_slots expert slots in HBM (stacked as
  * in moe_layer, slot s at s * fpx_matrix_bytes), not E experts:
  *   slot_of     device int32 [E]: the HBM slot that holds expert e's three matrices, or -1 when e is
  *               cold (only in the cold tier);
@@ -221,7 +222,7 @@ typedef struct {
  * as moe_layer_decode. Returns FPX_EINVAL if a cold pointer is not pinned host memory; the staging
  * slots are overwritten by every call, so calls sharing them must be ordered on one stream. The
  * pages' own design computes cold experts on the CPU cores; here every expert runs on the GPU and
- * only the weights move. */
+ * only the weights move (the Paiton page's streaming mode). */
 int moe_layer_decode_tiered(const moe_layer* layer, const moe_tiers* tiers, const uint16_t* x, int q, int k,
                             float* y, int32_t* idx_out, float* w_out, float* logits_out, void* ws,
                             size_t ws_bytes, void* stream);
