@@ -167,6 +167,20 @@ def dist_env():
     return world, rank, local
 
 
+def over_ranks(secs, nbytes, world, device="cuda"):
+    """The whole job's time and work: the slowest rank's seconds and the sum of the bytes all ranks
+    streamed (every rank streams its own replica). Collective on the default process group."""
+    if world <= 1:
+        return secs, float(nbytes)
+    import torch
+    t = torch.tensor([secs, float(nbytes)], dtype=torch.float64, device=device)
+    tmax = t.clone()
+    torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
+    tsum = t.clone()
+    torch.distributed.all_reduce(tsum, op=torch.distributed.ReduceOp.SUM)
+    return float(tmax[0]), float(tsum[1])
+
+
 # ---------------------------------------------------------------------------- clocks (NVML)
 
 class ClockSampler:
@@ -578,14 +592,7 @@ def run_fpx(args):
     with ClockSampler(local) as clk:
         secs = timed(r4, args.steps, args.warmup, world)
     step_bytes = sum(bytes_per_batch[i % N_BATCHES] for i in range(args.steps))
-    # slowest rank decides the time; every rank streams its own replica
-    t = torch.tensor([secs, float(step_bytes)], dtype=torch.float64, device="cuda")
-    if world > 1:
-        tmax = t.clone(); torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
-        tsum = t.clone(); torch.distributed.all_reduce(tsum, op=torch.distributed.ReduceOp.SUM)
-        secs, total_bytes = float(tmax[0]), float(tsum[1])
-    else:
-        total_bytes = float(step_bytes)
+    secs, total_bytes = over_ranks(secs, step_bytes, world)
     value = total_bytes / secs / 1e9
     ms_step = secs / args.steps * 1e3
 
@@ -607,12 +614,11 @@ def run_fpx(args):
     u1 = r1.union_sizes()
     b1 = [sum(layer_bytes(n) for n in u) for u in u1]
     s1 = max(10, args.steps // 2)
-    secs1 = timed(r1, s1, args.warmup, world)
-    bytes1 = sum(b1[i % N_BATCHES] for i in range(s1)) * world
+    secs1, bytes1 = over_ranks(timed(r1, s1, args.warmup, world), sum(b1[i % N_BATCHES] for i in range(s1)), world)
 
     e2e_steps = max(10, min(args.steps, 200))
     e2e_secs, h2d, d2h = e2e_pass(r4, e2e_steps, world)
-    e2e_bytes = sum(bytes_per_batch[i % N_BATCHES] for i in range(e2e_steps)) * world
+    e2e_secs, e2e_bytes = over_ranks(e2e_secs, sum(bytes_per_batch[i % N_BATCHES] for i in range(e2e_steps)), world)
 
     pf = prefill_measure(fpx, stack.layers[0], args.warmup)
     dc = commit_measure(fpx, peak)
