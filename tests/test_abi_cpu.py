@@ -153,3 +153,19 @@ def test_tiered_argument_errors():
     assert call(t(), q=5) == fpx.FPX_EINVAL
     assert call(t(slot_of=FAKE + 2)) == fpx.FPX_EALIGN
     assert call(t(), wsb=ws - 16) == fpx.FPX_ESPACE
+
+
+def test_bench_traffic_needs_matching_sources(tmp_path, monkeypatch):
+    """bench.py reports a recorded DRAM count only while the layer sources match the capture's digest."""
+    import json
+    import bench
+    alg = 1_000_000
+    got = bench.recorded_traffic("k_gate_up", alg)
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    if rec["csrc"] == bench.csrc_digest():
+        assert got == round(rec["kernels"]["k_gate_up"]["dram_per_algorithmic_byte"] * alg)
+    else:
+        assert got is None
+    monkeypatch.setattr(bench, "csrc_digest", lambda: "0" * 16)  # sources changed since the capture
+    assert bench.recorded_traffic("k_gate_up", alg) is None
+    assert bench.recorded_traffic("no_such_kernel", alg) is None

@@ -157,3 +157,18 @@ def test_gemv_idot_within_grid_bound(fmt):
     yi2, _ = oracle.gemv_idot(fmt, Wq, N, K, xi)
     y2, _ = oracle.gemv(fmt, Wq, N, K, xi)
     assert np.array_equal(yi2, y2)
+
+
+def test_gemv_idot_special_cases():
+    """All-zero activations give exact zeros; one nonzero entry per block lies on the grid (it is the
+    block maximum, 8 significant bits at most) and gives the plain product exactly."""
+    N, K = 9, 256
+    Wq = synth.matrix(2, N, K, seed=3)
+    yi, M = oracle.gemv_idot(2, Wq, N, K, np.zeros((2, K)))
+    assert np.all(yi == 0.0) and np.all(M == 0.0)
+    x = np.zeros((2, K))
+    x[0, ::32] = [1.5, -0.375, 3.0, 0.75 * 2.0 ** -20, 2.0 ** 20, -7.0, 0.25, 96.0]
+    x[1, 5::32] = -np.ldexp(1.0, np.arange(-4, 4))
+    yi, _ = oracle.gemv_idot(2, Wq, N, K, x)
+    y, _ = oracle.gemv(2, Wq, N, K, x)
+    assert np.array_equal(yi, y)
