@@ -395,8 +395,9 @@ int orc_route(const float* R, int E, int H, const double* x, int q, int k, doubl
 }
 
 /* One expert applied to nt tokens (rows of X, stride H): g = G x, u = U x, h = silu(g) u, y = D h.
- * Also the first-order error magnitudes: Mg = sum |G x|, Mu = sum |U x|,
- * Mh = |silu'(g) u| Mg + |silu(g)| Mu + |h|, My_i = sum_j |D_ij| Mh_j.
+ * Also the first-order error magnitudes: Mg = sum |G x|, Mu = sum |U x| (the gate and up GEMVs' own
+ * allowances), Mh = |silu'(g) u| Mg + |silu(g)| Mu + |h|, My_i = sum_j |D_ij| Mh_j: the gate and up
+ * allowances carried through h, plus the down GEMV's own allowance sum_j |D_ij h_j| (the |h| term).
  * Writes Y[nt][H] and MY[nt][H]. */
 static int expert_apply(int fg, int fd, const uint8_t* G, const uint8_t* U, const uint8_t* D, int H,
                         int I, const double* X, int nt, double* Y, double* MY) {
@@ -444,9 +445,13 @@ static int expert_apply(int fg, int fd, const uint8_t* G, const uint8_t* U, cons
 /* The layer: route, run every selected expert once for all tokens that chose it and the shared
  * expert for all tokens, then combine out[t] = sum_r w[t][r] y_{e(t,r)}[t] + y_shared[t] (rank order,
  * shared last).
- * Tolerance magnitude M[t][i] (first-order propagation of a 2e-3 * sum|w x| bound through every
- * step): sum_r (w_r My_r,i + |y_r,i| Mw_r) + My_shared,i, with the router weight magnitude
- * Mw_r = (s'_r Ml_r + w_r sum_s s'_s Ml_s) / S, s = sigmoid(logit), s' = s(1-s), S = sum_s s. */
+ * Tolerance magnitude M[t][i]: the largest first-order change of out[t][i] when every GEMV output of
+ * the layer (logits, gate, up and down rows, routed and shared) is off by up to its own
+ * 2e-3 * sum|w x| allowance, each with its worst sign:
+ *   M = sum_r w_r My_r,i + sum_r s'_r Ml_r |y_r,i - ybar_i| / S + My_shared,i,
+ * with s = sigmoid(logit), s' = s (1 - s), S = sum_r s_r, ybar_i = sum_r w_r y_r,i (a logit error
+ * dl_r moves out by s'_r (y_r - ybar) dl_r / S, since dw_j/dl_r = s'_r (delta_jr - w_j) / S) and My the
+ * expert's magnitude from expert_apply. */
 int orc_moe_layer(int H, int I, int E, const float* R, const uint8_t* const* gate,
                   const uint8_t* const* up, const uint8_t* const* down, const uint8_t* sh_gate,
                   const uint8_t* sh_up, const uint8_t* sh_down, const double* x, int q, int k,
@@ -473,17 +478,14 @@ int orc_moe_layer(int H, int I, int E, const float* R, const uint8_t* const* gat
         }
     }
     for (int t = 0; t < q; t++) {
-        double S = 0.0, dsum = 0.0;
+        /* mw[t][r] = s'_r Ml_r / S: the output's sensitivity to logit r's allowance, per unit of
+         * |y_r - ybar| */
+        double S = 0.0;
+        for (int r = 0; r < k; r++) S += sigmoid(logits[(int64_t)t * E + idx[t * k + r]]);
         for (int r = 0; r < k; r++) {
             int e = idx[t * k + r];
             double s = sigmoid(logits[(int64_t)t * E + e]);
-            S += s;
-            dsum += s * (1.0 - s) * ml[(int64_t)t * E + e];
-        }
-        for (int r = 0; r < k; r++) {
-            int e = idx[t * k + r];
-            double s = sigmoid(logits[(int64_t)t * E + e]);
-            mw[t * k + r] = (s * (1.0 - s) * ml[(int64_t)t * E + e] + w[t * k + r] * dsum) / S;
+            mw[t * k + r] = s * (1.0 - s) * ml[(int64_t)t * E + e] / S;
         }
     }
     {
@@ -519,8 +521,10 @@ int orc_moe_layer(int H, int I, int E, const float* R, const uint8_t* const* gat
                 for (int r = 0; r < k; r++) {
                     int64_t o = ((int64_t)t * k + r) * H + i;
                     acc += w[t * k + r] * yr[o];
-                    mag += w[t * k + r] * myr[o] + fabs(yr[o]) * mw[t * k + r];
+                    mag += w[t * k + r] * myr[o];
                 }
+                for (int r = 0; r < k; r++)  /* acc = ybar here */
+                    mag += fabs(yr[((int64_t)t * k + r) * H + i] - acc) * mw[t * k + r];
                 y[(int64_t)t * H + i] = acc + ys[(int64_t)t * H + i];
                 if (M) M[(int64_t)t * H + i] = mag + mys[(int64_t)t * H + i];
             }
