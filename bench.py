@@ -444,6 +444,18 @@ def recorded_traffic(kernel, alg_bytes):
 
 # ---------------------------------------------------------------------------- CPU oracle
 
+def cpu_model():
+    """The host CPU's model name (first 'model name' line of /proc/cpuinfo), or None."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
 def oracle_layer_steps(stack_seed, r_trace, idx, budget_s, max_layers):
     """Times the oracle on whole layer-steps of the q=4 pass (teacher-forced on the GPU's residual):
     returns (seconds, packed bytes, layers)."""
@@ -645,6 +657,8 @@ def run_fpx(args):
                "layer_steps_per_s": round(args.layers * s1 * world / secs1, 1),
                "tokens_per_s": round(s1 * world / secs1, 1)},
         "kernels_ms": {n: round(float(v), 5) for n, v in zip(names, kavg)},
+        # achieved GB/s of every layer kernel: its algorithmic bytes (above) over its event-timed duration
+        "kernels_gbs": {n: round(a / (float(v) / 1e3) / 1e9, 1) for n, a, v in zip(names, alg, kavg)},
         "roofline": {"kernel": names[dom], "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(names[dom], alg[dom]), "algorithmic_bytes_per_launch": round(alg[dom]),
@@ -666,11 +680,19 @@ def run_fpx(args):
             r4.rin.copy_(r4.batches[0])
             fpx.moe_stack_verify(stack.layers, r4.rin, Q, K_TOP, r4.rL, r4.ws, r4.ws_b, idx_out=r4.idx, r_trace=tr)
             r4.stream.synchronize()
-        cs, cb, cl = oracle_layer_steps(0, tr.cpu().numpy(), r4.idx.cpu().numpy(), args.cpu_seconds, args.layers)
-        out["cpu_baseline"] = {"value": round(cb / cs / 1e9, 5), "unit": "GB/s", "cores": oracle.threads(),
-                               "kind": "oracle", "sample": f"{cl} whole layer-steps (layers 0..{cl - 1}) of the q=4 "
+        trn, idn = tr.cpu().numpy(), r4.idx.cpu().numpy()
+        cs, cb, cl = oracle_layer_steps(0, trn, idn, args.cpu_seconds, args.layers)
+        cores = oracle.threads()
+        prev = oracle.set_threads(1)  # the same layer-steps on one core, at least one, bounded in time
+        cs1, cb1, cl1 = oracle_layer_steps(0, trn, idn, args.cpu_seconds / 2, args.layers)
+        oracle.set_threads(prev)
+        out["cpu_baseline"] = {"value": round(cb / cs / 1e9, 5), "unit": "GB/s", "cores": cores,
+                               "kind": "oracle", "cpu_model": cpu_model(),
+                               "sample": f"{cl} whole layer-steps (layers 0..{cl - 1}) of the q=4 "
                                f"verify pass on token batch 0, teacher-forced on the GPU residual; {cs:.1f} s",
-                               "seconds": round(cs, 2), "bytes": cb}
+                               "seconds": round(cs, 2), "bytes": cb,
+                               "single_thread": {"value": round(cb1 / cs1 / 1e9, 5), "unit": "GB/s", "cores": 1,
+                                                 "layer_steps": cl1, "seconds": round(cs1, 2)}}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -685,7 +707,6 @@ def run_reference(args):
         return
     import oracle
     import synth
-    import bit_block_quantized_wt_b300 as fpx
     budget = args.ref_seconds
     layer = 0
     R = synth.router(E, H, 0, layer)
@@ -702,7 +723,7 @@ def run_reference(args):
     def sample(rows):
         t0, nbytes = time.perf_counter(), 0
         for i, (fmt, m, N, Kd) in enumerate(mats):
-            rb = Kd // 32 * fpx.fpx_block_bytes(fmt)
+            rb = Kd // 32 * oracle.block_bytes(fmt)
             r0 = (i * 97) % (N - rows + 1)
             oracle.gemv(fmt, m[r0 * rb:(r0 + rows) * rb], rows, Kd, x if Kd == H else hvec)
             nbytes += rows * rb
@@ -726,7 +747,7 @@ def run_reference(args):
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "config": {"workload": WORKLOAD, "layers": LAYERS, "q": Q, "top_k": K_TOP},
            "cpu_baseline": {"value": round(v, 5), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
-                            "sample": desc},
+                            "cpu_model": cpu_model(), "sample": desc},
            "e2e": {"value": round(v, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 

@@ -95,6 +95,7 @@ _SIGS = {
                                             ctypes.c_void_p, ctypes.c_void_p]),
     "fpx_quantize_weighted": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "fpx_debug_ring_wait": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_int]),
 }
 
 # Every symbol include/fpx.h declares (the export test checks them against the header).
@@ -255,3 +256,9 @@ def fpx_quantize_weighted(fmt, W, N, K, out, importance=None, dev_status=None, s
     """Importance-weighted quantizer (see include/fpx.h)."""
     _check(lib().fpx_quantize_weighted(fmt, _ptr(W), N, K, _ptr(importance), _ptr(out), _ptr(dev_status),
                                        _stream(stream)), "fpx_quantize_weighted")
+
+
+def fpx_debug_ring_wait(wait_ns, drop_stage=-1):
+    """Test hook for the layer kernels' bounded waits (see include/fpx.h): the wait limit in
+    nanoseconds and a weight copy for CTA 0 of the gate/up kernel to withhold (-1: none)."""
+    _check(lib().fpx_debug_ring_wait(wait_ns, drop_stage), "fpx_debug_ring_wait")

@@ -103,20 +103,30 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* b, uint32_t parity
     return ok != 0;
 }
 
-// Waits for the phase with the given parity, giving up after kWaitNs of wall time (or kSpinLimit
+// Waits for the phase with the given parity, giving up after limit_ns of wall time (or kSpinLimit
 // polls; each poll may suspend the thread for up to kSleepNs). Returns false when it gives up.
 constexpr uint32_t kSpinLimit = 1u << 24;
 constexpr uint64_t kWaitNs = 500000000ull;  // 0.5 s
 constexpr uint32_t kSleepNs = 20000;       // 20 us per poll
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint64_t limit_ns = kWaitNs) {
     if (mbar_try_wait(b, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 0; i < kSpinLimit; i++) {
         if (mbar_try_wait_sleep(b, parity, kSleepNs)) return true;
-        if (global_ns() - t0 > kWaitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return false;
 }
+
+// Test hooks of the streaming rings, one copy per translation unit (only the MoE layer file exposes a
+// setter, fpx_debug_ring_wait): the wall-time limit of the waits between a ring's producer and its
+// consumers (a stage's data, a free slot), and a stage index at which CTA 0's producer of the gate/up
+// kernel stops issuing copies, as if that copy were lost (-1: none). Waits for copies already issued
+// (the producer's drain, the activation tables) keep the fixed kWaitNs, so no copy can land in the
+// shared memory of a CTA that has exited.
+static __device__ uint64_t g_ring_wait_ns = kWaitNs;
+static __device__ int32_t g_ring_drop_stage = -1;
+__device__ __forceinline__ uint64_t ring_wait_ns() { return *reinterpret_cast<volatile uint64_t*>(&g_ring_wait_ns); }
 
 // The same on 32-bit shared addresses, for the consumer hot loops: one poll inline, the bounded
 // sleeping wait out of line (taken only when a stage has not landed yet).
@@ -129,11 +139,11 @@ __device__ __forceinline__ bool mbar_poll(uint32_t b, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Whole warp; true when every lane saw the phase complete within the wait limits.
+// Whole warp; true when every lane saw the phase complete within the wait limits (ring_wait_ns()).
 static __device__ __noinline__ bool mbar_wait_warp_slow(uint32_t b, uint32_t parity) {
     bool done = mbar_poll(b, parity);
     if (!done) {
-        const uint64_t t0 = global_ns();
+        const uint64_t t0 = global_ns(), limit = ring_wait_ns();
         for (uint32_t i = 0; i < kSpinLimit && !done; i++) {
             uint32_t ok;
             asm volatile(
@@ -142,7 +152,7 @@ static __device__ __noinline__ bool mbar_wait_warp_slow(uint32_t b, uint32_t par
                 : "r"(b), "r"(parity), "r"(kSleepNs)
                 : "memory");
             done = ok != 0;
-            if (!done && global_ns() - t0 > kWaitNs) break;
+            if (!done && global_ns() - t0 > limit) break;
         }
     }
     return __all_sync(0xffffffffu, done);
@@ -297,13 +307,17 @@ __device__ __forceinline__ int b_active_index(int lane) {
     return ((g >> 2) == (t >> 1)) ? 8 * (t >> 1) + 2 * (g & 3) + (t & 1) : -1;
 }
 
-// Column scale: x' = x * 2^(14 - floor(log2 max|x|)) keeps every column in binary16 normal range with
-// its largest element in [2^14, 2^15). Returns the exponent shift (0 for an all-zero column).
+// Column scale: x' = x * 2^(14 - floor(log2 max|x|)) puts a column's largest element in [2^14, 2^15).
+// Every element within 2^28 of the largest is then a binary16 normal (a bfloat16 element within 2^31
+// is exact), so the encoding adds at most 2^-11 |x| to an element, plus 2^(e - 40) for elements that
+// fall into the binary16 subnormal range (max |x| in [2^(e-1), 2^e)). Returns the exponent shift (0 for
+// an all-zero column), at most 110 so that 2^(shift + 3) stays a binary32 normal (a column whose largest
+// element is below 2^-96 is scaled less; it is still exact down to 2^-24 of that scale).
 __device__ __forceinline__ int column_shift(float amax) {
     if (!(amax > 0.0f) || !isfinite(amax)) return 0;
     int e;
     frexpf(amax, &e);  // amax in [2^(e-1), 2^e)
-    return 14 - (e - 1);
+    return min(14 - (e - 1), 110);
 }
 
 // ------------------------------------------------------------------ activation tables, batched
@@ -971,7 +985,7 @@ struct CtaRing {
     // Consumer warp: waits for stage n. The result is the same on all 32 lanes; on timeout lane 0
     // flags FPX_ETIMEOUT.
     __device__ __forceinline__ bool wait(uint32_t n, int32_t* st) const {
-        const bool ok = __any_sync(0xffffffffu, mbar_wait(full + (n % NS), (n / NS) & 1u));
+        const bool ok = __any_sync(0xffffffffu, mbar_wait(full + (n % NS), (n / NS) & 1u, ring_wait_ns()));
         if (!ok && (threadIdx.x & 31) == 0) flag(st, FPX_ETIMEOUT);
         return ok;
     }
@@ -999,9 +1013,11 @@ struct CtaRing {
         if ((threadIdx.x & 31) == 0) mbar_arrive_u32(smem_u32(empty) + p.idx * 8u);
     }
 
-    // Producer: waits (bounded) until stage n's slot is free, i.e. every consumer released n - NS.
+    // Producer: waits (bounded by ring_wait_ns()) until stage n's slot is free, i.e. every consumer
+    // released n - NS.
     __device__ __forceinline__ bool acquire(uint32_t n) const {
-        return n < (uint32_t)NS || mbar_wait(empty + (n % NS), ((n / NS) + 1u) & 1u);
+        return n < (uint32_t)NS || mbar_try_wait(empty + (n % NS), ((n / NS) + 1u) & 1u) ||
+               mbar_wait(empty + (n % NS), ((n / NS) + 1u) & 1u, ring_wait_ns());
     }
 
     // Producer, before exiting: waits (bounded) for the copies of the last stages it issued, so that

@@ -25,7 +25,17 @@ constexpr int kThreads = 256;  // router and top-k kernels
 constexpr int kMaxK = 8;
 constexpr int kMaxQ = 4;
 constexpr int kMaxE = 1024;
-constexpr int kMaxPieces = 3;  // partial results per task (see StageList)
+
+// Fixed pieces. A task of S stages (one output matrix x one row block, streamed along K) is computed
+// as pieces_of(S) pieces of consecutive stages, piece p covering stages [p S / P, (p + 1) S / P) with
+// its own accumulators starting at zero; each piece writes its own partial buffer and the next kernel
+// adds the pieces of a task in piece order. The split depends on the matrix shape alone, never on the
+// expert union, the grid or the other tokens, so every column of a batched call is computed with the
+// same roundings as a call on that column alone ("DeepSeek V4 Flash hits 32 tok/s on AMD Ryzen AI
+// MAX+ 395", paragraph 3: each packed weight decoded once and applied to every verification column).
+__host__ __device__ constexpr int pieces_of(int S) { return (S + 3) / 4; }
+__host__ __device__ constexpr int piece_begin(int S, int p) { return p * S / pieces_of(S); }
+constexpr int kMaxPieces = pieces_of(4608 / 256);  // H, I <= 4608
 
 // Programmatic dependent launch: each layer kernel is launched so that it may start while the
 // previous kernel's last CTAs still run; grid_dep_wait() blocks until that kernel has completed and
@@ -56,8 +66,8 @@ inline Ws ws_layout(int H, int I, int E, int q, int k) {
     w.nuni = o; o += 16;  // n_uni, then the router's arrival counter
     w.gu_piece = (size_t)2 * (q * k + 1) * q * I;
     w.yi_piece = (size_t)(q * k + 1) * q * H;
-    w.gu = o; o = up16(o + sizeof(float) * kMaxPieces * w.gu_piece);
-    w.yi = o; o = up16(o + sizeof(float) * kMaxPieces * w.yi_piece);
+    w.gu = o; o = up16(o + sizeof(float) * pieces_of(H / stage_k(2)) * w.gu_piece);  // FP2 tasks have the most pieces
+    w.yi = o; o = up16(o + sizeof(float) * pieces_of(I / stage_k(3)) * w.yi_piece);
     w.gt = o; o = up16(o + tset_bytes(H));
     w.dt = o; o = up16(o + (size_t)(q * k + 1) * dset_bytes(I));
     w.total = o;
@@ -198,13 +208,13 @@ __global__ void k_topk(const float* __restrict__ logits, int E, int q, int k, in
 
 // Computes the layer input u (bfloat16, in shared memory) and logits[t][e] for this CTA's 2 experts.
 // MODE 0: input x is bfloat16. MODE 1: input is the residual r; u = RN_bf16(r / rms(r)) in one pass
-// over r held in registers (q * H / 4 <= kRouterV * kRouterThreads float4 groups), and CTA 0
+// over r held in registers (q * ceil(H / 4096) <= kRouterV float4 groups per thread), and CTA 0
 // publishes u (for the gate/up kernel) and r (the trace). 15 warps per expert, each a fifteenth of H;
 // the slice sums are added in order; the last warp packs this CTA's slice of the gate/up activation
 // tables meanwhile. With k > 0, the last CTA to finish routes every token (top-k,
 // weights, union) and publishes the routing for the gate/up and down kernels.
 constexpr int kRouterThreads = 1024;
-constexpr int kRouterV = 5;  // q * H <= 20480: H <= 5120 at q = 4
+constexpr int kRouterV = 8;  // q * ceil(H / 4096) <= 8: every q at H <= 4608 (the layer limit)
 
 struct RouterArgs {
     const float* R;
@@ -286,6 +296,7 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
     // per-token maxima of |u| (the tables' column scales) and, MODE 1, sums of squares of r
     float ss[kMaxQ] = {0.f, 0.f, 0.f, 0.f}, mx[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
     float4 rv[kRouterV];
+    const int n_i = h4r > kRouterThreads ? 2 : 1;  // groups of a token per thread (H <= 8192)
     if (MODE == 0) {
         for (int i = threadIdx.x; i < n4; i += blockDim.x) {
             const uint2 pk = reinterpret_cast<const uint2*>(xin)[i];
@@ -297,21 +308,23 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
             for (int tt = 0; tt < kMaxQ; tt++) mx[tt] = tt == t ? fmaxf(mx[tt], mm) : mx[tt];
         }
     } else {
+        // thread x holds groups j = x + 1024 i (i < n_i) of every token, in slot t n_i + i: a token's
+        // sum of squares runs through the same threads and the same reduction tree whatever q, so a
+        // column normalises to the same bits alone or in a batch
         const float4* r4 = reinterpret_cast<const float4*>(rin);
 #pragma unroll
-        for (int i = 0; i < kRouterV; i++) {
-            const int idx = threadIdx.x + i * kRouterThreads;
-            rv[i] = idx < n4 ? r4[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sl = 0; sl < kRouterV; sl++) {
+            const int t = n_i == 1 ? sl : sl >> 1, j = threadIdx.x + (sl - t * n_i) * kRouterThreads;
+            rv[sl] = t < q && j < h4r ? r4[t * h4r + j] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int i = 0; i < kRouterV; i++) {
-            const int idx = threadIdx.x + i * kRouterThreads;
-            if (idx < n4) {
-                const int t = tok_of(idx);
+        for (int sl = 0; sl < kRouterV; sl++) {
+            const int t = n_i == 1 ? sl : sl >> 1, j = threadIdx.x + (sl - t * n_i) * kRouterThreads;
+            if (t < q && j < h4r) {
                 float a = 0.f;
-                a = fmaf(rv[i].x, rv[i].x, a); a = fmaf(rv[i].y, rv[i].y, a);
-                a = fmaf(rv[i].z, rv[i].z, a); a = fmaf(rv[i].w, rv[i].w, a);
-                const float mm = fmaxf(fmaxf(fabsf(rv[i].x), fabsf(rv[i].y)), fmaxf(fabsf(rv[i].z), fabsf(rv[i].w)));
+                a = fmaf(rv[sl].x, rv[sl].x, a); a = fmaf(rv[sl].y, rv[sl].y, a);
+                a = fmaf(rv[sl].z, rv[sl].z, a); a = fmaf(rv[sl].w, rv[sl].w, a);
+                const float mm = fmaxf(fmaxf(fabsf(rv[sl].x), fabsf(rv[sl].y)), fmaxf(fabsf(rv[sl].z), fabsf(rv[sl].w)));
 #pragma unroll
                 for (int tt = 0; tt < kMaxQ; tt++) {
                     ss[tt] += tt == t ? a : 0.f;
@@ -347,17 +360,17 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
     __syncthreads();
     if (MODE == 1) {
 #pragma unroll
-        for (int i = 0; i < kRouterV; i++) {
-            const int idx = threadIdx.x + i * kRouterThreads;
-            if (idx < n4) {
-                const float iv = inv_s[tok_of(idx)];
-                const __nv_bfloat162 lo = __floats2bfloat162_rn(rv[i].x * iv, rv[i].y * iv);
-                const __nv_bfloat162 hi = __floats2bfloat162_rn(rv[i].z * iv, rv[i].w * iv);
+        for (int sl = 0; sl < kRouterV; sl++) {
+            const int t = n_i == 1 ? sl : sl >> 1, j = threadIdx.x + (sl - t * n_i) * kRouterThreads, idx = t * h4r + j;
+            if (t < q && j < h4r) {
+                const float iv = inv_s[t];
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(rv[sl].x * iv, rv[sl].y * iv);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(rv[sl].z * iv, rv[sl].w * iv);
                 const uint2 pk = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
                 reinterpret_cast<uint2*>(u_s)[idx] = pk;
                 if (blockIdx.x == 0) {
                     reinterpret_cast<uint2*>(u_out)[idx] = pk;
-                    if (r_trace) reinterpret_cast<float4*>(r_trace)[idx] = rv[i];
+                    if (r_trace) reinterpret_cast<float4*>(r_trace)[idx] = rv[sl];
                 }
             }
         }
@@ -449,55 +462,43 @@ __device__ inline void load_route(Route& r, const WsPtrs& ws, int qk) {
     __syncthreads();
 }
 
-// The work of a streaming kernel as a list of stages: nA tasks of sA stages of cost cA each, then nB
-// tasks of sB stages of cost cB. CTA b of G owns the stages whose start cost c has
-// floor(c G / total) == b: a contiguous range of about total / G, so every CTA streams about the same
-// bytes whatever the task sizes. A task cut by CTA boundaries is computed in pieces (at most
-// kMaxPieces: the host caps G so that every CTA's share is at least the largest task / (kMaxPieces -
-// 1)), each written to its own partial buffer; the next kernel adds a task's pieces in order.
-struct StageList {
-    // All products stay below 2^32: stages <= 22032, costs <= 64 and G <= 148 (checked on the host by
-    // partition_fits), so the partition needs only 32-bit divisions.
-    uint32_t nA, sA, cA, nB, sB, cB;
-    __host__ __device__ __forceinline__ uint32_t stages() const { return nA * sA + nB * sB; }
-    __host__ __device__ __forceinline__ uint32_t total() const { return nA * sA * cA + nB * sB * cB; }
-    __host__ __device__ __forceinline__ uint32_t cost_before(uint32_t s) const {
-        const uint32_t a = nA * sA;
-        return s <= a ? s * cA : a * cA + (s - a) * cB;
-    }
-    __host__ __device__ __forceinline__ uint32_t owner(uint32_t s, uint32_t G) const { return cost_before(s) * G / total(); }
-    // first stage of CTA b (b == G: stages())
+// The units of a streaming kernel (one unit = one piece of one task): nA units of cost cA (the routed
+// experts' tasks, in task order, pieces in order), then nB units of cost cB (the shared expert's). CTA b
+// of G owns the units whose start cost c has floor(c G / total) == b: a contiguous range of about
+// total / G, so every CTA streams about the same bytes whatever the union.
+struct UnitList {
+    // All products stay below 2^32 (checked on the host by fits): the partition needs only 32-bit
+    // divisions.
+    uint32_t nA, cA, nB, cB;
+    __host__ __device__ __forceinline__ uint32_t units() const { return nA + nB; }
+    __host__ __device__ __forceinline__ uint32_t total() const { return nA * cA + nB * cB; }
+    // first unit of CTA b (b == G: units()): the smallest u with cost_before(u) * G >= total * b
     __host__ __device__ __forceinline__ uint32_t first(uint32_t b, uint32_t G) const {
-        const uint32_t a = nA * sA, tgt = total() * b;  // smallest s with cost_before(s) * G >= tgt
-        if (tgt <= a * cA * G) return (tgt + G * cA - 1) / (G * cA);
-        return a + (tgt - a * cA * G + G * cB - 1) / (G * cB);
+        const uint32_t tgt = total() * b;
+        if (tgt <= nA * cA * G) return (tgt + G * cA - 1) / (G * cA);
+        return nA + (tgt - nA * cA * G + G * cB - 1) / (G * cB);
     }
-    __host__ __device__ __forceinline__ uint32_t task_of(uint32_t s) const {
-        const uint32_t a = nA * sA;
-        return s < a ? s / sA : nA + (s - a) / sB;
-    }
-    __host__ __device__ __forceinline__ uint32_t task_first(uint32_t t) const { return t < nA ? t * sA : nA * sA + (t - nA) * sB; }
-    __host__ __device__ __forceinline__ uint32_t task_len(uint32_t t) const { return t < nA ? sA : sB; }
-    __host__ __device__ __forceinline__ int pieces(uint32_t t, uint32_t G) const {
-        const uint32_t f = task_first(t);
-        return (int)(owner(f + task_len(t) - 1, G) - owner(f, G) + 1);
-    }
-    __host__ __device__ __forceinline__ int piece(uint32_t t, uint32_t b, uint32_t G) const { return (int)(b - owner(task_first(t), G)); }
-    __host__ bool partition_fits(uint32_t G) const { return (uint64_t)nA * sA * cA + (uint64_t)nB * sB * cB <= 0xFFFFFFFFull / (G + 1); }
+    __host__ bool fits(uint32_t G) const { return (uint64_t)nA * cA + (uint64_t)nB * cB <= 0xFFFFFFFFull / (G + 1); }
 };
 
 // Relative time of a stage (in units of about 1 KB of a fast decode): bytes streamed for FP2 and FP3;
 // FP4 boxes (17 KB) weighted for their slower decode, which the down kernel's FP3 stages outpace more.
 constexpr uint32_t kCostFP2 = 20, kCostFP3 = 28, kCostFP4Gu = 23, kCostFP4Dn = 34;
 
-// Stage lists of the gate/up kernel (FP2 tasks: matrix x 256-row block, H/256 stages; FP4: matrix x
+__host__ __device__ constexpr uint32_t unit_cost(uint32_t c, int S) { return (c * S + pieces_of(S) / 2) / pieces_of(S); }
+
+// Unit lists of the gate/up kernel (FP2 tasks: matrix x 256-row block, H/256 stages; FP4: matrix x
 // 64-row block, H/512 stages) and of the down kernel (FP3: item x 256-row block, I/256 stages; FP4:
 // 64-row block, I/512 stages).
-__host__ __device__ inline StageList gate_up_stages(int n_uni, int H, int I) {
-    return StageList{2u * n_uni * (I / 256), (uint32_t)(H / stage_k(2)), kCostFP2, 2u * (I / 64), (uint32_t)(H / stage_k(4)), kCostFP4Gu};
+__host__ __device__ inline UnitList gate_up_units(int n_uni, int H, int I) {
+    const int sA = H / stage_k(2), sB = H / stage_k(4);
+    return UnitList{2u * n_uni * (I / 256) * pieces_of(sA), unit_cost(kCostFP2, sA), 2u * (I / 64) * pieces_of(sB),
+                    unit_cost(kCostFP4Gu, sB)};
 }
-__host__ __device__ inline StageList down_stages(int n_uni, int H, int I) {
-    return StageList{(uint32_t)n_uni * (H / 256), (uint32_t)(I / stage_k(3)), kCostFP3, (uint32_t)(H / 64), (uint32_t)(I / stage_k(4)), kCostFP4Dn};
+__host__ __device__ inline UnitList down_units(int n_uni, int H, int I) {
+    const int sA = I / stage_k(3), sB = I / stage_k(4);
+    return UnitList{(uint32_t)n_uni * (H / 256) * pieces_of(sA), unit_cost(kCostFP3, sA), (uint32_t)(H / 64) * pieces_of(sB),
+                    unit_cost(kCostFP4Dn, sB)};
 }
 
 // ------------------------------------------------------------------ K2: gate/up
@@ -505,7 +506,7 @@ __host__ __device__ inline StageList down_stages(int n_uni, int H, int I) {
 // Task = (output matrix, row block): the union's gate and up matrices (FP2, 256-row blocks of I,
 // H/256 stages each), then the shared expert's gate and up (FP4, 64-row blocks, H/512 stages).
 // Matrix m = 2 * item + (0 gate | 1 up), the shared expert being item n_uni. Each CTA owns a
-// contiguous range of stages of about equal cost (StageList); its producer thread streams the
+// contiguous range of units (fixed pieces of tasks) of about equal cost (UnitList); its producer thread streams the
 // range's boxes through the CTA ring and all consumer warps decode every box. Outputs g and u
 // (binary32) go to ws.gu[piece][m][token][row]; k_hpack adds the pieces and forms h = silu(g) u.
 struct GateUpArgs {
@@ -526,27 +527,38 @@ template <int NS>
 using DnRing = CtaRing<NS, stage_bytes(3)>;
 static_assert(stage_bytes(4) <= stage_bytes(2), "FP4 box fits a slot");
 
+// One unit of the gate/up kernel: a piece of a task, stages [s_beg, s_end) of the task.
 struct GuTask {
     int mat;      // output matrix index
     int fp4;      // shared expert (FP4) task
     int row0;     // first output row
     int64_t off;  // byte offset of the task's first tile in its (stacked) matrix
+    int piece, s_beg, s_end;
 };
 
-__device__ __forceinline__ GuTask gu_task(uint32_t t, const Route& r, const LayerMaps& m) {
-    const int I = m.I, rb2 = I / 256, n2 = 2 * r.n_uni * rb2;
+__device__ __forceinline__ GuTask gu_unit(uint32_t u, const Route& r, const LayerMaps& m) {
+    const int I = m.I, rb2 = I / 256, sA = m.H / stage_k(2), pA = pieces_of(sA);
+    const uint32_t nA = (uint32_t)(2 * r.n_uni * rb2 * pA);
     GuTask k;
-    if (t < n2) {
-        k.mat = (int)t / rb2;
+    if (u < nA) {
+        const int t = (int)u / pA;
+        k.piece = (int)u - t * pA;
+        k.mat = t / rb2;
         k.fp4 = 0;
-        k.row0 = ((int)t % rb2) * 256;
+        k.row0 = (t % rb2) * 256;
         k.off = r.slot[k.mat >> 1] * m.mb2 + tile_offset(2, k.row0, m.H);
+        k.s_beg = piece_begin(sA, k.piece);
+        k.s_end = piece_begin(sA, k.piece + 1);
     } else {
-        const int t4 = (int)t - n2, rb4 = I / 64;
+        const int sB = m.H / stage_k(4), pB = pieces_of(sB), rb4 = I / 64;
+        const int t4 = (int)(u - nA) / pB;
+        k.piece = (int)(u - nA) - t4 * pB;
         k.mat = 2 * r.n_uni + t4 / rb4;
         k.fp4 = 1;
         k.row0 = (t4 % rb4) * 64;
         k.off = tile_offset(4, k.row0, m.H);
+        k.s_beg = piece_begin(sB, k.piece);
+        k.s_end = piece_begin(sB, k.piece + 1);
     }
     return k;
 }
@@ -575,19 +587,22 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
     }
     load_route(r, A.ws, Q * A.k);
 
-    const StageList SL = gate_up_stages(r.n_uni, H, I);
-    const uint32_t G = A.G, s0 = SL.first(blockIdx.x, G), s1 = SL.first(blockIdx.x + 1, G);
+    const UnitList UL = gate_up_units(r.n_uni, H, I);
+    const uint32_t G = A.G, u0 = UL.first(blockIdx.x, G), u1 = UL.first(blockIdx.x + 1, G);
 
     if (warp == kWarps) {  // producer: streams the range's boxes while the consumers load the tables
         if (lane == 0) {
             uint32_t issued = 0;
             bool live = true;
-            for (uint32_t sg = s0; sg < s1 && live;) {
-                const uint32_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
-                const GuTask k = gu_task(tk, r, A.m);
-                for (; sg < te; sg++, issued++) {
+            // test hook: CTA 0 may withhold one copy (a lost message); its consumers' bounded waits
+            // then run out and report FPX_ETIMEOUT
+            const int32_t drop = blockIdx.x == 0 ? *reinterpret_cast<volatile int32_t*>(&g_ring_drop_stage) : -1;
+            for (uint32_t u = u0; u < u1 && live; u++) {
+                const GuTask k = gu_unit(u, r, A.m);
+                for (int s = k.s_beg; s < k.s_end; s++, issued++) {
+                    if (drop >= 0 && issued == (uint32_t)drop) { live = false; break; }
                     if (!R.acquire(issued)) { flag(A.ws.status, FPX_ETIMEOUT); live = false; break; }
-                    gu_issue(A, k, (int)(sg - tf), R.slot(issued), R.bar(issued));
+                    gu_issue(A, k, s, R.slot(issued), R.bar(issued));
                 }
             }
             R.drain(issued);
@@ -613,34 +628,31 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
     const uint32_t oq2_lane = lane_oq(oq2, 0, t);
     uint32_t bad = 0;
     typename decltype(R)::Pos pos{0u, 0u};
-    for (uint32_t sg = s0; sg < s1;) {
-        // the stages of one task inside this CTA's range: one piece of the task
-        const uint32_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
-        const GuTask k = gu_task(tk, r, A.m);
+    for (uint32_t u = u0; u < u1; u++) {
+        const GuTask k = gu_unit(u, r, A.m);
         float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         if (!k.fp4) {
-            const uint32_t s = (uint32_t)(sg - tf);
-            frag_stages<2>(R, pos, (int)(te - sg), warp * 32 + g, t, tab2_lane + s * tab2_step, tab2_step, oq2_lane + s * 256u,
+            const uint32_t s = (uint32_t)k.s_beg;
+            frag_stages<2>(R, pos, k.s_end - k.s_beg, warp * 32 + g, t, tab2_lane + s * tab2_step, tab2_step, oq2_lane + s * 256u,
                            magic, y, ok);
-            sg = te;
-        }
-        for (; sg < te; sg++) {  // FP4 (shared expert) stages
-            const int s = (int)(sg - tf);
-            if (ok) ok = R.wait_at(pos);
-            if (ok) {  // after a timeout the producer gives up too once this warp stops releasing
-                const int ch0 = s * box_chunks(4) + 4 * (warp >> 2);
-                box_tiles<4, 1, 4>(R.slot_at(pos) + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4), L4,
-                                   lane_tab(tab4, S.zero, a_idx, ch0), 0u, 0u, magic, *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
-                R.release_at(pos);
+        } else {
+            for (int s = k.s_beg; s < k.s_end; s++) {  // FP4 (shared expert) stages
+                if (ok) ok = R.wait_at(pos);
+                if (ok) {  // after a timeout the producer gives up too once this warp stops releasing
+                    const int ch0 = s * box_chunks(4) + 4 * (warp >> 2);
+                    box_tiles<4, 1, 4>(R.slot_at(pos) + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4), L4,
+                                       lane_tab(tab4, S.zero, a_idx, ch0), 0u, 0u, magic, *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
+                    R.release_at(pos);
+                }
+                R.next(pos);
             }
-            R.next(pos);
         }
         pair_reduce(y[0]);
         pair_reduce(y[1]);
-        if (k.fp4) fp4_reduce(S.red, y[0]);  // the same tasks run on every consumer warp
+        if (k.fp4) fp4_reduce(S.red, y[0]);  // the same units run on every consumer warp
         if (ok && t < 2 && (!k.fp4 || warp < 4)) {
             const int rb = k.row0 + (k.fp4 ? 16 : 32) * warp + g;
-            float* out = A.ws.gu + SL.piece(tk, blockIdx.x, G) * A.ws.gu_piece + (size_t)k.mat * Q * I;
+            float* out = A.ws.gu + (size_t)k.piece * A.ws.gu_piece + (size_t)k.mat * Q * I;
 #pragma unroll
             for (int i = 0; i < 4; i++) {
                 const int tok = 2 * t + (i & 1), rr = rb + 8 * (i >> 1);
@@ -665,7 +677,6 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
 // global memory. Token slots >= q get zero entries.
 struct HpackArgs {
     int H, I, k;
-    int G;  // grid of the gate/up kernel (its stage partition)
     WsPtrs ws;
 };
 
@@ -677,7 +688,6 @@ __global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__
     __shared__ __align__(16) float h_s[kHpackV * 4 * kHpackThreads];  // [I]
     __shared__ float red[kHpackThreads / 32];
     __shared__ int sh_s;
-    __shared__ int8_t np_s[2][kHpackV * 4 * kHpackThreads / 64];  // pieces of the gate / up task of each row block
     grid_dep_trigger();
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int I = A.I, j = blockIdx.x / 4, tok = blockIdx.x % 4;
@@ -690,33 +700,27 @@ __global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__
         const float4* g = reinterpret_cast<const float4*>(A.ws.gu + ((size_t)(2 * j) * Q + tok) * I);
         const float4* u = reinterpret_cast<const float4*>(A.ws.gu + ((size_t)(2 * j + 1) * Q + tok) * I);
         const size_t pstride = A.ws.gu_piece / 4;
-        // pieces of the item's gate and up tasks (routed: 256-row blocks 2j * (I/256) + rb and
-        // (2j+1) * (I/256) + rb; shared: 64-row blocks nA + rb and nA + I/64 + rb), one thread each
-        const StageList SL = gate_up_stages(n_uni, A.H, I);
-        const int rbs = j < n_uni ? 256 : 64, nrb = I / rbs;
-        if (threadIdx.x < 2 * nrb) {
-            const int m = threadIdx.x / nrb, rb = threadIdx.x % nrb;
-            const uint32_t tk = j < n_uni ? (uint32_t)(2 * j + m) * nrb + rb : SL.nA + (uint32_t)m * nrb + rb;
-            np_s[m][rb] = (int8_t)SL.pieces(tk, A.G);
-        }
-        __syncthreads();
+        // the fixed pieces of the item's gate and up tasks (routed: FP2, H/256 stages; shared: FP4,
+        // H/512 stages), added in piece order
+        const int np = pieces_of(j < n_uni ? A.H / stage_k(2) : A.H / stage_k(4));
         float4 ga[kHpackV], ua[kHpackV];
 #pragma unroll
         for (int v = 0; v < kHpackV; v++) {
             const int e = threadIdx.x + v * kHpackThreads;
             const bool in = e < I / 4;
-            const int ng = in ? np_s[0][4 * e / rbs] : 0, nu = in ? np_s[1][4 * e / rbs] : 0;
             float4 gp[kMaxPieces], up[kMaxPieces];
 #pragma unroll
             for (int p = 0; p < kMaxPieces; p++) {
-                gp[p] = p < ng ? __ldcg(g + p * pstride + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-                up[p] = p < nu ? __ldcg(u + p * pstride + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                gp[p] = in && p < np ? __ldcg(g + p * pstride + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                up[p] = in && p < np ? __ldcg(u + p * pstride + e) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             ga[v] = gp[0]; ua[v] = up[0];
 #pragma unroll
             for (int p = 1; p < kMaxPieces; p++) {
-                if (p < ng) { ga[v].x += gp[p].x; ga[v].y += gp[p].y; ga[v].z += gp[p].z; ga[v].w += gp[p].w; }
-                if (p < nu) { ua[v].x += up[p].x; ua[v].y += up[p].y; ua[v].z += up[p].z; ua[v].w += up[p].w; }
+                if (p < np) {
+                    ga[v].x += gp[p].x; ga[v].y += gp[p].y; ga[v].z += gp[p].z; ga[v].w += gp[p].w;
+                    ua[v].x += up[p].x; ua[v].y += up[p].y; ua[v].z += up[p].z; ua[v].w += up[p].w;
+                }
             }
         }
 #pragma unroll
@@ -770,7 +774,7 @@ __global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__
 
 // Task = (item, row block of H): the union's down matrices (FP3, 256-row blocks, I/256 stages), then
 // the shared expert's (FP4, 64-row blocks, I/512 stages). Each CTA owns a contiguous range of stages
-// of about equal cost (StageList), which spans at most two items; it copies their activation tables
+// of units of about equal cost (UnitList), which spans at most two items; it copies their activation tables
 // (built by k_hpack) at start. Outputs go to ws.yi[piece][item][token][row]; k_combine adds them up.
 struct DownArgs {
     LayerMaps m;
@@ -781,24 +785,36 @@ struct DownArgs {
     uint32_t magic;
 };
 
+// One unit of the down kernel: a piece of a task, stages [s_beg, s_end) of the task.
 struct DnTask {
     int item, fp4, row0;
     int64_t off;  // byte offset of the task's first tile in its (stacked) matrix
+    int piece, s_beg, s_end;
 };
 
-__device__ __forceinline__ DnTask dn_task(uint32_t t, const Route& r, const LayerMaps& m) {
-    const int H = m.H, rb3 = H / 256, n3 = r.n_uni * rb3;
+__device__ __forceinline__ DnTask dn_unit(uint32_t u, const Route& r, const LayerMaps& m) {
+    const int H = m.H, rb3 = H / 256, sA = m.I / stage_k(3), pA = pieces_of(sA);
+    const uint32_t nA = (uint32_t)(r.n_uni * rb3 * pA);
     DnTask k;
-    if (t < n3) {
-        k.item = (int)t / rb3;
+    if (u < nA) {
+        const int t = (int)u / pA;
+        k.piece = (int)u - t * pA;
+        k.item = t / rb3;
         k.fp4 = 0;
-        k.row0 = ((int)t % rb3) * 256;
+        k.row0 = (t % rb3) * 256;
         k.off = r.slot[k.item] * m.mb3 + tile_offset(3, k.row0, m.I);
+        k.s_beg = piece_begin(sA, k.piece);
+        k.s_end = piece_begin(sA, k.piece + 1);
     } else {
+        const int sB = m.I / stage_k(4), pB = pieces_of(sB);
+        const int t4 = (int)(u - nA) / pB;
+        k.piece = (int)(u - nA) - t4 * pB;
         k.item = r.n_uni;
         k.fp4 = 1;
-        k.row0 = ((int)t - n3) * 64;
+        k.row0 = t4 * 64;
         k.off = tile_offset(4, k.row0, m.I);
+        k.s_beg = piece_begin(sB, k.piece);
+        k.s_end = piece_begin(sB, k.piece + 1);
     }
     return k;
 }
@@ -824,10 +840,10 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
     grid_dep_trigger();
     load_route(r, A.ws, Q * A.k);
 
-    const StageList SL = down_stages(r.n_uni, H, I);
-    const uint32_t G = A.G, s0 = SL.first(blockIdx.x, G), s1 = SL.first(blockIdx.x + 1, G);
-    if (s0 >= s1) return;  // CTA-uniform: nothing to do
-    const int item_lo = dn_task(SL.task_of(s0), r, A.m).item, item_hi = dn_task(SL.task_of(s1 - 1), r, A.m).item;
+    const UnitList UL = down_units(r.n_uni, H, I);
+    const uint32_t G = A.G, u0 = UL.first(blockIdx.x, G), u1 = UL.first(blockIdx.x + 1, G);
+    if (u0 >= u1) return;  // CTA-uniform: nothing to do
+    const int item_lo = dn_unit(u0, r, A.m).item, item_hi = dn_unit(u1 - 1, r, A.m).item;
     if (item_hi - item_lo > 1) {  // cannot happen for the grids make_plan picks (each share < one item)
         if (threadIdx.x == 0) flag(A.ws.status, FPX_EINVAL);
         return;
@@ -837,12 +853,11 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
         if (lane == 0) {
             uint32_t issued = 0;
             bool live = true;
-            for (uint32_t sg = s0; sg < s1 && live;) {
-                const uint32_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
-                const DnTask k = dn_task(tk, r, A.m);
-                for (; sg < te; sg++, issued++) {
+            for (uint32_t u = u0; u < u1 && live; u++) {
+                const DnTask k = dn_unit(u, r, A.m);
+                for (int s = k.s_beg; s < k.s_end; s++, issued++) {
                     if (!R.acquire(issued)) { flag(A.ws.status, FPX_ETIMEOUT); live = false; break; }
-                    dn_issue(A, k, (int)(sg - tf), R.slot(issued), R.bar(issued));
+                    dn_issue(A, k, s, R.slot(issued), R.bar(issued));
                 }
             }
             R.drain(issued);
@@ -874,38 +889,35 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
     const LaneOfs L4 = lane_ofs<4>(t);
     uint32_t bad = 0;
     typename decltype(R)::Pos pos{0u, 0u};
-    for (uint32_t sg = s0; sg < s1;) {
-        // the stages of one task inside this CTA's range: one piece of the task
-        const uint32_t tk = SL.task_of(sg), tf = SL.task_first(tk), te = min(s1, tf + SL.task_len(tk));
-        const DnTask k = dn_task(tk, r, A.m);
+    for (uint32_t u = u0; u < u1; u++) {
+        const DnTask k = dn_unit(u, r, A.m);
         const int sl = k.item - item_lo;
         const uint8_t* ts = S.tabs + (size_t)sl * dset_copy_bytes(I);
         const uint2* tab = reinterpret_cast<const uint2*>(ts);
         const float* oq = reinterpret_cast<const float*>(ts + btab_bytes(I));
         float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         if (!k.fp4) {
-            const uint32_t s = (uint32_t)(sg - tf), b_step = a_idx >= 0 ? 4u * 512u : 0u;
-            frag_stages<3>(R, pos, (int)(te - sg), warp * 32 + g, t, lane_tab(tab, S.zero, a_idx, 0) + s * b_step, b_step,
+            const uint32_t s = (uint32_t)k.s_beg, b_step = a_idx >= 0 ? 4u * 512u : 0u;
+            frag_stages<3>(R, pos, k.s_end - k.s_beg, warp * 32 + g, t, lane_tab(tab, S.zero, a_idx, 0) + s * b_step, b_step,
                            lane_oq(oq, 0, t) + s * 256u, magic, y, ok);
-            sg = te;
-        }
-        for (; sg < te; sg++) {  // FP4 (shared expert) stages
-            const int s = (int)(sg - tf);
-            if (ok) ok = R.wait_at(pos);
-            if (ok) {
-                const int ch0 = s * box_chunks(4) + 4 * (warp >> 2);
-                box_tiles<4, 1, 4>(R.slot_at(pos) + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4), L4,
-                                   lane_tab(tab, S.zero, a_idx, ch0), 0u, 0u, magic, *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
-                R.release_at(pos);
+        } else {
+            for (int s = k.s_beg; s < k.s_end; s++) {  // FP4 (shared expert) stages
+                if (ok) ok = R.wait_at(pos);
+                if (ok) {
+                    const int ch0 = s * box_chunks(4) + 4 * (warp >> 2);
+                    box_tiles<4, 1, 4>(R.slot_at(pos) + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4), L4,
+                                       lane_tab(tab, S.zero, a_idx, ch0), 0u, 0u, magic, *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
+                    R.release_at(pos);
+                }
+                R.next(pos);
             }
-            R.next(pos);
         }
         pair_reduce(y[0]);
         pair_reduce(y[1]);
         if (k.fp4) fp4_reduce(S.red, y[0]);
         if (ok && t < 2 && (!k.fp4 || warp < 4)) {
             const int rb = k.row0 + (k.fp4 ? 16 : 32) * warp + g;
-            float* out = A.ws.yi + SL.piece(tk, blockIdx.x, G) * A.ws.yi_piece + (size_t)k.item * Q * H;
+            float* out = A.ws.yi + (size_t)k.piece * A.ws.yi_piece + (size_t)k.item * Q * H;
 #pragma unroll
             for (int i = 0; i < 4; i++) {
                 const int tok = 2 * t + (i & 1), rr = rb + 8 * (i >> 1);
@@ -928,7 +940,6 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
 // output; consecutive threads take consecutive rows.
 struct CombineArgs {
     int H, I, k;
-    int G;  // grid of the down kernel (its stage partition)
     WsPtrs ws;
     float* out;  // MODE 0: y [q][H]; MODE 1: residual r [q][H], updated in place
 };
@@ -941,7 +952,6 @@ template <int Q, int MODE>
 __global__ void __launch_bounds__(kCombineThreads) k_combine(const __grid_constant__ CombineArgs A) {
     __shared__ Route r;
     __shared__ float wsel[kMaxQ * kMaxK + 1][kMaxQ];  // weight of token t for union item j, NaN if unselected
-    __shared__ int8_t np_s[kMaxQ * kMaxK + 1][4];       // pieces of each item's task for this CTA's rows
     grid_dep_trigger();
     load_route(r, A.ws, Q * A.k);  // from the router kernel (completed two launches ago)
     for (int i = threadIdx.x; i < r.n_uni * Q; i += blockDim.x) {
@@ -951,18 +961,8 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(const __grid_consta
             if (r.idx[tok * A.k + rr] == r.uni[j]) wv = r.w[tok * A.k + rr];
         wsel[j][tok] = wv;
     }
-    // this CTA's kCombineThreads consecutive outputs lie in one token's rows [row0, row0 + 256): one
-    // 256-row block of each routed down task, four 64-row blocks of the shared one
-    const int H = A.H;
-    const StageList SL = down_stages(r.n_uni, H, A.I);
-    const int row0 = (blockIdx.x * kCombineThreads) % H;
-    for (int i = threadIdx.x; i < (r.n_uni + 1) * 4; i += blockDim.x) {
-        const int jj = i / 4, sub = i % 4;
-        int np = 0;
-        if (jj < r.n_uni) np = sub == 0 ? SL.pieces((uint32_t)jj * (H / 256) + row0 / 256, A.G) : 0;
-        else np = SL.pieces(SL.nA + row0 / 64 + sub, A.G);
-        np_s[jj][sub] = (int8_t)np;
-    }
+    // the fixed pieces of the routed (FP3, I/256 stages) and shared (FP4, I/512 stages) down tasks
+    const int H = A.H, np_r = pieces_of(A.I / stage_k(3)), np_s = pieces_of(A.I / stage_k(4));
     __syncthreads();
     grid_dep_wait();  // the down kernel's outputs
     const int o = blockIdx.x * kCombineThreads + threadIdx.x;
@@ -982,13 +982,14 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(const __grid_consta
         for (int u = 0; u < kCombineBatch; u++) {
             const int jj = min(j0 + u, jmax);
 #pragma unroll
-            for (int p = 0; p < kMaxPieces; p++) pv[u][p] = __ldcg(col + p * A.ws.yi_piece + (size_t)jj * istride);
+            for (int p = 0; p < kMaxPieces; p++)
+                pv[u][p] = p < np_r ? __ldcg(col + p * A.ws.yi_piece + (size_t)jj * istride) : 0.0f;
         }
 #pragma unroll
         for (int u = 0; u < kCombineBatch; u++) {
             const int jj = j0 + u;
             if (jj > r.n_uni) break;
-            const int np = jj < r.n_uni ? np_s[jj][0] : np_s[jj][(rr - row0) / 64];
+            const int np = jj < r.n_uni ? np_r : np_s;
             float yv = pv[u][0];
 #pragma unroll
             for (int p = 1; p < kMaxPieces; p++)
@@ -1020,8 +1021,7 @@ int check_layer(const moe_layer* L) {
         return FPX_EINVAL;
     // the stage partitions' 32-bit arithmetic, for the largest union and grid
     const int nmax = kMaxQ * kMaxK < L->E ? kMaxQ * kMaxK : L->E;
-    if (!gate_up_stages(nmax, L->H, L->I).partition_fits(1024) || !down_stages(nmax, L->H, L->I).partition_fits(1024))
-        return FPX_EINVAL;
+    if (!gate_up_units(nmax, L->H, L->I).fits(1024) || !down_units(nmax, L->H, L->I).fits(1024)) return FPX_EINVAL;
     return FPX_OK;
 }
 
@@ -1035,16 +1035,12 @@ Plan make_plan(const moe_layer& L, int q, int k) {
     Plan p{};
     p.g_router = (L.E + 1) / 2;
     p.sm_router = sizeof(uint16_t) * (size_t)q * L.H;
-    // largest grid (at most the SM count) whose per-CTA share of the smallest possible stage list (a
-    // union of k experts) is at least the largest task / (kMaxPieces - 1): no task has more pieces
-    auto grid_for = [&](const StageList& L) {
-        const int64_t big = L.sA * L.cA > L.sB * L.cB ? L.sA * L.cA : L.sB * L.cB;
-        int64_t gg = L.total() * (kMaxPieces - 1) / big;
-        return (int)(gg < di.sms ? (gg < 1 ? 1 : gg) : di.sms);
-    };
-    p.g_gate = grid_for(gate_up_stages(k, L.H, L.I));
+    // one CTA per SM, but no more CTAs than the units of the smallest union (k experts), so that a
+    // CTA's share stays below one routed item's units (the down kernel holds the tables of two items)
+    auto grid_for = [&](const UnitList& U) { return (int)(U.units() < (uint32_t)di.sms ? U.units() : (uint32_t)di.sms); };
+    p.g_gate = grid_for(gate_up_units(k, L.H, L.I));
     p.sm_gate = cta_smem_bytes(GuRing::kBytes, tset_copy_bytes(L.H));
-    p.g_down = grid_for(down_stages(k, L.H, L.I));
+    p.g_down = grid_for(down_units(k, L.H, L.I));
     p.ns_down = cta_smem_bytes(DnRing<5>::kBytes, 2 * dset_copy_bytes(L.I)) + 2048 <= 227 * 1024 ? 5 : 2;
     p.sm_down = cta_smem_bytes(p.ns_down == 5 ? DnRing<5>::kBytes : DnRing<2>::kBytes, 2 * dset_copy_bytes(L.I));
     p.g_comb = (q * L.H + kCombineThreads - 1) / kCombineThreads;
@@ -1168,7 +1164,7 @@ template <int Q, int MODE>
 int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, const float* r, float* out,
                  int32_t* idx_out, float* w_out, float* logits_out, float* r_trace, WsPtrs ws, bool clear,
                  cudaEvent_t const* ev, bool pdl_first, cudaStream_t s, const StageArgs* tier = nullptr) {
-    if (MODE == 1 && (size_t)Q * L.H > (size_t)4 * kRouterV * kRouterThreads) return FPX_EINVAL;  // router registers
+    if (MODE == 1 && Q * ((L.H / 4 + kRouterThreads - 1) / kRouterThreads) > kRouterV) return FPX_EINVAL;  // router registers
     GateUpArgs ga{};
     DownArgs da{};
     int st = make_layer_maps(L, &ga.m);
@@ -1192,13 +1188,13 @@ int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, co
     ra.idx_out = idx_out; ra.w_out = w_out; ra.logits_out = logits_out;
     auto kdown = p.ns_down == 5 ? k_down<Q, MODE, 5> : k_down<Q, MODE, 2>;
     HpackArgs ha{};
-    ha.H = L.H; ha.I = L.I; ha.k = k; ha.G = p.g_gate; ha.ws = ws;
+    ha.H = L.H; ha.I = L.I; ha.k = k; ha.ws = ws;
     if (cudaFuncSetAttribute(k_router<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_router) ||
         cudaFuncSetAttribute(k_gate_up<Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_gate) ||
         cudaFuncSetAttribute(kdown, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.sm_down))
         return FPX_ECUDA;
     CombineArgs ca{};
-    ca.H = L.H; ca.I = L.I; ca.k = k; ca.G = p.g_down; ca.ws = ws; ca.out = out;
+    ca.H = L.H; ca.I = L.I; ca.k = k; ca.ws = ws; ca.out = out;
     // timing events between the kernels would break the dependent-launch edges: no overlap then
     const bool pdl = ev == nullptr;
     cudaError_t e = cudaSuccess;
@@ -1348,6 +1344,15 @@ int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int
         if (st) return st;
     }
     if (events && cudaEventRecord(reinterpret_cast<cudaEvent_t const*>(events)[kKernelsPerLayer * n_layers], s) != cudaSuccess)
+        return FPX_ECUDA;
+    return FPX_OK;
+}
+
+int fpx_debug_ring_wait(uint64_t wait_ns, int drop_stage) {
+    if (wait_ns == 0 || wait_ns > kWaitNs || drop_stage < -1) return FPX_EINVAL;
+    const int32_t drop = drop_stage;
+    if (cudaMemcpyToSymbol(g_ring_wait_ns, &wait_ns, sizeof(wait_ns)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_ring_drop_stage, &drop, sizeof(drop)) != cudaSuccess)
         return FPX_ECUDA;
     return FPX_OK;
 }

@@ -36,10 +36,11 @@
  *     (the caller zeroes it), or the first word of the workspace (zeroed by each layer or stack call
  *     when it starts). Read it after the stream completes (fpx_read_status).
  *   - Results are deterministic: no floating-point atomics, and every reduction has a fixed order
- *     for given inputs and shapes, so a repeated call gives the same bits. In fpx_gemv_q that order
- *     depends on neither q nor the other columns (column t is bit-identical to a q = 1 call). In the
- *     layer calls the streamed work is split by the size of the expert union, so a column's rounding
- *     can change with the other columns of the batch (never its routing), within the tolerance.
+ *     for given inputs and shapes, so a repeated call gives the same bits. That order depends on
+ *     neither q nor the other columns: column t of a q-column call (fpx_gemv_q, fpx_gemv_q_idot,
+ *     moe_layer_decode, moe_layer_decode_tiered, moe_stack_verify) is bit-identical to a q = 1 call
+ *     on column t alone. In the layer calls every expert matrix is streamed in pieces whose K ranges
+ *     are fixed by the matrix shape (never by the expert union or the grid), added in piece order.
  */
 #ifndef FPX_H
 #define FPX_H
@@ -286,6 +287,17 @@ size_t moe_prefill_workspace_bytes(const moe_layer* layer, int T, int k);
 int moe_layer_prefill(const moe_layer* layer, const uint16_t* x, int T, int k, float* y, int32_t* idx_out,
                       float* w_out, float* logits_out, int32_t* perm_out, int32_t* offsets_out, void* ws,
                       size_t ws_bytes, void* stream);
+
+/* Test hook for the bounded device waits of the layer kernels (moe_layer_decode, _tiered, _static_ws,
+ * moe_stack_verify) on the current device; not for production use. wait_ns (1 .. 500,000,000; the
+ * default is 500,000,000) bounds each wait between a streaming kernel's producer and its consumers.
+ * drop_stage >= 0 makes CTA 0 of the gate/up kernel withhold its drop_stage-th weight copy, as if
+ * it were lost: its consumers wait wait_ns for it, give up, set FPX_ETIMEOUT in the status word and
+ * return, every copy that was issued having landed first; the result of that call is undefined, and
+ * later calls (with drop_stage = -1, the default) are unaffected. Host call, synchronous (it writes
+ * two device variables); make it between calls, never while a layer call runs. FPX_EINVAL for
+ * arguments out of range. The pages have no counterpart: this exists to test failure detection. */
+int fpx_debug_ring_wait(uint64_t wait_ns, int drop_stage);
 
 /* Speculative verify/commit for B sequences (B >= 0, 1 <= q <= 16, V >= 1): the target scored q
  * positions of each sequence (the seed and q - 1 draft tokens) in one pass; logits is binary32

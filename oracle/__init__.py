@@ -42,6 +42,7 @@ def lib():
             "orc_block_bytes": (I, [I]),
             "orc_matrix_bytes": (I64, [I, I64, I64]),
             "orc_threads": (I, []),
+            "orc_set_threads": (I, [I]),
             "orc_decode_block": (I, [I, P, P]),
             "orc_dequantize": (I, [I, P, I64, I64, P]),
             "orc_gemv": (I, [I, P, I64, I64, P, I, P, P]),
@@ -81,6 +82,11 @@ def matrix_bytes(fmt, N, K):
 
 def threads():
     return lib().orc_threads()
+
+
+def set_threads(n):
+    """Sets the OpenMP thread count of later oracle calls; returns the previous count."""
+    return lib().orc_set_threads(n)
 
 
 def decode_block(fmt, blk):

@@ -38,6 +38,17 @@ int orc_threads(void) {
 #endif
 }
 
+/* Sets the number of OpenMP threads later calls use (n >= 1); returns the previous number. */
+int orc_set_threads(int n) {
+    int prev = orc_threads();
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+    return prev;
+}
+
 /* Value of a binary16 bit pattern (exact in binary64). */
 static double binary16_to_double(unsigned h) {
     unsigned ex = (h >> 10) & 31, man = h & 1023;

@@ -32,6 +32,7 @@
 int orc_block_bytes(int fmt);
 int64_t orc_matrix_bytes(int fmt, int64_t N, int64_t K);
 int orc_threads(void);
+int orc_set_threads(int n);
 
 /* One block -> 32 binary64 values. */
 int orc_decode_block(int fmt, const uint8_t* blk, double* w);

@@ -95,3 +95,41 @@ def routing_gap_ok(logits, k, bound):
     if s.shape[1] <= k:
         return np.ones(s.shape[0], bool)
     return (s[:, k - 1] - s[:, k]) > bound
+
+
+def f32_to_bf16_bits(x):
+    """Round-to-nearest-even binary32 -> bfloat16 bits (finite inputs)."""
+    b = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def wide_bf16(q, K, seed, spike_log2, block_span):
+    """Activations with a wide dynamic range, as (bfloat16 bits [q][K], binary32 values [q][K]): N(0, 1)
+    entries whose 32-entry blocks are scaled by 2^j, j uniform in [-block_span, block_span]; 5% +0,
+    5% -0, 5% bfloat16 subnormals of either sign; and one spike of magnitude 2^spike_log2 per column."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((q, K))
+    x *= np.repeat(2.0 ** rng.integers(-block_span, block_span + 1, size=(q, K // 32)), 32, axis=1)
+    m = rng.random((q, K))
+    x[m < 0.05] = 0.0
+    x[(m >= 0.05) & (m < 0.10)] = -0.0
+    sub = (m >= 0.10) & (m < 0.15)
+    x[sub] = rng.choice([-1.0, 1.0], sub.sum()) * rng.integers(1, 128, sub.sum()) * 2.0**-133
+    for t in range(q):
+        x[t, rng.integers(K)] = rng.choice([-1.0, 1.0]) * 2.0**spike_log2
+    bits = f32_to_bf16_bits(x.astype(np.float32))
+    return bits, synth.bf16_bits_to_f32(bits).reshape(q, K)
+
+
+def zero_fp4_codes(Wq, N, K, frac, seed):
+    """Copy of a packed FP4 matrix with a fraction `frac` of its codes set to +0 (code 0)."""
+    W = np.array(Wq, np.uint8, copy=True)
+    rng = np.random.default_rng(seed)
+    blk = W[: N * (K // 32) * 17].reshape(-1, 17)
+    codes = blk[:, 1:]
+    lo = rng.random(codes.shape) < frac
+    hi = rng.random(codes.shape) < frac
+    codes[lo] &= 0xF0
+    codes[hi] &= 0x0F
+    blk[:, 1:] = codes
+    return W

@@ -81,6 +81,13 @@ def test_layer_argument_errors():
     assert L.moe_stack_verify(arr, 0, FAKE, 4, 4, FAKE, None, None, FAKE, ws, None, None) == fpx.FPX_EINVAL
 
 
+def test_wait_hook_argument_errors():
+    L = fpx.lib()
+    assert L.fpx_debug_ring_wait(0, -1) == fpx.FPX_EINVAL             # no limit
+    assert L.fpx_debug_ring_wait(500_000_001, -1) == fpx.FPX_EINVAL   # above the default 0.5 s
+    assert L.fpx_debug_ring_wait(2_000_000, -2) == fpx.FPX_EINVAL     # stage index below -1
+
+
 def test_route_and_quant_argument_errors():
     L = fpx.lib()
     assert L.moe_route_topk(FAKE, 8, 64, FAKE, 4, 9, FAKE, FAKE, FAKE, FAKE, FAKE, None) == fpx.FPX_EINVAL

@@ -93,9 +93,31 @@ def test_prefill_exact_ties_go_to_lower_index():
 
 
 def test_prefill_full_size_config5():
-    """2048 tokens, top-6, hidden 4096, 256 experts: routing and argsort for every token, the output
-    of sampled tokens (first, last, a tail-tile token and two others)."""
+    """2048 tokens, top-6, hidden 4096, 256 experts: routing and argsort for every token; the output of
+    at least 64 tokens: for the 8 experts with the most pairs, the tokens at both ends of every 64-pair
+    tile of the expert's group (the grouped GEMM's tile edges and the group's ragged tail), then the
+    first and last token and seeded random ones."""
     need_gpu()
     L = DeviceLayer(4096, 2048, 256, seed=0, layer=0)
     bits, vals = synth.tokens_bf16(2048, 4096, seed=0)
-    check_prefill(L, bits, vals, 6, [0, 1, 777, 1500, 2047])
+    k = 6
+    y, idx, w, lg, perm, offs = run_prefill(L, bits, k)
+    for t in range(2048):
+        assert list(idx[t]) == list(topk_of(lg[t], k))
+    p_ref, o_ref = oracle.stable_argsort(idx.ravel(), L.E)
+    assert np.array_equal(perm, p_ref) and np.array_equal(offs, o_ref)
+    sizes = np.diff(offs)
+    picked = {0, 2047}
+    for e in np.argsort(-sizes, kind="stable")[:8]:
+        n = int(sizes[e])
+        for pos in sorted({p for t0 in range(0, n, 64) for p in (t0, min(t0 + 63, n - 1))}):
+            picked.add(int(perm[offs[e] + pos]) // k)
+    rng = np.random.default_rng(5)
+    while len(picked) < 64:
+        picked.add(int(rng.integers(2048)))
+    sample = np.array(sorted(picked))
+    orc = L.oracle(vals[sample].astype(np.float64), k, idx_force=idx[sample])
+    assert np.all(np.abs(lg[sample] - orc["logits"]) <= 1e-4 + 1e-4 * np.abs(orc["logits"]))
+    assert np.allclose(w[sample], orc["w"], rtol=1e-5, atol=0)
+    err = np.abs(y[sample].astype(np.float64) - orc["y"])
+    assert np.all(err <= TOL * orc["M"]), float((err / orc["M"]).max())

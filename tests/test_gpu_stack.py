@@ -1,6 +1,6 @@
 """moe_stack_verify against the oracle, layer by layer (teacher-forced on the GPU's residual), for the
-q = 4 pass and for the q = 1 pass of its first column (checked on its own trace: the two may differ in
-rounding, since the kernels split the streamed work by the size of the expert union)."""
+q = 4 pass; the q = 1 pass of a column is bit-identical to that column of the q = 4 pass (final state,
+every layer's residual and routing)."""
 import numpy as np
 import pytest
 import torch
@@ -45,20 +45,25 @@ def check_pass(layers, r0, k, sample):
     for l in sample:
         r_out = tr[l + 1] if l + 1 < len(layers) else rL
         check_layer_step(layers[l], tr[l], r_out, idx[l], k)
+    return rL, idx, tr
 
 
-def check_stack(layers, q, k, sample):
+def check_stack(layers, q, k, sample, columns):
     H = layers[0].H
     bits, vals = synth.tokens_bf16(q, H, seed=99)
     r0 = vals.astype(np.float32)
-    check_pass(layers, r0, k, sample)
-    check_pass(layers, r0[:1], k, sample)
+    rL, idx, tr = check_pass(layers, r0, k, sample)
+    for t in columns:  # the q = 1 pass of column t: the same bits as column t of the batch
+        rL1, idx1, tr1 = run_stack(layers, r0[t : t + 1], 1, k)
+        assert np.array_equal(idx1[:, 0], idx[:, t])
+        assert np.array_equal(tr1[:, 0], tr[:, t])
+        assert np.array_equal(rL1[0], rL[t])
 
 
 def test_stack_small():
     need_gpu()
     layers = [DeviceLayer(512, 512, 16, seed=7, layer=l) for l in range(5)]
-    check_stack(layers, 4, 2, range(5))
+    check_stack(layers, 4, 2, range(5), columns=range(4))
 
 
 @pytest.mark.slow
@@ -67,4 +72,4 @@ def test_stack_config4_full_size():
     checked against the oracle."""
     need_gpu()
     layers = [DeviceLayer(4096, 2048, 256, seed=0, layer=l) for l in range(43)]
-    check_stack(layers, 4, 4, [0, 21, 42])
+    check_stack(layers, 4, 4, [0, 21, 42], columns=[0, 3])
