@@ -26,6 +26,7 @@
 // partial is multiplied by the block scale 2^(e-127) (exact for every exponent).
 #include "fpx_mma.cuh"
 #include "route.cuh"
+#include "tc.cuh"
 
 using namespace fpx;
 
@@ -39,7 +40,7 @@ constexpr int kPMaxK = 8;
 
 struct PWs {
     size_t status, logits, idx, w, counts, offsets, perm, inv, units, nunits, x16, shx;
-    size_t g, u, gsh, ush, h16, shh, hsh16, shsh, yp, ysh, total;
+    size_t g, u, gsh, ush, h16, shh, hsh16, shsh, yp, ysh, xg, gshift, tcu_gu, tcu_dn, ntc, total;
 };
 
 inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -70,6 +71,11 @@ PWs pws_layout(int64_t T, int64_t E, int64_t H, int64_t I, int64_t k) {
     w.shsh = o; o = up256(o + 4 * T);
     w.yp = o; o = up256(o + 4 * P * H);
     w.ysh = o; o = up256(o + 4 * T * H);
+    w.xg = o; o = up256(o + 2 * P * H);                            // activations gathered per pair, K-permuted
+    w.gshift = o; o = up256(o + 4 * P);
+    w.tcu_gu = o; o = up256(o + 16 * (P / 128 + E) * (I / 256));  // tensor-core GEMM units
+    w.tcu_dn = o; o = up256(o + 16 * (P / 128 + E) * (H / 256));
+    w.ntc = o; o = up256(o + 16);
     w.total = o;
     return w;
 }
@@ -513,7 +519,329 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_pgemm(const __grid_constant
     }
 }
 
+// ------------------------------------------------------------------ tcgen05 grouped GEMM (routed)
+//
+// The routed experts' GEMMs on the fifth-generation tensor cores. A unit is (expert e, 256 weight
+// rows, up to 128 of the expert's pairs): D[256 x n] = W_e[rows][K] * B[pairs][K]^T, accumulated in
+// binary32 in tensor memory as two M = 128 halves. Per 64-wide K slab:
+//   warp 0       streams the packed weight box (one 1-D bulk copy per 256 x 256 box) into a 2-slot
+//                ring and the slab of B (a 2-D TMA tile, 64 x 128, 128-byte swizzle) into a stage;
+//   warps 2..9   decode the box in registers into binary16 weights d (2c - 3) or d (2c - 7) (rounded
+//                once, as in the rest of the prefill) and write them into the stage in the swizzled
+//                K-major layout the MMA reads;
+//   warp 1       (one thread) issues 4 x 2 tcgen05.mma of 128 x n x 16 and commits them to the
+//                stage's release barrier; after the last slab, to the accumulator barrier;
+//   warps 10..13 read the finished accumulator (tcgen05.ld), scale each column by 2^-shift of its B
+//                row and store out[pair][row]; two accumulator buffers let this overlap the next unit.
+// The decode writes each 16-weight group in the order its binary16 pairs come out of the register
+// decode (pair p = weights p and p + 8); the B rows are stored in the same order (kpermute16), so the
+// products pair up as in the plain dot product.
+constexpr int kTcN = 128;                                           // pairs per unit at most
+constexpr int kTcStages = 3;                                        // A/B slab stages
+constexpr int kTcRS = 2;                                            // packed boxes in flight
+constexpr int kTcDec = 8, kTcEpi = 4;                               // decoder and epilogue warps
+constexpr int kTcThreads = (2 + kTcDec + kTcEpi) * 32;
+constexpr int kTcASlab = 256 * 128;                                 // 256 rows x 64 binary16
+constexpr int kTcBSlab = kTcN * 128;                                // 128 rows x 64 binary16
+constexpr int kTcBox = stage_bytes(3);                              // ring slot (an FP2 box fits)
+constexpr int kTcSmem = kTcRS * kTcBox + kTcStages * (kTcASlab + kTcBSlab) + 1024;
+constexpr int kTcCols = 512;                                        // 2 buffers x 2 halves x 128 columns
+static_assert(kTcBox % 1024 == 0 && kTcASlab % 1024 == 0 && kTcBSlab % 1024 == 0, "1024-byte aligned stages");
+
+struct TcArgs {
+    CUtensorMap bmap;         // B: binary16 [rows][K], K-permuted, box 64 x 128, 128-byte swizzle
+    const uint8_t* W;         // box-tiled matrix of expert 0
+    int64_t mstride;          // bytes between experts' matrices
+    int M, K;
+    const int4* units;        // (expert, first B row, pairs, 256-row block)
+    const int32_t* nunits;
+    const int32_t* shift;     // power-of-two scale exponent of every B row
+    float* out;               // [B rows][M]
+    int32_t* status;
+};
+
+// 16 weights of one decoded code group as binary16 pairs (pair p = weights p and p + 8) with the block
+// scale folded in: a = 1024 + c 2^P (decode_fp2 / decode_fp3_box), then 2c - K0 exactly
+// (2^(1-P) a - (2^(11-P) + K0)), then the product with d rounded once.
+template <int K0, int P>
+__device__ __forceinline__ uint32_t tc_level(uint32_t a, uint32_t d2) {
+    return hmul2_u(hfma2_u(a, f16x2(P + 0 >= 1 ? 2.0 / double(1 << P) : 1.0), f16x2(-(double(1 << (11 - P)) + K0))), d2);
+}
+
+template <int FMT>
+__device__ __forceinline__ void tc_group(const uint32_t (&a)[8], uint32_t d2, int odd, uint32_t (&o)[8]) {
+    if constexpr (FMT == 2) {
+        o[0] = tc_level<3, pair_shift(2, 0)>(a[0], d2); o[1] = tc_level<3, pair_shift(2, 1)>(a[1], d2);
+        o[2] = tc_level<3, pair_shift(2, 2)>(a[2], d2); o[3] = tc_level<3, pair_shift(2, 3)>(a[3], d2);
+        o[4] = tc_level<3, pair_shift(2, 4)>(a[4], d2); o[5] = tc_level<3, pair_shift(2, 5)>(a[5], d2);
+        o[6] = tc_level<3, pair_shift(2, 6)>(a[6], d2); o[7] = tc_level<3, pair_shift(2, 7)>(a[7], d2);
+    } else if (!odd) {
+        o[0] = tc_level<7, fp3_box_shift(0, 0)>(a[0], d2); o[1] = tc_level<7, fp3_box_shift(0, 1)>(a[1], d2);
+        o[2] = tc_level<7, fp3_box_shift(0, 2)>(a[2], d2); o[3] = tc_level<7, fp3_box_shift(0, 3)>(a[3], d2);
+        o[4] = tc_level<7, fp3_box_shift(0, 4)>(a[4], d2); o[5] = tc_level<7, fp3_box_shift(0, 5)>(a[5], d2);
+        o[6] = tc_level<7, fp3_box_shift(0, 6)>(a[6], d2); o[7] = tc_level<7, fp3_box_shift(0, 7)>(a[7], d2);
+    } else {
+        o[0] = tc_level<7, fp3_box_shift(1, 0)>(a[0], d2); o[1] = tc_level<7, fp3_box_shift(1, 1)>(a[1], d2);
+        o[2] = tc_level<7, fp3_box_shift(1, 2)>(a[2], d2); o[3] = tc_level<7, fp3_box_shift(1, 3)>(a[3], d2);
+        o[4] = tc_level<7, fp3_box_shift(1, 4)>(a[4], d2); o[5] = tc_level<7, fp3_box_shift(1, 5)>(a[5], d2);
+        o[6] = tc_level<7, fp3_box_shift(1, 6)>(a[6], d2); o[7] = tc_level<7, fp3_box_shift(1, 7)>(a[7], d2);
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant__ TcArgs A) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint64_t bars[18];
+    __shared__ uint32_t taddr_s;
+    uint8_t* base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
+    uint8_t* ring = base;
+    uint8_t* As = base + kTcRS * kTcBox;
+    uint8_t* Bs = As + kTcStages * kTcASlab;
+    uint64_t* ring_full = bars;       // [kTcRS]
+    uint64_t* ring_empty = bars + 2;  // [kTcRS], kTcDec arrivals
+    uint64_t* a_full = bars + 4;      // [kTcStages], kTcDec arrivals
+    uint64_t* b_full = bars + 7;      // [kTcStages]
+    uint64_t* slab_free = bars + 10;  // [kTcStages], one tcgen05.commit
+    uint64_t* acc_full = bars + 13;   // [2], one tcgen05.commit
+    uint64_t* acc_free = bars + 15;   // [2], kTcEpi arrivals
+    uint64_t* done = bars + 17;       // the MMA thread's last commit
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
+    if (tid == 0) {
+        for (int i = 0; i < kTcRS; i++) { mbar_init(ring_full + i, 1); mbar_init(ring_empty + i, kTcDec); }
+        for (int i = 0; i < kTcStages; i++) { mbar_init(a_full + i, kTcDec); mbar_init(b_full + i, 1); mbar_init(slab_free + i, 1); }
+        for (int i = 0; i < 2; i++) { mbar_init(acc_full + i, 1); mbar_init(acc_free + i, kTcEpi); }
+        mbar_init(done, 1);
+    }
+    fence_barrier_init();
+    __syncthreads();
+    if (warp == 1) tmem_alloc(smem_u32(&taddr_s), kTcCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t taddr = taddr_s;
+    const int nunits = __ldg(A.nunits), G = gridDim.x, c = blockIdx.x;
+    const int nslab = A.K / 64;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- loads (one thread)
+        if (lane == 0) {
+            uint32_t gs = 0, gb = 0;
+            bool live = true;
+            for (int u = c; u < nunits && live; u += G) {
+                const int4 un = A.units[u];
+                const uint8_t* wb = A.W + (int64_t)un.x * A.mstride + (int64_t)un.w * (A.K / stage_k(FMT)) * stage_bytes(FMT);
+                for (int j = 0; j < nslab && live; j++, gs++) {
+                    if ((j & 3) == 0) {
+                        const uint32_t sl = gb % kTcRS;
+                        if (gb >= (uint32_t)kTcRS && !mbar_wait(ring_empty + sl, ((gb / kTcRS) + 1u) & 1u)) { live = false; break; }
+                        mbar_expect_tx(ring_full + sl, stage_bytes(FMT));
+                        bulk_load(ring + sl * kTcBox, wb + (int64_t)(j >> 2) * stage_bytes(FMT), stage_bytes(FMT), ring_full + sl);
+                        gb++;
+                    }
+                    const uint32_t st = gs % kTcStages;
+                    if (gs >= (uint32_t)kTcStages && !mbar_wait(slab_free + st, ((gs / kTcStages) + 1u) & 1u)) { live = false; break; }
+                    mbar_expect_tx(b_full + st, kTcBSlab);
+                    tma_load_2d(Bs + st * kTcBSlab, &A.bmap, 64 * j, un.y, b_full + st);
+                }
+            }
+            if (!live) flag(A.status, FPX_ETIMEOUT);
+            // no copy may land after the CTA exits
+            for (uint32_t i = gb > (uint32_t)kTcRS ? gb - kTcRS : 0u; i < gb; i++) mbar_wait(ring_full + i % kTcRS, (i / kTcRS) & 1u);
+            for (uint32_t i = gs > (uint32_t)kTcStages ? gs - kTcStages : 0u; i < gs; i++) mbar_wait(b_full + i % kTcStages, (i / kTcStages) & 1u);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issue (one thread)
+        if (lane == 0) {
+            uint32_t gs = 0, it = 0;
+            bool live = true;
+            for (int u = c; u < nunits && live; u += G, it++) {
+                const int4 un = A.units[u];
+                const uint32_t n16 = (uint32_t)((un.z + 15) & ~15), idesc = f16_idesc(128, n16);
+                const uint32_t ab = it & 1u;
+                if (it >= 2 && !mbar_wait(acc_free + ab, ((it / 2) + 1u) & 1u)) { live = false; break; }
+                tc_fence_after();
+                const uint32_t dcol = taddr + ab * 256u;
+                for (int j = 0; j < nslab && live; j++, gs++) {
+                    const uint32_t st = gs % kTcStages, ph = (gs / kTcStages) & 1u;
+                    if (!mbar_wait(a_full + st, ph) || !mbar_wait(b_full + st, ph)) { live = false; break; }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(As + st * kTcASlab), b0 = smem_u32(Bs + st * kTcBSlab);
+#pragma unroll
+                    for (int kk = 0; kk < 4; kk++) {
+                        const uint64_t bd = sw128_desc(b0 + 32u * kk);
+                        tc_mma_f16(dcol, sw128_desc(a0 + 32u * kk), bd, idesc, (j | kk) != 0);
+                        tc_mma_f16(dcol + 128u, sw128_desc(a0 + 16384u + 32u * kk), bd, idesc, (j | kk) != 0);
+                    }
+                    tc_commit(smem_u32(slab_free + st));
+                }
+                if (live) tc_commit(smem_u32(acc_full + ab));
+            }
+            if (!live) flag(A.status, FPX_ETIMEOUT);
+            tc_commit(smem_u32(done));
+        }
+    } else if (warp < 2 + kTcDec) {
+        // ---------------------------------------------------------------- decode (8 warps)
+        const int td = tid - 64;
+        uint32_t gs = 0, gb = 0;
+        bool live = true;
+        const uint32_t magic = kMagic;
+        for (int u = c; u < nunits && live; u += G) {
+            for (int bx = 0; bx < nslab / 4 && live; bx++, gb++) {
+                const uint32_t sl = gb % kTcRS;
+                if (!__any_sync(0xffffffffu, mbar_wait(ring_full + sl, (gb / kTcRS) & 1u))) { live = false; break; }
+                const uint32_t box = smem_u32(ring + sl * kTcBox);
+                // this thread's (row, t) items: rows r = i / 4, code group t = i % 4 of each row, i = td + 256 jj
+                uint32_t cw[4][6];
+                uint2 sc[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; jj++) {
+                    const int i = td + 256 * jj, row = i >> 2, t = i & 3;
+                    if constexpr (FMT == 2) {
+                        const uint4 v = lds128<0>(box + (uint32_t)(row * 64 + 16 * t));
+                        cw[jj][0] = v.x; cw[jj][1] = v.y; cw[jj][2] = v.z; cw[jj][3] = v.w;
+                    } else {
+                        const uint32_t cb = box + (uint32_t)(row * 96 + 24 * t);
+                        const uint2 v0 = lds64<0>(cb), v1 = lds64<8>(cb), v2 = lds64<16>(cb);
+                        cw[jj][0] = v0.x; cw[jj][1] = v0.y; cw[jj][2] = v1.x; cw[jj][3] = v1.y; cw[jj][4] = v2.x; cw[jj][5] = v2.y;
+                    }
+                    sc[jj] = lds64<0>(box + (uint32_t)(box_scale_offset(FMT) + row * 16 + 8 * (t >> 1)));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ring_empty + sl);
+#pragma unroll
+                for (int C = 0; C < 4; C++, gs++) {
+                    const uint32_t st = gs % kTcStages;
+                    if (live && gs >= (uint32_t)kTcStages)
+                        live = __any_sync(0xffffffffu, mbar_wait(slab_free + st, ((gs / kTcStages) + 1u) & 1u));
+                    if (!live) break;
+                    uint8_t* as = As + st * kTcASlab;
+#pragma unroll
+                    for (int jj = 0; jj < 4; jj++) {
+                        const int i = td + 256 * jj, row = i >> 2, t = i & 3;
+                        const uint32_t w = C < 2 ? sc[jj].x : sc[jj].y;
+                        const uint32_t dh = (C & 1) ? (w >> 16) : (w & 0xFFFFu);
+                        const uint32_t d2 = dh | (dh << 16);
+                        uint32_t a[8], b[8], o[8];
+                        if constexpr (FMT == 2) {
+                            decode_fp2(cw[jj][C], magic, a);
+                            tc_group<2>(a, d2, 0, o);
+                        } else {
+                            const int m = C >> 1;
+                            decode_fp3_box(cw[jj][3 * m], cw[jj][3 * m + 1], cw[jj][3 * m + 2], magic, a, b);
+                            if (C & 1) tc_group<3>(b, d2, 1, o);
+                            else tc_group<3>(a, d2, 0, o);
+                        }
+                        uint8_t* hb = as + (row >= 128 ? 16384 : 0);
+                        const uint32_t rr = (uint32_t)(row & 127);
+                        *reinterpret_cast<uint4*>(hb + sw128_offset(rr, 16 * t)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4*>(hb + sw128_offset(rr, 16 * t + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the MMA reads through the async proxy
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(a_full + st);
+                }
+            }
+        }
+        if (!live && lane == 0) flag(A.status, FPX_ETIMEOUT);
+    } else {
+        // ---------------------------------------------------------------- epilogue (4 warps)
+        const int q = warp & 3;  // tensor-memory lane quarter of this warp
+        uint32_t it = 0;
+        bool live = true;
+        for (int u = c; u < nunits && live; u += G, it++) {
+            const int4 un = A.units[u];
+            const uint32_t ab = it & 1u;
+            live = __any_sync(0xffffffffu, mbar_wait(acc_full + ab, (it / 2) & 1u));
+            if (!live) break;
+            tc_fence_after();
+            const int n = un.z, n16 = (n + 15) & ~15;
+            for (int h = 0; h < 2; h++) {
+                const int m = un.w * 256 + h * 128 + 32 * q + lane;
+                for (int c0 = 0; c0 < n16; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(taddr + ((uint32_t)(32 * q) << 16) + ab * 256u + (uint32_t)(h * 128 + c0), v);
+#pragma unroll
+                    for (int j = 0; j < 16; j++) {
+                        const int s = c0 + j;
+                        if (s < n) {
+                            const int rowb = un.y + s;
+                            A.out[(size_t)rowb * A.M + m] = v[j] * exp2i(-__ldg(A.shift + rowb));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_free + ab);
+        }
+        if (!live && lane == 0) flag(A.status, FPX_ETIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        mbar_wait(done, 0);  // every MMA of this CTA has completed
+        tmem_dealloc(taddr, kTcCols);
+    }
+}
+
+// B rows for the routed gate/up GEMMs: xg[s] = the binary16 activation row of pair perm[s]'s token,
+// each 16-element group stored in the decode's pair order (element p, then p + 8), and its scale
+// exponent gshift[s]. One warp per row.
+__global__ void __launch_bounds__(256) k_pgather(const __half* __restrict__ x16, const int32_t* __restrict__ shx,
+                                                 const int32_t* __restrict__ perm, int P, int k, int H, __half* __restrict__ xg,
+                                                 int32_t* __restrict__ gshift) {
+    const int s = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x & 31;
+    if (s >= P) return;
+    const int tok = perm[s] / k;
+    if (lane == 0) gshift[s] = shx[tok];
+    const uint4* src = reinterpret_cast<const uint4*>(x16 + (size_t)tok * H);
+    uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)s * H);
+    for (int gi = lane; gi < H / 16; gi += 32) {
+        const uint4 a = src[2 * gi], b = src[2 * gi + 1];
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int p = 0; p < 8; p++) o[p] = __byte_perm(w[p >> 1], w[4 + (p >> 1)], (p & 1) ? 0x7632u : 0x5410u);
+        dst[2 * gi] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[2 * gi + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// The tensor-core GEMM units of the routed experts: for every expert with pairs, its pairs in tiles of
+// up to 128 (in sorted order), times the M / 256 row blocks; the row blocks of a tile are consecutive,
+// so CTAs working at the same time share B tiles in L2. One CTA of 1024 threads (E <= 1024).
+__global__ void __launch_bounds__(1024) k_tcunits(const int32_t* __restrict__ offsets, int E, int MT, int4* units,
+                                                  int32_t* nunits) {
+    __shared__ int part[32];
+    const int e = threadIdx.x, lane = e & 31, wid = e / 32;
+    const int n = e < E ? offsets[e + 1] - offsets[e] : 0, nt = (n + kTcN - 1) / kTcN;
+    int incl = nt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) part[wid] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < wid; w++) before += part[w];
+    const int base = before + incl - nt;
+    for (int i = 0; i < nt; i++)
+        for (int mt = 0; mt < MT; mt++) {
+            const int s0 = offsets[e] + i * kTcN;
+            units[(size_t)(base + i) * MT + mt] = make_int4(e, s0, min(kTcN, offsets[e + 1] - s0), mt);
+        }
+    if (e == 1023) {
+        int tot = 0;
+        for (int w = 0; w < 32; w++) tot += part[w];
+        *nunits = tot * MT;
+    }
+}
+
 // h = silu(g) u for rows [0, Pr) of (g, u) -> binary16 rows scaled by 2^sh(row) (exact shift), shift[row].
+// PERM: each 16-element group stored in the tensor-core decode's pair order (element p, then p + 8).
+template <bool PERM>
 __global__ void __launch_bounds__(256) k_ph(const float* __restrict__ g, const float* __restrict__ u, int L,
                                             __half* __restrict__ h16, int32_t* __restrict__ shift) {
     __shared__ float red[8];
@@ -536,9 +864,29 @@ __global__ void __launch_bounds__(256) k_ph(const float* __restrict__ g, const f
     }
     __syncthreads();
     const float sc = exp2i(sh_s);
-    for (int i = threadIdx.x; i < L; i += blockDim.x) {
-        const float a = g[r * L + i], b = u[r * L + i];
-        h16[r * L + i] = __float2half_rn(((a / (1.0f + expf(-a))) * b) * sc);
+    if (!PERM) {
+        for (int i = threadIdx.x; i < L; i += blockDim.x) {
+            const float a = g[r * L + i], b = u[r * L + i];
+            h16[r * L + i] = __float2half_rn(((a / (1.0f + expf(-a))) * b) * sc);
+        }
+        return;
+    }
+    for (int gi = threadIdx.x; gi < L / 16; gi += blockDim.x) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            const float a = g[r * L + 16 * gi + j], b = u[r * L + 16 * gi + j];
+            v[j] = ((a / (1.0f + expf(-a))) * b) * sc;
+        }
+        uint32_t o[8];
+#pragma unroll
+        for (int p = 0; p < 8; p++) {
+            const __half2 hp = __halves2half2(__float2half_rn(v[p]), __float2half_rn(v[p + 8]));
+            o[p] = *reinterpret_cast<const uint32_t*>(&hp);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(h16 + r * L + 16 * gi);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
 }
 
@@ -567,6 +915,30 @@ cudaError_t launch_gemm(const PGemmArgs& a, int grid_units, cudaStream_t s) {
     if (grid_units <= 0) return cudaSuccess;
     k_pgemm<FMT><<<dim3(a.M / G::R, grid_units), kGemmThreads, G::SMEM, s>>>(a);
     return cudaGetLastError();
+}
+
+// A 2-D tensor map over B (binary16 [rows][K]) for the tensor-core GEMM: boxes of 64 elements x 128
+// rows with the 128-byte swizzle; rows past the end read as zeros.
+int make_b_map(CUtensorMap* m, const __half* B, int64_t rows, int64_t K) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return FPX_ECUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
+    cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(kTcN)};
+    cuuint32_t es[2] = {1u, 1u};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<__half*>(B), dims, strides, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FPX_OK : FPX_ECUDA;
+}
+
+template <int FMT>
+int launch_tc(TcArgs& a, const __half* B, int64_t rows, cudaStream_t s) {
+    int st = make_b_map(&a.bmap, B, rows, a.K);
+    if (st) return st;
+    if (cudaFuncSetAttribute(k_tcgemm<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess) return FPX_ECUDA;
+    k_tcgemm<FMT><<<device_info().sms, kTcThreads, kTcSmem, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? FPX_OK : FPX_ECUDA;
 }
 
 }  // namespace
@@ -617,6 +989,11 @@ int moe_layer_prefill(const moe_layer* L, const uint16_t* x, int T, int k, float
     int32_t* shsh = reinterpret_cast<int32_t*>(b + W.shsh);
     float* yp = reinterpret_cast<float*>(b + W.yp);
     float* ysh = reinterpret_cast<float*>(b + W.ysh);
+    __half* xg = reinterpret_cast<__half*>(b + W.xg);
+    int32_t* gshift = reinterpret_cast<int32_t*>(b + W.gshift);
+    int4* tcu_gu = reinterpret_cast<int4*>(b + W.tcu_gu);
+    int4* tcu_dn = reinterpret_cast<int4*>(b + W.tcu_dn);
+    int32_t* ntc = reinterpret_cast<int32_t*>(b + W.ntc);
     const int P = T * k;
 
     if (cudaMemsetAsync(status, 0, 16, s) != cudaSuccess || cudaMemsetAsync(counts, 0, 4 * (E + 1), s) != cudaSuccess)
@@ -629,34 +1006,39 @@ int moe_layer_prefill(const moe_layer* L, const uint16_t* x, int T, int k, float
     k_pscatter<<<E, 256, 0, s>>>(idx, P, offsets, perm, inv);
     if (cudaGetLastError() != cudaSuccess) return FPX_ECUDA;
 
-    const int max_units = P / kPT + E, tok_units = (T + kPT - 1) / kPT;
+    const int tok_units = (T + kPT - 1) / kPT;
     const int64_t mb2 = fpx_matrix_bytes(2, I, H), mb3 = fpx_matrix_bytes(3, H, I);
-    PGemmArgs a{};
-    a.status = status;
-    // routed gate and up: rows of x gathered by token, in expert order
-    a.M = I; a.K = H; a.B = x16; a.rows = perm; a.row_div = k; a.shift = shx;
-    a.units = units; a.nunits = nunits; a.offsets = offsets; a.mstride = mb2;
-    a.W = L->gate; a.out = g;
-    if (launch_gemm<2>(a, max_units, s) != cudaSuccess) return FPX_ECUDA;
-    a.W = L->up; a.out = u;
-    if (launch_gemm<2>(a, max_units, s) != cudaSuccess) return FPX_ECUDA;
+    // routed experts on the tcgen05 tensor cores: activations gathered per pair in expert order
+    k_pgather<<<(P + 7) / 8, 256, 0, s>>>(x16, shx, perm, P, k, H, xg, gshift);
+    k_tcunits<<<1, 1024, 0, s>>>(offsets, E, I / 256, tcu_gu, ntc);
+    k_tcunits<<<1, 1024, 0, s>>>(offsets, E, H / 256, tcu_dn, ntc + 1);
+    if (cudaGetLastError() != cudaSuccess) return FPX_ECUDA;
+    TcArgs ta{};
+    ta.status = status;
+    ta.M = I; ta.K = H; ta.units = tcu_gu; ta.nunits = ntc; ta.shift = gshift; ta.mstride = mb2;
+    ta.W = L->gate; ta.out = g;
+    int st = launch_tc<2>(ta, xg, P, s);
+    if (st) return st;
+    ta.W = L->up; ta.out = u;
+    if ((st = launch_tc<2>(ta, xg, P, s))) return st;
     // shared gate and up: every token
-    PGemmArgs sa = a;
-    sa.rows = nullptr; sa.row_div = 1; sa.units = nullptr; sa.nunits = nullptr; sa.offsets = nullptr; sa.mstride = 0;
-    sa.n_rows = T; sa.shift = shx;
+    PGemmArgs sa{};
+    sa.status = status;
+    sa.M = I; sa.K = H; sa.B = x16; sa.rows = nullptr; sa.row_div = 1; sa.units = nullptr; sa.nunits = nullptr;
+    sa.offsets = nullptr; sa.mstride = 0; sa.n_rows = T; sa.shift = shx;
     sa.W = L->sh_gate; sa.out = gsh;
     if (launch_gemm<4>(sa, tok_units, s) != cudaSuccess) return FPX_ECUDA;
     sa.W = L->sh_up; sa.out = ush;
     if (launch_gemm<4>(sa, tok_units, s) != cudaSuccess) return FPX_ECUDA;
-    // h in binary16 with per-row scales
-    k_ph<<<P, 256, 0, s>>>(g, u, I, h16, shh);
-    k_ph<<<T, 256, 0, s>>>(gsh, ush, I, hsh16, shsh);
+    // h in binary16 with per-row scales (routed rows K-permuted for the tensor-core GEMM)
+    k_ph<true><<<P, 256, 0, s>>>(g, u, I, h16, shh);
+    k_ph<false><<<T, 256, 0, s>>>(gsh, ush, I, hsh16, shsh);
     if (cudaGetLastError() != cudaSuccess) return FPX_ECUDA;
     // routed down: h rows already in expert order
-    PGemmArgs da = a;
-    da.M = H; da.K = I; da.B = h16; da.rows = nullptr; da.row_div = 1; da.shift = shh; da.mstride = mb3;
-    da.W = L->down; da.out = yp;
-    if (launch_gemm<3>(da, max_units, s) != cudaSuccess) return FPX_ECUDA;
+    TcArgs tda = ta;
+    tda.M = H; tda.K = I; tda.units = tcu_dn; tda.nunits = ntc + 1; tda.shift = shh; tda.mstride = mb3;
+    tda.W = L->down; tda.out = yp;
+    if ((st = launch_tc<3>(tda, h16, P, s))) return st;
     PGemmArgs dsa = sa;
     dsa.M = H; dsa.K = I; dsa.B = hsh16; dsa.shift = shsh; dsa.W = L->sh_down; dsa.out = ysh;
     if (launch_gemm<4>(dsa, tok_units, s) != cudaSuccess) return FPX_ECUDA;
