@@ -523,33 +523,47 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_pgemm(const __grid_constant
 //
 // The routed experts' GEMMs on the fifth-generation tensor cores. A unit is (expert e, 256 weight
 // rows, up to 128 of the expert's pairs): D[256 x n] = W_e[rows][K] * B[pairs][K]^T, accumulated in
-// binary32 in tensor memory as two M = 128 halves. Per 64-wide K slab:
-//   warp 0       streams the packed weight box (one 1-D bulk copy per 256 x 256 box) into a 2-slot
-//                ring and the slab of B (a 2-D TMA tile, 64 x 128, 128-byte swizzle) into a stage;
-//   warps 2..9   decode the box in registers into binary16 weights d (2c - 3) or d (2c - 7) (rounded
-//                once, as in the rest of the prefill) and write them into the stage in the swizzled
-//                K-major layout the MMA reads;
-//   warp 1       (one thread) issues 4 x 2 tcgen05.mma of 128 x n x 16 and commits them to the
-//                stage's release barrier; after the last slab, to the accumulator barrier;
-//   warps 10..13 read the finished accumulator (tcgen05.ld), scale each column by 2^-shift of its B
-//                row and store out[pair][row]; two accumulator buffers let this overlap the next unit.
-// The decode writes each 16-weight group in the order its binary16 pairs come out of the register
+// binary32 in tensor memory as two M = 128 halves. The decoded weights never touch shared memory: they
+// are the MMA's A operand in tensor memory. Per 64-wide K slab:
+//   warp 0       streams the packed weight boxes (one 1-D bulk copy per 256 x 256 box) into a ring;
+//   warp 1       streams the slab of B (2-D TMA tiles of 16 rows x 64, 128-byte swizzle, only the
+//                unit's n rows rounded up to 16) into a stage;
+//   warps 4..19  a weight row and 32 of the slab's 64 K per thread (tensor-memory lane quarter
+//                warp % 4): decode the 32 codes in registers into binary16 weights d (2c - 3) or
+//                d (2c - 7) (rounded once, as in the rest of the prefill) and store them into the slab's
+//                A stage with one tcgen05.st;
+//   warps 2, 3   (one thread each, one per accumulator half: a single issuing thread cannot keep the
+//                tensor core busy at n <= 64) issue 4 tcgen05.mma of 128 x n x 16 (A in tensor memory,
+//                B in shared memory) and commit them to the stages' release barriers; after the last
+//                slab, to the accumulator barrier;
+//   warps 20..23 read the finished accumulator (tcgen05.ld), scale each column by 2^-shift of its B
+//                row and store out[pair][row].
+// Tensor memory: columns 0..255 accumulators, 256..511 four A stages of 64 columns (two halves x 32).
+// A unit of n <= 64 pairs uses one of two 128-column accumulator buffers (halves at +0 and +64), so its
+// epilogue overlaps the next unit's MMAs; a larger unit uses both (halves at 0 and 128).
+// The decode produces each 16-weight group in the order its binary16 pairs come out of the register
 // decode (pair p = weights p and p + 8); the B rows are stored in the same order (kpermute16), so the
 // products pair up as in the plain dot product.
 constexpr int kTcN = 128;                                           // pairs per unit at most
-constexpr int kTcStages = 3;                                        // A/B slab stages
-constexpr int kTcRS = 2;                                            // packed boxes in flight
-constexpr int kTcDec = 8, kTcEpi = 4;                               // decoder and epilogue warps
-constexpr int kTcThreads = (2 + kTcDec + kTcEpi) * 32;
-constexpr int kTcASlab = 256 * 128;                                 // 256 rows x 64 binary16
+constexpr int kTcAStages = 4;                                       // A stages in tensor memory
+constexpr int kTcBStages = 8;                                       // B slab stages in shared memory
+constexpr int kTcRS = 3;                                            // packed boxes in flight
+constexpr int kTcDec = 16, kTcEpi = 4;                              // decoder and epilogue warps
+constexpr int kTcIss = 2;                                           // MMA-issuing warps (one per half)
+constexpr int kTcDec0 = 2 + kTcIss;                                 // first decoder warp
+constexpr int kTcThreads = (kTcDec0 + kTcDec + kTcEpi) * 32;
+constexpr int kTcBRows = 16;                                        // rows of one B tile load
 constexpr int kTcBSlab = kTcN * 128;                                // 128 rows x 64 binary16
 constexpr int kTcBox = stage_bytes(3);                              // ring slot (an FP2 box fits)
-constexpr int kTcSmem = kTcRS * kTcBox + kTcStages * (kTcASlab + kTcBSlab) + 1024;
-constexpr int kTcCols = 512;                                        // 2 buffers x 2 halves x 128 columns
-static_assert(kTcBox % 1024 == 0 && kTcASlab % 1024 == 0 && kTcBSlab % 1024 == 0, "1024-byte aligned stages");
+constexpr int kTcSmem = kTcRS * kTcBox + kTcBStages * kTcBSlab + 1024;
+constexpr int kTcCols = 512;
+constexpr uint32_t kTcACol = 256;                                   // first A-stage column
+static_assert(kTcBox % 1024 == 0 && kTcBSlab % 1024 == 0, "1024-byte aligned stages");
+static_assert(kTcSmem + kTcEpi * kTcN * 4 + 1024 <= 227 * 1024, "shared memory per CTA");
+static_assert(kTcACol + 64 * kTcAStages <= kTcCols, "tensor-memory columns");
 
 struct TcArgs {
-    CUtensorMap bmap;         // B: binary16 [rows][K], K-permuted, box 64 x 128, 128-byte swizzle
+    CUtensorMap bmap;         // B: binary16 [rows][K], K-permuted, box 64 x 16, 128-byte swizzle
     const uint8_t* W;         // box-tiled matrix of expert 0
     int64_t mstride;          // bytes between experts' matrices
     int M, K;
@@ -568,53 +582,111 @@ __device__ __forceinline__ uint32_t tc_level(uint32_t a, uint32_t d2) {
     return hmul2_u(hfma2_u(a, f16x2(P + 0 >= 1 ? 2.0 / double(1 << P) : 1.0), f16x2(-(double(1 << (11 - P)) + K0))), d2);
 }
 
-template <int FMT>
-__device__ __forceinline__ void tc_group(const uint32_t (&a)[8], uint32_t d2, int odd, uint32_t (&o)[8]) {
+// One code group: its 8 pairs into o[8 G .. 8 G + 7].
+template <int FMT, int G, int NO>
+__device__ __forceinline__ void tc_group(const uint32_t (&a)[8], uint32_t d2, int odd, uint32_t (&o)[NO]) {
     if constexpr (FMT == 2) {
-        o[0] = tc_level<3, pair_shift(2, 0)>(a[0], d2); o[1] = tc_level<3, pair_shift(2, 1)>(a[1], d2);
-        o[2] = tc_level<3, pair_shift(2, 2)>(a[2], d2); o[3] = tc_level<3, pair_shift(2, 3)>(a[3], d2);
-        o[4] = tc_level<3, pair_shift(2, 4)>(a[4], d2); o[5] = tc_level<3, pair_shift(2, 5)>(a[5], d2);
-        o[6] = tc_level<3, pair_shift(2, 6)>(a[6], d2); o[7] = tc_level<3, pair_shift(2, 7)>(a[7], d2);
+        o[8 * G + 0] = tc_level<3, pair_shift(2, 0)>(a[0], d2); o[8 * G + 1] = tc_level<3, pair_shift(2, 1)>(a[1], d2);
+        o[8 * G + 2] = tc_level<3, pair_shift(2, 2)>(a[2], d2); o[8 * G + 3] = tc_level<3, pair_shift(2, 3)>(a[3], d2);
+        o[8 * G + 4] = tc_level<3, pair_shift(2, 4)>(a[4], d2); o[8 * G + 5] = tc_level<3, pair_shift(2, 5)>(a[5], d2);
+        o[8 * G + 6] = tc_level<3, pair_shift(2, 6)>(a[6], d2); o[8 * G + 7] = tc_level<3, pair_shift(2, 7)>(a[7], d2);
     } else if (!odd) {
-        o[0] = tc_level<7, fp3_box_shift(0, 0)>(a[0], d2); o[1] = tc_level<7, fp3_box_shift(0, 1)>(a[1], d2);
-        o[2] = tc_level<7, fp3_box_shift(0, 2)>(a[2], d2); o[3] = tc_level<7, fp3_box_shift(0, 3)>(a[3], d2);
-        o[4] = tc_level<7, fp3_box_shift(0, 4)>(a[4], d2); o[5] = tc_level<7, fp3_box_shift(0, 5)>(a[5], d2);
-        o[6] = tc_level<7, fp3_box_shift(0, 6)>(a[6], d2); o[7] = tc_level<7, fp3_box_shift(0, 7)>(a[7], d2);
+        o[8 * G + 0] = tc_level<7, fp3_box_shift(0, 0)>(a[0], d2); o[8 * G + 1] = tc_level<7, fp3_box_shift(0, 1)>(a[1], d2);
+        o[8 * G + 2] = tc_level<7, fp3_box_shift(0, 2)>(a[2], d2); o[8 * G + 3] = tc_level<7, fp3_box_shift(0, 3)>(a[3], d2);
+        o[8 * G + 4] = tc_level<7, fp3_box_shift(0, 4)>(a[4], d2); o[8 * G + 5] = tc_level<7, fp3_box_shift(0, 5)>(a[5], d2);
+        o[8 * G + 6] = tc_level<7, fp3_box_shift(0, 6)>(a[6], d2); o[8 * G + 7] = tc_level<7, fp3_box_shift(0, 7)>(a[7], d2);
     } else {
-        o[0] = tc_level<7, fp3_box_shift(1, 0)>(a[0], d2); o[1] = tc_level<7, fp3_box_shift(1, 1)>(a[1], d2);
-        o[2] = tc_level<7, fp3_box_shift(1, 2)>(a[2], d2); o[3] = tc_level<7, fp3_box_shift(1, 3)>(a[3], d2);
-        o[4] = tc_level<7, fp3_box_shift(1, 4)>(a[4], d2); o[5] = tc_level<7, fp3_box_shift(1, 5)>(a[5], d2);
-        o[6] = tc_level<7, fp3_box_shift(1, 6)>(a[6], d2); o[7] = tc_level<7, fp3_box_shift(1, 7)>(a[7], d2);
+        o[8 * G + 0] = tc_level<7, fp3_box_shift(1, 0)>(a[0], d2); o[8 * G + 1] = tc_level<7, fp3_box_shift(1, 1)>(a[1], d2);
+        o[8 * G + 2] = tc_level<7, fp3_box_shift(1, 2)>(a[2], d2); o[8 * G + 3] = tc_level<7, fp3_box_shift(1, 3)>(a[3], d2);
+        o[8 * G + 4] = tc_level<7, fp3_box_shift(1, 4)>(a[4], d2); o[8 * G + 5] = tc_level<7, fp3_box_shift(1, 5)>(a[5], d2);
+        o[8 * G + 6] = tc_level<7, fp3_box_shift(1, 6)>(a[6], d2); o[8 * G + 7] = tc_level<7, fp3_box_shift(1, 7)>(a[7], d2);
     }
 }
+
+// Slab C (0..3) of a box row, code groups 2 p and 2 p + 1: cw[i] = the row's code words of group 2 p + i
+// (FP2: 4 words, word C is the slab's; FP3: 6 words, slab pair C / 2 at 3 (C / 2)); sc = the row's
+// binary16 scales 4 p + 0..3 (scale 4 p + C = block 2 C + p, both groups' block).
+template <int FMT, int C, int NW>
+__device__ __forceinline__ void tc_half_slab(const uint32_t (&cw)[2][NW], const uint2& sc, uint32_t magic, uint32_t (&o)[16]) {
+    const uint32_t sw = C < 2 ? sc.x : sc.y;
+    const uint32_t d = (C & 1) ? (sw >> 16) : (sw & 0xFFFFu);
+    const uint32_t d2 = d | (d << 16);
+    uint32_t a[8], b[8];
+    if constexpr (FMT == 2) {
+        decode_fp2(cw[0][C], magic, a); tc_group<2, 0>(a, d2, 0, o);
+        decode_fp2(cw[1][C], magic, a); tc_group<2, 1>(a, d2, 0, o);
+    } else {
+        constexpr int m = C >> 1, odd = C & 1;
+        decode_fp3_box(cw[0][3 * m], cw[0][3 * m + 1], cw[0][3 * m + 2], magic, a, b); tc_group<3, 0>(odd ? b : a, d2, odd, o);
+        decode_fp3_box(cw[1][3 * m], cw[1][3 * m + 1], cw[1][3 * m + 2], magic, a, b); tc_group<3, 1>(odd ? b : a, d2, odd, o);
+    }
+}
+
+// Waits (bounded by kWaitNs) for the phase with the given parity, sleeping ns between polls so that a
+// waiting warp leaves the issue slots to the decoding warps. false on a timeout.
+__device__ __forceinline__ bool tc_wait(uint64_t* b, uint32_t parity, uint32_t ns) {
+    if (mbar_try_wait(b, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < kSpinLimit; i++) {
+        __nanosleep(ns);
+        if (mbar_try_wait(b, parity)) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
+    }
+    return false;
+}
+
+// Accumulator placement of a unit (identical sequence in the MMA thread and the epilogue): a unit of
+// n16 <= 64 columns takes buffer `toggle` (flipping it), a larger one both buffers.
+struct TcAcc {
+    uint32_t toggle = 0, uses0 = 0, uses1 = 0, full0 = 0, full1 = 0;
+    // buffers mask, primary buffer, column of half h = col0 + h * hstep
+    __device__ void place(uint32_t n16, uint32_t& mask, uint32_t& prim, uint32_t& col0, uint32_t& hstep) {
+        if (n16 <= 64) {
+            prim = toggle; mask = 1u << toggle; col0 = toggle * 128u; hstep = 64u;
+            toggle ^= 1u;
+        } else {
+            prim = 0; mask = 3u; col0 = 0; hstep = 128u;
+        }
+    }
+    __device__ uint32_t uses(int b) const { return b ? uses1 : uses0; }
+    __device__ uint32_t fulls(uint32_t b) const { return b ? full1 : full0; }
+    __device__ void done(uint32_t mask, uint32_t prim) {
+        uses0 += mask & 1u;
+        uses1 += mask >> 1;
+        full0 += prim == 0u;
+        full1 += prim == 1u;
+    }
+};
 
 template <int FMT>
 __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant__ TcArgs A) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ uint64_t bars[18];
+    __shared__ uint64_t bars[2 * kTcRS + 2 * kTcAStages + 2 * kTcBStages + 5];
     __shared__ uint32_t taddr_s;
+    __shared__ float efac[kTcEpi][kTcN];  // per epilogue warp: 2^-shift of the unit's B rows
     uint8_t* base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
-    uint8_t* ring = base;
-    uint8_t* As = base + kTcRS * kTcBox;
-    uint8_t* Bs = As + kTcStages * kTcASlab;
-    uint64_t* ring_full = bars;       // [kTcRS]
-    uint64_t* ring_empty = bars + 2;  // [kTcRS], kTcDec arrivals
-    uint64_t* a_full = bars + 4;      // [kTcStages], kTcDec arrivals
-    uint64_t* b_full = bars + 7;      // [kTcStages]
-    uint64_t* slab_free = bars + 10;  // [kTcStages], one tcgen05.commit
-    uint64_t* acc_full = bars + 13;   // [2], one tcgen05.commit
-    uint64_t* acc_free = bars + 15;   // [2], kTcEpi arrivals
-    uint64_t* done = bars + 17;       // the MMA thread's last commit
+    uint8_t* Bs = base;
+    uint8_t* ring = base + kTcBStages * kTcBSlab;
+    uint64_t* ring_full = bars;                   // [kTcRS]
+    uint64_t* ring_empty = ring_full + kTcRS;     // [kTcRS], kTcDec arrivals
+    uint64_t* a_full = ring_empty + kTcRS;        // [kTcAStages], kTcDec arrivals
+    uint64_t* a_free = a_full + kTcAStages;       // [kTcAStages], one tcgen05.commit
+    uint64_t* b_full = a_free + kTcAStages;       // [kTcBStages]
+    uint64_t* b_free = b_full + kTcBStages;       // [kTcBStages], one tcgen05.commit
+    uint64_t* acc_full = b_free + kTcBStages;     // [2], one tcgen05.commit
+    uint64_t* acc_free = acc_full + 2;            // [2], kTcEpi arrivals
+    uint64_t* done = acc_free + 2;                // the MMA thread's last commit
     const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
     if (tid == 0) {
         for (int i = 0; i < kTcRS; i++) { mbar_init(ring_full + i, 1); mbar_init(ring_empty + i, kTcDec); }
-        for (int i = 0; i < kTcStages; i++) { mbar_init(a_full + i, kTcDec); mbar_init(b_full + i, 1); mbar_init(slab_free + i, 1); }
-        for (int i = 0; i < 2; i++) { mbar_init(acc_full + i, 1); mbar_init(acc_free + i, kTcEpi); }
-        mbar_init(done, 1);
+        for (int i = 0; i < kTcAStages; i++) { mbar_init(a_full + i, kTcDec); mbar_init(a_free + i, kTcIss); }
+        for (int i = 0; i < kTcBStages; i++) { mbar_init(b_full + i, 1); mbar_init(b_free + i, kTcIss); }
+        for (int i = 0; i < 2; i++) { mbar_init(acc_full + i, kTcIss); mbar_init(acc_free + i, kTcEpi); }
+        mbar_init(done, kTcIss);
     }
     fence_barrier_init();
     __syncthreads();
-    if (warp == 1) tmem_alloc(smem_u32(&taddr_s), kTcCols);
+    if (warp == 2) tmem_alloc(smem_u32(&taddr_s), kTcCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -622,121 +694,141 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
     const int nunits = __ldg(A.nunits), G = gridDim.x, c = blockIdx.x;
     const int nslab = A.K / 64;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- loads (one thread)
-        if (lane == 0) {
-            uint32_t gs = 0, gb = 0;
+    if (warp < 2) {
+        // ---------------------------------------------------------------- loads (one thread each, in
+        // warps of their own so that neither waits while the other sleeps): warp 0 the packed boxes,
+        // warp 1 the B slabs, each as far ahead as its own ring allows
+        if (warp == 0 && lane == 0) {
+            uint32_t gb = 0;
             bool live = true;
             for (int u = c; u < nunits && live; u += G) {
                 const int4 un = A.units[u];
                 const uint8_t* wb = A.W + (int64_t)un.x * A.mstride + (int64_t)un.w * (A.K / stage_k(FMT)) * stage_bytes(FMT);
-                for (int j = 0; j < nslab && live; j++, gs++) {
-                    if ((j & 3) == 0) {
-                        const uint32_t sl = gb % kTcRS;
-                        if (gb >= (uint32_t)kTcRS && !mbar_wait(ring_empty + sl, ((gb / kTcRS) + 1u) & 1u)) { live = false; break; }
-                        mbar_expect_tx(ring_full + sl, stage_bytes(FMT));
-                        bulk_load(ring + sl * kTcBox, wb + (int64_t)(j >> 2) * stage_bytes(FMT), stage_bytes(FMT), ring_full + sl);
-                        gb++;
-                    }
-                    const uint32_t st = gs % kTcStages;
-                    if (gs >= (uint32_t)kTcStages && !mbar_wait(slab_free + st, ((gs / kTcStages) + 1u) & 1u)) { live = false; break; }
-                    mbar_expect_tx(b_full + st, kTcBSlab);
-                    tma_load_2d(Bs + st * kTcBSlab, &A.bmap, 64 * j, un.y, b_full + st);
+                for (int bx = 0; bx < nslab / 4; bx++, gb++) {
+                    const uint32_t sl = gb % kTcRS;
+                    if (gb >= (uint32_t)kTcRS && !tc_wait(ring_empty + sl, ((gb / kTcRS) + 1u) & 1u, 200)) { live = false; break; }
+                    mbar_expect_tx(ring_full + sl, stage_bytes(FMT));
+                    bulk_load(ring + sl * kTcBox, wb + (int64_t)bx * stage_bytes(FMT), stage_bytes(FMT), ring_full + sl);
                 }
             }
             if (!live) flag(A.status, FPX_ETIMEOUT);
             // no copy may land after the CTA exits
             for (uint32_t i = gb > (uint32_t)kTcRS ? gb - kTcRS : 0u; i < gb; i++) mbar_wait(ring_full + i % kTcRS, (i / kTcRS) & 1u);
-            for (uint32_t i = gs > (uint32_t)kTcStages ? gs - kTcStages : 0u; i < gs; i++) mbar_wait(b_full + i % kTcStages, (i / kTcStages) & 1u);
-        }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issue (one thread)
-        if (lane == 0) {
-            uint32_t gs = 0, it = 0;
+        } else if (warp == 1 && lane == 0) {
+            uint32_t gs = 0;
             bool live = true;
-            for (int u = c; u < nunits && live; u += G, it++) {
+            for (int u = c; u < nunits && live; u += G) {
+                const int4 un = A.units[u];
+                const int nt = (un.z + kTcBRows - 1) / kTcBRows;
+                for (int j = 0; j < nslab; j++, gs++) {
+                    const uint32_t st = gs % kTcBStages;
+                    if (gs >= (uint32_t)kTcBStages && !tc_wait(b_free + st, ((gs / kTcBStages) + 1u) & 1u, 100)) { live = false; break; }
+                    mbar_expect_tx(b_full + st, (uint32_t)(nt * kTcBRows * 128));
+                    for (int r = 0; r < nt; r++)
+                        tma_load_2d(Bs + st * kTcBSlab + r * (kTcBRows * 128), &A.bmap, 64 * j, un.y + r * kTcBRows, b_full + st);
+                }
+            }
+            if (!live) flag(A.status, FPX_ETIMEOUT);
+            for (uint32_t i = gs > (uint32_t)kTcBStages ? gs - kTcBStages : 0u; i < gs; i++) mbar_wait(b_full + i % kTcBStages, (i / kTcBStages) & 1u);
+        }
+    } else if (warp < 2 + kTcIss) {
+        // ---------------------------------------------------------------- MMA issue (one thread per half)
+        if (lane == 0) {
+            const uint32_t h = (uint32_t)(warp - 2);
+            uint32_t gs = 0;
+            TcAcc acc;
+            bool live = true, pre_a = false, pre_b = false;  // pre_*: slab gs's barrier already seen complete
+            for (int u = c; u < nunits && live; u += G) {
                 const int4 un = A.units[u];
                 const uint32_t n16 = (uint32_t)((un.z + 15) & ~15), idesc = f16_idesc(128, n16);
-                const uint32_t ab = it & 1u;
-                if (it >= 2 && !mbar_wait(acc_free + ab, ((it / 2) + 1u) & 1u)) { live = false; break; }
+                uint32_t mask, prim, col0, hstep;
+                acc.place(n16, mask, prim, col0, hstep);
+                for (int b = 0; b < 2; b++)
+                    if (((mask >> b) & 1u) && acc.uses(b) > 0 && !mbar_wait(acc_free + b, (acc.uses(b) - 1u) & 1u)) live = false;
+                if (!live) break;
                 tc_fence_after();
-                const uint32_t dcol = taddr + ab * 256u;
+                const uint32_t dcol = taddr + col0 + h * hstep;
                 for (int j = 0; j < nslab && live; j++, gs++) {
-                    const uint32_t st = gs % kTcStages, ph = (gs / kTcStages) & 1u;
-                    if (!mbar_wait(a_full + st, ph) || !mbar_wait(b_full + st, ph)) { live = false; break; }
-                    tc_fence_after();
-                    const uint32_t a0 = smem_u32(As + st * kTcASlab), b0 = smem_u32(Bs + st * kTcBSlab);
-#pragma unroll
-                    for (int kk = 0; kk < 4; kk++) {
-                        const uint64_t bd = sw128_desc(b0 + 32u * kk);
-                        tc_mma_f16(dcol, sw128_desc(a0 + 32u * kk), bd, idesc, (j | kk) != 0);
-                        tc_mma_f16(dcol + 128u, sw128_desc(a0 + 16384u + 32u * kk), bd, idesc, (j | kk) != 0);
+                    const uint32_t sa = gs % kTcAStages, sb = gs % kTcBStages;
+                    if ((!pre_a && !mbar_wait(a_full + sa, (gs / kTcAStages) & 1u)) ||
+                        (!pre_b && !mbar_wait(b_full + sb, (gs / kTcBStages) & 1u))) {
+                        live = false;
+                        break;
                     }
-                    tc_commit(smem_u32(slab_free + st));
+                    tc_fence_after();
+                    // test the next slab's barriers now: the answers arrive while this slab's MMAs issue
+                    // (a blocking wait here would cost its full latency on every slab)
+                    const uint32_t gn = gs + 1u;
+                    pre_a = mbar_test_wait(a_full + gn % kTcAStages, (gn / kTcAStages) & 1u);
+                    pre_b = mbar_test_wait(b_full + gn % kTcBStages, (gn / kTcBStages) & 1u);
+                    const uint32_t a0 = taddr + kTcACol + 64u * sa + 32u * h;
+                    const uint64_t bd = sw128_desc(smem_u32(Bs + sb * kTcBSlab));  // + 2 per K step of 32 bytes
+#pragma unroll
+                    for (int kk = 0; kk < 4; kk++) tc_mma_f16_ta(dcol, a0 + 8u * kk, bd + 2u * kk, idesc, (j | kk) != 0);
+                    tc_commit(smem_u32(a_free + sa));
+                    tc_commit(smem_u32(b_free + sb));
                 }
-                if (live) tc_commit(smem_u32(acc_full + ab));
+                if (!live) break;
+                tc_commit(smem_u32(acc_full + prim));
+                acc.done(mask, prim);
             }
             if (!live) flag(A.status, FPX_ETIMEOUT);
             tc_commit(smem_u32(done));
         }
-    } else if (warp < 2 + kTcDec) {
-        // ---------------------------------------------------------------- decode (8 warps)
-        const int td = tid - 64;
+    } else if (warp < kTcDec0 + kTcDec) {
+        // ---------------------------------------------------------------- decode (16 warps): a weight
+        // row and half of each K slab per thread (code groups 2 p, 2 p + 1 of the slab's four)
+        const int dw = warp - kTcDec0, q = warp & 3, h = (dw >> 2) & 1, p = dw >> 3;
+        const int row = h * 128 + 32 * q + lane;
+        const uint32_t lane_base = taddr + ((uint32_t)(32 * q) << 16) + kTcACol + 32u * (uint32_t)h + 16u * (uint32_t)p;
+        // the row's two chunks are read in an order that depends on the lane, halving bank conflicts
+        const uint32_t rot = (uint32_t)(lane >> 2) & 1u;
+        constexpr int NW = FMT == 2 ? 4 : 6;  // code words of a group
         uint32_t gs = 0, gb = 0;
         bool live = true;
         const uint32_t magic = kMagic;
         for (int u = c; u < nunits && live; u += G) {
             for (int bx = 0; bx < nslab / 4 && live; bx++, gb++) {
                 const uint32_t sl = gb % kTcRS;
-                if (!__any_sync(0xffffffffu, mbar_wait(ring_full + sl, (gb / kTcRS) & 1u))) { live = false; break; }
+                if (!__any_sync(0xffffffffu, tc_wait(ring_full + sl, (gb / kTcRS) & 1u, 64))) { live = false; break; }
                 const uint32_t box = smem_u32(ring + sl * kTcBox);
-                // this thread's (row, t) items: rows r = i / 4, code group t = i % 4 of each row, i = td + 256 jj
-                uint32_t cw[4][6];
-                uint2 sc[4];
+                uint32_t v[2][NW], cw[2][NW];
 #pragma unroll
-                for (int jj = 0; jj < 4; jj++) {
-                    const int i = td + 256 * jj, row = i >> 2, t = i & 3;
+                for (int i = 0; i < 2; i++) {
+                    const uint32_t g = 2u * (uint32_t)p + (((uint32_t)i + rot) & 1u);
                     if constexpr (FMT == 2) {
-                        const uint4 v = lds128<0>(box + (uint32_t)(row * 64 + 16 * t));
-                        cw[jj][0] = v.x; cw[jj][1] = v.y; cw[jj][2] = v.z; cw[jj][3] = v.w;
+                        const uint4 x = lds128<0>(box + (uint32_t)row * 64u + 16u * g);
+                        v[i][0] = x.x; v[i][1] = x.y; v[i][2] = x.z; v[i][3] = x.w;
                     } else {
-                        const uint32_t cb = box + (uint32_t)(row * 96 + 24 * t);
-                        const uint2 v0 = lds64<0>(cb), v1 = lds64<8>(cb), v2 = lds64<16>(cb);
-                        cw[jj][0] = v0.x; cw[jj][1] = v0.y; cw[jj][2] = v1.x; cw[jj][3] = v1.y; cw[jj][4] = v2.x; cw[jj][5] = v2.y;
+                        const uint32_t cb = box + (uint32_t)row * 96u + 24u * g;
+                        const uint2 x0 = lds64<0>(cb), x1 = lds64<8>(cb), x2 = lds64<16>(cb);
+                        v[i][0] = x0.x; v[i][1] = x0.y; v[i][2] = x1.x; v[i][3] = x1.y; v[i][4] = x2.x; v[i][5] = x2.y;
                     }
-                    sc[jj] = lds64<0>(box + (uint32_t)(box_scale_offset(FMT) + row * 16 + 8 * (t >> 1)));
                 }
+                // scales 4 p + C (C = 0..3) of the row: blocks 2 C + p
+                const uint2 sc = lds64<0>(box + (uint32_t)(box_scale_offset(FMT) + row * 16 + 8 * p));
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ring_empty + sl);
 #pragma unroll
-                for (int C = 0; C < 4; C++, gs++) {
-                    const uint32_t st = gs % kTcStages;
-                    if (live && gs >= (uint32_t)kTcStages)
-                        live = __any_sync(0xffffffffu, mbar_wait(slab_free + st, ((gs / kTcStages) + 1u) & 1u));
-                    if (!live) break;
-                    uint8_t* as = As + st * kTcASlab;
+                for (int w = 0; w < NW; w++) {
+                    cw[0][w] = rot ? v[1][w] : v[0][w];
+                    cw[1][w] = rot ? v[0][w] : v[1][w];
+                }
 #pragma unroll
-                    for (int jj = 0; jj < 4; jj++) {
-                        const int i = td + 256 * jj, row = i >> 2, t = i & 3;
-                        const uint32_t w = C < 2 ? sc[jj].x : sc[jj].y;
-                        const uint32_t dh = (C & 1) ? (w >> 16) : (w & 0xFFFFu);
-                        const uint32_t d2 = dh | (dh << 16);
-                        uint32_t a[8], b[8], o[8];
-                        if constexpr (FMT == 2) {
-                            decode_fp2(cw[jj][C], magic, a);
-                            tc_group<2>(a, d2, 0, o);
-                        } else {
-                            const int m = C >> 1;
-                            decode_fp3_box(cw[jj][3 * m], cw[jj][3 * m + 1], cw[jj][3 * m + 2], magic, a, b);
-                            if (C & 1) tc_group<3>(b, d2, 1, o);
-                            else tc_group<3>(a, d2, 0, o);
-                        }
-                        uint8_t* hb = as + (row >= 128 ? 16384 : 0);
-                        const uint32_t rr = (uint32_t)(row & 127);
-                        *reinterpret_cast<uint4*>(hb + sw128_offset(rr, 16 * t)) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4*>(hb + sw128_offset(rr, 16 * t + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
-                    }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the MMA reads through the async proxy
+                for (int C = 0; C < 4; C++, gs++) {
+                    const uint32_t st = gs % kTcAStages;
+                    if (live && gs >= (uint32_t)kTcAStages)
+                        live = __any_sync(0xffffffffu, tc_wait(a_free + st, ((gs / kTcAStages) + 1u) & 1u, 64));
+                    if (!live) break;
+                    tc_fence_after();
+                    uint32_t o[16];
+                    if (C == 0) tc_half_slab<FMT, 0>(cw, sc, magic, o);
+                    else if (C == 1) tc_half_slab<FMT, 1>(cw, sc, magic, o);
+                    else if (C == 2) tc_half_slab<FMT, 2>(cw, sc, magic, o);
+                    else tc_half_slab<FMT, 3>(cw, sc, magic, o);
+                    tmem_st16(lane_base + 64u * st, o);
+                    tmem_st_wait();
+                    tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(a_full + st);
                 }
@@ -746,40 +838,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
     } else {
         // ---------------------------------------------------------------- epilogue (4 warps)
         const int q = warp & 3;  // tensor-memory lane quarter of this warp
-        uint32_t it = 0;
+        float* fac = efac[warp - kTcDec0 - kTcDec];
+        TcAcc acc;
         bool live = true;
-        for (int u = c; u < nunits && live; u += G, it++) {
+        for (int u = c; u < nunits && live; u += G) {
             const int4 un = A.units[u];
-            const uint32_t ab = it & 1u;
-            live = __any_sync(0xffffffffu, mbar_wait(acc_full + ab, (it / 2) & 1u));
+            const int n = un.z, n16 = (n + 15) & ~15;
+            // the unit's column factors 2^-shift, read before the accumulator is ready
+            __syncwarp();
+            for (int s = lane; s < n; s += 32) fac[s] = exp2i(-__ldg(A.shift + un.y + s));
+            __syncwarp();
+            uint32_t mask, prim, col0, hstep;
+            acc.place((uint32_t)n16, mask, prim, col0, hstep);
+            live = __any_sync(0xffffffffu, tc_wait(acc_full + prim, acc.fulls(prim) & 1u, 500));
             if (!live) break;
             tc_fence_after();
-            const int n = un.z, n16 = (n + 15) & ~15;
-            for (int h = 0; h < 2; h++) {
-                const int m = un.w * 256 + h * 128 + 32 * q + lane;
+            for (int hh = 0; hh < 2; hh++) {
+                const int m = un.w * 256 + hh * 128 + 32 * q + lane;
+                float* orow = A.out + (size_t)un.y * A.M + m;
                 for (int c0 = 0; c0 < n16; c0 += 16) {
                     float v[16];
-                    tmem_ld16(taddr + ((uint32_t)(32 * q) << 16) + ab * 256u + (uint32_t)(h * 128 + c0), v);
+                    tmem_ld16(taddr + ((uint32_t)(32 * q) << 16) + col0 + hstep * (uint32_t)hh + (uint32_t)c0, v);
 #pragma unroll
                     for (int j = 0; j < 16; j++) {
                         const int s = c0 + j;
-                        if (s < n) {
-                            const int rowb = un.y + s;
-                            A.out[(size_t)rowb * A.M + m] = v[j] * exp2i(-__ldg(A.shift + rowb));
-                        }
+                        if (s < n) orow[(size_t)s * A.M] = v[j] * fac[s];
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_free + ab);
+            if (lane == 0)
+                for (int b = 0; b < 2; b++)
+                    if ((mask >> b) & 1u) mbar_arrive(acc_free + b);
+            acc.done(mask, prim);
         }
         if (!live && lane == 0) flag(A.status, FPX_ETIMEOUT);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) {
+    if (warp == 2) {
         mbar_wait(done, 0);  // every MMA of this CTA has completed
         tmem_dealloc(taddr, kTcCols);
     }
@@ -917,14 +1016,14 @@ cudaError_t launch_gemm(const PGemmArgs& a, int grid_units, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// A 2-D tensor map over B (binary16 [rows][K]) for the tensor-core GEMM: boxes of 64 elements x 128
+// A 2-D tensor map over B (binary16 [rows][K]) for the tensor-core GEMM: boxes of 64 elements x 16
 // rows with the 128-byte swizzle; rows past the end read as zeros.
 int make_b_map(CUtensorMap* m, const __half* B, int64_t rows, int64_t K) {
     auto enc = tensor_map_encoder();
     if (!enc) return FPX_ECUDA;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
-    cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(kTcN)};
+    cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(kTcBRows)};
     cuuint32_t es[2] = {1u, 1u};
     const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<__half*>(B), dims, strides, box, es,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

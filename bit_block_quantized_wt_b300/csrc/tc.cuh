@@ -1,7 +1,8 @@
 // tcgen05 (fifth-generation tensor core) helpers for sm_103a: tensor-memory allocation, the MMA of
-// kind::f16 with binary32 accumulators in tensor memory, commit to an mbarrier, and loads of the
-// accumulator back into registers; shared-memory matrix descriptors for the K-major layout with the
-// 128-byte swizzle (the layout a TMA tiled load with CU_TENSOR_MAP_SWIZZLE_128B writes).
+// kind::f16 with binary32 accumulators in tensor memory (A from shared or tensor memory), commit to an
+// mbarrier, stores of registers into tensor memory and loads of the accumulator back into registers;
+// shared-memory matrix descriptors for the K-major layout with the 128-byte swizzle (the layout a TMA
+// tiled load with CU_TENSOR_MAP_SWIZZLE_128B writes).
 //
 // K-major, 128-byte swizzle: a tile of R rows x 64 binary16 elements (128 bytes per row) sits at a
 // 1024-byte-aligned address; row r occupies bytes r * 128 .. r * 128 + 127, and its 16-byte chunk c
@@ -57,6 +58,39 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+
+// One thread: D[tmem] (+)= A[tmem] * B[smem]^T for one 128 x N x 16 step with A in tensor memory: row m
+// of A in lane m, binary16 elements 2c and 2c + 1 of the K step in column a_tmem + c (low, high half).
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Whole warp: thread i writes r[0..31] to 32 consecutive columns of tensor-memory lane 32 q + i (q = the
+// warp's lane quarter, warp % 4), starting at column col of taddr (tmem_st16: 16 columns).
+// tmem_st_wait() makes them complete.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // One thread: the mbarrier at smem address `bar` receives one arrival when every tcgen05.mma this
 // thread issued before has completed (their shared-memory reads included).
