@@ -524,43 +524,53 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_pgemm(const __grid_constant
 // The routed experts' GEMMs on the fifth-generation tensor cores. A unit is (expert e, 256 weight
 // rows, up to 128 of the expert's pairs): D[256 x n] = W_e[rows][K] * B[pairs][K]^T, accumulated in
 // binary32 in tensor memory as two M = 128 halves. The decoded weights never touch shared memory: they
-// are the MMA's A operand in tensor memory. Per 64-wide K slab:
+// are the MMA's A operand in tensor memory. The K loop runs in stages of 128 (two 64-wide slabs):
 //   warp 0       streams the packed weight boxes (one 1-D bulk copy per 256 x 256 box) into a ring;
-//   warp 1       streams the slab of B (2-D TMA tiles of 16 rows x 64, 128-byte swizzle, only the
-//                unit's n rows rounded up to 16) into a stage;
-//   warps 4..19  a weight row and 32 of the slab's 64 K per thread (tensor-memory lane quarter
-//                warp % 4): decode the 32 codes in registers into binary16 weights d (2c - 3) or
-//                d (2c - 7) (rounded once, as in the rest of the prefill) and store them into the slab's
-//                A stage with one tcgen05.st;
+//   warp 1       streams the stage's B (2-D TMA tiles of 16 rows x 64, 128-byte swizzle, only the
+//                unit's n rows rounded up to 16) into a shared-memory stage;
+//   warps 4..19  a weight row and 64 of the stage's 128 K per thread (code groups 2 p, 2 p + 1 of both
+//                slabs; tensor-memory lane quarter warp % 4): decode the codes in registers into
+//                binary16 weights d (2c - 3) or d (2c - 7) (rounded once, as in the rest of the
+//                prefill) and store them into the A stage with one tcgen05.st;
 //   warps 2, 3   (one thread each, one per accumulator half: a single issuing thread cannot keep the
-//                tensor core busy at n <= 64) issue 4 tcgen05.mma of 128 x n x 16 (A in tensor memory,
+//                tensor core busy at n <= 64) issue 8 tcgen05.mma of 128 x n x 16 (A in tensor memory,
 //                B in shared memory) and commit them to the stages' release barriers; after the last
-//                slab, to the accumulator barrier;
+//                stage, to the accumulator barrier;
 //   warps 20..23 read the finished accumulator (tcgen05.ld), scale each column by 2^-shift of its B
 //                row and store out[pair][row].
-// Tensor memory: columns 0..255 accumulators, 256..511 four A stages of 64 columns (two halves x 32).
-// A unit of n <= 64 pairs uses one of two 128-column accumulator buffers (halves at +0 and +64), so its
-// epilogue overlaps the next unit's MMAs; a larger unit uses both (halves at 0 and 128).
+// Every handshake costs instructions in each of the 16 decoder warps; 128-wide stages halve them per
+// weight, which matters because the decode is issue-bound.
+// Tensor memory: columns 0..255 accumulators, 256..511 two A stages of 128 columns (two halves x 64;
+// within a half, the 8 K steps of 16 sit in the order 0, 1, 4, 5, 2, 3, 6, 7 so that each decoder
+// thread's 32 columns are contiguous). A unit of n <= 64 pairs uses one of two 128-column accumulator
+// buffers (halves at +0 and +64), so its epilogue overlaps the next unit's MMAs; a larger unit uses
+// both (halves at 0 and 128).
 // The decode produces each 16-weight group in the order its binary16 pairs come out of the register
 // decode (pair p = weights p and p + 8); the B rows are stored in the same order (kpermute16), so the
 // products pair up as in the plain dot product.
 constexpr int kTcN = 128;                                           // pairs per unit at most
-constexpr int kTcAStages = 4;                                       // A stages in tensor memory
-constexpr int kTcBStages = 8;                                       // B slab stages in shared memory
+constexpr int kTcSK = 128;                                          // K per stage
+constexpr int kTcAStages = 2;                                       // A stages in tensor memory
+constexpr int kTcBStages = 4;                                       // B stages in shared memory
 constexpr int kTcRS = 3;                                            // packed boxes in flight
 constexpr int kTcDec = 16, kTcEpi = 4;                              // decoder and epilogue warps
 constexpr int kTcIss = 2;                                           // MMA-issuing warps (one per half)
 constexpr int kTcDec0 = 2 + kTcIss;                                 // first decoder warp
 constexpr int kTcThreads = (kTcDec0 + kTcDec + kTcEpi) * 32;
 constexpr int kTcBRows = 16;                                        // rows of one B tile load
-constexpr int kTcBSlab = kTcN * 128;                                // 128 rows x 64 binary16
+constexpr int kTcBTile = kTcN * 128;                                // 128 rows x 64 binary16
+constexpr int kTcBStage = 2 * kTcBTile;                             // a stage: two 64-wide tiles
 constexpr int kTcBox = stage_bytes(3);                              // ring slot (an FP2 box fits)
-constexpr int kTcSmem = kTcRS * kTcBox + kTcBStages * kTcBSlab + 1024;
+constexpr int kTcSmem = kTcRS * kTcBox + kTcBStages * kTcBStage + 1024;
 constexpr int kTcCols = 512;
 constexpr uint32_t kTcACol = 256;                                   // first A-stage column
-static_assert(kTcBox % 1024 == 0 && kTcBSlab % 1024 == 0, "1024-byte aligned stages");
+static_assert(kTcBox % 1024 == 0 && kTcBTile % 1024 == 0, "1024-byte aligned stages");
 static_assert(kTcSmem + kTcEpi * kTcN * 4 + 1024 <= 227 * 1024, "shared memory per CTA");
-static_assert(kTcACol + 64 * kTcAStages <= kTcCols, "tensor-memory columns");
+static_assert(kTcACol + 128 * kTcAStages <= kTcCols, "tensor-memory columns");
+
+// Column block (8 columns) of K step kk (0..7 = slab kk / 4, code group kk % 4) within a half's 64
+// A-stage columns: thread p of a row owns blocks 4 p .. 4 p + 3 (groups 2 p, 2 p + 1 of both slabs).
+__host__ __device__ constexpr uint32_t tc_kblock(int kk) { return 4u * ((kk & 3) >> 1) + 2u * (kk >> 2) + (kk & 1); }
 
 struct TcArgs {
     CUtensorMap bmap;         // B: binary16 [rows][K], K-permuted, box 64 x 16, 128-byte swizzle
@@ -622,19 +632,6 @@ __device__ __forceinline__ void tc_half_slab(const uint32_t (&cw)[2][NW], const 
     }
 }
 
-// Waits (bounded by kWaitNs) for the phase with the given parity, sleeping ns between polls so that a
-// waiting warp leaves the issue slots to the decoding warps. false on a timeout.
-__device__ __forceinline__ bool tc_wait(uint64_t* b, uint32_t parity, uint32_t ns) {
-    if (mbar_try_wait(b, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t i = 0; i < kSpinLimit; i++) {
-        __nanosleep(ns);
-        if (mbar_try_wait(b, parity)) return true;
-        if (global_ns() - t0 > kWaitNs) return false;
-    }
-    return false;
-}
-
 // Accumulator placement of a unit (identical sequence in the MMA thread and the epilogue): a unit of
 // n16 <= 64 columns takes buffer `toggle` (flipping it), a larger one both buffers.
 struct TcAcc {
@@ -666,7 +663,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
     __shared__ float efac[kTcEpi][kTcN];  // per epilogue warp: 2^-shift of the unit's B rows
     uint8_t* base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
     uint8_t* Bs = base;
-    uint8_t* ring = base + kTcBStages * kTcBSlab;
+    uint8_t* ring = base + kTcBStages * kTcBStage;
     uint64_t* ring_full = bars;                   // [kTcRS]
     uint64_t* ring_empty = ring_full + kTcRS;     // [kTcRS], kTcDec arrivals
     uint64_t* a_full = ring_empty + kTcRS;        // [kTcAStages], kTcDec arrivals
@@ -692,7 +689,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
     tc_fence_after();
     const uint32_t taddr = taddr_s;
     const int nunits = __ldg(A.nunits), G = gridDim.x, c = blockIdx.x;
-    const int nslab = A.K / 64;
+    const int nslab = A.K / 64, nstage = A.K / kTcSK;
 
     if (warp < 2) {
         // ---------------------------------------------------------------- loads (one thread each, in
@@ -706,7 +703,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
                 const uint8_t* wb = A.W + (int64_t)un.x * A.mstride + (int64_t)un.w * (A.K / stage_k(FMT)) * stage_bytes(FMT);
                 for (int bx = 0; bx < nslab / 4; bx++, gb++) {
                     const uint32_t sl = gb % kTcRS;
-                    if (gb >= (uint32_t)kTcRS && !tc_wait(ring_empty + sl, ((gb / kTcRS) + 1u) & 1u, 200)) { live = false; break; }
+                    if (gb >= (uint32_t)kTcRS && !mbar_wait(ring_empty + sl, ((gb / kTcRS) + 1u) & 1u)) { live = false; break; }
                     mbar_expect_tx(ring_full + sl, stage_bytes(FMT));
                     bulk_load(ring + sl * kTcBox, wb + (int64_t)bx * stage_bytes(FMT), stage_bytes(FMT), ring_full + sl);
                 }
@@ -720,12 +717,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
             for (int u = c; u < nunits && live; u += G) {
                 const int4 un = A.units[u];
                 const int nt = (un.z + kTcBRows - 1) / kTcBRows;
-                for (int j = 0; j < nslab; j++, gs++) {
+                for (int j = 0; j < nstage; j++, gs++) {
                     const uint32_t st = gs % kTcBStages;
-                    if (gs >= (uint32_t)kTcBStages && !tc_wait(b_free + st, ((gs / kTcBStages) + 1u) & 1u, 100)) { live = false; break; }
-                    mbar_expect_tx(b_full + st, (uint32_t)(nt * kTcBRows * 128));
-                    for (int r = 0; r < nt; r++)
-                        tma_load_2d(Bs + st * kTcBSlab + r * (kTcBRows * 128), &A.bmap, 64 * j, un.y + r * kTcBRows, b_full + st);
+                    if (gs >= (uint32_t)kTcBStages && !mbar_wait(b_free + st, ((gs / kTcBStages) + 1u) & 1u)) { live = false; break; }
+                    mbar_expect_tx(b_full + st, (uint32_t)(2 * nt * kTcBRows * 128));
+                    for (int t = 0; t < 2; t++)
+                        for (int r = 0; r < nt; r++)
+                            tma_load_2d(Bs + st * kTcBStage + t * kTcBTile + r * (kTcBRows * 128), &A.bmap, kTcSK * j + 64 * t,
+                                        un.y + r * kTcBRows, b_full + st);
                 }
             }
             if (!live) flag(A.status, FPX_ETIMEOUT);
@@ -737,7 +736,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
             const uint32_t h = (uint32_t)(warp - 2);
             uint32_t gs = 0;
             TcAcc acc;
-            bool live = true, pre_a = false, pre_b = false;  // pre_*: slab gs's barrier already seen complete
+            bool live = true, pre_a = false, pre_b = false;  // pre_*: stage gs's barrier already seen complete
             for (int u = c; u < nunits && live; u += G) {
                 const int4 un = A.units[u];
                 const uint32_t n16 = (uint32_t)((un.z + 15) & ~15), idesc = f16_idesc(128, n16);
@@ -748,7 +747,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
                 if (!live) break;
                 tc_fence_after();
                 const uint32_t dcol = taddr + col0 + h * hstep;
-                for (int j = 0; j < nslab && live; j++, gs++) {
+                for (int j = 0; j < nstage && live; j++, gs++) {
                     const uint32_t sa = gs % kTcAStages, sb = gs % kTcBStages;
                     if ((!pre_a && !mbar_wait(a_full + sa, (gs / kTcAStages) & 1u)) ||
                         (!pre_b && !mbar_wait(b_full + sb, (gs / kTcBStages) & 1u))) {
@@ -756,15 +755,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
                         break;
                     }
                     tc_fence_after();
-                    // test the next slab's barriers now: the answers arrive while this slab's MMAs issue
+                    // test the next stage's barriers now: the answers arrive while this stage's MMAs issue
                     // (a blocking wait here would cost its full latency on every slab)
                     const uint32_t gn = gs + 1u;
                     pre_a = mbar_test_wait(a_full + gn % kTcAStages, (gn / kTcAStages) & 1u);
                     pre_b = mbar_test_wait(b_full + gn % kTcBStages, (gn / kTcBStages) & 1u);
-                    const uint32_t a0 = taddr + kTcACol + 64u * sa + 32u * h;
-                    const uint64_t bd = sw128_desc(smem_u32(Bs + sb * kTcBSlab));  // + 2 per K step of 32 bytes
+                    const uint32_t a0 = taddr + kTcACol + 128u * sa + 64u * h;
+                    // B: tile kk / 4 (16 KB = 1024 in the descriptor's address field), + 2 per K step of 32 bytes
+                    const uint64_t bd = sw128_desc(smem_u32(Bs + sb * kTcBStage));
 #pragma unroll
-                    for (int kk = 0; kk < 4; kk++) tc_mma_f16_ta(dcol, a0 + 8u * kk, bd + 2u * kk, idesc, (j | kk) != 0);
+                    for (int kk = 0; kk < 8; kk++)
+                        tc_mma_f16_ta(dcol, a0 + 8u * tc_kblock(kk), bd + 1024u * (kk >> 2) + 2u * (kk & 3), idesc, (j | kk) != 0);
                     tc_commit(smem_u32(a_free + sa));
                     tc_commit(smem_u32(b_free + sb));
                 }
@@ -777,10 +778,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
         }
     } else if (warp < kTcDec0 + kTcDec) {
         // ---------------------------------------------------------------- decode (16 warps): a weight
-        // row and half of each K slab per thread (code groups 2 p, 2 p + 1 of the slab's four)
+        // row per thread, code groups 2 p, 2 p + 1 of every slab
         const int dw = warp - kTcDec0, q = warp & 3, h = (dw >> 2) & 1, p = dw >> 3;
         const int row = h * 128 + 32 * q + lane;
-        const uint32_t lane_base = taddr + ((uint32_t)(32 * q) << 16) + kTcACol + 32u * (uint32_t)h + 16u * (uint32_t)p;
+        const uint32_t lane_base = taddr + ((uint32_t)(32 * q) << 16) + kTcACol + 64u * (uint32_t)h + 32u * (uint32_t)p;
         // the row's two chunks are read in an order that depends on the lane, halving bank conflicts
         const uint32_t rot = (uint32_t)(lane >> 2) & 1u;
         constexpr int NW = FMT == 2 ? 4 : 6;  // code words of a group
@@ -790,7 +791,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
         for (int u = c; u < nunits && live; u += G) {
             for (int bx = 0; bx < nslab / 4 && live; bx++, gb++) {
                 const uint32_t sl = gb % kTcRS;
-                if (!__any_sync(0xffffffffu, tc_wait(ring_full + sl, (gb / kTcRS) & 1u, 64))) { live = false; break; }
+                if (!__any_sync(0xffffffffu, mbar_wait(ring_full + sl, (gb / kTcRS) & 1u))) { live = false; break; }
                 const uint32_t box = smem_u32(ring + sl * kTcBox);
                 uint32_t v[2][NW], cw[2][NW];
 #pragma unroll
@@ -814,19 +815,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
                     cw[0][w] = rot ? v[1][w] : v[0][w];
                     cw[1][w] = rot ? v[0][w] : v[1][w];
                 }
+                // the box's two stages: slabs 0, 1 and 2, 3
 #pragma unroll
-                for (int C = 0; C < 4; C++, gs++) {
+                for (int S = 0; S < 2; S++, gs++) {
                     const uint32_t st = gs % kTcAStages;
                     if (live && gs >= (uint32_t)kTcAStages)
-                        live = __any_sync(0xffffffffu, tc_wait(a_free + st, ((gs / kTcAStages) + 1u) & 1u, 64));
+                        live = __any_sync(0xffffffffu, mbar_wait(a_free + st, ((gs / kTcAStages) + 1u) & 1u));
                     if (!live) break;
                     tc_fence_after();
-                    uint32_t o[16];
-                    if (C == 0) tc_half_slab<FMT, 0>(cw, sc, magic, o);
-                    else if (C == 1) tc_half_slab<FMT, 1>(cw, sc, magic, o);
-                    else if (C == 2) tc_half_slab<FMT, 2>(cw, sc, magic, o);
-                    else tc_half_slab<FMT, 3>(cw, sc, magic, o);
-                    tmem_st16(lane_base + 64u * st, o);
+                    uint32_t o[32];
+                    uint32_t(&o0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[0]);
+                    uint32_t(&o1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[16]);
+                    if (S == 0) {
+                        tc_half_slab<FMT, 0>(cw, sc, magic, o0);
+                        tc_half_slab<FMT, 1>(cw, sc, magic, o1);
+                    } else {
+                        tc_half_slab<FMT, 2>(cw, sc, magic, o0);
+                        tc_half_slab<FMT, 3>(cw, sc, magic, o1);
+                    }
+                    tmem_st32(lane_base + 128u * st, o);
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
@@ -850,7 +857,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
             __syncwarp();
             uint32_t mask, prim, col0, hstep;
             acc.place((uint32_t)n16, mask, prim, col0, hstep);
-            live = __any_sync(0xffffffffu, tc_wait(acc_full + prim, acc.fulls(prim) & 1u, 500));
+            live = __any_sync(0xffffffffu, mbar_wait(acc_full + prim, acc.fulls(prim) & 1u));
             if (!live) break;
             tc_fence_after();
             for (int hh = 0; hh < 2; hh++) {
