@@ -763,9 +763,11 @@ def main():
     p.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--ref-seconds", type=float, default=90.0)
-    p.add_argument("--part", choices=["all", "idot", "tiered"], default="all",
+    p.add_argument("--part", choices=["all", "idot", "tiered", "prefill", "commit", "quantize"], default="all",
                    help="idot: only the integer-dot / tensor-core GEMV comparison; tiered: only the two-tier "
-                        "residency measurement on a one-layer stack (one JSON object each)")
+                        "residency measurement on a one-layer stack; prefill: only the prefill of one layer "
+                        "(--warmup calls, then --steps timed calls); commit: only the verify/commit rule; "
+                        "quantize: only the importance-weighted quantizer (one JSON object each)")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -777,12 +779,20 @@ def main():
         torch.cuda.set_device(0)
         fpx.lib()
         print(json.dumps(idot_measure(fpx, peaks()[0])), flush=True)
-    elif args.part == "tiered":
+    elif args.part in ("tiered", "prefill", "commit", "quantize"):
         import torch
         import bit_block_quantized_wt_b300 as fpx
         torch.cuda.set_device(0)
         fpx.lib()
-        print(json.dumps(tiered_measure(fpx, Stack(1))), flush=True)
+        if args.part == "tiered":
+            res = tiered_measure(fpx, Stack(1))
+        elif args.part == "prefill":
+            res = prefill_measure(fpx, Stack(1).layers[0], args.warmup, reps=args.steps)
+        elif args.part == "commit":
+            res = commit_measure(fpx, peaks()[0], reps=args.steps)
+        else:
+            res = quantize_weighted_measure(fpx, reps=args.steps)
+        print(json.dumps(res), flush=True)
     else:
         run_fpx(args)
 

@@ -9,21 +9,26 @@
 // project's reading of running the same layer on many tokens at once.
 //
 // Pipeline (one stream, no host synchronisation):
-//   k_px16     x (bfloat16) -> binary16 rows scaled by a per-token power of two (exact), + shifts
+//   k_to_f16   x (bfloat16) -> binary16 rows scaled by a per-token power of two (exact), + shifts
 //   k_plogits  logits[t][e] = sum_h R[e][h] x[t][h], binary32, fixed order over h
 //   k_ptopk    one warp per token: top-k by logit (ties to the lower index), sigmoid weights
 //   k_phist / k_pscan / k_pscatter: stable counting sort of the T*k pairs p = t*k + r by expert:
-//              perm[s] = p in expert order (p ascending within an expert), inv[p] = s, offsets[E+1],
-//              and the list of 64-pair GEMM tiles (expert, first sorted position)
-//   k_pgemm    grouped GEMM: out[s][m] = sum_k W_e[m][k] b_s[k] for the rows s of a tile
+//              perm[s] = p in expert order (p ascending within an expert), inv[p] = s, offsets[E+1]
+//   k_pgather  the pairs' activation rows in expert order, each 16-group in the decode's pair order
+//   k_tcunits  the tensor-core GEMM units (expert, pair tile of <= 128, 256-row block)
+//   k_tcgemm   grouped GEMM on the tcgen05 tensor cores: out[s][m] = sum_k W_e[m][k] b_s[k]
+//              (routed gate / up FP2, routed down FP3; the shared expert's FP4 gate / up / down over
+//              every token after k_fp4_rowexp, k_perm4 and k_tcunits_dense)
 //   k_ph       h = silu(g) u (binary32), then binary16 rows scaled by a per-row power of two
 //   k_pcombine out[t] = sum_r w[t][r] y[inv[t*k+r]] (ranks in order) + y_shared[t]
 //
 // GEMM arithmetic. B is the activation row in binary16 times its power-of-two scale (exact). FP2 /
 // FP3: the A operand is the weight d (2c - 3) or d (2c - 7) rounded once to binary16 (relative error
-// at most 2^-11 per weight, a quarter of the 2e-3 bound), so the MMAs accumulate across blocks. FP4:
-// A is the E2M1 value times 2^-14 (exact) and each MMA pair covers one 32-weight block whose binary32
-// partial is multiplied by the block scale 2^(e-127) (exact for every exponent).
+// at most 2^-11 per weight, a quarter of the 2e-3 bound). FP4: the E2M1 value times 2^(e - E_m + 1),
+// E_m the row's largest block exponent; exact in binary16 for blocks within 2^14 of the row's largest
+// scale, smaller ones rounded as binary16 subnormals and blocks more than 2^24 below it dropped (their
+// share of the row is below 2^-24 of its largest block's). The row factor 2^(E_m - 128) is applied to
+// the binary32 accumulator. The tensor core accumulates in binary32 across the whole K.
 #include "fpx_mma.cuh"
 #include "route.cuh"
 #include "tc.cuh"
@@ -32,15 +37,14 @@ using namespace fpx;
 
 namespace {
 
-constexpr int kPT = 64;              // pairs (or tokens) per GEMM tile: 8 MMA column tiles
-constexpr int kGemmThreads = 256;    // 8 warps
 constexpr int kPMaxK = 8;
 
 // ------------------------------------------------------------------ workspace
 
 struct PWs {
-    size_t status, logits, idx, w, counts, offsets, perm, inv, units, nunits, x16, shx;
-    size_t g, u, gsh, ush, h16, shh, hsh16, shsh, yp, ysh, xg, gshift, tcu_gu, tcu_dn, ntc, total;
+    size_t status, logits, idx, w, counts, offsets, perm, inv, x16, shx;
+    size_t g, u, gsh, ush, h16, shh, hsh16, shsh, yp, ysh, xg, gshift, tcu_gu, tcu_dn, ntc;
+    size_t xs4, rexp, tcu_sgu, tcu_sdn, total;
 };
 
 inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -57,8 +61,6 @@ PWs pws_layout(int64_t T, int64_t E, int64_t H, int64_t I, int64_t k) {
     w.offsets = o; o = up256(o + 4 * (E + 1));
     w.perm = o; o = up256(o + 4 * P);
     w.inv = o; o = up256(o + 4 * P);
-    w.units = o; o = up256(o + 8 * (P / kPT + E));
-    w.nunits = o; o = up256(o + 16);
     w.x16 = o; o = up256(o + 2 * T * H);
     w.shx = o; o = up256(o + 4 * T);
     w.g = o; o = up256(o + 4 * P * I);
@@ -76,6 +78,10 @@ PWs pws_layout(int64_t T, int64_t E, int64_t H, int64_t I, int64_t k) {
     w.tcu_gu = o; o = up256(o + 16 * (P / 128 + E) * (I / 256));  // tensor-core GEMM units
     w.tcu_dn = o; o = up256(o + 16 * (P / 128 + E) * (H / 256));
     w.ntc = o; o = up256(o + 16);
+    w.xs4 = o; o = up256(o + 2 * T * H);                           // tokens in the FP4 decode's pair order
+    w.rexp = o; o = up256(o + 4 * (2 * I + H));                    // FP4 row exponents: gate, up, down
+    w.tcu_sgu = o; o = up256(o + 16 * ((T + 127) / 128) * (I / 256));  // shared expert's units
+    w.tcu_sdn = o; o = up256(o + 16 * ((T + 127) / 128) * (H / 256));
     w.total = o;
     return w;
 }
@@ -194,32 +200,21 @@ __global__ void k_phist(const int32_t* __restrict__ idx, int P, int E, int32_t* 
     atomicAdd(counts + e, 1);
 }
 
-// One CTA of 1024 threads (E <= 1024): offsets = exclusive scan of counts; tiles of kPT sorted
-// positions per expert, listed in expert order as (expert, first position).
-__global__ void __launch_bounds__(1024) k_pscan(const int32_t* __restrict__ counts, int E, int32_t* offsets,
-                                                int2* units, int32_t* nunits) {
-    __shared__ int32_t a[1024], b[1024];
+// One CTA of 1024 threads (E <= 1024): offsets = exclusive scan of counts.
+__global__ void __launch_bounds__(1024) k_pscan(const int32_t* __restrict__ counts, int E, int32_t* offsets) {
+    __shared__ int32_t a[1024];
     const int e = threadIdx.x;
-    const int n = e < E ? counts[e] : 0, nt = (n + kPT - 1) / kPT;
+    const int n = e < E ? counts[e] : 0;
     a[e] = n;
-    b[e] = nt;
     __syncthreads();
-    for (int o = 1; o < 1024; o <<= 1) {  // inclusive scans (Hillis-Steele)
-        const int va = e >= o ? a[e - o] : 0, vb = e >= o ? b[e - o] : 0;
+    for (int o = 1; o < 1024; o <<= 1) {  // inclusive scan (Hillis-Steele)
+        const int va = e >= o ? a[e - o] : 0;
         __syncthreads();
         a[e] += va;
-        b[e] += vb;
         __syncthreads();
     }
-    const int off = a[e] - n, ub = b[e] - nt;
-    if (e < E) {
-        offsets[e] = off;
-        for (int j = 0; j < nt; j++) units[ub + j] = make_int2(e, off + j * kPT);
-    }
-    if (e == E - 1) {
-        offsets[E] = a[e];
-        *nunits = b[e];
-    }
+    if (e < E) offsets[e] = a[e] - n;
+    if (e == E - 1) offsets[E] = a[e];
 }
 
 // One CTA per expert: the pairs routed to it, in increasing pair index (stable).
@@ -249,274 +244,17 @@ __global__ void __launch_bounds__(256) k_pscatter(const int32_t* __restrict__ id
     }
 }
 
-// ------------------------------------------------------------------ grouped GEMM
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// binary16 pair (lo, hi) of exactly representable values, at compile time
-constexpr uint32_t f16x2_pair(double lo, double hi) { return (uint32_t(f16_bits(hi)) << 16) | f16_bits(lo); }
-// decode constants (see a_frag)
-constexpr uint32_t kF2Mul0 = f16x2_pair(1.0, 0.25), kF2Add0 = f16x2_pair(-1027.0, -259.0);
-constexpr uint32_t kF2Mul2 = f16x2_pair(0.0625, 0.015625), kF2Add2 = f16x2_pair(-67.0, -19.0);
-constexpr uint32_t kF3Mul = f16x2_pair(1.0, 1.0), kF3Add = f16x2_pair(-1031.0, -1031.0);
+// ------------------------------------------------------------------ binary16 pair arithmetic
 
 __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
     asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
-
-struct PGemmArgs {
-    const uint8_t* W;         // box-tiled matrix of expert 0, or the shared matrix
-    int64_t mstride;          // bytes between consecutive experts' matrices (0: shared)
-    int M, K;                 // rows and columns of each matrix
-    const __half* B;          // binary16 activation rows [*][K]
-    const int32_t* rows;      // routed gate/up: perm (B row = perm[s] / row_div); else B row = s
-    int row_div;
-    const int32_t* shift;     // power-of-two scale of each B row
-    const int2* units;        // routed: tiles (expert, first sorted position); NULL: shared
-    const int32_t* nunits;
-    const int32_t* offsets;   // routed: expert ranges
-    int n_rows;               // shared: number of rows (tokens)
-    float* out;               // [rows][M]
-    int32_t* status;
-};
-
-template <int FMT>
-struct PGeo {
-    static constexpr int R = stage_rows(FMT);                 // weight rows per tile (box rows)
-    static constexpr int SK = stage_k(FMT);                   // weights per row per stage
-    static constexpr int WB = stage_bytes(FMT);               // weight box bytes
-    static constexpr int BP = SK * 2 + 32;                    // B row pitch (bytes): conflict-free 64-bit loads
-    static constexpr int BB = kPT * BP;                       // B tile bytes
-    static constexpr int BUF = WB + BB;
-    static constexpr int SMEM = 2 * BUF + 2 * kPT * 4;        // + B row indices and shifts
-    static constexpr int NB = SK / 32;                        // blocks per stage
-    static constexpr int RT = FMT == 4 ? 1 : 2;               // 16-row tiles per warp
-    static constexpr int NT = FMT == 4 ? 4 : 8;               // 8-column tiles per warp
-};
-
-// FP3 code j of pair slot (odd, p): the 3-bit field of the box layout (see fp3_slot).
-__device__ __forceinline__ uint32_t fp3_code(uint32_t W0, uint32_t W1, uint32_t W2, int f, int hh) {
-    if (f < 0) return ((W0 >> (16 * hh)) & 1u) | (((W1 >> (16 * hh)) & 1u) << 1) | (((W2 >> (16 * hh)) & 1u) << 2);
-    const uint32_t w = f < 16 ? W0 : f < 32 ? W1 : W2;
-    return (w >> (16 * hh + (f & 15))) & 7u;
-}
-
-// A fragment registers of one row for block b, half ww: a0 = k-slots (2t, 2t + 1), a2 = (2t + 8, 2t + 9),
-// holding codes 16 ww + 4t + {0, 1} and {2, 3} of the block (B is loaded with the same order). A code c
-// placed at binary16 mantissa bit P reads 1024 + c 2^P; one HFMA2 maps it to 2c - 3 (FP2) or 2c - 7
-// (FP3) with constants exact in binary16 (P >= 1 keeps them within 11 significant bits).
 __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
-}
-
-template <int FMT>
-__device__ __forceinline__ void a_frag(uint32_t wbox, int row, int b, int ww, int t, uint32_t& a0, uint32_t& a2) {
-    if constexpr (FMT == 2) {
-        const int C = b >> 1, hb = b & 1;
-        uint32_t wd;
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wd) : "r"(wbox + (uint32_t)(row * 64 + 4 * (4 * (2 * hb + ww) + C))));
-        // byte t (codes 4t .. 4t + 3, 2 bits each) in both halves, shifted up by one: c0 at P = 1 (low),
-        // c1 at P = 3 (high), c2 at P = 5 (low), c3 at P = 7 (high)
-        const uint32_t v2 = __byte_perm(wd, 0u, (uint32_t)t | 0x40u | ((uint32_t)t << 8) | 0x4000u) << 1;
-        a0 = hfma2_u((v2 & 0x00180006u) | kMagic, kF2Mul0, kF2Add0);
-        a2 = hfma2_u((v2 & 0x01800060u) | kMagic, kF2Mul2, kF2Add2);
-    } else if constexpr (FMT == 3) {
-        const int C = b >> 1, hb = b & 1, m = C >> 1, odd = C & 1;
-        const int tl = 2 * hb + ww;  // the layout thread whose group holds these codes
-        const uint32_t base = wbox + (uint32_t)(row * 96 + 24 * tl + 12 * m);
-        uint32_t W0, W1, W2;
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(W0) : "r"(base));
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(W1) : "r"(base + 4));
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(W2) : "r"(base + 8));
-        const int hh = t >> 1, p0 = 4 * (t & 1);
-        uint32_t c[4];
-#pragma unroll
-        for (int i = 0; i < 4; i++) c[i] = fp3_code(W0, W1, W2, fp3_slot(odd, p0 + i), hh);
-        // P = 1: 1024 + 2c - 1031 = 2c - 7
-        a0 = hfma2_u(((c[0] | (c[1] << 16)) << 1) | kMagic, kF3Mul, kF3Add);
-        a2 = hfma2_u(((c[2] | (c[3] << 16)) << 1) | kMagic, kF3Mul, kF3Add);
-    } else {
-        const uint32_t o = wbox + (uint32_t)(row * 272 + 17 * b + 1 + 8 * ww + 2 * t);
-        uint16_t lo, hi;
-        asm volatile("ld.shared.u8 %0, [%1];" : "=h"(lo) : "r"(o));
-        asm volatile("ld.shared.u8 %0, [%1];" : "=h"(hi) : "r"(o + 1));
-        const uint32_t v = (uint32_t)lo | ((uint32_t)hi << 8);
-        const uint32_t v2 = v | (v << 12), v3 = v2 >> 8;
-        a0 = ((v2 & 0x00070007u) << 9) | ((v2 & 0x00080008u) << 12);
-        a2 = ((v3 & 0x00070007u) << 9) | ((v3 & 0x00080008u) << 12);
-    }
-}
-
-// FP2 / FP3: the binary16 scale of block b of a row, in both halves of a pair.
-template <int FMT>
-__device__ __forceinline__ uint32_t blk_scale2(uint32_t wbox, int row, int b) {
-    const int C = b >> 1, hb = b & 1;
-    uint16_t d;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(d) : "r"(wbox + (uint32_t)(box_scale_offset(FMT) + row * 16 + 2 * (4 * hb + C))));
-    return (uint32_t)d | ((uint32_t)d << 16);
-}
-
-// Scale of block b of a row (binary32); FP4: 2^(e - 127) * 2^14 (undoing the decode's 2^-14), 0 and a
-// flag for the invalid exponent 255.
-template <int FMT>
-__device__ __forceinline__ float blk_scale(uint32_t wbox, int row, int b, uint32_t& bad) {
-    if constexpr (FMT == 4) {
-        uint16_t e;
-        asm volatile("ld.shared.u8 %0, [%1];" : "=h"(e) : "r"(wbox + (uint32_t)(row * 272 + 17 * b)));
-        bad |= e == 255;
-        return e == 255 ? 0.f : exp2i((int)e - 127 + 14);
-    } else {
-        const int C = b >> 1, hb = b & 1;
-        uint16_t d;
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(d) : "r"(wbox + (uint32_t)(box_scale_offset(FMT) + row * 16 + 2 * (4 * hb + C))));
-        return __half2float(__ushort_as_half(d));
-    }
-}
-
-template <int FMT>
-__global__ void __launch_bounds__(kGemmThreads, 2) k_pgemm(const __grid_constant__ PGemmArgs A) {
-    using G = PGeo<FMT>;
-    extern __shared__ __align__(128) uint8_t smem[];
-    int32_t* brow_s = reinterpret_cast<int32_t*>(smem + 2 * G::BUF);
-    int32_t* bsh_s = brow_s + kPT;
-    const int u = blockIdx.y;
-    int e = 0, s0, n;
-    if (A.units) {
-        if (u >= __ldg(A.nunits)) return;
-        const int2 un = A.units[u];
-        e = un.x;
-        s0 = un.y;
-        n = min(kPT, A.offsets[e + 1] - s0);
-    } else {
-        s0 = u * kPT;
-        if (s0 >= A.n_rows) return;
-        n = min(kPT, A.n_rows - s0);
-    }
-    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    if (threadIdx.x < kPT) {
-        const int s = s0 + threadIdx.x;
-        const int br = threadIdx.x < n ? (A.rows ? A.rows[s] / A.row_div : s) : -1;
-        brow_s[threadIdx.x] = br;
-        bsh_s[threadIdx.x] = br >= 0 ? A.shift[br] : 0;
-    }
-    __syncthreads();
-    const int rb = blockIdx.x;  // row block of R rows
-    const int nks = A.K / G::SK;
-    const uint8_t* wbase = A.W + (int64_t)e * A.mstride + (int64_t)rb * nks * G::WB;
-    const uint32_t sbase = smem_u32(smem);
-
-    auto issue = [&](int ks, int buf) {
-        const uint32_t wdst = sbase + (uint32_t)(buf * G::BUF), bdst = wdst + G::WB;
-        const uint8_t* wsrc = wbase + (int64_t)ks * G::WB;
-        for (int c = threadIdx.x; c < G::WB / 16; c += kGemmThreads) cp_async16(wdst + 16 * c, wsrc + 16 * c, 16);
-        constexpr int CPR = G::SK * 2 / 16;  // 16-byte chunks per B row
-        for (int c = threadIdx.x; c < kPT * CPR; c += kGemmThreads) {
-            const int r = c / CPR, j = c % CPR;
-            const int br = brow_s[r];
-            const __half* src = br >= 0 ? A.B + (size_t)br * A.K + (size_t)ks * G::SK + 8 * j : A.B;
-            cp_async16(bdst + (uint32_t)(r * G::BP + 16 * j), src, br >= 0 ? 16u : 0u);
-        }
-        cp_async_commit();
-    };
-
-    float y[G::RT][G::NT][4];
-#pragma unroll
-    for (int i = 0; i < G::RT; i++)
-#pragma unroll
-        for (int j = 0; j < G::NT; j++) y[i][j][0] = y[i][j][1] = y[i][j][2] = y[i][j][3] = 0.f;
-    uint32_t bad = 0;
-    // warp layout: FP2 / FP3: rows 32w .. 32w + 31 (two tiles), all 64 columns; FP4: rows
-    // 16 (w % 4) .. +15, columns 32 (w / 4) .. +31
-    const int row0 = FMT == 4 ? 16 * (warp & 3) : 32 * warp;
-    const int col0 = FMT == 4 ? 32 * (warp >> 2) : 0;
-
-    issue(0, 0);
-    for (int ks = 0; ks < nks; ks++) {
-        if (ks + 1 < nks) {
-            issue(ks + 1, (ks + 1) & 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        const uint32_t wbox = sbase + (uint32_t)((ks & 1) * G::BUF), btile = wbox + G::WB;
-#pragma unroll 1
-        for (int b = 0; b < G::NB; b++) {
-            uint32_t af[G::RT][2][4];  // [row tile][half][a0 a1 a2 a3]
-            float d[G::RT][2];
-#pragma unroll
-            for (int i = 0; i < G::RT; i++) {
-                const int r0 = row0 + 16 * i + g, r8 = r0 + 8;
-#pragma unroll
-                for (int ww = 0; ww < 2; ww++) {
-                    a_frag<FMT>(wbox, r0, b, ww, t, af[i][ww][0], af[i][ww][2]);
-                    a_frag<FMT>(wbox, r8, b, ww, t, af[i][ww][1], af[i][ww][3]);
-                }
-                if constexpr (FMT == 4) {
-                    d[i][0] = blk_scale<FMT>(wbox, r0, b, bad);
-                    d[i][1] = blk_scale<FMT>(wbox, r8, b, bad);
-                } else {  // fold the block scale into the binary16 weights
-                    const uint32_t d0 = blk_scale2<FMT>(wbox, r0, b), d8 = blk_scale2<FMT>(wbox, r8, b);
-#pragma unroll
-                    for (int ww = 0; ww < 2; ww++) {
-                        af[i][ww][0] = hmul2_u(af[i][ww][0], d0);
-                        af[i][ww][2] = hmul2_u(af[i][ww][2], d0);
-                        af[i][ww][1] = hmul2_u(af[i][ww][1], d8);
-                        af[i][ww][3] = hmul2_u(af[i][ww][3], d8);
-                    }
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < G::NT; j++) {
-                const uint32_t ba = btile + (uint32_t)((col0 + 8 * j + g) * G::BP + 2 * (32 * b + 4 * t));
-                uint32_t b00, b01, b10, b11;
-                asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(b00), "=r"(b01) : "r"(ba));
-                asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(b10), "=r"(b11) : "r"(ba + 32));
-#pragma unroll
-                for (int i = 0; i < G::RT; i++) {
-                    if constexpr (FMT == 4) {
-                        float p[4];
-                        mma_first(p, af[i][0][0], af[i][0][1], af[i][0][2], af[i][0][3], b00, b01);
-                        mma_acc(p, af[i][1][0], af[i][1][1], af[i][1][2], af[i][1][3], b10, b11);
-                        y[i][j][0] = fmaf(d[i][0], p[0], y[i][j][0]);
-                        y[i][j][1] = fmaf(d[i][0], p[1], y[i][j][1]);
-                        y[i][j][2] = fmaf(d[i][1], p[2], y[i][j][2]);
-                        y[i][j][3] = fmaf(d[i][1], p[3], y[i][j][3]);
-                    } else {
-                        mma_acc(y[i][j], af[i][0][0], af[i][0][1], af[i][0][2], af[i][0][3], b00, b01);
-                        mma_acc(y[i][j], af[i][1][0], af[i][1][1], af[i][1][2], af[i][1][3], b10, b11);
-                    }
-                }
-            }
-        }
-        __syncthreads();  // the buffer is refilled by the next issue
-    }
-    if (__any_sync(0xffffffffu, bad != 0u) && lane == 0) flag(A.status, FPX_EDATA);
-    // epilogue: out[s][m] = y * 2^-shift(s)
-#pragma unroll
-    for (int j = 0; j < G::NT; j++) {
-#pragma unroll
-        for (int c = 0; c < 2; c++) {
-            const int col = col0 + 8 * j + 2 * t + c;
-            if (col >= n) continue;
-            const float sc = exp2i(-bsh_s[col]);
-            float* o = A.out + (size_t)(s0 + col) * A.M + (size_t)rb * G::R;
-#pragma unroll
-            for (int i = 0; i < G::RT; i++) {
-                o[row0 + 16 * i + g] = y[i][j][c] * sc;
-                o[row0 + 16 * i + g + 8] = y[i][j][2 + c] * sc;
-            }
-        }
-    }
 }
 
 // ------------------------------------------------------------------ tcgen05 grouped GEMM (routed)
@@ -551,8 +289,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_pgemm(const __grid_constant
 constexpr int kTcN = 128;                                           // pairs per unit at most
 constexpr int kTcSK = 128;                                          // K per stage
 constexpr int kTcAStages = 2;                                       // A stages in tensor memory
-constexpr int kTcBStages = 4;                                       // B stages in shared memory
-constexpr int kTcRS = 3;                                            // packed boxes in flight
 constexpr int kTcDec = 16, kTcEpi = 4;                              // decoder and epilogue warps
 constexpr int kTcIss = 2;                                           // MMA-issuing warps (one per half)
 constexpr int kTcDec0 = 2 + kTcIss;                                 // first decoder warp
@@ -560,17 +296,32 @@ constexpr int kTcThreads = (kTcDec0 + kTcDec + kTcEpi) * 32;
 constexpr int kTcBRows = 16;                                        // rows of one B tile load
 constexpr int kTcBTile = kTcN * 128;                                // 128 rows x 64 binary16
 constexpr int kTcBStage = 2 * kTcBTile;                             // a stage: two 64-wide tiles
-constexpr int kTcBox = stage_bytes(3);                              // ring slot (an FP2 box fits)
-constexpr int kTcSmem = kTcRS * kTcBox + kTcBStages * kTcBStage + 1024;
+// Ring slot of packed weights: FP2 / FP3 one 256 x 256 box (FP3's 28 KB), FP4 the four 64-row boxes
+// of 256 rows x 512 K; slots in flight; B stages.
+__host__ __device__ constexpr int tc_slot_bytes(int fmt) { return fmt == 4 ? 4 * stage_bytes(4) : stage_bytes(3); }
+__host__ __device__ constexpr int tc_slot_k(int fmt) { return fmt == 4 ? 512 : 256; }
+__host__ __device__ constexpr int tc_ring_slots(int fmt) { return fmt == 4 ? 2 : 3; }
+__host__ __device__ constexpr int tc_bstages(int fmt) { return fmt == 4 ? 2 : 4; }
+// (+ 1024 for aligning the base, + 64: the FP4 decode's last word load may run 20 bytes past a row)
+__host__ __device__ constexpr int tc_smem(int fmt) {
+    return tc_ring_slots(fmt) * tc_slot_bytes(fmt) + tc_bstages(fmt) * kTcBStage + 1024 + 64;
+}
+constexpr int kTcMaxRS = 3, kTcMaxBS = 4;
 constexpr int kTcCols = 512;
 constexpr uint32_t kTcACol = 256;                                   // first A-stage column
-static_assert(kTcBox % 1024 == 0 && kTcBTile % 1024 == 0, "1024-byte aligned stages");
-static_assert(kTcSmem + kTcEpi * kTcN * 4 + 1024 <= 227 * 1024, "shared memory per CTA");
+static_assert(tc_slot_bytes(2) % 1024 == 0 && tc_slot_bytes(4) % 1024 == 0 && kTcBTile % 1024 == 0, "1024-byte aligned stages");
+static_assert(tc_smem(2) + kTcEpi * kTcN * 4 + 1024 <= 227 * 1024 && tc_smem(4) + kTcEpi * kTcN * 4 + 1024 <= 227 * 1024,
+              "shared memory per CTA");
 static_assert(kTcACol + 128 * kTcAStages <= kTcCols, "tensor-memory columns");
 
-// Column block (8 columns) of K step kk (0..7 = slab kk / 4, code group kk % 4) within a half's 64
-// A-stage columns: thread p of a row owns blocks 4 p .. 4 p + 3 (groups 2 p, 2 p + 1 of both slabs).
-__host__ __device__ constexpr uint32_t tc_kblock(int kk) { return 4u * ((kk & 3) >> 1) + 2u * (kk >> 2) + (kk & 1); }
+// Column block (8 columns) of K step kk (0..7, 16 K each) within a half's 64 A-stage columns. FP2 /
+// FP3 (kk = slab kk / 4, code group kk % 4): thread p of a row owns blocks 4 p .. 4 p + 3 (groups 2 p,
+// 2 p + 1 of both slabs). FP4: thread p owns the stage's 32-weight blocks 2 p, 2 p + 1, i.e. K steps
+// 4 p .. 4 p + 3 in order.
+template <int FMT>
+__host__ __device__ constexpr uint32_t tc_kblock(int kk) {
+    return FMT == 4 ? (uint32_t)kk : 4u * ((kk & 3) >> 1) + 2u * (kk >> 2) + (kk & 1);
+}
 
 struct TcArgs {
     CUtensorMap bmap;         // B: binary16 [rows][K], K-permuted, box 64 x 16, 128-byte swizzle
@@ -580,6 +331,7 @@ struct TcArgs {
     const int4* units;        // (expert, first B row, pairs, 256-row block)
     const int32_t* nunits;
     const int32_t* shift;     // power-of-two scale exponent of every B row
+    const int32_t* rowexp;    // FP4: largest valid block exponent of every weight row (else unused)
     float* out;               // [B rows][M]
     int32_t* status;
 };
@@ -658,7 +410,8 @@ struct TcAcc {
 template <int FMT>
 __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant__ TcArgs A) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ uint64_t bars[2 * kTcRS + 2 * kTcAStages + 2 * kTcBStages + 5];
+    constexpr int kTcRS = tc_ring_slots(FMT), kTcBStages = tc_bstages(FMT), kTcBox = tc_slot_bytes(FMT);
+    __shared__ uint64_t bars[2 * kTcMaxRS + 2 * kTcAStages + 2 * kTcMaxBS + 5];
     __shared__ uint32_t taddr_s;
     __shared__ float efac[kTcEpi][kTcN];  // per epilogue warp: 2^-shift of the unit's B rows
     uint8_t* base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
@@ -700,12 +453,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
             bool live = true;
             for (int u = c; u < nunits && live; u += G) {
                 const int4 un = A.units[u];
-                const uint8_t* wb = A.W + (int64_t)un.x * A.mstride + (int64_t)un.w * (A.K / stage_k(FMT)) * stage_bytes(FMT);
-                for (int bx = 0; bx < nslab / 4; bx++, gb++) {
+                const int nkb = A.K / stage_k(FMT);  // boxes along K
+                const uint8_t* wb = A.W + (int64_t)un.x * A.mstride + (int64_t)un.w * (256 / stage_rows(FMT)) * nkb * stage_bytes(FMT);
+                for (int bx = 0; bx < A.K / tc_slot_k(FMT); bx++, gb++) {
                     const uint32_t sl = gb % kTcRS;
                     if (gb >= (uint32_t)kTcRS && !mbar_wait(ring_empty + sl, ((gb / kTcRS) + 1u) & 1u)) { live = false; break; }
-                    mbar_expect_tx(ring_full + sl, stage_bytes(FMT));
-                    bulk_load(ring + sl * kTcBox, wb + (int64_t)bx * stage_bytes(FMT), stage_bytes(FMT), ring_full + sl);
+                    mbar_expect_tx(ring_full + sl, FMT == 4 ? 4 * stage_bytes(4) : stage_bytes(FMT));
+                    if constexpr (FMT == 4) {
+                        // the unit's four 64-row boxes at this K
+                        for (int i = 0; i < 4; i++)
+                            bulk_load(ring + sl * kTcBox + i * stage_bytes(4), wb + ((int64_t)i * nkb + bx) * stage_bytes(4),
+                                      stage_bytes(4), ring_full + sl);
+                    } else {
+                        bulk_load(ring + sl * kTcBox, wb + (int64_t)bx * stage_bytes(FMT), stage_bytes(FMT), ring_full + sl);
+                    }
                 }
             }
             if (!live) flag(A.status, FPX_ETIMEOUT);
@@ -765,7 +526,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
                     const uint64_t bd = sw128_desc(smem_u32(Bs + sb * kTcBStage));
 #pragma unroll
                     for (int kk = 0; kk < 8; kk++)
-                        tc_mma_f16_ta(dcol, a0 + 8u * tc_kblock(kk), bd + 1024u * (kk >> 2) + 2u * (kk & 3), idesc, (j | kk) != 0);
+                        tc_mma_f16_ta(dcol, a0 + 8u * tc_kblock<FMT>(kk), bd + 1024u * (kk >> 2) + 2u * (kk & 3), idesc, (j | kk) != 0);
                     tc_commit(smem_u32(a_free + sa));
                     tc_commit(smem_u32(b_free + sb));
                 }
@@ -788,6 +549,68 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
         uint32_t gs = 0, gb = 0;
         bool live = true;
         const uint32_t magic = kMagic;
+        uint32_t bad = 0;
+        if constexpr (FMT == 4) {
+            // A row of the unit lies in 64-row box row / 64 of the slot, at byte (row % 64) * 272; a stage
+            // (128 K) holds blocks 4 S .. 4 S + 3 of the box row, 17 bytes each; this thread decodes blocks
+            // 4 S + 2 p and 4 S + 2 p + 1 (one scale byte, then 16 bytes of two E2M1 codes each)
+            const uint32_t row_ofs = (uint32_t)(row >> 6) * stage_bytes(4) + (uint32_t)(row & 63) * 272u;
+            for (int u = c; u < nunits && live; u += G) {
+                const int erow = __ldg(A.rowexp + A.units[u].w * 256 + row);
+                for (int bx = 0; bx < A.K / 512 && live; bx++, gb++) {
+                    const uint32_t sl = gb % kTcRS;
+                    if (!__any_sync(0xffffffffu, mbar_wait(ring_full + sl, (gb / kTcRS) & 1u))) { live = false; break; }
+                    const uint32_t rbase = smem_u32(ring + sl * kTcBox) + row_ofs;
+#pragma unroll
+                    for (int S = 0; S < 4; S++, gs++) {
+                        // both blocks' scale bytes and codes (the codes realigned to words)
+                        uint32_t e[2], cw[2][4];
+#pragma unroll
+                        for (int j = 0; j < 2; j++) {
+                            const uint32_t ob = rbase + 17u * (uint32_t)(4 * S + 2 * p + j);
+                            e[j] = lds8<0>(ob);
+                            const uint32_t cb = (ob + 1u) & ~3u, cs = 8u * ((ob + 1u) & 3u);
+                            uint32_t x[5];
+#pragma unroll
+                            for (int i = 0; i < 5; i++) x[i] = lds32<0>(cb + 4u * (uint32_t)i);
+#pragma unroll
+                            for (int i = 0; i < 4; i++) cw[j][i] = __funnelshift_r(x[i], x[i + 1], cs);
+                        }
+                        if (S == 3) {
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(ring_empty + sl);
+                        }
+                        const uint32_t st = gs % kTcAStages;
+                        if (live && gs >= (uint32_t)kTcAStages)
+                            live = __any_sync(0xffffffffu, mbar_wait(a_free + st, ((gs / kTcAStages) + 1u) & 1u));
+                        if (!live) break;
+                        tc_fence_after();
+                        uint32_t o[32];
+#pragma unroll
+                        for (int j = 0; j < 2; j++) {
+                            // 2^(e - erow + 15) in binary16 (normal, subnormal or zero): times the decoded
+                            // E2M1 value * 2^-14 gives value * 2^(e - erow + 1), exact while normal
+                            const int f = (int)e[j] - erow + 30;
+                            uint32_t mb = f >= 1 ? (uint32_t)f << 10 : f >= -9 ? 1u << (f + 9) : 0u;
+                            if (e[j] == 255u) { mb = 0u; bad = 1u; }
+                            const uint32_t m2 = mb | (mb << 16);
+                            uint32_t a[8];
+                            decode_fp4(cw[j][0], cw[j][1], a);
+#pragma unroll
+                            for (int k = 0; k < 8; k++) o[16 * j + k] = hmul2_u(a[k], m2);
+                            decode_fp4(cw[j][2], cw[j][3], a);
+#pragma unroll
+                            for (int k = 0; k < 8; k++) o[16 * j + 8 + k] = hmul2_u(a[k], m2);
+                        }
+                        tmem_st32(lane_base + 128u * st, o);
+                        tmem_st_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(a_full + st);
+                    }
+                }
+            }
+        } else {
         for (int u = c; u < nunits && live; u += G) {
             for (int bx = 0; bx < nslab / 4 && live; bx++, gb++) {
                 const uint32_t sl = gb % kTcRS;
@@ -841,7 +664,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
                 }
             }
         }
+        }
         if (!live && lane == 0) flag(A.status, FPX_ETIMEOUT);
+        if (__any_sync(0xffffffffu, bad != 0u) && lane == 0) flag(A.status, FPX_EDATA);
     } else {
         // ---------------------------------------------------------------- epilogue (4 warps)
         const int q = warp & 3;  // tensor-memory lane quarter of this warp
@@ -863,13 +688,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
             for (int hh = 0; hh < 2; hh++) {
                 const int m = un.w * 256 + hh * 128 + 32 * q + lane;
                 float* orow = A.out + (size_t)un.y * A.M + m;
+                // FP4: the decode scaled row m by 2^(128 - rowexp[m]); undo it with the column factor
+                const float rf = FMT == 4 ? exp2i(__ldg(A.rowexp + m) - 128) : 1.0f;
                 for (int c0 = 0; c0 < n16; c0 += 16) {
                     float v[16];
                     tmem_ld16(taddr + ((uint32_t)(32 * q) << 16) + col0 + hstep * (uint32_t)hh + (uint32_t)c0, v);
 #pragma unroll
                     for (int j = 0; j < 16; j++) {
                         const int s = c0 + j;
-                        if (s < n) orow[(size_t)s * A.M] = v[j] * fac[s];
+                        if (s < n) orow[(size_t)s * A.M] = v[j] * (fac[s] * rf);
                     }
                 }
             }
@@ -946,8 +773,10 @@ __global__ void __launch_bounds__(1024) k_tcunits(const int32_t* __restrict__ of
 }
 
 // h = silu(g) u for rows [0, Pr) of (g, u) -> binary16 rows scaled by 2^sh(row) (exact shift), shift[row].
-// PERM: each 16-element group stored in the tensor-core decode's pair order (element p, then p + 8).
-template <bool PERM>
+// Each 16-element group is stored in a tensor-core decode's pair order (element lo(p), then lo(p) + D
+// at positions 2 p, 2 p + 1): PERM 1 the FP2 / FP3 order (lo(p) = p, D = 8), PERM 2 the FP4 order
+// (lo(p) = p + 4 (p / 4), D = 4).
+template <int PERM>
 __global__ void __launch_bounds__(256) k_ph(const float* __restrict__ g, const float* __restrict__ u, int L,
                                             __half* __restrict__ h16, int32_t* __restrict__ shift) {
     __shared__ float red[8];
@@ -970,13 +799,6 @@ __global__ void __launch_bounds__(256) k_ph(const float* __restrict__ g, const f
     }
     __syncthreads();
     const float sc = exp2i(sh_s);
-    if (!PERM) {
-        for (int i = threadIdx.x; i < L; i += blockDim.x) {
-            const float a = g[r * L + i], b = u[r * L + i];
-            h16[r * L + i] = __float2half_rn(((a / (1.0f + expf(-a))) * b) * sc);
-        }
-        return;
-    }
     for (int gi = threadIdx.x; gi < L / 16; gi += blockDim.x) {
         float v[16];
 #pragma unroll
@@ -987,13 +809,68 @@ __global__ void __launch_bounds__(256) k_ph(const float* __restrict__ g, const f
         uint32_t o[8];
 #pragma unroll
         for (int p = 0; p < 8; p++) {
-            const __half2 hp = __halves2half2(__float2half_rn(v[p]), __float2half_rn(v[p + 8]));
+            const int lo = PERM == 1 ? p : p + 4 * (p >> 2), hi = lo + (PERM == 1 ? 8 : 4);
+            const __half2 hp = __halves2half2(__float2half_rn(v[lo]), __float2half_rn(v[hi]));
             o[p] = *reinterpret_cast<const uint32_t*>(&hp);
         }
         uint4* dst = reinterpret_cast<uint4*>(h16 + r * L + 16 * gi);
         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
+}
+
+// dst row r = src row r (binary16 [R][L]) with each 16-element group in the FP4 decode's pair order
+// (elements p + 4 (p / 4) and p + 4 (p / 4) + 4 at positions 2 p, 2 p + 1). One thread per group.
+__global__ void __launch_bounds__(256) k_perm4(const __half* __restrict__ src, int64_t ngroups, __half* __restrict__ dst) {
+    const int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gi >= ngroups) return;
+    const uint4 a = reinterpret_cast<const uint4*>(src)[2 * gi], b = reinterpret_cast<const uint4*>(src)[2 * gi + 1];
+    // words: a = elements (0,1)(2,3)(4,5)(6,7), b = (8,9) .. (14,15); pair p of each 8: (k, k + 4)
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int p = 0; p < 8; p++) {
+        const int lo = p + 4 * (p >> 2), hi = lo + 4;
+        const uint32_t wl = w[lo >> 1], wh = w[hi >> 1];
+        o[p] = __byte_perm(wl, wh, ((lo & 1) ? 0x0032u : 0x0010u) | ((hi & 1) ? 0x7600u : 0x5400u));
+    }
+    reinterpret_cast<uint4*>(dst)[2 * gi] = make_uint4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<uint4*>(dst)[2 * gi + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// rowexp[m] = the largest block exponent e != 255 of row m of a box-tiled FP4 matrix [M][K] (0 when
+// none): the tensor-core decode scales row m by 2^(128 - rowexp[m]) to keep it in binary16 range. One
+// warp per row; blockIdx.y picks one of three matrices.
+struct RowExpArgs {
+    const uint8_t* W[3];
+    int M[3], K[3];
+    int32_t* out[3];
+};
+__global__ void __launch_bounds__(256) k_fp4_rowexp(const __grid_constant__ RowExpArgs A) {
+    const int mi = blockIdx.y, row = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int M = A.M[mi], K = A.K[mi];
+    if (row >= M) return;
+    const int nkb = K / 512;
+    const uint8_t* rb = A.W[mi] + (int64_t)(row >> 6) * nkb * stage_bytes(4) + (row & 63) * 272;
+    int e = 0;
+    for (int b = lane; b < K / 32; b += 32) {
+        const int v = __ldg(rb + (int64_t)(b >> 4) * stage_bytes(4) + 17 * (b & 15));
+        if (v != 255) e = max(e, v);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) e = max(e, __shfl_xor_sync(0xffffffffu, e, o));
+    if (lane == 0) A.out[mi][row] = e;
+}
+
+// Units of a dense GEMM over T rows of B (the shared expert): tiles of 128 rows, times MT 256-row
+// blocks of the weights, row blocks of a tile consecutive.
+__global__ void k_tcunits_dense(int T, int MT, int4* units, int32_t* nunits) {
+    const int nt = (T + kTcN - 1) / kTcN;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nt * MT; i += gridDim.x * blockDim.x) {
+        const int t = i / MT, mt = i % MT;
+        units[i] = make_int4(0, t * kTcN, min(kTcN, T - t * kTcN), mt);
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) *nunits = nt * MT;
 }
 
 // out[t][c] = sum_r w[t][r] * yp[inv[t*k + r]][c] (ranks in order) + ysh[t][c].
@@ -1011,16 +888,6 @@ __global__ void __launch_bounds__(256) k_pcombine(const float* __restrict__ yp, 
     for (int r = 0; r < kPMaxK; r++)
         if (r < k) acc = r == 0 ? w[(size_t)t * k] * v[0] : fmaf(w[(size_t)t * k + r], v[r], acc);
     out[o] = acc + ysh[o];
-}
-
-template <int FMT>
-cudaError_t launch_gemm(const PGemmArgs& a, int grid_units, cudaStream_t s) {
-    using G = PGeo<FMT>;
-    cudaError_t e = cudaFuncSetAttribute(k_pgemm<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
-    if (e != cudaSuccess) return e;
-    if (grid_units <= 0) return cudaSuccess;
-    k_pgemm<FMT><<<dim3(a.M / G::R, grid_units), kGemmThreads, G::SMEM, s>>>(a);
-    return cudaGetLastError();
 }
 
 // A 2-D tensor map over B (binary16 [rows][K]) for the tensor-core GEMM: boxes of 64 elements x 16
@@ -1042,8 +909,8 @@ template <int FMT>
 int launch_tc(TcArgs& a, const __half* B, int64_t rows, cudaStream_t s) {
     int st = make_b_map(&a.bmap, B, rows, a.K);
     if (st) return st;
-    if (cudaFuncSetAttribute(k_tcgemm<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess) return FPX_ECUDA;
-    k_tcgemm<FMT><<<device_info().sms, kTcThreads, kTcSmem, s>>>(a);
+    if (cudaFuncSetAttribute(k_tcgemm<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(FMT)) != cudaSuccess) return FPX_ECUDA;
+    k_tcgemm<FMT><<<device_info().sms, kTcThreads, tc_smem(FMT), s>>>(a);
     return cudaGetLastError() == cudaSuccess ? FPX_OK : FPX_ECUDA;
 }
 
@@ -1081,8 +948,6 @@ int moe_layer_prefill(const moe_layer* L, const uint16_t* x, int T, int k, float
     int32_t* offsets = reinterpret_cast<int32_t*>(b + W.offsets);
     int32_t* perm = reinterpret_cast<int32_t*>(b + W.perm);
     int32_t* inv = reinterpret_cast<int32_t*>(b + W.inv);
-    int2* units = reinterpret_cast<int2*>(b + W.units);
-    int32_t* nunits = reinterpret_cast<int32_t*>(b + W.nunits);
     __half* x16 = reinterpret_cast<__half*>(b + W.x16);
     int32_t* shx = reinterpret_cast<int32_t*>(b + W.shx);
     float* g = reinterpret_cast<float*>(b + W.g);
@@ -1100,6 +965,10 @@ int moe_layer_prefill(const moe_layer* L, const uint16_t* x, int T, int k, float
     int4* tcu_gu = reinterpret_cast<int4*>(b + W.tcu_gu);
     int4* tcu_dn = reinterpret_cast<int4*>(b + W.tcu_dn);
     int32_t* ntc = reinterpret_cast<int32_t*>(b + W.ntc);
+    __half* xs4 = reinterpret_cast<__half*>(b + W.xs4);
+    int32_t* rexp = reinterpret_cast<int32_t*>(b + W.rexp);
+    int4* tcu_sgu = reinterpret_cast<int4*>(b + W.tcu_sgu);
+    int4* tcu_sdn = reinterpret_cast<int4*>(b + W.tcu_sdn);
     const int P = T * k;
 
     if (cudaMemsetAsync(status, 0, 16, s) != cudaSuccess || cudaMemsetAsync(counts, 0, 4 * (E + 1), s) != cudaSuccess)
@@ -1108,11 +977,10 @@ int moe_layer_prefill(const moe_layer* L, const uint16_t* x, int T, int k, float
     k_plogits<<<dim3((T + 63) / 64, (E + 63) / 64), 256, 0, s>>>(L->router, x, T, E, H, logits);
     k_ptopk<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, idx, w);
     k_phist<<<(P + 255) / 256, 256, 0, s>>>(idx, P, E, counts, status);
-    k_pscan<<<1, 1024, 0, s>>>(counts, E, offsets, units, nunits);
+    k_pscan<<<1, 1024, 0, s>>>(counts, E, offsets);
     k_pscatter<<<E, 256, 0, s>>>(idx, P, offsets, perm, inv);
     if (cudaGetLastError() != cudaSuccess) return FPX_ECUDA;
 
-    const int tok_units = (T + kPT - 1) / kPT;
     const int64_t mb2 = fpx_matrix_bytes(2, I, H), mb3 = fpx_matrix_bytes(3, H, I);
     // routed experts on the tcgen05 tensor cores: activations gathered per pair in expert order
     k_pgather<<<(P + 7) / 8, 256, 0, s>>>(x16, shx, perm, P, k, H, xg, gshift);
@@ -1127,27 +995,38 @@ int moe_layer_prefill(const moe_layer* L, const uint16_t* x, int T, int k, float
     if (st) return st;
     ta.W = L->up; ta.out = u;
     if ((st = launch_tc<2>(ta, xg, P, s))) return st;
-    // shared gate and up: every token
-    PGemmArgs sa{};
+    // shared gate and up (FP4): every token, on the tensor cores as well; the rows' exponents, the
+    // tokens in the FP4 decode's pair order and the dense units first
+    RowExpArgs rea{};
+    rea.W[0] = L->sh_gate; rea.W[1] = L->sh_up; rea.W[2] = L->sh_down;
+    rea.M[0] = I; rea.M[1] = I; rea.M[2] = H;
+    rea.K[0] = H; rea.K[1] = H; rea.K[2] = I;
+    rea.out[0] = rexp; rea.out[1] = rexp + I; rea.out[2] = rexp + 2 * I;
+    k_fp4_rowexp<<<dim3((unsigned)((std::max(H, I) + 7) / 8), 3), 256, 0, s>>>(rea);
+    k_perm4<<<(unsigned)(((int64_t)T * H / 16 + 255) / 256), 256, 0, s>>>(x16, (int64_t)T * H / 16, xs4);
+    k_tcunits_dense<<<1, 256, 0, s>>>(T, I / 256, tcu_sgu, ntc + 2);
+    k_tcunits_dense<<<1, 256, 0, s>>>(T, H / 256, tcu_sdn, ntc + 3);
+    if (cudaGetLastError() != cudaSuccess) return FPX_ECUDA;
+    TcArgs sa{};
     sa.status = status;
-    sa.M = I; sa.K = H; sa.B = x16; sa.rows = nullptr; sa.row_div = 1; sa.units = nullptr; sa.nunits = nullptr;
-    sa.offsets = nullptr; sa.mstride = 0; sa.n_rows = T; sa.shift = shx;
-    sa.W = L->sh_gate; sa.out = gsh;
-    if (launch_gemm<4>(sa, tok_units, s) != cudaSuccess) return FPX_ECUDA;
-    sa.W = L->sh_up; sa.out = ush;
-    if (launch_gemm<4>(sa, tok_units, s) != cudaSuccess) return FPX_ECUDA;
+    sa.M = I; sa.K = H; sa.units = tcu_sgu; sa.nunits = ntc + 2; sa.shift = shx; sa.mstride = 0;
+    sa.W = L->sh_gate; sa.rowexp = rexp; sa.out = gsh;
+    if ((st = launch_tc<4>(sa, xs4, T, s))) return st;
+    sa.W = L->sh_up; sa.rowexp = rexp + I; sa.out = ush;
+    if ((st = launch_tc<4>(sa, xs4, T, s))) return st;
     // h in binary16 with per-row scales (routed rows K-permuted for the tensor-core GEMM)
-    k_ph<true><<<P, 256, 0, s>>>(g, u, I, h16, shh);
-    k_ph<false><<<T, 256, 0, s>>>(gsh, ush, I, hsh16, shsh);
+    k_ph<1><<<P, 256, 0, s>>>(g, u, I, h16, shh);
+    k_ph<2><<<T, 256, 0, s>>>(gsh, ush, I, hsh16, shsh);
     if (cudaGetLastError() != cudaSuccess) return FPX_ECUDA;
     // routed down: h rows already in expert order
     TcArgs tda = ta;
     tda.M = H; tda.K = I; tda.units = tcu_dn; tda.nunits = ntc + 1; tda.shift = shh; tda.mstride = mb3;
     tda.W = L->down; tda.out = yp;
     if ((st = launch_tc<3>(tda, h16, P, s))) return st;
-    PGemmArgs dsa = sa;
-    dsa.M = H; dsa.K = I; dsa.B = hsh16; dsa.shift = shsh; dsa.W = L->sh_down; dsa.out = ysh;
-    if (launch_gemm<4>(dsa, tok_units, s) != cudaSuccess) return FPX_ECUDA;
+    TcArgs dsa = sa;
+    dsa.M = H; dsa.K = I; dsa.units = tcu_sdn; dsa.nunits = ntc + 3; dsa.shift = shsh;
+    dsa.W = L->sh_down; dsa.rowexp = rexp + 2 * I; dsa.out = ysh;
+    if ((st = launch_tc<4>(dsa, hsh16, T, s))) return st;
     k_pcombine<<<(unsigned)(((size_t)T * H + 255) / 256), 256, 0, s>>>(yp, ysh, w, inv, T, H, k, y);
     if (idx_out && cudaMemcpyAsync(idx_out, idx, 4 * (size_t)P, cudaMemcpyDeviceToDevice, s) != cudaSuccess) return FPX_ECUDA;
     if (w_out && cudaMemcpyAsync(w_out, w, 4 * (size_t)P, cudaMemcpyDeviceToDevice, s) != cudaSuccess) return FPX_ECUDA;

@@ -265,7 +265,7 @@ int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int
                      void* stream);
 
 /* Workspace bytes moe_layer_prefill needs for T tokens and top-k (16-byte aligned; about
- * T*k*(10 I + 4 H) + T*(10 I + 6 H) bytes: 0.55 GB at T = 2048, k = 6, H = 4096, I = 2048).
+ * T*k*(10 I + 6 H) + T*(10 I + 8 H) bytes: 0.66 GB at T = 2048, k = 6, H = 4096, I = 2048).
  * 0 for invalid arguments. */
 size_t moe_prefill_workspace_bytes(const moe_layer* layer, int T, int k);
 
@@ -279,8 +279,11 @@ size_t moe_prefill_workspace_bytes(const moe_layer* layer, int T, int k);
  *     and the shared expert over all tokens;
  *   - out[t] = sum_r w[t][r] y_{e(t,r)}[t] (ranks in order) + y_shared[t].
  * x is bfloat16 [T][H], y binary32 [T][H]. Nullable outputs: idx_out [T][k], w_out [T][k],
- * logits_out [T][E], perm_out [T*k], offsets_out [E+1]. The GEMMs take the activations as binary16 rows scaled by a
- * power of two per row (h likewise), so every product is exact and only binary32 sums round. ws
+ * logits_out [T][E], perm_out [T*k], offsets_out [E+1]. The GEMMs (tcgen05 tensor cores) take the
+ * activations as binary16 rows scaled by a power of two per row (h likewise; exact), FP2 / FP3
+ * weights d (2c - 3), d (2c - 7) rounded once to binary16 (relative error <= 2^-11) and FP4 weights
+ * scaled per row by a power of two (exact for blocks within 2^14 of the row's largest block scale,
+ * binary16 subnormals below that, zero below 2^-25 of it); the sums are binary32. ws
  * holds moe_prefill_workspace_bytes(layer, T, k) bytes (ws_bytes); its first word is the status
  * word. [P-dsv4] paragraph 3 (TOP_K, ARGSORT), [P-apu] section "Lucebox's Optimization Trio"; the
  * grouping of a batch by expert is this project's reading (the pages describe decode). */
