@@ -580,11 +580,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
                             __syncwarp();
                             if (lane == 0) mbar_arrive(ring_empty + sl);
                         }
-                        const uint32_t st = gs % kTcAStages;
-                        if (live && gs >= (uint32_t)kTcAStages)
-                            live = __any_sync(0xffffffffu, mbar_wait(a_free + st, ((gs / kTcAStages) + 1u) & 1u));
-                        if (!live) break;
-                        tc_fence_after();
                         uint32_t o[32];
 #pragma unroll
                         for (int j = 0; j < 2; j++) {
@@ -602,6 +597,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
 #pragma unroll
                             for (int k = 0; k < 8; k++) o[16 * j + 8 + k] = hmul2_u(a[k], m2);
                         }
+                        const uint32_t st = gs % kTcAStages;
+                        if (live && gs >= (uint32_t)kTcAStages)
+                            live = __any_sync(0xffffffffu, mbar_wait(a_free + st, ((gs / kTcAStages) + 1u) & 1u));
+                        if (!live) break;
+                        tc_fence_after();
                         tmem_st32(lane_base + 128u * st, o);
                         tmem_st_wait();
                         tc_fence_before();
@@ -641,11 +641,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
                 // the box's two stages: slabs 0, 1 and 2, 3
 #pragma unroll
                 for (int S = 0; S < 2; S++, gs++) {
-                    const uint32_t st = gs % kTcAStages;
-                    if (live && gs >= (uint32_t)kTcAStages)
-                        live = __any_sync(0xffffffffu, mbar_wait(a_free + st, ((gs / kTcAStages) + 1u) & 1u));
-                    if (!live) break;
-                    tc_fence_after();
+                    // decode first, then wait for the stage: the decode overlaps the MMAs that still
+                    // read the stage, so it is not on the stage's round trip
                     uint32_t o[32];
                     uint32_t(&o0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[0]);
                     uint32_t(&o1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[16]);
@@ -656,6 +653,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tcgemm(const __grid_constant_
                         tc_half_slab<FMT, 2>(cw, sc, magic, o0);
                         tc_half_slab<FMT, 3>(cw, sc, magic, o1);
                     }
+                    const uint32_t st = gs % kTcAStages;
+                    if (live && gs >= (uint32_t)kTcAStages)
+                        live = __any_sync(0xffffffffu, mbar_wait(a_free + st, ((gs / kTcAStages) + 1u) & 1u));
+                    if (!live) break;
+                    tc_fence_after();
                     tmem_st32(lane_base + 128u * st, o);
                     tmem_st_wait();
                     tc_fence_before();
