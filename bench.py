@@ -632,11 +632,14 @@ def run_fpx(args):
     e2e_secs, h2d, d2h = e2e_pass(r4, e2e_steps, world)
     e2e_secs, e2e_bytes = over_ranks(e2e_secs, sum(bytes_per_batch[i % N_BATCHES] for i in range(e2e_steps)), world)
 
-    pf = prefill_measure(fpx, stack.layers[0], args.warmup)
-    dc = commit_measure(fpx, peak)
-    qw = quantize_weighted_measure(fpx)
-    idm = idot_measure(fpx, peak)
-    tm = tiered_measure(fpx, stack)
+    if args.part == "stack":  # the stack pass alone (profiling runs)
+        pf = dc = qw = idm = tm = None
+    else:
+        pf = prefill_measure(fpx, stack.layers[0], args.warmup)
+        dc = commit_measure(fpx, peak)
+        qw = quantize_weighted_measure(fpx)
+        idm = idot_measure(fpx, peak)
+        tm = tiered_measure(fpx, stack)
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -673,7 +676,7 @@ def run_fpx(args):
         "gpu_launches": args.steps * NK * args.layers,
         "clocks": clk.summary(),
     }
-    if rank == 0 and world == 1 and not args.skip_cpu:
+    if rank == 0 and world == 1 and not args.skip_cpu and args.part != "stack":
         import oracle
         with torch.cuda.stream(r4.stream):
             tr = torch.empty(args.layers, Q, H, device="cuda")
@@ -763,8 +766,9 @@ def main():
     p.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--ref-seconds", type=float, default=90.0)
-    p.add_argument("--part", choices=["all", "idot", "tiered", "prefill", "commit", "quantize"], default="all",
-                   help="idot: only the integer-dot / tensor-core GEMV comparison; tiered: only the two-tier "
+    p.add_argument("--part", choices=["all", "stack", "idot", "tiered", "prefill", "commit", "quantize"], default="all",
+                   help="stack: only the stack passes (q = 4, q = 1, end to end; no CPU baseline); "
+                        "idot: only the integer-dot / tensor-core GEMV comparison; tiered: only the two-tier "
                         "residency measurement on a one-layer stack; prefill: only the prefill of one layer "
                         "(--warmup calls, then --steps timed calls); commit: only the verify/commit rule; "
                         "quantize: only the importance-weighted quantizer (one JSON object each)")
