@@ -27,15 +27,18 @@ constexpr int kMaxQ = 4;
 constexpr int kMaxE = 1024;
 
 // Fixed pieces. A task of S stages (one output matrix x one row block, streamed along K) is computed
-// as pieces_of(S) pieces of consecutive stages, piece p covering stages [p S / P, (p + 1) S / P) with
+// as pieces_of(S, D) pieces of consecutive stages, piece p covering stages [p S / P, (p + 1) S / P) with
 // its own accumulators starting at zero; each piece writes its own partial buffer and the next kernel
 // adds the pieces of a task in piece order. The split depends on the matrix shape alone, never on the
 // expert union, the grid or the other tokens, so every column of a batched call is computed with the
 // same roundings as a call on that column alone ("DeepSeek V4 Flash hits 32 tok/s on AMD Ryzen AI
 // MAX+ 395", paragraph 3: each packed weight decoded once and applied to every verification column).
-__host__ __device__ constexpr int pieces_of(int S) { return (S + 3) / 4; }
-__host__ __device__ constexpr int piece_begin(int S, int p) { return p * S / pieces_of(S); }
-constexpr int kMaxPieces = pieces_of(4608 / 256);  // H, I <= 4608
+// Stages per piece: D_gu for the gate/up tasks, D_dn for the down tasks (coarser pieces cost fewer
+// partial outputs; finer ones balance the CTAs better, which matters more for the shorter down tasks).
+constexpr int kSppGu = 8, kSppDn = 4;
+__host__ __device__ constexpr int pieces_of(int S, int D) { return (S + D - 1) / D; }
+__host__ __device__ constexpr int piece_begin(int S, int D, int p) { return p * S / pieces_of(S, D); }
+constexpr int kMaxPieces = pieces_of(4608 / 256, kSppDn < kSppGu ? kSppDn : kSppGu);  // H, I <= 4608
 
 // Programmatic dependent launch: each layer kernel is launched so that it may start while the
 // previous kernel's last CTAs still run; grid_dep_wait() blocks until that kernel has completed and
@@ -66,8 +69,8 @@ inline Ws ws_layout(int H, int I, int E, int q, int k) {
     w.nuni = o; o += 16;  // n_uni, then the router's arrival counter
     w.gu_piece = (size_t)2 * (q * k + 1) * q * I;
     w.yi_piece = (size_t)(q * k + 1) * q * H;
-    w.gu = o; o = up16(o + sizeof(float) * pieces_of(H / stage_k(2)) * w.gu_piece);  // FP2 tasks have the most pieces
-    w.yi = o; o = up16(o + sizeof(float) * pieces_of(I / stage_k(3)) * w.yi_piece);
+    w.gu = o; o = up16(o + sizeof(float) * pieces_of(H / stage_k(2), kSppGu) * w.gu_piece);  // FP2 tasks have the most pieces
+    w.yi = o; o = up16(o + sizeof(float) * pieces_of(I / stage_k(3), kSppDn) * w.yi_piece);
     w.gt = o; o = up16(o + tset_bytes(H));
     w.dt = o; o = up16(o + (size_t)(q * k + 1) * dset_bytes(I));
     w.total = o;
@@ -485,20 +488,22 @@ struct UnitList {
 // FP4 boxes (17 KB) weighted for their slower decode, which the down kernel's FP3 stages outpace more.
 constexpr uint32_t kCostFP2 = 20, kCostFP3 = 28, kCostFP4Gu = 23, kCostFP4Dn = 34;
 
-__host__ __device__ constexpr uint32_t unit_cost(uint32_t c, int S) { return (c * S + pieces_of(S) / 2) / pieces_of(S); }
+__host__ __device__ constexpr uint32_t unit_cost(uint32_t c, int S, int D) {
+    return (c * S + pieces_of(S, D) / 2) / pieces_of(S, D);
+}
 
 // Unit lists of the gate/up kernel (FP2 tasks: matrix x 256-row block, H/256 stages; FP4: matrix x
 // 64-row block, H/512 stages) and of the down kernel (FP3: item x 256-row block, I/256 stages; FP4:
 // 64-row block, I/512 stages).
 __host__ __device__ inline UnitList gate_up_units(int n_uni, int H, int I) {
     const int sA = H / stage_k(2), sB = H / stage_k(4);
-    return UnitList{2u * n_uni * (I / 256) * pieces_of(sA), unit_cost(kCostFP2, sA), 2u * (I / 64) * pieces_of(sB),
-                    unit_cost(kCostFP4Gu, sB)};
+    return UnitList{2u * n_uni * (I / 256) * pieces_of(sA, kSppGu), unit_cost(kCostFP2, sA, kSppGu),
+                    2u * (I / 64) * pieces_of(sB, kSppGu), unit_cost(kCostFP4Gu, sB, kSppGu)};
 }
 __host__ __device__ inline UnitList down_units(int n_uni, int H, int I) {
     const int sA = I / stage_k(3), sB = I / stage_k(4);
-    return UnitList{(uint32_t)n_uni * (H / 256) * pieces_of(sA), unit_cost(kCostFP3, sA), (uint32_t)(H / 64) * pieces_of(sB),
-                    unit_cost(kCostFP4Dn, sB)};
+    return UnitList{(uint32_t)n_uni * (H / 256) * pieces_of(sA, kSppDn), unit_cost(kCostFP3, sA, kSppDn),
+                    (uint32_t)(H / 64) * pieces_of(sB, kSppDn), unit_cost(kCostFP4Dn, sB, kSppDn)};
 }
 
 // ------------------------------------------------------------------ K2: gate/up
@@ -537,7 +542,7 @@ struct GuTask {
 };
 
 __device__ __forceinline__ GuTask gu_unit(uint32_t u, const Route& r, const LayerMaps& m) {
-    const int I = m.I, rb2 = I / 256, sA = m.H / stage_k(2), pA = pieces_of(sA);
+    const int I = m.I, rb2 = I / 256, sA = m.H / stage_k(2), pA = pieces_of(sA, kSppGu);
     const uint32_t nA = (uint32_t)(2 * r.n_uni * rb2 * pA);
     GuTask k;
     if (u < nA) {
@@ -547,18 +552,18 @@ __device__ __forceinline__ GuTask gu_unit(uint32_t u, const Route& r, const Laye
         k.fp4 = 0;
         k.row0 = (t % rb2) * 256;
         k.off = r.slot[k.mat >> 1] * m.mb2 + tile_offset(2, k.row0, m.H);
-        k.s_beg = piece_begin(sA, k.piece);
-        k.s_end = piece_begin(sA, k.piece + 1);
+        k.s_beg = piece_begin(sA, kSppGu, k.piece);
+        k.s_end = piece_begin(sA, kSppGu, k.piece + 1);
     } else {
-        const int sB = m.H / stage_k(4), pB = pieces_of(sB), rb4 = I / 64;
+        const int sB = m.H / stage_k(4), pB = pieces_of(sB, kSppGu), rb4 = I / 64;
         const int t4 = (int)(u - nA) / pB;
         k.piece = (int)(u - nA) - t4 * pB;
         k.mat = 2 * r.n_uni + t4 / rb4;
         k.fp4 = 1;
         k.row0 = (t4 % rb4) * 64;
         k.off = tile_offset(4, k.row0, m.H);
-        k.s_beg = piece_begin(sB, k.piece);
-        k.s_end = piece_begin(sB, k.piece + 1);
+        k.s_beg = piece_begin(sB, kSppGu, k.piece);
+        k.s_end = piece_begin(sB, kSppGu, k.piece + 1);
     }
     return k;
 }
@@ -702,7 +707,7 @@ __global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__
         const size_t pstride = A.ws.gu_piece / 4;
         // the fixed pieces of the item's gate and up tasks (routed: FP2, H/256 stages; shared: FP4,
         // H/512 stages), added in piece order
-        const int np = pieces_of(j < n_uni ? A.H / stage_k(2) : A.H / stage_k(4));
+        const int np = pieces_of(j < n_uni ? A.H / stage_k(2) : A.H / stage_k(4), kSppGu);
         float4 ga[kHpackV], ua[kHpackV];
 #pragma unroll
         for (int v = 0; v < kHpackV; v++) {
@@ -793,7 +798,7 @@ struct DnTask {
 };
 
 __device__ __forceinline__ DnTask dn_unit(uint32_t u, const Route& r, const LayerMaps& m) {
-    const int H = m.H, rb3 = H / 256, sA = m.I / stage_k(3), pA = pieces_of(sA);
+    const int H = m.H, rb3 = H / 256, sA = m.I / stage_k(3), pA = pieces_of(sA, kSppDn);
     const uint32_t nA = (uint32_t)(r.n_uni * rb3 * pA);
     DnTask k;
     if (u < nA) {
@@ -803,18 +808,18 @@ __device__ __forceinline__ DnTask dn_unit(uint32_t u, const Route& r, const Laye
         k.fp4 = 0;
         k.row0 = (t % rb3) * 256;
         k.off = r.slot[k.item] * m.mb3 + tile_offset(3, k.row0, m.I);
-        k.s_beg = piece_begin(sA, k.piece);
-        k.s_end = piece_begin(sA, k.piece + 1);
+        k.s_beg = piece_begin(sA, kSppDn, k.piece);
+        k.s_end = piece_begin(sA, kSppDn, k.piece + 1);
     } else {
-        const int sB = m.I / stage_k(4), pB = pieces_of(sB);
+        const int sB = m.I / stage_k(4), pB = pieces_of(sB, kSppDn);
         const int t4 = (int)(u - nA) / pB;
         k.piece = (int)(u - nA) - t4 * pB;
         k.item = r.n_uni;
         k.fp4 = 1;
         k.row0 = t4 * 64;
         k.off = tile_offset(4, k.row0, m.I);
-        k.s_beg = piece_begin(sB, k.piece);
-        k.s_end = piece_begin(sB, k.piece + 1);
+        k.s_beg = piece_begin(sB, kSppDn, k.piece);
+        k.s_end = piece_begin(sB, kSppDn, k.piece + 1);
     }
     return k;
 }
@@ -962,7 +967,7 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(const __grid_consta
         wsel[j][tok] = wv;
     }
     // the fixed pieces of the routed (FP3, I/256 stages) and shared (FP4, I/512 stages) down tasks
-    const int H = A.H, np_r = pieces_of(A.I / stage_k(3)), np_s = pieces_of(A.I / stage_k(4));
+    const int H = A.H, np_r = pieces_of(A.I / stage_k(3), kSppDn), np_s = pieces_of(A.I / stage_k(4), kSppDn);
     __syncthreads();
     grid_dep_wait();  // the down kernel's outputs
     const int o = blockIdx.x * kCombineThreads + threadIdx.x;
