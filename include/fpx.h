@@ -237,7 +237,7 @@ int moe_layer_decode_tiered(const moe_layer* layer, const moe_tiers* tiers, cons
  * status word is copied to dev_status (nullable, device, 4-byte aligned) at the end of the call.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  *   - Shapes whose moe_workspace_bytes() exceeds 16 MiB fail with FPX_ESPACE (the decode shapes,
- *     H = 4096, I = 2048, E = 256, q <= 4, k <= 8, need at most 13.7 MB).
+ *     H = 4096, I = 2048, E = 256, q <= 4, k <= 8, need at most 9.4 MB).
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *     that device current; make that first call before capturing a stream into a graph.
  *   - Every call on a device shares the one array, which keeps the previous call's contents: calls
