@@ -10,7 +10,8 @@
 //
 // Pipeline (one stream, no host synchronisation):
 //   k_to_f16   x (bfloat16) -> binary16 rows scaled by a per-token power of two (exact), + shifts
-//   k_plogits  logits[t][e] = sum_h R[e][h] x[t][h], binary32, fixed order over h
+//   k_rsplit / k_plogits_tc  logits[t][e] = sum_h R[e][h] x[t][h] on the tcgen05 tensor cores: the
+//              binary32 router split into three exact bfloat16 parts, binary32 sums
 //   k_ptopk    one warp per token: top-k by logit (ties to the lower index), sigmoid weights
 //   k_phist / k_pscan / k_pscatter: stable counting sort of the T*k pairs p = t*k + r by expert:
 //              perm[s] = p in expert order (p ascending within an expert), inv[p] = s, offsets[E+1]
@@ -44,7 +45,7 @@ constexpr int kPMaxK = 8;
 struct PWs {
     size_t status, logits, idx, w, counts, offsets, perm, inv, x16, shx;
     size_t g, u, gsh, ush, h16, shh, hsh16, shsh, yp, ysh, xg, gshift, tcu_gu, tcu_dn, ntc;
-    size_t xs4, rexp, tcu_sgu, tcu_sdn, total;
+    size_t xs4, rexp, tcu_sgu, tcu_sdn, rsplit, total;
 };
 
 inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -82,6 +83,7 @@ PWs pws_layout(int64_t T, int64_t E, int64_t H, int64_t I, int64_t k) {
     w.rexp = o; o = up256(o + 4 * (2 * I + H));                    // FP4 row exponents: gate, up, down
     w.tcu_sgu = o; o = up256(o + 16 * ((T + 127) / 128) * (I / 256));  // shared expert's units
     w.tcu_sdn = o; o = up256(o + 16 * ((T + 127) / 128) * (H / 256));
+    w.rsplit = o; o = up256(o + 2 * 3 * E * H);                    // router weights as three bfloat16 parts
     w.total = o;
     return w;
 }
@@ -122,56 +124,6 @@ __global__ void __launch_bounds__(256) k_to_f16(const void* __restrict__ src, in
 }
 
 // ------------------------------------------------------------------ routing
-
-// logits[t][e] = sum_h R[e][h] x[t][h] (binary32; the sum runs over h in order for every (t, e), so
-// equal router rows give equal logits). Tile: 64 tokens x 64 experts, 16 x 16 threads of 4 x 4; the
-// next 32-wide slice of h is loaded into registers while the current one is used.
-__global__ void __launch_bounds__(256) k_plogits(const float* __restrict__ R, const uint16_t* __restrict__ x, int T,
-                                                 int E, int H, float* __restrict__ logits) {
-    __shared__ float xs[2][32][65];
-    __shared__ float rs[2][32][65];
-    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-    const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
-    float acc[4][4] = {};
-    float xv[8], rv[8];
-    auto load = [&](int h0) {
-#pragma unroll
-        for (int v = 0; v < 8; v++) {
-            const int i = threadIdx.x + 256 * v, rr = i / 32, kk = i % 32;
-            const int t = t0 + rr, e = e0 + rr;
-            xv[v] = t < T ? __uint_as_float((uint32_t)x[(size_t)t * H + h0 + kk] << 16) : 0.f;
-            rv[v] = e < E ? R[(size_t)e * H + h0 + kk] : 0.f;
-        }
-    };
-    load(0);
-    for (int h0 = 0, buf = 0; h0 < H; h0 += 32, buf ^= 1) {
-#pragma unroll
-        for (int v = 0; v < 8; v++) {
-            const int i = threadIdx.x + 256 * v, rr = i / 32, kk = i % 32;
-            xs[buf][kk][rr] = xv[v];
-            rs[buf][kk][rr] = rv[v];
-        }
-        __syncthreads();
-        if (h0 + 32 < H) load(h0 + 32);
-#pragma unroll 8
-        for (int kk = 0; kk < 32; kk++) {
-            float a[4], b[4];
-#pragma unroll
-            for (int i = 0; i < 4; i++) { a[i] = xs[buf][kk][ty + 16 * i]; b[i] = rs[buf][kk][tx + 16 * i]; }
-#pragma unroll
-            for (int i = 0; i < 4; i++)
-#pragma unroll
-                for (int j = 0; j < 4; j++) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; i++)
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const int t = t0 + ty + 16 * i, e = e0 + tx + 16 * j;
-            if (t < T && e < E) logits[(size_t)t * E + e] = acc[i][j];
-        }
-}
 
 // One warp per token.
 __global__ void __launch_bounds__(256) k_ptopk(const float* __restrict__ logits, int T, int E, int k, int32_t* idx,
@@ -892,6 +844,140 @@ __global__ void __launch_bounds__(256) k_pcombine(const float* __restrict__ yp, 
     out[o] = acc + ysh[o];
 }
 
+// ------------------------------------------------------------------ router logits on tcgen05
+
+// logits[t][e] = sum_h R[e][h] x[t][h] on the tensor cores: R (binary32) is split into three
+// bfloat16 parts R = R1 + R2 + R3 (exact: 3 x 8 significant bits), every product of a part with the
+// bfloat16 activation is exact in binary32, and the tensor core sums the three parts' products over h
+// in binary32. The sum runs in the same order for every (t, e), so equal router rows give equal
+// logits. CTA = 128 experts x 64 tokens: warp 0 streams 64-wide K slabs of the three parts and of x
+// (2-D TMA tiles, 128-byte swizzle) into a 3-stage ring, warp 1 issues 3 x 4 MMAs of 128 x 64 x 16
+// per slab (bfloat16 inputs, binary32 accumulator in tensor memory), warps 2..5 write the logits.
+constexpr int kLgM = 128, kLgN = 64, kLgStages = 3, kLgThreads = 6 * 32;
+constexpr int kLgA = kLgM * 128, kLgB = kLgN * 128;               // one part's tile, the token tile
+constexpr int kLgStage = 3 * kLgA + kLgB;
+constexpr int kLgSmem = kLgStages * kLgStage + 1024;
+static_assert(kLgSmem <= 227 * 1024 && kLgStage % 1024 == 0, "logit GEMM shared memory");
+
+// r[i] -> three bfloat16 parts (rows [p][E][H] of rs): r1 = RN(r), r2 = RN(r - r1), r3 = RN(r - r1 - r2)
+__global__ void __launch_bounds__(256) k_rsplit(const float* __restrict__ r, int64_t n, __nv_bfloat16* __restrict__ rs) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float v = r[i];
+    const __nv_bfloat16 a = __float2bfloat16_rn(v);
+    const float d1 = v - __bfloat162float(a);  // exact (Sterbenz / the low bits of v)
+    const __nv_bfloat16 b = __float2bfloat16_rn(d1);
+    const __nv_bfloat16 c = __float2bfloat16_rn(d1 - __bfloat162float(b));
+    rs[i] = a;
+    rs[n + i] = b;
+    rs[2 * n + i] = c;
+}
+
+struct LgArgs {
+    CUtensorMap amap;  // rs: bfloat16 [3 E][H], box 64 x 128
+    CUtensorMap bmap;  // x: bfloat16 [T][H], box 64 x 64
+    int T, E, H;
+    float* logits;
+    int32_t* status;
+};
+
+__global__ void __launch_bounds__(kLgThreads, 1) k_plogits_tc(const __grid_constant__ LgArgs A) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint64_t full[kLgStages], empty[kLgStages], done;
+    __shared__ uint32_t taddr_s;
+    uint8_t* base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int e0 = blockIdx.x * kLgM, t0 = blockIdx.y * kLgN, nslab = A.H / 64;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kLgStages; i++) { mbar_init(full + i, 1); mbar_init(empty + i, 1); }
+        mbar_init(&done, 1);
+    }
+    fence_barrier_init();
+    __syncthreads();
+    if (warp == 1) tmem_alloc(smem_u32(&taddr_s), kLgN);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t taddr = taddr_s;
+    if (warp == 0) {
+        if (lane == 0) {
+            bool live = true;
+            for (int j = 0; j < nslab && live; j++) {
+                const int st = j % kLgStages;
+                if (j >= kLgStages && !mbar_wait(empty + st, ((j / kLgStages) + 1) & 1)) { live = false; break; }
+                uint8_t* sb = base + st * kLgStage;
+                mbar_expect_tx(full + st, kLgStage);
+                for (int p = 0; p < 3; p++) tma_load_2d(sb + p * kLgA, &A.amap, 64 * j, p * A.E + e0, full + st);
+                tma_load_2d(sb + 3 * kLgA, &A.bmap, 64 * j, t0, full + st);
+            }
+            if (!live) flag(A.status, FPX_ETIMEOUT);
+            const int j0 = nslab > kLgStages ? nslab - kLgStages : 0;
+            for (int j = j0; j < nslab; j++) mbar_wait(full + j % kLgStages, (j / kLgStages) & 1);  // no copy outlives the CTA
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // binary32 accumulator, bfloat16 A and B (bits 7-9 and 10-12 = 1), K-major, N / 8, M / 16
+            const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kLgN >> 3) << 17) | ((uint32_t)(kLgM >> 4) << 24);
+            bool live = true;
+            for (int j = 0; j < nslab && live; j++) {
+                const int st = j % kLgStages;
+                if (!mbar_wait(full + st, (j / kLgStages) & 1)) { live = false; break; }
+                tc_fence_after();
+                const uint32_t sb = smem_u32(base + st * kLgStage);
+                const uint64_t bd = sw128_desc(sb + 3 * kLgA);
+#pragma unroll
+                for (int kk = 0; kk < 4; kk++)
+#pragma unroll
+                    for (int p = 0; p < 3; p++)
+                        tc_mma_f16(taddr, sw128_desc(sb + p * kLgA) + 2u * kk, bd + 2u * kk, idesc, (j | kk | p) != 0);
+                tc_commit(smem_u32(empty + st));
+            }
+            if (!live) flag(A.status, FPX_ETIMEOUT);
+            tc_commit(smem_u32(&done));
+        }
+    } else {
+        // epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31 = experts e0 + 32 (w % 4) + lane
+        const int q = warp & 3;
+        const bool ok = __any_sync(0xffffffffu, mbar_wait(&done, 0));
+        if (!ok) { if (lane == 0) flag(A.status, FPX_ETIMEOUT); }
+        else {
+            tc_fence_after();
+            const int e = e0 + 32 * q + lane;
+            for (int c0 = 0; c0 < kLgN; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    const int t = t0 + c0 + i;
+                    if (t < A.T && e < A.E) A.logits[(size_t)t * A.E + e] = v[i];
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        mbar_wait(&done, 0);  // every MMA has completed
+        tmem_dealloc(taddr, kLgN);
+    }
+}
+
+// A 2-D tensor map over a bfloat16 [rows][K] matrix with box 64 x box_rows and the 128-byte swizzle;
+// rows past the end read as zeros.
+int make_bf16_map(CUtensorMap* m, const void* p, int64_t rows, int64_t K, int box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return FPX_ECUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
+    cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t es[2] = {1u, 1u};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(p), dims, strides, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FPX_OK : FPX_ECUDA;
+}
+
 // A 2-D tensor map over B (binary16 [rows][K]) for the tensor-core GEMM: boxes of 64 elements x 16
 // rows with the 128-byte swizzle; rows past the end read as zeros.
 int make_b_map(CUtensorMap* m, const __half* B, int64_t rows, int64_t K) {
@@ -976,7 +1062,16 @@ int moe_layer_prefill(const moe_layer* L, const uint16_t* x, int T, int k, float
     if (cudaMemsetAsync(status, 0, 16, s) != cudaSuccess || cudaMemsetAsync(counts, 0, 4 * (E + 1), s) != cudaSuccess)
         return FPX_ECUDA;
     k_to_f16<false><<<T, 256, 0, s>>>(x, H, x16, shx);
-    k_plogits<<<dim3((T + 63) / 64, (E + 63) / 64), 256, 0, s>>>(L->router, x, T, E, H, logits);
+    {
+        __nv_bfloat16* rs = reinterpret_cast<__nv_bfloat16*>(b + W.rsplit);
+        const int64_t n = (int64_t)E * H;
+        k_rsplit<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(L->router, n, rs);
+        LgArgs la{};
+        la.T = T; la.E = E; la.H = H; la.logits = logits; la.status = status;
+        if (make_bf16_map(&la.amap, rs, 3 * (int64_t)E, H, kLgM) || make_bf16_map(&la.bmap, x, T, H, kLgN)) return FPX_ECUDA;
+        if (cudaFuncSetAttribute(k_plogits_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kLgSmem) != cudaSuccess) return FPX_ECUDA;
+        k_plogits_tc<<<dim3((E + kLgM - 1) / kLgM, (T + kLgN - 1) / kLgN), kLgThreads, kLgSmem, s>>>(la);
+    }
     k_ptopk<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, idx, w);
     k_phist<<<(P + 255) / 256, 256, 0, s>>>(idx, P, E, counts, status);
     k_pscan<<<1, 1024, 0, s>>>(counts, E, offsets);

@@ -265,13 +265,16 @@ int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int
                      void* stream);
 
 /* Workspace bytes moe_layer_prefill needs for T tokens and top-k (16-byte aligned; about
- * T*k*(10 I + 6 H) + T*(10 I + 8 H) bytes: 0.66 GB at T = 2048, k = 6, H = 4096, I = 2048).
+ * T*k*(10 I + 6 H) + T*(10 I + 8 H) + 6 E H bytes: 0.67 GB at T = 2048, k = 6, H = 4096, I = 2048,
+ * E = 256).
  * 0 for invalid arguments. */
 size_t moe_prefill_workspace_bytes(const moe_layer* layer, int T, int k);
 
 /* Batched prefill of one MoE layer over T tokens (T >= 1, 1 <= k <= 8, k <= E <= 1024):
- *   - route every token as moe_route_topk does (binary32 logits, top-k by logit with ties to the
- *     lower expert index, sigmoid weights renormalised over the k selected);
+ *   - route every token by the rule of moe_route_topk (top-k by logit with ties to the lower expert
+ *     index, sigmoid weights renormalised over the k selected) on binary32 logits summed on the
+ *     tensor cores from exact products (the router split into three bfloat16 parts); the summation
+ *     order differs from moe_route_topk's, so logits agree to binary32 rounding, not bit for bit;
  *   - stable argsort of the T*k pairs p = t*k + r by expert: perm[s] = p lists the pairs in expert
  *     order, p ascending within an expert; offsets[e] .. offsets[e+1] is expert e's range;
  *   - run each routed expert once over its pairs (grouped GEMMs on the tensor cores over the same
