@@ -733,13 +733,22 @@ __global__ void __launch_bounds__(1024) k_tcunits(const int32_t* __restrict__ of
 template <int PERM>
 __global__ void __launch_bounds__(256) k_ph(const float* __restrict__ g, const float* __restrict__ u, int L,
                                             __half* __restrict__ h16, int32_t* __restrict__ shift) {
+    __shared__ __align__(16) float h_s[4608];  // the row's h (L <= 4608), so g and u are read once
     __shared__ float red[8];
     __shared__ int sh_s;
     const size_t r = blockIdx.x;
     float m = 0.f;
-    for (int i = threadIdx.x; i < L; i += blockDim.x) {
-        const float a = g[r * L + i], b = u[r * L + i];
-        m = fmaxf(m, fabsf((a / (1.0f + expf(-a))) * b));
+    const float4* g4 = reinterpret_cast<const float4*>(g + r * L);
+    const float4* u4 = reinterpret_cast<const float4*>(u + r * L);
+    for (int i = threadIdx.x; i < L / 4; i += blockDim.x) {
+        const float4 a = __ldcs(g4 + i), b = __ldcs(u4 + i);
+        float4 h;
+        h.x = (a.x / (1.0f + expf(-a.x))) * b.x;
+        h.y = (a.y / (1.0f + expf(-a.y))) * b.y;
+        h.z = (a.z / (1.0f + expf(-a.z))) * b.z;
+        h.w = (a.w / (1.0f + expf(-a.w))) * b.w;
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w))));
+        reinterpret_cast<float4*>(h_s)[i] = h;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -756,10 +765,7 @@ __global__ void __launch_bounds__(256) k_ph(const float* __restrict__ g, const f
     for (int gi = threadIdx.x; gi < L / 16; gi += blockDim.x) {
         float v[16];
 #pragma unroll
-        for (int j = 0; j < 16; j++) {
-            const float a = g[r * L + 16 * gi + j], b = u[r * L + 16 * gi + j];
-            v[j] = ((a / (1.0f + expf(-a))) * b) * sc;
-        }
+        for (int j = 0; j < 16; j++) v[j] = h_s[16 * gi + j] * sc;
         uint32_t o[8];
 #pragma unroll
         for (int p = 0; p < 8; p++) {
@@ -1016,7 +1022,7 @@ int moe_layer_prefill(const moe_layer* L, const uint16_t* x, int T, int k, float
                       void* stream) {
     if (!L || T < 1 || k < 1 || k > kPMaxK || L->E < k || L->E > kRouteMaxE) return FPX_EINVAL;
     const int H = L->H, I = L->I, E = L->E;
-    if (H < 512 || I < 512 || H % 512 || I % 512) return FPX_EINVAL;
+    if (H < 512 || I < 512 || H % 512 || I % 512 || I > 4608) return FPX_EINVAL;
     if ((int64_t)T * k > INT32_MAX / 2 || (int64_t)T * H > INT32_MAX) return FPX_EINVAL;
     if (!x || !y || !ws || !L->router || !L->gate || !L->up || !L->down || !L->sh_gate || !L->sh_up || !L->sh_down)
         return FPX_EINVAL;
