@@ -1183,10 +1183,13 @@ __device__ __forceinline__ uint32_t word_of(const uint4& c) {
 // bytes per chunk in the table) and the offset quad from oq (64 bytes per chunk).
 __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint32_t (&a0)[8], const uint32_t (&a8)[8], const uint4& b0,
                                           const uint4& b1, const float4& c4) {
+    // two accumulator chains (K steps 0, 2 and 1, 3) joined at the end: half the dependent MMA latency
+    float acc2[4];
     mma_c(acc, a0[0], a8[0], a0[1], a8[1], b0.x, b0.y, c4);
-    mma_acc(acc, a0[2], a8[2], a0[3], a8[3], b0.z, b0.w);
+    mma_c(acc2, a0[2], a8[2], a0[3], a8[3], b0.z, b0.w, make_float4(0.f, 0.f, 0.f, 0.f));
     mma_acc(acc, a0[4], a8[4], a0[5], a8[5], b1.x, b1.y);
-    mma_acc(acc, a0[6], a8[6], a0[7], a8[7], b1.z, b1.w);
+    mma_acc(acc2, a0[6], a8[6], a0[7], a8[7], b1.z, b1.w);
+    acc[0] += acc2[0]; acc[1] += acc2[1]; acc[2] += acc2[2]; acc[3] += acc2[3];
 }
 
 template <int C>
