@@ -848,11 +848,22 @@ __device__ __forceinline__ void box_tiles(uint32_t row, const LaneOfs& L, uint32
             const float d0 = i == 0 ? row_decode<FMT, 0, C>(ra, L, magic, a0, g0, bad) : row_decode<FMT, 16 * P, C>(ra, L, magic, a0, g0, bad);
             const float d8 = i == 0 ? row_decode<FMT, 8 * P, C>(ra, L, magic, a8, g8, bad) : row_decode<FMT, 24 * P, C>(ra, L, magic, a8, g8, bad);
             float acc[4];
-            mma_c(acc, a0[0], a8[0], a0[1], a8[1], b0.x, b0.y, c4);
-            mma_acc(acc, a0[2], a8[2], a0[3], a8[3], b0.z, b0.w);
-            mma_acc(acc, a0[4], a8[4], a0[5], a8[5], b1.x, b1.y);
-            mma_acc(acc, a0[6], a8[6], a0[7], a8[7], b1.z, b1.w);
-            if constexpr (FMT == 3) plane_mma(acc, g0, g8, h0, h1);
+            if constexpr (FMT == 3) {
+                mma_c(acc, a0[0], a8[0], a0[1], a8[1], b0.x, b0.y, c4);
+                mma_acc(acc, a0[2], a8[2], a0[3], a8[3], b0.z, b0.w);
+                mma_acc(acc, a0[4], a8[4], a0[5], a8[5], b1.x, b1.y);
+                mma_acc(acc, a0[6], a8[6], a0[7], a8[7], b1.z, b1.w);
+                plane_mma(acc, g0, g8, h0, h1);
+            } else {
+                // two accumulator chains (alternate K steps) joined at the end: half the dependent
+                // latency (measured: FP2 q = 4 GEMV 3.10 -> 3.18 TB/s; FP3's eight-MMA chain gained nothing)
+                float acc2[4];
+                mma_c(acc, a0[0], a8[0], a0[1], a8[1], b0.x, b0.y, c4);
+                mma_c(acc2, a0[2], a8[2], a0[3], a8[3], b0.z, b0.w, make_float4(0.f, 0.f, 0.f, 0.f));
+                mma_acc(acc, a0[4], a8[4], a0[5], a8[5], b1.x, b1.y);
+                mma_acc(acc2, a0[6], a8[6], a0[7], a8[7], b1.z, b1.w);
+                acc[0] += acc2[0]; acc[1] += acc2[1]; acc[2] += acc2[2]; acc[3] += acc2[3];
+            }
             y[i][0] = fmaf(d0, acc[0], y[i][0]);
             y[i][1] = fmaf(d0, acc[1], y[i][1]);
             y[i][2] = fmaf(d8, acc[2], y[i][2]);
