@@ -33,11 +33,27 @@
 
 namespace fpx {
 
-constexpr int kWarps = 8;  // consumer warps of a tensor-core CTA (plus one producer warp)
+constexpr int kWarps = 8;  // consumer warps of a dense-GEMV CTA (plus producer warps)
 
-// Barrier among the kWarps consumer warps only (the producer warp does not take part).
+// Barrier among the kWarps consumer warps only (the producer warps do not take part).
 __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+}
+
+// The MoE layer's streaming CTAs (gate/up, down): kLWarps consumer warps plus one producer warp. Each
+// consumer warp decodes kLTiles 16-row tiles of every FP2 / FP3 box (256 rows). A warp loads the
+// activation fragments of a chunk once for all its tiles, so 16 warps of one tile (four per scheduler)
+// measured slower than 8 warps of two (k_gate_up 36.8 against 35.2 us): the extra table loads cost
+// more than the added latency hiding gained.
+constexpr int kLWarps = 8;
+constexpr int kLTiles = 256 / 16 / kLWarps;
+constexpr int kLThreads = (kLWarps + 1) * 32;
+constexpr int kFp4Parts = kLWarps / 4;  // FP4 boxes (64 rows = 4 tiles): warps split the 8 chunks
+static_assert(kLTiles * 16 * kLWarps == 256 && 8 % kFp4Parts == 0, "layer CTA geometry");
+
+// Barrier among the kLWarps consumer warps of a layer CTA.
+__device__ __forceinline__ void layer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kLWarps * 32) : "memory");
 }
 
 // ------------------------------------------------------------------ compile-time binary16 bits
@@ -880,7 +896,6 @@ __device__ __forceinline__ void report_bad(uint32_t bad, int32_t* st) {
 
 // ------------------------------------------------------------------ per-warp TMA ring (dense GEMV)
 
-constexpr int kCtaThreads = (kWarps + 1) * 32;  // + one producer warp that issues every TMA load
 constexpr int kStages = 4;           // TMA ring depth per warp
 constexpr int kSlotBytes = 4352;     // one stage: 16 FP4 rows x 272 B, or an FP2 / FP3 box
 constexpr int kRingBytes = kWarps * kStages * kSlotBytes;
@@ -981,17 +996,18 @@ __device__ inline void init_rings(const Smem& s) {
 // so small per-warp boxes cannot keep up with HBM, and the issuing must stay off the consumers'
 // path. The MoE kernels stage one large box per step for the whole CTA: FP2/FP3 boxes of 256 rows
 // (20 and 28 KB), FP4 boxes of 64 rows (17 KB), in a ring of NS slots of SB bytes filled by one
-// producer thread (warp kWarps). All kWarps consumer warps read every stage:
-//   FP2/FP3 box: warp w decodes rows [32w, 32w + 32) (two 16-row tiles), all 4 chunks.
-//   FP4 box: warp w decodes rows [16 (w % 4), +16), chunks 4 (w / 4) .. 4 (w / 4) + 3; the two
-//   partial sums of a row (warps w, w + 4) are added in warp order at the end of the task.
+// producer thread (warp kLWarps). All kLWarps consumer warps read every stage:
+//   FP2/FP3 box: warp w decodes rows [16 kLTiles w, +16 kLTiles) (kLTiles 16-row tiles), all 4 chunks.
+//   FP4 box: warp w decodes rows [16 (w % 4), +16), chunks 8 / kFp4Parts consecutive from
+//   (8 / kFp4Parts) (w / 4); the kFp4Parts partial sums of a row (warps w % 4, w % 4 + 4, ...) are
+//   added in warp order at the end of the task.
 constexpr int kCtaRing = 143360;  // 7 x 20480 (FP2 boxes) = 5 x 28672 (FP3 boxes)
 
 __host__ __device__ constexpr int stage_rows(int fmt) { return fmt == 4 ? 64 : 256; }
 __host__ __device__ constexpr int stage_bytes(int fmt) { return box_bytes(fmt) * stage_rows(fmt); }
 // weights of a row covered by one box
 __host__ __device__ constexpr int stage_k(int fmt) { return 64 * box_chunks(fmt); }
-static_assert(stage_rows(2) == 32 * kWarps && stage_rows(4) * 2 == 16 * kWarps, "rows per warp");
+static_assert(stage_rows(2) == 16 * kLTiles * kLWarps && stage_rows(4) == 64, "rows per warp");
 
 template <int NS, int SB>
 struct CtaRing {
@@ -999,7 +1015,7 @@ struct CtaRing {
     static constexpr int kBytes = NS * SB;
     uint8_t* slots;
     uint64_t* full;   // arrival count 1 (the producer's expect_tx) + the box's transaction bytes
-    uint64_t* empty;  // arrival count kWarps
+    uint64_t* empty;  // arrival count kLWarps
 
     __device__ __forceinline__ uint8_t* slot(uint32_t n) const { return slots + (size_t)(n % NS) * SB; }
     __device__ __forceinline__ uint64_t* bar(uint32_t n) const { return full + (n % NS); }
@@ -1054,12 +1070,12 @@ struct CtaSmem {
     uint8_t* ring;
     uint64_t* bars;  // 256 bytes: full[NS], empty[NS], then (at bars + 16) the tables' barrier
     uint2* zero;     // kZeroBytes of zeros
-    float* red;      // kWarps * 64 floats: cross-warp partial sums
+    float* red;      // kLWarps * 64 floats: cross-warp partial sums
     uint8_t* tabs;   // activation tables, copied from global memory
     uint64_t* tbar;
 };
 
-constexpr int kRedBytes = kWarps * 64 * 4;
+constexpr int kRedBytes = kLWarps * 64 * 4;
 
 // ring (ring_bytes), barriers, zero area, reduction area, tables (tab_bytes), alignment slack
 __host__ __device__ constexpr size_t cta_smem_bytes(int ring_bytes, int tab_bytes) {
@@ -1085,7 +1101,7 @@ template <int NS, int SB>
 __device__ inline CtaRing<NS, SB> cta_init(const CtaSmem& s) {
     CtaRing<NS, SB> R{s.ring, s.bars, s.bars + NS};
     if (threadIdx.x < NS) mbar_init(R.full + threadIdx.x, 1);
-    else if (threadIdx.x < 2 * NS) mbar_init(R.empty + (threadIdx.x - NS), kWarps);
+    else if (threadIdx.x < 2 * NS) mbar_init(R.empty + (threadIdx.x - NS), kLWarps);
     else if (threadIdx.x == 2 * NS) mbar_init(s.tbar, 1);
     for (int i = threadIdx.x; i < kZeroBytes / 16; i += blockDim.x) reinterpret_cast<uint4*>(s.zero)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_barrier_init();
@@ -1149,27 +1165,27 @@ __device__ __forceinline__ float scale_of(const uint2& s) {
 
 // One consumer warp's share of a staged FP2/FP3 box (rows g and g + 8 of its two 16-row tiles): the
 // code words and scales, loaded in one pass so the ring slot can be released before the MMAs run.
-template <int FMT>
+template <int FMT, int NT>
 struct Frag;
-template <>
-struct Frag<2> {
-    uint4 c[2][2];  // [tile][row g / g + 8]: words of chunks 0..3
-    uint2 s[2][2];
+template <int NT>
+struct Frag<2, NT> {
+    uint4 c[NT][2];  // [tile][row g / g + 8]: words of chunks 0..3
+    uint2 s[NT][2];
 };
-template <>
-struct Frag<3> {
-    uint2 c[2][2][3];  // words W0..W5
-    uint2 s[2][2];
+template <int NT>
+struct Frag<3, NT> {
+    uint2 c[NT][2][3];  // words W0..W5
+    uint2 s[NT][2];
 };
 
 // `row` = the warp's first row + g; t = lane % 4.
-template <int FMT>
-__device__ __forceinline__ void frag_load(Frag<FMT>& f, uint32_t slot, int row, int t) {
+template <int FMT, int NT>
+__device__ __forceinline__ void frag_load(Frag<FMT, NT>& f, uint32_t slot, int row, int t) {
     constexpr int CB = box_code_bytes(FMT);
     const uint32_t cb = slot + (uint32_t)(row * CB + (FMT == 2 ? 16 : 24) * t);
     const uint32_t sb = slot + (uint32_t)(box_scale_offset(FMT) + row * 16 + 8 * (t >> 1));
 #pragma unroll
-    for (int i = 0; i < 2; i++) {
+    for (int i = 0; i < NT; i++) {
 #pragma unroll
         for (int h = 0; h < 2; h++) {
             const uint32_t r = (uint32_t)(16 * i + 8 * h);
@@ -1210,13 +1226,13 @@ __device__ __forceinline__ float4 oq_quad(uint32_t oq) {
 }
 
 // Chunks C0 and C0 + 1 of a fragment, accumulated into y[tile][4] (rows g, g + 8 as in box_tiles).
-template <int FMT, int C0>
-__device__ __forceinline__ void frag_mma(const Frag<FMT>& f, uint32_t b, uint32_t oq, uint32_t magic, float (&y)[2][4]) {
+template <int FMT, int C0, int NT>
+__device__ __forceinline__ void frag_mma(const Frag<FMT, NT>& f, uint32_t b, uint32_t oq, uint32_t magic, float (&y)[NT][4]) {
     const uint4 b0 = lds128<C0 * 512>(b), b1 = lds128<C0 * 512 + 16>(b);
     const uint4 e0 = lds128<(C0 + 1) * 512>(b), e1 = lds128<(C0 + 1) * 512 + 16>(b);
     const float4 q0 = oq_quad<C0>(oq), q1 = oq_quad<C0 + 1>(oq);
 #pragma unroll
-    for (int i = 0; i < 2; i++) {
+    for (int i = 0; i < NT; i++) {
         uint32_t a0[8], a8[8], c0[8], c8[8];
         if constexpr (FMT == 2) {
             decode_fp2(word_of<C0>(f.c[i][0]), magic, a0);
@@ -1248,48 +1264,51 @@ __device__ __forceinline__ void frag_mma(const Frag<FMT>& f, uint32_t b, uint32_
 // lane's table entry and offset quad addresses for the task's stage s_first (advanced by b_step and
 // 256 bytes per stage). On a timeout the warp stops waiting and releasing (so the producer gives up
 // too) and ok turns false; the caller reports it.
-template <int FMT, class RING>
-__device__ __forceinline__ bool frag_step(const RING& R, const Frag<FMT>& cur, Frag<FMT>& nxt, typename RING::Pos& p, int& left,
-                                          int row, int t, uint32_t& b, uint32_t b_step, uint32_t& q, uint32_t magic,
-                                          float (&y)[2][4], bool& ok) {
+template <int FMT, int NT, class RING>
+__device__ __forceinline__ bool frag_step(const RING& R, const Frag<FMT, NT>& cur, Frag<FMT, NT>& nxt, typename RING::Pos& p,
+                                          int& left, int row, int t, uint32_t& b, uint32_t b_step, uint32_t& q, uint32_t magic,
+                                          float (&y)[NT][4], bool& ok) {
     if (ok) R.release_at(p);
     R.next(p);
     const bool more = --left > 0;
-    frag_mma<FMT, 0>(cur, b, q, magic, y);
+    frag_mma<FMT, 0, NT>(cur, b, q, magic, y);
     if (more && ok) {
         ok = R.wait_at(p);
-        if (ok) frag_load<FMT>(nxt, R.slot_at(p), row, t);
+        if (ok) frag_load<FMT, NT>(nxt, R.slot_at(p), row, t);
     }
-    frag_mma<FMT, 2>(cur, b, q, magic, y);
+    frag_mma<FMT, 2, NT>(cur, b, q, magic, y);
     b += b_step;
     q += 256u;
     return more;
 }
 
-template <int FMT, class RING>
+template <int FMT, int NT, class RING>
 __device__ __forceinline__ void frag_stages(const RING& R, typename RING::Pos& p, int count, int row, int t, uint32_t b,
-                                            uint32_t b_step, uint32_t q, uint32_t magic, float (&y)[2][4], bool& ok) {
-    Frag<FMT> fa, fb;
+                                            uint32_t b_step, uint32_t q, uint32_t magic, float (&y)[NT][4], bool& ok) {
+    Frag<FMT, NT> fa, fb;
     if (ok) ok = R.wait_at(p);
-    if (ok) frag_load<FMT>(fa, R.slot_at(p), row, t);
+    if (ok) frag_load<FMT, NT>(fa, R.slot_at(p), row, t);
     int left = count;
-    while (frag_step<FMT>(R, fa, fb, p, left, row, t, b, b_step, q, magic, y, ok) &&
-           frag_step<FMT>(R, fb, fa, p, left, row, t, b, b_step, q, magic, y, ok)) {
+    while (frag_step<FMT, NT>(R, fa, fb, p, left, row, t, b, b_step, q, magic, y, ok) &&
+           frag_step<FMT, NT>(R, fb, fa, p, left, row, t, b, b_step, q, magic, y, ok)) {
     }
 }
 
-// Adds the two FP4 partial sums of each row (warps w, w + 4) in warp order. Every consumer warp calls
-// it with its pair-reduced y; afterwards warps 0..3 hold the sums. Contains two consumer barriers.
+// Adds the kFp4Parts FP4 partial sums of each row (warps w % 4, w % 4 + 4, ...) in warp order. Every
+// consumer warp calls it with its pair-reduced y; afterwards warps 0..3 hold the sums. Contains two
+// consumer barriers.
 __device__ inline void fp4_reduce(float* red, float (&y)[4]) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     if (warp >= 4 && t < 2)
 #pragma unroll
         for (int i = 0; i < 4; i++) red[(warp - 4) * 64 + (g + 8 * (i >> 1)) * 4 + 2 * t + (i & 1)] = y[i];
-    consumers_sync();
+    layer_sync();
     if (warp < 4 && t < 2)
 #pragma unroll
-        for (int i = 0; i < 4; i++) y[i] += red[warp * 64 + (g + 8 * (i >> 1)) * 4 + 2 * t + (i & 1)];
-    consumers_sync();
+        for (int i = 0; i < 4; i++)
+#pragma unroll
+            for (int pp = 1; pp < kFp4Parts; pp++) y[i] += red[(warp + 4 * (pp - 1)) * 64 + (g + 8 * (i >> 1)) * 4 + 2 * t + (i & 1)];
+    layer_sync();
 }
 
 }  // namespace fpx

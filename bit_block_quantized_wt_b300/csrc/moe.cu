@@ -576,7 +576,7 @@ __device__ __forceinline__ void gu_issue(const GateUpArgs& A, const GuTask& k, i
 }
 
 template <int Q>
-__global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constant__ GateUpArgs A) {
+__global__ void __launch_bounds__(kLThreads, 1) k_gate_up(const __grid_constant__ GateUpArgs A) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ Route r;
     __shared__ int shift[kMaxQ];
@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
     const UnitList UL = gate_up_units(r.n_uni, H, I);
     const uint32_t G = A.G, u0 = UL.first(blockIdx.x, G), u1 = UL.first(blockIdx.x + 1, G);
 
-    if (warp == kWarps) {  // producer: streams the range's boxes while the consumers load the tables
+    if (warp == kLWarps) {  // producer: streams the range's boxes while the consumers load the tables
         if (lane == 0) {
             uint32_t issued = 0;
             bool live = true;
@@ -619,7 +619,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
     if (threadIdx.x < kMaxQ) shift[threadIdx.x] = __ldcg(reinterpret_cast<const int*>(A.ws.gt + tset_copy_bytes(H)) + threadIdx.x);
     bool ok = __any_sync(0xffffffffu, mbar_wait(S.tbar, 0));
     if (!ok && lane == 0) flag(A.ws.status, FPX_ETIMEOUT);
-    consumers_sync();
+    layer_sync();
     const uint2* tab2 = reinterpret_cast<const uint2*>(S.tabs);
     const uint2* tab4 = reinterpret_cast<const uint2*>(S.tabs + btab_bytes(H));
     const float* oq2 = reinterpret_cast<const float*>(S.tabs + 2 * btab_bytes(H));
@@ -633,30 +633,34 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
     const uint32_t oq2_lane = lane_oq(oq2, 0, t);
     uint32_t bad = 0;
     typename decltype(R)::Pos pos{0u, 0u};
+    constexpr int kFp4Ch = 8 / kFp4Parts;  // FP4 chunks per warp
     for (uint32_t u = u0; u < u1; u++) {
         const GuTask k = gu_unit(u, r, A.m);
-        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float y[kLTiles][4];
+#pragma unroll
+        for (int i = 0; i < kLTiles; i++) y[i][0] = y[i][1] = y[i][2] = y[i][3] = 0.f;
         if (!k.fp4) {
             const uint32_t s = (uint32_t)k.s_beg;
-            frag_stages<2>(R, pos, k.s_end - k.s_beg, warp * 32 + g, t, tab2_lane + s * tab2_step, tab2_step, oq2_lane + s * 256u,
-                           magic, y, ok);
+            frag_stages<2, kLTiles>(R, pos, k.s_end - k.s_beg, warp * 16 * kLTiles + g, t, tab2_lane + s * tab2_step, tab2_step,
+                                    oq2_lane + s * 256u, magic, y, ok);
         } else {
             for (int s = k.s_beg; s < k.s_end; s++) {  // FP4 (shared expert) stages
                 if (ok) ok = R.wait_at(pos);
                 if (ok) {  // after a timeout the producer gives up too once this warp stops releasing
-                    const int ch0 = s * box_chunks(4) + 4 * (warp >> 2);
-                    box_tiles<4, 1, 4>(R.slot_at(pos) + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4), L4,
-                                       lane_tab(tab4, S.zero, a_idx, ch0), 0u, 0u, magic, *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
+                    const int ch0 = s * box_chunks(4) + kFp4Ch * (warp >> 2);
+                    box_tiles<4, 1, kFp4Ch>(R.slot_at(pos) + ((warp & 3) * 16 + g) * box_bytes(4) + kFp4Ch * (warp >> 2) * chunk_bytes(4),
+                                            L4, lane_tab(tab4, S.zero, a_idx, ch0), 0u, 0u, magic,
+                                            *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
                     R.release_at(pos);
                 }
                 R.next(pos);
             }
         }
-        pair_reduce(y[0]);
-        pair_reduce(y[1]);
+#pragma unroll
+        for (int i = 0; i < kLTiles; i++) pair_reduce(y[i]);
         if (k.fp4) fp4_reduce(S.red, y[0]);  // the same units run on every consumer warp
         if (ok && t < 2 && (!k.fp4 || warp < 4)) {
-            const int rb = k.row0 + (k.fp4 ? 16 : 32) * warp + g;
+            const int rb = k.row0 + (k.fp4 ? 16 : 16 * kLTiles) * warp + g;
             float* out = A.ws.gu + (size_t)k.piece * A.ws.gu_piece + (size_t)k.mat * Q * I;
 #pragma unroll
             for (int i = 0; i < 4; i++) {
@@ -665,7 +669,9 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_gate_up(const __grid_constan
                     // undo the per-token activation scale (and the 2^-14 of the FP4 decode)
                     const float sc = exp2i((k.fp4 ? 14 : 0) - shift[tok]);
                     out[(size_t)tok * I + rr] = y[0][i] * sc;
-                    if (!k.fp4) out[(size_t)tok * I + rr + 16] = y[1][i] * sc;
+#pragma unroll
+                    for (int ti = 1; ti < kLTiles; ti++)
+                        if (!k.fp4) out[(size_t)tok * I + rr + 16 * ti] = y[ti][i] * sc;
                 }
             }
         }
@@ -831,7 +837,7 @@ __device__ __forceinline__ void dn_issue(const DownArgs& A, const DnTask& k, int
 }
 
 template <int Q, int MODE, int NS>
-__global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__ DownArgs A) {
+__global__ void __launch_bounds__(kLThreads, 1) k_down(const __grid_constant__ DownArgs A) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ Route r;
     __shared__ int shift[2][kMaxQ];
@@ -854,7 +860,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
         return;
     }
 
-    if (warp == kWarps) {  // producer: streams the range's boxes while the consumers load the tables
+    if (warp == kLWarps) {  // producer: streams the range's boxes while the consumers load the tables
         if (lane == 0) {
             uint32_t issued = 0;
             bool live = true;
@@ -885,7 +891,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
     }
     bool ok = __any_sync(0xffffffffu, mbar_wait(S.tbar, 0));
     if (!ok && lane == 0) flag(A.ws.status, FPX_ETIMEOUT);
-    consumers_sync();
+    layer_sync();
 
     // Every consumer warp runs the same sequence of consumer barriers whether or not a wait timed
     // out, so a timeout never leaves a barrier short of arrivals.
@@ -894,34 +900,38 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
     const LaneOfs L4 = lane_ofs<4>(t);
     uint32_t bad = 0;
     typename decltype(R)::Pos pos{0u, 0u};
+    constexpr int kFp4Ch = 8 / kFp4Parts;  // FP4 chunks per warp
     for (uint32_t u = u0; u < u1; u++) {
         const DnTask k = dn_unit(u, r, A.m);
         const int sl = k.item - item_lo;
         const uint8_t* ts = S.tabs + (size_t)sl * dset_copy_bytes(I);
         const uint2* tab = reinterpret_cast<const uint2*>(ts);
         const float* oq = reinterpret_cast<const float*>(ts + btab_bytes(I));
-        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float y[kLTiles][4];
+#pragma unroll
+        for (int i = 0; i < kLTiles; i++) y[i][0] = y[i][1] = y[i][2] = y[i][3] = 0.f;
         if (!k.fp4) {
             const uint32_t s = (uint32_t)k.s_beg, b_step = a_idx >= 0 ? 4u * 512u : 0u;
-            frag_stages<3>(R, pos, k.s_end - k.s_beg, warp * 32 + g, t, lane_tab(tab, S.zero, a_idx, 0) + s * b_step, b_step,
-                           lane_oq(oq, 0, t) + s * 256u, magic, y, ok);
+            frag_stages<3, kLTiles>(R, pos, k.s_end - k.s_beg, warp * 16 * kLTiles + g, t, lane_tab(tab, S.zero, a_idx, 0) + s * b_step,
+                                    b_step, lane_oq(oq, 0, t) + s * 256u, magic, y, ok);
         } else {
             for (int s = k.s_beg; s < k.s_end; s++) {  // FP4 (shared expert) stages
                 if (ok) ok = R.wait_at(pos);
                 if (ok) {
-                    const int ch0 = s * box_chunks(4) + 4 * (warp >> 2);
-                    box_tiles<4, 1, 4>(R.slot_at(pos) + ((warp & 3) * 16 + g) * box_bytes(4) + 4 * (warp >> 2) * chunk_bytes(4), L4,
-                                       lane_tab(tab, S.zero, a_idx, ch0), 0u, 0u, magic, *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
+                    const int ch0 = s * box_chunks(4) + kFp4Ch * (warp >> 2);
+                    box_tiles<4, 1, kFp4Ch>(R.slot_at(pos) + ((warp & 3) * 16 + g) * box_bytes(4) + kFp4Ch * (warp >> 2) * chunk_bytes(4),
+                                            L4, lane_tab(tab, S.zero, a_idx, ch0), 0u, 0u, magic,
+                                            *reinterpret_cast<float(*)[1][4]>(&y[0]), bad);
                     R.release_at(pos);
                 }
                 R.next(pos);
             }
         }
-        pair_reduce(y[0]);
-        pair_reduce(y[1]);
+#pragma unroll
+        for (int i = 0; i < kLTiles; i++) pair_reduce(y[i]);
         if (k.fp4) fp4_reduce(S.red, y[0]);
         if (ok && t < 2 && (!k.fp4 || warp < 4)) {
-            const int rb = k.row0 + (k.fp4 ? 16 : 32) * warp + g;
+            const int rb = k.row0 + (k.fp4 ? 16 : 16 * kLTiles) * warp + g;
             float* out = A.ws.yi + (size_t)k.piece * A.ws.yi_piece + (size_t)k.item * Q * H;
 #pragma unroll
             for (int i = 0; i < 4; i++) {
@@ -929,7 +939,9 @@ __global__ void __launch_bounds__(kCtaThreads, 1) k_down(const __grid_constant__
                 if (tok < Q) {
                     const float sc = exp2i((k.fp4 ? 14 : 0) - shift[sl][tok]);
                     out[(size_t)tok * H + rr] = y[0][i] * sc;
-                    if (!k.fp4) out[(size_t)tok * H + rr + 16] = y[1][i] * sc;
+#pragma unroll
+                    for (int ti = 1; ti < kLTiles; ti++)
+                        if (!k.fp4) out[(size_t)tok * H + rr + 16 * ti] = y[ti][i] * sc;
                 }
             }
         }
@@ -1211,11 +1223,11 @@ int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, co
         e = e ? e : launch(k_stage, 4 * device_info().sms, kStageThreads, 0, s, pdl, sa);
     }
     if (ev) cudaEventRecord(ev[1], s);
-    e = e ? e : launch(k_gate_up<Q>, p.g_gate, kCtaThreads, p.sm_gate, s, pdl, ga);
+    e = e ? e : launch(k_gate_up<Q>, p.g_gate, kLThreads, p.sm_gate, s, pdl, ga);
     if (ev) cudaEventRecord(ev[2], s);
     e = e ? e : launch(k_hpack<Q>, 4 * (Q * k + 1), kHpackThreads, 0, s, pdl, ha);
     if (ev) cudaEventRecord(ev[3], s);
-    e = e ? e : launch(kdown, p.g_down, kCtaThreads, p.sm_down, s, pdl, da);
+    e = e ? e : launch(kdown, p.g_down, kLThreads, p.sm_down, s, pdl, da);
     if (ev) cudaEventRecord(ev[4], s);
     e = e ? e : launch(k_combine<Q, MODE>, p.g_comb, kCombineThreads, 0, s, pdl, ca);
     return e == cudaSuccess ? launch_status() : FPX_ECUDA;
