@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import bit_block_quantized_wt_b300 as fpx
+import oracle
 import synth
 from gpu_util import DeviceLayer, dev, host, need_gpu, read_status, routing_gap_ok, topk_of
 
@@ -35,11 +36,11 @@ def check_layer(L, bits, vals, k):
         assert list(idx[t]) == list(topk_of(lg[t], k))
     orc = L.oracle(vals.astype(np.float64), k, idx_force=idx)
     assert np.all(np.abs(lg - orc["logits"]) <= 1e-4 + 1e-4 * np.abs(orc["logits"]))
-    # where the oracle's own top-k is unique within the logit error, it must agree
-    own = L.oracle(vals.astype(np.float64), k) if L.E <= 64 else None
-    if own is not None:
-        ok = routing_gap_ok(own["logits"], k, 1e-4)
-        assert np.array_equal(own["idx"][ok], idx[ok])
+    # where the oracle's own top-k (on its binary64 logits) is unique within the logit error, it must
+    # agree; at every size (the oracle's router alone, without expanding every expert)
+    own = oracle.route(L.R_host, vals.astype(np.float64), k)
+    ok = routing_gap_ok(own["logits"], k, 1e-4)
+    assert np.array_equal(own["idx"][ok], idx[ok])
     assert np.allclose(w, orc["w"], rtol=1e-5, atol=0)
     err = np.abs(y.astype(np.float64) - orc["y"])
     assert np.all(err <= TOL * orc["M"]), float((err / orc["M"]).max())
