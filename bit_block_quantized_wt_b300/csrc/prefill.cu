@@ -236,7 +236,8 @@ __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
 // buffers (halves at +0 and +64), so its epilogue overlaps the next unit's MMAs; a larger unit uses
 // both (halves at 0 and 128).
 // The decode produces each 16-weight group in the order its binary16 pairs come out of the register
-// decode (pair p = weights p and p + 8); the B rows are stored in the same order (kpermute16), so the
+// decode (FP2 / FP3: pair p = weights p and p + 8; FP4: weights p + 4 (p / 4) and that + 4); the B rows
+// are stored in the same order (k_pgather and k_ph<1> for FP2 / FP3, k_perm4 and k_ph<2> for FP4), so the
 // products pair up as in the plain dot product.
 constexpr int kTcN = 128;                                           // pairs per unit at most
 constexpr int kTcSK = 128;                                          // K per stage
