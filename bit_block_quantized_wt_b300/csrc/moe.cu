@@ -234,6 +234,9 @@ struct RouterArgs {
     float* logits_out;
 };
 
+// Dynamic shared memory of the router: u [q][H] bfloat16, then two binary32 router rows.
+inline size_t router_smem(int q, int H) { return sizeof(uint16_t) * (size_t)q * H + 2 * sizeof(float) * (size_t)H; }
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -272,7 +275,8 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
     uint16_t* __restrict__ u_out = A.u_out;
     float* __restrict__ r_trace = A.r_trace;
     int32_t* status_to_clear = A.status_to_clear;
-    extern __shared__ __align__(16) uint16_t u_s[];  // [q][H] bfloat16 bits
+    extern __shared__ __align__(16) uint16_t u_s[];  // [q][H] bfloat16 bits, then this CTA's router rows
+    __shared__ __align__(8) uint64_t rbar;
     __shared__ float red[kRouterThreads / 32][kMaxQ];
     __shared__ float redm[kRouterThreads / 32][kMaxQ];
     __shared__ float inv_s[kMaxQ];
@@ -280,16 +284,22 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     // expert e = 2 * blockIdx + (warp >= kSlices): warps 0 .. kSlices - 1 and kSlices .. 2 kSlices - 1
     // each take a slice of the row's H / 4 float4 groups (the same slicing for both, so equal rows
-    // give bit-equal logits); the last warp packs the gate/up tables meanwhile (k > 0). The first batch
-    // of router weights does not depend on the previous kernel: load it before waiting.
+    // give bit-equal logits); the last warp packs the gate/up tables meanwhile (k > 0). The router
+    // weights do not depend on the previous kernel: one bulk copy stages this CTA's rows (adjacent in
+    // R) in shared memory while the CTA waits.
     constexpr int kSlices = 15, kPackWarp = kRouterThreads / 32 - 1;
     const int e = blockIdx.x * 2 + (warp >= kSlices), sl = warp % kSlices;
     const bool dots = warp < 2 * kSlices;
     const int h4r = H / 4, g0 = h4r * sl / kSlices, g1 = dots ? h4r * (sl + 1) / kSlices : g0;
-    const float4* row = reinterpret_cast<const float4*>(R + (size_t)(e < E ? e : 0) * H);
-    float4 pre[4];
-#pragma unroll
-    for (int b = 0; b < 4; b++) pre[b] = e < E && g0 + lane + 32 * b < g1 ? __ldg(row + g0 + lane + 32 * b) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float* w_s = reinterpret_cast<float*>(u_s + (size_t)q * H);  // q H * 2 bytes: a multiple of 32
+    if (threadIdx.x == 0) {
+        const uint32_t bytes = (uint32_t)(min(2, E - 2 * (int)blockIdx.x) * H) * 4u;
+        mbar_init(&rbar, 1);
+        fence_barrier_init();
+        fence_proxy_async();
+        mbar_expect_tx(&rbar, bytes);
+        bulk_load_hint(w_s, R + (size_t)blockIdx.x * 2 * H, bytes, &rbar, l2_evict_first());
+    }
     grid_dep_trigger();
     grid_dep_wait();  // r and the workspace come from the previous kernel
     if (status_to_clear && blockIdx.x == 0 && threadIdx.x == 0) *status_to_clear = 0;
@@ -346,18 +356,16 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
 #pragma unroll
         for (int tt = 0; tt < kMaxQ; tt++) { red[warp][tt] = ss[tt]; redm[warp][tt] = mx[tt]; }
     __syncthreads();
-    if (warp == 0) {
-#pragma unroll
-        for (int tt = 0; tt < kMaxQ; tt++) {
-            const float s = MODE == 1 ? warp_sum(red[lane][tt]) : 0.f, m = warp_max(redm[lane][tt]);
-            if (lane == 0) {
-                // max |u| = RN_bf16(max |r| * inv): rounding and scaling by inv > 0 are monotonic
-                const float iv = MODE == 1 ? 1.0f / sqrtf(s / (float)H + 1e-6f) : 1.0f;
-                const float mu = MODE == 1 ? __bfloat162float(__float2bfloat16_rn(m * iv)) : m;
-                inv_s[tt] = iv;
-                sh_s[tt] = column_shift(mu);
-                if (A.k > 0 && blockIdx.x == 0) reinterpret_cast<int*>(A.ws.gt + tset_copy_bytes(H))[tt] = sh_s[tt];
-            }
+    if (warp < kMaxQ) {  // warp tt reduces token tt's partials (the tokens in parallel)
+        const int tt = warp;
+        const float s = MODE == 1 ? warp_sum(red[lane][tt]) : 0.f, m = warp_max(redm[lane][tt]);
+        if (lane == 0) {
+            // max |u| = RN_bf16(max |r| * inv): rounding and scaling by inv > 0 are monotonic
+            const float iv = MODE == 1 ? 1.0f / sqrtf(s / (float)H + 1e-6f) : 1.0f;
+            const float mu = MODE == 1 ? __bfloat162float(__float2bfloat16_rn(m * iv)) : m;
+            inv_s[tt] = iv;
+            sh_s[tt] = column_shift(mu);
+            if (A.k > 0 && blockIdx.x == 0) reinterpret_cast<int*>(A.ws.gt + tset_copy_bytes(H))[tt] = sh_s[tt];
         }
     }
     __syncthreads();
@@ -381,24 +389,22 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
     }
     if (A.k > 0 && warp == kPackWarp) pack_gate_up_slice(u_s, sh_s, A.ws.gt, H, q);
     float acc[kMaxQ] = {0.f, 0.f, 0.f, 0.f};
-    if (e < E) {
-        for (int base = g0 + lane; base < g1; base += 4 * 32) {
-            float4 wv[4];
-#pragma unroll
-            for (int b = 0; b < 4; b++)
-                wv[b] = base == g0 + lane ? pre[b] : base + 32 * b < g1 ? __ldg(row + base + 32 * b) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int b = 0; b < 4; b++) {
-                const int h4 = base + 32 * b;
-                if (h4 >= g1) break;
+    if (dots) {
+        // the staged rows (a bounded wait; a lost copy leaves the logits at zero and flags a timeout)
+        const bool ok = mbar_wait(&rbar, 0);
+        if (!ok && lane == 0) flag(A.ws.status, FPX_ETIMEOUT);
+        if (ok && e < E) {
+            const float4* row = reinterpret_cast<const float4*>(w_s) + (size_t)(warp >= kSlices) * h4r;
+            for (int h4 = g0 + lane; h4 < g1; h4 += 32) {  // ascending h4: the order of the sums
+                const float4 wv = row[h4];
 #pragma unroll
                 for (int t = 0; t < kMaxQ; t++) {
                     if (t < q) {
                         const uint2 ub = reinterpret_cast<const uint2*>(u_s + (size_t)t * H)[h4];
-                        acc[t] = fmaf(wv[b].x, __uint_as_float(ub.x << 16), acc[t]);
-                        acc[t] = fmaf(wv[b].y, __uint_as_float(ub.x & 0xFFFF0000u), acc[t]);
-                        acc[t] = fmaf(wv[b].z, __uint_as_float(ub.y << 16), acc[t]);
-                        acc[t] = fmaf(wv[b].w, __uint_as_float(ub.y & 0xFFFF0000u), acc[t]);
+                        acc[t] = fmaf(wv.x, __uint_as_float(ub.x << 16), acc[t]);
+                        acc[t] = fmaf(wv.y, __uint_as_float(ub.x & 0xFFFF0000u), acc[t]);
+                        acc[t] = fmaf(wv.z, __uint_as_float(ub.y << 16), acc[t]);
+                        acc[t] = fmaf(wv.w, __uint_as_float(ub.y & 0xFFFF0000u), acc[t]);
                     }
                 }
             }
@@ -420,15 +426,16 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const __grid_constant
         }
     }
     if (A.k == 0) return;
-    // The last CTA to finish routes every token (one thread publishes the CTA's logits: the barrier
-    // orders them before its fence and atomic).
+    // The last CTA to finish routes every token. One thread counts the CTA in with an acquire-release
+    // atomic: the barrier orders the CTA's logit stores before its release, and the last CTA's
+    // acquire makes every CTA's logits visible to it (the barrier after it passes that on).
     __shared__ Route rt;
     __shared__ int last;
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        last = atomicAdd(A.ws.nuni + 1, 1) == (int)gridDim.x - 1;
-        __threadfence();
+        int old;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(A.ws.nuni + 1) : "memory");
+        last = old == (int)gridDim.x - 1;
     }
     __syncthreads();
     if (!last) return;  // CTA-uniform
@@ -568,11 +575,12 @@ __device__ __forceinline__ GuTask gu_unit(uint32_t u, const Route& r, const Laye
     return k;
 }
 
-__device__ __forceinline__ void gu_issue(const GateUpArgs& A, const GuTask& k, int s, uint8_t* slot, uint64_t* bar) {
+__device__ __forceinline__ void gu_issue(const GateUpArgs& A, const GuTask& k, int s, uint8_t* slot, uint64_t* bar,
+                                         uint64_t pol) {
     const int fmt = k.fp4 ? 4 : 2;
     const uint8_t* base = k.fp4 ? ((k.mat & 1) ? A.m.sh_up : A.m.sh_gate) : ((k.mat & 1) ? A.m.up : A.m.gate);
     mbar_expect_tx(bar, stage_bytes(fmt));
-    bulk_load(slot, base + k.off + (int64_t)s * stage_bytes(fmt), stage_bytes(fmt), bar);
+    bulk_load_hint(slot, base + k.off + (int64_t)s * stage_bytes(fmt), stage_bytes(fmt), bar, pol);
 }
 
 template <int Q>
@@ -599,6 +607,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_gate_up(const __grid_constant_
         if (lane == 0) {
             uint32_t issued = 0;
             bool live = true;
+            const uint64_t pol = l2_evict_first();
             // test hook: CTA 0 may withhold one copy (a lost message); its consumers' bounded waits
             // then run out and report FPX_ETIMEOUT
             const int32_t drop = blockIdx.x == 0 ? *reinterpret_cast<volatile int32_t*>(&g_ring_drop_stage) : -1;
@@ -607,7 +616,7 @@ __global__ void __launch_bounds__(kLThreads, 1) k_gate_up(const __grid_constant_
                 for (int s = k.s_beg; s < k.s_end; s++, issued++) {
                     if (drop >= 0 && issued == (uint32_t)drop) { live = false; break; }
                     if (!R.acquire(issued)) { flag(A.ws.status, FPX_ETIMEOUT); live = false; break; }
-                    gu_issue(A, k, s, R.slot(issued), R.bar(issued));
+                    gu_issue(A, k, s, R.slot(issued), R.bar(issued), pol);
                 }
             }
             R.drain(issued);
@@ -830,10 +839,11 @@ __device__ __forceinline__ DnTask dn_unit(uint32_t u, const Route& r, const Laye
     return k;
 }
 
-__device__ __forceinline__ void dn_issue(const DownArgs& A, const DnTask& k, int s, uint8_t* slot, uint64_t* bar) {
+__device__ __forceinline__ void dn_issue(const DownArgs& A, const DnTask& k, int s, uint8_t* slot, uint64_t* bar,
+                                         uint64_t pol) {
     const int fmt = k.fp4 ? 4 : 3;
     mbar_expect_tx(bar, stage_bytes(fmt));
-    bulk_load(slot, (k.fp4 ? A.m.sh_down : A.m.down) + k.off + (int64_t)s * stage_bytes(fmt), stage_bytes(fmt), bar);
+    bulk_load_hint(slot, (k.fp4 ? A.m.sh_down : A.m.down) + k.off + (int64_t)s * stage_bytes(fmt), stage_bytes(fmt), bar, pol);
 }
 
 template <int Q, int MODE, int NS>
@@ -864,11 +874,12 @@ __global__ void __launch_bounds__(kLThreads, 1) k_down(const __grid_constant__ D
         if (lane == 0) {
             uint32_t issued = 0;
             bool live = true;
+            const uint64_t pol = l2_evict_first();
             for (uint32_t u = u0; u < u1 && live; u++) {
                 const DnTask k = dn_unit(u, r, A.m);
                 for (int s = k.s_beg; s < k.s_end; s++, issued++) {
                     if (!R.acquire(issued)) { flag(A.ws.status, FPX_ETIMEOUT); live = false; break; }
-                    dn_issue(A, k, s, R.slot(issued), R.bar(issued));
+                    dn_issue(A, k, s, R.slot(issued), R.bar(issued), pol);
                 }
             }
             R.drain(issued);
@@ -1051,7 +1062,7 @@ Plan make_plan(const moe_layer& L, int q, int k) {
     DeviceInfo di = device_info();
     Plan p{};
     p.g_router = (L.E + 1) / 2;
-    p.sm_router = sizeof(uint16_t) * (size_t)q * L.H;
+    p.sm_router = router_smem(q, L.H);
     // one CTA per SM, but no more CTAs than the units of the smallest union (k experts), so that a
     // CTA's share stays below one routed item's units (the down kernel holds the tables of two items)
     auto grid_for = [&](const UnitList& U) { return (int)(U.units() < (uint32_t)di.sms ? U.units() : (uint32_t)di.sms); };
@@ -1256,7 +1267,7 @@ int moe_route_topk(const float* R, int E, int H, const uint16_t* x, int q, int k
     if (!R || !x || !logits || !idx || !w || !uni || !n_uni) return FPX_EINVAL;
     if (!aligned(R, 16) || !aligned(x, 4) || !aligned(logits, 4)) return FPX_EALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t sm = sizeof(uint16_t) * (size_t)q * H;
+    const size_t sm = router_smem(q, H);
     if (sm > (size_t)device_info().smem_optin) return FPX_EINVAL;
     if (cudaFuncSetAttribute(k_router<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) return FPX_ECUDA;
     RouterArgs ra{};

@@ -130,18 +130,7 @@ __global__ void __launch_bounds__(256) k_ptopk(const float* __restrict__ logits,
                                                float* w) {
     const int t = blockIdx.x * 8 + threadIdx.x / 32;
     if (t >= T) return;
-    int32_t ii[kPMaxK];
-    float ww[kPMaxK];
-    warp_topk(logits + (size_t)t * E, E, k, ii, ww);
-    if ((threadIdx.x & 31) < k) {
-        const int r = threadIdx.x & 31;
-        int32_t iv = ii[0];
-        float wv = ww[0];
-        for (int j = 1; j < kPMaxK; j++)
-            if (j == r) { iv = ii[j]; wv = ww[j]; }
-        idx[(size_t)t * k + r] = iv;
-        w[(size_t)t * k + r] = wv;
-    }
+    warp_topk(logits + (size_t)t * E, E, k, idx + (size_t)t * k, w + (size_t)t * k);
 }
 
 __global__ void k_phist(const int32_t* __restrict__ idx, int P, int E, int32_t* counts, int32_t* status) {

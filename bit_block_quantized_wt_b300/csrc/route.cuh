@@ -13,7 +13,8 @@ constexpr int kRouteMaxK = 8;      // experts per token
 constexpr int kRouteMaxE = 1024;   // routed experts per layer
 
 // Warp-level top-k of lg[0..E) (descending, ties to the lower index), with sigmoid weights
-// normalised over the selected k. Each lane keeps its E / 32 logits in registers (NM >= E / 32 slots).
+// normalised over the selected k: lane r < k writes idx[r] and w[r]. Each lane keeps its E / 32 logits
+// in registers (NM >= E / 32 slots).
 template <int NM>
 __device__ void warp_topk_n(const float* lg, int E, int k, int32_t* idx, float* w) {
     const int lane = threadIdx.x & 31;
@@ -21,29 +22,40 @@ __device__ void warp_topk_n(const float* lg, int E, int k, int32_t* idx, float* 
 #pragma unroll
     for (int m = 0; m < NM; m++) v[m] = lane + 32 * m < E ? __ldcg(lg + lane + 32 * m) : 0.0f;
     uint32_t taken = 0;  // bit m: element lane + 32 m already selected
+    // rounds unrolled up to the largest k, so that the selected values stay in registers
     float sig[kRouteMaxK];
-    for (int r = 0; r < k; r++) {
-        float bv = 0.0f;
-        int bi = -1;
+    int sel[kRouteMaxK];
 #pragma unroll
-        for (int m = 0; m < NM; m++) {
-            const int e = lane + 32 * m;  // ascending: equal values keep the lower index
-            if (e < E && !((taken >> m) & 1u) && (bi < 0 || v[m] > bv)) { bv = v[m]; bi = e; }
-        }
+    for (int r = 0; r < kRouteMaxK; r++) {
+        if (r < k) {
+            float bv = 0.0f;
+            int bi = -1;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            bool better = oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi));
-            if (better) { bv = ov; bi = oi; }
+            for (int m = 0; m < NM; m++) {
+                const int e = lane + 32 * m;  // ascending: equal values keep the lower index
+                if (e < E && !((taken >> m) & 1u) && (bi < 0 || v[m] > bv)) { bv = v[m]; bi = e; }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                bool better = oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi));
+                if (better) { bv = ov; bi = oi; }
+            }
+            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+            sel[r] = bi;
+            sig[r] = 1.0f / (1.0f + expf(-bv));
         }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        idx[r] = bi;
-        sig[r] = 1.0f / (1.0f + expf(-bv));
     }
     float S = sig[0];
-    for (int r = 1; r < k; r++) S += sig[r];
-    for (int r = 0; r < k; r++) w[r] = sig[r] / S;
+#pragma unroll
+    for (int r = 1; r < kRouteMaxK; r++)
+        if (r < k) S += sig[r];
+    if (lane < k) {  // lane r writes rank r
+#pragma unroll
+        for (int r = 0; r < kRouteMaxK; r++)
+            if (r == lane) { idx[r] = sel[r]; w[r] = sig[r] / S; }
+    }
 }
 
 __device__ inline void warp_topk(const float* lg, int E, int k, int32_t* idx, float* w) {

@@ -154,8 +154,10 @@ int fpx_gemv_q_idot(int fmt, const uint8_t* Wq, int64_t N, int64_t K, const void
  * (R binary32 [E][H], x bfloat16 [q][H]); idx[t][r], r < k, the k largest logits in descending order,
  * ties to the lower expert index; w[t][r] = sigmoid(l) / sum over the k selected sigmoids; uni the
  * sorted distinct experts of all tokens (n_uni of them, at most q*k; uni has q*k entries).
- * Limits: 1 <= k <= 8, k <= E <= 1024, H % 16 == 0. logits [q][E] is required: it is also the
- * top-k input. [P-apu], [P-dsv4] paragraph 3. */
+ * Limits: 1 <= k <= 8, k <= E <= 1024, H % 16 == 0, and (2q + 8) H bytes within the device's shared
+ * memory per block (x and two router rows are staged there: H <= 14528 at q = 4 with 227 KB),
+ * FPX_EINVAL otherwise. logits [q][E] is required: it is also the top-k input. [P-apu], [P-dsv4]
+ * paragraph 3. */
 int moe_route_topk(const float* R, int E, int H, const uint16_t* x, int q, int k, float* logits,
                    int32_t* idx, float* w, int32_t* uni, int32_t* n_uni, void* stream);
 

@@ -93,6 +93,8 @@ def test_route_and_quant_argument_errors():
     assert L.moe_route_topk(FAKE, 8, 64, FAKE, 4, 9, FAKE, FAKE, FAKE, FAKE, FAKE, None) == fpx.FPX_EINVAL
     assert L.moe_route_topk(FAKE, 8, 64, FAKE, 4, 2, None, FAKE, FAKE, FAKE, FAKE, None) == fpx.FPX_EINVAL
     assert L.moe_route_topk(FAKE, 2000, 64, FAKE, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None) == fpx.FPX_EINVAL
+    # x and two router rows staged in shared memory: (2 q + 8) H = 256 KB does not fit
+    assert L.moe_route_topk(FAKE, 8, 16384, FAKE, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None) == fpx.FPX_EINVAL
     assert L.fpx_quantize(2, FAKE, 4, 48, None, FAKE, None, None) == fpx.FPX_EINVAL
     assert L.fpx_quantize(2, FAKE, 4, 64, None, FAKE + 1, None, None) == fpx.FPX_EALIGN
     assert L.fpx_dequantize(9, FAKE, 4, 64, FAKE, None, None) == fpx.FPX_EINVAL

@@ -38,7 +38,7 @@ def check_route(R, bits, vals, k):
 
 
 @pytest.mark.parametrize("E,H,q,k", [(8, 64, 1, 1), (8, 64, 4, 3), (16, 256, 3, 8), (64, 512, 4, 6), (1024, 256, 2, 8),
-                                     (256, 4096, 4, 4), (256, 4096, 4, 6)])
+                                     (256, 4096, 4, 4), (256, 4096, 4, 6), (9, 128, 3, 4), (1023, 64, 4, 8)])
 def test_route_matches_oracle(E, H, q, k):
     need_gpu()
     R = synth.router(E, H, seed=E + H)
