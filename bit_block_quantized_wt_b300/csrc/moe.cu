@@ -702,6 +702,7 @@ struct HpackArgs {
 
 constexpr int kHpackThreads = 512;
 constexpr int kHpackV = 3;  // float4 groups per thread, all loaded at once: I <= 3 * 4 * 512
+static_assert(kHpackV * 4 * kHpackThreads >= 4608, "h buffer holds I <= 4608");
 
 template <int Q>
 __global__ void __launch_bounds__(kHpackThreads) k_hpack(const __grid_constant__ HpackArgs A) {
@@ -1037,7 +1038,10 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(const __grid_consta
 // ------------------------------------------------------------------ launch plumbing
 
 int check_layer(const moe_layer* L) {
-    if (!L || L->H < 512 || L->I < 512 || L->H % 512 || L->I % 512 || L->E < 1 || L->E > kMaxE) return FPX_EINVAL;
+    // H, I <= 4608: the fixed piece arrays (kMaxPieces), the router's registers and k_hpack's buffer
+    if (!L || L->H < 512 || L->I < 512 || L->H % 512 || L->I % 512 || L->H > 4608 || L->I > 4608 || L->E < 1 ||
+        L->E > kMaxE)
+        return FPX_EINVAL;
     if (!L->router || !L->gate || !L->up || !L->down || !L->sh_gate || !L->sh_up || !L->sh_down) return FPX_EINVAL;
     if (!aligned(L->router, 16) || !aligned(L->gate, 16) || !aligned(L->up, 16) || !aligned(L->down, 16) ||
         !aligned(L->sh_gate, 16) || !aligned(L->sh_up, 16) || !aligned(L->sh_down, 16))

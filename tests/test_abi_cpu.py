@@ -67,7 +67,8 @@ def test_layer_argument_errors():
                                                                      None, wsp, wsb, None)
     assert call(_layer(H=500)) == fpx.FPX_EINVAL
     assert call(_layer(I=100)) == fpx.FPX_EINVAL
-    assert call(_layer(H=5120)) == fpx.FPX_EINVAL  # shared-memory tables too large
+    assert call(_layer(H=5120)) == fpx.FPX_EINVAL  # above the 4608 limit (and its tables too large)
+    assert call(_layer(I=5632)) == fpx.FPX_EINVAL  # above the 4608 limit, although its tables would fit
     assert call(_layer(E=0)) == fpx.FPX_EINVAL
     assert call(_layer(down=None)) == fpx.FPX_EINVAL
     assert call(_layer(gate=FAKE + 4)) == fpx.FPX_EALIGN
