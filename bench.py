@@ -523,68 +523,89 @@ def idot_measure(fpx, peak, reps=10):
 
 def tiered_measure(fpx, stack, reps=16):
     """moe_layer_decode_tiered on layer 0 with the 128 even-numbered experts in HBM slots and the other
-    128 in pinned host memory (Q * K_TOP staging slots), against moe_layer_decode on the all-HBM layer;
-    q = 4, top-4, 8 token batches rotating, CUDA events. Staged bytes: the cold experts of each batch's
-    union (gate + up + down), counted from the routing."""
+    128 in pinned host memory, against moe_layer_decode on the all-HBM layer; q = 4, top-4, CUDA
+    events. Without a cache (Q * K_TOP staging slots, 8 token batches rotating) every call copies the
+    cold experts of its union (gate + up + down, counted from the routing). With the staging cache:
+    16 slots on the same 8 rotating batches, and 64 slots on a new batch every call (no repeated
+    tokens); their copies per call come from the cache's copy count."""
     import torch
     import synth
     g, u, d, sh, R = stack.bufs[0]
     mb_gu, mb_d = fpx.fpx_matrix_bytes(2, I, H), fpx.fpx_matrix_bytes(3, H, I)
+    per_expert = 2 * mb_gu + mb_d
     hot = torch.arange(0, E, 2)
-    n_hot, n_stage = len(hot), Q * K_TOP
-    n_slots = n_hot + n_stage
-    arrays = []
-    for full, mb in ((g, mb_gu), (u, mb_gu), (d, mb_d)):
-        a = torch.zeros(n_slots * mb, dtype=torch.uint8, device="cuda")
-        a.view(n_slots, mb)[:n_hot] = full.view(E, mb)[hot.cuda()]
-        arrays.append(a)
+    n_hot = len(hot)
     cold = [full.cpu().pin_memory() for full in (g, u, d)]
     slot_of = torch.full((E,), -1, dtype=torch.int32)
     slot_of[hot] = torch.arange(n_hot, dtype=torch.int32)
     slot_of = slot_of.cuda()
-    lay = fpx.moe_layer(H=H, I=I, E=E, router=R.data_ptr(), gate=arrays[0].data_ptr(), up=arrays[1].data_ptr(),
-                        down=arrays[2].data_ptr(), sh_gate=sh[0].data_ptr(), sh_up=sh[1].data_ptr(),
-                        sh_down=sh[2].data_ptr())
-    tiers = fpx.moe_tiers(slot_of=slot_of.data_ptr(), cold_gate=cold[0].data_ptr(), cold_up=cold[1].data_ptr(),
-                          cold_down=cold[2].data_ptr(), n_slots=n_slots, stage_slot0=n_hot, n_stage=n_stage)
-    ws_b = fpx.moe_workspace_bytes(lay, Q, K_TOP)
+    keep = []
+
+    def tiered_layer(n_stage, cached):
+        n_slots = n_hot + n_stage
+        arrays = []
+        for full, mb in ((g, mb_gu), (u, mb_gu), (d, mb_d)):
+            a = torch.zeros(n_slots * mb, dtype=torch.uint8, device="cuda")
+            a.view(n_slots, mb)[:n_hot] = full.view(E, mb)[hot.cuda()]
+            arrays.append(a)
+        cache = torch.zeros(2 + 2 * n_stage, dtype=torch.int32, device="cuda") if cached else None
+        keep.append((arrays, cache))
+        lay = fpx.moe_layer(H=H, I=I, E=E, router=R.data_ptr(), gate=arrays[0].data_ptr(), up=arrays[1].data_ptr(),
+                            down=arrays[2].data_ptr(), sh_gate=sh[0].data_ptr(), sh_up=sh[1].data_ptr(),
+                            sh_down=sh[2].data_ptr())
+        tiers = fpx.moe_tiers(slot_of=slot_of.data_ptr(), cold_gate=cold[0].data_ptr(), cold_up=cold[1].data_ptr(),
+                              cold_down=cold[2].data_ptr(), n_slots=n_slots, stage_slot0=n_hot, n_stage=n_stage,
+                              cache=cache.data_ptr() if cached else None)
+        if cached:
+            fpx.moe_tiers_cache_reset(tiers)
+        return lay, tiers, cache
+
+    ws_b = fpx.moe_workspace_bytes(stack.layers[0], Q, K_TOP)
     ws = torch.empty(ws_b, dtype=torch.uint8, device="cuda")
-    xs = [torch.from_numpy(synth.tokens_bf16(Q, H, seed=2000 + b)[0].view(np.int16)).cuda() for b in range(N_BATCHES)]
+    rot = [torch.from_numpy(synth.tokens_bf16(Q, H, seed=2000 + b)[0].view(np.int16)).cuda() for b in range(N_BATCHES)]
+    fresh = [torch.from_numpy(synth.tokens_bf16(Q, H, seed=3000 + b)[0].view(np.int16)).cuda() for b in range(reps + 3)]
     y = torch.empty(Q, H, device="cuda")
     idx = torch.empty(Q, K_TOP, dtype=torch.int32, device="cuda")
-
-    def run(tiered, b):
-        if tiered:
-            fpx.moe_layer_decode_tiered(lay, tiers, xs[b % N_BATCHES], Q, K_TOP, y, ws, ws_b, idx_out=idx)
-        else:
-            fpx.moe_layer_decode(stack.layers[0], xs[b % N_BATCHES], Q, K_TOP, y, ws, ws_b, idx_out=idx)
-
     n_cold = []
     for b in range(N_BATCHES):
-        run(False, b)
+        fpx.moe_layer_decode(stack.layers[0], rot[b], Q, K_TOP, y, ws, ws_b, idx_out=idx)
         torch.cuda.synchronize()
-        uni = set(idx.cpu().numpy().ravel().tolist())
-        n_cold.append(sum(1 for e in uni if e % 2 == 1))
+        n_cold.append(sum(1 for e in set(idx.cpu().numpy().ravel().tolist()) if e % 2 == 1))
+    modes = {"all_hbm": (None, rot), "two_tier": (tiered_layer(Q * K_TOP, False), rot),
+             "two_tier_cache16": (tiered_layer(Q * K_TOP, True), rot), "two_tier_cache64_fresh": (tiered_layer(64, True), fresh)}
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    res = {}
-    for name, tiered in (("all_hbm", False), ("two_tier", True)):
+    res, copies = {}, {}
+    for name, (tl, xs) in modes.items():
+        def run(b):
+            if tl is None:
+                fpx.moe_layer_decode(stack.layers[0], xs[b % len(xs)], Q, K_TOP, y, ws, ws_b, idx_out=idx)
+            else:
+                fpx.moe_layer_decode_tiered(tl[0], tl[1], xs[b % len(xs)], Q, K_TOP, y, ws, ws_b, idx_out=idx)
         for b in range(3):
-            run(tiered, b)
+            run(b)
         torch.cuda.synchronize()
+        c0 = int(tl[2][1]) if tl is not None and tl[2] is not None else None
         e0.record()
-        for b in range(reps):
-            run(tiered, b)
+        for b in range(3, 3 + reps):
+            run(b)
         e1.record()
         e1.synchronize()
         res[name] = e0.elapsed_time(e1) / reps
+        if c0 is not None:
+            copies[name] = (int(tl[2][1]) - c0) / reps
     st = fpx.fpx_read_status(ws[:4].view(torch.int32))
-    staged = float(np.mean([n_cold[b % N_BATCHES] for b in range(reps)])) * (2 * mb_gu + mb_d)
+    cold_rot = float(np.mean([n_cold[b % N_BATCHES] for b in range(3, 3 + reps)]))
+    staged = cold_rot * per_expert
     extra = res["two_tier"] - res["all_hbm"]
-    return {"workload": f"layer 0 (H {H}, I {I}, {E} experts, q {Q}, top-{K_TOP}); even experts in HBM, odd in pinned "
-                        "host memory", "hot_experts": n_hot, "status": st,
-            "ms_per_layer_all_hbm": round(res["all_hbm"], 4), "ms_per_layer_two_tier": round(res["two_tier"], 4),
-            "cold_experts_per_call": round(staged / (2 * mb_gu + mb_d), 2), "staged_MB_per_call": round(staged / 1e6, 2),
-            "staged_GB_per_s": round(staged / (extra / 1e3) / 1e9, 1) if extra > 0 else None, "reps": reps}
+    out = {"workload": f"layer 0 (H {H}, I {I}, {E} experts, q {Q}, top-{K_TOP}); even experts in HBM, odd in pinned "
+                       "host memory", "hot_experts": n_hot, "status": st,
+           "ms_per_layer_all_hbm": round(res["all_hbm"], 4), "ms_per_layer_two_tier": round(res["two_tier"], 4),
+           "cold_experts_per_call": round(cold_rot, 2), "staged_MB_per_call": round(staged / 1e6, 2),
+           "staged_GB_per_s": round(staged / (extra / 1e3) / 1e9, 1) if extra > 0 else None, "reps": reps}
+    for name in ("two_tier_cache16", "two_tier_cache64_fresh"):
+        out[name] = {"ms_per_layer": round(res[name], 4), "copied_experts_per_call": round(copies[name], 2),
+                     "staged_MB_per_call": round(copies[name] * per_expert / 1e6, 2)}
+    return out
 
 
 def run_fpx(args):

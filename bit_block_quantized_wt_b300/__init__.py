@@ -38,10 +38,10 @@ class moe_layer(ctypes.Structure):
 
 class moe_tiers(ctypes.Structure):
     """Mirror of the C struct: device slot_of [E], host (pinned) cold-tier gate/up/down arrays, the
-    number of HBM slots and the staging slot range."""
+    number of HBM slots, the staging slot range and the optional device cache of staged experts."""
     _fields_ = [("slot_of", ctypes.c_void_p), ("cold_gate", ctypes.c_void_p), ("cold_up", ctypes.c_void_p),
                 ("cold_down", ctypes.c_void_p), ("n_slots", ctypes.c_int), ("stage_slot0", ctypes.c_int),
-                ("n_stage", ctypes.c_int)]
+                ("n_stage", ctypes.c_int), ("cache", ctypes.c_void_p)]
 
 
 _lib = None
@@ -81,6 +81,7 @@ _SIGS = {
                                                ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                                ctypes.c_void_p]),
+    "moe_tiers_cache_reset": (ctypes.c_int, [ctypes.POINTER(moe_tiers), ctypes.c_void_p]),
     "moe_stack_verify": (ctypes.c_int, [ctypes.POINTER(moe_layer), ctypes.c_int, ctypes.c_void_p,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
@@ -209,6 +210,11 @@ def moe_layer_decode_tiered(layer, tiers, x, q, k, y, ws, ws_bytes, idx_out=None
     _check(lib().moe_layer_decode_tiered(ctypes.byref(layer), ctypes.byref(tiers), _ptr(x), q, k, _ptr(y),
                                          _ptr(idx_out), _ptr(w_out), _ptr(logits_out), _ptr(ws), ws_bytes,
                                          _stream(stream)), "moe_layer_decode_tiered")
+
+
+def moe_tiers_cache_reset(tiers, stream=None):
+    """Empties the two-tier staging cache tiers.cache (see include/fpx.h)."""
+    _check(lib().moe_tiers_cache_reset(ctypes.byref(tiers), _stream(stream)), "moe_tiers_cache_reset")
 
 
 def moe_layer_decode_static_ws(layer, x, q, k, y, idx_out=None, w_out=None, logits_out=None,

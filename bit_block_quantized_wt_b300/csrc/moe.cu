@@ -50,7 +50,7 @@ __device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontro
 // ------------------------------------------------------------------ workspace
 
 struct Ws {
-    size_t status, logits, u, idx, w, uni, uslot, nuni, gu, yi, gt, dt, total;
+    size_t status, logits, u, idx, w, uni, uslot, nuni, stage, gu, yi, gt, dt, total;
     size_t gu_piece, yi_piece;  // floats between consecutive piece buffers
 };
 
@@ -67,6 +67,7 @@ inline Ws ws_layout(int H, int I, int E, int q, int k) {
     w.uni = o; o = up16(o + sizeof(int32_t) * q * k);
     w.uslot = o; o = up16(o + sizeof(int32_t) * q * k);
     w.nuni = o; o += 16;  // n_uni, then the router's arrival counter
+    w.stage = o; o = up16(o + sizeof(int32_t) * (1 + 2 * q * k));  // two-tier copy list
     w.gu_piece = (size_t)2 * (q * k + 1) * q * I;
     w.yi_piece = (size_t)(q * k + 1) * q * H;
     w.gu = o; o = up16(o + sizeof(float) * pieces_of(H / stage_k(2), kSppGu) * w.gu_piece);  // FP2 tasks have the most pieces
@@ -91,6 +92,7 @@ struct WsPtrs {
     uint8_t* gt;  // gate/up activation tables (table set for K = H), built by the router kernel
     uint8_t* dt;  // down activation tables, one table set for K = I per item, built by k_hpack
     int32_t* uslot;  // matrix slot of every union item (the expert id, or its slot in a two-tier layer)
+    int32_t* stage;  // two-tier copy list: [count, expert[q k], slot[q k]]
 };
 
 inline WsPtrs ws_ptrs(void* ws, const Ws& l) {
@@ -101,7 +103,8 @@ inline WsPtrs ws_ptrs(void* ws, const Ws& l) {
                   reinterpret_cast<int32_t*>(b + l.nuni),   reinterpret_cast<float*>(b + l.gu),
                   reinterpret_cast<float*>(b + l.yi),       l.gu_piece,
                   l.yi_piece,                                reinterpret_cast<uint8_t*>(b + l.gt),
-                  reinterpret_cast<uint8_t*>(b + l.dt),      reinterpret_cast<int32_t*>(b + l.uslot)};
+                  reinterpret_cast<uint8_t*>(b + l.dt),      reinterpret_cast<int32_t*>(b + l.uslot),
+                  reinterpret_cast<int32_t*>(b + l.stage)};
 }
 
 // Everything the gate/up and down kernels need about one layer: the stacked box-tiled matrices
@@ -1084,12 +1087,19 @@ Plan make_plan(const moe_layer& L, int q, int k) {
 // A two-tier layer keeps the hot experts' matrices in HBM slots and the others (the cold tier) in
 // pinned host memory ("Token Freedom via APU ...", section "Asymmetric Dual-GPU": popular experts in
 // the fast memory, cold ones in the large pool; the Paiton page on DeepSeek V4.1 Flash, section
-// "Keeping useful work on the GPU": cold experts streamed to the GPU when that pays). After routing, k_stage gives
-// every cold expert of the union a staging slot, copies its gate, up and down matrices from host
-// memory into that slot (reads over the host link, 16 bytes per thread per load), and rewrites the
-// union's slot list; the gate/up and down kernels then stream every item from HBM as usual, and the
-// combine still matches tokens to items by expert id, so the result is bit-identical to a layer whose
-// experts are all in HBM.
+// "Keeping useful work on the GPU": cold experts streamed to the GPU when that pays). After routing,
+// k_stage_plan gives every cold expert of the union a staging slot and lists the copies; k_stage
+// copies their gate, up and down matrices from host memory into those slots (reads over the host
+// link, 16 bytes per thread per load) and the union's slot list is rewritten; the gate/up and down
+// kernels then stream every item from HBM as usual, and the combine still matches tokens to items by
+// expert id, so the result is bit-identical to a layer whose experts are all in HBM.
+//
+// With a cache (moe_tiers.cache) the staging slots keep their experts across calls: a cold expert
+// already in a slot is not copied again, and a missing one takes the least recently used slot that
+// this call does not use. The host link moves about 51 GB/s against the HBM's 6.5 TB/s, so the copies
+// dominate a call; not copying is what shortens it.
+
+constexpr int kMaxStageCache = 1024;  // staging slots a cache can track
 
 struct StageArgs {
     const int32_t* slot_of;               // [E]: HBM slot of expert e, or < 0 for the cold tier
@@ -1097,43 +1107,122 @@ struct StageArgs {
     uint8_t *gate, *up, *down;            // the layer's HBM slot arrays
     int64_t mb2, mb3;
     int E, n_slots, stage0, n_stage, qk;
+    int32_t* cache;  // nullable: [clock, copies so far, expert of staging slot i (n_stage), last use of slot i (n_stage)]
     WsPtrs ws;
 };
 
+// One warp: the staging slot of every cold item of the union and the list of copies (ws.stage), in
+// union order (ascending expert). Without a cache the i-th cold item takes staging slot i and is
+// copied. With one: a slot that holds the expert is used as it is; otherwise the slot with the
+// oldest last use among those this call has not taken (ties to the lower slot) receives it.
+__global__ void __launch_bounds__(32) k_stage_plan(const __grid_constant__ StageArgs A) {
+    grid_dep_trigger();  // the copy kernel waits for this grid before it reads the list
+    grid_dep_wait();     // the union comes from the router kernel
+    __shared__ int32_t cexp[kMaxStageCache], cuse[kMaxStageCache];
+    __shared__ uint32_t taken[kMaxStageCache / 32];
+    const int lane = threadIdx.x;
+    const int n = min(__ldcg(A.ws.nuni), A.qk);
+    const bool cached = A.cache != nullptr;
+    const int ns = A.n_stage;
+    const uint32_t clock = cached ? (uint32_t)__ldcg(A.cache) + 1u : 0u;
+    // item `lane`: its expert and HBM slot (a slot outside the arrays or inside the staging range
+    // cannot hold a hot expert: the expert is treated as cold and the status reports it)
+    int e_l = -1, sl_l = -1;
+    bool bad = false;
+    if (lane < n) {
+        e_l = __ldcg(A.ws.uni + lane);
+        sl_l = e_l >= 0 && e_l < A.E ? A.slot_of[e_l] : -1;
+        if (sl_l >= A.n_slots || (sl_l >= A.stage0 && sl_l < A.stage0 + ns)) {
+            bad = true;
+            sl_l = -1;
+        }
+    }
+    if (cached) {
+        for (int i = lane; i < ns; i += 32) {
+            cexp[i] = __ldcg(A.cache + 2 + i);
+            cuse[i] = __ldcg(A.cache + 2 + ns + i);
+        }
+        for (int i = lane; i < kMaxStageCache / 32; i += 32) taken[i] = 0u;
+    }
+    __syncwarp();
+    int ncold = 0, ncopy = 0;
+    for (int j = 0; j < n; j++) {
+        const int e = __shfl_sync(0xffffffffu, e_l, j);
+        int sl = __shfl_sync(0xffffffffu, sl_l, j);
+        if (sl < 0 && e >= 0 && e < A.E) {
+            int i = ncold;
+            bool copy = true;
+            if (cached) {
+                int hit = -1;
+                for (int b = 0; b < ns && hit < 0; b += 32) {
+                    const uint32_t m = __ballot_sync(0xffffffffu, b + lane < ns && cexp[b + lane] == e);
+                    if (m) hit = b + __ffs(m) - 1;
+                }
+                if (hit >= 0) {
+                    i = hit;
+                    copy = false;
+                } else {  // oldest last use (as a distance back from this call's clock), lower slot on ties
+                    uint64_t best = ~0ull;
+                    for (int s2 = lane; s2 < ns; s2 += 32)
+                        if (!((taken[s2 >> 5] >> (s2 & 31)) & 1u)) {
+                            const uint64_t key = ((uint64_t)(0xFFFFFFFFu - (clock - (uint32_t)cuse[s2])) << 32) | (uint32_t)s2;
+                            best = key < best ? key : best;
+                        }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const uint64_t ob = __shfl_xor_sync(0xffffffffu, best, o);
+                        best = ob < best ? ob : best;
+                    }
+                    i = (int)(best & 0xFFFFFFFFu);  // n_stage >= q k: a free slot always exists
+                }
+                if (lane == 0) {
+                    cexp[i] = e;
+                    cuse[i] = (int32_t)clock;
+                    taken[i >> 5] |= 1u << (i & 31);
+                }
+                __syncwarp();
+            }
+            sl = A.stage0 + i;
+            if (copy && lane == 0) {
+                A.ws.stage[1 + ncopy] = e;
+                A.ws.stage[1 + A.qk + ncopy] = sl;
+            }
+            ncopy += copy;
+            ncold++;
+        }
+        if (lane == 0) A.ws.uslot[j] = sl;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag(A.ws.status, FPX_EDATA);
+    if (lane == 0) A.ws.stage[0] = ncopy;
+    if (cached) {
+        for (int i = lane; i < ns; i += 32) {
+            A.cache[2 + i] = cexp[i];
+            A.cache[2 + ns + i] = cuse[i];
+        }
+        if (lane == 0) {
+            A.cache[0] = (int32_t)clock;
+            A.cache[1] += ncopy;
+        }
+    }
+}
+
 constexpr int kStageThreads = 256;
 
+// Copies the listed cold experts (gate, up and down matrices) from the host tier into their slots.
 __global__ void __launch_bounds__(kStageThreads) k_stage(const __grid_constant__ StageArgs A) {
     grid_dep_trigger();  // the gate/up kernel waits for this grid before it reads the slots or weights
-    grid_dep_wait();     // the union comes from the router kernel
+    grid_dep_wait();     // the list comes from k_stage_plan
     __shared__ int32_t src[kMaxQ * kMaxK], dst[kMaxQ * kMaxK];
-    __shared__ int ncold;
-    if (threadIdx.x == 0) {
-        const int n = __ldcg(A.ws.nuni);
-        int nc = 0;
-        bool bad = false;
-        for (int j = 0; j < n && j < A.qk; j++) {
-            const int e = __ldcg(A.ws.uni + j);
-            int sl = e >= 0 && e < A.E ? A.slot_of[e] : -1;
-            // a slot outside the arrays or inside the staging range cannot hold a hot expert
-            if (sl >= A.n_slots || (sl >= A.stage0 && sl < A.stage0 + A.n_stage)) {
-                bad = true;
-                sl = -1;
-            }
-            if (sl < 0 && e >= 0 && e < A.E && nc < A.n_stage) {
-                src[nc] = e;
-                dst[nc] = A.stage0 + nc;
-                sl = A.stage0 + nc;
-                nc++;
-            }
-            if (blockIdx.x == 0) A.ws.uslot[j] = sl;
-        }
-        if (bad && blockIdx.x == 0) flag(A.ws.status, FPX_EDATA);
-        ncold = nc;
+    __shared__ int ncopy;
+    if (threadIdx.x == 0) ncopy = min(__ldcg(A.ws.stage), A.qk);
+    if (threadIdx.x < A.qk) {
+        src[threadIdx.x] = __ldcg(A.ws.stage + 1 + threadIdx.x);
+        dst[threadIdx.x] = __ldcg(A.ws.stage + 1 + A.qk + threadIdx.x);
     }
     __syncthreads();
     // copy the cold items: per item gate (mb2), up (mb2), down (mb3) bytes, in 16-byte units
     const int64_t u2 = A.mb2 / 16, u3 = A.mb3 / 16, per = 2 * u2 + u3;
-    const int64_t total = per * ncold;
+    const int64_t total = per * ncopy;
     const int64_t stride = (int64_t)gridDim.x * kStageThreads;
     int64_t u = (int64_t)blockIdx.x * kStageThreads + threadIdx.x;
     auto addr = [&](int64_t v, const uint4*& from, uint4*& to) {
@@ -1235,6 +1324,7 @@ int launch_layer(const moe_layer& L, const Plan& p, int k, const uint16_t* x, co
     if (tier) {
         StageArgs sa = *tier;
         sa.ws = ws;
+        e = e ? e : launch(k_stage_plan, 1, 32, 0, s, pdl, sa);
         e = e ? e : launch(k_stage, 4 * device_info().sms, kStageThreads, 0, s, pdl, sa);
     }
     if (ev) cudaEventRecord(ev[1], s);
@@ -1312,9 +1402,10 @@ int moe_layer_decode_tiered(const moe_layer* layer, const moe_tiers* tiers, cons
     if (!tiers->slot_of || !tiers->cold_gate || !tiers->cold_up || !tiers->cold_down) return FPX_EINVAL;
     const int need = q * k < layer->E ? q * k : layer->E;  // the largest union
     if (tiers->n_slots < 1 || tiers->stage_slot0 < 0 || tiers->n_stage < need ||
-        (int64_t)tiers->stage_slot0 + tiers->n_stage > tiers->n_slots)
+        (int64_t)tiers->stage_slot0 + tiers->n_stage > tiers->n_slots || (tiers->cache && tiers->n_stage > kMaxStageCache))
         return FPX_EINVAL;
-    if (!aligned(ws, 16) || !aligned(x, 4) || !aligned(y, 4) || !aligned(tiers->slot_of, 4)) return FPX_EALIGN;
+    if (!aligned(ws, 16) || !aligned(x, 4) || !aligned(y, 4) || !aligned(tiers->slot_of, 4) || !aligned(tiers->cache, 4))
+        return FPX_EALIGN;
     Ws wl = ws_layout(layer->H, layer->I, layer->E, q, k);
     if (ws_bytes < wl.total) return FPX_ESPACE;
     // the cold tier must be pinned host memory the device can read
@@ -1345,9 +1436,22 @@ int moe_layer_decode_tiered(const moe_layer* layer, const moe_tiers* tiers, cons
     sa.stage0 = tiers->stage_slot0;
     sa.n_stage = tiers->n_stage;
     sa.qk = q * k;
+    sa.cache = tiers->cache;
     Plan p = make_plan(*layer, q, k);
     return dispatch_q<0>(q, *layer, p, k, x, nullptr, y, idx_out, w_out, logits_out, nullptr, wp, true, nullptr, false, s,
                          &sa);
+}
+
+int moe_tiers_cache_reset(const moe_tiers* tiers, void* stream) {
+    if (!tiers || !tiers->cache || tiers->n_stage < 1 || tiers->n_stage > kMaxStageCache) return FPX_EINVAL;
+    if (!aligned(tiers->cache, 4)) return FPX_EALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t n = (size_t)tiers->n_stage;
+    // clock and copy count 0, every slot empty (-1), last uses 0
+    if (cudaMemsetAsync(tiers->cache, 0, sizeof(int32_t) * (2 + 2 * n), s) != cudaSuccess ||
+        cudaMemsetAsync(tiers->cache + 2, 0xFF, sizeof(int32_t) * n, s) != cudaSuccess)
+        return FPX_ECUDA;
+    return FPX_OK;
 }
 
 int moe_stack_verify(const moe_layer* layers, int n_layers, const float* r0, int q, int k, float* rL, int32_t* idx_out,

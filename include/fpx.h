@@ -206,7 +206,12 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
  *               link, so they must stay pinned and unchanged during the call;
  *   stage_slot0, n_stage: the HBM slots [stage_slot0, stage_slot0 + n_stage) that receive the cold
  *               experts a call needs; n_stage >= min(q * k, E), stage_slot0 + n_stage <= n_slots,
- *               and no hot expert may sit in that range. */
+ *               and no hot expert may sit in that range;
+ *   cache       nullable device int32 [2 + 2 n_stage] (n_stage <= 1024 then): the staging slots keep
+ *               their experts across calls (see moe_tiers_cache_reset). Layout: [0] a call counter,
+ *               [1] the number of experts copied so far, [2 + i] the expert held by staging slot i
+ *               (-1: none), [2 + n_stage + i] the counter value of slot i's last use. NULL: every
+ *               call copies every cold expert of its union. */
 typedef struct {
     const int32_t* slot_of;
     const uint8_t* cold_gate;
@@ -215,20 +220,32 @@ typedef struct {
     int n_slots;
     int stage_slot0;
     int n_stage;
+    int32_t* cache;
 } moe_tiers;
 
-/* moe_layer_decode on a two-tier layer: after routing, every cold expert of the union is copied from
- * the host tier into a staging slot (in ascending expert order: the i-th cold item takes slot
- * stage_slot0 + i), and the layer runs on the slots. Results (y, routing, logits) are bit-identical to
- * moe_layer_decode on a layer holding all E experts in HBM. A slot_of entry >= n_slots or inside the
- * staging range sets FPX_EDATA in the status word and that expert is treated as cold. Same workspace
- * as moe_layer_decode. Returns FPX_EINVAL if a cold pointer is not pinned host memory; the staging
- * slots are overwritten by every call, so calls sharing them must be ordered on one stream. The
- * pages' own design computes cold experts on the CPU cores; here every expert runs on the GPU and
- * only the weights move (the Paiton page's streaming mode). */
+/* moe_layer_decode on a two-tier layer: after routing, every cold expert of the union gets a staging
+ * slot and the layer runs on the slots. Without a cache the i-th cold item (ascending expert order)
+ * takes slot stage_slot0 + i and is copied from the host tier. With tiers->cache, a cold expert that a
+ * staging slot already holds is used there without a copy; each other one is copied into the slot
+ * whose last use is oldest among the slots this call has not taken (ties to the lower slot), and the
+ * cache records it. Results (y, routing, logits) are bit-identical to moe_layer_decode on a layer
+ * holding all E experts in HBM. A slot_of entry >= n_slots or inside the staging range sets FPX_EDATA
+ * in the status word and that expert is treated as cold. Same workspace as moe_layer_decode. Returns
+ * FPX_EINVAL if a cold pointer is not pinned host memory or (with a cache) n_stage > 1024; calls
+ * sharing staging slots or a cache must be ordered on one stream. The pages' own design computes
+ * cold experts on the CPU cores; here every expert runs on the GPU and only the weights move (the
+ * Paiton page's streaming mode). The host link (about 51 GB/s measured) is the bound of a call that
+ * copies: an expert's three matrices take about 0.18 ms, against about 0.07 ms for the whole layer
+ * from HBM, which is why a cached expert is not copied again. */
 int moe_layer_decode_tiered(const moe_layer* layer, const moe_tiers* tiers, const uint16_t* x, int q, int k,
                             float* y, int32_t* idx_out, float* w_out, float* logits_out, void* ws,
                             size_t ws_bytes, void* stream);
+
+/* Empties tiers->cache (enqueued on stream): counter and copy count 0, no expert in any staging slot.
+ * Call it before the first moe_layer_decode_tiered with that cache, and again whenever the cold tier's
+ * contents, slot_of or the staging slots change outside these calls: the cache trusts that a slot
+ * still holds the expert it recorded. FPX_EINVAL without a cache or with n_stage outside 1..1024. */
+int moe_tiers_cache_reset(const moe_tiers* tiers, void* stream);
 
 /* moe_layer_decode for callers that cannot allocate device memory: a plugin or library running
  * inside a host framework that owns every device allocation (its own arena or allocator) and allows

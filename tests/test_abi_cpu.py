@@ -82,6 +82,29 @@ def test_layer_argument_errors():
     assert L.moe_stack_verify(arr, 0, FAKE, 4, 4, FAKE, None, None, FAKE, ws, None, None) == fpx.FPX_EINVAL
 
 
+def test_tiers_cache_argument_errors():
+    L = fpx.lib()
+    t = fpx.moe_tiers(slot_of=FAKE, cold_gate=FAKE, cold_up=FAKE, cold_down=FAKE, n_slots=32, stage_slot0=16,
+                      n_stage=16, cache=None)
+    assert L.moe_tiers_cache_reset(None, None) == fpx.FPX_EINVAL
+    assert L.moe_tiers_cache_reset(ctypes.byref(t), None) == fpx.FPX_EINVAL  # no cache
+    t.cache = FAKE
+    t.n_stage = 0
+    assert L.moe_tiers_cache_reset(ctypes.byref(t), None) == fpx.FPX_EINVAL
+    t.n_stage = 1025  # a cache tracks at most 1024 staging slots
+    assert L.moe_tiers_cache_reset(ctypes.byref(t), None) == fpx.FPX_EINVAL
+    t.n_stage, t.cache = 16, FAKE + 2
+    assert L.moe_tiers_cache_reset(ctypes.byref(t), None) == fpx.FPX_EALIGN
+    lay = _layer()
+    ws = fpx.moe_workspace_bytes(lay, 4, 4)
+    call = lambda tt: L.moe_layer_decode_tiered(ctypes.byref(lay), ctypes.byref(tt), FAKE, 4, 4, FAKE, None, None,
+                                                None, FAKE, ws, None)
+    t.cache, t.n_slots, t.n_stage = FAKE, 1041, 1025
+    assert call(t) == fpx.FPX_EINVAL  # too many staging slots for the cache
+    t.n_slots, t.n_stage, t.cache = 32, 16, FAKE + 2
+    assert call(t) == fpx.FPX_EALIGN
+
+
 def test_wait_hook_argument_errors():
     L = fpx.lib()
     assert L.fpx_debug_ring_wait(0, -1) == fpx.FPX_EINVAL             # no limit
