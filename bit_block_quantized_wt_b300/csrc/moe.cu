@@ -969,7 +969,8 @@ __global__ void __launch_bounds__(kLThreads, 1) k_down(const __grid_constant__ D
 
 // out[t][h] (MODE 0) or r[t][h] += (MODE 1) sum over token t's selected experts, in ascending expert
 // order, of w * y_e[t][h] (pieces added in order first), then the shared expert's y[t][h]. One thread per
-// output; consecutive threads take consecutive rows.
+// output; consecutive threads take consecutive rows. Only the token's k items and the shared one are
+// loaded, all at once.
 struct CombineArgs {
     int H, I, k;
     WsPtrs ws;
@@ -977,21 +978,29 @@ struct CombineArgs {
 };
 
 constexpr int kCombineThreads = 256;
-constexpr int kCombineBatch = 17;  // items whose loads are in flight together: q * k = 16 routed + shared
 constexpr int kKernelsPerLayer = 5;  // router, gate/up, h + down tables, down, combine
 
 template <int Q, int MODE>
 __global__ void __launch_bounds__(kCombineThreads) k_combine(const __grid_constant__ CombineArgs A) {
     __shared__ Route r;
-    __shared__ float wsel[kMaxQ * kMaxK + 1][kMaxQ];  // weight of token t for union item j, NaN if unselected
+    __shared__ int sel[kMaxQ][kMaxK];     // union index of token t's selected experts, ascending
+    __shared__ float selw[kMaxQ][kMaxK];  // their weights
     grid_dep_trigger();
     load_route(r, A.ws, Q * A.k);  // from the router kernel (completed two launches ago)
-    for (int i = threadIdx.x; i < r.n_uni * Q; i += blockDim.x) {
-        const int j = i / Q, tok = i % Q;
-        float wv = __int_as_float(0x7fc00000);
-        for (int rr = 0; rr < A.k; rr++)
-            if (r.idx[tok * A.k + rr] == r.uni[j]) wv = r.w[tok * A.k + rr];
-        wsel[j][tok] = wv;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    if (warp < Q) {  // warp t: the union items token t selected (each selected once), in union order
+        const int tok = warp;
+        float wv = 0.f;
+        bool on = false;
+        if (lane < r.n_uni)
+            for (int rr = 0; rr < A.k; rr++)
+                if (r.idx[tok * A.k + rr] == r.uni[lane]) { on = true; wv = r.w[tok * A.k + rr]; }
+        const uint32_t m = __ballot_sync(0xffffffffu, on);
+        if (on) {
+            const int pos = __popc(m & ((1u << lane) - 1u));
+            sel[tok][pos] = lane;
+            selw[tok][pos] = wv;
+        }
     }
     // the fixed pieces of the routed (FP3, I/256 stages) and shared (FP4, I/512 stages) down tasks
     const int H = A.H, np_r = pieces_of(A.I / stage_k(3), kSppDn), np_s = pieces_of(A.I / stage_k(4), kSppDn);
@@ -999,40 +1008,35 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(const __grid_consta
     grid_dep_wait();  // the down kernel's outputs
     const int o = blockIdx.x * kCombineThreads + threadIdx.x;
     if (o >= Q * H) return;
-    const int tok = o / H, rr = o % H;
+    const int tok = o / H, rr = o % H, k = A.k;
     const float* col = A.ws.yi + (size_t)tok * H + rr;
     const size_t istride = (size_t)Q * H;
-    // every piece slot of items 0 .. q * k lies in the workspace, so the loads of a batch are issued
-    // unconditionally (all in flight at once) and unused values are dropped; then the fixed-order sum
-    // (pieces of an item in order, items in ascending expert order, the shared expert n_uni last)
-    float acc = 0.0f, ysh = 0.0f;
-    bool first = true;
-    const int jmax = Q * A.k;  // last item slot of the workspace
-    for (int j0 = 0; j0 <= r.n_uni; j0 += kCombineBatch) {
-        float pv[kCombineBatch][kMaxPieces];
+    float pv[kMaxK][kMaxPieces], ps[kMaxPieces];
 #pragma unroll
-        for (int u = 0; u < kCombineBatch; u++) {
-            const int jj = min(j0 + u, jmax);
+    for (int i = 0; i < kMaxK; i++) {
+        const size_t jo = (size_t)(i < k ? sel[tok][i] : 0) * istride;
 #pragma unroll
-            for (int p = 0; p < kMaxPieces; p++)
-                pv[u][p] = p < np_r ? __ldcg(col + p * A.ws.yi_piece + (size_t)jj * istride) : 0.0f;
-        }
+        for (int p = 0; p < kMaxPieces; p++) pv[i][p] = i < k && p < np_r ? __ldcg(col + p * A.ws.yi_piece + jo) : 0.0f;
+    }
 #pragma unroll
-        for (int u = 0; u < kCombineBatch; u++) {
-            const int jj = j0 + u;
-            if (jj > r.n_uni) break;
-            const int np = jj < r.n_uni ? np_r : np_s;
-            float yv = pv[u][0];
+    for (int p = 0; p < kMaxPieces; p++)
+        ps[p] = p < np_s ? __ldcg(col + p * A.ws.yi_piece + (size_t)r.n_uni * istride) : 0.0f;
+    // the fixed-order sum: pieces of an item in order, items in ascending expert order, shared last
+    float acc = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kMaxK; i++) {
+        if (i < k) {
+            float yv = pv[i][0];
 #pragma unroll
             for (int p = 1; p < kMaxPieces; p++)
-                if (p < np) yv += pv[u][p];
-            if (jj == r.n_uni) { ysh = yv; break; }
-            const float wv = wsel[jj][tok];
-            if (wv != wv) continue;  // expert not selected by this token
-            acc = first ? wv * yv : fmaf(wv, yv, acc);
-            first = false;
+                if (p < np_r) yv += pv[i][p];
+            acc = i == 0 ? selw[tok][i] * yv : fmaf(selw[tok][i], yv, acc);
         }
     }
+    float ysh = ps[0];
+#pragma unroll
+    for (int p = 1; p < kMaxPieces; p++)
+        if (p < np_s) ysh += ps[p];
     acc += ysh;
     if (MODE == 0) A.out[o] = acc;
     else A.out[o] = A.out[o] + acc;
