@@ -700,7 +700,8 @@ int fpx_gemv_q(int fmt, const uint8_t* Wq, int64_t N, int64_t K, const void* x, 
     if (N > INT32_MAX || K > INT32_MAX / 8) return FPX_EINVAL;
     if (N == 0) return FPX_OK;
     if (!Wq || !x || !y) return FPX_EINVAL;
-    if (!aligned(Wq, 16) || !aligned(x, 4) || !aligned(y, 4)) return FPX_EALIGN;
+    // the tensor-core path's table builder reads x in 16-byte units
+    if (!aligned(Wq, 16) || !aligned(x, 16) || !aligned(y, 4)) return FPX_EALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return cudaMemsetAsync(y, 0, sizeof(float) * (size_t)q * N, s) == cudaSuccess ? FPX_OK : FPX_ECUDA;
     int bf = x_dtype == FPX_DTYPE_BF16;

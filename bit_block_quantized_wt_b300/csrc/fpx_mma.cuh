@@ -549,12 +549,13 @@ __device__ __forceinline__ void add_offsets(uint8_t* ts, int K, int tok, int k0,
 // Builds the activation tables for columns src[tok][k] (tok < q <= 4, K % 64 == 0) in format FMT:
 // tab (FP2, FP3 low plane, or FP4), tab_hi (FP3 high plane) and, for FP2/FP3, the negated block
 // offsets oq (the MMA's initial accumulator); WITH4 also builds the FP4 table tab4 from the same
-// columns. shift[4] receives the column shifts. Each thread owns whole 16-weight code groups: it
+// columns. BOX3: FP3 as the one box-layout table of the tiled boxes (pack_fp3b; tab_hi unused).
+// shift[4] receives the column shifts. Each thread owns whole 16-weight code groups: it
 // issues all of a pass's loads before using them and writes each table entry with two 16-byte
 // stores. CONS: only the kWarps consumer warps (threads 0 .. 32 kWarps - 1) take part and
 // synchronise on the consumer barrier, so the producer warp can issue loads meanwhile; otherwise the
 // whole CTA.
-template <int FMT, bool WITH4, bool CONS = false, class SRC>
+template <int FMT, bool WITH4, bool CONS = false, bool BOX3 = false, class SRC>
 __device__ void build_tables(const SRC src, int K, int q, uint2* tab, uint2* tab_hi, uint2* tab4, float* oq, int* shift,
                              float* red4) {
     constexpr int V = SRC::V;
@@ -596,7 +597,7 @@ __device__ void build_tables(const SRC src, int K, int q, uint2* tab, uint2* tab
         if (((i & 15) >> 1 & 3) >= q) {
             reinterpret_cast<uint4*>(tab + (size_t)i * 4)[0] = z;
             reinterpret_cast<uint4*>(tab + (size_t)i * 4)[1] = z;
-            if (FMT == 3) {
+            if (FMT == 3 && !BOX3) {
                 reinterpret_cast<uint4*>(tab_hi + (size_t)i * 4)[0] = z;
                 reinterpret_cast<uint4*>(tab_hi + (size_t)i * 4)[1] = z;
             }
@@ -634,6 +635,9 @@ __device__ void build_tables(const SRC src, int K, int q, uint2* tab, uint2* tab
                 uint32_t w[8];
                 if constexpr (FMT == 2) {
                     pack_fp2(v[it], sh, w, part);
+                    store_entry(tab, e, w);
+                } else if constexpr (FMT == 3 && BOX3) {
+                    pack_fp3b(v[it], sh, c & 1, w, part);
                     store_entry(tab, e, w);
                 } else if constexpr (FMT == 3) {
                     uint32_t wh[8];

@@ -1363,7 +1363,7 @@ int moe_route_topk(const float* R, int E, int H, const uint16_t* x, int q, int k
                    int32_t* uni, int32_t* n_uni, void* stream) {
     if (E < 1 || E > kMaxE || H < 16 || H % 16 || q < 1 || q > kMaxQ || k < 1 || k > kMaxK || k > E) return FPX_EINVAL;
     if (!R || !x || !logits || !idx || !w || !uni || !n_uni) return FPX_EINVAL;
-    if (!aligned(R, 16) || !aligned(x, 4) || !aligned(logits, 4)) return FPX_EALIGN;
+    if (!aligned(R, 16) || !aligned(x, 8) || !aligned(logits, 4)) return FPX_EALIGN;  // x read in 8-byte units
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t sm = router_smem(q, H);
     if (sm > (size_t)device_info().smem_optin) return FPX_EINVAL;
@@ -1387,7 +1387,7 @@ int moe_layer_decode(const moe_layer* layer, const uint16_t* x, int q, int k, fl
     int st = check_layer(layer);
     if (st) return st;
     if (q < 1 || q > kMaxQ || k < 1 || k > kMaxK || k > layer->E || !x || !y || !ws) return FPX_EINVAL;
-    if (!aligned(ws, 16) || !aligned(x, 4) || !aligned(y, 4)) return FPX_EALIGN;
+    if (!aligned(ws, 16) || !aligned(x, 8) || !aligned(y, 4)) return FPX_EALIGN;  // the router reads x in 8-byte units
     Ws wl = ws_layout(layer->H, layer->I, layer->E, q, k);
     if (ws_bytes < wl.total) return FPX_ESPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1408,7 +1408,7 @@ int moe_layer_decode_tiered(const moe_layer* layer, const moe_tiers* tiers, cons
     if (tiers->n_slots < 1 || tiers->stage_slot0 < 0 || tiers->n_stage < need ||
         (int64_t)tiers->stage_slot0 + tiers->n_stage > tiers->n_slots || (tiers->cache && tiers->n_stage > kMaxStageCache))
         return FPX_EINVAL;
-    if (!aligned(ws, 16) || !aligned(x, 4) || !aligned(y, 4) || !aligned(tiers->slot_of, 4) || !aligned(tiers->cache, 4))
+    if (!aligned(ws, 16) || !aligned(x, 8) || !aligned(y, 4) || !aligned(tiers->slot_of, 4) || !aligned(tiers->cache, 4))
         return FPX_EALIGN;
     Ws wl = ws_layout(layer->H, layer->I, layer->E, q, k);
     if (ws_bytes < wl.total) return FPX_ESPACE;

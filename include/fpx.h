@@ -27,7 +27,9 @@
  *
  * Conventions for every call:
  *   - Pointers named in a signature are DEVICE pointers owned by the caller, unless a comment says
- *     host. Matrix and workspace pointers must be 16-byte aligned (FPX_EALIGN otherwise); vectors 4-.
+ *     host. Matrix and workspace pointers must be 16-byte aligned (FPX_EALIGN otherwise); vectors 4-,
+ *     except where a call says otherwise (the activations of the tensor-core GEMVs 16-, of the
+ *     router and decode-layer calls 8-byte, which their kernels read in 16- or 8-byte units).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream), never
  *     allocate and never synchronise; they are safe to capture in a CUDA graph. The return value
  *     reports argument errors and launch failures only.
@@ -124,7 +126,8 @@ int fpx_tile_matrices(int fmt, const uint8_t* src, int64_t N, int64_t K, int cou
  * Every packed block is read from memory and decoded once per call, whatever q. x is [q][K]
  * contiguous, binary32 (x_dtype FPX_DTYPE_F32) or bfloat16 (FPX_DTYPE_BF16); y is [q][N] binary32.
  * Column t of the result is bit-identical to a q = 1 call on x[t]. An FP4 scale byte of 255 sets
- * the FPX_EDATA bit of *dev_status (nullable; that block counts as zeros). [P-dsv4] paragraph 3, [P-apu]. */
+ * the FPX_EDATA bit of *dev_status (nullable; that block counts as zeros). x must be 16-byte aligned
+ * (FPX_EALIGN otherwise). [P-dsv4] paragraph 3, [P-apu]. */
 int fpx_gemv_q(int fmt, const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_dtype, int q,
                float* y, int32_t* dev_status, void* stream);
 
@@ -140,7 +143,7 @@ size_t fpx_gemv_idot_workspace_bytes(int64_t K, int q);
  * (|X| <= 2^14, sent as a signed high byte and an unsigned low byte), so every block dot product is an
  * exact integer and y[t][n] = sum_b d_nb 2^(e_tb - 14) sum_j v_j X_j, i.e. the plain GEMV of
  * x_hat = X 2^(e-14) up to binary32 rounding of the block terms and of their sums (|x_hat - x| <=
- * 2^(e-15)). Same arguments and layouts as fpx_gemv_q, plus a caller workspace ws (16-byte aligned,
+ * 2^(e-15)). Same arguments and layouts as fpx_gemv_q (x 4-byte aligned suffices), plus a caller workspace ws (16-byte aligned,
  * >= fpx_gemv_idot_workspace_bytes(K, q) bytes, else FPX_ESPACE; overwritten) that carries the activation table from the
  * first kernel to the second. Requires K % 256 == 0 (FP2 / FP3) or K % 512 == 0 (FP4), so rows are
  * whole 16-byte units, and K * q small enough for the table to sit in shared memory next to two weight
@@ -156,7 +159,7 @@ int fpx_gemv_q_idot(int fmt, const uint8_t* Wq, int64_t N, int64_t K, const void
  * sorted distinct experts of all tokens (n_uni of them, at most q*k; uni has q*k entries).
  * Limits: 1 <= k <= 8, k <= E <= 1024, H % 16 == 0, and (2q + 8) H bytes within the device's shared
  * memory per block (x and two router rows are staged there: H <= 14528 at q = 4 with 227 KB),
- * FPX_EINVAL otherwise. logits [q][E] is required: it is also the top-k input. [P-apu], [P-dsv4]
+ * FPX_EINVAL otherwise; x 8-byte aligned (FPX_EALIGN otherwise). logits [q][E] is required: it is also the top-k input. [P-apu], [P-dsv4]
  * paragraph 3. */
 int moe_route_topk(const float* R, int E, int H, const uint16_t* x, int q, int k, float* logits,
                    int32_t* idx, float* w, int32_t* uni, int32_t* n_uni, void* stream);
@@ -186,7 +189,7 @@ size_t moe_workspace_bytes(const moe_layer* layer, int q, int k);
 /* One MoE decode/verify layer for q tokens (1 <= q <= 4, 1 <= k <= 8): route each token, run every
  * selected expert once for all q columns (g = G x, u = U x, h = silu(g) u in binary32, y = D h), the
  * shared expert for all tokens, and combine out[t] = sum_r w[t][r] y_{e(t,r)}[t] + y_shared[t]
- * (ranks in order, shared last). x is bfloat16 [q][H], y binary32 [q][H]; idx_out (nullable) gets
+ * (ranks in order, shared last). x is bfloat16 [q][H] (8-byte aligned), y binary32 [q][H]; idx_out (nullable) gets
  * idx[q][k], w_out (nullable) w[q][k], logits_out (nullable) logits[q][E]. `ws` must hold
  * moe_workspace_bytes(layer, q, k) bytes (ws_bytes); its first word is the status word. The layer
  * pointer is read on the host during the call only. [P-dsv4] paragraph 3, [P-zh], [P-apu]. */

@@ -45,6 +45,7 @@ FAKE = 1 << 20  # an aligned non-null address; these calls must fail before touc
     ((2, None, 8, 64, FAKE, 1, 1, FAKE), fpx.FPX_EINVAL),   # null weights
     ((2, FAKE + 8, 8, 64, FAKE, 1, 1, FAKE), fpx.FPX_EALIGN),  # weights not 16-byte aligned
     ((2, FAKE, 8, 64, FAKE + 2, 1, 1, FAKE), fpx.FPX_EALIGN),  # x not 4-byte aligned
+    ((2, FAKE, 8, 64, FAKE + 4, 1, 1, FAKE), fpx.FPX_EALIGN),  # x not 16-byte aligned (read in 16-byte units)
 ])
 def test_gemv_argument_errors(args, expect):
     fmt, W, N, K, x, dt, q, y = args
@@ -77,6 +78,8 @@ def test_layer_argument_errors():
     assert call(good, k=17) == fpx.FPX_EINVAL
     assert call(good, wsb=ws - 16) == fpx.FPX_ESPACE
     assert call(good, wsp=FAKE + 8) == fpx.FPX_EALIGN
+    # the router reads x in 8-byte units
+    assert L.moe_layer_decode(ctypes.byref(good), FAKE + 4, 4, 4, FAKE, None, None, None, FAKE, ws, None) == fpx.FPX_EALIGN
     arr = (fpx.moe_layer * 2)(good, _layer(I=1024))
     assert L.moe_stack_verify(arr, 2, FAKE, 4, 4, FAKE, None, None, FAKE, ws, None, None) == fpx.FPX_EINVAL
     assert L.moe_stack_verify(arr, 0, FAKE, 4, 4, FAKE, None, None, FAKE, ws, None, None) == fpx.FPX_EINVAL
@@ -117,6 +120,7 @@ def test_route_and_quant_argument_errors():
     assert L.moe_route_topk(FAKE, 8, 64, FAKE, 4, 9, FAKE, FAKE, FAKE, FAKE, FAKE, None) == fpx.FPX_EINVAL
     assert L.moe_route_topk(FAKE, 8, 64, FAKE, 4, 2, None, FAKE, FAKE, FAKE, FAKE, None) == fpx.FPX_EINVAL
     assert L.moe_route_topk(FAKE, 2000, 64, FAKE, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None) == fpx.FPX_EINVAL
+    assert L.moe_route_topk(FAKE, 8, 64, FAKE + 4, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None) == fpx.FPX_EALIGN
     # x and two router rows staged in shared memory: (2 q + 8) H = 256 KB does not fit
     assert L.moe_route_topk(FAKE, 8, 16384, FAKE, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None) == fpx.FPX_EINVAL
     assert L.fpx_quantize(2, FAKE, 4, 48, None, FAKE, None, None) == fpx.FPX_EINVAL
