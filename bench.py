@@ -488,8 +488,10 @@ ID_N, ID_K = 148 * 64 * 16, 4096  # integer-dot comparison: 151,552 rows (FP2 19
 
 def idot_measure(fpx, peak, reps=10):
     """fpx_gemv_q_idot (byte-permute expansion + dp4a) against fpx_gemv_q (binary16 decode + tensor-core
-    MMA) on the same packed matrices, q = 4 and q = 1, CUDA events. Packed bytes are uniform (scales
-    included; the values do not change the work). Bytes per call: the packed matrix."""
+    MMA) and fpx_gemv_q_tiled (the same decode on the box-tiled layout, streamed like the MoE layer's
+    experts) on matrices of the same size, q = 4 and q = 1, CUDA events. Packed bytes are uniform
+    (scales included; the values do not change the work, and a tiled matrix of uniform bytes is again
+    uniform). Bytes per call: the packed matrix."""
     import torch
     g = torch.Generator(device="cuda").manual_seed(13)
     res = {}
@@ -497,6 +499,8 @@ def idot_measure(fpx, peak, reps=10):
     y = torch.empty(4, ID_N, device="cuda")
     wsb = fpx.fpx_gemv_idot_workspace_bytes(ID_K, 4)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    wtb = max(fpx.fpx_gemv_tiled_workspace_bytes(fmt, ID_N, ID_K, 4) for fmt in (2, 3, 4))
+    wt = torch.empty(wtb, dtype=torch.uint8, device="cuda")
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for fmt in (2, 3, 4):
         nb = fpx.fpx_matrix_bytes(fmt, ID_N, ID_K)
@@ -504,7 +508,9 @@ def idot_measure(fpx, peak, reps=10):
         for q in ((4, 1) if fmt == 2 else (4,)):
             for name, call in (("int_dot", lambda: fpx.fpx_gemv_q_idot(fmt, Wq, ID_N, ID_K, x, fpx.FPX_DTYPE_BF16, q,
                                                                         y, ws, wsb)),
-                               ("tensor_core", lambda: fpx.fpx_gemv_q(fmt, Wq, ID_N, ID_K, x, fpx.FPX_DTYPE_BF16, q, y))):
+                               ("tensor_core", lambda: fpx.fpx_gemv_q(fmt, Wq, ID_N, ID_K, x, fpx.FPX_DTYPE_BF16, q, y)),
+                               ("tensor_core_tiled", lambda: fpx.fpx_gemv_q_tiled(fmt, Wq, ID_N, ID_K, x, fpx.FPX_DTYPE_BF16,
+                                                                                  q, y, wt, wtb))):
                 for _ in range(3):
                     call()
                 torch.cuda.synchronize()

@@ -65,6 +65,10 @@ _SIGS = {
     "fpx_gemv_q_idot": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "fpx_gemv_tiled_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int]),
+    "fpx_gemv_q_tiled": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
     "moe_route_topk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
@@ -186,6 +190,16 @@ def fpx_gemv_q_idot(fmt, Wq, N, K, x, x_dtype, q, y, ws, ws_bytes, dev_status=No
     """Integer-dot variant of fpx_gemv_q (see include/fpx.h)."""
     _check(lib().fpx_gemv_q_idot(fmt, _ptr(Wq), N, K, _ptr(x), x_dtype, q, _ptr(y), _ptr(ws), ws_bytes,
                                  _ptr(dev_status), _stream(stream)), "fpx_gemv_q_idot")
+
+
+def fpx_gemv_tiled_workspace_bytes(fmt, N, K, q):
+    return lib().fpx_gemv_tiled_workspace_bytes(fmt, N, K, q)
+
+
+def fpx_gemv_q_tiled(fmt, Wt, N, K, x, x_dtype, q, y, ws, ws_bytes, dev_status=None, stream=None):
+    """fpx_gemv_q on a box-tiled matrix (see include/fpx.h)."""
+    _check(lib().fpx_gemv_q_tiled(fmt, _ptr(Wt), N, K, _ptr(x), x_dtype, q, _ptr(y), _ptr(ws), ws_bytes,
+                                  _ptr(dev_status), _stream(stream)), "fpx_gemv_q_tiled")
 
 
 def moe_route_topk(R, E, H, x, q, k, logits, idx, w, uni, n_uni, stream=None):

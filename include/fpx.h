@@ -153,6 +153,26 @@ size_t fpx_gemv_idot_workspace_bytes(int64_t K, int q);
 int fpx_gemv_q_idot(int fmt, const uint8_t* Wq, int64_t N, int64_t K, const void* x, int x_dtype, int q,
                     float* y, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* Workspace bytes fpx_gemv_q_tiled needs for these shapes: P * q * N * 4 (the partial rows of P > 1
+ * pieces, see below), else 16. 0 for invalid arguments. */
+size_t fpx_gemv_tiled_workspace_bytes(int fmt, int64_t N, int64_t K, int q);
+
+/* fpx_gemv_q on one box-tiled matrix (fpx_tile_matrices with count 1): y[t][n] = sum_k W[n][k] x[t][k]
+ * for t < q (1 <= q <= 4), streamed the way the MoE layer kernels stream their experts (one bulk copy
+ * per tile of R rows, decoded by the same tensor-core engine; exact products, binary32 sums). Requires
+ * N % R == 0 (R = 256 for FP2 / FP3, 64 for FP4), K % 256 == 0 (FP2 / FP3) or K % 512 == 0 (FP4), and
+ * the activation table (9 K bytes FP2 / FP3, 8 K FP4) beside a 140 KB ring within the shared memory
+ * per block (K <= 9728 with 227 KB), FPX_EINVAL otherwise; Wt, x and ws 16-byte aligned, y 4-byte.
+ * ws holds at least fpx_gemv_tiled_workspace_bytes(fmt, N, K, q) bytes (FPX_ESPACE otherwise) and is
+ * overwritten. A row tile's K range is split into P = min(K / stage, ceil(592 / (N / R))) pieces of
+ * consecutive stages (stage = 256 weights FP2 / FP3, 512 FP4), a function of N and K alone, whose sums
+ * are added in piece order: column t of the result is bit-identical to a q = 1 call on x[t]. The sums
+ * run in another order than fpx_gemv_q's, so the two agree within the GEMV tolerance, not bit for
+ * bit. An FP4 scale byte of 255 sets FPX_EDATA in *dev_status (nullable; that block counts as zeros).
+ * [P-dsv4] paragraph 3. */
+int fpx_gemv_q_tiled(int fmt, const uint8_t* Wt, int64_t N, int64_t K, const void* x, int x_dtype, int q,
+                     float* y, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /* Router + top-k + normalise + union for q tokens (1 <= q <= 4): logits[t][e] = sum_h R[e][h] x[t][h]
  * (R binary32 [E][H], x bfloat16 [q][H]); idx[t][r], r < k, the k largest logits in descending order,
  * ties to the lower expert index; w[t][r] = sigmoid(l) / sum over the k selected sigmoids; uni the

@@ -108,6 +108,26 @@ def test_tiers_cache_argument_errors():
     assert call(t) == fpx.FPX_EALIGN
 
 
+def test_tiled_gemv_argument_errors():
+    L = fpx.lib()
+    assert fpx.fpx_gemv_tiled_workspace_bytes(2, 256, 4096, 4) == 16 * 4 * 256 * 4  # 16 pieces of one stage
+    assert fpx.fpx_gemv_tiled_workspace_bytes(2, 151552, 4096, 4) == 16            # 592 tiles: one piece
+    assert fpx.fpx_gemv_tiled_workspace_bytes(2, 255, 4096, 4) == 0
+    bf = fpx.FPX_DTYPE_BF16
+    call = lambda fmt=2, W=FAKE, N=256, K=512, x=FAKE, q=4, ws=FAKE, wb=1 << 20: L.fpx_gemv_q_tiled(
+        fmt, W, N, K, x, bf, q, FAKE, ws, wb, None, None)
+    assert call(fmt=5) == fpx.FPX_EINVAL
+    assert call(N=255) == fpx.FPX_EINVAL    # not whole row tiles
+    assert call(fmt=4, N=96) == fpx.FPX_EINVAL
+    assert call(K=384) == fpx.FPX_EINVAL    # not whole stages
+    assert call(fmt=4, K=768) == fpx.FPX_EINVAL
+    assert call(q=5) == fpx.FPX_EINVAL
+    assert call(ws=None) == fpx.FPX_EINVAL
+    assert call(W=FAKE + 8) == fpx.FPX_EALIGN
+    assert call(x=FAKE + 8) == fpx.FPX_EALIGN
+    assert call(wb=15) == fpx.FPX_ESPACE
+
+
 def test_wait_hook_argument_errors():
     L = fpx.lib()
     assert L.fpx_debug_ring_wait(0, -1) == fpx.FPX_EINVAL             # no limit
