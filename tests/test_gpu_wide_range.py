@@ -1,5 +1,5 @@
-"""Activations with a wide dynamic range through the tensor-core paths (dense GEMV, decode layer,
-prefill): +-0, bfloat16 subnormals, 32-entry blocks scaled by up to 2^+-20 and one spike per column.
+"""Activations with a wide dynamic range through the tensor-core paths (dense GEMV on row-major and
+box-tiled matrices, decode layer, prefill): +-0, bfloat16 subnormals, 32-entry blocks scaled by up to 2^+-20 and one spike per column.
 
 The tensor-core kernels take a column (or, in the prefill, a row) as binary16 scaled by one power of two
 that puts its largest element in [2^14, 2^15). A bfloat16 element within 2^31 of the column's largest is
@@ -44,6 +44,50 @@ def test_gemv_wide_range_fp2_fp3(fmt, spike):
     assert np.all(err <= TOL * M), float((err / M).max())
     for t in range(4):  # still bit-identical to a one-column call
         assert np.array_equal(gemv(fmt, Wq, N, K, bits[t : t + 1])[0], y[t])
+
+
+def gemv_tiled(fmt, Wq, N, K, bits):
+    """The same GEMV on the box-tiled copy of the matrix (fpx_gemv_q_tiled)."""
+    q = bits.shape[0]
+    src = dev(Wq)
+    Wt = torch.empty_like(src)
+    fpx.fpx_tile_matrices(fmt, src, N, K, 1, src.numel(), Wt, Wt.numel())
+    y = torch.full((q, N), float("nan"), device="cuda")
+    wb = fpx.fpx_gemv_tiled_workspace_bytes(fmt, N, K, q)
+    ws = torch.empty(wb, dtype=torch.uint8, device="cuda")
+    st = status_word()
+    fpx.fpx_gemv_q_tiled(fmt, Wt, N, K, dev(bits), fpx.FPX_DTYPE_BF16, q, y, ws, wb, dev_status=st)
+    assert read_status(st) == 0
+    return host(y)
+
+
+@pytest.mark.parametrize("fmt", [2, 3])
+@pytest.mark.parametrize("spike", [20, 60])
+def test_tiled_gemv_wide_range_fp2_fp3(fmt, spike):
+    need_gpu()
+    N, K = 512, 2048
+    Wq = synth.matrix(fmt, N, K, seed=50 + fmt)
+    bits, vals = wide_bf16(4, K, seed=spike + fmt + 7, spike_log2=spike, block_span=20)
+    y = gemv_tiled(fmt, Wq, N, K, bits)
+    yo, M = oracle.gemv(fmt, Wq, N, K, vals.astype(np.float64))
+    err = np.abs(y.astype(np.float64) - yo)
+    assert np.all(err <= TOL * M), float((err / M).max())
+    for t in range(4):
+        assert np.array_equal(gemv_tiled(fmt, Wq, N, K, bits[t : t + 1])[0], y[t])
+
+
+def test_tiled_gemv_fp4_zero_codes_spanning_2_60_meets_the_encoding_bound():
+    need_gpu()
+    N, K = 256, 2048
+    Wq = zero_fp4_codes(synth.matrix(4, N, K, seed=46), N, K, 0.5, seed=3)
+    bits, vals = wide_bf16(4, K, seed=6, spike_log2=60, block_span=20)
+    y = gemv_tiled(4, Wq, N, K, bits)
+    yo, M = oracle.gemv(4, Wq, N, K, vals.astype(np.float64))
+    absw = np.abs(oracle.dequantize(4, Wq, N, K)).sum(axis=1)
+    _, e = np.frexp(np.abs(vals.astype(np.float64)).max(axis=1))
+    bound = TOL * M + np.ldexp(1.0, e - 40)[:, None] * absw[None, :]
+    err = np.abs(y.astype(np.float64) - yo)
+    assert np.all(err <= bound), float((err / bound).max())
 
 
 def test_gemv_fp4_zero_codes_within_binary16_range():
