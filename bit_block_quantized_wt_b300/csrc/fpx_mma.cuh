@@ -18,12 +18,12 @@
 // unchanged.
 //
 // Exact decode. A pair of 2-bit codes is moved into the mantissa of a binary16 pair with one LOP3
-// (mask | 0x6400, the binary16 1024), and one HFMA2 removes the offset and applies the codebook:
-// 2 * (1024 + c * 2^P) - (2048 + 3 * 2^P) = 2^P (2c - 3). Every constant and result is exact in
-// binary16; the activation is stored as x * 2^-P so A * B = (2c - 3) * x exactly. FP3 adds the high bit
-// plane with a second HFMA2 (constants chosen so the intermediate stays exact), FP4 maps E2M1 bits
-// straight onto binary16 bits (value * 2^-14). Products are exact in binary32; only the tensor-core
-// accumulation rounds.
+// (mask | 0x6400, the binary16 1024), so the pair holds 1024 + c * 2^P exactly. The activation table
+// holds B = 2 x * 2^-P, and the MMA starts from the per-block constant -sum B (1024 + 1.5 * 2^P) (the
+// offset quads), so it sums (2c - 3) x directly. FP3 works the same way with 3-bit codes: one plane
+// in the box layout of the layer kernels, a low and a high plane (each its own MMAs) in the row-major
+// GEMV. FP4 maps E2M1 bits straight onto binary16 bits (value * 2^-14). Products are exact in
+// binary32; only the tensor-core accumulation rounds.
 #pragma once
 
 #include <cuda.h>
@@ -231,27 +231,12 @@ __device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint3
         : "memory");
 }
 
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
 // D = A * B + C, m16n8k16, binary16 inputs, binary32 accumulators.
 __device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// D = A * B (accumulators start at zero).
-__device__ __forceinline__ void mma_first(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1) {
-    const float z = 0.0f;
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
 }
 
 // ------------------------------------------------------------------ decode into A pairs
@@ -278,7 +263,6 @@ __host__ __device__ constexpr int fp3_box_shift(int odd, int p) {
 }
 
 constexpr uint32_t kMagic = 0x64006400u;  // binary16 pair (1024, 1024)
-constexpr uint32_t kTwo = f16x2(2.0);
 
 // Eight A pairs from 16 FP2 codes (2 bits each, code k at bits 2k..2k+1 of w): pair i holds codes
 // (i, i + 8) as the binary16 values 1024 + c * 2^P, one LOP3 each. The activations are stored as
@@ -297,30 +281,6 @@ __device__ __forceinline__ void decode_fp2(uint32_t w, uint32_t magic, uint32_t 
     a[5] = (s8 & 0x000C000Cu) | magic;
     a[6] = (s8 & 0x00300030u) | magic;
     a[7] = (s8 & 0x00C000C0u) | magic;
-}
-
-// FP3 high-bit plane: pair i places its two high bits at mantissa bit Q (i) and uses
-// A = (1024 + 2^Q h) * 2^(P+3-Q) + [2 (1024 + 2^P l) - (2048 + 7 * 2^P + 2^(P+13-Q))]
-//   = 2^P (2l + 8h - 7) = 2^P (2c - 7); the bracket (first HFMA2) is exact for 3 <= Q <= 9.
-template <int P, int Q>
-__host__ __device__ constexpr uint32_t fp3_off() { return f16x2(-(2048.0 + 7.0 * (1 << P) + double(1 << (P + 13 - Q)))); }
-template <int P, int Q>
-__host__ __device__ constexpr uint32_t fp3_mul() { return f16x2(P + 3 - Q >= 0 ? double(1 << (P + 3 - Q)) : 1.0 / double(1 << (Q - P - 3))); }
-
-// lo: 16 low-plane codes as in FP2; hg: the 16 high bits (bit k = code k).
-__device__ __forceinline__ void decode_fp3(uint32_t lo, uint32_t hg, uint32_t magic, uint32_t (&a)[8]) {
-    const uint32_t s2 = lo << 2, s8 = lo >> 8;
-    // spread the high bits: bit k -> k (k < 8), bit 8 + k -> 16 + k
-    const uint32_t sp = __byte_perm(hg, 0u, 0x4140);
-    const uint32_t h3 = sp << 3, h2 = sp << 2;  // pair i < 7: Q = i + 3; pair 7: Q = 9
-    a[0] = hfma2((h3 & 0x00080008u) | magic, fp3_mul<2, 3>(), hfma2((s2 & 0x000C000Cu) | magic, kTwo, fp3_off<2, 3>()));
-    a[1] = hfma2((h3 & 0x00100010u) | magic, fp3_mul<2, 4>(), hfma2((lo & 0x000C000Cu) | magic, kTwo, fp3_off<2, 4>()));
-    a[2] = hfma2((h3 & 0x00200020u) | magic, fp3_mul<4, 5>(), hfma2((lo & 0x00300030u) | magic, kTwo, fp3_off<4, 5>()));
-    a[3] = hfma2((h3 & 0x00400040u) | magic, fp3_mul<6, 6>(), hfma2((lo & 0x00C000C0u) | magic, kTwo, fp3_off<6, 6>()));
-    a[4] = hfma2((h3 & 0x00800080u) | magic, fp3_mul<8, 7>(), hfma2((lo & 0x03000300u) | magic, kTwo, fp3_off<8, 7>()));
-    a[5] = hfma2((h3 & 0x01000100u) | magic, fp3_mul<2, 8>(), hfma2((s8 & 0x000C000Cu) | magic, kTwo, fp3_off<2, 8>()));
-    a[6] = hfma2((h3 & 0x02000200u) | magic, fp3_mul<4, 9>(), hfma2((s8 & 0x00300030u) | magic, kTwo, fp3_off<4, 9>()));
-    a[7] = hfma2((h2 & 0x02000200u) | magic, fp3_mul<6, 9>(), hfma2((s8 & 0x00C000C0u) | magic, kTwo, fp3_off<6, 9>()));
 }
 
 // FP4: E2M1 nibble (s, e1, e0, m) -> binary16 bits (s << 15) | (e1 e0 m) << 9, i.e. the E2M1 value
@@ -401,36 +361,6 @@ struct SrcF32 {  // binary32 columns
         }
     }
 };
-struct SrcSilu {  // h = silu(g) * u from binary32 g and u columns (an expert's gated activation)
-    static constexpr int V = 1;
-    const float* g;
-    const float* u;
-    size_t half;  // nonzero: g and u are each the sum of two partials, the second `half` floats on
-    __device__ __forceinline__ void load16(size_t e0, float (&v)[16]) const {
-        const float4* pg = reinterpret_cast<const float4*>(g + e0);
-        const float4* pu = reinterpret_cast<const float4*>(u + e0);
-        float gg[16], uu[16];
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const float4 a = pg[i], b = pu[i];
-            gg[4 * i] = a.x; gg[4 * i + 1] = a.y; gg[4 * i + 2] = a.z; gg[4 * i + 3] = a.w;
-            uu[4 * i] = b.x; uu[4 * i + 1] = b.y; uu[4 * i + 2] = b.z; uu[4 * i + 3] = b.w;
-        }
-        if (half) {
-            const float4* qg = reinterpret_cast<const float4*>(g + half + e0);
-            const float4* qu = reinterpret_cast<const float4*>(u + half + e0);
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const float4 a = qg[i], b = qu[i];
-                gg[4 * i] += a.x; gg[4 * i + 1] += a.y; gg[4 * i + 2] += a.z; gg[4 * i + 3] += a.w;
-                uu[4 * i] += b.x; uu[4 * i + 1] += b.y; uu[4 * i + 2] += b.z; uu[4 * i + 3] += b.w;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 16; i++) v[i] = (gg[i] / (1.0f + expf(-gg[i]))) * uu[i];
-    }
-};
-
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&h);
@@ -1010,7 +940,6 @@ __device__ inline void init_rings(const Smem& s) {
     fence_barrier_init();
     __syncthreads();
 }
-
 
 // ------------------------------------------------------------------ CTA-wide stages
 

@@ -16,11 +16,6 @@
 
 namespace fpx {
 
-// Byte offset of element (r, k), k < 64, in a K-major 128-byte-swizzled tile.
-__host__ __device__ constexpr uint32_t sw128_offset(uint32_t r, uint32_t k) {
-    return (r >> 3) * 1024u + (r & 7u) * 128u + ((((k >> 3) ^ (r & 7u)) & 7u) << 4) + (k & 7u) * 2u;
-}
-
 // Shared-memory matrix descriptor: start address >> 4 (bits 0-13), leading byte offset >> 4 (bits
 // 16-29; not used by swizzled K-major layouts, set to 16 bytes), stride byte offset >> 4 (bits 32-45:
 // 1024 bytes between 8-row groups), the fixed value 1 at bits 46-47, base offset 0 (the tile is
@@ -71,8 +66,7 @@ __device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, 
 }
 
 // Whole warp: thread i writes r[0..31] to 32 consecutive columns of tensor-memory lane 32 q + i (q = the
-// warp's lane quarter, warp % 4), starting at column col of taddr (tmem_st16: 16 columns).
-// tmem_st_wait() makes them complete.
+// warp's lane quarter, warp % 4), starting at column col of taddr. tmem_st_wait() makes them complete.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -81,13 +75,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
         "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
         "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
