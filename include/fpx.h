@@ -267,7 +267,9 @@ int moe_layer_decode_tiered(const moe_layer* layer, const moe_tiers* tiers, cons
 /* Empties tiers->cache (enqueued on stream): counter and copy count 0, no expert in any staging slot.
  * Call it before the first moe_layer_decode_tiered with that cache, and again whenever the cold tier's
  * contents, slot_of or the staging slots change outside these calls: the cache trusts that a slot
- * still holds the expert it recorded. FPX_EINVAL without a cache or with n_stage outside 1..1024. */
+ * still holds the expert it recorded. FPX_EINVAL without a cache or with n_stage outside 1..1024.
+ * Part of the two-tier residency ([P-apu] section "Asymmetric Dual-GPU"); the pages do not say how
+ * streamed experts are kept, so the least-recently-used rule is this library's. */
 int moe_tiers_cache_reset(const moe_tiers* tiers, void* stream);
 
 /* moe_layer_decode for callers that cannot allocate device memory: a plugin or library running
